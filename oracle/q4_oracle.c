@@ -1,0 +1,323 @@
+/*
+ * q4_oracle.c -- plain CPU oracle for the Q4_0-weight x Q8_0-activation
+ * decode GEMV  y = W.x  (T token columns).
+ *
+ * TEST INFRASTRUCTURE ONLY.  Nothing on the product path links, loads or
+ * calls this file.  Only the test suite, the smoke check and the benchmark's
+ * CPU-baseline leg use it.  It shares no code, header, table or helper with
+ * the CUDA library; the two only ever see the same input bytes.
+ *
+ * Every function is the plain definition written out, with no blocking,
+ * fusion or reordering.  Floating-point results that the method leaves in
+ * fp32 (the quantiser) are computed in fp32 exactly as defined; the GEMV
+ * output is formed in fp64, where every product is exact.
+ *
+ * Sources (page title, section):
+ *  - minfer README, "How it works": gemv_dp4a is a q4_0 GEMV with int8
+ *    activations; mega streams packed q4 weights with int8 activations.
+ *  - minfer README, "The optimization journey", M9: SIMD nibble masking and
+ *    the folded -8 offset, sum (n-8)x = sum n.x - 8 sum x.
+ *  - minfer README, M15/M16: both kernels form identical per-block integer
+ *    sums, then scale and accumulate them in float.
+ *  - colibri qwen36 docs, dense int8 IDOT GEMV: an int8 activation scale of
+ *    amax/127, exact int32 products scaled afterwards.
+ * The block formats, as the GGML q4_0 / q8_0 names denote them:
+ *  - Q4_0 block: 32 weights; bytes 0-1 an fp16 scale d (little-endian);
+ *    bytes 2..17 hold qs[16]; element j (j < 16) is the low nibble of qs[j],
+ *    element j+16 its high nibble; the weight is (n - 8) * d.
+ *  - Q8_0 block: 32 activations; d = amax/127 stored as fp16; each
+ *    q = round-half-away-from-zero(x * (1/d)) as int8 (all zero if amax = 0).
+ *    Byte layout: fp16 d then 32 int8 (34 bytes).
+ *
+ * Readings where the pages are silent (each also listed in the design notes):
+ *  - 1/d is taken from the fp32 d, before d is rounded to fp16.
+ *  - x * (1/d) is one fp32 multiply, rounded to nearest even.
+ *  - amax = 0 gives d = 0, 1/d := 0, all q = 0.
+ *  - argmax: lowest index among equal maxima, equality by IEEE == (so -0 == +0).
+ *
+ * ORC_MUTANT (compile-time, default 0) plants one known mistake; the test
+ * suite builds each mutant and checks that its pins reject it.
+ */
+#include <math.h>
+#include <stdint.h>
+#include <stdlib.h>
+#include <string.h>
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#ifndef ORC_MUTANT
+#define ORC_MUTANT 0
+#endif
+
+#define QK 32
+#define Q4_0_BYTES 18
+#define Q8_0_BYTES 34
+
+/* ---------------------------------------------------------------- binary16 */
+
+/* binary16 -> binary32, exact: normal (1024+m)*2^(e-25), subnormal m*2^-24. */
+float orc_half_to_float(uint16_t h)
+{
+    int s = (h >> 15) & 1, e = (h >> 10) & 0x1F, m = h & 0x3FF;
+    double v;
+    if (e == 0)
+        v = ldexp((double)m, -24);
+    else if (e == 31)
+        v = m ? NAN : INFINITY;
+    else
+        v = ldexp((double)(1024 + m), e - 25);
+    return (float)(s ? -v : v);
+}
+
+/* Round a non-negative double with an integral-or-half fraction to the
+ * nearest integer, ties to even (written out, independent of fenv). */
+static double round_half_even(double q)
+{
+    double r = floor(q), frac = q - r;
+    if (frac > 0.5 || (frac == 0.5 && fmod(r, 2.0) != 0.0))
+        r += 1.0;
+    return r;
+}
+
+/* binary32 -> binary16, round to nearest even, subnormals kept, overflow to
+ * infinity (IEEE 754 binary16: 1 sign, 5 exponent bits with bias 15, 10
+ * fraction bits). */
+uint16_t orc_float_to_half_rn(float f)
+{
+    uint16_t sign = signbit(f) ? 0x8000 : 0;
+    double a = fabs((double)f);
+    if (isnan(f))
+        return sign | 0x7E00;
+    if (isinf(f))
+        return sign | 0x7C00;
+    if (a < ldexp(1.0, -14)) {                  /* subnormal: quantum 2^-24 */
+        double q = a * 16777216.0;              /* exact */
+#if ORC_MUTANT == 8
+        double r = floor(q);                    /* MUTANT: truncation */
+#else
+        double r = round_half_even(q);
+#endif
+        return sign | (uint16_t)r;              /* r == 1024 is the smallest normal */
+    }
+    int e;
+    frexp(a, &e);                               /* a in [2^(e-1), 2^e) */
+    int E = e - 1;
+    double q = ldexp(a, 10 - E);                /* in [1024, 2048), exact */
+#if ORC_MUTANT == 8
+    double r = floor(q);
+#else
+    double r = round_half_even(q);
+#endif
+    if (r == 2048.0) {
+        r = 1024.0;
+        E += 1;
+    }
+    if (E > 15)
+        return sign | 0x7C00;
+    return sign | (uint16_t)(((E + 15) << 10) | ((int)r - 1024));
+}
+
+/* ------------------------------------------------------------ Q8_0 quantise */
+
+static long g_range_violations = 0;
+
+/* Number of |x * (1/d)| values that rounded beyond 127 so far (the
+ * arithmetic bounds it by 127; a non-zero count flags a broken build). */
+long orc_range_violations(void) { return g_range_violations; }
+
+/* One block of 32 fp32 activations -> (fp16 d, int8 q[32]). */
+void orc_quantize_block_q8_0(const float *x, uint16_t *d_out, int8_t *q)
+{
+    float amax = 0.0f;
+    for (int j = 0; j < QK; j++) {
+#if ORC_MUTANT == 7
+        float a = x[j];                         /* MUTANT: signed max */
+#else
+        float a = fabsf(x[j]);
+#endif
+        if (a > amax)
+            amax = a;
+    }
+    float d = amax / 127.0f;
+    uint16_t dh = orc_float_to_half_rn(d);
+#if ORC_MUTANT == 4
+    float dr = orc_half_to_float(dh);           /* MUTANT: 1/d from fp16 d */
+    float id = (dr != 0.0f) ? 1.0f / dr : 0.0f;
+#else
+    float id = (d != 0.0f) ? 1.0f / d : 0.0f;
+#endif
+    *d_out = dh;
+    for (int j = 0; j < QK; j++) {
+        float v = x[j] * id;
+#if ORC_MUTANT == 3
+        float r = rintf(v);                     /* MUTANT: ties to even */
+#else
+        float r = roundf(v);                    /* C99: halfway cases away from zero */
+#endif
+        if (r > 127.0f || r < -127.0f) {        /* unreachable for finite x: counted */
+            g_range_violations++;
+            r = r > 0.0f ? 127.0f : -127.0f;
+        }
+        q[j] = (int8_t)r;
+    }
+}
+
+/* x fp32 [T][K] -> xq in GGML Q8_0 block layout [T][K/32][34]. */
+void orc_quantize_q8_0(const float *x, int T, int64_t K, uint8_t *xq)
+{
+    int64_t nb = K / QK;
+    for (int t = 0; t < T; t++)
+        for (int64_t b = 0; b < nb; b++) {
+            uint8_t *blk = xq + ((int64_t)t * nb + b) * Q8_0_BYTES;
+            uint16_t d;
+            int8_t q[QK];
+            orc_quantize_block_q8_0(x + (int64_t)t * K + b * QK, &d, q);
+            blk[0] = (uint8_t)(d & 0xFF);
+            blk[1] = (uint8_t)(d >> 8);
+            memcpy(blk + 2, q, QK);
+        }
+}
+
+/* ------------------------------------------------------------ block sums */
+
+static uint16_t rd16(const uint8_t *p) { return (uint16_t)(p[0] | (p[1] << 8)); }
+
+/* Nibble value of element e (0..31) of a Q4_0 block. */
+static int q4_nibble(const uint8_t *wblk, int e)
+{
+#if ORC_MUTANT == 1
+    e = (e + 16) % 32;                          /* MUTANT: swapped nibble halves */
+#endif
+    uint8_t byte = wblk[2 + (e % 16)];
+    return e < 16 ? (byte & 0x0F) : (byte >> 4);
+}
+
+/* isum = sum_j (n_j - 8) * q_j over one block, exact int32 (|isum| <= 32512). */
+int32_t orc_block_isum(const uint8_t *wblk, const uint8_t *xblk)
+{
+    const int8_t *q = (const int8_t *)(xblk + 2);
+    int32_t s = 0;
+    for (int j = 0; j < QK; j++) {
+#if ORC_MUTANT == 2
+        s += q4_nibble(wblk, j) * q[j];         /* MUTANT: -8 offset dropped */
+#else
+        s += (q4_nibble(wblk, j) - 8) * q[j];
+#endif
+    }
+    return s;
+}
+
+static const uint8_t *xq_block(const uint8_t *xq, int64_t nb, int t, int64_t b)
+{
+#if ORC_MUTANT == 6
+    b = (b + 1) % nb;                           /* MUTANT: wrong block index */
+#endif
+    return xq + ((int64_t)t * nb + b) * Q8_0_BYTES;
+}
+
+/* isums [T][N][nb] for W (GGML Q4_0, [N][nb][18]) and xq (GGML Q8_0). */
+void orc_block_isums(const uint8_t *W, int64_t N, int64_t K, const uint8_t *xq, int T,
+                     int32_t *isums)
+{
+    int64_t nb = K / QK;
+    for (int t = 0; t < T; t++)
+        for (int64_t i = 0; i < N; i++)
+            for (int64_t b = 0; b < nb; b++)
+                isums[((int64_t)t * N + i) * nb + b] =
+                    orc_block_isum(W + (i * nb + b) * Q4_0_BYTES, xq_block(xq, nb, t, b));
+}
+
+/* ------------------------------------------------------------------ GEMV */
+
+/* One output: y64 = sum_b d_w(i,b) * d_x(t,b) * isum(t,i,b) in fp64 (every
+ * product exact), S = sum_b |same term| (the tolerance's scale). */
+static void gemv_one(const uint8_t *W, int64_t nb, const uint8_t *xq, int t, int64_t i,
+                     double *y, double *S)
+{
+    double acc = 0.0, mag = 0.0;
+    for (int64_t b = 0; b < nb; b++) {
+        const uint8_t *wblk = W + (i * nb + b) * Q4_0_BYTES;
+        const uint8_t *xblk = xq_block(xq, nb, t, b);
+        double dw = (double)orc_half_to_float(rd16(wblk));
+#if ORC_MUTANT == 5
+        double dx = 1.0;                        /* MUTANT: activation scale dropped */
+#else
+        double dx = (double)orc_half_to_float(rd16(xblk));
+#endif
+        double term = dw * dx * (double)orc_block_isum(wblk, xblk);
+        acc += term;
+        mag += fabs(term);
+    }
+    *y = acc;
+    *S = mag;
+}
+
+/* y64, S: [T][N].  OpenMP over rows when built with -fopenmp. */
+void orc_gemv_f64(const uint8_t *W, int64_t N, int64_t K, const uint8_t *xq, int T,
+                  double *y64, double *S)
+{
+    int64_t nb = K / QK;
+    for (int t = 0; t < T; t++) {
+#pragma omp parallel for schedule(static)
+        for (int64_t i = 0; i < N; i++) {
+#if ORC_MUTANT == 10
+            int64_t o = i * T + t;              /* MUTANT: transposed output */
+#else
+            int64_t o = (int64_t)t * N + i;
+#endif
+            gemv_one(W, nb, xq, t, i, &y64[o], &S[o]);
+        }
+    }
+}
+
+/* Selected rows only: y64, S are [T][nrows]. */
+void orc_gemv_rows_f64(const uint8_t *W, int64_t N, int64_t K, const uint8_t *xq, int T,
+                       const int64_t *rows, int64_t nrows, double *y64, double *S)
+{
+    int64_t nb = K / QK;
+    (void)N;
+    for (int t = 0; t < T; t++)
+        for (int64_t r = 0; r < nrows; r++)
+            gemv_one(W, nb, xq, t, rows[r], &y64[(int64_t)t * nrows + r],
+                     &S[(int64_t)t * nrows + r]);
+}
+
+/* --------------------------------------------------------------- argmax */
+
+/* Lowest index i with y[i] maximal; equality is IEEE == (-0 == +0). */
+int64_t orc_argmax_f32(const float *y, int64_t N)
+{
+    int64_t best = 0;
+    for (int64_t i = 1; i < N; i++) {
+#if ORC_MUTANT == 9
+        if (y[i] >= y[best])                    /* MUTANT: ties to highest index */
+#else
+        if (y[i] > y[best])
+#endif
+            best = i;
+    }
+    return best;
+}
+
+int64_t orc_argmax_f64(const double *y, int64_t N)
+{
+    int64_t best = 0;
+    for (int64_t i = 1; i < N; i++)
+        if (y[i] > y[best])
+            best = i;
+    return best;
+}
+
+/* ------------------------------------------------------------------ misc */
+
+int orc_num_threads(void)
+{
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}
+
+int orc_mutant(void) { return ORC_MUTANT; }

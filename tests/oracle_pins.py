@@ -1,0 +1,294 @@
+"""Pins that tie the CPU oracle to facts outside itself.
+
+Each pin takes a loaded oracle and raises AssertionError on a mismatch.  The
+sources are: hand-worked blocks (tests/golden/hand_blocks.json), closed
+forms, invariants of the definitions, numpy's binary16 cast (an independent
+library implementation of IEEE 754 rounding), and an fp64 dequantise-then-dot
+brute force on tiny shapes.  test_oracle_pins.py runs them against the
+oracle; it also builds planted-mistake variants of the oracle and checks
+that every one of them fails at least one pin.
+"""
+from __future__ import annotations
+
+import json
+import os
+
+import numpy as np
+
+import synth
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden", "hand_blocks.json")
+
+
+def golden():
+    with open(GOLDEN) as f:
+        return json.load(f)
+
+
+def _x_block(entry) -> np.ndarray:
+    x = np.zeros(32, np.float32)
+    for k, v in entry["x_nonzero"].items():
+        x[int(k)] = v
+    return x
+
+
+def _q_block(entry) -> np.ndarray:
+    q = np.zeros(32, np.int8)
+    for k, v in entry["q_nonzero"].items():
+        q[int(k)] = v
+    return q
+
+
+def _xq_bytes(d_bits: int, q: np.ndarray) -> np.ndarray:
+    return np.concatenate([np.array([d_bits & 0xFF, d_bits >> 8], np.uint8), q.view(np.uint8)])
+
+
+def _wq_bytes(d_bits: int, qs) -> np.ndarray:
+    return np.concatenate([np.array([d_bits & 0xFF, d_bits >> 8], np.uint8), np.array(qs, np.uint8)])
+
+
+# ------------------------------------------------------------------ binary16
+
+def pin_half_decode_all(o):
+    """Every binary16 pattern decodes like numpy's float16 -> float32 cast."""
+    bits = np.arange(65536, dtype=np.uint16)
+    ref = bits.view(np.float16).astype(np.float32)
+    got = np.array([o.half_to_float(int(b)) for b in bits], np.float32)
+    nan = np.isnan(ref)
+    assert np.array_equal(np.isnan(got), nan)
+    assert np.array_equal(got[~nan].view(np.uint32), ref[~nan].view(np.uint32))
+
+
+def pin_half_encode_against_numpy(o):
+    """float32 -> binary16 RN-even matches numpy's cast on halfway points,
+    neighbours of halfway points, the overflow threshold, subnormals and a
+    random sweep (numpy's cast is an independent IEEE implementation)."""
+    finite = np.arange(0, 0x7C00, dtype=np.uint16).view(np.float16).astype(np.float64)
+    mids = (finite[:-1] + finite[1:]) / 2.0          # exact halfway points (fit in fp32)
+    cand = np.concatenate([finite, mids]).astype(np.float32)
+    up = np.nextafter(cand, np.float32(np.inf))
+    dn = np.nextafter(cand, np.float32(0))
+    rng = np.random.default_rng(7)
+    rand = (rng.standard_normal(20000) * np.exp2(rng.integers(-30, 18, 20000))).astype(np.float32)
+    extra = np.array([65519.99, 65520.0, 65536.0, 1e9, 2.0 ** -25, 2.0 ** -24 * 1.5, 5.96e-8], np.float32)
+    vals = np.concatenate([cand, up, dn, rand, extra])
+    vals = np.concatenate([vals, -vals])
+    with np.errstate(over="ignore"):
+        ref = vals.astype(np.float16).view(np.uint16)
+    sample = np.random.default_rng(8).choice(vals.size, size=min(vals.size, 60000), replace=False)
+    for i in sample:
+        assert o.float_to_half(float(vals[i])) == int(ref[i]), (vals[i], hex(ref[i]))
+
+
+def pin_half_round_trip(o):
+    """encode(decode(h)) == h for every finite binary16, -0 included."""
+    for h in list(range(0, 0x7C00)) + list(range(0x8000, 0xFC00)):
+        assert o.float_to_half(o.half_to_float(h)) == h, hex(h)
+
+
+# ------------------------------------------------------------------ Q8_0
+
+def pin_q8_hand_blocks(o):
+    for e in golden()["q8_0"]:
+        d, q = o.quantize_block(_x_block(e))
+        assert d == int(e["d_bits"], 16), (e["name"], hex(d))
+        assert np.array_equal(q, _q_block(e)), (e["name"], q)
+
+
+def pin_q8_constant_block(o):
+    """x == c on a whole block gives q == 127 everywhere and d = fp16(c/127)."""
+    for c in (1.0, 0.3, 7.25, 1000.0, 1e-3):
+        d, q = o.quantize_block(np.full(32, c, np.float32))
+        assert np.all(q == 127), (c, q)
+        assert d == int(np.float16(np.float32(c) / np.float32(127.0)).view(np.uint16)), c
+
+
+def pin_q8_symmetry_and_range(o):
+    """q(-x) == -q(x) with the same d; |q| <= 127; the amax element maps to +-127."""
+    rng = np.random.default_rng(11)
+    for _ in range(300):
+        x = synth.activations(int(rng.integers(1 << 30)), 1, 32)[0]
+        d1, q1 = o.quantize_block(x)
+        d2, q2 = o.quantize_block(-x)
+        assert d1 == d2 and np.array_equal(q2, -q1)
+        assert np.abs(q1.astype(np.int32)).max() == 127
+        k = int(np.argmax(np.abs(x)))
+        assert abs(int(q1[k])) == 127
+    assert o.range_violations() == 0
+
+
+def pin_q8_power_of_two_scaling(o):
+    """Scaling a block by 2^k leaves q unchanged and scales d by 2^k exactly
+    while fp16(d) stays a normal number."""
+    rng = np.random.default_rng(12)
+    for _ in range(100):
+        x = (rng.standard_normal(32) * 3).astype(np.float32)
+        d0, q0 = o.quantize_block(x)
+        for k in (-3, 1, 4):
+            d1, q1 = o.quantize_block((x * np.float32(2.0 ** k)).astype(np.float32))
+            assert np.array_equal(q0, q1)
+            f0 = np.uint16(d0).view(np.float16).astype(np.float64)
+            f1 = np.uint16(d1).view(np.float16).astype(np.float64)
+            assert f1 == f0 * 2.0 ** k
+
+
+def pin_q8_layout(o):
+    """The T x K quantiser lays blocks out as [t][b] with fp16 d then 32 int8."""
+    x = synth.activations(5, 3, 96)
+    xq = o.quantize(x)
+    assert xq.shape == (3, 3, 34)
+    for t in range(3):
+        for b in range(3):
+            d, q = o.quantize_block(x[t, 32 * b: 32 * b + 32])
+            assert int(xq[t, b, 0]) | (int(xq[t, b, 1]) << 8) == d
+            assert np.array_equal(xq[t, b, 2:].view(np.int8), q)
+
+
+# ------------------------------------------------------------------ Q4_0 sums / GEMV
+
+def _hand_xq(name):
+    e = [e for e in golden()["q8_0"] if e["name"] == name][0]
+    return _xq_bytes(int(e["d_bits"], 16), _q_block(e))
+
+
+def pin_q4_hand_block(o):
+    for e in golden()["q4_0"]:
+        w = _wq_bytes(int(e["w_d_bits"], 16), e["w_qs"])
+        xq = _hand_xq(e["x_block"])
+        assert o.block_isum(w, xq) == e["isum"]
+        y, S = o.gemv(w.reshape(1, 18), 1, 32, xq.reshape(1, 1, 34), 1)
+        assert y[0, 0] == e["y"]
+        assert S[0, 0] == abs(e["y"])
+
+
+def pin_closed_forms(o):
+    for e in golden()["closed_forms"]:
+        K = e["K"]
+        W = synth.with_nibbles(synth.q4_0_weights(1, 4, K), K, e["nibble"])
+        W = synth.with_scales(W, K, int(e["w_d_bits"], 16))
+        x = np.full((1, K), e["x_value"], np.float32)
+        xq = o.quantize(x)
+        y, S = o.gemv(W, 4, K, xq, 1)
+        assert np.all(y == e["y"]), (e["name"], y)
+        if "isum" in e:
+            assert np.all(o.block_isums(W, 4, K, xq, 1) == e["isum"])
+
+
+def pin_zero_scale(o):
+    """A zero weight scale gives y == 0 (and argmax 0 on an all-zero output)."""
+    K = 128
+    W = synth.with_scales(synth.q4_0_weights(2, 8, K), K, 0x0000)
+    xq = o.quantize(synth.activations(3, 2, K))
+    y, S = o.gemv(W, 8, K, xq, 2)
+    assert np.all(y == 0.0) and np.all(S == 0.0)
+    assert o.argmax_f32(y[0].astype(np.float32)) == 0
+
+
+def pin_nibble_complement(o):
+    """Replacing every nibble n by 15-n maps isum to -isum - sum(q) (from
+    (15-n-8) = -(n-8) - 1)."""
+    K = 256
+    W = synth.q4_0_weights(4, 6, K)
+    Wc = W.copy().reshape(6, K // 32, 18)
+    Wc[:, :, 2:] = 0xFF - Wc[:, :, 2:]
+    Wc = Wc.reshape(W.shape)
+    xq = o.quantize(synth.activations(5, 2, K))
+    i1 = o.block_isums(W, 6, K, xq, 2).astype(np.int64)
+    i2 = o.block_isums(Wc, 6, K, xq, 2).astype(np.int64)
+    qsum = xq[:, :, 2:].view(np.int8).astype(np.int64).sum(axis=2)      # [T, nb]
+    assert np.array_equal(i2, -i1 - qsum[:, None, :])
+
+
+def _dequant_f64(W, N, K):
+    """Brute force: every weight as (n - 8) * d in fp64, [N, K]."""
+    nb = K // 32
+    blk = W.reshape(N, nb, 18)
+    d = blk[:, :, 0:2].copy().view("<f2").astype(np.float64)[:, :, 0]
+    qs = blk[:, :, 2:]
+    n = np.concatenate([qs & 0x0F, qs >> 4], axis=2).astype(np.float64)  # elements 0..15, 16..31
+    return ((n - 8.0) * d[:, :, None]).reshape(N, K)
+
+
+def _dequant_x_f64(xq, T, K):
+    nb = K // 32
+    d = xq[:, :, 0:2].copy().view("<f2").astype(np.float64)[:, :, 0]
+    q = xq[:, :, 2:].view(np.int8).astype(np.float64)
+    return (q * d[:, :, None]).reshape(T, K)
+
+
+def pin_bruteforce_dequant_dot(o):
+    """Dequantise both operands to fp64 and take numpy's dot: equals y64."""
+    rng = np.random.default_rng(13)
+    for trial in range(24):
+        N = int(rng.integers(1, 48))
+        K = 32 * int(rng.integers(1, 9))
+        T = int(rng.integers(1, 9))
+        W = synth.q4_0_weights(100 + trial, N, K)
+        x = synth.activations(200 + trial, T, K)
+        xq = o.quantize(x)
+        y, S = o.gemv(W, N, K, xq, T)
+        ref = _dequant_x_f64(xq, T, K) @ _dequant_f64(W, N, K).T
+        assert np.allclose(y, ref, rtol=1e-12, atol=1e-12 * max(1.0, float(np.abs(ref).max())))
+        assert np.all(S >= np.abs(y) - 1e-9)
+
+
+def pin_row_permutation(o):
+    K, N, T = 192, 20, 3
+    W = synth.q4_0_weights(21, N, K)
+    xq = o.quantize(synth.activations(22, T, K))
+    perm = np.random.default_rng(23).permutation(N)
+    y, _ = o.gemv(W, N, K, xq, T)
+    yp, _ = o.gemv(np.ascontiguousarray(W[perm]), N, K, xq, T)
+    assert np.array_equal(yp, y[:, perm])
+
+
+def pin_token_columns_independent(o):
+    """Column t of a T-token GEMV equals the 1-token GEMV of that column."""
+    K, N, T = 160, 24, 5
+    W = synth.q4_0_weights(31, N, K)
+    xq = o.quantize(synth.activations(32, T, K))
+    y, S = o.gemv(W, N, K, xq, T)
+    for t in range(T):
+        y1, S1 = o.gemv(W, N, K, np.ascontiguousarray(xq[t:t + 1]), 1)
+        assert np.array_equal(y1[0], y[t]) and np.array_equal(S1[0], S[t])
+
+
+def pin_rows_subset(o):
+    K, N, T = 96, 30, 2
+    W = synth.q4_0_weights(41, N, K)
+    xq = o.quantize(synth.activations(42, T, K))
+    y, S = o.gemv(W, N, K, xq, T)
+    rows = np.array([0, 7, 29, 3])
+    yr, Sr = o.gemv_rows(W, N, K, xq, T, rows)
+    assert np.array_equal(yr, y[:, rows]) and np.array_equal(Sr, S[:, rows])
+
+
+def pin_scale_linearity(o):
+    """Doubling every weight scale (exact in fp16) doubles y64 exactly."""
+    K, N = 128, 10
+    W = synth.q4_0_weights(51, N, K)
+    W2 = W.copy().reshape(N, K // 32, 18)
+    d = W2[:, :, 0:2].copy().view("<f2")[:, :, 0]
+    W2[:, :, 0:2] = (d.astype(np.float32) * 2).astype("<f2").view(np.uint8).reshape(N, K // 32, 2)
+    W2 = W2.reshape(W.shape)
+    xq = o.quantize(synth.activations(52, 1, K))
+    y1, _ = o.gemv(W, N, K, xq, 1)
+    y2, _ = o.gemv(W2, N, K, xq, 1)
+    assert np.array_equal(y2, 2 * y1)
+
+
+# ------------------------------------------------------------------ argmax
+
+def pin_argmax_rules(o):
+    assert o.argmax_f32(np.array([1, 3, 3, 2], np.float32)) == 1
+    assert o.argmax_f32(np.array([-0.0, 0.0, -1.0], np.float32)) == 0
+    assert o.argmax_f32(np.array([-1.0, 0.0, -0.0], np.float32)) == 1
+    assert o.argmax_f32(np.zeros(9, np.float32)) == 0
+    assert o.argmax_f32(np.array([-5.0, -2.0, -2.0, -7.0], np.float32)) == 1
+    y = np.random.default_rng(61).standard_normal(1000).astype(np.float32)
+    y[[100, 400, 900]] = y.max() + 1
+    assert o.argmax_f32(y) == 100
+    assert o.argmax_f64(np.array([2.0, 5.0, 5.0], np.float64)) == 1
+
+
+PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -1,0 +1,44 @@
+"""The CPU oracle against its pins, and every planted mistake against them.
+
+CPU only.  See tests/oracle_pins.py for what each pin checks and why it is
+independent of the oracle's own code.
+"""
+import tempfile
+
+import pytest
+
+import oracle
+from tests import oracle_pins as P
+
+
+@pytest.mark.parametrize("pin", P.PINS, ids=lambda f: f.__name__)
+def test_pin(orc, pin):
+    pin(orc)
+
+
+# Planted mistakes (ORC_MUTANT in q4_oracle.c):
+#  1 swapped nibble halves, 2 dropped -8 offset, 3 ties-to-even rounding,
+#  4 inverse scale from the fp16 d, 5 activation scale dropped,
+#  6 wrong activation block index, 7 signed instead of absolute max,
+#  8 truncating fp16 encode, 9 argmax ties to the highest index,
+#  10 transposed output.
+MUTANTS = list(range(1, 11))
+
+
+@pytest.fixture(scope="module")
+def mutdir():
+    with tempfile.TemporaryDirectory(prefix="orc_mut_") as d:
+        yield d
+
+
+@pytest.mark.parametrize("m", MUTANTS)
+def test_pins_reject_mutant(mutdir, m):
+    o = oracle.Oracle(oracle.build_mutant(m, mutdir))
+    assert o.mutant() == m
+    failed = []
+    for pin in P.PINS:
+        try:
+            pin(o)
+        except AssertionError:
+            failed.append(pin.__name__)
+    assert failed, f"mutant {m} passed every pin"
