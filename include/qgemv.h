@@ -1,0 +1,222 @@
+/*
+ * qgemv.h -- C ABI of libqgemv: the batch-1 / few-token decode GEMV
+ * y = W.x with Q4_0 weights and Q8_0-quantised activations, on one GB300.
+ *
+ * The operation (minfer README, "How it works": gemv_dp4a, a q4_0 GEMV with
+ * int8 activations; "The optimization journey", M3.5 and M9):
+ *   - W is an N x K matrix in Q4_0 blocks of 32 weights along K: an fp16
+ *     scale d, then 16 bytes whose low nibble is element j and high nibble
+ *     element j+16 (j < 16); weight = (n - 8) * d.  18 bytes per block.
+ *   - x holds T token columns of K fp32 values.  Each block of 32 is
+ *     quantised to Q8_0: d = amax/127 (fp32, stored as fp16), and
+ *     q = round-half-away-from-zero(x * (1/d)) as int8, 1/d taken from the
+ *     fp32 d (all zero when amax = 0).
+ *   - For every output row i, token t and block b the exact integer sum
+ *     isum = sum_j (n_j - 8) * q_j is formed (minfer M15/M16: "identical
+ *     per-block integer sums"), scaled by d_w * d_x and accumulated in fp32.
+ *
+ * Summation order.  Every entry point, for every T and every launch shape,
+ * accumulates one output in the same fixed order, which depends on K only:
+ * K is cut into segments of 16 blocks; inside a segment the blocks with
+ * b % 4 == j form four running sums (fp32 fused multiply-add, in increasing
+ * b, starting from +0), combined as (s0 + s1) + (s2 + s3); the segment
+ * results are then added in increasing segment order.  So a token's outputs
+ * are bit-identical whether it runs alone or with up to 7 others (minfer
+ * M16), and the argmax of every entry point agrees with the argmax of its
+ * own y.
+ *
+ * Data layouts (all little-endian, all in device memory unless stated):
+ *   W, QGEMV_W_GGML   : GGML row-major Q4_0, [N][K/32] blocks of 18 bytes.
+ *   W, QGEMV_W_PACKED : the same bytes re-laid out by qgemv_pack_q4_0
+ *                       (same byte count, 18*N*K/32).  Rows are grouped in
+ *                       slabs of 16; a slab holds K/32 blocks for 16 rows in
+ *                       "quads" of up to 4 blocks: first the 16 rows x 4
+ *                       blocks of nibble bytes (row-major, 16 bytes each),
+ *                       then their fp16 scales ([row r8 < 8][block][r8, r8+8]).
+ *                       The last N % 16 rows stay in GGML layout after the
+ *                       slabs.
+ *   xq (Q8_0, planar) : for R rows of K values, R*K int8 values ([r][k]),
+ *                       then R*K/32 fp16 scales ([r][b]), then zero padding
+ *                       to a multiple of 16 bytes: qgemv_xq_bytes(R, K).
+ *   x                 : fp32 [T][K] (token-major).
+ *   y                 : fp32 [T][N] (token-major).
+ *
+ * Ownership and errors.  The caller owns every buffer.  The library never
+ * allocates, frees or synchronises in these calls: every call only validates
+ * its arguments on the host and enqueues kernels on the given stream, so
+ * results are ready in stream order.  Invalid arguments return an error
+ * before anything is enqueued.  A launch failure returns QGEMV_ERR_CUDA.  A
+ * kernel that waits too long on one of its own asynchronous copies gives up,
+ * records QGEMV_ERR_TIMEOUT in a per-device status word (see
+ * qgemv_device_status) and returns; its outputs are then undefined.  No C++
+ * exception crosses the ABI.  Calls are thread-safe; two calls that share a
+ * workspace must not overlap on the GPU.
+ *
+ * Workspace.  Calls that take (ws, ws_bytes) use it for split-K partial
+ * sums, completion counters, argmax candidates and (for fp32-input calls)
+ * the quantised activations.  The matching *_workspace_bytes query gives the
+ * size (device-independent).  The workspace must be zero-filled once before
+ * its first use (e.g. cudaMemsetAsync); every call that completes without a
+ * device-status error leaves its counters at zero again, so it can be reused
+ * directly.
+ *
+ * Alignment: W, xq and ws 16 bytes; x and y 4 bytes; strides accordingly.
+ * Limits: K % 32 == 0; 1 <= T <= 8 for the GEMV calls; 1 <= N < 2^31.
+ */
+#ifndef QGEMV_H
+#define QGEMV_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A CUDA stream handle (identical to cudaStream_t); NULL is the legacy
+ * default stream. */
+struct CUstream_st;
+typedef struct CUstream_st *qgemv_stream_t;
+
+typedef enum {
+    QGEMV_OK = 0,
+    QGEMV_ERR_INVALID_ARG = 1, /* null pointer, bad size, overlap, T out of range */
+    QGEMV_ERR_MISALIGNED = 2,  /* a pointer or stride breaks the alignment rules */
+    QGEMV_ERR_UNSUPPORTED = 3, /* a shape the kernels do not cover (T*K too large) */
+    QGEMV_ERR_WORKSPACE = 4,   /* ws is NULL or smaller than the query says */
+    QGEMV_ERR_CUDA = 5,        /* a CUDA runtime call failed (launch, attribute) */
+    QGEMV_ERR_TIMEOUT = 6,     /* reported through qgemv_device_status only */
+    QGEMV_ERR_BAD_ID = 7,      /* gather: an expert id outside [0, n_experts) */
+    QGEMV_ERR_INTERNAL = 8
+} qgemv_status;
+
+typedef enum { QGEMV_W_GGML = 0, QGEMV_W_PACKED = 1 } qgemv_wlayout;
+
+/* Human-readable name of a status code (static string). */
+const char *qgemv_status_string(qgemv_status s);
+
+/* Library version as 10000*major + 100*minor + patch. */
+int qgemv_version(void);
+
+/* Bytes of an N x K Q4_0 matrix in either layout: 18 * N * K / 32.
+ * Returns 0 for an invalid shape. */
+size_t qgemv_q4_0_bytes(int64_t N, int64_t K);
+
+/* Bytes of a planar Q8_0 buffer for R rows of K: R*K + roundup16(2*R*K/32).
+ * Returns 0 for an invalid shape. */
+size_t qgemv_xq_bytes(int R, int64_t K);
+
+/* Re-lay out an N x K GGML Q4_0 matrix into the packed device layout (a
+ * byte permutation, so the result has the same size).  Done once at load
+ * time; minfer README M15 repacks weights at load into row groups so that a
+ * warp reads contiguous bytes.  w_ggml and w_packed are device buffers of
+ * qgemv_q4_0_bytes(N, K) bytes that must not overlap; w_packed must be
+ * 16-byte aligned. */
+qgemv_status qgemv_pack_q4_0(const void *w_ggml, void *w_packed, int64_t N, int64_t K,
+                             qgemv_stream_t stream);
+
+/* Inverse of qgemv_pack_q4_0 (w_packed 16-byte aligned). */
+qgemv_status qgemv_unpack_q4_0(const void *w_packed, void *w_ggml, int64_t N, int64_t K,
+                               qgemv_stream_t stream);
+
+/* Quantise fp32 activations to planar Q8_0 (block rule above; minfer README
+ * "How it works": int8 activations; colibri qwen36 docs, dense int8 IDOT
+ * GEMV: scale amax/127).  x is [batch][R][K] fp32; xq receives `batch`
+ * consecutive planar buffers of qgemv_xq_bytes(R, K) bytes each.  R >= 1
+ * rows (not limited to 8), batch >= 1.  xq must be 16-byte aligned. */
+qgemv_status qgemv_quantize_q8_0(const float *x, void *xq, int R, int64_t K, int batch,
+                                 qgemv_stream_t stream);
+
+/* Workspace bytes for qgemv_q4_0, qgemv_q4_0_f32 and qgemv_q4_0_argmax on
+ * an N x K matrix with T tokens (0 for an invalid shape). */
+size_t qgemv_workspace_bytes(int64_t N, int64_t K, int T);
+
+/* y[T][N] = W . x for T pre-quantised token columns (xq, planar Q8_0 of T
+ * rows).  Weights are streamed once from HBM (minfer README, M15: decode is
+ * bandwidth / bytes per token). */
+qgemv_status qgemv_q4_0(const void *W, qgemv_wlayout layout, const void *xq, float *y,
+                        int64_t N, int64_t K, int T, void *ws, size_t ws_bytes,
+                        qgemv_stream_t stream);
+
+/* Same as qgemv_q4_0 with fp32 input x[T][K]: the activations are quantised
+ * into the workspace first (a separate kernel, chained with programmatic
+ * dependent launch so the GEMV's weight stream starts while it runs). */
+qgemv_status qgemv_q4_0_f32(const void *W, qgemv_wlayout layout, const float *x, float *y,
+                            int64_t N, int64_t K, int T, void *ws, size_t ws_bytes,
+                            qgemv_stream_t stream);
+
+/* lm_head GEMV with fused argmax (minfer README "How it works": device-side
+ * argmax; M19: per-CTA candidates merged associatively).  idx[t] (int64,
+ * device) receives, per token, the lowest row index whose output is maximal
+ * (equality by IEEE ==, so -0 equals +0).  y_or_null, when not NULL,
+ * receives the full y[T][N] exactly as qgemv_q4_0 would write it. */
+qgemv_status qgemv_q4_0_argmax(const void *W, qgemv_wlayout layout, const void *xq,
+                               float *y_or_null, int64_t *idx, int64_t N, int64_t K, int T,
+                               void *ws, size_t ws_bytes, qgemv_stream_t stream);
+
+/* One GEMV of a sequence (layer set): weights, planar Q8_0 activations of
+ * T rows, and output y[T][N]. */
+typedef struct {
+    const void *W;
+    const void *xq;
+    float *y;
+    int64_t N;
+    int64_t K;
+} qgemv_seq_item;
+
+/* Workspace bytes for qgemv_q4_0_seq on this list (0 if invalid). */
+size_t qgemv_seq_workspace_bytes(const qgemv_seq_item *items, int n, int T);
+
+/* Run n GEMVs (host array `items`, read during the call only) in list order
+ * in one persistent launch per 224 items (minfer README M15: one persistent
+ * kernel streams every matrix of the token and keeps DRAM busy).  Every
+ * item's inputs must be ready when the call is enqueued: no item may read
+ * another item's y.  All items share T and the layout. */
+qgemv_status qgemv_q4_0_seq(const qgemv_seq_item *items, int n, qgemv_wlayout layout, int T,
+                            void *ws, size_t ws_bytes, qgemv_stream_t stream);
+
+/* One matrix of a routed-expert (MoE) gather: expert e's copy of this
+ * matrix starts at W + e * expert_stride (bytes); slot s reads activations
+ * xq + s * xq_stride (bytes; 0 = shared by all slots) and writes
+ * y + s * y_stride (floats). */
+typedef struct {
+    const void *W;
+    int64_t expert_stride;
+    const void *xq;
+    int64_t xq_stride;
+    float *y;
+    int64_t y_stride;
+    int64_t N;
+    int64_t K;
+} qgemv_gather_matrix;
+
+/* Workspace bytes for qgemv_q4_0_gather (0 if invalid). */
+size_t qgemv_gather_workspace_bytes(const qgemv_gather_matrix *mats, int n_mats, int n_ids, int T);
+
+/* Routed-expert GEMV (colibri qwen36 docs: 256 experts, top-8 + 1 shared;
+ * only the selected experts' bytes are streamed).  For every slot
+ * s < n_ids and every matrix m: y_m[s] = W_m[ids[s]] . xq_m[s].  ids is a
+ * device int32 array; an id outside [0, n_experts) is not read from: its
+ * outputs are left untouched and the device status word records
+ * QGEMV_ERR_BAD_ID.  One launch covers all matrices and slots (n_mats <= 4). */
+qgemv_status qgemv_q4_0_gather(const qgemv_gather_matrix *mats, int n_mats, const int32_t *ids,
+                               int n_ids, int n_experts, qgemv_wlayout layout, int T, void *ws,
+                               size_t ws_bytes, qgemv_stream_t stream);
+
+/* Test hook: the exact per-block integer sums the GEMV kernels form,
+ * isums[T][N][K/32] int32 (device), from the same unpack / int8-dot code. */
+qgemv_status qgemv_debug_block_isums(const void *W, qgemv_wlayout layout, const void *xq,
+                                     int32_t *isums, int64_t N, int64_t K, int T,
+                                     qgemv_stream_t stream);
+
+/* Read and clear the current device's status word: QGEMV_OK, or the first
+ * asynchronous error a kernel recorded (QGEMV_ERR_TIMEOUT, QGEMV_ERR_BAD_ID)
+ * into *code_out.  Synchronises with the device (a query, not part of the
+ * hot path).  Returns QGEMV_ERR_CUDA if the device cannot be read. */
+qgemv_status qgemv_device_status(int *code_out);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* QGEMV_H */

@@ -1,0 +1,215 @@
+"""Python binding of libqgemv (include/qgemv.h): the Q4_0-weight x
+Q8_0-activation decode GEMV on one GB300.
+
+Argument marshalling only: every step runs in the library's CUDA kernels.
+Tensors supply device pointers; work is enqueued on the current torch CUDA
+stream.  The library is loaded from this directory (libqgemv.so, built by
+``quantized_q4_weight_gb300._build.build()``); if it is missing, every call
+raises -- there is no fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import _build
+
+QK = 32
+Q4_0_BYTES = 18
+W_GGML, W_PACKED = 0, 1
+
+STATUS = {0: "QGEMV_OK", 1: "QGEMV_ERR_INVALID_ARG", 2: "QGEMV_ERR_MISALIGNED", 3: "QGEMV_ERR_UNSUPPORTED",
+          4: "QGEMV_ERR_WORKSPACE", 5: "QGEMV_ERR_CUDA", 6: "QGEMV_ERR_TIMEOUT", 7: "QGEMV_ERR_BAD_ID",
+          8: "QGEMV_ERR_INTERNAL"}
+
+
+class QgemvError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {STATUS.get(code, code)}")
+        self.code = code
+
+
+class SeqItem(ctypes.Structure):
+    _fields_ = [("W", ctypes.c_void_p), ("xq", ctypes.c_void_p), ("y", ctypes.c_void_p),
+                ("N", ctypes.c_int64), ("K", ctypes.c_int64)]
+
+
+class GatherMatrix(ctypes.Structure):
+    _fields_ = [("W", ctypes.c_void_p), ("expert_stride", ctypes.c_int64), ("xq", ctypes.c_void_p),
+                ("xq_stride", ctypes.c_int64), ("y", ctypes.c_void_p), ("y_stride", ctypes.c_int64),
+                ("N", ctypes.c_int64), ("K", ctypes.c_int64)]
+
+
+_lib = None
+
+_VP, _I64, _I32, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
+_SIGS = {
+    "qgemv_status_string": ([_I32], ctypes.c_char_p),
+    "qgemv_version": ([], _I32),
+    "qgemv_q4_0_bytes": ([_I64, _I64], _SZ),
+    "qgemv_xq_bytes": ([_I32, _I64], _SZ),
+    "qgemv_pack_q4_0": ([_VP, _VP, _I64, _I64, _VP], _I32),
+    "qgemv_unpack_q4_0": ([_VP, _VP, _I64, _I64, _VP], _I32),
+    "qgemv_quantize_q8_0": ([_VP, _VP, _I32, _I64, _I32, _VP], _I32),
+    "qgemv_workspace_bytes": ([_I64, _I64, _I32], _SZ),
+    "qgemv_q4_0": ([_VP, _I32, _VP, _VP, _I64, _I64, _I32, _VP, _SZ, _VP], _I32),
+    "qgemv_q4_0_f32": ([_VP, _I32, _VP, _VP, _I64, _I64, _I32, _VP, _SZ, _VP], _I32),
+    "qgemv_q4_0_argmax": ([_VP, _I32, _VP, _VP, _VP, _I64, _I64, _I32, _VP, _SZ, _VP], _I32),
+    "qgemv_seq_workspace_bytes": ([ctypes.POINTER(SeqItem), _I32, _I32], _SZ),
+    "qgemv_q4_0_seq": ([ctypes.POINTER(SeqItem), _I32, _I32, _I32, _VP, _SZ, _VP], _I32),
+    "qgemv_gather_workspace_bytes": ([ctypes.POINTER(GatherMatrix), _I32, _I32, _I32], _SZ),
+    "qgemv_q4_0_gather": ([ctypes.POINTER(GatherMatrix), _I32, _VP, _I32, _I32, _I32, _I32, _VP, _SZ, _VP], _I32),
+    "qgemv_debug_block_isums": ([_VP, _I32, _VP, _VP, _I64, _I64, _I32, _VP], _I32),
+    "qgemv_device_status": ([ctypes.POINTER(ctypes.c_int)], _I32),
+}
+
+
+def lib_path() -> str:
+    return _build.LIB
+
+
+def lib() -> ctypes.CDLL:
+    """The loaded C library (raises if it has not been built)."""
+    global _lib
+    if _lib is None:
+        if not os.path.exists(_build.LIB):
+            raise RuntimeError(f"libqgemv is not built ({_build.LIB} missing): run "
+                               "quantized_q4_weight_gb300._build.build() first")
+        L = ctypes.CDLL(_build.LIB)
+        for name, (args, res) in _SIGS.items():
+            f = getattr(L, name)
+            f.argtypes = args
+            f.restype = res
+        _lib = L
+    return _lib
+
+
+def _check(code: int, what: str):
+    if code != 0:
+        raise QgemvError(code, what)
+
+
+def _stream(stream=None):
+    s = stream if stream is not None else torch.cuda.current_stream()
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def _ptr(t):
+    if t is None:
+        return None
+    assert t.is_cuda and t.is_contiguous(), "tensors must be contiguous CUDA tensors"
+    return ctypes.c_void_p(t.data_ptr())
+
+
+# ----------------------------------------------------------------- sizes
+
+def q4_0_bytes(N: int, K: int) -> int:
+    return int(lib().qgemv_q4_0_bytes(N, K))
+
+
+def xq_bytes(R: int, K: int) -> int:
+    return int(lib().qgemv_xq_bytes(R, K))
+
+
+def workspace_bytes(N: int, K: int, T: int) -> int:
+    return int(lib().qgemv_workspace_bytes(N, K, T))
+
+
+def new_workspace(nbytes: int, device=None) -> torch.Tensor:
+    """A zero-filled workspace (the library keeps its counters at zero)."""
+    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
+
+
+# ----------------------------------------------------------------- calls
+
+def pack_q4_0(w_ggml: torch.Tensor, N: int, K: int, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    out = out if out is not None else torch.empty(q4_0_bytes(N, K), dtype=torch.uint8, device=w_ggml.device)
+    _check(lib().qgemv_pack_q4_0(_ptr(w_ggml), _ptr(out), N, K, _stream(stream)), "qgemv_pack_q4_0")
+    return out
+
+
+def unpack_q4_0(w_packed: torch.Tensor, N: int, K: int, out: torch.Tensor | None = None, stream=None):
+    out = out if out is not None else torch.empty(q4_0_bytes(N, K), dtype=torch.uint8, device=w_packed.device)
+    _check(lib().qgemv_unpack_q4_0(_ptr(w_packed), _ptr(out), N, K, _stream(stream)), "qgemv_unpack_q4_0")
+    return out
+
+
+def quantize_q8_0(x: torch.Tensor, R: int, K: int, batch: int = 1, out: torch.Tensor | None = None, stream=None):
+    """x fp32 [batch, R, K] (any shape with that many elements) -> planar Q8_0 bytes."""
+    assert x.dtype == torch.float32 and x.numel() == batch * R * K
+    out = out if out is not None else torch.empty(batch * xq_bytes(R, K), dtype=torch.uint8, device=x.device)
+    _check(lib().qgemv_quantize_q8_0(_ptr(x), _ptr(out), R, K, batch, _stream(stream)), "qgemv_quantize_q8_0")
+    return out
+
+
+def gemv(W, layout: int, xq, N: int, K: int, T: int, ws, y=None, stream=None) -> torch.Tensor:
+    y = y if y is not None else torch.empty((T, N), dtype=torch.float32, device=W.device)
+    _check(lib().qgemv_q4_0(_ptr(W), layout, _ptr(xq), _ptr(y), N, K, T, _ptr(ws), ws.numel(), _stream(stream)),
+           "qgemv_q4_0")
+    return y
+
+
+def gemv_f32(W, layout: int, x, N: int, K: int, T: int, ws, y=None, stream=None) -> torch.Tensor:
+    y = y if y is not None else torch.empty((T, N), dtype=torch.float32, device=W.device)
+    _check(lib().qgemv_q4_0_f32(_ptr(W), layout, _ptr(x), _ptr(y), N, K, T, _ptr(ws), ws.numel(), _stream(stream)),
+           "qgemv_q4_0_f32")
+    return y
+
+
+def gemv_argmax(W, layout: int, xq, N: int, K: int, T: int, ws, y=None, idx=None, stream=None):
+    idx = idx if idx is not None else torch.empty(T, dtype=torch.int64, device=W.device)
+    _check(lib().qgemv_q4_0_argmax(_ptr(W), layout, _ptr(xq), _ptr(y), _ptr(idx), N, K, T, _ptr(ws), ws.numel(),
+                                   _stream(stream)), "qgemv_q4_0_argmax")
+    return idx
+
+
+def seq_items(entries) -> ctypes.Array:
+    """entries: iterable of (W, xq, y, N, K) with CUDA tensors."""
+    entries = list(entries)
+    arr = (SeqItem * len(entries))()
+    for i, (W, xq, y, N, K) in enumerate(entries):
+        arr[i] = SeqItem(W.data_ptr(), xq.data_ptr(), y.data_ptr(), N, K)
+    return arr
+
+
+def seq_workspace_bytes(items: ctypes.Array, T: int) -> int:
+    return int(lib().qgemv_seq_workspace_bytes(items, len(items), T))
+
+
+def gemv_seq(items: ctypes.Array, layout: int, T: int, ws, stream=None):
+    _check(lib().qgemv_q4_0_seq(items, len(items), layout, T, _ptr(ws), ws.numel(), _stream(stream)),
+           "qgemv_q4_0_seq")
+
+
+def gather_mats(entries) -> ctypes.Array:
+    """entries: (W, expert_stride_bytes, xq, xq_stride_bytes, y, y_stride_floats, N, K)."""
+    entries = list(entries)
+    arr = (GatherMatrix * len(entries))()
+    for i, (W, ws_, xq, xs, y, ys, N, K) in enumerate(entries):
+        arr[i] = GatherMatrix(W.data_ptr(), ws_, xq.data_ptr(), xs, y.data_ptr(), ys, N, K)
+    return arr
+
+
+def gather_workspace_bytes(mats: ctypes.Array, n_ids: int, T: int) -> int:
+    return int(lib().qgemv_gather_workspace_bytes(mats, len(mats), n_ids, T))
+
+
+def gemv_gather(mats: ctypes.Array, ids, n_experts: int, layout: int, T: int, ws, stream=None):
+    _check(lib().qgemv_q4_0_gather(mats, len(mats), _ptr(ids), ids.numel(), n_experts, layout, T, _ptr(ws),
+                                   ws.numel(), _stream(stream)), "qgemv_q4_0_gather")
+
+
+def block_isums(W, layout: int, xq, N: int, K: int, T: int, stream=None) -> torch.Tensor:
+    out = torch.empty((T, N, K // QK), dtype=torch.int32, device=W.device)
+    _check(lib().qgemv_debug_block_isums(_ptr(W), layout, _ptr(xq), _ptr(out), N, K, T, _stream(stream)),
+           "qgemv_debug_block_isums")
+    return out
+
+
+def device_status() -> int:
+    """Read and clear the device status word (synchronises)."""
+    code = ctypes.c_int(0)
+    _check(lib().qgemv_device_status(ctypes.byref(code)), "qgemv_device_status")
+    return int(code.value)

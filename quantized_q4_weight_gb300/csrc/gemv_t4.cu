@@ -1,0 +1,8 @@
+// gemv_t4.cu -- streaming GEMV kernel instantiations for T = 4 token columns.
+#include "launch_stream.cuh"
+
+namespace qg {
+template cudaError_t launch_stream<4, MAXG_SMALL, false>(const Params<MAXG_SMALL> &, int, size_t, cudaStream_t, bool);
+template cudaError_t launch_stream<4, MAXG_SMALL, true>(const Params<MAXG_SMALL> &, int, size_t, cudaStream_t, bool);
+template cudaError_t launch_stream<4, MAXG_SEQ, false>(const Params<MAXG_SEQ> &, int, size_t, cudaStream_t, bool);
+}  // namespace qg

@@ -1,0 +1,172 @@
+// kernels_misc.cu -- activation quantiser, weight pack / unpack and the
+// block-sum test hook.
+#include "qgemv_launch.h"
+
+namespace qg {
+
+// ------------------------------------------------------------ Q8_0 quantiser
+//
+// One warp per block of 32 activations (minfer README "How it works": int8
+// activations; colibri qwen36 docs, dense int8 IDOT GEMV: scale amax/127):
+// amax by a shuffle tree of fmaxf (exact), d = amax / 127 (IEEE division),
+// 1/d from the fp32 d (0 when d = 0), q = roundf(x * (1/d)) -- roundf rounds
+// halfway cases away from zero -- and d stored as fp16, round to nearest even.
+__global__ void __launch_bounds__(256) quantize_q8_0_kernel(const float *__restrict__ x, uint8_t *__restrict__ xq,
+                                                            int R, int K, long long nblocks, long long xq_bytes)
+{
+    pdl_launch_dependents();
+    pdl_wait();
+    const int nb = K / QK;
+    const int lane = threadIdx.x & 31;
+    const long long per_batch = static_cast<long long>(R) * nb;
+    for (long long gb = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; gb < nblocks;
+         gb += (static_cast<long long>(gridDim.x) * blockDim.x) >> 5) {
+        const long long bi = gb / per_batch;
+        const long long rem = gb - bi * per_batch;
+        const int r = static_cast<int>(rem / nb), b = static_cast<int>(rem - static_cast<long long>(r) * nb);
+        const float v = __ldg(x + (bi * R + r) * K + b * QK + lane);
+        float amax = fabsf(v);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+        const float d = __fdiv_rn(amax, 127.0f);
+        const float id = (d != 0.0f) ? __fdiv_rn(1.0f, d) : 0.0f;
+        const float q = roundf(__fmul_rn(v, id));
+        uint8_t *dst = xq + bi * xq_bytes;
+        dst[static_cast<long long>(r) * K + b * QK + lane] = static_cast<uint8_t>(static_cast<int8_t>(static_cast<int>(q)));
+        if (lane == 0) {
+            const unsigned short dh = __half_as_ushort(__float2half_rn(d));
+            reinterpret_cast<unsigned short *>(dst + static_cast<long long>(R) * K)[rem] = dh;
+        }
+        if (rem == 0) {  // zero the padding after the scales
+            const long long used = static_cast<long long>(R) * K + 2 * per_batch;
+            if (used + lane < xq_bytes) dst[used + lane] = 0;
+        }
+    }
+}
+
+cudaError_t launch_quantize(const float *x, void *xq, int R, long long K, int batch, cudaStream_t st)
+{
+    const long long nblocks = static_cast<long long>(batch) * R * (K / QK);
+    const long long xqb = static_cast<long long>(xq_bytes_host(R, K));
+    long long grid = (nblocks + 7) / 8;
+    if (grid > 65535) grid = 65535;
+    quantize_q8_0_kernel<<<static_cast<unsigned>(grid), 256, 0, st>>>(x, static_cast<uint8_t *>(xq), R,
+                                                                    static_cast<int>(K), nblocks, xqb);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------ pack / unpack
+//
+// Packed layout (see include/qgemv.h): slab s of rows [16s, 16s+16) holds
+// quads q of nbq = min(4, nb - 4q) blocks at s * 288 * nb + 1152 * q:
+// nibbles [r][jq][16 bytes], then fp16 scales [r % 8][jq][r / 8].  Rows past
+// the last full slab keep their GGML position, so the byte offset of their
+// blocks is the same in both layouts.
+
+__device__ __forceinline__ void packed_offsets(long long row, int b, int nb, long long &nib_off, long long &sc_off)
+{
+    const long long s = row / SLAB_ROWS;
+    const int r = static_cast<int>(row - s * SLAB_ROWS);
+    const int q = b / QUAD, jq = b - q * QUAD;
+    const int nbq = min(QUAD, nb - q * QUAD);
+    const long long base = s * static_cast<long long>(SLAB_COL_BYTES) * nb + static_cast<long long>(q) * QUAD_BYTES;
+    nib_off = base + (r * nbq + jq) * 16;
+    sc_off = base + 256 * nbq + ((r % 8) * nbq + jq) * 4 + (r / 8) * 2;
+}
+
+__global__ void __launch_bounds__(256) pack_kernel(const uint8_t *__restrict__ src, uint8_t *__restrict__ dst,
+                                                   long long N, int nb, bool to_packed)
+{
+    const long long nfull = N / SLAB_ROWS;
+    const long long total = N * nb;
+    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const long long row = i / nb;
+        const int b = static_cast<int>(i - row * nb);
+        const long long g_off = i * Q4_BYTES;
+        if (row >= nfull * SLAB_ROWS) {  // tail rows: same offset in both layouts
+            const unsigned short *s16 = reinterpret_cast<const unsigned short *>(src + g_off);
+            unsigned short *d16 = reinterpret_cast<unsigned short *>(dst + g_off);
+#pragma unroll
+            for (int k = 0; k < 9; ++k) d16[k] = s16[k];
+            continue;
+        }
+        long long nib_off, sc_off;
+        packed_offsets(row, b, nb, nib_off, sc_off);
+        if (to_packed) {
+            uint4 nib;
+            unsigned d;
+            load_ggml_block(src + g_off, nib, d);
+            *reinterpret_cast<uint4 *>(dst + nib_off) = nib;
+            *reinterpret_cast<unsigned short *>(dst + sc_off) = static_cast<unsigned short>(d);
+        } else {
+            const uint4 nib = *reinterpret_cast<const uint4 *>(src + nib_off);
+            const unsigned short d = *reinterpret_cast<const unsigned short *>(src + sc_off);
+            unsigned short *d16 = reinterpret_cast<unsigned short *>(dst + g_off);
+            d16[0] = d;
+            const unsigned w[4] = {nib.x, nib.y, nib.z, nib.w};
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                d16[1 + 2 * k] = static_cast<unsigned short>(w[k] & 0xFFFFu);
+                d16[2 + 2 * k] = static_cast<unsigned short>(w[k] >> 16);
+            }
+        }
+    }
+}
+
+cudaError_t launch_pack(const void *src, void *dst, long long N, long long K, bool to_packed, cudaStream_t st)
+{
+    const long long total = N * (K / QK);
+    long long grid = (total + 255) / 256;
+    if (grid > 65535) grid = 65535;
+    pack_kernel<<<static_cast<unsigned>(grid), 256, 0, st>>>(static_cast<const uint8_t *>(src),
+                                                           static_cast<uint8_t *>(dst), N,
+                                                           static_cast<int>(K / QK), to_packed);
+    return cudaGetLastError();
+}
+
+// ------------------------------------------------------------ block sums (test hook)
+//
+// Same unpack, dp4a chain and folded offset as the GEMV kernel
+// (block_dot_magic / block_fold_const), minus the magic bias.
+__global__ void __launch_bounds__(256) isums_kernel(const uint8_t *__restrict__ W, bool packed,
+                                                    const uint8_t *__restrict__ xq, int32_t *__restrict__ isums,
+                                                    long long N, int K, int T)
+{
+    const int nb = K / QK;
+    const long long nfull = N / SLAB_ROWS;
+    const long long total = static_cast<long long>(T) * N * nb;
+    for (long long i = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; i < total;
+         i += static_cast<long long>(gridDim.x) * blockDim.x) {
+        const long long t = i / (N * nb);
+        const long long rem = i - t * N * nb;
+        const long long row = rem / nb;
+        const int b = static_cast<int>(rem - row * nb);
+        uint4 nib;
+        if (packed && row < nfull * SLAB_ROWS) {
+            long long nib_off, sc_off;
+            packed_offsets(row, b, nb, nib_off, sc_off);
+            nib = *reinterpret_cast<const uint4 *>(W + nib_off);
+        } else {
+            unsigned d;
+            load_ggml_block(W + (row * nb + b) * Q4_BYTES, nib, d);
+        }
+        const uint4 *xp = reinterpret_cast<const uint4 *>(xq + t * K + static_cast<long long>(b) * QK);
+        const uint4 qa = xp[0], qb = xp[1];
+        isums[i] = block_dot_magic(nib, qa, qb, block_fold_const(qa, qb)) - MAGIC_I;
+    }
+}
+
+cudaError_t launch_isums(const void *W, bool packed, const void *xq, int32_t *isums, long long N, long long K, int T,
+                         cudaStream_t st)
+{
+    const long long total = static_cast<long long>(T) * N * (K / QK);
+    long long grid = (total + 255) / 256;
+    if (grid > 65535) grid = 65535;
+    isums_kernel<<<static_cast<unsigned>(grid), 256, 0, st>>>(static_cast<const uint8_t *>(W), packed,
+                                                            static_cast<const uint8_t *>(xq), isums, N,
+                                                            static_cast<int>(K), T);
+    return cudaGetLastError();
+}
+
+}  // namespace qg

@@ -1,0 +1,541 @@
+// qgemv_api.cu -- the C ABI of libqgemv (include/qgemv.h): argument
+// validation, launch planning and kernel launches.  Host code only, apart
+// from the per-device status word.
+#include <cstring>
+#include <memory>
+#include <mutex>
+#include <vector>
+
+#include "../../include/qgemv.h"
+#include "qgemv_launch.h"
+
+using namespace qg;
+
+// Per-device status word: kernels record the first asynchronous error here.
+__device__ unsigned g_qgemv_status = 0;
+
+namespace {
+
+constexpr int kMaxDevices = 64;
+
+struct DevInfo {
+    bool ready = false;
+    int sms = 0;
+    int smem_optin = 0;
+    unsigned *status = nullptr;
+};
+
+std::mutex g_dev_mu;
+DevInfo g_dev[kMaxDevices];
+
+qgemv_status device_info(DevInfo &out)
+{
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QGEMV_ERR_CUDA;
+    std::lock_guard<std::mutex> lock(g_dev_mu);
+    DevInfo &d = g_dev[dev];
+    if (!d.ready) {
+        if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return QGEMV_ERR_CUDA;
+        if (cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            return QGEMV_ERR_CUDA;
+        void *p = nullptr;
+        if (cudaGetSymbolAddress(&p, g_qgemv_status) != cudaSuccess) return QGEMV_ERR_CUDA;
+        d.status = static_cast<unsigned *>(p);
+        d.ready = true;
+    }
+    out = d;
+    return QGEMV_OK;
+}
+
+inline bool aligned(const void *p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+inline long long align_up(long long v, long long a) { return (v + a - 1) / a * a; }
+
+struct Range {
+    uintptr_t lo, hi;
+};
+inline Range range(const void *p, long long bytes)
+{
+    const uintptr_t a = reinterpret_cast<uintptr_t>(p);
+    return Range{a, a + static_cast<uintptr_t>(bytes)};
+}
+inline bool overlap(Range a, Range b) { return a.lo < b.hi && b.lo < a.hi; }
+
+bool shape_ok(long long N, long long K)
+{
+    return N >= 1 && N < (1ll << 31) && K >= QK && K % QK == 0 && K <= (1ll << 24) && N * (K / QK) < (1ll << 40);
+}
+
+// One matrix family of a launch, as the caller describes it.
+struct GroupSpec {
+    const void *W;
+    long long w_stride;
+    const void *xq;
+    long long xq_stride;
+    float *y;
+    long long y_stride;
+    long long N, K;
+    int count;
+};
+
+// Launch plan: the kernel parameter block (without device pointers into the
+// workspace until `ws` is given), the workspace size and the shared memory.
+template <int MAXG>
+struct Plan {
+    Params<MAXG> P;
+    long long ws_bytes = 0;
+    size_t smem = 0;
+};
+
+// Workspace layout: [arrival counter, 256 B][argmax candidates][split-K
+// counters and partials per split group].
+template <int MAXG>
+qgemv_status make_plan(const GroupSpec *gs, int n, int T, bool ggml, bool argmax, uint8_t *ws, int smem_limit,
+                       Plan<MAXG> &pl)
+{
+    if (n < 1 || n > MAXG) return QGEMV_ERR_INTERNAL;
+    Params<MAXG> &P = pl.P;
+    memset(&P, 0, sizeof(P));
+    P.ngroups = n;
+    P.ggml = ggml ? 1 : 0;
+    long long total_slabs = 0;
+    for (int i = 0; i < n; ++i) {
+        const long long nb = gs[i].K / QK;
+        const long long nslabs = ggml ? (gs[i].N + SLAB_ROWS - 1) / SLAB_ROWS : gs[i].N / SLAB_ROWS;
+        total_slabs += nslabs * gs[i].count;
+        (void)nb;
+    }
+    long long off = 256;  // argmax arrival counter lives at offset 0
+    if (argmax) {
+        P.am_cnt = ws ? reinterpret_cast<unsigned *>(ws) : nullptr;
+        P.am_cand = ws ? reinterpret_cast<unsigned long long *>(ws + off) : nullptr;
+        off = align_up(off + static_cast<long long>(MAX_GRID) * T * 8, 256);
+    }
+    long long bytes = 0, items = 0;
+    int kmax = 0, nbmax = 0;
+    for (int i = 0; i < n; ++i) {
+        Group &g = P.g[i];
+        const GroupSpec &s = gs[i];
+        g.W = static_cast<const uint8_t *>(s.W);
+        g.w_stride = s.w_stride;
+        g.xq = static_cast<const uint8_t *>(s.xq);
+        g.xq_stride = s.xq_stride;
+        g.y = s.y;
+        g.y_stride = s.y_stride;
+        g.N = static_cast<int>(s.N);
+        g.K = static_cast<int>(s.K);
+        g.count = s.count;
+        g.nb = g.K / QK;
+        g.nseg = (g.nb + SEG_BLOCKS - 1) / SEG_BLOCKS;
+        if (ggml) {
+            g.nslabs = (g.N + SLAB_ROWS - 1) / SLAB_ROWS;
+            g.tail_rows = 0;
+        } else {
+            g.nslabs = g.N / SLAB_ROWS;
+            g.tail_rows = g.N % SLAB_ROWS;
+        }
+        g.split = (g.nseg > 1 && g.nslabs > 0 && total_slabs < SPLIT_SLAB_THRESHOLD) ? g.nseg : 1;
+        g.items_per_inst = g.nslabs * g.split + (g.tail_rows > 0 ? 1 : 0);
+        g.xq_bytes = static_cast<int>(xq_bytes_host(T, g.K));
+        g.slab_bytes = static_cast<long long>(SLAB_COL_BYTES) * g.nb;
+        g.inst_bytes = g.nslabs * g.slab_bytes + static_cast<long long>(g.tail_rows) * g.nb * Q4_BYTES;
+        g.byte_begin = bytes;
+        g.item_begin = items;
+        bytes += g.inst_bytes * g.count;
+        items += static_cast<long long>(g.items_per_inst) * g.count;
+        if (g.split > 1) {
+            const long long nc = static_cast<long long>(g.count) * g.nslabs;
+            g.cnt = ws ? reinterpret_cast<unsigned *>(ws + off) : nullptr;
+            off = align_up(off + nc * 4, 256);
+            g.part = ws ? reinterpret_cast<float *>(ws + off) : nullptr;
+            off = align_up(off + nc * g.nseg * T * 16 * 4, 256);
+        }
+        if (g.K > kmax) kmax = g.K;
+        if (g.nb > nbmax) nbmax = g.nb;
+    }
+    P.total_bytes = bytes;
+    P.total_items = items;
+    P.kmax = kmax;
+    P.nbmax = nbmax;
+    pl.ws_bytes = off;
+
+    // Shared memory: activations [T][kmax], scales, folded constants, barriers, rings.
+    const long long xsize = static_cast<long long>(T) * kmax;
+    const long long dsize = roundup16(2ll * T * nbmax);
+    P.off_d = static_cast<int>(xsize);
+    P.off_cd = static_cast<int>(align_up(xsize + dsize, 16));
+    P.off_bar = static_cast<int>(align_up(P.off_cd + 8ll * T * nbmax, 128));
+    P.ring_depth = 0;
+    for (int D = MAX_RING; D >= 1; --D) {
+        const long long ring_off = align_up(P.off_bar + 8ll * (NWARPS * D + 1), 128);
+        const long long total = ring_off + (ggml ? 0 : static_cast<long long>(NWARPS) * D * SEG_BYTES);
+        if (smem_limit <= 0 || total <= smem_limit) {
+            P.ring_depth = D;
+            P.off_ring = static_cast<int>(ring_off);
+            pl.smem = static_cast<size_t>(total);
+            break;
+        }
+    }
+    if (P.ring_depth == 0) return QGEMV_ERR_UNSUPPORTED;
+    return QGEMV_OK;
+}
+
+template <int MAXG, bool ARGMAX>
+cudaError_t dispatch_T(const Params<MAXG> &P, int T, int grid, size_t smem, cudaStream_t st, bool pdl)
+{
+    switch (T) {
+    case 1: return launch_stream<1, MAXG, ARGMAX>(P, grid, smem, st, pdl);
+    case 2: return launch_stream<2, MAXG, ARGMAX>(P, grid, smem, st, pdl);
+    case 3: return launch_stream<3, MAXG, ARGMAX>(P, grid, smem, st, pdl);
+    case 4: return launch_stream<4, MAXG, ARGMAX>(P, grid, smem, st, pdl);
+    case 5: return launch_stream<5, MAXG, ARGMAX>(P, grid, smem, st, pdl);
+    case 6: return launch_stream<6, MAXG, ARGMAX>(P, grid, smem, st, pdl);
+    case 7: return launch_stream<7, MAXG, ARGMAX>(P, grid, smem, st, pdl);
+    case 8: return launch_stream<8, MAXG, ARGMAX>(P, grid, smem, st, pdl);
+    default: return cudaErrorInvalidValue;
+    }
+}
+
+// The dynamic shared-memory budget of one CTA (static arrays of the kernel
+// take well under 1 KB).
+inline int smem_budget(const DevInfo &d) { return d.smem_optin - 1024; }
+
+// Shared argument checks of the single-matrix GEMV calls.
+qgemv_status check_single(const void *W, qgemv_wlayout layout, const void *xin, long long xin_bytes,
+                          const float *y, long long N, long long K, int T, const void *ws)
+{
+    if (!shape_ok(N, K) || T < 1 || T > 8) return QGEMV_ERR_INVALID_ARG;
+    if (layout != QGEMV_W_GGML && layout != QGEMV_W_PACKED) return QGEMV_ERR_INVALID_ARG;
+    if (!W || !xin) return QGEMV_ERR_INVALID_ARG;
+    if (!aligned(W, layout == QGEMV_W_PACKED ? 16 : 2)) return QGEMV_ERR_MISALIGNED;
+    if (ws && !aligned(ws, 256)) return QGEMV_ERR_MISALIGNED;
+    if (y) {
+        if (!aligned(y, 4)) return QGEMV_ERR_MISALIGNED;
+        const Range ry = range(y, 4ll * T * N);
+        if (overlap(ry, range(W, 18ll * N * (K / QK))) || overlap(ry, range(xin, xin_bytes)))
+            return QGEMV_ERR_INVALID_ARG;
+    }
+    return QGEMV_OK;
+}
+
+long long single_ws_bytes(long long N, long long K, int T, bool with_xq, long long *xq_off)
+{
+    GroupSpec gs{nullptr, 0, nullptr, 0, nullptr, 0, N, K, 1};
+    Plan<MAXG_SMALL> pl;
+    make_plan<MAXG_SMALL>(&gs, 1, T, false, true, nullptr, 0, pl);
+    Plan<MAXG_SMALL> pg;  // the GGML layout splits its partial slab too
+    make_plan<MAXG_SMALL>(&gs, 1, T, true, true, nullptr, 0, pg);
+    long long b = pl.ws_bytes > pg.ws_bytes ? pl.ws_bytes : pg.ws_bytes;
+    if (xq_off) *xq_off = b;
+    if (with_xq) b += align_up(xq_bytes_host(T, K), 256);
+    return b;
+}
+
+qgemv_status run_single(const void *W, qgemv_wlayout layout, const void *xq, float *y, long long *idx, long long N,
+                        long long K, int T, void *ws, size_t ws_bytes, cudaStream_t st, bool argmax, bool pdl)
+{
+    DevInfo dev;
+    qgemv_status s = device_info(dev);
+    if (s != QGEMV_OK) return s;
+    GroupSpec gs{W, 0, xq, 0, y, 0, N, K, 1};
+    Plan<MAXG_SMALL> pl;
+    s = make_plan<MAXG_SMALL>(&gs, 1, T, layout == QGEMV_W_GGML, argmax, static_cast<uint8_t *>(ws),
+                              smem_budget(dev), pl);
+    if (s != QGEMV_OK) return s;
+    if (static_cast<long long>(ws_bytes) < pl.ws_bytes) return QGEMV_ERR_WORKSPACE;
+    pl.P.status = dev.status;
+    pl.P.am_idx = reinterpret_cast<long long *>(idx);
+    const int grid = dev.sms < MAX_GRID ? dev.sms : MAX_GRID;
+    const cudaError_t e = argmax ? dispatch_T<MAXG_SMALL, true>(pl.P, T, grid, pl.smem, st, pdl)
+                                 : dispatch_T<MAXG_SMALL, false>(pl.P, T, grid, pl.smem, st, pdl);
+    return e == cudaSuccess ? QGEMV_OK : QGEMV_ERR_CUDA;
+}
+
+}  // namespace
+
+// =====================================================================
+extern "C" {
+
+const char *qgemv_status_string(qgemv_status s)
+{
+    switch (s) {
+    case QGEMV_OK: return "QGEMV_OK";
+    case QGEMV_ERR_INVALID_ARG: return "QGEMV_ERR_INVALID_ARG";
+    case QGEMV_ERR_MISALIGNED: return "QGEMV_ERR_MISALIGNED";
+    case QGEMV_ERR_UNSUPPORTED: return "QGEMV_ERR_UNSUPPORTED";
+    case QGEMV_ERR_WORKSPACE: return "QGEMV_ERR_WORKSPACE";
+    case QGEMV_ERR_CUDA: return "QGEMV_ERR_CUDA";
+    case QGEMV_ERR_TIMEOUT: return "QGEMV_ERR_TIMEOUT";
+    case QGEMV_ERR_BAD_ID: return "QGEMV_ERR_BAD_ID";
+    case QGEMV_ERR_INTERNAL: return "QGEMV_ERR_INTERNAL";
+    }
+    return "QGEMV_UNKNOWN_STATUS";
+}
+
+int qgemv_version(void) { return 100; }
+
+size_t qgemv_q4_0_bytes(int64_t N, int64_t K)
+{
+    if (!shape_ok(N, K)) return 0;
+    return static_cast<size_t>(18ll * N * (K / QK));
+}
+
+size_t qgemv_xq_bytes(int R, int64_t K)
+{
+    if (R < 1 || K < QK || K % QK != 0 || K > (1ll << 24)) return 0;
+    return static_cast<size_t>(xq_bytes_host(R, K));
+}
+
+qgemv_status qgemv_pack_q4_0(const void *w_ggml, void *w_packed, int64_t N, int64_t K, qgemv_stream_t stream)
+{
+    if (!shape_ok(N, K) || !w_ggml || !w_packed) return QGEMV_ERR_INVALID_ARG;
+    if (!aligned(w_packed, 16) || !aligned(w_ggml, 2)) return QGEMV_ERR_MISALIGNED;
+    const long long bytes = 18ll * N * (K / QK);
+    if (overlap(range(w_ggml, bytes), range(w_packed, bytes))) return QGEMV_ERR_INVALID_ARG;
+    return launch_pack(w_ggml, w_packed, N, K, true, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? QGEMV_OK
+               : QGEMV_ERR_CUDA;
+}
+
+qgemv_status qgemv_unpack_q4_0(const void *w_packed, void *w_ggml, int64_t N, int64_t K, qgemv_stream_t stream)
+{
+    if (!shape_ok(N, K) || !w_ggml || !w_packed) return QGEMV_ERR_INVALID_ARG;
+    if (!aligned(w_packed, 16) || !aligned(w_ggml, 2)) return QGEMV_ERR_MISALIGNED;
+    const long long bytes = 18ll * N * (K / QK);
+    if (overlap(range(w_ggml, bytes), range(w_packed, bytes))) return QGEMV_ERR_INVALID_ARG;
+    return launch_pack(w_packed, w_ggml, N, K, false, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? QGEMV_OK
+               : QGEMV_ERR_CUDA;
+}
+
+qgemv_status qgemv_quantize_q8_0(const float *x, void *xq, int R, int64_t K, int batch, qgemv_stream_t stream)
+{
+    if (!x || !xq || R < 1 || batch < 1 || K < QK || K % QK != 0 || K > (1ll << 24)) return QGEMV_ERR_INVALID_ARG;
+    if (static_cast<long long>(R) * batch > (1ll << 31)) return QGEMV_ERR_INVALID_ARG;
+    if (!aligned(xq, 16) || !aligned(x, 4)) return QGEMV_ERR_MISALIGNED;
+    if (overlap(range(x, 4ll * batch * R * K), range(xq, xq_bytes_host(R, K) * batch))) return QGEMV_ERR_INVALID_ARG;
+    return launch_quantize(x, xq, R, K, batch, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? QGEMV_OK
+               : QGEMV_ERR_CUDA;
+}
+
+size_t qgemv_workspace_bytes(int64_t N, int64_t K, int T)
+{
+    if (!shape_ok(N, K) || T < 1 || T > 8) return 0;
+    return static_cast<size_t>(single_ws_bytes(N, K, T, true, nullptr));
+}
+
+qgemv_status qgemv_q4_0(const void *W, qgemv_wlayout layout, const void *xq, float *y, int64_t N, int64_t K, int T,
+                        void *ws, size_t ws_bytes, qgemv_stream_t stream)
+{
+    qgemv_status s = check_single(W, layout, xq, shape_ok(N, K) ? xq_bytes_host(T, K) : 0, y, N, K, T, ws);
+    if (s != QGEMV_OK) return s;
+    if (!y) return QGEMV_ERR_INVALID_ARG;
+    if (!aligned(xq, 16)) return QGEMV_ERR_MISALIGNED;
+    if (!ws) return QGEMV_ERR_WORKSPACE;
+    if (overlap(range(y, 4ll * T * N), range(ws, static_cast<long long>(ws_bytes)))) return QGEMV_ERR_INVALID_ARG;
+    return run_single(W, layout, xq, y, nullptr, N, K, T, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream), false,
+                      false);
+}
+
+qgemv_status qgemv_q4_0_f32(const void *W, qgemv_wlayout layout, const float *x, float *y, int64_t N, int64_t K,
+                            int T, void *ws, size_t ws_bytes, qgemv_stream_t stream)
+{
+    qgemv_status s = check_single(W, layout, x, 4ll * T * K, y, N, K, T, ws);
+    if (s != QGEMV_OK) return s;
+    if (!y) return QGEMV_ERR_INVALID_ARG;
+    if (!aligned(x, 4)) return QGEMV_ERR_MISALIGNED;
+    if (!ws) return QGEMV_ERR_WORKSPACE;
+    long long xq_off = 0;
+    const long long need = single_ws_bytes(N, K, T, true, &xq_off);
+    if (static_cast<long long>(ws_bytes) < need) return QGEMV_ERR_WORKSPACE;
+    if (overlap(range(y, 4ll * T * N), range(ws, need)) || overlap(range(x, 4ll * T * K), range(ws, need)))
+        return QGEMV_ERR_INVALID_ARG;
+    uint8_t *xq = static_cast<uint8_t *>(ws) + xq_off;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (launch_quantize(x, xq, T, K, 1, st) != cudaSuccess) return QGEMV_ERR_CUDA;
+    // The GEMV only reads what the quantiser writes after griddepcontrol.wait,
+    // so it may start (and stream weights) while the quantiser runs.
+    return run_single(W, layout, xq, y, nullptr, N, K, T, ws, static_cast<size_t>(xq_off), st, false, true);
+}
+
+qgemv_status qgemv_q4_0_argmax(const void *W, qgemv_wlayout layout, const void *xq, float *y_or_null, int64_t *idx,
+                               int64_t N, int64_t K, int T, void *ws, size_t ws_bytes, qgemv_stream_t stream)
+{
+    qgemv_status s = check_single(W, layout, xq, shape_ok(N, K) ? xq_bytes_host(T, K) : 0, y_or_null, N, K, T, ws);
+    if (s != QGEMV_OK) return s;
+    if (!idx) return QGEMV_ERR_INVALID_ARG;
+    if (!aligned(xq, 16) || !aligned(idx, 8)) return QGEMV_ERR_MISALIGNED;
+    if (!ws) return QGEMV_ERR_WORKSPACE;
+    const Range rw = range(ws, static_cast<long long>(ws_bytes));
+    if (overlap(range(idx, 8ll * T), rw) || (y_or_null && overlap(range(y_or_null, 4ll * T * N), rw)))
+        return QGEMV_ERR_INVALID_ARG;
+    return run_single(W, layout, xq, y_or_null, reinterpret_cast<long long *>(idx), N, K, T, ws, ws_bytes,
+                      reinterpret_cast<cudaStream_t>(stream), true, false);
+}
+
+size_t qgemv_seq_workspace_bytes(const qgemv_seq_item *items, int n, int T)
+{
+    if (!items || n < 1 || T < 1 || T > 8) return 0;
+    long long total = 0;
+    for (int c0 = 0; c0 < n; c0 += MAXG_SEQ) {
+        const int cn = (n - c0) < MAXG_SEQ ? (n - c0) : MAXG_SEQ;
+        std::vector<GroupSpec> gs(cn);
+        for (int i = 0; i < cn; ++i) {
+            const qgemv_seq_item &it = items[c0 + i];
+            if (!shape_ok(it.N, it.K)) return 0;
+            gs[i] = GroupSpec{it.W, 0, it.xq, 0, it.y, 0, it.N, it.K, 1};
+        }
+        std::unique_ptr<Plan<MAXG_SEQ>> pa(new Plan<MAXG_SEQ>()), pb(new Plan<MAXG_SEQ>());
+        make_plan<MAXG_SEQ>(gs.data(), cn, T, false, false, nullptr, 0, *pa);
+        make_plan<MAXG_SEQ>(gs.data(), cn, T, true, false, nullptr, 0, *pb);
+        const long long b = pa->ws_bytes > pb->ws_bytes ? pa->ws_bytes : pb->ws_bytes;
+        if (b > total) total = b;  // consecutive launches reuse the workspace
+    }
+    return static_cast<size_t>(total);
+}
+
+qgemv_status qgemv_q4_0_seq(const qgemv_seq_item *items, int n, qgemv_wlayout layout, int T, void *ws,
+                            size_t ws_bytes, qgemv_stream_t stream)
+{
+    if (!items || n < 1 || T < 1 || T > 8) return QGEMV_ERR_INVALID_ARG;
+    if (layout != QGEMV_W_GGML && layout != QGEMV_W_PACKED) return QGEMV_ERR_INVALID_ARG;
+    if (!ws) return QGEMV_ERR_WORKSPACE;
+    if (!aligned(ws, 256)) return QGEMV_ERR_MISALIGNED;
+    const Range rw = range(ws, static_cast<long long>(ws_bytes));
+    for (int i = 0; i < n; ++i) {
+        const qgemv_seq_item &a = items[i];
+        if (!shape_ok(a.N, a.K) || !a.W || !a.xq || !a.y) return QGEMV_ERR_INVALID_ARG;
+        if (!aligned(a.W, layout == QGEMV_W_PACKED ? 16 : 2) || !aligned(a.xq, 16) || !aligned(a.y, 4))
+            return QGEMV_ERR_MISALIGNED;
+        const Range ry = range(a.y, 4ll * T * a.N);
+        if (overlap(ry, rw)) return QGEMV_ERR_INVALID_ARG;
+        for (int k = 0; k < n; ++k) {
+            const qgemv_seq_item &b = items[k];
+            if (overlap(ry, range(b.W, 18ll * b.N * (b.K / QK))) || overlap(ry, range(b.xq, xq_bytes_host(T, b.K))))
+                return QGEMV_ERR_INVALID_ARG;
+            if (k != i && overlap(ry, range(b.y, 4ll * T * b.N))) return QGEMV_ERR_INVALID_ARG;
+        }
+    }
+    DevInfo dev;
+    qgemv_status s = device_info(dev);
+    if (s != QGEMV_OK) return s;
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    const int grid = dev.sms < MAX_GRID ? dev.sms : MAX_GRID;
+    std::vector<GroupSpec> gs(MAXG_SEQ);
+    std::unique_ptr<Plan<MAXG_SEQ>> pl(new Plan<MAXG_SEQ>());
+    for (int c0 = 0; c0 < n; c0 += MAXG_SEQ) {
+        const int cn = (n - c0) < MAXG_SEQ ? (n - c0) : MAXG_SEQ;
+        for (int i = 0; i < cn; ++i) {
+            const qgemv_seq_item &it = items[c0 + i];
+            gs[i] = GroupSpec{it.W, 0, it.xq, 0, it.y, 0, it.N, it.K, 1};
+        }
+        s = make_plan<MAXG_SEQ>(gs.data(), cn, T, layout == QGEMV_W_GGML, false, static_cast<uint8_t *>(ws),
+                                smem_budget(dev), *pl);
+        if (s != QGEMV_OK) return s;
+        if (static_cast<long long>(ws_bytes) < pl->ws_bytes) return QGEMV_ERR_WORKSPACE;
+        pl->P.status = dev.status;
+        if (dispatch_T<MAXG_SEQ, false>(pl->P, T, grid, pl->smem, st, false) != cudaSuccess) return QGEMV_ERR_CUDA;
+    }
+    return QGEMV_OK;
+}
+
+static qgemv_status gather_specs(const qgemv_gather_matrix *mats, int n_mats, int n_ids, int T, GroupSpec *gs)
+{
+    if (!mats || n_mats < 1 || n_mats > MAXG_SMALL || n_ids < 1 || T < 1 || T > 8) return QGEMV_ERR_INVALID_ARG;
+    for (int m = 0; m < n_mats; ++m) {
+        const qgemv_gather_matrix &a = mats[m];
+        if (!shape_ok(a.N, a.K)) return QGEMV_ERR_INVALID_ARG;
+        if (n_ids > 1 && a.y_stride < static_cast<long long>(T) * a.N) return QGEMV_ERR_INVALID_ARG;
+        if (a.expert_stride < 0 || a.xq_stride < 0) return QGEMV_ERR_INVALID_ARG;
+        gs[m] = GroupSpec{a.W, a.expert_stride, a.xq, a.xq_stride, a.y, a.y_stride, a.N, a.K, n_ids};
+    }
+    return QGEMV_OK;
+}
+
+size_t qgemv_gather_workspace_bytes(const qgemv_gather_matrix *mats, int n_mats, int n_ids, int T)
+{
+    GroupSpec gs[MAXG_SMALL];
+    if (gather_specs(mats, n_mats, n_ids, T, gs) != QGEMV_OK) return 0;
+    Plan<MAXG_SMALL> a, b;
+    make_plan<MAXG_SMALL>(gs, n_mats, T, false, false, nullptr, 0, a);
+    make_plan<MAXG_SMALL>(gs, n_mats, T, true, false, nullptr, 0, b);
+    return static_cast<size_t>(a.ws_bytes > b.ws_bytes ? a.ws_bytes : b.ws_bytes);
+}
+
+qgemv_status qgemv_q4_0_gather(const qgemv_gather_matrix *mats, int n_mats, const int32_t *ids, int n_ids,
+                               int n_experts, qgemv_wlayout layout, int T, void *ws, size_t ws_bytes,
+                               qgemv_stream_t stream)
+{
+    GroupSpec gs[MAXG_SMALL];
+    qgemv_status s = gather_specs(mats, n_mats, n_ids, T, gs);
+    if (s != QGEMV_OK) return s;
+    if (layout != QGEMV_W_GGML && layout != QGEMV_W_PACKED) return QGEMV_ERR_INVALID_ARG;
+    if (!ids || n_experts < 1) return QGEMV_ERR_INVALID_ARG;
+    if (!aligned(ids, 4)) return QGEMV_ERR_MISALIGNED;
+    if (!ws) return QGEMV_ERR_WORKSPACE;
+    if (!aligned(ws, 256)) return QGEMV_ERR_MISALIGNED;
+    const Range rw = range(ws, static_cast<long long>(ws_bytes));
+    for (int m = 0; m < n_mats; ++m) {
+        const qgemv_gather_matrix &a = mats[m];
+        if (!a.W || !a.xq || !a.y) return QGEMV_ERR_INVALID_ARG;
+        const size_t wa = layout == QGEMV_W_PACKED ? 16 : 2;
+        if (!aligned(a.W, wa) || a.expert_stride % static_cast<long long>(wa) != 0 || !aligned(a.xq, 16) ||
+            a.xq_stride % 16 != 0 || !aligned(a.y, 4))
+            return QGEMV_ERR_MISALIGNED;
+        const Range ry = range(a.y, 4ll * ((n_ids - 1) * a.y_stride + static_cast<long long>(T) * a.N));
+        if (overlap(ry, rw)) return QGEMV_ERR_INVALID_ARG;
+        for (int k = 0; k < n_mats; ++k) {
+            const qgemv_gather_matrix &b = mats[k];
+            const long long wb = (n_experts - 1) * b.expert_stride + 18ll * b.N * (b.K / QK);
+            const long long xb = (n_ids - 1) * b.xq_stride + xq_bytes_host(T, b.K);
+            if (overlap(ry, range(b.W, wb)) || overlap(ry, range(b.xq, xb))) return QGEMV_ERR_INVALID_ARG;
+            if (k != m && overlap(ry, range(b.y, 4ll * ((n_ids - 1) * b.y_stride + static_cast<long long>(T) * b.N))))
+                return QGEMV_ERR_INVALID_ARG;
+        }
+    }
+    DevInfo dev;
+    s = device_info(dev);
+    if (s != QGEMV_OK) return s;
+    Plan<MAXG_SMALL> pl;
+    s = make_plan<MAXG_SMALL>(gs, n_mats, T, layout == QGEMV_W_GGML, false, static_cast<uint8_t *>(ws),
+                              smem_budget(dev), pl);
+    if (s != QGEMV_OK) return s;
+    if (static_cast<long long>(ws_bytes) < pl.ws_bytes) return QGEMV_ERR_WORKSPACE;
+    pl.P.status = dev.status;
+    pl.P.ids = ids;
+    pl.P.n_experts = n_experts;
+    const int grid = dev.sms < MAX_GRID ? dev.sms : MAX_GRID;
+    return dispatch_T<MAXG_SMALL, false>(pl.P, T, grid, pl.smem, reinterpret_cast<cudaStream_t>(stream), false) ==
+                   cudaSuccess
+               ? QGEMV_OK
+               : QGEMV_ERR_CUDA;
+}
+
+qgemv_status qgemv_debug_block_isums(const void *W, qgemv_wlayout layout, const void *xq, int32_t *isums, int64_t N,
+                                     int64_t K, int T, qgemv_stream_t stream)
+{
+    if (!shape_ok(N, K) || T < 1 || T > 8 || !W || !xq || !isums) return QGEMV_ERR_INVALID_ARG;
+    if (layout != QGEMV_W_GGML && layout != QGEMV_W_PACKED) return QGEMV_ERR_INVALID_ARG;
+    if (!aligned(W, layout == QGEMV_W_PACKED ? 16 : 2) || !aligned(xq, 16) || !aligned(isums, 4))
+        return QGEMV_ERR_MISALIGNED;
+    return launch_isums(W, layout == QGEMV_W_PACKED, xq, isums, N, K, T, reinterpret_cast<cudaStream_t>(stream)) ==
+                   cudaSuccess
+               ? QGEMV_OK
+               : QGEMV_ERR_CUDA;
+}
+
+qgemv_status qgemv_device_status(int *code_out)
+{
+    if (!code_out) return QGEMV_ERR_INVALID_ARG;
+    DevInfo dev;
+    qgemv_status s = device_info(dev);
+    if (s != QGEMV_OK) return s;
+    if (cudaDeviceSynchronize() != cudaSuccess) return QGEMV_ERR_CUDA;
+    unsigned v = 0, zero = 0;
+    if (cudaMemcpy(&v, dev.status, sizeof(v), cudaMemcpyDeviceToHost) != cudaSuccess) return QGEMV_ERR_CUDA;
+    if (cudaMemcpy(dev.status, &zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess) return QGEMV_ERR_CUDA;
+    *code_out = static_cast<int>(v);
+    return QGEMV_OK;
+}
+
+}  // extern "C"

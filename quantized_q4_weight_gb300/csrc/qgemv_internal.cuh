@@ -1,0 +1,272 @@
+// qgemv_internal.cuh -- shared definitions of libqgemv's kernels and host code.
+//
+// Arithmetic (minfer README, "The optimization journey", M9 and M15/M16):
+//   isum(t,i,b) = sum_j (n_j - 8) q_j  (exact int32), formed with dp4a on the
+//   unsigned nibbles and the folded offset -8 * sum_j q_j (M9: "folded -8
+//   offset"); y += (d_w * d_x) * isum in fp32, in the fixed order described
+//   in include/qgemv.h (it depends on K only, and is the same for every T).
+#pragma once
+
+#include <cuda_fp16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+namespace qg {
+
+constexpr int QK = 32;                // weights per Q4_0 / Q8_0 block
+constexpr int Q4_BYTES = 18;          // fp16 scale + 16 nibble bytes
+constexpr int SLAB_ROWS = 16;         // rows per packed slab
+constexpr int QUAD = 4;               // blocks per quad tile
+constexpr int SEG_BLOCKS = 16;        // blocks per summation segment (= one pipeline stage)
+constexpr int SLAB_COL_BYTES = SLAB_ROWS * Q4_BYTES;    // 288: one block column of a slab
+constexpr int QUAD_BYTES = QUAD * SLAB_COL_BYTES;       // 1152
+constexpr int SEG_BYTES = SEG_BLOCKS * SLAB_COL_BYTES;  // 4608
+constexpr int NWARPS = 8;             // consumer warps per CTA (one CTA per SM)
+constexpr int NTHREADS = NWARPS * 32;
+constexpr int MAX_RING = 6;           // pipeline stages per warp, upper bound
+constexpr int MAX_GRID = 1024;        // argmax candidate slots
+constexpr int SPLIT_SLAB_THRESHOLD = 2048;  // split K only when a launch has fewer slabs
+constexpr int MAGIC_I = 0x4B400000;   // bits of 12582912.0f = 1.5 * 2^23
+constexpr float MAGIC_F = 12582912.0f;
+
+// Status codes written by kernels into the per-device status word.
+constexpr unsigned ST_TIMEOUT = 6;
+constexpr unsigned ST_BAD_ID = 7;
+
+// One matrix family of a launch: a single GEMV (count = 1), or one matrix
+// of a routed-expert gather (count = slots).
+struct Group {
+    const uint8_t *W;       // instance 0 weights (packed or GGML)
+    long long w_stride;     // bytes between instances (experts)
+    const uint8_t *xq;      // planar Q8_0 of slot 0
+    long long xq_stride;    // bytes between slots (0: shared)
+    float *y;               // y[T][N] of slot 0
+    long long y_stride;     // floats between slots
+    int N, K, count, split;
+    int nb, nseg, nslabs, tail_rows;  // nslabs: slab items (GGML: ceil(N/16)); tail: packed N%16
+    int items_per_inst;               // nslabs * split + (tail_rows > 0)
+    int xq_bytes;                     // planar Q8_0 bytes per slot (T rows)
+    long long inst_bytes;             // 18 * N * nb
+    long long slab_bytes;             // 288 * nb
+    long long byte_begin, item_begin; // prefixes over the launch
+    unsigned *cnt;                    // split-K arrival counters [count][nslabs]
+    float *part;                      // split-K partials [count][nslabs][nseg][T][16]
+};
+
+template <int MAXG>
+struct Params {
+    int ngroups;
+    int ggml;               // weights in GGML layout (no TMA staging)
+    int ring_depth;         // stages per warp
+    int kmax, nbmax;        // largest K / blocks per row over the groups
+    int off_d, off_cd, off_bar, off_ring;  // dynamic shared-memory layout
+    const int *ids;         // gather: slot -> expert id (nullptr: slot index)
+    int n_experts;
+    long long total_bytes, total_items;
+    unsigned long long *am_cand;  // argmax: [gridDim][T] candidate keys
+    unsigned *am_cnt;             // argmax: CTA arrival counter
+    long long *am_idx;            // argmax: result [T]
+    unsigned *status;             // per-device status word
+    Group g[MAXG];
+};
+
+constexpr int MAXG_SMALL = 4;
+constexpr int MAXG_SEQ = 224;  // keeps the parameter block under the 32 KB kernel-parameter limit
+
+// ------------------------------------------------------------------ PTX helpers
+
+__device__ __forceinline__ uint32_t smem_addr(const void *p)
+{
+    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ void mbar_init(uint64_t *bar, unsigned count)
+{
+    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(smem_addr(bar)), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init()
+{
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint64_t *bar, unsigned bytes)
+{
+    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(smem_addr(bar)), "r"(bytes)
+                 : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint64_t *bar, unsigned parity)
+{
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_addr(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+// 1-D bulk asynchronous copy global -> own CTA's shared memory, completing
+// on an mbarrier (transaction bytes).  dst, src 16-byte aligned; bytes % 16 == 0.
+__device__ __forceinline__ void bulk_g2s(void *dst, const void *src, unsigned bytes, uint64_t *bar,
+                                         uint64_t policy)
+{
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint"
+        " [%0], [%1], %2, [%3], %4;" ::"r"(smem_addr(dst)),
+        "l"(src), "r"(bytes), "r"(smem_addr(bar)), "l"(policy)
+        : "memory");
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_first()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ uint64_t l2_policy_evict_last()
+{
+    uint64_t p;
+    asm volatile("createpolicy.fractional.L2::evict_last.b64 %0, 1.0;" : "=l"(p));
+    return p;
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem()
+{
+    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ uint64_t global_timer_ns()
+{
+    uint64_t t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    return t;
+}
+
+// Programmatic dependent launch: wait for the preceding grid's completion
+// and memory flush / allow the next grid to be scheduled early.
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
+
+// sum of 4 (unsigned byte of a) * (signed byte of b) + c.
+__device__ __forceinline__ int dp4a_us(unsigned a, int b, int c)
+{
+    int d;
+    asm("dp4a.u32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+// sum of 4 (signed byte of a) * (signed byte of b) + c.
+__device__ __forceinline__ int dp4a_ss(int a, int b, int c)
+{
+    int d;
+    asm("dp4a.s32.s32 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+constexpr uint64_t WAIT_LIMIT_NS = 2000000000ull;  // 2 s: far beyond any single copy
+constexpr uint64_t DRAIN_LIMIT_NS = 100000000ull;  // 0.1 s per stage when draining after an abort
+
+// Bounded wait on an mbarrier phase.  Gives up after `limit_ns`, raises the
+// CTA's abort flag and records ST_TIMEOUT; returns false then (and at once
+// when the CTA has already aborted).
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t *bar, unsigned parity, volatile int *abort_flag,
+                                                  unsigned *status, uint64_t limit_ns)
+{
+    if (mbar_try_wait(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (;;) {
+        if (*abort_flag) return false;
+        for (int i = 0; i < 32; ++i)
+            if (mbar_try_wait(bar, parity)) return true;
+        if (global_timer_ns() - t0 > limit_ns) {
+            *abort_flag = 1;
+            atomicCAS(status, 0u, ST_TIMEOUT);
+            return false;
+        }
+    }
+}
+
+// Wait used only while draining copies after an abort (ignores the flag).
+__device__ __forceinline__ void mbar_drain(uint64_t *bar, unsigned parity)
+{
+    const uint64_t t0 = global_timer_ns();
+    while (!mbar_try_wait(bar, parity))
+        if (global_timer_ns() - t0 > DRAIN_LIMIT_NS) return;
+}
+
+// ------------------------------------------------------------- block arithmetic
+
+// fp16 bits -> fp32 (exact).
+__device__ __forceinline__ float h2f(unsigned bits16)
+{
+    return __half2float(__ushort_as_half(static_cast<unsigned short>(bits16 & 0xFFFFu)));
+}
+
+// MAGIC_I + isum for one weight block and one activation block, where
+// c = MAGIC_I - 8 * sum(q) (the folded offset).  n = 4 words of nibble
+// bytes (byte k: element k low nibble, element k+16 high nibble);
+// qa = activation elements 0..15, qb = elements 16..31.
+__device__ __forceinline__ int block_dot_magic(const uint4 &n, const uint4 &qa, const uint4 &qb, int c)
+{
+    int s = c;
+    s = dp4a_us(n.x & 0x0F0F0F0Fu, (int)qa.x, s);
+    s = dp4a_us(n.y & 0x0F0F0F0Fu, (int)qa.y, s);
+    s = dp4a_us(n.z & 0x0F0F0F0Fu, (int)qa.z, s);
+    s = dp4a_us(n.w & 0x0F0F0F0Fu, (int)qa.w, s);
+    s = dp4a_us((n.x >> 4) & 0x0F0F0F0Fu, (int)qb.x, s);
+    s = dp4a_us((n.y >> 4) & 0x0F0F0F0Fu, (int)qb.y, s);
+    s = dp4a_us((n.z >> 4) & 0x0F0F0F0Fu, (int)qb.z, s);
+    s = dp4a_us((n.w >> 4) & 0x0F0F0F0Fu, (int)qb.w, s);
+    return s;
+}
+
+// The folded-offset constant of one activation block: MAGIC_I - 8 * sum(q).
+__device__ __forceinline__ int block_fold_const(const uint4 &qa, const uint4 &qb)
+{
+    const int ones = 0x01010101;
+    int s = 0;
+    s = dp4a_ss((int)qa.x, ones, s);
+    s = dp4a_ss((int)qa.y, ones, s);
+    s = dp4a_ss((int)qa.z, ones, s);
+    s = dp4a_ss((int)qa.w, ones, s);
+    s = dp4a_ss((int)qb.x, ones, s);
+    s = dp4a_ss((int)qb.y, ones, s);
+    s = dp4a_ss((int)qb.z, ones, s);
+    s = dp4a_ss((int)qb.w, ones, s);
+    return MAGIC_I - 8 * s;
+}
+
+// (MAGIC_I + isum) read as a float is 12582912 + isum exactly (|isum| < 2^22);
+// subtracting 12582912 gives (float)isum exactly.
+__device__ __forceinline__ float magic_to_float(int s) { return __fsub_rn(__int_as_float(s), MAGIC_F); }
+
+// Order-preserving 64-bit key for argmax: larger value first, then lower
+// row.  -0 is folded onto +0 so IEEE equality decides ties.
+__device__ __forceinline__ unsigned long long argmax_key(float v, unsigned row)
+{
+    if (v == 0.0f) v = 0.0f;
+    unsigned u = __float_as_uint(v);
+    unsigned k = (u & 0x80000000u) ? ~u : (u | 0x80000000u);
+    return (static_cast<unsigned long long>(k) << 32) | static_cast<unsigned long long>(0xFFFFFFFFu - row);
+}
+
+// One 18-byte Q4_0 block in GGML layout (only 2-byte aligned) from global memory.
+__device__ __forceinline__ void load_ggml_block(const uint8_t *p, uint4 &nib, unsigned &d)
+{
+    const unsigned short *h = reinterpret_cast<const unsigned short *>(p);
+    d = __ldg(h);
+    unsigned w[8];
+#pragma unroll
+    for (int k = 0; k < 8; ++k) w[k] = __ldg(h + 1 + k);
+    nib.x = w[0] | (w[1] << 16);
+    nib.y = w[2] | (w[3] << 16);
+    nib.z = w[4] | (w[5] << 16);
+    nib.w = w[6] | (w[7] << 16);
+}
+
+}  // namespace qg

@@ -1,0 +1,27 @@
+// qgemv_launch.h -- internal host-side interface between the C ABI and the
+// kernel translation units.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "qgemv_internal.cuh"
+
+namespace qg {
+
+inline long long roundup16(long long v) { return (v + 15) & ~15ll; }
+
+// Planar Q8_0 bytes for R rows of K (see include/qgemv.h).
+inline long long xq_bytes_host(long long R, long long K) { return R * K + roundup16(2 * R * (K / QK)); }
+
+cudaError_t launch_quantize(const float *x, void *xq, int R, long long K, int batch, cudaStream_t st);
+cudaError_t launch_pack(const void *src, void *dst, long long N, long long K, bool to_packed, cudaStream_t st);
+cudaError_t launch_isums(const void *W, bool packed, const void *xq, int32_t *isums, long long N, long long K, int T,
+                         cudaStream_t st);
+
+// The streaming GEMV kernel, one instantiation per (T, parameter-block size,
+// argmax).  Defined in gemv_t<T>.cu.
+template <int T, int MAXG, bool ARGMAX>
+cudaError_t launch_stream(const Params<MAXG> &P, int grid, size_t smem, cudaStream_t st, bool pdl);
+
+}  // namespace qg

@@ -1,0 +1,115 @@
+"""The C ABI without a GPU: the library loads, exports every function that
+include/qgemv.h declares, and rejects bad arguments on the host before any
+CUDA call (so these run on a machine without a GPU)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+import quantized_q4_weight_gb300 as q
+from quantized_q4_weight_gb300 import _build
+
+HEADER = os.path.join(_build.INCLUDE, "qgemv.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    _build.build()
+    return q.lib()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(qgemv_[a-z0-9_]+)\s*\(", text)))
+
+
+def test_exports_every_declared_function(L):
+    names = declared_functions()
+    assert len(names) >= 15
+    for n in names:
+        assert hasattr(L, n), n
+    # and the binding knows their signatures
+    assert set(names) == set(q._SIGS), set(names) ^ set(q._SIGS)
+
+
+def test_status_strings(L):
+    for code, name in q.STATUS.items():
+        assert L.qgemv_status_string(code).decode() == name
+    assert L.qgemv_version() >= 100
+
+
+def test_sizes(L):
+    assert L.qgemv_q4_0_bytes(1536, 1536) == 1327104
+    assert L.qgemv_q4_0_bytes(151936, 1536) == 131272704
+    assert L.qgemv_q4_0_bytes(10, 33) == 0
+    assert L.qgemv_q4_0_bytes(0, 32) == 0
+    assert L.qgemv_xq_bytes(1, 1536) == 1536 + 96
+    assert L.qgemv_xq_bytes(1, 32) == 32 + 16            # 2 scale bytes padded to 16
+    assert L.qgemv_xq_bytes(8, 11008) == 8 * 11008 + 8 * 344 * 2
+    assert L.qgemv_xq_bytes(0, 32) == 0
+
+
+def test_layer_set_bytes_match_the_pages(L):
+    # minfer README: 0.868 GB/token for Qwen2.5-1.5B (layers + q4 lm_head) and
+    # 1.736 GB for 3B; the layer sets alone are 736,985,088 and 1,560,674,304 B.
+    import synth
+    l15 = sum(L.qgemv_q4_0_bytes(N, K) for _, N, K in synth.layer_set(synth.QWEN25_1P5B_LAYER, 28))
+    l3 = sum(L.qgemv_q4_0_bytes(N, K) for _, N, K in synth.layer_set(synth.QWEN25_3B_LAYER, 36))
+    assert l15 == 736985088 and l3 == 1560674304
+    assert round((l15 + L.qgemv_q4_0_bytes(151936, 1536)) / 1e9, 3) == 0.868
+    assert round((l3 + L.qgemv_q4_0_bytes(151936, 2048)) / 1e9, 3) == 1.736
+
+
+def test_workspace_queries(L):
+    # split-K only when a launch has few slabs: a long list needs no partials
+    small = L.qgemv_workspace_bytes(1536, 8960, 1)
+    assert small > 256
+    assert L.qgemv_workspace_bytes(1536, 8960, 8) > small
+    assert L.qgemv_workspace_bytes(1536, 30, 1) == 0
+    assert L.qgemv_workspace_bytes(1536, 64, 9) == 0
+    items = (q.SeqItem * 2)(q.SeqItem(16, 4096, 8192, 40000, 1536), q.SeqItem(32, 4096, 8192, 1536, 8960))
+    assert L.qgemv_seq_workspace_bytes(items, 2, 1) == 256
+    assert L.qgemv_seq_workspace_bytes(items, 0, 1) == 0
+
+
+FAKE = 1 << 40          # a plausible device address; never dereferenced on these paths
+
+
+def test_gemv_rejects_bad_arguments(L):
+    s = None
+    ws = FAKE + (1 << 30)
+    ok = dict(W=FAKE, layout=1, xq=FAKE + (1 << 28), y=FAKE + (1 << 29), N=64, K=128, T=1, ws=ws, nbytes=1 << 20)
+
+    def call(**kw):
+        a = dict(ok, **kw)
+        return L.qgemv_q4_0(a["W"], a["layout"], a["xq"], a["y"], a["N"], a["K"], a["T"], a["ws"], a["nbytes"], s)
+
+    assert call(T=0) == 1 and call(T=9) == 1
+    assert call(K=100) == 1 and call(K=0) == 1 and call(N=0) == 1
+    assert call(W=None) == 1 and call(xq=None) == 1 and call(y=None) == 1
+    assert call(layout=7) == 1
+    assert call(W=FAKE + 8) == 2                       # packed weights need 16-byte alignment
+    assert call(xq=FAKE + (1 << 28) + 4) == 2
+    assert call(y=FAKE + (1 << 29) + 2) == 2
+    assert call(ws=None) == 4
+    assert call(y=FAKE + 64) == 1                      # y overlaps W
+    assert call(y=ws + 256) == 1                       # y overlaps the workspace
+
+
+def test_other_calls_reject_bad_arguments(L):
+    s = None
+    assert L.qgemv_pack_q4_0(FAKE, FAKE + 96, 16, 64, s) == 1           # overlap
+    assert L.qgemv_pack_q4_0(FAKE, FAKE + (1 << 30) + 8, 16, 64, s) == 2
+    assert L.qgemv_quantize_q8_0(FAKE, FAKE + (1 << 30), 0, 64, 1, s) == 1
+    assert L.qgemv_quantize_q8_0(FAKE, FAKE + (1 << 30) + 4, 1, 64, 1, s) == 2
+    assert L.qgemv_q4_0_argmax(FAKE, 1, FAKE + (1 << 28), None, None, 64, 64, 1, FAKE + (1 << 30), 4096, s) == 1
+    items = (q.SeqItem * 2)(q.SeqItem(FAKE, FAKE + (1 << 28), FAKE + (1 << 29), 64, 64),
+                            q.SeqItem(FAKE + (1 << 27), FAKE + (1 << 28), FAKE + (1 << 29) + 64, 64, 64))
+    assert L.qgemv_q4_0_seq(items, 2, 1, 1, FAKE + (1 << 30), 4096, s) == 1     # two outputs overlap
+    assert L.qgemv_q4_0_seq(items, 0, 1, 1, FAKE + (1 << 30), 4096, s) == 1
+    mats = (q.GatherMatrix * 1)(q.GatherMatrix(FAKE, 4608, FAKE + (1 << 28), 0, FAKE + (1 << 29), 10, 64, 128))
+    assert L.qgemv_q4_0_gather(mats, 1, FAKE + (1 << 31), 2, 4, 1, 1, FAKE + (1 << 30), 4096, s) == 1  # y_stride < T*N
+    assert L.qgemv_q4_0_gather(mats, 1, None, 1, 4, 1, 1, FAKE + (1 << 30), 4096, s) == 1
+    assert L.qgemv_debug_block_isums(FAKE, 1, FAKE, None, 16, 64, 1, s) == 1
