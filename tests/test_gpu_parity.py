@@ -1,0 +1,332 @@
+"""CUDA path against the CPU oracle, through the C ABI, on small and ragged
+shapes that span several slabs, segments and quads.
+
+Bit-exact: Q8_0 activation bytes, per-block int32 sums, pack/unpack bytes,
+argmax indices (against the argmax of the GPU's own y), and y across T,
+layouts, split-K and entry points (the library's order depends on K only).
+Within |y - y64| <= 1e-5 * S + 1e-6: every fp32 output against the fp64
+reference.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import quantized_q4_weight_gb300 as q
+import synth
+from tests import oracle_pins as P
+from tests.gpu_util import blocks_to_planar, check_close, planar_to_blocks, to_dev
+
+pytestmark = pytest.mark.gpu
+
+DEV = "cuda"
+
+
+@pytest.fixture(scope="module")
+def orc():
+    from quantized_q4_weight_gb300 import _build
+    _build.build()
+    oracle.build()
+    q.lib()
+    torch.cuda.init()
+    return oracle.load()
+
+
+def weights(seed, N, K, layout):
+    Wg = synth.q4_0_weights(seed, N, K)
+    Wd = to_dev(Wg)
+    return Wg, (q.pack_q4_0(Wd, N, K) if layout == q.W_PACKED else Wd)
+
+
+def quantized(seed, T, K):
+    x = synth.activations(seed, T, K)
+    xd = torch.from_numpy(x).to(DEV)
+    return x, xd, q.quantize_q8_0(xd, T, K)
+
+
+def ws_for(N, K, T):
+    return q.new_workspace(q.workspace_bytes(N, K, T))
+
+
+# ----------------------------------------------------------------- quantiser
+
+@pytest.mark.parametrize("R,K,batch", [(1, 32, 1), (1, 1536, 1), (3, 96, 2), (8, 11008, 1), (9, 512, 3),
+                                       (5, 8960, 1), (2, 64, 7)])
+def test_quantize_bit_exact(orc, R, K, batch):
+    x = synth.activations(100 + R + K + batch, batch * R, K)
+    xq = q.quantize_q8_0(torch.from_numpy(x).to(DEV), R, K, batch).cpu().numpy()
+    n = q.xq_bytes(R, K)
+    assert xq.size == n * batch
+    for b in range(batch):
+        ref = orc.quantize(x[b * R:(b + 1) * R])
+        assert np.array_equal(xq[b * n:(b + 1) * n], blocks_to_planar(ref, n))
+
+
+def test_quantize_hand_blocks_and_edges(orc):
+    xs = [P._x_block(e) for e in P.golden()["q8_0"]]
+    rng = np.random.default_rng(3)
+    xs += [np.full(32, -3.0, np.float32), np.full(32, 1e-30, np.float32),            # tiny amax
+           (rng.standard_normal(32) * 1e4).astype(np.float32),
+           np.where(np.arange(32) % 2 == 0, 0.5, -0.5).astype(np.float32) * 127 / 63.5]
+    x = np.stack(xs).reshape(1, -1).astype(np.float32)
+    K = x.shape[1]
+    xq = q.quantize_q8_0(torch.from_numpy(x).to(DEV), 1, K).cpu().numpy()
+    assert np.array_equal(xq, blocks_to_planar(orc.quantize(x), q.xq_bytes(1, K)))
+    for i, e in enumerate(P.golden()["q8_0"]):
+        blk = planar_to_blocks(xq, 1, K)[0, i]
+        assert int(blk[0]) | (int(blk[1]) << 8) == int(e["d_bits"], 16)
+        assert np.array_equal(blk[2:].view(np.int8), P._q_block(e))
+
+
+# ----------------------------------------------------------------- pack
+
+@pytest.mark.parametrize("N,K", [(1, 32), (15, 64), (16, 128), (17, 96), (33, 160), (100, 544), (48, 2080)])
+def test_pack_roundtrip_and_layout(orc, N, K):
+    Wg = synth.q4_0_weights(N * K, N, K)
+    Wd = to_dev(Wg)
+    Wp = q.pack_q4_0(Wd, N, K)
+    assert torch.equal(q.unpack_q4_0(Wp, N, K), Wd)
+    # the layout as include/qgemv.h states it
+    got = Wp.cpu().numpy()
+    nb = K // 32
+    blk = Wg.reshape(N, nb, 18)
+    nfull = N // 16
+    for s in range(nfull):
+        base = s * 288 * nb
+        for qd in range((nb + 3) // 4):
+            nbq = min(4, nb - 4 * qd)
+            qb = base + 1152 * qd
+            for r in range(16):
+                for jq in range(nbq):
+                    b = 4 * qd + jq
+                    o = qb + (r * nbq + jq) * 16
+                    assert np.array_equal(got[o:o + 16], blk[16 * s + r, b, 2:])
+                    so = qb + 256 * nbq + ((r % 8) * nbq + jq) * 4 + (r // 8) * 2
+                    assert np.array_equal(got[so:so + 2], blk[16 * s + r, b, :2])
+    tail = nfull * 16 * nb * 18
+    assert np.array_equal(got[tail:], Wg.reshape(-1)[tail:])
+
+
+# ----------------------------------------------------------------- block sums
+
+@pytest.mark.parametrize("layout", [q.W_PACKED, q.W_GGML])
+@pytest.mark.parametrize("N,K,T", [(16, 32, 1), (17, 544, 3), (40, 1536, 8), (5, 96, 2)])
+def test_block_isums_bit_exact(orc, layout, N, K, T):
+    Wg, W = weights(11 * N + K, N, K, layout)
+    x, xd, xq = quantized(13 * N + T, T, K)
+    got = q.block_isums(W, layout, xq, N, K, T).cpu().numpy()
+    ref = orc.block_isums(Wg, N, K, orc.quantize(x), T)
+    assert np.array_equal(got, ref)
+
+
+def test_block_isums_range_extremes(orc):
+    K, N = 64, 16
+    W = synth.with_scales(synth.with_nibbles(synth.q4_0_weights(1, N, K), K, 0), K, 0x3C00)
+    x = np.full((1, K), -127.0, np.float32)
+    xq = q.quantize_q8_0(torch.from_numpy(x).to(DEV), 1, K)
+    got = q.block_isums(q.pack_q4_0(to_dev(W), N, K), q.W_PACKED, xq, N, K, 1).cpu().numpy()
+    assert np.all(got == 32512)
+
+
+# ----------------------------------------------------------------- GEMV vs oracle
+
+SHAPES = [(1, 32), (15, 64), (16, 512), (17, 544), (64, 1536), (100, 2080), (48, 8960), (300, 1024), (33, 11008)]
+
+
+@pytest.mark.parametrize("layout", [q.W_PACKED, q.W_GGML])
+@pytest.mark.parametrize("N,K", SHAPES)
+@pytest.mark.parametrize("T", [1, 2, 5, 8])
+def test_gemv_matches_oracle(orc, layout, N, K, T):
+    Wg, W = weights(7 * N + K, N, K, layout)
+    x, xd, xq = quantized(3 * N + K + T, T, K)
+    y = q.gemv(W, layout, xq, N, K, T, ws_for(N, K, T))
+    torch.cuda.synchronize()
+    assert q.device_status() == 0
+    y64, S = orc.gemv(Wg, N, K, orc.quantize(x), T)
+    check_close(y.cpu().numpy(), y64, S, f"N={N} K={K} T={T}")
+
+
+def test_closed_forms_on_gpu(orc):
+    for e in P.golden()["closed_forms"]:
+        K, N = e["K"], 20
+        Wg = synth.with_scales(synth.with_nibbles(synth.q4_0_weights(1, N, K), K, e["nibble"]), K,
+                               int(e["w_d_bits"], 16))
+        x = np.full((1, K), e["x_value"], np.float32)
+        xq = q.quantize_q8_0(torch.from_numpy(x).to(DEV), 1, K)
+        for layout in (q.W_PACKED, q.W_GGML):
+            W = q.pack_q4_0(to_dev(Wg), N, K) if layout == q.W_PACKED else to_dev(Wg)
+            y = q.gemv(W, layout, xq, N, K, 1, ws_for(N, K, 1)).cpu().numpy()
+            assert np.all(y == e["y"]), (e["name"], y)
+
+
+def test_hand_block_on_gpu(orc):
+    for e in P.golden()["q4_0"]:
+        w = P._wq_bytes(int(e["w_d_bits"], 16), e["w_qs"])
+        xe = [g for g in P.golden()["q8_0"] if g["name"] == e["x_block"]][0]
+        x = P._x_block(xe).reshape(1, 32)
+        W = to_dev(np.tile(w, 16))                        # 16 identical rows = one slab
+        xq = q.quantize_q8_0(torch.from_numpy(x).to(DEV), 1, 32)
+        for layout, Wl in ((q.W_GGML, W), (q.W_PACKED, q.pack_q4_0(W, 16, 32))):
+            assert np.all(q.block_isums(Wl, layout, xq, 16, 32, 1).cpu().numpy() == e["isum"])
+            assert np.all(q.gemv(Wl, layout, xq, 16, 32, 1, ws_for(16, 32, 1)).cpu().numpy() == e["y"])
+
+
+# ----------------------------------------------------------------- bit identity
+
+@pytest.mark.parametrize("N,K", [(50, 8960), (40, 1536), (7, 544), (300, 2048)])
+def test_bit_identical_across_T_layouts_and_paths(orc, N, K):
+    Wg, Wp = weights(5 * N + K, N, K, q.W_PACKED)
+    Wd = to_dev(Wg)
+    x, xd, xq8 = quantized(9 * N, 8, K)
+    y8 = q.gemv(Wp, q.W_PACKED, xq8, N, K, 8, ws_for(N, K, 8)).cpu()
+    y8g = q.gemv(Wd, q.W_GGML, xq8, N, K, 8, ws_for(N, K, 8)).cpu()
+    assert torch.equal(y8.view(torch.int32), y8g.view(torch.int32))
+    for t in range(8):
+        xq1 = q.quantize_q8_0(xd[t:t + 1].contiguous(), 1, K)
+        y1 = q.gemv(Wp, q.W_PACKED, xq1, N, K, 1, ws_for(N, K, 1)).cpu()
+        assert torch.equal(y1[0].view(torch.int32), y8[t].view(torch.int32)), t
+    # fp32-input entry point == quantise + GEMV
+    yf = q.gemv_f32(Wp, q.W_PACKED, xd, N, K, 8, ws_for(N, K, 8)).cpu()
+    assert torch.equal(yf.view(torch.int32), y8.view(torch.int32))
+    # a long sequence launch (no split-K) gives the same bits as the single call (split-K when K > 512)
+    reps = 160
+    ys = [torch.empty((8, N), dtype=torch.float32, device=DEV) for _ in range(reps)]
+    items = q.seq_items([(Wp, xq8, ys[i], N, K) for i in range(reps)])
+    ws = q.new_workspace(q.seq_workspace_bytes(items, 8))
+    q.gemv_seq(items, q.W_PACKED, 8, ws)
+    for i in (0, reps // 2, reps - 1):
+        assert torch.equal(ys[i].cpu().view(torch.int32), y8.view(torch.int32))
+
+
+# ----------------------------------------------------------------- argmax
+
+@pytest.mark.parametrize("layout", [q.W_PACKED, q.W_GGML])
+@pytest.mark.parametrize("N,K,T", [(1, 32, 1), (4099, 1536, 1), (1000, 544, 3), (20000, 256, 8), (48, 8960, 2)])
+def test_argmax(orc, layout, N, K, T):
+    Wg, W = weights(17 * N + K, N, K, layout)
+    x, xd, xq = quantized(19 * N + T, T, K)
+    ws = ws_for(N, K, T)
+    y = torch.empty((T, N), dtype=torch.float32, device=DEV)
+    idx = q.gemv_argmax(W, layout, xq, N, K, T, ws, y=y).cpu().numpy()
+    idx2 = q.gemv_argmax(W, layout, xq, N, K, T, ws).cpu().numpy()        # y not written
+    yref = q.gemv(W, layout, xq, N, K, T, ws).cpu().numpy()
+    assert np.array_equal(y.cpu().numpy().view(np.int32), yref.view(np.int32))
+    y64, S = orc.gemv(Wg, N, K, orc.quantize(x), T)
+    for t in range(T):
+        assert idx[t] == idx2[t] == orc.argmax_f32(yref[t])
+        i64 = orc.argmax_f64(y64[t])
+        if idx[t] != i64:   # only a near-tie of the fp64 reference may differ
+            assert abs(y64[t, idx[t]] - y64[t, i64]) <= oracle.tolerance(S[t, idx[t]]) + oracle.tolerance(S[t, i64])
+
+
+def test_argmax_ties_and_zero_rows(orc):
+    N, K, T = 5000, 256, 2
+    Wg = synth.q4_0_weights(23, N, K)
+    Wg[4000] = Wg[1234]          # identical rows
+    Wg[4999] = Wg[1234]
+    x, xd, xq = quantized(24, T, K)
+    Wp = q.pack_q4_0(to_dev(Wg), N, K)
+    y = q.gemv(Wp, q.W_PACKED, xq, N, K, T, ws_for(N, K, T)).cpu().numpy()
+    # make row 1234 the maximum for token 0 by construction: scale it up
+    blk = Wg.reshape(N, K // 32, 18).copy()
+    for r in (1234, 4000, 4999):
+        blk[r, :, 0:2] = np.array([0x00, 0x7A], np.uint8)     # d = 49152 on every block
+    Wg2 = blk.reshape(Wg.shape)
+    Wp2 = q.pack_q4_0(to_dev(Wg2), N, K)
+    y2 = q.gemv(Wp2, q.W_PACKED, xq, N, K, T, ws_for(N, K, T)).cpu().numpy()
+    idx = q.gemv_argmax(Wp2, q.W_PACKED, xq, N, K, T, ws_for(N, K, T)).cpu().numpy()
+    for t in range(T):
+        assert idx[t] == orc.argmax_f32(y2[t])
+        if y2[t, 1234] == y2[t].max():
+            assert idx[t] == 1234
+    # all-zero scales: every output is +-0 and the answer is row 0
+    Wz = q.pack_q4_0(to_dev(synth.with_scales(Wg, K, 0x0000)), N, K)
+    assert np.all(q.gemv_argmax(Wz, q.W_PACKED, xq, N, K, T, ws_for(N, K, T)).cpu().numpy() == 0)
+    # negative-zero scales give -0 outputs that tie with +0
+    Wn = q.pack_q4_0(to_dev(synth.with_scales(Wg, K, 0x8000)), N, K)
+    assert np.all(q.gemv_argmax(Wn, q.W_PACKED, xq, N, K, T, ws_for(N, K, T)).cpu().numpy() == 0)
+    del y
+
+
+# ----------------------------------------------------------------- sequence and gather
+
+def test_seq_matches_single_calls(orc):
+    shapes = [(2048, 1536), (1536, 1536), (96, 8960), (17, 544), (64, 32), (300, 2048)]
+    T = 3
+    entries, refs = [], []
+    for i, (N, K) in enumerate(shapes):
+        Wg, Wp = weights(40 + i, N, K, q.W_PACKED)
+        x, xd, xq = quantized(60 + i, T, K)
+        y = torch.full((T, N), float("nan"), dtype=torch.float32, device=DEV)
+        entries.append((Wp, xq, y, N, K))
+        refs.append((Wg, x, q.gemv(Wp, q.W_PACKED, xq, N, K, T, ws_for(N, K, T)).cpu()))
+    items = q.seq_items(entries)
+    ws = q.new_workspace(q.seq_workspace_bytes(items, T))
+    q.gemv_seq(items, q.W_PACKED, T, ws)
+    torch.cuda.synchronize()
+    for (Wp, xq, y, N, K), (Wg, x, yref) in zip(entries, refs):
+        assert torch.equal(y.cpu().view(torch.int32), yref.view(torch.int32)), (N, K)
+        y64, S = orc.gemv(Wg, N, K, orc.quantize(x), T)
+        check_close(y.cpu().numpy(), y64, S, f"seq N={N} K={K}")
+
+
+@pytest.mark.parametrize("layout", [q.W_PACKED, q.W_GGML])
+def test_gather_matches_single_calls(orc, layout):
+    n_experts, d_model, d_ff, T = 12, 512, 160, 1
+    shapes = [("gate", d_ff, d_model), ("up", d_ff, d_model), ("down", d_model, d_ff)]
+    ids_np = np.array([3, 7, 3, 11, 0], np.int32)          # repeats allowed
+    n_ids = ids_np.size
+    mats, checks = [], []
+    for m, (name, N, K) in enumerate(shapes):
+        per = q.q4_0_bytes(N, K)
+        Wg_all = [synth.q4_0_weights(500 + 10 * m + e, N, K) for e in range(n_experts)]
+        Wd = torch.cat([to_dev(w) for w in Wg_all])
+        W = torch.cat([q.pack_q4_0(to_dev(w), N, K) for w in Wg_all]) if layout == q.W_PACKED else Wd
+        shared = name != "down"
+        xs = synth.activations(700 + m, 1 if shared else n_ids, K)
+        xqb = q.xq_bytes(T, K)
+        xq = q.quantize_q8_0(torch.from_numpy(xs).to(DEV), T, K, batch=xs.shape[0])
+        y = torch.full((n_ids, T, N), float("nan"), dtype=torch.float32, device=DEV)
+        mats.append((W, per, xq, 0 if shared else xqb, y, T * N, N, K))
+        checks.append((Wg_all, W, per, xs, xq, xqb, y, N, K, shared))
+    gm = q.gather_mats(mats)
+    ws = q.new_workspace(q.gather_workspace_bytes(gm, n_ids, T))
+    ids = torch.from_numpy(ids_np).to(DEV)
+    q.gemv_gather(gm, ids, n_experts, layout, T, ws)
+    torch.cuda.synchronize()
+    assert q.device_status() == 0
+    for Wg_all, W, per, xs, xq, xqb, y, N, K, shared in checks:
+        for s in range(n_ids):
+            e = int(ids_np[s])
+            xqs = xq[(0 if shared else s) * xqb:((0 if shared else s) + 1) * xqb]
+            Ws = W[e * per:(e + 1) * per]
+            yref = q.gemv(Ws, layout, xqs, N, K, T, ws_for(N, K, T)).cpu()
+            assert torch.equal(y[s].cpu().view(torch.int32), yref.view(torch.int32))
+            y64, S = orc.gemv(Wg_all[e], N, K, orc.quantize(xs[0 if shared else s][None]), T)
+            check_close(y[s].cpu().numpy(), y64, S, "gather")
+    # an expert id out of range: nothing read for that slot, status recorded
+    bad = torch.tensor([1, 99], dtype=torch.int32, device=DEV)
+    for W, _, xq, _, y, _, N, K in mats:
+        y.fill_(-1.0)
+    q.gemv_gather(gm, bad, n_experts, layout, T, ws)
+    torch.cuda.synchronize()
+    assert q.device_status() == 7                         # QGEMV_ERR_BAD_ID
+    for W, _, xq, _, y, _, N, K in mats:
+        assert torch.all(y[1] == -1.0) and not torch.all(y[0] == -1.0)
+    assert q.device_status() == 0
+
+
+# ----------------------------------------------------------------- workspace contract
+
+def test_workspace_left_zeroed_and_reusable(orc):
+    N, K, T = 96, 8960, 4            # few slabs: split-K with counters
+    Wg, Wp = weights(77, N, K, q.W_PACKED)
+    x, xd, xq = quantized(78, T, K)
+    ws = ws_for(N, K, T)
+    y1 = q.gemv(Wp, q.W_PACKED, xq, N, K, T, ws).cpu()
+    idx = q.gemv_argmax(Wp, q.W_PACKED, xq, N, K, T, ws).cpu()
+    y2 = q.gemv(Wp, q.W_PACKED, xq, N, K, T, ws).cpu()
+    assert torch.equal(y1.view(torch.int32), y2.view(torch.int32))
+    torch.cuda.synchronize()
+    assert int(ws[:4].view(torch.int32)[0]) == 0           # argmax arrival counter
+    assert idx.shape == (T,)

@@ -1,0 +1,96 @@
+"""The benchmark's workloads at full size, in the launch configuration that
+bench.py times, checked against the CPU oracle: every output where the
+oracle finishes in seconds, sampled rows of every GEMV otherwise."""
+import numpy as np
+import pytest
+import torch
+
+import bench
+import oracle
+import quantized_q4_weight_gb300 as q
+from tests.gpu_util import check_close
+
+pytestmark = pytest.mark.gpu
+DEV = torch.device("cuda", 0)
+
+
+@pytest.fixture(scope="module")
+def orc():
+    from quantized_q4_weight_gb300 import _build
+    _build.build()
+    oracle.build()
+    return oracle.load()
+
+
+def host(t: torch.Tensor) -> np.ndarray:
+    return t.detach().cpu().numpy()
+
+
+@pytest.mark.parametrize("name,T", [("qwen2.5-1.5b_layerset", 1), ("qwen2.5-3b_verify", 8),
+                                    ("qwen2.5-3b_verify", 1)])
+def test_layer_sets_sampled(orc, name, T):
+    wl = bench.build_workload(name, DEV, T=T, keep_host=True)
+    wl.quantize()
+    wl.gemv()
+    torch.cuda.synchronize()
+    assert q.device_status() == 0
+    rng = np.random.default_rng(5)
+    xs = {K: host(wl.x[K]) for K in wl.kidx}
+    for i, (nm, N, K) in enumerate(wl.mats):
+        slot = wl.kidx[K].index(i)
+        xq = orc.quantize(xs[K][slot])
+        if i < 5:   # activation bytes of the first layer, bit-exact
+            xqb = q.xq_bytes(T, K)
+            got = host(wl.xq[K][slot * xqb:(slot + 1) * xqb])
+            assert np.array_equal(got[:T * K].reshape(T, K // 32, 32), xq[:, :, 2:])
+        rows = np.unique(np.concatenate([[0, N - 1], rng.integers(0, N, 6)]))
+        y64, S = orc.gemv_rows(wl.host[i], N, K, xq, T, rows)
+        check_close(host(wl.y[i])[:, rows], y64, S, f"{name} {nm}")
+
+
+def test_lm_head_argmax_full(orc):
+    wl = bench.build_workload("lm_head_argmax", DEV, keep_host=True)
+    y = torch.empty((wl.T, wl.N), dtype=torch.float32, device=DEV)
+    for c in range(len(wl.W)):
+        wl.quantize()
+        wl.copy = c
+        wl.gemv()
+        idx = host(wl.idx).copy()
+        q.gemv(wl.W[c], q.W_PACKED, wl.xqb, wl.N, wl.K, wl.T, wl.ws, y=y)
+        yh = host(y)
+        xq = orc.quantize(host(wl.x))
+        y64, S = orc.gemv(wl.host[c], wl.N, wl.K, xq, wl.T)
+        check_close(yh, y64, S, "lm_head")
+        for t in range(wl.T):
+            assert idx[t] == orc.argmax_f32(yh[t])
+            i64 = orc.argmax_f64(y64[t])
+            if idx[t] != i64:
+                assert abs(y64[t, idx[t]] - y64[t, i64]) <= oracle.tolerance(S[t, idx[t]]) + oracle.tolerance(S[t, i64])
+
+
+def test_single_full(orc):
+    wl = bench.build_workload("single_1536", DEV, keep_host=True)
+    wl.gemv()
+    torch.cuda.synchronize()
+    xq = orc.quantize(host(wl.x))
+    y64, S = orc.gemv(wl.host[0], wl.N, wl.K, xq, wl.T)
+    check_close(host(wl.y), y64, S, "single")
+
+
+def test_moe_full(orc):
+    wl = bench.build_workload("moe_top8_shared", DEV, keep_host=True)
+    wl.quantize()
+    wl.tok = 0
+    wl.gemv()            # token 0, expert set 0
+    torch.cuda.synchronize()
+    assert q.device_status() == 0
+    ids = host(wl.ids[0])
+    xin = orc.quantize(host(wl.x_in))
+    xdn = host(wl.x_dn)
+    outs = [host(wl.yg), host(wl.yu), host(wl.yd)]
+    shapes = [(512, 2048), (512, 2048), (2048, 512)]
+    for m, (N, K) in enumerate(shapes):
+        for s, e in enumerate(ids):
+            xq = xin if m < 2 else orc.quantize(xdn[s:s + 1])
+            y64, S = orc.gemv(wl.host[(m, int(e))], N, K, xq, 1)
+            check_close(outs[m][s], y64, S, f"moe m={m} slot={s}")
