@@ -373,6 +373,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qgemv_stream_kernel(const __grid_
                 continue;
             }
             const bool direct = P.ggml || inf.kind != 0;
+            const bool split = g.split > 1 && inf.kind == 0;  // a packed tail is never split
             const uint8_t *rows_base =
                 inf.kind != 0 ? inf.Wi + static_cast<long long>(g.nslabs) * g.slab_bytes
                               : inf.Wi + static_cast<long long>(inf.slab) * SLAB_ROWS * nb * Q4_BYTES;
@@ -412,7 +413,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qgemv_stream_kernel(const __grid_
                 }
                 combine_phases<T>(acc);
 
-                if (g.split > 1) {
+                if (split) {
                     // split-K: publish this segment's partial sums
                     float *pb = g.part + ((static_cast<long long>(inf.e) * g.nslabs + inf.slab) * g.nseg + s) * T * 16;
                     if (j == 0) {
@@ -432,7 +433,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qgemv_stream_kernel(const __grid_
 
             float *ye = g.y + static_cast<long long>(inf.e) * g.y_stride;
             const int row0 = inf.slab * SLAB_ROWS;
-            if (g.split > 1) {
+            if (split) {
                 __threadfence();
                 __syncwarp();
                 unsigned old = 0;
