@@ -55,10 +55,11 @@
  * Workspace.  Calls that take (ws, ws_bytes) use it for split-K partial
  * sums, completion counters, argmax candidates and (for fp32-input calls)
  * the quantised activations.  The matching *_workspace_bytes query gives the
- * size (device-independent).  The workspace must be zero-filled once before
- * its first use (e.g. cudaMemsetAsync); every call that completes without a
- * device-status error leaves its counters at zero again, so it can be reused
- * directly.
+ * size (device-independent, at least 16 KB).  Its first 16 KB hold
+ * completion counters and must be zero-filled once before the first use
+ * (e.g. cudaMemsetAsync); every call that completes without a device-status
+ * error leaves them at zero again, so a workspace can be reused directly,
+ * by calls of any kind and shape, as long as it is large enough.
  *
  * Alignment: W, xq and ws 16 bytes; x and y 4 bytes; strides accordingly.
  * Limits: K % 32 == 0; 1 <= T <= 8 for the GEMV calls; 1 <= N < 2^31.

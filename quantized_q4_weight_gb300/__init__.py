@@ -119,7 +119,7 @@ def workspace_bytes(N: int, K: int, T: int) -> int:
 
 def new_workspace(nbytes: int, device=None) -> torch.Tensor:
     """A zero-filled workspace (the library keeps its counters at zero)."""
-    return torch.zeros(max(int(nbytes), 256), dtype=torch.uint8, device=device or "cuda")
+    return torch.zeros(max(int(nbytes), 16384), dtype=torch.uint8, device=device or "cuda")
 
 
 # ----------------------------------------------------------------- calls

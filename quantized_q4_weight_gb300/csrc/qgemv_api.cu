@@ -86,8 +86,14 @@ struct Plan {
     size_t smem = 0;
 };
 
-// Workspace layout: [arrival counter, 256 B][argmax candidates][split-K
-// counters and partials per split group].
+// Workspace layout, the same for every entry point: a counter area of
+// CNT_AREA bytes (index 0: argmax arrival counter; then the split-K
+// counters of each split group), then the data (argmax candidates, split-K
+// partials).  Counters are only ever used as counters and every completed
+// call leaves them at zero, so calls of any kind may share a workspace.
+constexpr long long CNT_AREA = 16384;
+static_assert(CNT_AREA / 4 > SPLIT_SLAB_THRESHOLD, "split-K counters must fit the counter area");
+
 template <int MAXG>
 qgemv_status make_plan(const GroupSpec *gs, int n, int T, bool ggml, bool argmax, uint8_t *ws, int smem_limit,
                        Plan<MAXG> &pl)
@@ -104,7 +110,8 @@ qgemv_status make_plan(const GroupSpec *gs, int n, int T, bool ggml, bool argmax
         total_slabs += nslabs * gs[i].count;
         (void)nb;
     }
-    long long off = 256;  // argmax arrival counter lives at offset 0
+    long long off = CNT_AREA;  // data
+    long long cnt_off = 4;     // counters (argmax arrival counter at 0)
     if (argmax) {
         P.am_cnt = ws ? reinterpret_cast<unsigned *>(ws) : nullptr;
         P.am_cand = ws ? reinterpret_cast<unsigned long long *>(ws + off) : nullptr;
@@ -144,8 +151,9 @@ qgemv_status make_plan(const GroupSpec *gs, int n, int T, bool ggml, bool argmax
         items += static_cast<long long>(g.items_per_inst) * g.count;
         if (g.split > 1) {
             const long long nc = static_cast<long long>(g.count) * g.nslabs;
-            g.cnt = ws ? reinterpret_cast<unsigned *>(ws + off) : nullptr;
-            off = align_up(off + nc * 4, 256);
+            g.cnt = ws ? reinterpret_cast<unsigned *>(ws + cnt_off) : nullptr;
+            cnt_off += nc * 4;
+            if (cnt_off > CNT_AREA) return QGEMV_ERR_INTERNAL;
             g.part = ws ? reinterpret_cast<float *>(ws + off) : nullptr;
             off = align_up(off + nc * g.nseg * T * 16 * 4, 256);
         }

@@ -65,12 +65,12 @@ def test_layer_set_bytes_match_the_pages(L):
 def test_workspace_queries(L):
     # split-K only when a launch has few slabs: a long list needs no partials
     small = L.qgemv_workspace_bytes(1536, 8960, 1)
-    assert small > 256
+    assert small > 16384
     assert L.qgemv_workspace_bytes(1536, 8960, 8) > small
     assert L.qgemv_workspace_bytes(1536, 30, 1) == 0
     assert L.qgemv_workspace_bytes(1536, 64, 9) == 0
     items = (q.SeqItem * 2)(q.SeqItem(16, 4096, 8192, 40000, 1536), q.SeqItem(32, 4096, 8192, 1536, 8960))
-    assert L.qgemv_seq_workspace_bytes(items, 2, 1) == 256
+    assert L.qgemv_seq_workspace_bytes(items, 2, 1) == 16384
     assert L.qgemv_seq_workspace_bytes(items, 0, 1) == 0
 
 
