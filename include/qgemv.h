@@ -155,6 +155,27 @@ qgemv_status qgemv_q4_0_argmax(const void *W, qgemv_wlayout layout, const void *
                                float *y_or_null, int64_t *idx, int64_t N, int64_t K, int T,
                                void *ws, size_t ws_bytes, qgemv_stream_t stream);
 
+/* Allocation-free variant of qgemv_q4_0_argmax (the paper has no
+ * counterpart; this is a convenience of this library).  For callers that
+ * cannot allocate device memory where they run the lm_head -- a plugin that
+ * only receives its input and output tensors, a runtime with a fixed memory
+ * budget, or code inside a region where allocation is not allowed -- it
+ * takes no workspace: its scratch is one 4 MiB array in the library's own
+ * device memory, held by every GPU that loads the library until the process
+ * exits.  Arguments and results are those of qgemv_q4_0_argmax.
+ *   - Shapes whose scratch would exceed 4 MiB (see qgemv_workspace_bytes
+ *     minus the activation area) return QGEMV_ERR_UNSUPPORTED.
+ *   - The first call on a device looks up the array's device address (once
+ *     per device, with that device current); make that first call before
+ *     any stream capture.
+ *   - Every call shares the array and clears its counters at the start (an
+ *     asynchronous memset on `stream`); calls that overlap on the GPU, from
+ *     any stream or thread, race and give undefined results.
+ *   - It allocates and frees nothing. */
+qgemv_status qgemv_q4_0_argmax_noalloc(const void *W, qgemv_wlayout layout, const void *xq,
+                                       float *y_or_null, int64_t *idx, int64_t N, int64_t K, int T,
+                                       qgemv_stream_t stream);
+
 /* One GEMV of a sequence (layer set): weights, planar Q8_0 activations of
  * T rows, and output y[T][N]. */
 typedef struct {

@@ -547,3 +547,51 @@ qgemv_status qgemv_device_status(int *code_out)
 }
 
 }  // extern "C"
+
+// =====================================================================
+// Allocation-free lm_head argmax.
+//
+// Some callers cannot allocate device memory at the point where they run
+// the lm_head: a plugin that a host framework hands only its input and
+// output tensors, a runtime whose device memory is fixed up front, or code
+// already inside a region where allocation is forbidden.  For them this
+// entry point takes its scratch (completion counters, per-CTA argmax
+// candidates, split-K partial sums) from one fixed array that lives in the
+// library's own device memory, so the caller passes inputs and outputs only.
+
+namespace {
+constexpr long long kNoAllocScratchBytes = 4ll << 20;  // 4 MiB per device
+std::mutex g_noalloc_mu;
+void *g_noalloc_ptr[kMaxDevices] = {};
+}  // namespace
+
+// Held by every GPU that loads the library until the process exits.
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+extern "C" qgemv_status qgemv_q4_0_argmax_noalloc(const void *W, qgemv_wlayout layout, const void *xq,
+                                                  float *y_or_null, int64_t *idx, int64_t N, int64_t K, int T,
+                                                  qgemv_stream_t stream)
+{
+    if (!shape_ok(N, K) || T < 1 || T > 8) return QGEMV_ERR_INVALID_ARG;
+    if (single_ws_bytes(N, K, T, false, nullptr) > kNoAllocScratchBytes) return QGEMV_ERR_UNSUPPORTED;
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QGEMV_ERR_CUDA;
+    void *scratch = nullptr;
+    {
+        // Once per device, with that device current: the array's device
+        // address (host code cannot use the symbol itself as a pointer).
+        std::lock_guard<std::mutex> lock(g_noalloc_mu);
+        if (g_noalloc_ptr[dev] == nullptr) {
+            void *p = nullptr;
+            if (cudaGetSymbolAddress(&p, g_noalloc_scratch) != cudaSuccess || p == nullptr) return QGEMV_ERR_CUDA;
+            g_noalloc_ptr[dev] = p;
+        }
+        scratch = g_noalloc_ptr[dev];
+    }
+    // All calls share the array and it keeps the last call's contents: the
+    // counters must start at zero, so clear them on the caller's stream.
+    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
+    if (cudaMemsetAsync(scratch, 0, static_cast<size_t>(CNT_AREA), st) != cudaSuccess) return QGEMV_ERR_CUDA;
+    return qgemv_q4_0_argmax(W, layout, xq, y_or_null, idx, N, K, T, scratch,
+                             static_cast<size_t>(kNoAllocScratchBytes), stream);
+}
