@@ -253,11 +253,12 @@ def build_moe(T, seed, dev, sets=4, n_experts=256, top_k=8, d_model=2048, d_ff=5
     return wl
 
 
-def build_workload(name: str, dev, T: int | None = None, keep_host: bool = False) -> Workload:
+def build_workload(name: str, dev, T: int | None = None, keep_host: bool = False,
+                   layers: int | None = None) -> Workload:
     spec = synth.WORKLOADS[name]
     if spec["kind"] == "seq":
         T = T or spec.get("T", 1)
-        return build_layerset(name, spec["layer"], spec["layers"], T, spec["seed"], dev, keep_host)
+        return build_layerset(name, spec["layer"], layers or spec["layers"], T, spec["seed"], dev, keep_host)
     if spec["kind"] == "argmax":
         return build_lm_head(T or spec["T"], spec["seed"], dev, spec["copies"], keep_host, spec["N"], spec["K"])
     if spec["kind"] == "single":
@@ -447,6 +448,8 @@ def main(argv=None):
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=20)
+    ap.add_argument("--layers", type=int, default=None,
+                    help="fewer layers of a layer-set workload (smaller profiling captures only)")
     args = ap.parse_args(argv)
     assert args.warmup >= 3, "at least 3 warm-up steps"
     if args.impl == "reference":
@@ -467,7 +470,7 @@ def main(argv=None):
     Ts = [args.T] if args.T else list(spec.get("Ts", [spec.get("T", 1)]))
     results = {}
     for T in Ts:
-        results[T] = measure(args, build_workload(args.workload, dev, T=T), dev, world, rank)
+        results[T] = measure(args, build_workload(args.workload, dev, T=T, layers=args.layers), dev, world, rank)
         torch.cuda.empty_cache()
     head = results[Ts[0]]
     if rank == 0:
