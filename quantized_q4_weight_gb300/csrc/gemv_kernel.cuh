@@ -55,9 +55,10 @@ __device__ __forceinline__ ItemInfo decode_item(const Params<MAXG> &P, long long
     const int gi = group_of_item(P, i, gi_hint);
     gi_hint = gi;
     const Group &g = P.g[gi];
-    const long long local = i - g.item_begin;
-    const int e = static_cast<int>(local / g.items_per_inst);
-    const int r = static_cast<int>(local - static_cast<long long>(e) * g.items_per_inst);
+    const int local = static_cast<int>(i - g.item_begin);  // a launch has < 2^31 items
+    const int ipi = g.items_per_inst;
+    const int e = local / ipi;
+    const int r = local - e * ipi;
     int expert = e;
     it.bad = false;
     if (P.ids != nullptr) {
@@ -68,11 +69,12 @@ __device__ __forceinline__ ItemInfo decode_item(const Params<MAXG> &P, long long
     it.gi = gi;
     it.e = e;
     it.Wi = g.W + static_cast<long long>(expert) * g.w_stride;
-    if (r < g.nslabs * g.split) {
+    const int split = g.split;
+    if (r < g.nslabs * split) {
         it.kind = 0;
-        it.slab = r / g.split;
-        const int part = r - it.slab * g.split;
-        const int spp = (g.nseg + g.split - 1) / g.split;
+        it.slab = r / split;
+        const int part = r - it.slab * split;
+        const int spp = (g.nseg + split - 1) / split;
         it.seg0 = part * spp;
         it.seg1 = min(g.nseg, it.seg0 + spp);
         it.rows = min(SLAB_ROWS, g.N - it.slab * SLAB_ROWS);
@@ -123,8 +125,8 @@ __device__ __forceinline__ long long run_end(const Params<MAXG> &P, long long i,
     const int gi = group_of_item(P, i, gi_hint);
     gi_hint = gi;
     const Group &g = P.g[gi];
-    const long long e = (i - g.item_begin) / g.items_per_inst;
-    const long long end = g.item_begin + (e + 1) * g.items_per_inst;
+    const int e = static_cast<int>(i - g.item_begin) / g.items_per_inst;
+    const long long end = g.item_begin + static_cast<long long>(e + 1) * g.items_per_inst;
     return end < i1 ? end : i1;
 }
 
@@ -142,10 +144,10 @@ struct StageCursor {
         return (P.ggml || info.kind != 0 || info.bad) ? 0 : info.seg1 - info.seg0;
     }
 
-    // Move to this warp's next item (it + NWARPS, or the first one of a later run).
+    // Move to this warp's next item (it + nwarps, or the first one of a later run).
     __device__ __forceinline__ bool next_item(const Params<MAXG> &P, int warp)
     {
-        it += NWARPS;
+        it += P.nwarps;
         while (it >= rend) {
             const long long ra = rend;
             if (ra >= i1) return false;
@@ -236,6 +238,28 @@ __device__ __forceinline__ void segment_from_stage(const uint8_t *stage, int s, 
     }
 }
 
+// A full segment (16 blocks = 4 full quads) from a shared-memory stage:
+// branch-free, every load of the segment issued before the arithmetic.
+template <int T>
+__device__ __forceinline__ void segment_full_from_stage(const uint8_t *stage, int s, int K, int nb, int r8, int j,
+                                                        const int8_t *xs_q, const int2 *xs_cd, float (&acc)[2][T])
+{
+    const int lo = (r8 * QUAD + j) * 16;
+    uint4 n0[4], n1[4];
+    unsigned sc[4];
+#pragma unroll
+    for (int qq = 0; qq < 4; ++qq) {
+        const uint8_t *q = stage + qq * QUAD_BYTES;
+        n0[qq] = *reinterpret_cast<const uint4 *>(q + lo);
+        n1[qq] = *reinterpret_cast<const uint4 *>(q + lo + 8 * QUAD * 16);
+        sc[qq] = *reinterpret_cast<const unsigned *>(q + 256 * QUAD + (r8 * QUAD + j) * 4);
+    }
+#pragma unroll
+    for (int qq = 0; qq < 4; ++qq)
+        fma_block<T>(n0[qq], n1[qq], h2f(sc[qq]), h2f(sc[qq] >> 16), SEG_BLOCKS * s + QUAD * qq + j, K, nb, xs_q,
+                     xs_cd, acc);
+}
+
 // One segment read directly from GGML-layout rows in global memory (rows of
 // the packed tail, or every row when the weights are not packed).
 template <int T>
@@ -274,15 +298,20 @@ __device__ __forceinline__ void combine_phases(float (&acc)[2][T])
         }
 }
 
+// Warps per CTA a T-token kernel may use: 16 for T <= 2, 8 above (the
+// wider accumulators need more than 128 registers per thread).
+__host__ __device__ constexpr int max_warps_for(int T) { return T <= 2 ? NWARPS_MAX : 8; }
+
 template <int T, int MAXG, bool ARGMAX>
-__global__ void __launch_bounds__(NTHREADS, 1) qgemv_stream_kernel(const __grid_constant__ Params<MAXG> P)
+__global__ void __launch_bounds__(max_warps_for(T) * 32, 1) qgemv_stream_kernel(const __grid_constant__ Params<MAXG> P)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_abort;
     __shared__ int s_last;
-    __shared__ unsigned long long s_best[NWARPS * T];
+    __shared__ unsigned long long s_best[NWARPS_MAX * T];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const int nw = P.nwarps, nthreads = nw * 32;
     const int r8 = lane >> 2, j = lane & 3;
     const int D = P.ring_depth;
     int8_t *xs_q = reinterpret_cast<int8_t *>(smem);
@@ -290,7 +319,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qgemv_stream_kernel(const __grid_
     int2 *xs_cd = reinterpret_cast<int2 *>(smem + P.off_cd);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + P.off_bar);
     uint64_t *wbar = bars + warp * D;
-    uint64_t *xbar = bars + NWARPS * D;
+    uint64_t *xbar = bars + nw * D;
     uint8_t *ring = smem + P.off_ring + static_cast<size_t>(warp) * D * SEG_BYTES;
     volatile int *abort_flag = &s_abort;
 
@@ -313,9 +342,12 @@ __global__ void __launch_bounds__(NTHREADS, 1) qgemv_stream_kernel(const __grid_
     const uint64_t pol_x = l2_policy_evict_last();
 
     // Weights do not depend on the preceding kernel: start streaming them now.
+    // Ring bookkeeping: `issued` stages were copied; the next one to consume
+    // sits in slot `slot`, whose mbarrier is in phase `phase`.
     StageCursor<MAXG> cur;
     cur.init(P, i0, i1, warp);
-    long long issued = 0, consumed = 0;
+    int issued = 0, consumed = 0, slot = 0;
+    unsigned phase = 0;
     for (int d = 0; d < D && cur.valid; ++d) {
         if (lane == 0) {
             mbar_arrive_expect_tx(&wbar[d], cur.bytes(P));
@@ -339,7 +371,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qgemv_stream_kernel(const __grid_
         const long long rb = run_end(P, ra, i1, gi_hint);
         const Group &g = P.g[gi_hint];
         const int K = g.K, nb = g.nb, N = g.N;
-        const int e_run = static_cast<int>((ra - g.item_begin) / g.items_per_inst);
+        const int e_run = static_cast<int>(ra - g.item_begin) / g.items_per_inst;
 
         // ---- this run's activations into shared memory (whole CTA)
         __syncthreads();
@@ -357,7 +389,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qgemv_stream_kernel(const __grid_
         if (xok) x_unconfirmed = false;
         xphase ^= 1u;
         if (xok)
-            for (int i = tid; i < T * nb; i += NTHREADS) {
+            for (int i = tid; i < T * nb; i += nthreads) {
                 const int t = i / nb, b = i - t * nb;
                 const uint4 *qp = reinterpret_cast<const uint4 *>(xs_q + t * K + b * QK);
                 const int c = block_fold_const(qp[0], qp[1]);
@@ -366,7 +398,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qgemv_stream_kernel(const __grid_
         __syncthreads();
 
         // ---- this warp's items of the run
-        for (long long it = ra + warp; it < rb; it += NWARPS) {
+        for (long long it = ra + warp; it < rb; it += nw) {
             const ItemInfo inf = decode_item(P, it, gi_item);
             if (inf.bad) {
                 if (lane == 0) atomicCAS(P.status, 0u, ST_BAD_ID);
@@ -393,22 +425,30 @@ __global__ void __launch_bounds__(NTHREADS, 1) qgemv_stream_kernel(const __grid_
                 if (direct) {
                     if (xok) segment_from_ggml<T>(rows_base, inf.rows, s, K, nb, r8, j, xs_q, xs_cd, acc);
                 } else {
-                    const int slot = static_cast<int>(consumed % D);
-                    const unsigned par = static_cast<unsigned>((consumed / D) & 1);
-                    const bool ok = mbar_wait_bounded(&wbar[slot], par, abort_flag, P.status, WAIT_LIMIT_NS);
-                    ++consumed;
-                    if (ok && xok)
-                        segment_from_stage<T>(ring + slot * SEG_BYTES, s, K, nb, r8, j, xs_q, xs_cd, acc);
+                    const bool ok = mbar_wait_bounded(&wbar[slot], phase, abort_flag, P.status, WAIT_LIMIT_NS);
+                    const uint8_t *stage = ring + slot * SEG_BYTES;
+                    if (ok && xok) {
+                        if (SEG_BLOCKS * (s + 1) <= nb)
+                            segment_full_from_stage<T>(stage, s, K, nb, r8, j, xs_q, xs_cd, acc);
+                        else
+                            segment_from_stage<T>(stage, s, K, nb, r8, j, xs_q, xs_cd, acc);
+                    }
                     __syncwarp();
                     const int aborted = __shfl_sync(0xFFFFFFFFu, *abort_flag, 0);
-                    if (cur.valid && !aborted) {
+                    if (cur.valid && !aborted) {  // refill the slot just consumed
                         if (lane == 0) {
                             fence_proxy_async_smem();
-                            mbar_arrive_expect_tx(&wbar[slot], cur.bytes(P));
-                            bulk_g2s(ring + slot * SEG_BYTES, cur.src(P), cur.bytes(P), &wbar[slot], pol_w);
+                            const unsigned nbytes = cur.bytes(P);
+                            mbar_arrive_expect_tx(&wbar[slot], nbytes);
+                            bulk_g2s(ring + slot * SEG_BYTES, cur.src(P), nbytes, &wbar[slot], pol_w);
                         }
                         cur.advance(P, warp);
                         ++issued;
+                    }
+                    ++consumed;
+                    if (++slot == D) {
+                        slot = 0;
+                        phase ^= 1u;
                     }
                 }
                 combine_phases<T>(acc);
@@ -475,8 +515,13 @@ __global__ void __launch_bounds__(NTHREADS, 1) qgemv_stream_kernel(const __grid_
     }
 
     // Copies still in flight (only after an abort): wait for them, bounded.
-    for (long long n = consumed; n < issued; ++n)
-        mbar_drain(&wbar[n % D], static_cast<unsigned>((n / D) & 1));
+    for (int n = consumed; n < issued; ++n) {
+        mbar_drain(&wbar[slot], phase);
+        if (++slot == D) {
+            slot = 0;
+            phase ^= 1u;
+        }
+    }
     if (x_unconfirmed) mbar_drain(xbar, xphase ^ 1u);
 
     if (ARGMAX) {
@@ -493,7 +538,7 @@ __global__ void __launch_bounds__(NTHREADS, 1) qgemv_stream_kernel(const __grid_
         __syncthreads();
         if (tid < T) {
             unsigned long long m = 0ull;
-            for (int w = 0; w < NWARPS; ++w) m = max(m, s_best[w * T + tid]);
+            for (int w = 0; w < nw; ++w) m = max(m, s_best[w * T + tid]);
             P.am_cand[static_cast<long long>(blockIdx.x) * T + tid] = m;
         }
         __threadfence();

@@ -34,7 +34,7 @@ cudaError_t launch_stream(const Params<MAXG> &P, int grid, size_t smem, cudaStre
     }
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
-    cfg.blockDim = dim3(NTHREADS);
+    cfg.blockDim = dim3(static_cast<unsigned>(P.nwarps * 32));
     cfg.dynamicSmemBytes = smem;
     cfg.stream = st;
     cudaLaunchAttribute attr[1];

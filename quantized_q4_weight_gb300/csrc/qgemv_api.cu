@@ -7,6 +7,7 @@
 #include <vector>
 
 #include "../../include/qgemv.h"
+#include "gemv_kernel.cuh"
 #include "qgemv_launch.h"
 
 using namespace qg;
@@ -172,18 +173,28 @@ qgemv_status make_plan(const GroupSpec *gs, int n, int T, bool ggml, bool argmax
     P.off_d = static_cast<int>(xsize);
     P.off_cd = static_cast<int>(align_up(xsize + dsize, 16));
     P.off_bar = static_cast<int>(align_up(P.off_cd + 8ll * T * nbmax, 128));
+    // Warps per CTA and stages per warp: 16 warps with at least two stages
+    // each when they fit (more warps hide the block arithmetic's latency),
+    // else 8 warps with as many stages as fit.
     P.ring_depth = 0;
-    for (int D = MAX_RING; D >= 1; --D) {
-        const long long ring_off = align_up(P.off_bar + 8ll * (NWARPS * D + 1), 128);
-        const long long total = ring_off + (ggml ? 0 : static_cast<long long>(NWARPS) * D * SEG_BYTES);
-        if (smem_limit <= 0 || total <= smem_limit) {
-            P.ring_depth = D;
-            P.off_ring = static_cast<int>(ring_off);
-            pl.smem = static_cast<size_t>(total);
-            break;
+    const int choices[2][2] = {{max_warps_for(T), 2}, {8, 1}};
+    for (const auto &c : choices) {
+        const int nw = c[0];
+        for (int D = MAX_RING; D >= c[1]; --D) {
+            const long long ring_off = align_up(P.off_bar + 8ll * (nw * D + 1), 128);
+            const long long total = ring_off + (ggml ? 0 : static_cast<long long>(nw) * D * SEG_BYTES);
+            if (smem_limit <= 0 || total <= smem_limit) {
+                P.nwarps = nw;
+                P.ring_depth = D;
+                P.off_ring = static_cast<int>(ring_off);
+                pl.smem = static_cast<size_t>(total);
+                break;
+            }
         }
+        if (P.ring_depth) break;
     }
     if (P.ring_depth == 0) return QGEMV_ERR_UNSUPPORTED;
+    if (items >= (1ll << 31)) return QGEMV_ERR_UNSUPPORTED;
     return QGEMV_OK;
 }
 

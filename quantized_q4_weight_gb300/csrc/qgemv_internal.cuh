@@ -21,8 +21,8 @@ constexpr int SEG_BLOCKS = 16;        // blocks per summation segment (= one pip
 constexpr int SLAB_COL_BYTES = SLAB_ROWS * Q4_BYTES;    // 288: one block column of a slab
 constexpr int QUAD_BYTES = QUAD * SLAB_COL_BYTES;       // 1152
 constexpr int SEG_BYTES = SEG_BLOCKS * SLAB_COL_BYTES;  // 4608
-constexpr int NWARPS = 8;             // consumer warps per CTA (one CTA per SM)
-constexpr int NTHREADS = NWARPS * 32;
+constexpr int NWARPS_MAX = 16;        // consumer warps per CTA (one CTA per SM); 8..16 at run time
+constexpr int NTHREADS_MAX = NWARPS_MAX * 32;
 constexpr int MAX_RING = 6;           // pipeline stages per warp, upper bound
 constexpr int MAX_GRID = 1024;        // argmax candidate slots
 constexpr int SPLIT_SLAB_THRESHOLD = 2048;  // split K only when a launch has fewer slabs
@@ -57,6 +57,7 @@ template <int MAXG>
 struct Params {
     int ngroups;
     int ggml;               // weights in GGML layout (no TMA staging)
+    int nwarps;             // warps per CTA (blockDim.x / 32)
     int ring_depth;         // stages per warp
     int kmax, nbmax;        // largest K / blocks per row over the groups
     int off_d, off_cd, off_bar, off_ring;  // dynamic shared-memory layout
