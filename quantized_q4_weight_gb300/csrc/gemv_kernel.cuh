@@ -201,7 +201,9 @@ struct StageCursor {
     }
 };
 
-// acc[h][t] += (d_w(h) * d_x(t)) * isum for one block b of rows h = 0, 1.
+// acc[h][t] += (d_w(h) * d_x(t)) * isum for one block b of rows h = 0, 1,
+// formed as (d_w * (d_x / 16)) * (16 isum): the same real product, so one
+// fused multiply-add rounds it exactly as (d_w * d_x) * isum would.
 template <int T>
 __device__ __forceinline__ void fma_block(const uint4 &n0, const uint4 &n1, float dw0, float dw1, int b, int K,
                                           int nb, const int8_t *xs_q, const int2 *xs_cd, float (&acc)[2][T])
@@ -211,9 +213,9 @@ __device__ __forceinline__ void fma_block(const uint4 &n0, const uint4 &n1, floa
         const uint4 *xp = reinterpret_cast<const uint4 *>(xs_q + t * K + b * QK);
         const uint4 qa = xp[0], qb = xp[1];
         const int2 cd = xs_cd[t * nb + b];
-        const int s0 = block_dot_magic(n0, qa, qb, cd.x);
-        const int s1 = block_dot_magic(n1, qa, qb, cd.x);
-        const float dx = __int_as_float(cd.y);
+        const int s0 = block_dot16_magic(n0, qa, qb, cd.x);   // MAGIC + 16 isum
+        const int s1 = block_dot16_magic(n1, qa, qb, cd.x);
+        const float dx = __int_as_float(cd.y);                // d_x / 16 (exact)
         acc[0][t] = __fmaf_rn(__fmul_rn(dw0, dx), magic_to_float(s0), acc[0][t]);
         acc[1][t] = __fmaf_rn(__fmul_rn(dw1, dx), magic_to_float(s1), acc[1][t]);
     }
@@ -302,226 +304,589 @@ __device__ __forceinline__ void combine_phases(float (&acc)[2][T])
 // wider accumulators need more than 128 registers per thread).
 __host__ __device__ constexpr int max_warps_for(int T) { return T <= 2 ? NWARPS_MAX : 8; }
 
+// ------------------------------------------------------------------ balanced mode
+//
+// When a CTA's runs (consecutive items of one GEMV instance) all fit their
+// activations in shared memory at once, the CTA loads them all up front and
+// splits its stages (16-block segments) evenly over its warps: warp w takes
+// the contiguous stages [S w / nw, S (w + 1) / nw).  A slab cut by such a
+// boundary keeps the fixed summation order: the warp holding its first
+// segments processes them first and leaves their ordered sum H in shared
+// memory; the warp holding the rest processes them last, continuing the
+// ordered sum from H.  Each warp therefore walks: its boundary head, its
+// whole slabs, its boundary tail.
+
+constexpr int MAX_RUNS = 32;
+
+struct RunInfo {
+    const uint8_t *Wi;  // instance weights (expert resolved)
+    float *y;           // instance output
+    int stage0;         // CTA-local index of the run's first stage
+    int nstages;        // stages of the run in this CTA (items * nseg)
+    int first_local;    // index of the run's first item within its instance
+    int gi, e;          // group, instance (slot)
+    int nseg, nb, K, N, nslabs;
+    int xq_off;         // shared-memory offset of the run's activations
+    int bad;            // gather slot with an expert id out of range
+};
+
+// Walks CTA-local stages over up to three intervals, in order, keeping
+// (run, item-in-run, segment) incrementally.  With tma_only it skips stages
+// that are not copied by TMA (GGML rows, packed tails, bad slots).
+struct SpanWalker {
+    int ivb[3], ive[3];
+    int iv, k, r, ii, s;
+    bool valid;
+
+    __device__ __forceinline__ void locate(const RunInfo *runs)
+    {
+        while (k >= runs[r].stage0 + runs[r].nstages) ++r;
+        while (k < runs[r].stage0) --r;
+        const int ks = k - runs[r].stage0;
+        ii = ks / runs[r].nseg;
+        s = ks - ii * runs[r].nseg;
+    }
+
+    __device__ __forceinline__ bool stage_is_tma(const RunInfo *runs, bool ggml) const
+    {
+        const RunInfo &R = runs[r];
+        return !ggml && !R.bad && R.first_local + ii < R.nslabs;
+    }
+
+    __device__ __forceinline__ void enter_interval(const RunInfo *runs)
+    {
+        while (iv < 3 && ivb[iv] >= ive[iv]) ++iv;
+        valid = iv < 3;
+        if (valid) {
+            k = ivb[iv];
+            locate(runs);
+        }
+    }
+
+    __device__ __forceinline__ void step(const RunInfo *runs)
+    {
+        ++k;
+        if (k >= ive[iv]) {
+            ++iv;
+            enter_interval(runs);
+            return;
+        }
+        if (++s == runs[r].nseg) {
+            s = 0;
+            if (k >= runs[r].stage0 + runs[r].nstages) {
+                ++r;
+                ii = 0;
+            } else {
+                ++ii;
+            }
+        }
+    }
+
+    __device__ __forceinline__ void init(const RunInfo *runs, const int (&b)[3], const int (&e)[3], bool tma_only,
+                                         bool ggml)
+    {
+        for (int i = 0; i < 3; ++i) {
+            ivb[i] = b[i];
+            ive[i] = e[i];
+        }
+        iv = 0;
+        r = 0;
+        enter_interval(runs);
+        if (tma_only)
+            while (valid && !stage_is_tma(runs, ggml)) step(runs);
+    }
+
+    __device__ __forceinline__ void advance_tma(const RunInfo *runs, bool ggml)
+    {
+        do step(runs);
+        while (valid && !stage_is_tma(runs, ggml));
+    }
+
+    __device__ __forceinline__ const uint8_t *src(const RunInfo *runs) const
+    {
+        const RunInfo &R = runs[r];
+        return R.Wi + static_cast<long long>(R.first_local + ii) * SLAB_COL_BYTES * R.nb +
+               static_cast<long long>(s) * SEG_BYTES;
+    }
+
+    __device__ __forceinline__ unsigned bytes(const RunInfo *runs) const
+    {
+        return static_cast<unsigned>(SLAB_COL_BYTES * min(SEG_BLOCKS, runs[r].nb - SEG_BLOCKS * s));
+    }
+};
+
+// Per-warp ring of TMA stages: slot / phase of the next stage to consume.
+struct Ring {
+    uint8_t *base;
+    uint64_t *bar;
+    int D, slot, issued, consumed;
+    unsigned phase;
+
+    __device__ __forceinline__ uint8_t *stage() const { return base + slot * SEG_BYTES; }
+
+    __device__ __forceinline__ void issue(int lane, int into, const uint8_t *src, unsigned nbytes, uint64_t pol)
+    {
+        if (lane == 0) {
+            fence_proxy_async_smem();
+            mbar_arrive_expect_tx(&bar[into], nbytes);
+            bulk_g2s(base + into * SEG_BYTES, src, nbytes, &bar[into], pol);
+        }
+        ++issued;
+    }
+
+    __device__ __forceinline__ void pop()
+    {
+        ++consumed;
+        if (++slot == D) {
+            slot = 0;
+            phase ^= 1u;
+        }
+    }
+
+    __device__ __forceinline__ void drain()
+    {
+        while (consumed < issued) {
+            mbar_drain(&bar[slot], phase);
+            pop();
+        }
+    }
+};
+
+template <int T, bool ARGMAX>
+__device__ __forceinline__ void store_rows(float *ye, int N, int row0, int rows, int r8, int j, const float (&yv)[2][T],
+                                           unsigned long long (&best)[T])
+{
+    if (j != 0) return;
+#pragma unroll
+    for (int h = 0; h < 2; ++h) {
+        const int lr = r8 + 8 * h;
+        if (lr < rows) {
+            const int row = row0 + lr;
+#pragma unroll
+            for (int t = 0; t < T; ++t) {
+                if (ye != nullptr) ye[static_cast<long long>(t) * N + row] = yv[h][t];
+                if (ARGMAX) best[t] = max(best[t], argmax_key(yv[h][t], static_cast<unsigned>(row)));
+            }
+        }
+    }
+}
+
+// Bounded spin on a shared-memory flag written by another warp of the CTA.
+__device__ __forceinline__ bool wait_flag(volatile int *flag, volatile int *abort_flag, unsigned *status)
+{
+    if (*flag) return true;
+    const uint64_t t0 = global_timer_ns();
+    while (!*flag) {
+        if (*abort_flag) return false;
+        if (global_timer_ns() - t0 > WAIT_LIMIT_NS) {
+            *abort_flag = 1;
+            atomicCAS(status, 0u, ST_TIMEOUT);
+            return false;
+        }
+    }
+    return true;
+}
+
 template <int T, int MAXG, bool ARGMAX>
 __global__ void __launch_bounds__(max_warps_for(T) * 32, 1) qgemv_stream_kernel(const __grid_constant__ Params<MAXG> P)
 {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_abort;
     __shared__ int s_last;
+    __shared__ int s_nruns;  // > 0: balanced mode with this many runs
+    __shared__ int s_stages;
     __shared__ unsigned long long s_best[NWARPS_MAX * T];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nw = P.nwarps, nthreads = nw * 32;
     const int r8 = lane >> 2, j = lane & 3;
     const int D = P.ring_depth;
-    int8_t *xs_q = reinterpret_cast<int8_t *>(smem);
-    const unsigned short *xs_d = reinterpret_cast<const unsigned short *>(smem + P.off_d);
-    int2 *xs_cd = reinterpret_cast<int2 *>(smem + P.off_cd);
     uint64_t *bars = reinterpret_cast<uint64_t *>(smem + P.off_bar);
-    uint64_t *wbar = bars + warp * D;
     uint64_t *xbar = bars + nw * D;
-    uint8_t *ring = smem + P.off_ring + static_cast<size_t>(warp) * D * SEG_BYTES;
+    RunInfo *runs = reinterpret_cast<RunInfo *>(smem + P.off_runs);
+    float *hbuf = reinterpret_cast<float *>(smem + P.off_hbuf);          // [nw][T][16]
+    volatile int *hflag = reinterpret_cast<volatile int *>(smem + P.off_hflag);
     volatile int *abort_flag = &s_abort;
 
-    if (tid == 0) {
-        s_abort = 0;
-        mbar_init(xbar, 1);
-    }
-    if (lane == 0)
-        for (int d = 0; d < D; ++d) mbar_init(&wbar[d], 1);
-    fence_mbar_init();
-    __syncthreads();
-    pdl_launch_dependents();
+    Ring ring;
+    ring.base = smem + P.off_ring + static_cast<size_t>(warp) * D * SEG_BYTES;
+    ring.bar = bars + warp * D;
+    ring.D = D;
+    ring.slot = 0;
+    ring.phase = 0;
+    ring.issued = 0;
+    ring.consumed = 0;
 
     const long long b0 = P.total_bytes * blockIdx.x / gridDim.x;
     const long long b1 = P.total_bytes * (blockIdx.x + 1) / gridDim.x;
     const long long i0 = first_item_at_or_after(P, b0);
     const long long i1 = first_item_at_or_after(P, b1);
 
+    if (tid == 0) {
+        s_abort = 0;
+        mbar_init(xbar, 1);
+        // Run table for the balanced mode (thread 0 walks the CTA's runs).
+        int nr = 0, stages = 0, nseg_max = 0, xoff = 0;
+        bool fits = P.balanced_ok != 0;
+        int gh = 0;
+        for (long long ra = i0; ra < i1 && fits;) {
+            const long long rb = run_end(P, ra, i1, gh);
+            const Group &g = P.g[gh];
+            if (nr == MAX_RUNS) {
+                fits = false;
+                break;
+            }
+            const int local = static_cast<int>(ra - g.item_begin);
+            const int e = local / g.items_per_inst;
+            int expert = e, bad = 0;
+            if (P.ids != nullptr) {
+                expert = __ldg(P.ids + e);
+                bad = (expert < 0 || expert >= P.n_experts) ? 1 : 0;
+                if (bad) expert = 0;
+            }
+            RunInfo &R = runs[nr];
+            R.Wi = g.W + static_cast<long long>(expert) * g.w_stride;
+            R.y = g.y + static_cast<long long>(e) * g.y_stride;
+            R.stage0 = stages;
+            R.nstages = static_cast<int>(rb - ra) * g.nseg;
+            R.first_local = local - e * g.items_per_inst;
+            R.gi = gh;
+            R.e = e;
+            R.nseg = g.nseg;
+            R.nb = g.nb;
+            R.K = g.K;
+            R.N = g.N;
+            R.nslabs = g.nslabs;
+            R.xq_off = xoff;
+            R.bad = bad;
+            const int slot_bytes = (T * g.K + static_cast<int>(roundup16_dev(2 * T * g.nb)) + 8 * T * g.nb + 127) & ~127;
+            xoff += slot_bytes;
+            stages += R.nstages;
+            nseg_max = max(nseg_max, g.nseg);
+            ++nr;
+            ra = rb;
+        }
+        if (xoff > P.xq_area || stages / nw < nseg_max || nr == 0) fits = false;
+        s_nruns = fits ? nr : 0;
+        s_stages = stages;
+    }
+    if (lane == 0)
+        for (int d = 0; d < D; ++d) mbar_init(&ring.bar[d], 1);
+    if (tid < nw) hflag[tid] = 0;
+    fence_mbar_init();
+    __syncthreads();
+    pdl_launch_dependents();
+
     const uint64_t pol_w = l2_policy_evict_first();
     const uint64_t pol_x = l2_policy_evict_last();
-
-    // Weights do not depend on the preceding kernel: start streaming them now.
-    // Ring bookkeeping: `issued` stages were copied; the next one to consume
-    // sits in slot `slot`, whose mbarrier is in phase `phase`.
-    StageCursor<MAXG> cur;
-    cur.init(P, i0, i1, warp);
-    int issued = 0, consumed = 0, slot = 0;
-    unsigned phase = 0;
-    for (int d = 0; d < D && cur.valid; ++d) {
-        if (lane == 0) {
-            mbar_arrive_expect_tx(&wbar[d], cur.bytes(P));
-            bulk_g2s(ring + d * SEG_BYTES, cur.src(P), cur.bytes(P), &wbar[d], pol_w);
-        }
-        cur.advance(P, warp);
-        ++issued;
-    }
-
-    // Activations (and every output) depend on the preceding kernel.
-    pdl_wait();
+    const int nruns = s_nruns;
 
     unsigned long long best[T];
 #pragma unroll
     for (int t = 0; t < T; ++t) best[t] = 0ull;
-
-    int gi_hint = 0, gi_item = 0;
-    unsigned xphase = 0;
     bool x_unconfirmed = false;  // thread 0: an activation copy was issued but not seen complete
-    for (long long ra = i0; ra < i1;) {
-        const long long rb = run_end(P, ra, i1, gi_hint);
-        const Group &g = P.g[gi_hint];
-        const int K = g.K, nb = g.nb, N = g.N;
-        const int e_run = static_cast<int>(ra - g.item_begin) / g.items_per_inst;
+    unsigned xphase = 0;
 
-        // ---- this run's activations into shared memory (whole CTA)
-        __syncthreads();
-        if (tid == 0 && !*abort_flag) {
-            x_unconfirmed = true;
-            fence_proxy_async_smem();
-            const uint8_t *src = g.xq + static_cast<long long>(e_run) * g.xq_stride;
-            const unsigned qbytes = static_cast<unsigned>(T * K);
-            const unsigned dbytes = static_cast<unsigned>(g.xq_bytes) - qbytes;
-            mbar_arrive_expect_tx(xbar, qbytes + dbytes);
-            bulk_g2s(xs_q, src, qbytes, xbar, pol_x);
-            bulk_g2s(smem + P.off_d, src + qbytes, dbytes, xbar, pol_x);
+    if (nruns > 0) {
+        // ================================================= balanced mode
+        const int S = s_stages;
+        const int a = static_cast<int>(static_cast<long long>(S) * warp / nw);
+        const int b = static_cast<int>(static_cast<long long>(S) * (warp + 1) / nw);
+        // boundary items: is stage p inside (not at the start of) an item?
+        auto item_start = [&](int p) {
+            int r = 0;
+            while (p >= runs[r].stage0 + runs[r].nstages) ++r;
+            return p - (p - runs[r].stage0) % runs[r].nseg;
+        };
+        int head_b = b, tail_e = a;
+        if (b < S && b > a) {
+            const int st = item_start(b);
+            if (st != b) head_b = st;  // [st, b) is the head of an item continued by warp + 1
         }
-        const bool xok = mbar_wait_bounded(xbar, xphase, abort_flag, P.status, WAIT_LIMIT_NS);
-        if (xok) x_unconfirmed = false;
+        if (a > 0 && a < b) {
+            const int st = item_start(a);
+            if (st != a) {
+                int r = 0;
+                while (a >= runs[r].stage0 + runs[r].nstages) ++r;
+                tail_e = st + runs[r].nseg;  // [a, tail_e) finishes an item begun by warp - 1
+            }
+        }
+        const int ivb[3] = {head_b, tail_e, a};
+        const int ive[3] = {b, head_b, tail_e};
+
+        // weights first (they do not depend on the preceding kernel)
+        SpanWalker cur;
+        cur.init(runs, ivb, ive, true, P.ggml != 0);
+        for (int d = 0; d < D && cur.valid; ++d) {
+            ring.issue(lane, d, cur.src(runs), cur.bytes(runs), pol_w);
+            cur.advance_tma(runs, P.ggml != 0);
+        }
+        pdl_wait();
+        // every run's activations, one transaction count on one barrier
+        if (tid == 0 && !*abort_flag) {
+            unsigned tx = 0;
+            for (int r = 0; r < nruns; ++r) tx += static_cast<unsigned>(P.g[runs[r].gi].xq_bytes);
+            x_unconfirmed = true;
+            mbar_arrive_expect_tx(xbar, tx);
+            for (int r = 0; r < nruns; ++r) {
+                const RunInfo &R = runs[r];
+                const Group &g = P.g[R.gi];
+                const uint8_t *src = g.xq + static_cast<long long>(R.e) * g.xq_stride;
+                const unsigned qbytes = static_cast<unsigned>(T * R.K);
+                const unsigned dbytes = static_cast<unsigned>(g.xq_bytes) - qbytes;
+                bulk_g2s(smem + R.xq_off, src, qbytes, xbar, pol_x);
+                bulk_g2s(smem + R.xq_off + qbytes, src + qbytes, dbytes, xbar, pol_x);
+            }
+        }
+        const bool xok = mbar_wait_bounded(xbar, 0, abort_flag, P.status, WAIT_LIMIT_NS);
         xphase ^= 1u;
+        if (xok) x_unconfirmed = false;
         if (xok)
-            for (int i = tid; i < T * nb; i += nthreads) {
-                const int t = i / nb, b = i - t * nb;
-                const uint4 *qp = reinterpret_cast<const uint4 *>(xs_q + t * K + b * QK);
-                const int c = block_fold_const(qp[0], qp[1]);
-                xs_cd[i] = make_int2(c, __float_as_int(h2f(xs_d[i])));
+            for (int r = 0; r < nruns; ++r) {
+                const RunInfo &R = runs[r];
+                const int8_t *xq = reinterpret_cast<const int8_t *>(smem + R.xq_off);
+                const unsigned short *xd = reinterpret_cast<const unsigned short *>(smem + R.xq_off + T * R.K);
+                int2 *cd = reinterpret_cast<int2 *>(smem + R.xq_off + T * R.K +
+                                                    static_cast<int>(roundup16_dev(2 * T * R.nb)));
+                for (int i = tid; i < T * R.nb; i += nthreads) {
+                    const int t = i / R.nb, bb = i - t * R.nb;
+                    const uint4 *qp = reinterpret_cast<const uint4 *>(xq + t * R.K + bb * QK);
+                    cd[i] = make_int2(block_fold16_const(qp[0], qp[1]), __float_as_int(__fmul_rn(h2f(xd[i]), 0.0625f)));
+                }
             }
         __syncthreads();
 
-        // ---- this warp's items of the run
-        for (long long it = ra + warp; it < rb; it += nw) {
-            const ItemInfo inf = decode_item(P, it, gi_item);
-            if (inf.bad) {
-                if (lane == 0) atomicCAS(P.status, 0u, ST_BAD_ID);
-                continue;
-            }
-            const bool direct = P.ggml || inf.kind != 0;
-            const bool split = g.split > 1 && inf.kind == 0;  // a packed tail is never split
-            const uint8_t *rows_base =
-                inf.kind != 0 ? inf.Wi + static_cast<long long>(g.nslabs) * g.slab_bytes
-                              : inf.Wi + static_cast<long long>(inf.slab) * SLAB_ROWS * nb * Q4_BYTES;
+        // compute, in the walker's order
+        SpanWalker w;
+        w.init(runs, ivb, ive, false, P.ggml != 0);
+        while (w.valid) {
+            const RunInfo &R = runs[w.r];
+            const int iv = w.iv, ii = w.ii, s_first = w.s;
+            const int seg_end = min(R.nseg, s_first + (w.ive[iv] - w.k));   // this visit's segments
+            const int li = R.first_local + ii;
+            const bool tail_item = li >= R.nslabs;
+            const bool direct = P.ggml != 0 || tail_item;
+            const Group &g = P.g[R.gi];
+            const int rows = tail_item ? g.tail_rows : min(SLAB_ROWS, R.N - li * SLAB_ROWS);
+            const int row0 = li * SLAB_ROWS;
+            const uint8_t *rows_base = R.Wi + static_cast<long long>(li) * SLAB_ROWS * R.nb * Q4_BYTES;
+            const int8_t *xs_q = reinterpret_cast<const int8_t *>(smem + R.xq_off);
+            const int2 *xs_cd = reinterpret_cast<const int2 *>(smem + R.xq_off + T * R.K +
+                                                               static_cast<int>(roundup16_dev(2 * T * R.nb)));
             float yv[2][T];
 #pragma unroll
             for (int h = 0; h < 2; ++h)
 #pragma unroll
                 for (int t = 0; t < T; ++t) yv[h][t] = 0.0f;
-
-            for (int s = inf.seg0; s < inf.seg1; ++s) {
+            if (s_first > 0) {
+                // tail of an item begun by warp - 1: continue from its ordered sum
+                if (lane == 0) wait_flag(&hflag[warp - 1], abort_flag, P.status);
+                __syncwarp();
+                __threadfence_block();
+                const float *H = hbuf + (warp - 1) * T * 16;
+#pragma unroll
+                for (int t = 0; t < T; ++t) {
+                    yv[0][t] = H[t * 16 + r8];
+                    yv[1][t] = H[t * 16 + r8 + 8];
+                }
+            }
+            for (int sg = s_first; sg < seg_end; ++sg) {
                 float acc[2][T];
 #pragma unroll
                 for (int h = 0; h < 2; ++h)
 #pragma unroll
                     for (int t = 0; t < T; ++t) acc[h][t] = 0.0f;
-
-                if (direct) {
-                    if (xok) segment_from_ggml<T>(rows_base, inf.rows, s, K, nb, r8, j, xs_q, xs_cd, acc);
+                if (R.bad) {
+                    // nothing is read for an out-of-range expert id
+                } else if (direct) {
+                    if (xok) segment_from_ggml<T>(rows_base, rows, sg, R.K, R.nb, r8, j, xs_q, xs_cd, acc);
                 } else {
-                    const bool ok = mbar_wait_bounded(&wbar[slot], phase, abort_flag, P.status, WAIT_LIMIT_NS);
-                    const uint8_t *stage = ring + slot * SEG_BYTES;
+                    const bool ok = mbar_wait_bounded(&ring.bar[ring.slot], ring.phase, abort_flag, P.status,
+                                                      WAIT_LIMIT_NS);
                     if (ok && xok) {
-                        if (SEG_BLOCKS * (s + 1) <= nb)
-                            segment_full_from_stage<T>(stage, s, K, nb, r8, j, xs_q, xs_cd, acc);
+                        if (SEG_BLOCKS * (sg + 1) <= R.nb)
+                            segment_full_from_stage<T>(ring.stage(), sg, R.K, R.nb, r8, j, xs_q, xs_cd, acc);
                         else
-                            segment_from_stage<T>(stage, s, K, nb, r8, j, xs_q, xs_cd, acc);
+                            segment_from_stage<T>(ring.stage(), sg, R.K, R.nb, r8, j, xs_q, xs_cd, acc);
                     }
                     __syncwarp();
                     const int aborted = __shfl_sync(0xFFFFFFFFu, *abort_flag, 0);
-                    if (cur.valid && !aborted) {  // refill the slot just consumed
-                        if (lane == 0) {
-                            fence_proxy_async_smem();
-                            const unsigned nbytes = cur.bytes(P);
-                            mbar_arrive_expect_tx(&wbar[slot], nbytes);
-                            bulk_g2s(ring + slot * SEG_BYTES, cur.src(P), nbytes, &wbar[slot], pol_w);
-                        }
-                        cur.advance(P, warp);
-                        ++issued;
+                    if (cur.valid && !aborted) {
+                        ring.issue(lane, ring.slot, cur.src(runs), cur.bytes(runs), pol_w);
+                        cur.advance_tma(runs, P.ggml != 0);
                     }
-                    ++consumed;
-                    if (++slot == D) {
-                        slot = 0;
-                        phase ^= 1u;
-                    }
+                    ring.pop();
                 }
                 combine_phases<T>(acc);
-
-                if (split) {
-                    // split-K: publish this segment's partial sums
-                    float *pb = g.part + ((static_cast<long long>(inf.e) * g.nslabs + inf.slab) * g.nseg + s) * T * 16;
-                    if (j == 0) {
 #pragma unroll
-                        for (int t = 0; t < T; ++t) {
-                            pb[t * 16 + r8] = acc[0][t];
-                            pb[t * 16 + r8 + 8] = acc[1][t];
-                        }
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int t = 0; t < T; ++t) yv[h][t] = (sg == 0) ? acc[h][t] : __fadd_rn(yv[h][t], acc[h][t]);
+            }
+            if (seg_end < R.nseg) {
+                // head of an item that warp + 1 finishes: leave the ordered sum
+                if (j == 0) {
+                    float *H = hbuf + warp * T * 16;
+#pragma unroll
+                    for (int t = 0; t < T; ++t) {
+                        H[t * 16 + r8] = yv[0][t];
+                        H[t * 16 + r8 + 8] = yv[1][t];
                     }
-                } else {
+                }
+                __threadfence_block();
+                __syncwarp();
+                if (lane == 0) hflag[warp] = 1;
+            } else if (!R.bad) {
+                store_rows<T, ARGMAX>(R.y, R.N, row0, rows, r8, j, yv, best);
+            } else if (lane == 0) {
+                atomicCAS(P.status, 0u, ST_BAD_ID);
+            }
+            // move the walker past this visit
+            for (int sg = s_first; sg < seg_end; ++sg) w.step(runs);
+        }
+    } else {
+        // ================================================= run-synced mode
+        // (small launches, split-K, or activations that do not all fit)
+        int8_t *xs_q = reinterpret_cast<int8_t *>(smem);
+        const unsigned short *xs_d = reinterpret_cast<const unsigned short *>(smem + P.off_d);
+        int2 *xs_cd = reinterpret_cast<int2 *>(smem + P.off_cd);
+        StageCursor<MAXG> cur;
+        cur.init(P, i0, i1, warp);
+        for (int d = 0; d < D && cur.valid; ++d) {
+            ring.issue(lane, d, cur.src(P), cur.bytes(P), pol_w);
+            cur.advance(P, warp);
+        }
+        pdl_wait();
+
+        int gi_hint = 0, gi_item = 0;
+        for (long long ra = i0; ra < i1;) {
+            const long long rb = run_end(P, ra, i1, gi_hint);
+            const Group &g = P.g[gi_hint];
+            const int K = g.K, nb = g.nb, N = g.N;
+            const int e_run = static_cast<int>(ra - g.item_begin) / g.items_per_inst;
+
+            __syncthreads();
+            if (tid == 0 && !*abort_flag) {
+                x_unconfirmed = true;
+                fence_proxy_async_smem();
+                const uint8_t *src = g.xq + static_cast<long long>(e_run) * g.xq_stride;
+                const unsigned qbytes = static_cast<unsigned>(T * K);
+                const unsigned dbytes = static_cast<unsigned>(g.xq_bytes) - qbytes;
+                mbar_arrive_expect_tx(xbar, qbytes + dbytes);
+                bulk_g2s(xs_q, src, qbytes, xbar, pol_x);
+                bulk_g2s(smem + P.off_d, src + qbytes, dbytes, xbar, pol_x);
+            }
+            const bool xok = mbar_wait_bounded(xbar, xphase, abort_flag, P.status, WAIT_LIMIT_NS);
+            if (xok) x_unconfirmed = false;
+            xphase ^= 1u;
+            if (xok)
+                for (int i = tid; i < T * nb; i += nthreads) {
+                    const int t = i / nb, bb = i - t * nb;
+                    const uint4 *qp = reinterpret_cast<const uint4 *>(xs_q + t * K + bb * QK);
+                    xs_cd[i] = make_int2(block_fold16_const(qp[0], qp[1]),
+                                         __float_as_int(__fmul_rn(h2f(xs_d[i]), 0.0625f)));
+                }
+            __syncthreads();
+
+            for (long long it = ra + warp; it < rb; it += nw) {
+                const ItemInfo inf = decode_item(P, it, gi_item);
+                if (inf.bad) {
+                    if (lane == 0) atomicCAS(P.status, 0u, ST_BAD_ID);
+                    continue;
+                }
+                const bool direct = P.ggml || inf.kind != 0;
+                const bool split = g.split > 1 && inf.kind == 0;  // a packed tail is never split
+                const uint8_t *rows_base =
+                    inf.kind != 0 ? inf.Wi + static_cast<long long>(g.nslabs) * g.slab_bytes
+                                  : inf.Wi + static_cast<long long>(inf.slab) * SLAB_ROWS * nb * Q4_BYTES;
+                float yv[2][T];
+#pragma unroll
+                for (int h = 0; h < 2; ++h)
+#pragma unroll
+                    for (int t = 0; t < T; ++t) yv[h][t] = 0.0f;
+
+                for (int sg = inf.seg0; sg < inf.seg1; ++sg) {
+                    float acc[2][T];
 #pragma unroll
                     for (int h = 0; h < 2; ++h)
 #pragma unroll
-                        for (int t = 0; t < T; ++t) yv[h][t] = (s == 0) ? acc[h][t] : __fadd_rn(yv[h][t], acc[h][t]);
+                        for (int t = 0; t < T; ++t) acc[h][t] = 0.0f;
+                    if (direct) {
+                        if (xok) segment_from_ggml<T>(rows_base, inf.rows, sg, K, nb, r8, j, xs_q, xs_cd, acc);
+                    } else {
+                        const bool ok = mbar_wait_bounded(&ring.bar[ring.slot], ring.phase, abort_flag, P.status,
+                                                          WAIT_LIMIT_NS);
+                        if (ok && xok) {
+                            if (SEG_BLOCKS * (sg + 1) <= nb)
+                                segment_full_from_stage<T>(ring.stage(), sg, K, nb, r8, j, xs_q, xs_cd, acc);
+                            else
+                                segment_from_stage<T>(ring.stage(), sg, K, nb, r8, j, xs_q, xs_cd, acc);
+                        }
+                        __syncwarp();
+                        const int aborted = __shfl_sync(0xFFFFFFFFu, *abort_flag, 0);
+                        if (cur.valid && !aborted) {
+                            ring.issue(lane, ring.slot, cur.src(P), cur.bytes(P), pol_w);
+                            cur.advance(P, warp);
+                        }
+                        ring.pop();
+                    }
+                    combine_phases<T>(acc);
+                    if (split) {
+                        float *pb =
+                            g.part + ((static_cast<long long>(inf.e) * g.nslabs + inf.slab) * g.nseg + sg) * T * 16;
+                        if (j == 0) {
+#pragma unroll
+                            for (int t = 0; t < T; ++t) {
+                                pb[t * 16 + r8] = acc[0][t];
+                                pb[t * 16 + r8 + 8] = acc[1][t];
+                            }
+                        }
+                    } else {
+#pragma unroll
+                        for (int h = 0; h < 2; ++h)
+#pragma unroll
+                            for (int t = 0; t < T; ++t)
+                                yv[h][t] = (sg == 0) ? acc[h][t] : __fadd_rn(yv[h][t], acc[h][t]);
+                    }
                 }
-            }
 
-            float *ye = g.y + static_cast<long long>(inf.e) * g.y_stride;
-            const int row0 = inf.slab * SLAB_ROWS;
-            if (split) {
-                __threadfence();
-                __syncwarp();
-                unsigned old = 0;
-                unsigned *cnt = g.cnt + static_cast<long long>(inf.e) * g.nslabs + inf.slab;
-                if (lane == 0) old = atomicAdd(cnt, 1u);
-                old = __shfl_sync(0xFFFFFFFFu, old, 0);
-                if (old == static_cast<unsigned>(g.split - 1)) {
+                float *ye = g.y + static_cast<long long>(inf.e) * g.y_stride;
+                const int row0 = inf.slab * SLAB_ROWS;
+                if (split) {
                     __threadfence();
-                    const float *pb = g.part + (static_cast<long long>(inf.e) * g.nslabs + inf.slab) * g.nseg * T * 16;
-                    if (lane < inf.rows) {
-                        const int row = row0 + lane;
-#pragma unroll
-                        for (int t = 0; t < T; ++t) {
-                            float v = __ldcg(pb + t * 16 + lane);
-                            for (int s2 = 1; s2 < g.nseg; ++s2) v = __fadd_rn(v, __ldcg(pb + (s2 * T + t) * 16 + lane));
-                            if (ye != nullptr) ye[static_cast<long long>(t) * N + row] = v;
-                            if (ARGMAX) best[t] = max(best[t], argmax_key(v, static_cast<unsigned>(row)));
-                        }
-                    }
                     __syncwarp();
-                    if (lane == 0) *cnt = 0u;
-                }
-            } else if (j == 0) {
+                    unsigned old = 0;
+                    unsigned *cnt = g.cnt + static_cast<long long>(inf.e) * g.nslabs + inf.slab;
+                    if (lane == 0) old = atomicAdd(cnt, 1u);
+                    old = __shfl_sync(0xFFFFFFFFu, old, 0);
+                    if (old == static_cast<unsigned>(g.split - 1)) {
+                        __threadfence();
+                        const float *pb =
+                            g.part + (static_cast<long long>(inf.e) * g.nslabs + inf.slab) * g.nseg * T * 16;
+                        if (lane < inf.rows) {
+                            const int row = row0 + lane;
 #pragma unroll
-                for (int h = 0; h < 2; ++h) {
-                    const int lr = r8 + 8 * h;
-                    if (lr < inf.rows) {
-                        const int row = row0 + lr;
-#pragma unroll
-                        for (int t = 0; t < T; ++t) {
-                            if (ye != nullptr) ye[static_cast<long long>(t) * N + row] = yv[h][t];
-                            if (ARGMAX) best[t] = max(best[t], argmax_key(yv[h][t], static_cast<unsigned>(row)));
+                            for (int t = 0; t < T; ++t) {
+                                float v = __ldcg(pb + t * 16 + lane);
+                                for (int s2 = 1; s2 < g.nseg; ++s2)
+                                    v = __fadd_rn(v, __ldcg(pb + (s2 * T + t) * 16 + lane));
+                                if (ye != nullptr) ye[static_cast<long long>(t) * N + row] = v;
+                                if (ARGMAX) best[t] = max(best[t], argmax_key(v, static_cast<unsigned>(row)));
+                            }
                         }
+                        __syncwarp();
+                        if (lane == 0) *cnt = 0u;
                     }
+                } else {
+                    store_rows<T, ARGMAX>(ye, N, row0, inf.rows, r8, j, yv, best);
                 }
             }
+            ra = rb;
         }
-        ra = rb;
     }
 
     // Copies still in flight (only after an abort): wait for them, bounded.
-    for (int n = consumed; n < issued; ++n) {
-        mbar_drain(&wbar[slot], phase);
-        if (++slot == D) {
-            slot = 0;
-            phase ^= 1u;
-        }
-    }
+    ring.drain();
     if (x_unconfirmed) mbar_drain(xbar, xphase ^ 1u);
 
     if (ARGMAX) {
@@ -549,7 +914,8 @@ __global__ void __launch_bounds__(max_warps_for(T) * 32, 1) qgemv_stream_kernel(
             __threadfence();
             if (tid < T) {
                 unsigned long long m = 0ull;
-                for (unsigned c = 0; c < gridDim.x; ++c) m = max(m, __ldcg(P.am_cand + static_cast<long long>(c) * T + tid));
+                for (unsigned c = 0; c < gridDim.x; ++c)
+                    m = max(m, __ldcg(P.am_cand + static_cast<long long>(c) * T + tid));
                 P.am_idx[tid] = static_cast<long long>(0xFFFFFFFFull - (m & 0xFFFFFFFFull));
             }
             if (tid == 0) *P.am_cnt = 0u;

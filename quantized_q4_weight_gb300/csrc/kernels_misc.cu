@@ -127,8 +127,8 @@ cudaError_t launch_pack(const void *src, void *dst, long long N, long long K, bo
 
 // ------------------------------------------------------------ block sums (test hook)
 //
-// Same unpack, dp4a chain and folded offset as the GEMV kernel
-// (block_dot_magic / block_fold_const), minus the magic bias.
+// Same unpack, dp4a chains and folded offset as the GEMV kernel
+// (block_dot16_magic / block_fold16_const), minus the magic bias, over 16.
 __global__ void __launch_bounds__(256) isums_kernel(const uint8_t *__restrict__ W, bool packed,
                                                     const uint8_t *__restrict__ xq, int32_t *__restrict__ isums,
                                                     long long N, int K, int T)
@@ -153,7 +153,7 @@ __global__ void __launch_bounds__(256) isums_kernel(const uint8_t *__restrict__ 
         }
         const uint4 *xp = reinterpret_cast<const uint4 *>(xq + t * K + static_cast<long long>(b) * QK);
         const uint4 qa = xp[0], qb = xp[1];
-        isums[i] = block_dot_magic(nib, qa, qb, block_fold_const(qa, qb)) - MAGIC_I;
+        isums[i] = (block_dot16_magic(nib, qa, qb, block_fold16_const(qa, qb)) - MAGIC_I) >> 4;
     }
 }
 

@@ -167,31 +167,42 @@ qgemv_status make_plan(const GroupSpec *gs, int n, int T, bool ggml, bool argmax
     P.nbmax = nbmax;
     pl.ws_bytes = off;
 
-    // Shared memory: activations [T][kmax], scales, folded constants, barriers, rings.
+    // Shared memory: [activation area][run table][boundary sums][flags][barriers][rings].
+    // The activation area holds one run's activations in the run-synced mode
+    // ([T][kmax] int8, fp16 scales, folded constants) and as many runs as fit
+    // in the balanced mode.
     const long long xsize = static_cast<long long>(T) * kmax;
     const long long dsize = roundup16(2ll * T * nbmax);
     P.off_d = static_cast<int>(xsize);
     P.off_cd = static_cast<int>(align_up(xsize + dsize, 16));
-    P.off_bar = static_cast<int>(align_up(P.off_cd + 8ll * T * nbmax, 128));
-    // Warps per CTA and stages per warp: 16 warps with at least two stages
-    // each when they fit (more warps hide the block arithmetic's latency),
-    // else 8 warps with as many stages as fit.
+    const long long need_x = align_up(P.off_cd + 8ll * T * nbmax, 128);
+    const long long tables = align_up(static_cast<long long>(MAX_RUNS) * sizeof(RunInfo), 128) +
+                             align_up(static_cast<long long>(NWARPS_MAX) * T * 16 * 4, 128) + 128;
+    P.balanced_ok = 1;
+    for (int i = 0; i < n; ++i)
+        if (P.g[i].split > 1) P.balanced_ok = 0;
     P.ring_depth = 0;
-    const int choices[2][2] = {{max_warps_for(T), 2}, {8, 1}};
+    // 2 stages per warp and the widest warp count that leaves room for the
+    // activations; then 8 warps; then a single stage.
+    const int choices[3][2] = {{max_warps_for(T), 2}, {8, 2}, {8, 1}};
     for (const auto &c : choices) {
-        const int nw = c[0];
-        for (int D = MAX_RING; D >= c[1]; --D) {
-            const long long ring_off = align_up(P.off_bar + 8ll * (nw * D + 1), 128);
-            const long long total = ring_off + (ggml ? 0 : static_cast<long long>(nw) * D * SEG_BYTES);
-            if (smem_limit <= 0 || total <= smem_limit) {
-                P.nwarps = nw;
-                P.ring_depth = D;
-                P.off_ring = static_cast<int>(ring_off);
-                pl.smem = static_cast<size_t>(total);
-                break;
-            }
+        const int nw = c[0], D = c[1];
+        const long long bars = align_up(8ll * (nw * D + 1), 128);
+        const long long rings = ggml ? 0 : static_cast<long long>(nw) * D * SEG_BYTES;
+        long long xa = smem_limit > 0 ? smem_limit - tables - bars - rings : need_x;
+        xa = xa / 128 * 128;
+        if (xa >= need_x) {
+            P.nwarps = nw;
+            P.ring_depth = D;
+            P.xq_area = static_cast<int>(xa);
+            P.off_runs = static_cast<int>(xa);
+            P.off_hbuf = static_cast<int>(xa + align_up(static_cast<long long>(MAX_RUNS) * sizeof(RunInfo), 128));
+            P.off_hflag = static_cast<int>(P.off_hbuf + align_up(static_cast<long long>(NWARPS_MAX) * T * 16 * 4, 128));
+            P.off_bar = static_cast<int>(xa + tables);
+            P.off_ring = static_cast<int>(xa + tables + bars);
+            pl.smem = static_cast<size_t>(xa + tables + bars + rings);
+            break;
         }
-        if (P.ring_depth) break;
     }
     if (P.ring_depth == 0) return QGEMV_ERR_UNSUPPORTED;
     if (items >= (1ll << 31)) return QGEMV_ERR_UNSUPPORTED;

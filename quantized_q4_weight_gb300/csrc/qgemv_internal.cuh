@@ -61,6 +61,9 @@ struct Params {
     int ring_depth;         // stages per warp
     int kmax, nbmax;        // largest K / blocks per row over the groups
     int off_d, off_cd, off_bar, off_ring;  // dynamic shared-memory layout
+    int off_runs, off_hbuf, off_hflag;     //   (balanced-mode tables)
+    int xq_area;            // bytes at offset 0 for activations
+    int balanced_ok;        // every group unsplit: CTAs may balance by stages
     const int *ids;         // gather: slot -> expert id (nullptr: slot index)
     int n_experts;
     long long total_bytes, total_items;
@@ -202,32 +205,37 @@ __device__ __forceinline__ void mbar_drain(uint64_t *bar, unsigned parity)
 
 // ------------------------------------------------------------- block arithmetic
 
+__device__ __forceinline__ int roundup16_dev(int v) { return (v + 15) & ~15; }
+
 // fp16 bits -> fp32 (exact).
 __device__ __forceinline__ float h2f(unsigned bits16)
 {
     return __half2float(__ushort_as_half(static_cast<unsigned short>(bits16 & 0xFFFFu)));
 }
 
-// MAGIC_I + isum for one weight block and one activation block, where
-// c = MAGIC_I - 8 * sum(q) (the folded offset).  n = 4 words of nibble
-// bytes (byte k: element k low nibble, element k+16 high nibble);
-// qa = activation elements 0..15, qb = elements 16..31.
-__device__ __forceinline__ int block_dot_magic(const uint4 &n, const uint4 &qa, const uint4 &qb, int c)
+// MAGIC_I + 16 * isum for one weight block and one activation block, where
+// c16 = MAGIC_I - 128 * sum(q) (the folded -8 offset, times 16).  n = 4 words
+// of nibble bytes (byte k: element k in the low nibble, element k+16 in the
+// high nibble); qa = activation elements 0..15, qb = elements 16..31.  The
+// low nibbles are masked in place; the high nibbles are masked without a
+// shift, so each byte holds 16 * n and that chain sums 16x; the two dp4a
+// chains meet in one shift-add.  |16 * isum| <= 520192 < 2^22.
+__device__ __forceinline__ int block_dot16_magic(const uint4 &n, const uint4 &qa, const uint4 &qb, int c16)
 {
-    int s = c;
-    s = dp4a_us(n.x & 0x0F0F0F0Fu, (int)qa.x, s);
-    s = dp4a_us(n.y & 0x0F0F0F0Fu, (int)qa.y, s);
-    s = dp4a_us(n.z & 0x0F0F0F0Fu, (int)qa.z, s);
-    s = dp4a_us(n.w & 0x0F0F0F0Fu, (int)qa.w, s);
-    s = dp4a_us((n.x >> 4) & 0x0F0F0F0Fu, (int)qb.x, s);
-    s = dp4a_us((n.y >> 4) & 0x0F0F0F0Fu, (int)qb.y, s);
-    s = dp4a_us((n.z >> 4) & 0x0F0F0F0Fu, (int)qb.z, s);
-    s = dp4a_us((n.w >> 4) & 0x0F0F0F0Fu, (int)qb.w, s);
-    return s;
+    int lo = 0, hi = c16;
+    lo = dp4a_us(n.x & 0x0F0F0F0Fu, (int)qa.x, lo);
+    hi = dp4a_us(n.x & 0xF0F0F0F0u, (int)qb.x, hi);
+    lo = dp4a_us(n.y & 0x0F0F0F0Fu, (int)qa.y, lo);
+    hi = dp4a_us(n.y & 0xF0F0F0F0u, (int)qb.y, hi);
+    lo = dp4a_us(n.z & 0x0F0F0F0Fu, (int)qa.z, lo);
+    hi = dp4a_us(n.z & 0xF0F0F0F0u, (int)qb.z, hi);
+    lo = dp4a_us(n.w & 0x0F0F0F0Fu, (int)qa.w, lo);
+    hi = dp4a_us(n.w & 0xF0F0F0F0u, (int)qb.w, hi);
+    return (lo << 4) + hi;
 }
 
-// The folded-offset constant of one activation block: MAGIC_I - 8 * sum(q).
-__device__ __forceinline__ int block_fold_const(const uint4 &qa, const uint4 &qb)
+// The folded-offset constant of one activation block: MAGIC_I - 128 * sum(q).
+__device__ __forceinline__ int block_fold16_const(const uint4 &qa, const uint4 &qb)
 {
     const int ones = 0x01010101;
     int s = 0;
@@ -239,11 +247,11 @@ __device__ __forceinline__ int block_fold_const(const uint4 &qa, const uint4 &qb
     s = dp4a_ss((int)qb.y, ones, s);
     s = dp4a_ss((int)qb.z, ones, s);
     s = dp4a_ss((int)qb.w, ones, s);
-    return MAGIC_I - 8 * s;
+    return MAGIC_I - 128 * s;
 }
 
-// (MAGIC_I + isum) read as a float is 12582912 + isum exactly (|isum| < 2^22);
-// subtracting 12582912 gives (float)isum exactly.
+// (MAGIC_I + v) read as a float is 12582912 + v exactly for |v| < 2^22;
+// subtracting 12582912 gives (float)v exactly.
 __device__ __forceinline__ float magic_to_float(int s) { return __fsub_rn(__int_as_float(s), MAGIC_F); }
 
 // Order-preserving 64-bit key for argmax: larger value first, then lower

@@ -330,3 +330,39 @@ def test_workspace_left_zeroed_and_reusable(orc):
     torch.cuda.synchronize()
     assert int(ws[:4].view(torch.int32)[0]) == 0           # argmax arrival counter
     assert idx.shape == (T,)
+
+
+@pytest.mark.parametrize("layout", [q.W_PACKED, q.W_GGML])
+@pytest.mark.parametrize("T", [1, 3, 8])
+def test_seq_balanced_mode_bit_identical(orc, layout, T):
+    """Lists with more than 2048 slabs run unsplit, with CTAs balanced by
+    16-block stages (slabs cut between warps); the bits must equal the single
+    calls (which split K) and stay within the bound of the oracle."""
+    shapes = [(2048, 1536), (1000, 2080), (1536, 8960), (17, 544), (301, 1024), (64, 11008), (8960, 1536)] * 3
+    entries, refs = [], []
+    cache = {}
+    for i, (N, K) in enumerate(shapes):
+        if (N, K) not in cache:
+            Wg, W = weights(300 + N + K, N, K, layout)
+            x, xd, xq = quantized(400 + N + K + T, T, K)
+            yref = q.gemv(W, layout, xq, N, K, T, ws_for(N, K, T)).cpu()
+            cache[(N, K)] = (Wg, W, x, xq, yref)
+        Wg, W, x, xq, yref = cache[(N, K)]
+        y = torch.full((T, N), float("nan"), dtype=torch.float32, device=DEV)
+        entries.append((W, xq, y, N, K))
+        refs.append(((N, K), yref))
+    items = q.seq_items(entries)
+    ws = q.new_workspace(q.seq_workspace_bytes(items, T))
+    for rep in range(2):
+        for e in entries:
+            e[2].fill_(float("nan"))
+        q.gemv_seq(items, layout, T, ws)
+        torch.cuda.synchronize()
+        assert q.device_status() == 0
+        for (W, xq, y, N, K), (key, yref) in zip(entries, refs):
+            assert torch.equal(y.cpu().view(torch.int32), yref.view(torch.int32)), (key, rep)
+    rng = np.random.default_rng(T)
+    for (N, K), (Wg, W, x, xq, yref) in cache.items():
+        rows = np.unique(rng.integers(0, N, 12))
+        y64, S = orc.gemv_rows(Wg, N, K, orc.quantize(x), T, rows)
+        check_close(yref.numpy()[:, rows], y64, S, f"balanced N={N} K={K}")
