@@ -495,7 +495,7 @@ __global__ void __launch_bounds__(max_warps_for(T) * 32, 1) qgemv_stream_kernel(
     __shared__ int s_last;
     __shared__ int s_nruns;  // > 0: balanced mode with this many runs
     __shared__ int s_stages;
-    __shared__ unsigned long long s_best[NWARPS_MAX * T];
+    __shared__ unsigned long long s_best[max_warps_for(T) * T];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nw = P.nwarps, nthreads = nw * 32;

@@ -225,9 +225,9 @@ cudaError_t dispatch_T(const Params<MAXG> &P, int T, int grid, size_t smem, cuda
     }
 }
 
-// The dynamic shared-memory budget of one CTA (static arrays of the kernel
-// take well under 1 KB).
-inline int smem_budget(const DevInfo &d) { return d.smem_optin - 1024; }
+// The dynamic shared-memory budget of one CTA (the kernel's static arrays
+// take at most 600 bytes).
+inline int smem_budget(const DevInfo &d) { return d.smem_optin - 2048; }
 
 // Shared argument checks of the single-matrix GEMV calls.
 qgemv_status check_single(const void *W, qgemv_wlayout layout, const void *xin, long long xin_bytes,
