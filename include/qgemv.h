@@ -197,6 +197,26 @@ size_t qgemv_seq_workspace_bytes(const qgemv_seq_item *items, int n, int T);
 qgemv_status qgemv_q4_0_seq(const qgemv_seq_item *items, int n, qgemv_wlayout layout, int T,
                             void *ws, size_t ws_bytes, qgemv_stream_t stream);
 
+/* One GEMV of a sequence with fp32 input x[T][K]. */
+typedef struct {
+    const void *W;
+    const float *x;
+    float *y;
+    int64_t N;
+    int64_t K;
+} qgemv_seq_f32_item;
+
+/* Workspace bytes for qgemv_q4_0_seq_f32 on this list (0 if invalid). */
+size_t qgemv_seq_f32_workspace_bytes(const qgemv_seq_f32_item *items, int n, int T);
+
+/* qgemv_q4_0_seq with fp32 inputs: every item's activations are quantised
+ * (Q8_0, as qgemv_quantize_q8_0) into the workspace by one launch, and the
+ * GEMV launch follows with programmatic dependent launch, so its weight
+ * stream starts while the quantiser runs (minfer README M15: the activation
+ * is quantised once, then the weights stream). */
+qgemv_status qgemv_q4_0_seq_f32(const qgemv_seq_f32_item *items, int n, qgemv_wlayout layout, int T,
+                                void *ws, size_t ws_bytes, qgemv_stream_t stream);
+
 /* One matrix of a routed-expert (MoE) gather: expert e's copy of this
  * matrix starts at W + e * expert_stride (bytes); slot s reads activations
  * xq + s * xq_stride (bytes; 0 = shared by all slots) and writes

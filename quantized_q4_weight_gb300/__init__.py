@@ -36,6 +36,11 @@ class SeqItem(ctypes.Structure):
                 ("N", ctypes.c_int64), ("K", ctypes.c_int64)]
 
 
+class SeqF32Item(ctypes.Structure):
+    _fields_ = [("W", ctypes.c_void_p), ("x", ctypes.c_void_p), ("y", ctypes.c_void_p),
+                ("N", ctypes.c_int64), ("K", ctypes.c_int64)]
+
+
 class GatherMatrix(ctypes.Structure):
     _fields_ = [("W", ctypes.c_void_p), ("expert_stride", ctypes.c_int64), ("xq", ctypes.c_void_p),
                 ("xq_stride", ctypes.c_int64), ("y", ctypes.c_void_p), ("y_stride", ctypes.c_int64),
@@ -60,6 +65,8 @@ _SIGS = {
     "qgemv_q4_0_argmax_noalloc": ([_VP, _I32, _VP, _VP, _VP, _I64, _I64, _I32, _VP], _I32),
     "qgemv_seq_workspace_bytes": ([ctypes.POINTER(SeqItem), _I32, _I32], _SZ),
     "qgemv_q4_0_seq": ([ctypes.POINTER(SeqItem), _I32, _I32, _I32, _VP, _SZ, _VP], _I32),
+    "qgemv_seq_f32_workspace_bytes": ([ctypes.POINTER(SeqF32Item), _I32, _I32], _SZ),
+    "qgemv_q4_0_seq_f32": ([ctypes.POINTER(SeqF32Item), _I32, _I32, _I32, _VP, _SZ, _VP], _I32),
     "qgemv_gather_workspace_bytes": ([ctypes.POINTER(GatherMatrix), _I32, _I32, _I32], _SZ),
     "qgemv_q4_0_gather": ([ctypes.POINTER(GatherMatrix), _I32, _VP, _I32, _I32, _I32, _I32, _VP, _SZ, _VP], _I32),
     "qgemv_debug_block_isums": ([_VP, _I32, _VP, _VP, _I64, _I64, _I32, _VP], _I32),
@@ -182,6 +189,24 @@ def seq_workspace_bytes(items: ctypes.Array, T: int) -> int:
 def gemv_seq(items: ctypes.Array, layout: int, T: int, ws, stream=None):
     _check(lib().qgemv_q4_0_seq(items, len(items), layout, T, _ptr(ws), ws.numel(), _stream(stream)),
            "qgemv_q4_0_seq")
+
+
+def seq_f32_items(entries) -> ctypes.Array:
+    """entries: iterable of (W, x, y, N, K) with CUDA tensors (x fp32 [T, K])."""
+    entries = list(entries)
+    arr = (SeqF32Item * len(entries))()
+    for i, (W, x, y, N, K) in enumerate(entries):
+        arr[i] = SeqF32Item(W.data_ptr(), x.data_ptr(), y.data_ptr(), N, K)
+    return arr
+
+
+def seq_f32_workspace_bytes(items: ctypes.Array, T: int) -> int:
+    return int(lib().qgemv_seq_f32_workspace_bytes(items, len(items), T))
+
+
+def gemv_seq_f32(items: ctypes.Array, layout: int, T: int, ws, stream=None):
+    _check(lib().qgemv_q4_0_seq_f32(items, len(items), layout, T, _ptr(ws), ws.numel(), _stream(stream)),
+           "qgemv_q4_0_seq_f32")
 
 
 def gather_mats(entries) -> ctypes.Array:

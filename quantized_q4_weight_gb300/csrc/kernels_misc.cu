@@ -11,36 +11,42 @@ namespace qg {
 // amax by a shuffle tree of fmaxf (exact), d = amax / 127 (IEEE division),
 // 1/d from the fp32 d (0 when d = 0), q = roundf(x * (1/d)) -- roundf rounds
 // halfway cases away from zero -- and d stored as fp16, round to nearest even.
+// One warp quantises block `rem` (row r = rem / nb, block b = rem % nb) of
+// a planar buffer `dst` of R rows of K.
+__device__ __forceinline__ void quantize_block_warp(const float *__restrict__ x, uint8_t *__restrict__ dst, int R,
+                                                    int K, long long rem, long long xq_bytes, int lane)
+{
+    const int nb = K / QK;
+    const int r = static_cast<int>(rem / nb), b = static_cast<int>(rem - static_cast<long long>(r) * nb);
+    const float v = __ldg(x + static_cast<long long>(r) * K + b * QK + lane);
+    float amax = fabsf(v);
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+    const float d = __fdiv_rn(amax, 127.0f);
+    const float id = (d != 0.0f) ? __fdiv_rn(1.0f, d) : 0.0f;
+    const float q = roundf(__fmul_rn(v, id));
+    dst[static_cast<long long>(r) * K + b * QK + lane] = static_cast<uint8_t>(static_cast<int8_t>(static_cast<int>(q)));
+    if (lane == 0) {
+        const unsigned short dh = __half_as_ushort(__float2half_rn(d));
+        reinterpret_cast<unsigned short *>(dst + static_cast<long long>(R) * K)[rem] = dh;
+    }
+    if (rem == 0) {  // zero the padding after the scales
+        const long long used = static_cast<long long>(R) * K + 2ll * R * nb;
+        if (used + lane < xq_bytes) dst[used + lane] = 0;
+    }
+}
+
 __global__ void __launch_bounds__(256) quantize_q8_0_kernel(const float *__restrict__ x, uint8_t *__restrict__ xq,
                                                             int R, int K, long long nblocks, long long xq_bytes)
 {
     pdl_launch_dependents();
     pdl_wait();
-    const int nb = K / QK;
     const int lane = threadIdx.x & 31;
-    const long long per_batch = static_cast<long long>(R) * nb;
+    const long long per_batch = static_cast<long long>(R) * (K / QK);
     for (long long gb = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; gb < nblocks;
          gb += (static_cast<long long>(gridDim.x) * blockDim.x) >> 5) {
         const long long bi = gb / per_batch;
-        const long long rem = gb - bi * per_batch;
-        const int r = static_cast<int>(rem / nb), b = static_cast<int>(rem - static_cast<long long>(r) * nb);
-        const float v = __ldg(x + (bi * R + r) * K + b * QK + lane);
-        float amax = fabsf(v);
-#pragma unroll
-        for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
-        const float d = __fdiv_rn(amax, 127.0f);
-        const float id = (d != 0.0f) ? __fdiv_rn(1.0f, d) : 0.0f;
-        const float q = roundf(__fmul_rn(v, id));
-        uint8_t *dst = xq + bi * xq_bytes;
-        dst[static_cast<long long>(r) * K + b * QK + lane] = static_cast<uint8_t>(static_cast<int8_t>(static_cast<int>(q)));
-        if (lane == 0) {
-            const unsigned short dh = __half_as_ushort(__float2half_rn(d));
-            reinterpret_cast<unsigned short *>(dst + static_cast<long long>(R) * K)[rem] = dh;
-        }
-        if (rem == 0) {  // zero the padding after the scales
-            const long long used = static_cast<long long>(R) * K + 2 * per_batch;
-            if (used + lane < xq_bytes) dst[used + lane] = 0;
-        }
+        quantize_block_warp(x + bi * per_batch * QK, xq + bi * xq_bytes, R, K, gb - bi * per_batch, xq_bytes, lane);
     }
 }
 
@@ -52,6 +58,35 @@ cudaError_t launch_quantize(const float *x, void *xq, int R, long long K, int ba
     if (grid > 65535) grid = 65535;
     quantize_q8_0_kernel<<<static_cast<unsigned>(grid), 256, 0, st>>>(x, static_cast<uint8_t *>(xq), R,
                                                                     static_cast<int>(K), nblocks, xqb);
+    return cudaGetLastError();
+}
+
+// A list of activation vectors (one per GEMV of a sequence) in one launch:
+// warp -> global block -> item by binary search over the block prefixes.
+__global__ void __launch_bounds__(256) quantize_list_kernel(const __grid_constant__ QuantList L)
+{
+    pdl_launch_dependents();
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    for (long long gb = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; gb < L.total_blocks;
+         gb += (static_cast<long long>(gridDim.x) * blockDim.x) >> 5) {
+        int lo = 0, hi = L.n - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (L.it[mid].block0 <= gb) lo = mid;
+            else hi = mid - 1;
+        }
+        const QuantItem &it = L.it[lo];
+        quantize_block_warp(it.x, it.xq, it.R, it.K, gb - it.block0, it.xq_bytes, lane);
+    }
+}
+
+cudaError_t launch_quantize_list(const QuantList &L, cudaStream_t st)
+{
+    long long grid = (L.total_blocks + 7) / 8;
+    if (grid > 65535) grid = 65535;
+    if (grid < 1) grid = 1;
+    quantize_list_kernel<<<static_cast<unsigned>(grid), 256, 0, st>>>(L);
     return cudaGetLastError();
 }
 

@@ -424,8 +424,8 @@ size_t qgemv_seq_workspace_bytes(const qgemv_seq_item *items, int n, int T)
     return static_cast<size_t>(total);
 }
 
-qgemv_status qgemv_q4_0_seq(const qgemv_seq_item *items, int n, qgemv_wlayout layout, int T, void *ws,
-                            size_t ws_bytes, qgemv_stream_t stream)
+static qgemv_status check_seq(const qgemv_seq_item *items, int n, qgemv_wlayout layout, int T, void *ws,
+                              size_t ws_bytes)
 {
     if (!items || n < 1 || T < 1 || T > 8) return QGEMV_ERR_INVALID_ARG;
     if (layout != QGEMV_W_GGML && layout != QGEMV_W_PACKED) return QGEMV_ERR_INVALID_ARG;
@@ -446,13 +446,23 @@ qgemv_status qgemv_q4_0_seq(const qgemv_seq_item *items, int n, qgemv_wlayout la
             if (k != i && overlap(ry, range(b.y, 4ll * T * b.N))) return QGEMV_ERR_INVALID_ARG;
         }
     }
+    return QGEMV_OK;
+}
+
+// The launches of a sequence (checked): one persistent GEMV launch per
+// MAXG_SEQ items; with fp32 inputs, each preceded by one quantiser launch
+// that writes the activations into `xq_ws` (the GEMV is then chained with
+// programmatic dependent launch).
+static qgemv_status launch_seq(const qgemv_seq_item *items, const float *const *xs, int n, qgemv_wlayout layout,
+                               int T, void *ws, size_t ws_bytes, cudaStream_t st)
+{
     DevInfo dev;
     qgemv_status s = device_info(dev);
     if (s != QGEMV_OK) return s;
-    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     const int grid = dev.sms < MAX_GRID ? dev.sms : MAX_GRID;
     std::vector<GroupSpec> gs(MAXG_SEQ);
     std::unique_ptr<Plan<MAXG_SEQ>> pl(new Plan<MAXG_SEQ>());
+    std::unique_ptr<QuantList> ql(xs ? new QuantList() : nullptr);
     for (int c0 = 0; c0 < n; c0 += MAXG_SEQ) {
         const int cn = (n - c0) < MAXG_SEQ ? (n - c0) : MAXG_SEQ;
         for (int i = 0; i < cn; ++i) {
@@ -464,9 +474,85 @@ qgemv_status qgemv_q4_0_seq(const qgemv_seq_item *items, int n, qgemv_wlayout la
         if (s != QGEMV_OK) return s;
         if (static_cast<long long>(ws_bytes) < pl->ws_bytes) return QGEMV_ERR_WORKSPACE;
         pl->P.status = dev.status;
-        if (dispatch_T<MAXG_SEQ, false>(pl->P, T, grid, pl->smem, st, false) != cudaSuccess) return QGEMV_ERR_CUDA;
+        if (xs) {
+            ql->n = cn;
+            long long blocks = 0;
+            for (int i = 0; i < cn; ++i) {
+                const qgemv_seq_item &it = items[c0 + i];
+                ql->it[i] = QuantItem{xs[c0 + i], static_cast<uint8_t *>(const_cast<void *>(it.xq)), T,
+                                      static_cast<int>(it.K), xq_bytes_host(T, it.K), blocks};
+                blocks += static_cast<long long>(T) * (it.K / QK);
+            }
+            ql->total_blocks = blocks;
+            if (launch_quantize_list(*ql, st) != cudaSuccess) return QGEMV_ERR_CUDA;
+        }
+        if (dispatch_T<MAXG_SEQ, false>(pl->P, T, grid, pl->smem, st, xs != nullptr) != cudaSuccess)
+            return QGEMV_ERR_CUDA;
     }
     return QGEMV_OK;
+}
+
+qgemv_status qgemv_q4_0_seq(const qgemv_seq_item *items, int n, qgemv_wlayout layout, int T, void *ws,
+                            size_t ws_bytes, qgemv_stream_t stream)
+{
+    const qgemv_status s = check_seq(items, n, layout, T, ws, ws_bytes);
+    if (s != QGEMV_OK) return s;
+    return launch_seq(items, nullptr, n, layout, T, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+}
+
+// Workspace of the fp32-input sequence: the sequence's own, then each item's
+// quantised activations (256-byte aligned).
+static long long seq_f32_layout(const qgemv_seq_f32_item *items, int n, int T, std::vector<long long> *xq_off)
+{
+    std::vector<qgemv_seq_item> tmp(n);
+    for (int i = 0; i < n; ++i) {
+        if (!shape_ok(items[i].N, items[i].K)) return 0;
+        tmp[i] = qgemv_seq_item{items[i].W, nullptr, items[i].y, items[i].N, items[i].K};
+    }
+    long long off = static_cast<long long>(qgemv_seq_workspace_bytes(tmp.data(), n, T));
+    if (off == 0) return 0;
+    off = align_up(off, 256);
+    for (int i = 0; i < n; ++i) {
+        if (xq_off) xq_off->push_back(off);
+        off = align_up(off + xq_bytes_host(T, items[i].K), 256);
+    }
+    return off;
+}
+
+size_t qgemv_seq_f32_workspace_bytes(const qgemv_seq_f32_item *items, int n, int T)
+{
+    if (!items || n < 1 || T < 1 || T > 8) return 0;
+    return static_cast<size_t>(seq_f32_layout(items, n, T, nullptr));
+}
+
+qgemv_status qgemv_q4_0_seq_f32(const qgemv_seq_f32_item *items, int n, qgemv_wlayout layout, int T, void *ws,
+                                size_t ws_bytes, qgemv_stream_t stream)
+{
+    if (!items || n < 1 || T < 1 || T > 8) return QGEMV_ERR_INVALID_ARG;
+    if (!ws) return QGEMV_ERR_WORKSPACE;
+    std::vector<long long> xq_off;
+    const long long need = seq_f32_layout(items, n, T, &xq_off);
+    if (need == 0) return QGEMV_ERR_INVALID_ARG;
+    if (static_cast<long long>(ws_bytes) < need) return QGEMV_ERR_WORKSPACE;
+    std::vector<qgemv_seq_item> sq(n);
+    std::vector<const float *> xs(n);
+    const Range rw = range(ws, need);
+    for (int i = 0; i < n; ++i) {
+        const qgemv_seq_f32_item &a = items[i];
+        if (!a.x) return QGEMV_ERR_INVALID_ARG;
+        if (!aligned(a.x, 4)) return QGEMV_ERR_MISALIGNED;
+        if (overlap(range(a.x, 4ll * T * a.K), rw)) return QGEMV_ERR_INVALID_ARG;
+        for (int k = 0; k < n; ++k)
+            if (a.y && overlap(range(a.y, 4ll * T * a.N), range(items[k].x, 4ll * T * items[k].K)))
+                return QGEMV_ERR_INVALID_ARG;
+        sq[i] = qgemv_seq_item{a.W, static_cast<uint8_t *>(ws) + xq_off[i], a.y, a.N, a.K};
+        xs[i] = a.x;
+    }
+    // the sequence's own workspace ends where the activations begin
+    qgemv_status s = check_seq(sq.data(), n, layout, T, ws, static_cast<size_t>(xq_off[0]));
+    if (s != QGEMV_OK) return s;
+    return launch_seq(sq.data(), xs.data(), n, layout, T, ws, static_cast<size_t>(xq_off[0]),
+                      reinterpret_cast<cudaStream_t>(stream));
 }
 
 static qgemv_status gather_specs(const qgemv_gather_matrix *mats, int n_mats, int n_ids, int T, GroupSpec *gs)

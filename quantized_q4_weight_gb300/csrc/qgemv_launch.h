@@ -15,6 +15,20 @@ inline long long roundup16(long long v) { return (v + 15) & ~15ll; }
 inline long long xq_bytes_host(long long R, long long K) { return R * K + roundup16(2 * R * (K / QK)); }
 
 cudaError_t launch_quantize(const float *x, void *xq, int R, long long K, int batch, cudaStream_t st);
+
+struct QuantItem {
+    const float *x;      // fp32 [R][K]
+    uint8_t *xq;         // planar Q8_0 of R rows
+    int R, K;
+    long long xq_bytes;
+    long long block0;    // first global block of this item
+};
+struct QuantList {
+    int n;
+    long long total_blocks;
+    QuantItem it[MAXG_SEQ];
+};
+cudaError_t launch_quantize_list(const QuantList &L, cudaStream_t st);
 cudaError_t launch_pack(const void *src, void *dst, long long N, long long K, bool to_packed, cudaStream_t st);
 cudaError_t launch_isums(const void *W, bool packed, const void *xq, int32_t *isums, long long N, long long K, int T,
                          cudaStream_t st);

@@ -366,3 +366,26 @@ def test_seq_balanced_mode_bit_identical(orc, layout, T):
         rows = np.unique(rng.integers(0, N, 12))
         y64, S = orc.gemv_rows(Wg, N, K, orc.quantize(x), T, rows)
         check_close(yref.numpy()[:, rows], y64, S, f"balanced N={N} K={K}")
+
+
+def test_seq_f32_equals_quantize_then_seq(orc):
+    shapes = [(2048, 1536), (17, 544), (1536, 8960), (100, 2080)] * 40
+    T = 2
+    entries_f, entries_q, ys_f, ys_q = [], [], [], []
+    for i, (N, K) in enumerate(shapes):
+        Wg, Wp = weights(900 + N + K, N, K, q.W_PACKED) if i < 4 else (None, entries_f[i % 4][0])
+        x = torch.from_numpy(synth.activations(950 + i, T, K)).to(DEV)
+        yf = torch.empty((T, N), dtype=torch.float32, device=DEV)
+        yq = torch.empty((T, N), dtype=torch.float32, device=DEV)
+        entries_f.append((Wp, x, yf, N, K))
+        entries_q.append((Wp, q.quantize_q8_0(x, T, K), yq, N, K))
+        ys_f.append(yf)
+        ys_q.append(yq)
+    itf = q.seq_f32_items(entries_f)
+    itq = q.seq_items(entries_q)
+    q.gemv_seq_f32(itf, q.W_PACKED, T, q.new_workspace(q.seq_f32_workspace_bytes(itf, T)))
+    q.gemv_seq(itq, q.W_PACKED, T, q.new_workspace(q.seq_workspace_bytes(itq, T)))
+    torch.cuda.synchronize()
+    assert q.device_status() == 0
+    for a, b in zip(ys_f, ys_q):
+        assert torch.equal(a.cpu().view(torch.int32), b.cpu().view(torch.int32))

@@ -30,31 +30,32 @@ def host(t: torch.Tensor) -> np.ndarray:
                                     ("qwen2.5-3b_verify", 1)])
 def test_layer_sets_sampled(orc, name, T):
     wl = bench.build_workload(name, DEV, T=T, keep_host=True)
-    wl.quantize()
-    wl.gemv()
+    wl.step()                                   # fp32 inputs, one quantiser + one GEMV launch
     torch.cuda.synchronize()
     assert q.device_status() == 0
+    y_step = [host(y).copy() for y in wl.y]
+    wl.kernel()                                 # pre-quantised inputs, the GEMV launch alone
+    torch.cuda.synchronize()
     rng = np.random.default_rng(5)
-    xs = {K: host(wl.x[K]) for K in wl.kidx}
     for i, (nm, N, K) in enumerate(wl.mats):
-        slot = wl.kidx[K].index(i)
-        xq = orc.quantize(xs[K][slot])
+        assert np.array_equal(y_step[i].view(np.int32), host(wl.y[i]).view(np.int32)), nm
+        x = host(wl.x[i])
+        xq = orc.quantize(x)
         if i < 5:   # activation bytes of the first layer, bit-exact
-            xqb = q.xq_bytes(T, K)
-            got = host(wl.xq[K][slot * xqb:(slot + 1) * xqb])
+            got = host(wl.xq[i])
             assert np.array_equal(got[:T * K].reshape(T, K // 32, 32), xq[:, :, 2:])
+            assert np.array_equal(got[T * K:T * K + 2 * T * (K // 32)].reshape(T, K // 32, 2), xq[:, :, :2])
         rows = np.unique(np.concatenate([[0, N - 1], rng.integers(0, N, 6)]))
         y64, S = orc.gemv_rows(wl.host[i], N, K, xq, T, rows)
-        check_close(host(wl.y[i])[:, rows], y64, S, f"{name} {nm}")
+        check_close(y_step[i][:, rows], y64, S, f"{name} {nm}")
 
 
 def test_lm_head_argmax_full(orc):
     wl = bench.build_workload("lm_head_argmax", DEV, keep_host=True)
     y = torch.empty((wl.T, wl.N), dtype=torch.float32, device=DEV)
     for c in range(len(wl.W)):
-        wl.quantize()
         wl.copy = c
-        wl.gemv()
+        wl.step()
         idx = host(wl.idx).copy()
         q.gemv(wl.W[c], q.W_PACKED, wl.xqb, wl.N, wl.K, wl.T, wl.ws, y=y)
         yh = host(y)
@@ -70,7 +71,7 @@ def test_lm_head_argmax_full(orc):
 
 def test_single_full(orc):
     wl = bench.build_workload("single_1536", DEV, keep_host=True)
-    wl.gemv()
+    wl.step()
     torch.cuda.synchronize()
     xq = orc.quantize(host(wl.x))
     y64, S = orc.gemv(wl.host[0], wl.N, wl.K, xq, wl.T)
@@ -79,9 +80,8 @@ def test_single_full(orc):
 
 def test_moe_full(orc):
     wl = bench.build_workload("moe_top8_shared", DEV, keep_host=True)
-    wl.quantize()
     wl.tok = 0
-    wl.gemv()            # token 0, expert set 0
+    wl.step()            # token 0, expert set 0
     torch.cuda.synchronize()
     assert q.device_status() == 0
     ids = host(wl.ids[0])
