@@ -251,6 +251,17 @@ qgemv_status qgemv_debug_block_isums(const void *W, qgemv_wlayout layout, const 
                                      int32_t *isums, int64_t N, int64_t K, int T,
                                      qgemv_stream_t stream);
 
+/* Measurement hook: stream `bytes` of device memory from `src` once, with
+ * no arithmetic, to measure the HBM read bandwidth an access pattern
+ * reaches (minfer README M15: bench/roofline.cu).  method 0: one CTA per SM
+ * of `warps` warps, each keeping `depth` 1-D bulk copies of `stage_bytes` in
+ * flight into shared memory (the GEMV kernel's pattern); method 1: 128-bit
+ * global loads, `warps` warps per CTA, two CTAs per SM, 4 (depth <= 4) or 8
+ * loads in flight per thread.  `sink` (8 bytes, device) is written only in
+ * a case that never occurs, so the loads stay live. */
+qgemv_status qgemv_debug_stream_read(const void *src, size_t bytes, int method, int warps, int depth,
+                                     int stage_bytes, unsigned long long *sink, qgemv_stream_t stream);
+
 /* Read and clear the current device's status word: QGEMV_OK, or the first
  * asynchronous error a kernel recorded (QGEMV_ERR_TIMEOUT, QGEMV_ERR_BAD_ID)
  * into *code_out.  Synchronises with the device (a query, not part of the

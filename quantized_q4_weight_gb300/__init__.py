@@ -70,6 +70,7 @@ _SIGS = {
     "qgemv_gather_workspace_bytes": ([ctypes.POINTER(GatherMatrix), _I32, _I32, _I32], _SZ),
     "qgemv_q4_0_gather": ([ctypes.POINTER(GatherMatrix), _I32, _VP, _I32, _I32, _I32, _I32, _VP, _SZ, _VP], _I32),
     "qgemv_debug_block_isums": ([_VP, _I32, _VP, _VP, _I64, _I64, _I32, _VP], _I32),
+    "qgemv_debug_stream_read": ([_VP, _SZ, _I32, _I32, _I32, _I32, _VP, _VP], _I32),
     "qgemv_device_status": ([ctypes.POINTER(ctypes.c_int)], _I32),
 }
 
@@ -232,6 +233,12 @@ def block_isums(W, layout: int, xq, N: int, K: int, T: int, stream=None) -> torc
     _check(lib().qgemv_debug_block_isums(_ptr(W), layout, _ptr(xq), _ptr(out), N, K, T, _stream(stream)),
            "qgemv_debug_block_isums")
     return out
+
+
+def stream_read(src, method: int, warps: int, depth: int, stage_bytes: int, sink, stream=None):
+    """Measurement hook: stream all of `src` once (see qgemv_debug_stream_read)."""
+    _check(lib().qgemv_debug_stream_read(_ptr(src), src.numel() * src.element_size(), method, warps, depth,
+                                         stage_bytes, _ptr(sink), _stream(stream)), "qgemv_debug_stream_read")
 
 
 def device_status() -> int:

@@ -640,6 +640,24 @@ qgemv_status qgemv_debug_block_isums(const void *W, qgemv_wlayout layout, const 
                : QGEMV_ERR_CUDA;
 }
 
+qgemv_status qgemv_debug_stream_read(const void *src, size_t bytes, int method, int warps, int depth,
+                                     int stage_bytes, unsigned long long *sink, qgemv_stream_t stream)
+{
+    if (!src || !sink || bytes < 16 || (method != 0 && method != 1) || warps < 1 || warps > 32 || depth < 1)
+        return QGEMV_ERR_INVALID_ARG;
+    if (method == 0 && (stage_bytes < 16 || stage_bytes % 16 != 0 || depth > 16 ||
+                        static_cast<long long>(warps) * depth * stage_bytes > 200 * 1024))
+        return QGEMV_ERR_INVALID_ARG;
+    if (!aligned(src, 16) || !aligned(sink, 8)) return QGEMV_ERR_MISALIGNED;
+    DevInfo dev;
+    qgemv_status s = device_info(dev);
+    if (s != QGEMV_OK) return s;
+    return launch_stream_bench(src, static_cast<long long>(bytes), method, warps, depth, stage_bytes, sink, dev.status,
+                               dev.sms, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? QGEMV_OK
+               : QGEMV_ERR_CUDA;
+}
+
 qgemv_status qgemv_device_status(int *code_out)
 {
     if (!code_out) return QGEMV_ERR_INVALID_ARG;

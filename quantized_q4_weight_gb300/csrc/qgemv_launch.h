@@ -29,6 +29,8 @@ struct QuantList {
     QuantItem it[MAXG_SEQ];
 };
 cudaError_t launch_quantize_list(const QuantList &L, cudaStream_t st);
+cudaError_t launch_stream_bench(const void *src, long long bytes, int method, int warps, int depth, int stage_bytes,
+                                unsigned long long *out, unsigned *status, int sms, cudaStream_t st);
 cudaError_t launch_pack(const void *src, void *dst, long long N, long long K, bool to_packed, cudaStream_t st);
 cudaError_t launch_isums(const void *W, bool packed, const void *xq, int32_t *isums, long long N, long long K, int T,
                          cudaStream_t st);
