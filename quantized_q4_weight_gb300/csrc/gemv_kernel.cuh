@@ -330,88 +330,118 @@ struct RunInfo {
     int bad;            // gather slot with an expert id out of range
 };
 
-// Walks CTA-local stages over up to three intervals, in order, keeping
-// (run, item-in-run, segment) incrementally.  With tma_only it skips stages
-// that are not copied by TMA (GGML rows, packed tails, bad slots).
-struct SpanWalker {
-    int ivb[3], ive[3];
-    int iv, k, r, ii, s;
+// Walks CTA-local stages over up to three intervals, in order, keeping the
+// position (run r, item ii of the run, segment s) and the current run's
+// fields in registers; the run table is read only when the run changes.
+struct Walker {
+    int k, kend, iv;             // current stage, end of the current interval, interval index
+    int b1, e1, b2, e2;          // intervals 1 and 2
+    int r, ii, s, item_end, run_end_k;
+    int nseg, nb, first_local, nslabs, bad;
+    const uint8_t *Wi;
     bool valid;
+
+    __device__ __forceinline__ void load_run(const RunInfo *runs)
+    {
+        const RunInfo &R = runs[r];
+        run_end_k = R.stage0 + R.nstages;
+        nseg = R.nseg;
+        nb = R.nb;
+        first_local = R.first_local;
+        nslabs = R.nslabs;
+        bad = R.bad;
+        Wi = R.Wi;
+    }
 
     __device__ __forceinline__ void locate(const RunInfo *runs)
     {
         while (k >= runs[r].stage0 + runs[r].nstages) ++r;
         while (k < runs[r].stage0) --r;
+        load_run(runs);
         const int ks = k - runs[r].stage0;
-        ii = ks / runs[r].nseg;
-        s = ks - ii * runs[r].nseg;
+        ii = ks / nseg;
+        s = ks - ii * nseg;
+        item_end = k - s + nseg;
     }
 
-    __device__ __forceinline__ bool stage_is_tma(const RunInfo *runs, bool ggml) const
+    __device__ __forceinline__ bool enter(const RunInfo *runs, int b, int e)
     {
-        const RunInfo &R = runs[r];
-        return !ggml && !R.bad && R.first_local + ii < R.nslabs;
+        k = b;
+        kend = e;
+        if (b >= e) return false;
+        locate(runs);
+        return true;
     }
 
-    __device__ __forceinline__ void enter_interval(const RunInfo *runs)
+    __device__ __forceinline__ void next_interval(const RunInfo *runs)
     {
-        while (iv < 3 && ivb[iv] >= ive[iv]) ++iv;
-        valid = iv < 3;
-        if (valid) {
-            k = ivb[iv];
-            locate(runs);
-        }
-    }
-
-    __device__ __forceinline__ void step(const RunInfo *runs)
-    {
-        ++k;
-        if (k >= ive[iv]) {
+        valid = false;
+        while (iv < 2) {
             ++iv;
-            enter_interval(runs);
-            return;
-        }
-        if (++s == runs[r].nseg) {
-            s = 0;
-            if (k >= runs[r].stage0 + runs[r].nstages) {
-                ++r;
-                ii = 0;
-            } else {
-                ++ii;
+            if (enter(runs, iv == 1 ? b1 : b2, iv == 1 ? e1 : e2)) {
+                valid = true;
+                return;
             }
         }
     }
 
-    __device__ __forceinline__ void init(const RunInfo *runs, const int (&b)[3], const int (&e)[3], bool tma_only,
-                                         bool ggml)
+    __device__ __forceinline__ void init(const RunInfo *runs, int b0, int e0, int b1_, int e1_, int b2_, int e2_)
     {
-        for (int i = 0; i < 3; ++i) {
-            ivb[i] = b[i];
-            ive[i] = e[i];
-        }
+        b1 = b1_;
+        e1 = e1_;
+        b2 = b2_;
+        e2 = e2_;
         iv = 0;
         r = 0;
-        enter_interval(runs);
-        if (tma_only)
-            while (valid && !stage_is_tma(runs, ggml)) step(runs);
+        valid = enter(runs, b0, e0);
+        if (!valid) next_interval(runs);
     }
 
-    __device__ __forceinline__ void advance_tma(const RunInfo *runs, bool ggml)
+    // Jump to the start of the next item (or the next interval).
+    __device__ __forceinline__ void next_item(const RunInfo *runs)
     {
-        do step(runs);
-        while (valid && !stage_is_tma(runs, ggml));
+        if (item_end >= kend) {
+            next_interval(runs);
+            return;
+        }
+        k = item_end;
+        s = 0;
+        if (k >= run_end_k) {
+            ++r;
+            load_run(runs);
+            ii = 0;
+        } else {
+            ++ii;
+        }
+        item_end = k + nseg;
     }
 
-    __device__ __forceinline__ const uint8_t *src(const RunInfo *runs) const
+    // One stage forward.
+    __device__ __forceinline__ void step(const RunInfo *runs)
     {
-        const RunInfo &R = runs[r];
-        return R.Wi + static_cast<long long>(R.first_local + ii) * SLAB_COL_BYTES * R.nb +
-               static_cast<long long>(s) * SEG_BYTES;
+        if (k + 1 == item_end || k + 1 >= kend) {
+            next_item(runs);
+            return;
+        }
+        ++k;
+        ++s;
     }
 
-    __device__ __forceinline__ unsigned bytes(const RunInfo *runs) const
+    __device__ __forceinline__ bool item_is_tma(bool ggml) const { return !ggml && !bad && first_local + ii < nslabs; }
+
+    __device__ __forceinline__ void skip_untransferred(const RunInfo *runs, bool ggml)
     {
-        return static_cast<unsigned>(SLAB_COL_BYTES * min(SEG_BLOCKS, runs[r].nb - SEG_BLOCKS * s));
+        while (valid && !item_is_tma(ggml)) next_item(runs);
+    }
+
+    __device__ __forceinline__ const uint8_t *src() const
+    {
+        return Wi + static_cast<long long>(first_local + ii) * SLAB_COL_BYTES * nb + static_cast<long long>(s) * SEG_BYTES;
+    }
+
+    __device__ __forceinline__ unsigned bytes() const
+    {
+        return static_cast<unsigned>(SLAB_COL_BYTES * min(SEG_BLOCKS, nb - SEG_BLOCKS * s));
     }
 };
 
@@ -611,15 +641,16 @@ __global__ void __launch_bounds__(max_warps_for(T) * 32, 1) qgemv_stream_kernel(
                 tail_e = st + runs[r].nseg;  // [a, tail_e) finishes an item begun by warp - 1
             }
         }
-        const int ivb[3] = {head_b, tail_e, a};
-        const int ive[3] = {b, head_b, tail_e};
+        const bool ggml = P.ggml != 0;
 
         // weights first (they do not depend on the preceding kernel)
-        SpanWalker cur;
-        cur.init(runs, ivb, ive, true, P.ggml != 0);
+        Walker cur;
+        cur.init(runs, head_b, b, tail_e, head_b, a, tail_e);
+        cur.skip_untransferred(runs, ggml);
         for (int d = 0; d < D && cur.valid; ++d) {
-            ring.issue(lane, d, cur.src(runs), cur.bytes(runs), pol_w);
-            cur.advance_tma(runs, P.ggml != 0);
+            ring.issue(lane, d, cur.src(), cur.bytes(), pol_w);
+            cur.step(runs);
+            cur.skip_untransferred(runs, ggml);
         }
         pdl_wait();
         // every run's activations, one transaction count on one barrier
@@ -646,8 +677,7 @@ __global__ void __launch_bounds__(max_warps_for(T) * 32, 1) qgemv_stream_kernel(
                 const RunInfo &R = runs[r];
                 const int8_t *xq = reinterpret_cast<const int8_t *>(smem + R.xq_off);
                 const unsigned short *xd = reinterpret_cast<const unsigned short *>(smem + R.xq_off + T * R.K);
-                int2 *cd = reinterpret_cast<int2 *>(smem + R.xq_off + T * R.K +
-                                                    static_cast<int>(roundup16_dev(2 * T * R.nb)));
+                int2 *cd = reinterpret_cast<int2 *>(smem + R.xq_off + T * R.K + roundup16_dev(2 * T * R.nb));
                 for (int i = tid; i < T * R.nb; i += nthreads) {
                     const int t = i / R.nb, bb = i - t * R.nb;
                     const uint4 *qp = reinterpret_cast<const uint4 *>(xq + t * R.K + bb * QK);
@@ -656,30 +686,29 @@ __global__ void __launch_bounds__(max_warps_for(T) * 32, 1) qgemv_stream_kernel(
             }
         __syncthreads();
 
-        // compute, in the walker's order
-        SpanWalker w;
-        w.init(runs, ivb, ive, false, P.ggml != 0);
+        // compute, one visit (the segments of one slab inside one interval) at a time
+        Walker w;
+        w.init(runs, head_b, b, tail_e, head_b, a, tail_e);
+        bool ok = xok;
         while (w.valid) {
             const RunInfo &R = runs[w.r];
-            const int iv = w.iv, ii = w.ii, s_first = w.s;
-            const int seg_end = min(R.nseg, s_first + (w.ive[iv] - w.k));   // this visit's segments
-            const int li = R.first_local + ii;
-            const bool tail_item = li >= R.nslabs;
-            const bool direct = P.ggml != 0 || tail_item;
-            const Group &g = P.g[R.gi];
-            const int rows = tail_item ? g.tail_rows : min(SLAB_ROWS, R.N - li * SLAB_ROWS);
-            const int row0 = li * SLAB_ROWS;
-            const uint8_t *rows_base = R.Wi + static_cast<long long>(li) * SLAB_ROWS * R.nb * Q4_BYTES;
+            const int s_first = w.s;
+            const int seg_end = min(w.nseg, s_first + (w.kend - w.k));
+            const int li = w.first_local + w.ii;
+            const bool tail_item = li >= w.nslabs;
+            const bool direct = ggml || tail_item;
+            const int K = R.K, nb = w.nb;
+            const int rows = tail_item ? P.g[R.gi].tail_rows : min(SLAB_ROWS, R.N - li * SLAB_ROWS);
+            const uint8_t *rows_base = w.Wi + static_cast<long long>(li) * SLAB_ROWS * nb * Q4_BYTES;
             const int8_t *xs_q = reinterpret_cast<const int8_t *>(smem + R.xq_off);
-            const int2 *xs_cd = reinterpret_cast<const int2 *>(smem + R.xq_off + T * R.K +
-                                                               static_cast<int>(roundup16_dev(2 * T * R.nb)));
+            const int2 *xs_cd = reinterpret_cast<const int2 *>(smem + R.xq_off + T * K + roundup16_dev(2 * T * nb));
             float yv[2][T];
 #pragma unroll
             for (int h = 0; h < 2; ++h)
 #pragma unroll
                 for (int t = 0; t < T; ++t) yv[h][t] = 0.0f;
             if (s_first > 0) {
-                // tail of an item begun by warp - 1: continue from its ordered sum
+                // tail of a slab begun by warp - 1: continue from its ordered sum
                 if (lane == 0) wait_flag(&hflag[warp - 1], abort_flag, P.status);
                 __syncwarp();
                 __threadfence_block();
@@ -696,24 +725,23 @@ __global__ void __launch_bounds__(max_warps_for(T) * 32, 1) qgemv_stream_kernel(
                 for (int h = 0; h < 2; ++h)
 #pragma unroll
                     for (int t = 0; t < T; ++t) acc[h][t] = 0.0f;
-                if (R.bad) {
+                if (w.bad) {
                     // nothing is read for an out-of-range expert id
                 } else if (direct) {
-                    if (xok) segment_from_ggml<T>(rows_base, rows, sg, R.K, R.nb, r8, j, xs_q, xs_cd, acc);
+                    if (ok) segment_from_ggml<T>(rows_base, rows, sg, K, nb, r8, j, xs_q, xs_cd, acc);
                 } else {
-                    const bool ok = mbar_wait_bounded(&ring.bar[ring.slot], ring.phase, abort_flag, P.status,
-                                                      WAIT_LIMIT_NS);
-                    if (ok && xok) {
-                        if (SEG_BLOCKS * (sg + 1) <= R.nb)
-                            segment_full_from_stage<T>(ring.stage(), sg, R.K, R.nb, r8, j, xs_q, xs_cd, acc);
+                    if (ok) ok = mbar_wait_bounded(&ring.bar[ring.slot], ring.phase, abort_flag, P.status, WAIT_LIMIT_NS);
+                    if (ok) {
+                        if (SEG_BLOCKS * (sg + 1) <= nb)
+                            segment_full_from_stage<T>(ring.stage(), sg, K, nb, r8, j, xs_q, xs_cd, acc);
                         else
-                            segment_from_stage<T>(ring.stage(), sg, R.K, R.nb, r8, j, xs_q, xs_cd, acc);
+                            segment_from_stage<T>(ring.stage(), sg, K, nb, r8, j, xs_q, xs_cd, acc);
                     }
                     __syncwarp();
-                    const int aborted = __shfl_sync(0xFFFFFFFFu, *abort_flag, 0);
-                    if (cur.valid && !aborted) {
-                        ring.issue(lane, ring.slot, cur.src(runs), cur.bytes(runs), pol_w);
-                        cur.advance_tma(runs, P.ggml != 0);
+                    if (cur.valid && ok) {  // refill the slot just consumed
+                        ring.issue(lane, ring.slot, cur.src(), cur.bytes(), pol_w);
+                        cur.step(runs);
+                        cur.skip_untransferred(runs, ggml);
                     }
                     ring.pop();
                 }
@@ -723,8 +751,8 @@ __global__ void __launch_bounds__(max_warps_for(T) * 32, 1) qgemv_stream_kernel(
 #pragma unroll
                     for (int t = 0; t < T; ++t) yv[h][t] = (sg == 0) ? acc[h][t] : __fadd_rn(yv[h][t], acc[h][t]);
             }
-            if (seg_end < R.nseg) {
-                // head of an item that warp + 1 finishes: leave the ordered sum
+            if (seg_end < w.nseg) {
+                // head of a slab that warp + 1 finishes: leave the ordered sum
                 if (j == 0) {
                     float *H = hbuf + warp * T * 16;
 #pragma unroll
@@ -736,13 +764,12 @@ __global__ void __launch_bounds__(max_warps_for(T) * 32, 1) qgemv_stream_kernel(
                 __threadfence_block();
                 __syncwarp();
                 if (lane == 0) hflag[warp] = 1;
-            } else if (!R.bad) {
-                store_rows<T, ARGMAX>(R.y, R.N, row0, rows, r8, j, yv, best);
+            } else if (!w.bad) {
+                store_rows<T, ARGMAX>(R.y, R.N, li * SLAB_ROWS, rows, r8, j, yv, best);
             } else if (lane == 0) {
                 atomicCAS(P.status, 0u, ST_BAD_ID);
             }
-            // move the walker past this visit
-            for (int sg = s_first; sg < seg_end; ++sg) w.step(runs);
+            w.next_item(runs);
         }
     } else {
         // ================================================= run-synced mode
