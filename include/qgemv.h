@@ -262,6 +262,14 @@ qgemv_status qgemv_debug_block_isums(const void *W, qgemv_wlayout layout, const 
 qgemv_status qgemv_debug_stream_read(const void *src, size_t bytes, int method, int warps, int depth,
                                      int stage_bytes, unsigned long long *sink, qgemv_stream_t stream);
 
+/* Tuning: how the streaming kernel is launched.  ctas_per_sm = CTAs resident
+ * per SM (1 = one CTA of up to 16 warps; 2 = two CTAs of 8 warps, T <= 2
+ * only), waves = CTAs per SM slot in one launch (more, smaller CTAs let the
+ * block scheduler hand more work to SMs that stream faster).  0 restores the
+ * default for either.  Results do not depend on it (the summation order is
+ * fixed by K).  Process-wide; affects launches enqueued afterwards. */
+qgemv_status qgemv_set_launch_shape(int ctas_per_sm, int waves);
+
 /* Read and clear the current device's status word: QGEMV_OK, or the first
  * asynchronous error a kernel recorded (QGEMV_ERR_TIMEOUT, QGEMV_ERR_BAD_ID)
  * into *code_out.  Synchronises with the device (a query, not part of the

@@ -71,6 +71,7 @@ _SIGS = {
     "qgemv_q4_0_gather": ([ctypes.POINTER(GatherMatrix), _I32, _VP, _I32, _I32, _I32, _I32, _VP, _SZ, _VP], _I32),
     "qgemv_debug_block_isums": ([_VP, _I32, _VP, _VP, _I64, _I64, _I32, _VP], _I32),
     "qgemv_debug_stream_read": ([_VP, _SZ, _I32, _I32, _I32, _I32, _VP, _VP], _I32),
+    "qgemv_set_launch_shape": ([_I32, _I32], _I32),
     "qgemv_device_status": ([ctypes.POINTER(ctypes.c_int)], _I32),
 }
 
@@ -239,6 +240,11 @@ def stream_read(src, method: int, warps: int, depth: int, stage_bytes: int, sink
     """Measurement hook: stream all of `src` once (see qgemv_debug_stream_read)."""
     _check(lib().qgemv_debug_stream_read(_ptr(src), src.numel() * src.element_size(), method, warps, depth,
                                          stage_bytes, _ptr(sink), _stream(stream)), "qgemv_debug_stream_read")
+
+
+def set_launch_shape(ctas_per_sm: int = 0, waves: int = 0):
+    """Tuning of the streaming kernel's launch (0 = default); results are unchanged."""
+    _check(lib().qgemv_set_launch_shape(ctas_per_sm, waves), "qgemv_set_launch_shape")
 
 
 def device_status() -> int:

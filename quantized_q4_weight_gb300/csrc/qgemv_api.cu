@@ -1,6 +1,7 @@
 // qgemv_api.cu -- the C ABI of libqgemv (include/qgemv.h): argument
 // validation, launch planning and kernel launches.  Host code only, apart
 // from the per-device status word.
+#include <atomic>
 #include <cstring>
 #include <memory>
 #include <mutex>
@@ -22,9 +23,15 @@ constexpr int kMaxDevices = 64;
 struct DevInfo {
     bool ready = false;
     int sms = 0;
-    int smem_optin = 0;
+    int smem_optin = 0;   // per CTA
+    int smem_per_sm = 0;
     unsigned *status = nullptr;
 };
+
+// Launch shape of the streaming kernel: CTAs resident per SM (1, or 2 of
+// 8 warps for T <= 2) and waves of CTAs per launch.  More, smaller CTAs let
+// the block scheduler give more work to SMs that stream faster.
+std::atomic<int> g_ctas_per_sm{0}, g_waves{0};
 
 std::mutex g_dev_mu;
 DevInfo g_dev[kMaxDevices];
@@ -38,6 +45,8 @@ qgemv_status device_info(DevInfo &out)
     if (!d.ready) {
         if (cudaDeviceGetAttribute(&d.sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return QGEMV_ERR_CUDA;
         if (cudaDeviceGetAttribute(&d.smem_optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) != cudaSuccess)
+            return QGEMV_ERR_CUDA;
+        if (cudaDeviceGetAttribute(&d.smem_per_sm, cudaDevAttrMaxSharedMemoryPerMultiprocessor, dev) != cudaSuccess)
             return QGEMV_ERR_CUDA;
         void *p = nullptr;
         if (cudaGetSymbolAddress(&p, g_qgemv_status) != cudaSuccess) return QGEMV_ERR_CUDA;
@@ -97,7 +106,7 @@ static_assert(CNT_AREA / 4 > SPLIT_SLAB_THRESHOLD, "split-K counters must fit th
 
 template <int MAXG>
 qgemv_status make_plan(const GroupSpec *gs, int n, int T, bool ggml, bool argmax, uint8_t *ws, int smem_limit,
-                       Plan<MAXG> &pl)
+                       Plan<MAXG> &pl, int ctas_per_sm = 1)
 {
     if (n < 1 || n > MAXG) return QGEMV_ERR_INTERNAL;
     Params<MAXG> &P = pl.P;
@@ -184,7 +193,8 @@ qgemv_status make_plan(const GroupSpec *gs, int n, int T, bool ggml, bool argmax
     P.ring_depth = 0;
     // 2 stages per warp and the widest warp count that leaves room for the
     // activations; then 8 warps; then a single stage.
-    const int choices[3][2] = {{max_warps_for(T), 2}, {8, 2}, {8, 1}};
+    const int wide = ctas_per_sm > 1 ? 8 : max_warps_for(T);
+    const int choices[3][2] = {{wide, 2}, {8, 2}, {8, 1}};
     for (const auto &c : choices) {
         const int nw = c[0], D = c[1];
         const long long bars = align_up(8ll * (nw * D + 1), 128);
@@ -225,9 +235,25 @@ cudaError_t dispatch_T(const Params<MAXG> &P, int T, int grid, size_t smem, cuda
     }
 }
 
-// The dynamic shared-memory budget of one CTA (the kernel's static arrays
-// take at most 600 bytes).
-inline int smem_budget(const DevInfo &d) { return d.smem_optin - 2048; }
+// CTAs per SM for a T-token launch, and the dynamic shared-memory budget of
+// one CTA (the kernel's static arrays take at most 600 bytes).
+inline int ctas_per_sm_for(int T)
+{
+    const int c = g_ctas_per_sm.load(std::memory_order_relaxed);
+    if (T > 2) return 1;  // 8 warps of wide accumulators fill the register file
+    return c >= 1 && c <= 2 ? c : 2;
+}
+inline int smem_budget(const DevInfo &d, int ctas_per_sm)
+{
+    const int per = ctas_per_sm > 1 ? d.smem_per_sm / ctas_per_sm - 1024 : d.smem_optin;
+    return per - 2048;
+}
+inline int grid_for(const DevInfo &d, int ctas_per_sm)
+{
+    const int w = g_waves.load(std::memory_order_relaxed);
+    const long long g = static_cast<long long>(d.sms) * ctas_per_sm * (w >= 1 ? w : 2);
+    return static_cast<int>(g < MAX_GRID ? g : MAX_GRID);
+}
 
 // Shared argument checks of the single-matrix GEMV calls.
 qgemv_status check_single(const void *W, qgemv_wlayout layout, const void *xin, long long xin_bytes,
@@ -268,13 +294,14 @@ qgemv_status run_single(const void *W, qgemv_wlayout layout, const void *xq, flo
     if (s != QGEMV_OK) return s;
     GroupSpec gs{W, 0, xq, 0, y, 0, N, K, 1};
     Plan<MAXG_SMALL> pl;
+    const int cps = ctas_per_sm_for(T);
     s = make_plan<MAXG_SMALL>(&gs, 1, T, layout == QGEMV_W_GGML, argmax, static_cast<uint8_t *>(ws),
-                              smem_budget(dev), pl);
+                              smem_budget(dev, cps), pl, cps);
     if (s != QGEMV_OK) return s;
     if (static_cast<long long>(ws_bytes) < pl.ws_bytes) return QGEMV_ERR_WORKSPACE;
     pl.P.status = dev.status;
     pl.P.am_idx = reinterpret_cast<long long *>(idx);
-    const int grid = dev.sms < MAX_GRID ? dev.sms : MAX_GRID;
+    const int grid = grid_for(dev, cps);
     const cudaError_t e = argmax ? dispatch_T<MAXG_SMALL, true>(pl.P, T, grid, pl.smem, st, pdl)
                                  : dispatch_T<MAXG_SMALL, false>(pl.P, T, grid, pl.smem, st, pdl);
     return e == cudaSuccess ? QGEMV_OK : QGEMV_ERR_CUDA;
@@ -459,7 +486,8 @@ static qgemv_status launch_seq(const qgemv_seq_item *items, const float *const *
     DevInfo dev;
     qgemv_status s = device_info(dev);
     if (s != QGEMV_OK) return s;
-    const int grid = dev.sms < MAX_GRID ? dev.sms : MAX_GRID;
+    const int cps = ctas_per_sm_for(T);
+    const int grid = grid_for(dev, cps);
     std::vector<GroupSpec> gs(MAXG_SEQ);
     std::unique_ptr<Plan<MAXG_SEQ>> pl(new Plan<MAXG_SEQ>());
     std::unique_ptr<QuantList> ql(xs ? new QuantList() : nullptr);
@@ -470,7 +498,7 @@ static qgemv_status launch_seq(const qgemv_seq_item *items, const float *const *
             gs[i] = GroupSpec{it.W, 0, it.xq, 0, it.y, 0, it.N, it.K, 1};
         }
         s = make_plan<MAXG_SEQ>(gs.data(), cn, T, layout == QGEMV_W_GGML, false, static_cast<uint8_t *>(ws),
-                                smem_budget(dev), *pl);
+                                smem_budget(dev, cps), *pl, cps);
         if (s != QGEMV_OK) return s;
         if (static_cast<long long>(ws_bytes) < pl->ws_bytes) return QGEMV_ERR_WORKSPACE;
         pl->P.status = dev.status;
@@ -613,14 +641,15 @@ qgemv_status qgemv_q4_0_gather(const qgemv_gather_matrix *mats, int n_mats, cons
     s = device_info(dev);
     if (s != QGEMV_OK) return s;
     Plan<MAXG_SMALL> pl;
+    const int cps = ctas_per_sm_for(T);
     s = make_plan<MAXG_SMALL>(gs, n_mats, T, layout == QGEMV_W_GGML, false, static_cast<uint8_t *>(ws),
-                              smem_budget(dev), pl);
+                              smem_budget(dev, cps), pl, cps);
     if (s != QGEMV_OK) return s;
     if (static_cast<long long>(ws_bytes) < pl.ws_bytes) return QGEMV_ERR_WORKSPACE;
     pl.P.status = dev.status;
     pl.P.ids = ids;
     pl.P.n_experts = n_experts;
-    const int grid = dev.sms < MAX_GRID ? dev.sms : MAX_GRID;
+    const int grid = grid_for(dev, cps);
     return dispatch_T<MAXG_SMALL, false>(pl.P, T, grid, pl.smem, reinterpret_cast<cudaStream_t>(stream), false) ==
                    cudaSuccess
                ? QGEMV_OK
@@ -656,6 +685,14 @@ qgemv_status qgemv_debug_stream_read(const void *src, size_t bytes, int method, 
                                dev.sms, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
                ? QGEMV_OK
                : QGEMV_ERR_CUDA;
+}
+
+qgemv_status qgemv_set_launch_shape(int ctas_per_sm, int waves)
+{
+    if (ctas_per_sm < 0 || ctas_per_sm > 2 || waves < 0 || waves > 6) return QGEMV_ERR_INVALID_ARG;
+    g_ctas_per_sm.store(ctas_per_sm);
+    g_waves.store(waves);
+    return QGEMV_OK;
 }
 
 qgemv_status qgemv_device_status(int *code_out)
