@@ -323,7 +323,7 @@ def traffic_record(workload: str, T: int):
 class ClockSampler:
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
-             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap,clocks.mem")
 
     def __init__(self, gpu_index: int):
         self.gpu = gpu_index
@@ -350,7 +350,7 @@ class ClockSampler:
         except Exception:
             self.proc.kill()
         self.fh.close()
-        sm, mx, reasons = [], None, set()
+        sm, mx, mem, reasons = [], None, [], set()
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         with open(self.path) as f:
             for line in f:
@@ -365,10 +365,18 @@ class ClockSampler:
                 for n, v in zip(names, parts[5:9]):
                     if v.lower() == "active":
                         reasons.add(n)
+                if len(parts) > 9:
+                    try:
+                        mem.append(float(parts[9]))
+                    except ValueError:
+                        pass
         os.unlink(self.path)
         if not sm:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+        out = {"sm_mhz": statistics.median(sm), "sm_max_mhz": mx, "reasons": sorted(reasons), "samples": len(sm)}
+        if mem:
+            out["mem_mhz"] = statistics.median(mem)
+        return out
 
 
 # ============================================================ CPU baseline (oracle)

@@ -30,10 +30,6 @@ cudaError_t launch_stream(const Params<MAXG> &P, int grid, size_t smem, cudaStre
         e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                  optin - static_cast<int>(fa.sharedSizeBytes));
         if (e != cudaSuccess) return e;
-        // the whole unified L1/shared array as shared memory, so that two
-        // CTAs of half the budget can be resident on one SM
-        e = cudaFuncSetAttribute(kern, cudaFuncAttributePreferredSharedMemoryCarveout, 100);
-        if (e != cudaSuccess) return e;
         raised.fetch_or(bit, std::memory_order_release);
     }
     cudaLaunchConfig_t cfg = {};

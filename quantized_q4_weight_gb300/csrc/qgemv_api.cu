@@ -1,6 +1,7 @@
 // qgemv_api.cu -- the C ABI of libqgemv (include/qgemv.h): argument
 // validation, launch planning and kernel launches.  Host code only, apart
 // from the per-device status word.
+#include <algorithm>
 #include <atomic>
 #include <cstring>
 #include <memory>
@@ -237,11 +238,12 @@ cudaError_t dispatch_T(const Params<MAXG> &P, int T, int grid, size_t smem, cuda
 
 // CTAs per SM for a T-token launch, and the dynamic shared-memory budget of
 // one CTA (the kernel's static arrays take at most 600 bytes).
-inline int ctas_per_sm_for(int T)
+inline int ctas_per_sm_for(int T, bool sequence)
 {
     const int c = g_ctas_per_sm.load(std::memory_order_relaxed);
     if (T > 2) return 1;  // 8 warps of wide accumulators fill the register file
-    return c >= 1 && c <= 2 ? c : 2;
+    if (c >= 1 && c <= 2) return c;
+    return sequence ? 2 : 1;  // measured: long lists gain from two CTAs per SM, single matrices do not
 }
 inline int smem_budget(const DevInfo &d, int ctas_per_sm)
 {
@@ -251,7 +253,7 @@ inline int smem_budget(const DevInfo &d, int ctas_per_sm)
 inline int grid_for(const DevInfo &d, int ctas_per_sm)
 {
     const int w = g_waves.load(std::memory_order_relaxed);
-    const long long g = static_cast<long long>(d.sms) * ctas_per_sm * (w >= 1 ? w : 2);
+    const long long g = static_cast<long long>(d.sms) * ctas_per_sm * (w >= 1 ? w : 1);
     return static_cast<int>(g < MAX_GRID ? g : MAX_GRID);
 }
 
@@ -294,7 +296,7 @@ qgemv_status run_single(const void *W, qgemv_wlayout layout, const void *xq, flo
     if (s != QGEMV_OK) return s;
     GroupSpec gs{W, 0, xq, 0, y, 0, N, K, 1};
     Plan<MAXG_SMALL> pl;
-    const int cps = ctas_per_sm_for(T);
+    const int cps = ctas_per_sm_for(T, false);
     s = make_plan<MAXG_SMALL>(&gs, 1, T, layout == QGEMV_W_GGML, argmax, static_cast<uint8_t *>(ws),
                               smem_budget(dev, cps), pl, cps);
     if (s != QGEMV_OK) return s;
@@ -458,20 +460,30 @@ static qgemv_status check_seq(const qgemv_seq_item *items, int n, qgemv_wlayout 
     if (layout != QGEMV_W_GGML && layout != QGEMV_W_PACKED) return QGEMV_ERR_INVALID_ARG;
     if (!ws) return QGEMV_ERR_WORKSPACE;
     if (!aligned(ws, 256)) return QGEMV_ERR_MISALIGNED;
-    const Range rw = range(ws, static_cast<long long>(ws_bytes));
+    // Every output range must overlap no other range (weights and activations
+    // may be shared between items): sort all ranges, sweep once.
+    struct Tagged {
+        Range r;
+        bool out;
+    };
+    std::vector<Tagged> v;
+    v.reserve(3 * static_cast<size_t>(n) + 1);
+    v.push_back(Tagged{range(ws, static_cast<long long>(ws_bytes)), false});
     for (int i = 0; i < n; ++i) {
         const qgemv_seq_item &a = items[i];
         if (!shape_ok(a.N, a.K) || !a.W || !a.xq || !a.y) return QGEMV_ERR_INVALID_ARG;
         if (!aligned(a.W, layout == QGEMV_W_PACKED ? 16 : 2) || !aligned(a.xq, 16) || !aligned(a.y, 4))
             return QGEMV_ERR_MISALIGNED;
-        const Range ry = range(a.y, 4ll * T * a.N);
-        if (overlap(ry, rw)) return QGEMV_ERR_INVALID_ARG;
-        for (int k = 0; k < n; ++k) {
-            const qgemv_seq_item &b = items[k];
-            if (overlap(ry, range(b.W, 18ll * b.N * (b.K / QK))) || overlap(ry, range(b.xq, xq_bytes_host(T, b.K))))
-                return QGEMV_ERR_INVALID_ARG;
-            if (k != i && overlap(ry, range(b.y, 4ll * T * b.N))) return QGEMV_ERR_INVALID_ARG;
-        }
+        v.push_back(Tagged{range(a.W, 18ll * a.N * (a.K / QK)), false});
+        v.push_back(Tagged{range(a.xq, xq_bytes_host(T, a.K)), false});
+        v.push_back(Tagged{range(a.y, 4ll * T * a.N), true});
+    }
+    std::sort(v.begin(), v.end(), [](const Tagged &x, const Tagged &y) { return x.r.lo < y.r.lo; });
+    uintptr_t hi_any = 0, hi_out = 0;
+    for (const Tagged &t : v) {
+        if (t.r.lo < (t.out ? hi_any : hi_out)) return QGEMV_ERR_INVALID_ARG;
+        if (t.r.hi > hi_any) hi_any = t.r.hi;
+        if (t.out && t.r.hi > hi_out) hi_out = t.r.hi;
     }
     return QGEMV_OK;
 }
@@ -486,7 +498,7 @@ static qgemv_status launch_seq(const qgemv_seq_item *items, const float *const *
     DevInfo dev;
     qgemv_status s = device_info(dev);
     if (s != QGEMV_OK) return s;
-    const int cps = ctas_per_sm_for(T);
+    const int cps = ctas_per_sm_for(T, true);
     const int grid = grid_for(dev, cps);
     std::vector<GroupSpec> gs(MAXG_SEQ);
     std::unique_ptr<Plan<MAXG_SEQ>> pl(new Plan<MAXG_SEQ>());
@@ -641,7 +653,7 @@ qgemv_status qgemv_q4_0_gather(const qgemv_gather_matrix *mats, int n_mats, cons
     s = device_info(dev);
     if (s != QGEMV_OK) return s;
     Plan<MAXG_SMALL> pl;
-    const int cps = ctas_per_sm_for(T);
+    const int cps = ctas_per_sm_for(T, false);
     s = make_plan<MAXG_SMALL>(gs, n_mats, T, layout == QGEMV_W_GGML, false, static_cast<uint8_t *>(ws),
                               smem_budget(dev, cps), pl, cps);
     if (s != QGEMV_OK) return s;
