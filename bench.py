@@ -432,6 +432,22 @@ def oracle_sample(workload: str, budget_s: float = 12.0, min_s: float = 3.0):
 
 # ============================================================ main
 
+def slowest_rank_ms(ms: float, world: int) -> float:
+    """Replicas only: every rank runs the same workload; the job's step time
+    is the slowest rank's (max over ranks)."""
+    if world <= 1:
+        return ms
+    import torch
+    t = torch.tensor([ms], dtype=torch.float64)
+    torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+    return float(t[0])
+
+
+def job_value(step_bytes: int, ms: float, world: int) -> float:
+    """Whole-job GB/s: the bytes all ranks processed / the slowest rank's time."""
+    return step_bytes * world / (ms * 1e-3) / 1e9
+
+
 def dist_env():
     ws = int(os.environ.get("WORLD_SIZE", "1"))
     rank = int(os.environ.get("RANK", "0"))
@@ -548,10 +564,7 @@ def measure(args, wl: Workload, dev, world, rank):
     torch.cuda.synchronize()
     clk = clocks.stop()
     gemv_ms = statistics.mean(a.elapsed_time(b) for a, b in ev)
-    if world > 1:
-        t = torch.tensor([ms], dtype=torch.float64)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t[0])
+    ms = slowest_rank_ms(ms, world)
     assert q.device_status() == 0
 
     # ---- end to end through the public API: pinned host inputs in, outputs out
@@ -579,7 +592,7 @@ def measure(args, wl: Workload, dev, world, rank):
     e2e_ms = e0.elapsed_time(e1) / args.e2e_steps
 
     peak, peak_kind = peaks()
-    gbs = wl.step_bytes / (ms * 1e-3) / 1e9 * world
+    gbs = job_value(wl.step_bytes, ms, world)
     achieved = wl.gemv_kernel_bytes / (gemv_ms * 1e-3) / 1e9
     cfg = dict(wl.config)
     cfg.update({"us_per_gemv": round(ms * 1e3 / wl.n_gemv, 3), "gemv_kernel_ms": round(gemv_ms, 5),
