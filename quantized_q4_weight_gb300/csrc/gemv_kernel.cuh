@@ -201,21 +201,46 @@ struct StageCursor {
     }
 };
 
+// ------------------------------------------------------------------ lane outputs
+//
+// The (row, token) outputs a lane owns.  dp4a lanes (one token): rows r8 and
+// r8 + 8 of the slab, every token; the four lanes of a row pair hold equal
+// values after the phase combine and lane j == 0 writes.  MMA lanes (T > 1):
+// rows g and g + 8, tokens 2j and 2j + 1 -- the accumulator layout of
+// mma.m16n8k32 (element k: row g + 8 (k >> 1), token 2j + (k & 1)).
+template <int T>
+struct LaneOut {
+    static constexpr bool MMA = use_mma(T);
+    static constexpr int N = MMA ? 4 : 2 * T;
+    __device__ static __forceinline__ int row(int k, int r8) { return MMA ? r8 + 8 * (k >> 1) : r8 + 8 * (k / T); }
+    __device__ static __forceinline__ int tok(int k, int j) { return MMA ? 2 * j + (k & 1) : k % T; }
+    __device__ static __forceinline__ bool owner(int k, int j) { return MMA ? (2 * j + (k & 1)) < T : j == 0; }
+};
+
+struct XqView {
+    const int8_t *q;   // token rows at q + t * xstride
+    int xstride;
+    const int2 *cd;    // [block][cdw] {folded constant, d_x / 16}
+    int cdw;
+};
+
+// ------------------------------------------------------------------ dp4a path (T == 1)
+
 // acc[h][t] += (d_w(h) * d_x(t)) * isum for one block b of rows h = 0, 1,
 // formed as (d_w * (d_x / 16)) * (16 isum): the same real product, so one
 // fused multiply-add rounds it exactly as (d_w * d_x) * isum would.
 template <int T>
-__device__ __forceinline__ void fma_block(const uint4 &n0, const uint4 &n1, float dw0, float dw1, int b, int K,
-                                          int nb, const int8_t *xs_q, const int2 *xs_cd, float (&acc)[2][T])
+__device__ __forceinline__ void fma_block(const uint4 &n0, const uint4 &n1, float dw0, float dw1, int b,
+                                          const XqView &xv, float (&acc)[2][T])
 {
 #pragma unroll
     for (int t = 0; t < T; ++t) {
-        const uint4 *xp = reinterpret_cast<const uint4 *>(xs_q + t * K + b * QK);
+        const uint4 *xp = reinterpret_cast<const uint4 *>(xv.q + t * xv.xstride + b * QK);
         const uint4 qa = xp[0], qb = xp[1];
-        const int2 cd = xs_cd[t * nb + b];
-        const int s0 = block_dot16_magic(n0, qa, qb, cd.x);   // MAGIC + 16 isum
+        const int2 cd = xv.cd[b * xv.cdw + t];
+        const int s0 = block_dot16_magic(n0, qa, qb, cd.x);  // MAGIC + 16 isum
         const int s1 = block_dot16_magic(n1, qa, qb, cd.x);
-        const float dx = __int_as_float(cd.y);                // d_x / 16 (exact)
+        const float dx = __int_as_float(cd.y);               // d_x / 16 (exact)
         acc[0][t] = __fmaf_rn(__fmul_rn(dw0, dx), magic_to_float(s0), acc[0][t]);
         acc[1][t] = __fmaf_rn(__fmul_rn(dw1, dx), magic_to_float(s1), acc[1][t]);
     }
@@ -223,8 +248,8 @@ __device__ __forceinline__ void fma_block(const uint4 &n0, const uint4 &n1, floa
 
 // One segment from a shared-memory stage in the packed quad layout.
 template <int T>
-__device__ __forceinline__ void segment_from_stage(const uint8_t *stage, int s, int K, int nb, int r8, int j,
-                                                   const int8_t *xs_q, const int2 *xs_cd, float (&acc)[2][T])
+__device__ __forceinline__ void segment_from_stage(const uint8_t *stage, int s, int nb, int r8, int j,
+                                                   const XqView &xv, float (&acc)[2][T])
 {
     const int nbs = min(SEG_BLOCKS, nb - SEG_BLOCKS * s);
 #pragma unroll
@@ -235,16 +260,16 @@ __device__ __forceinline__ void segment_from_stage(const uint8_t *stage, int s, 
             const uint4 n0 = *reinterpret_cast<const uint4 *>(q + (r8 * nbq + j) * 16);
             const uint4 n1 = *reinterpret_cast<const uint4 *>(q + ((r8 + 8) * nbq + j) * 16);
             const unsigned sc = *reinterpret_cast<const unsigned *>(q + 256 * nbq + (r8 * nbq + j) * 4);
-            fma_block<T>(n0, n1, h2f(sc), h2f(sc >> 16), SEG_BLOCKS * s + QUAD * qq + j, K, nb, xs_q, xs_cd, acc);
+            fma_block<T>(n0, n1, h2f(sc), h2f(sc >> 16), SEG_BLOCKS * s + QUAD * qq + j, xv, acc);
         }
     }
 }
 
-// A full segment (16 blocks = 4 full quads) from a shared-memory stage:
-// branch-free, every load of the segment issued before the arithmetic.
+// A full segment (16 blocks = 4 full quads): branch-free, every load of the
+// segment issued before the arithmetic.
 template <int T>
-__device__ __forceinline__ void segment_full_from_stage(const uint8_t *stage, int s, int K, int nb, int r8, int j,
-                                                        const int8_t *xs_q, const int2 *xs_cd, float (&acc)[2][T])
+__device__ __forceinline__ void segment_full_from_stage(const uint8_t *stage, int s, int r8, int j,
+                                                        const XqView &xv, float (&acc)[2][T])
 {
     const int lo = (r8 * QUAD + j) * 16;
     uint4 n0[4], n1[4];
@@ -258,15 +283,14 @@ __device__ __forceinline__ void segment_full_from_stage(const uint8_t *stage, in
     }
 #pragma unroll
     for (int qq = 0; qq < 4; ++qq)
-        fma_block<T>(n0[qq], n1[qq], h2f(sc[qq]), h2f(sc[qq] >> 16), SEG_BLOCKS * s + QUAD * qq + j, K, nb, xs_q,
-                     xs_cd, acc);
+        fma_block<T>(n0[qq], n1[qq], h2f(sc[qq]), h2f(sc[qq] >> 16), SEG_BLOCKS * s + QUAD * qq + j, xv, acc);
 }
 
 // One segment read directly from GGML-layout rows in global memory (rows of
 // the packed tail, or every row when the weights are not packed).
 template <int T>
-__device__ __forceinline__ void segment_from_ggml(const uint8_t *rows_base, int rows, int s, int K, int nb, int r8,
-                                                  int j, const int8_t *xs_q, const int2 *xs_cd, float (&acc)[2][T])
+__device__ __forceinline__ void segment_from_ggml(const uint8_t *rows_base, int rows, int s, int nb, int r8, int j,
+                                                  const XqView &xv, float (&acc)[2][T])
 {
     const int nbs = min(SEG_BLOCKS, nb - SEG_BLOCKS * s);
     const long long row_bytes = static_cast<long long>(nb) * Q4_BYTES;
@@ -279,7 +303,7 @@ __device__ __forceinline__ void segment_from_ggml(const uint8_t *rows_base, int 
             unsigned d0 = 0, d1 = 0;
             if (r8 < rows) load_ggml_block(rows_base + r8 * row_bytes + b * Q4_BYTES, n0, d0);
             if (r8 + 8 < rows) load_ggml_block(rows_base + (r8 + 8) * row_bytes + b * Q4_BYTES, n1, d1);
-            fma_block<T>(n0, n1, h2f(d0), h2f(d1), b, K, nb, xs_q, xs_cd, acc);
+            fma_block<T>(n0, n1, h2f(d0), h2f(d1), b, xv, acc);
         }
     }
 }
@@ -300,9 +324,205 @@ __device__ __forceinline__ void combine_phases(float (&acc)[2][T])
         }
 }
 
-// Warps per CTA a T-token kernel may use: 16 for T <= 2, 8 above (the
-// wider accumulators need more than 128 registers per thread).
-__host__ __device__ constexpr int max_warps_for(int T) { return T <= 2 ? NWARPS_MAX : 8; }
+// ------------------------------------------------------------------ MMA path (T > 1)
+//
+// One mma.sync.m16n8k32 (u8 x s8 -> s32) per block forms the 16 x 8 integer
+// block sums (16 rows of the slab, 8 token columns, zero past T).  Lane
+// (g, j) supplies word j of rows g and g + 8 (elements 4j..4j+3 in the low
+// nibbles, 16+4j..16+4j+3 in the high nibbles, both masked as 16 n) and
+// activation words j and 4 + j of token g; the accumulator starts at the
+// folded constant, so the result is MAGIC + 16 isum as on the dp4a path.
+// The lane keeps one fp32 sum per block phase (b % 4) and output, and the
+// same fused multiply-adds in the same order as a dp4a lane would.
+
+__device__ __forceinline__ void mma_u8s8(int (&d)[4], unsigned a0, unsigned a1, unsigned a2, unsigned a3,
+                                         unsigned b0, unsigned b1)
+{
+    asm volatile(
+        "mma.sync.aligned.m16n8k32.row.col.s32.u8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+r"(d[0]), "+r"(d[1]), "+r"(d[2]), "+r"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+template <int T>
+__device__ __forceinline__ void mma_block(unsigned wg, unsigned wg8, unsigned sc, int b, int g, int j,
+                                          const XqView &xv, float (&acc)[4])
+{
+    unsigned b0 = 0, b1 = 0;
+    if (g < T) {
+        const unsigned *xr = reinterpret_cast<const unsigned *>(xv.q + g * xv.xstride + b * QK);
+        b0 = xr[j];
+        b1 = xr[4 + j];
+    }
+    const int4 cd = *reinterpret_cast<const int4 *>(xv.cd + b * 8 + 2 * j);  // tokens 2j, 2j + 1
+    int d[4] = {cd.x, cd.z, cd.x, cd.z};
+    mma_u8s8(d, (wg << 4) & 0xF0F0F0F0u, (wg8 << 4) & 0xF0F0F0F0u, wg & 0xF0F0F0F0u, wg8 & 0xF0F0F0F0u, b0, b1);
+    const float dw0 = h2f(sc), dw1 = h2f(sc >> 16);
+    const float dx0 = __int_as_float(cd.y), dx1 = __int_as_float(cd.w);
+    acc[0] = __fmaf_rn(__fmul_rn(dw0, dx0), magic_to_float(d[0]), acc[0]);
+    acc[1] = __fmaf_rn(__fmul_rn(dw0, dx1), magic_to_float(d[1]), acc[1]);
+    acc[2] = __fmaf_rn(__fmul_rn(dw1, dx0), magic_to_float(d[2]), acc[2]);
+    acc[3] = __fmaf_rn(__fmul_rn(dw1, dx1), magic_to_float(d[3]), acc[3]);
+}
+
+// One segment from a stage; `full` segments (16 blocks) take the branch-free form.
+template <int T>
+__device__ __forceinline__ void mma_segment_from_stage(const uint8_t *stage, bool full, int s, int nb, int g, int j,
+                                                       const XqView &xv, float (&acc)[4][4])
+{
+    if (full) {
+#pragma unroll 1
+        for (int qq = 0; qq < 4; ++qq) {  // one quad's loads in flight at a time (register budget)
+            const uint8_t *q = stage + qq * QUAD_BYTES;
+            unsigned wg[4], wg8[4], sc[4];
+#pragma unroll
+            for (int jq = 0; jq < 4; ++jq) {
+                wg[jq] = *reinterpret_cast<const unsigned *>(q + (g * QUAD + jq) * 16 + 4 * j);
+                wg8[jq] = *reinterpret_cast<const unsigned *>(q + ((g + 8) * QUAD + jq) * 16 + 4 * j);
+                sc[jq] = *reinterpret_cast<const unsigned *>(q + 256 * QUAD + (g * QUAD + jq) * 4);
+            }
+#pragma unroll
+            for (int jq = 0; jq < 4; ++jq)
+                mma_block<T>(wg[jq], wg8[jq], sc[jq], SEG_BLOCKS * s + QUAD * qq + jq, g, j, xv, acc[jq]);
+        }
+        return;
+    }
+    const int nbs = min(SEG_BLOCKS, nb - SEG_BLOCKS * s);
+#pragma unroll
+    for (int qq = 0; qq < 4; ++qq) {
+        const int nbq = min(QUAD, nbs - QUAD * qq);
+        const uint8_t *q = stage + qq * QUAD_BYTES;
+#pragma unroll
+        for (int jq = 0; jq < 4; ++jq)
+            if (jq < nbq) {  // warp-uniform
+                const unsigned wg = *reinterpret_cast<const unsigned *>(q + (g * nbq + jq) * 16 + 4 * j);
+                const unsigned wg8 = *reinterpret_cast<const unsigned *>(q + ((g + 8) * nbq + jq) * 16 + 4 * j);
+                const unsigned sc = *reinterpret_cast<const unsigned *>(q + 256 * nbq + (g * nbq + jq) * 4);
+                mma_block<T>(wg, wg8, sc, SEG_BLOCKS * s + QUAD * qq + jq, g, j, xv, acc[jq]);
+            }
+    }
+}
+
+__device__ __forceinline__ unsigned ldg_u32_a2(const uint8_t *p)  // 2-byte aligned 32-bit load
+{
+    const unsigned short *h = reinterpret_cast<const unsigned short *>(p);
+    return static_cast<unsigned>(__ldg(h)) | (static_cast<unsigned>(__ldg(h + 1)) << 16);
+}
+
+template <int T>
+__device__ __forceinline__ void mma_segment_from_ggml(const uint8_t *rows_base, int rows, int s, int nb, int g, int j,
+                                                      const XqView &xv, float (&acc)[4][4])
+{
+    const int nbs = min(SEG_BLOCKS, nb - SEG_BLOCKS * s);
+    const long long row_bytes = static_cast<long long>(nb) * Q4_BYTES;
+#pragma unroll 1
+    for (int qq = 0; qq < 4; ++qq) {
+#pragma unroll
+        for (int jq = 0; jq < 4; ++jq) {  // static phase index: accumulators stay in registers
+            const int i = QUAD * qq + jq;
+            if (i < nbs) {                // warp-uniform
+                const int b = SEG_BLOCKS * s + i;
+                unsigned wg = 0, wg8 = 0, d0 = 0, d1 = 0;
+                if (g < rows) {
+                    const uint8_t *p = rows_base + g * row_bytes + b * Q4_BYTES;
+                    d0 = __ldg(reinterpret_cast<const unsigned short *>(p));
+                    wg = ldg_u32_a2(p + 2 + 4 * j);
+                }
+                if (g + 8 < rows) {
+                    const uint8_t *p = rows_base + (g + 8) * row_bytes + b * Q4_BYTES;
+                    d1 = __ldg(reinterpret_cast<const unsigned short *>(p));
+                    wg8 = ldg_u32_a2(p + 2 + 4 * j);
+                }
+                mma_block<T>(wg, wg8, d0 | (d1 << 16), b, g, j, xv, acc[jq]);
+            }
+        }
+    }
+}
+
+// ------------------------------------------------------------------ either path
+
+// The ordered sum of one segment for this lane's outputs.
+template <int T>
+__device__ __forceinline__ void segment_sum(bool from_stage, const uint8_t *stage, const uint8_t *rows_base, int rows,
+                                            int s, int nb, int r8, int j, const XqView &xv,
+                                            float (&P)[LaneOut<T>::N])
+{
+    const bool full = SEG_BLOCKS * (s + 1) <= nb;
+    if constexpr (use_mma(T)) {
+        float acc[4][4];
+#pragma unroll
+        for (int p = 0; p < 4; ++p)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) acc[p][k] = 0.0f;
+        if (from_stage)
+            mma_segment_from_stage<T>(stage, full, s, nb, r8, j, xv, acc);
+        else
+            mma_segment_from_ggml<T>(rows_base, rows, s, nb, r8, j, xv, acc);
+#pragma unroll
+        for (int k = 0; k < 4; ++k) P[k] = __fadd_rn(__fadd_rn(acc[0][k], acc[1][k]), __fadd_rn(acc[2][k], acc[3][k]));
+    } else {
+        float acc[2][T];
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int t = 0; t < T; ++t) acc[h][t] = 0.0f;
+        if (from_stage) {
+            if (full)
+                segment_full_from_stage<T>(stage, s, r8, j, xv, acc);
+            else
+                segment_from_stage<T>(stage, s, nb, r8, j, xv, acc);
+        } else {
+            segment_from_ggml<T>(rows_base, rows, s, nb, r8, j, xv, acc);
+        }
+        combine_phases<T>(acc);
+#pragma unroll
+        for (int h = 0; h < 2; ++h)
+#pragma unroll
+            for (int t = 0; t < T; ++t) P[h * T + t] = acc[h][t];
+    }
+}
+
+// Builds one run's activation image in shared memory after its copy landed:
+// per block and token the folded constant and d_x / 16 (MMA path: tokens
+// past T get a constant that yields exactly 0).
+template <int T>
+__device__ __forceinline__ void build_fold_constants(uint8_t *img, int K, int tid, int nthreads)
+{
+    const XqLayout L = xq_layout(T, K);
+    const int nb = K / QK;
+    const int8_t *xq = reinterpret_cast<const int8_t *>(img);
+    const unsigned short *xd = reinterpret_cast<const unsigned short *>(img + L.off_d);
+    int2 *cd = reinterpret_cast<int2 *>(img + L.off_cd);
+    for (int i = tid; i < L.cdw * nb; i += nthreads) {
+        const int b = i / L.cdw, t = i - b * L.cdw;
+        if (t < T) {
+            const uint4 *qp = reinterpret_cast<const uint4 *>(xq + t * L.xstride + b * QK);
+            cd[i] = make_int2(block_fold16_const(qp[0], qp[1]), __float_as_int(__fmul_rn(h2f(xd[t * nb + b]), 0.0625f)));
+        } else {
+            cd[i] = make_int2(MAGIC_I, 0);
+        }
+    }
+}
+
+// Copies one run's activations (planar Q8_0, T rows of K) into an image;
+// one copy per token row on the MMA path (padded rows).  Returns the bytes.
+template <int T>
+__device__ __forceinline__ unsigned copy_activations(uint8_t *img, const uint8_t *src, int K, unsigned dbytes,
+                                                     uint64_t *bar, uint64_t pol)
+{
+    const XqLayout L = xq_layout(T, K);
+    if (L.xstride == K) {
+        bulk_g2s(img, src, static_cast<unsigned>(T * K), bar, pol);
+    } else {
+#pragma unroll
+        for (int t = 0; t < T; ++t) bulk_g2s(img + t * L.xstride, src + t * K, static_cast<unsigned>(K), bar, pol);
+    }
+    bulk_g2s(img + L.off_d, src + T * K, dbytes, bar, pol);
+    return static_cast<unsigned>(T * K) + dbytes;
+}
+
+// Warps per CTA a T-token kernel may use (both paths fit 128 registers).
+__host__ __device__ constexpr int max_warps_for(int) { return NWARPS_MAX; }
 
 // ------------------------------------------------------------------ balanced mode
 //
@@ -482,20 +702,24 @@ struct Ring {
     }
 };
 
+// Write this lane's finished outputs (rows below `rows`) and fold them into
+// the argmax keys.
 template <int T, bool ARGMAX>
-__device__ __forceinline__ void store_rows(float *ye, int N, int row0, int rows, int r8, int j, const float (&yv)[2][T],
-                                           unsigned long long (&best)[T])
+__device__ __forceinline__ void store_outputs(float *ye, int N, int row0, int rows, int r8, int j,
+                                              const float (&yv)[LaneOut<T>::N], unsigned long long (&best)[T])
 {
-    if (j != 0) return;
+    using LO = LaneOut<T>;
 #pragma unroll
-    for (int h = 0; h < 2; ++h) {
-        const int lr = r8 + 8 * h;
-        if (lr < rows) {
+    for (int k = 0; k < LO::N; ++k) {
+        const int lr = LO::row(k, r8), t = LO::tok(k, j);
+        if (LO::owner(k, j) && lr < rows) {
             const int row = row0 + lr;
+            if (ye != nullptr) ye[static_cast<long long>(t) * N + row] = yv[k];
+            if (ARGMAX) {
+                const unsigned long long key = argmax_key(yv[k], static_cast<unsigned>(row));
 #pragma unroll
-            for (int t = 0; t < T; ++t) {
-                if (ye != nullptr) ye[static_cast<long long>(t) * N + row] = yv[h][t];
-                if (ARGMAX) best[t] = max(best[t], argmax_key(yv[h][t], static_cast<unsigned>(row)));
+                for (int u = 0; u < T; ++u)  // static indices: no local memory
+                    if (u == t) best[u] = max(best[u], key);
             }
         }
     }
@@ -520,6 +744,8 @@ __device__ __forceinline__ bool wait_flag(volatile int *flag, volatile int *abor
 template <int T, int MAXG, bool ARGMAX>
 __global__ void __launch_bounds__(max_warps_for(T) * 32, 1) qgemv_stream_kernel(const __grid_constant__ Params<MAXG> P)
 {
+    using LO = LaneOut<T>;
+    constexpr int NO = LO::N;
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_abort;
     __shared__ int s_last;
@@ -537,6 +763,7 @@ __global__ void __launch_bounds__(max_warps_for(T) * 32, 1) qgemv_stream_kernel(
     float *hbuf = reinterpret_cast<float *>(smem + P.off_hbuf);          // [nw][T][16]
     volatile int *hflag = reinterpret_cast<volatile int *>(smem + P.off_hflag);
     volatile int *abort_flag = &s_abort;
+    const bool ggml = P.ggml != 0;
 
     Ring ring;
     ring.base = smem + P.off_ring + static_cast<size_t>(warp) * D * SEG_BYTES;
@@ -589,8 +816,7 @@ __global__ void __launch_bounds__(max_warps_for(T) * 32, 1) qgemv_stream_kernel(
             R.nslabs = g.nslabs;
             R.xq_off = xoff;
             R.bad = bad;
-            const int slot_bytes = (T * g.K + static_cast<int>(roundup16_dev(2 * T * g.nb)) + 8 * T * g.nb + 127) & ~127;
-            xoff += slot_bytes;
+            xoff += xq_layout(T, g.K).bytes;
             stages += R.nstages;
             nseg_max = max(nseg_max, g.nseg);
             ++nr;
@@ -641,7 +867,6 @@ __global__ void __launch_bounds__(max_warps_for(T) * 32, 1) qgemv_stream_kernel(
                 tail_e = st + runs[r].nseg;  // [a, tail_e) finishes an item begun by warp - 1
             }
         }
-        const bool ggml = P.ggml != 0;
 
         // weights first (they do not depend on the preceding kernel)
         Walker cur;
@@ -662,28 +887,16 @@ __global__ void __launch_bounds__(max_warps_for(T) * 32, 1) qgemv_stream_kernel(
             for (int r = 0; r < nruns; ++r) {
                 const RunInfo &R = runs[r];
                 const Group &g = P.g[R.gi];
-                const uint8_t *src = g.xq + static_cast<long long>(R.e) * g.xq_stride;
-                const unsigned qbytes = static_cast<unsigned>(T * R.K);
-                const unsigned dbytes = static_cast<unsigned>(g.xq_bytes) - qbytes;
-                bulk_g2s(smem + R.xq_off, src, qbytes, xbar, pol_x);
-                bulk_g2s(smem + R.xq_off + qbytes, src + qbytes, dbytes, xbar, pol_x);
+                const unsigned dbytes = static_cast<unsigned>(g.xq_bytes - T * R.K);
+                copy_activations<T>(smem + R.xq_off, g.xq + static_cast<long long>(R.e) * g.xq_stride, R.K, dbytes,
+                                    xbar, pol_x);
             }
         }
         const bool xok = mbar_wait_bounded(xbar, 0, abort_flag, P.status, WAIT_LIMIT_NS);
         xphase ^= 1u;
         if (xok) x_unconfirmed = false;
         if (xok)
-            for (int r = 0; r < nruns; ++r) {
-                const RunInfo &R = runs[r];
-                const int8_t *xq = reinterpret_cast<const int8_t *>(smem + R.xq_off);
-                const unsigned short *xd = reinterpret_cast<const unsigned short *>(smem + R.xq_off + T * R.K);
-                int2 *cd = reinterpret_cast<int2 *>(smem + R.xq_off + T * R.K + roundup16_dev(2 * T * R.nb));
-                for (int i = tid; i < T * R.nb; i += nthreads) {
-                    const int t = i / R.nb, bb = i - t * R.nb;
-                    const uint4 *qp = reinterpret_cast<const uint4 *>(xq + t * R.K + bb * QK);
-                    cd[i] = make_int2(block_fold16_const(qp[0], qp[1]), __float_as_int(__fmul_rn(h2f(xd[i]), 0.0625f)));
-                }
-            }
+            for (int r = 0; r < nruns; ++r) build_fold_constants<T>(smem + runs[r].xq_off, runs[r].K, tid, nthreads);
         __syncthreads();
 
         // compute, one visit (the segments of one slab inside one interval) at a time
@@ -697,16 +910,15 @@ __global__ void __launch_bounds__(max_warps_for(T) * 32, 1) qgemv_stream_kernel(
             const int li = w.first_local + w.ii;
             const bool tail_item = li >= w.nslabs;
             const bool direct = ggml || tail_item;
-            const int K = R.K, nb = w.nb;
+            const int nb = w.nb;
             const int rows = tail_item ? P.g[R.gi].tail_rows : min(SLAB_ROWS, R.N - li * SLAB_ROWS);
             const uint8_t *rows_base = w.Wi + static_cast<long long>(li) * SLAB_ROWS * nb * Q4_BYTES;
-            const int8_t *xs_q = reinterpret_cast<const int8_t *>(smem + R.xq_off);
-            const int2 *xs_cd = reinterpret_cast<const int2 *>(smem + R.xq_off + T * K + roundup16_dev(2 * T * nb));
-            float yv[2][T];
+            const XqLayout L = xq_layout(T, R.K);
+            const XqView xv{reinterpret_cast<const int8_t *>(smem + R.xq_off), L.xstride,
+                            reinterpret_cast<const int2 *>(smem + R.xq_off + L.off_cd), L.cdw};
+            float yv[NO];
 #pragma unroll
-            for (int h = 0; h < 2; ++h)
-#pragma unroll
-                for (int t = 0; t < T; ++t) yv[h][t] = 0.0f;
+            for (int k = 0; k < NO; ++k) yv[k] = 0.0f;
             if (s_first > 0) {
                 // tail of a slab begun by warp - 1: continue from its ordered sum
                 if (lane == 0) wait_flag(&hflag[warp - 1], abort_flag, P.status);
@@ -714,28 +926,26 @@ __global__ void __launch_bounds__(max_warps_for(T) * 32, 1) qgemv_stream_kernel(
                 __threadfence_block();
                 const float *H = hbuf + (warp - 1) * T * 16;
 #pragma unroll
-                for (int t = 0; t < T; ++t) {
-                    yv[0][t] = H[t * 16 + r8];
-                    yv[1][t] = H[t * 16 + r8 + 8];
+                for (int k = 0; k < NO; ++k) {
+                    const int t = LO::tok(k, j);
+                    yv[k] = t < T ? H[t * 16 + LO::row(k, r8)] : 0.0f;
                 }
             }
             for (int sg = s_first; sg < seg_end; ++sg) {
-                float acc[2][T];
-#pragma unroll
-                for (int h = 0; h < 2; ++h)
-#pragma unroll
-                    for (int t = 0; t < T; ++t) acc[h][t] = 0.0f;
+                float Pk[NO];
+                bool have = false;
                 if (w.bad) {
                     // nothing is read for an out-of-range expert id
                 } else if (direct) {
-                    if (ok) segment_from_ggml<T>(rows_base, rows, sg, K, nb, r8, j, xs_q, xs_cd, acc);
+                    if (ok) {
+                        segment_sum<T>(false, nullptr, rows_base, rows, sg, nb, r8, j, xv, Pk);
+                        have = true;
+                    }
                 } else {
                     if (ok) ok = mbar_wait_bounded(&ring.bar[ring.slot], ring.phase, abort_flag, P.status, WAIT_LIMIT_NS);
                     if (ok) {
-                        if (SEG_BLOCKS * (sg + 1) <= nb)
-                            segment_full_from_stage<T>(ring.stage(), sg, K, nb, r8, j, xs_q, xs_cd, acc);
-                        else
-                            segment_from_stage<T>(ring.stage(), sg, K, nb, r8, j, xs_q, xs_cd, acc);
+                        segment_sum<T>(true, ring.stage(), nullptr, 0, sg, nb, r8, j, xv, Pk);
+                        have = true;
                     }
                     __syncwarp();
                     if (cur.valid && ok) {  // refill the slot just consumed
@@ -745,27 +955,24 @@ __global__ void __launch_bounds__(max_warps_for(T) * 32, 1) qgemv_stream_kernel(
                     }
                     ring.pop();
                 }
-                combine_phases<T>(acc);
+                if (!have) {
 #pragma unroll
-                for (int h = 0; h < 2; ++h)
+                    for (int k = 0; k < NO; ++k) Pk[k] = 0.0f;
+                }
 #pragma unroll
-                    for (int t = 0; t < T; ++t) yv[h][t] = (sg == 0) ? acc[h][t] : __fadd_rn(yv[h][t], acc[h][t]);
+                for (int k = 0; k < NO; ++k) yv[k] = (sg == 0) ? Pk[k] : __fadd_rn(yv[k], Pk[k]);
             }
             if (seg_end < w.nseg) {
                 // head of a slab that warp + 1 finishes: leave the ordered sum
-                if (j == 0) {
-                    float *H = hbuf + warp * T * 16;
+                float *H = hbuf + warp * T * 16;
 #pragma unroll
-                    for (int t = 0; t < T; ++t) {
-                        H[t * 16 + r8] = yv[0][t];
-                        H[t * 16 + r8 + 8] = yv[1][t];
-                    }
-                }
+                for (int k = 0; k < NO; ++k)
+                    if (LO::owner(k, j)) H[LO::tok(k, j) * 16 + LO::row(k, r8)] = yv[k];
                 __threadfence_block();
                 __syncwarp();
                 if (lane == 0) hflag[warp] = 1;
             } else if (!w.bad) {
-                store_rows<T, ARGMAX>(R.y, R.N, li * SLAB_ROWS, rows, r8, j, yv, best);
+                store_outputs<T, ARGMAX>(R.y, R.N, li * SLAB_ROWS, rows, r8, j, yv, best);
             } else if (lane == 0) {
                 atomicCAS(P.status, 0u, ST_BAD_ID);
             }
@@ -774,9 +981,6 @@ __global__ void __launch_bounds__(max_warps_for(T) * 32, 1) qgemv_stream_kernel(
     } else {
         // ================================================= run-synced mode
         // (small launches, split-K, or activations that do not all fit)
-        int8_t *xs_q = reinterpret_cast<int8_t *>(smem);
-        const unsigned short *xs_d = reinterpret_cast<const unsigned short *>(smem + P.off_d);
-        int2 *xs_cd = reinterpret_cast<int2 *>(smem + P.off_cd);
         StageCursor<MAXG> cur;
         cur.init(P, i0, i1, warp);
         for (int d = 0; d < D && cur.valid; ++d) {
@@ -791,28 +995,22 @@ __global__ void __launch_bounds__(max_warps_for(T) * 32, 1) qgemv_stream_kernel(
             const Group &g = P.g[gi_hint];
             const int K = g.K, nb = g.nb, N = g.N;
             const int e_run = static_cast<int>(ra - g.item_begin) / g.items_per_inst;
+            const XqLayout L = xq_layout(T, K);
+            const XqView xv{reinterpret_cast<const int8_t *>(smem), L.xstride,
+                            reinterpret_cast<const int2 *>(smem + L.off_cd), L.cdw};
 
             __syncthreads();
             if (tid == 0 && !*abort_flag) {
                 x_unconfirmed = true;
                 fence_proxy_async_smem();
-                const uint8_t *src = g.xq + static_cast<long long>(e_run) * g.xq_stride;
-                const unsigned qbytes = static_cast<unsigned>(T * K);
-                const unsigned dbytes = static_cast<unsigned>(g.xq_bytes) - qbytes;
-                mbar_arrive_expect_tx(xbar, qbytes + dbytes);
-                bulk_g2s(xs_q, src, qbytes, xbar, pol_x);
-                bulk_g2s(smem + P.off_d, src + qbytes, dbytes, xbar, pol_x);
+                const unsigned dbytes = static_cast<unsigned>(g.xq_bytes - T * K);
+                mbar_arrive_expect_tx(xbar, static_cast<unsigned>(T * K) + dbytes);
+                copy_activations<T>(smem, g.xq + static_cast<long long>(e_run) * g.xq_stride, K, dbytes, xbar, pol_x);
             }
             const bool xok = mbar_wait_bounded(xbar, xphase, abort_flag, P.status, WAIT_LIMIT_NS);
             if (xok) x_unconfirmed = false;
             xphase ^= 1u;
-            if (xok)
-                for (int i = tid; i < T * nb; i += nthreads) {
-                    const int t = i / nb, bb = i - t * nb;
-                    const uint4 *qp = reinterpret_cast<const uint4 *>(xs_q + t * K + bb * QK);
-                    xs_cd[i] = make_int2(block_fold16_const(qp[0], qp[1]),
-                                         __float_as_int(__fmul_rn(h2f(xs_d[i]), 0.0625f)));
-                }
+            if (xok) build_fold_constants<T>(smem, K, tid, nthreads);
             __syncthreads();
 
             for (long long it = ra + warp; it < rb; it += nw) {
@@ -821,33 +1019,29 @@ __global__ void __launch_bounds__(max_warps_for(T) * 32, 1) qgemv_stream_kernel(
                     if (lane == 0) atomicCAS(P.status, 0u, ST_BAD_ID);
                     continue;
                 }
-                const bool direct = P.ggml || inf.kind != 0;
+                const bool direct = ggml || inf.kind != 0;
                 const bool split = g.split > 1 && inf.kind == 0;  // a packed tail is never split
                 const uint8_t *rows_base =
                     inf.kind != 0 ? inf.Wi + static_cast<long long>(g.nslabs) * g.slab_bytes
                                   : inf.Wi + static_cast<long long>(inf.slab) * SLAB_ROWS * nb * Q4_BYTES;
-                float yv[2][T];
+                float yv[NO];
 #pragma unroll
-                for (int h = 0; h < 2; ++h)
-#pragma unroll
-                    for (int t = 0; t < T; ++t) yv[h][t] = 0.0f;
+                for (int k = 0; k < NO; ++k) yv[k] = 0.0f;
 
                 for (int sg = inf.seg0; sg < inf.seg1; ++sg) {
-                    float acc[2][T];
-#pragma unroll
-                    for (int h = 0; h < 2; ++h)
-#pragma unroll
-                        for (int t = 0; t < T; ++t) acc[h][t] = 0.0f;
+                    float Pk[NO];
+                    bool have = false;
                     if (direct) {
-                        if (xok) segment_from_ggml<T>(rows_base, inf.rows, sg, K, nb, r8, j, xs_q, xs_cd, acc);
+                        if (xok) {
+                            segment_sum<T>(false, nullptr, rows_base, inf.rows, sg, nb, r8, j, xv, Pk);
+                            have = true;
+                        }
                     } else {
                         const bool ok = mbar_wait_bounded(&ring.bar[ring.slot], ring.phase, abort_flag, P.status,
                                                           WAIT_LIMIT_NS);
                         if (ok && xok) {
-                            if (SEG_BLOCKS * (sg + 1) <= nb)
-                                segment_full_from_stage<T>(ring.stage(), sg, K, nb, r8, j, xs_q, xs_cd, acc);
-                            else
-                                segment_from_stage<T>(ring.stage(), sg, K, nb, r8, j, xs_q, xs_cd, acc);
+                            segment_sum<T>(true, ring.stage(), nullptr, 0, sg, nb, r8, j, xv, Pk);
+                            have = true;
                         }
                         __syncwarp();
                         const int aborted = __shfl_sync(0xFFFFFFFFu, *abort_flag, 0);
@@ -857,23 +1051,19 @@ __global__ void __launch_bounds__(max_warps_for(T) * 32, 1) qgemv_stream_kernel(
                         }
                         ring.pop();
                     }
-                    combine_phases<T>(acc);
+                    if (!have) {
+#pragma unroll
+                        for (int k = 0; k < NO; ++k) Pk[k] = 0.0f;
+                    }
                     if (split) {
                         float *pb =
                             g.part + ((static_cast<long long>(inf.e) * g.nslabs + inf.slab) * g.nseg + sg) * T * 16;
-                        if (j == 0) {
 #pragma unroll
-                            for (int t = 0; t < T; ++t) {
-                                pb[t * 16 + r8] = acc[0][t];
-                                pb[t * 16 + r8 + 8] = acc[1][t];
-                            }
-                        }
+                        for (int k = 0; k < NO; ++k)
+                            if (LO::owner(k, j)) pb[LO::tok(k, j) * 16 + LO::row(k, r8)] = Pk[k];
                     } else {
 #pragma unroll
-                        for (int h = 0; h < 2; ++h)
-#pragma unroll
-                            for (int t = 0; t < T; ++t)
-                                yv[h][t] = (sg == 0) ? acc[h][t] : __fadd_rn(yv[h][t], acc[h][t]);
+                        for (int k = 0; k < NO; ++k) yv[k] = (sg == 0) ? Pk[k] : __fadd_rn(yv[k], Pk[k]);
                     }
                 }
 
@@ -905,7 +1095,7 @@ __global__ void __launch_bounds__(max_warps_for(T) * 32, 1) qgemv_stream_kernel(
                         if (lane == 0) *cnt = 0u;
                     }
                 } else {
-                    store_rows<T, ARGMAX>(ye, N, row0, inf.rows, r8, j, yv, best);
+                    store_outputs<T, ARGMAX>(ye, N, row0, inf.rows, r8, j, yv, best);
                 }
             }
             ra = rb;

@@ -181,11 +181,10 @@ qgemv_status make_plan(const GroupSpec *gs, int n, int T, bool ggml, bool argmax
     // The activation area holds one run's activations in the run-synced mode
     // ([T][kmax] int8, fp16 scales, folded constants) and as many runs as fit
     // in the balanced mode.
-    const long long xsize = static_cast<long long>(T) * kmax;
-    const long long dsize = roundup16(2ll * T * nbmax);
-    P.off_d = static_cast<int>(xsize);
-    P.off_cd = static_cast<int>(align_up(xsize + dsize, 16));
-    const long long need_x = align_up(P.off_cd + 8ll * T * nbmax, 128);
+    long long need_x = 0;  // the largest single-run activation image
+    for (int i = 0; i < n; ++i) need_x = std::max<long long>(need_x, xq_layout(T, P.g[i].K).bytes);
+    P.off_d = 0;
+    P.off_cd = 0;
     const long long tables = align_up(static_cast<long long>(MAX_RUNS) * sizeof(RunInfo), 128) +
                              align_up(static_cast<long long>(NWARPS_MAX) * T * 16 * 4, 128) + 128;
     P.balanced_ok = 1;
@@ -241,7 +240,6 @@ cudaError_t dispatch_T(const Params<MAXG> &P, int T, int grid, size_t smem, cuda
 inline int ctas_per_sm_for(int T, bool sequence)
 {
     const int c = g_ctas_per_sm.load(std::memory_order_relaxed);
-    if (T > 2) return 1;  // 8 warps of wide accumulators fill the register file
     if (c >= 1 && c <= 2) return c;
     return sequence ? 2 : 1;  // measured: long lists gain from two CTAs per SM, single matrices do not
 }
