@@ -248,6 +248,20 @@ inline int smem_budget(const DevInfo &d, int ctas_per_sm)
     const int per = ctas_per_sm > 1 ? d.smem_per_sm / ctas_per_sm - 1024 : d.smem_optin;
     return per - 2048;
 }
+// Plan with the preferred CTAs per SM; if the activations do not fit two
+// CTAs' shared memory, one CTA per SM.
+template <int MAXG>
+qgemv_status plan_launch(const GroupSpec *gs, int n, int T, bool ggml, bool argmax, uint8_t *ws, const DevInfo &d,
+                         int &cps, Plan<MAXG> &pl)
+{
+    qgemv_status s = make_plan<MAXG>(gs, n, T, ggml, argmax, ws, smem_budget(d, cps), pl, cps);
+    if (s == QGEMV_ERR_UNSUPPORTED && cps > 1) {
+        cps = 1;
+        s = make_plan<MAXG>(gs, n, T, ggml, argmax, ws, smem_budget(d, cps), pl, cps);
+    }
+    return s;
+}
+
 inline int grid_for(const DevInfo &d, int ctas_per_sm)
 {
     const int w = g_waves.load(std::memory_order_relaxed);
@@ -294,9 +308,8 @@ qgemv_status run_single(const void *W, qgemv_wlayout layout, const void *xq, flo
     if (s != QGEMV_OK) return s;
     GroupSpec gs{W, 0, xq, 0, y, 0, N, K, 1};
     Plan<MAXG_SMALL> pl;
-    const int cps = ctas_per_sm_for(T, false);
-    s = make_plan<MAXG_SMALL>(&gs, 1, T, layout == QGEMV_W_GGML, argmax, static_cast<uint8_t *>(ws),
-                              smem_budget(dev, cps), pl, cps);
+    int cps = ctas_per_sm_for(T, false);
+    s = plan_launch<MAXG_SMALL>(&gs, 1, T, layout == QGEMV_W_GGML, argmax, static_cast<uint8_t *>(ws), dev, cps, pl);
     if (s != QGEMV_OK) return s;
     if (static_cast<long long>(ws_bytes) < pl.ws_bytes) return QGEMV_ERR_WORKSPACE;
     pl.P.status = dev.status;
@@ -496,8 +509,6 @@ static qgemv_status launch_seq(const qgemv_seq_item *items, const float *const *
     DevInfo dev;
     qgemv_status s = device_info(dev);
     if (s != QGEMV_OK) return s;
-    const int cps = ctas_per_sm_for(T, true);
-    const int grid = grid_for(dev, cps);
     std::vector<GroupSpec> gs(MAXG_SEQ);
     std::unique_ptr<Plan<MAXG_SEQ>> pl(new Plan<MAXG_SEQ>());
     std::unique_ptr<QuantList> ql(xs ? new QuantList() : nullptr);
@@ -507,8 +518,10 @@ static qgemv_status launch_seq(const qgemv_seq_item *items, const float *const *
             const qgemv_seq_item &it = items[c0 + i];
             gs[i] = GroupSpec{it.W, 0, it.xq, 0, it.y, 0, it.N, it.K, 1};
         }
-        s = make_plan<MAXG_SEQ>(gs.data(), cn, T, layout == QGEMV_W_GGML, false, static_cast<uint8_t *>(ws),
-                                smem_budget(dev, cps), *pl, cps);
+        int cps = ctas_per_sm_for(T, true);
+        s = plan_launch<MAXG_SEQ>(gs.data(), cn, T, layout == QGEMV_W_GGML, false, static_cast<uint8_t *>(ws), dev,
+                                  cps, *pl);
+        const int grid = grid_for(dev, cps);
         if (s != QGEMV_OK) return s;
         if (static_cast<long long>(ws_bytes) < pl->ws_bytes) return QGEMV_ERR_WORKSPACE;
         pl->P.status = dev.status;
@@ -651,9 +664,9 @@ qgemv_status qgemv_q4_0_gather(const qgemv_gather_matrix *mats, int n_mats, cons
     s = device_info(dev);
     if (s != QGEMV_OK) return s;
     Plan<MAXG_SMALL> pl;
-    const int cps = ctas_per_sm_for(T, false);
-    s = make_plan<MAXG_SMALL>(gs, n_mats, T, layout == QGEMV_W_GGML, false, static_cast<uint8_t *>(ws),
-                              smem_budget(dev, cps), pl, cps);
+    int cps = ctas_per_sm_for(T, false);
+    s = plan_launch<MAXG_SMALL>(gs, n_mats, T, layout == QGEMV_W_GGML, false, static_cast<uint8_t *>(ws), dev, cps,
+                                pl);
     if (s != QGEMV_OK) return s;
     if (static_cast<long long>(ws_bytes) < pl.ws_bytes) return QGEMV_ERR_WORKSPACE;
     pl.P.status = dev.status;
