@@ -31,8 +31,10 @@
  *                       (same byte count, 18*N*K/32).  Rows are grouped in
  *                       slabs of 16; a slab holds K/32 blocks for 16 rows in
  *                       "quads" of up to 4 blocks: first the 16 rows x 4
- *                       blocks of nibble bytes (row-major, 16 bytes each),
- *                       then their fp16 scales ([row r8 < 8][block][r8, r8+8]).
+ *                       blocks of nibble bytes (row-major, 16 bytes each;
+ *                       in a full quad, block jq of row r sits in chunk
+ *                       (jq + r/2) mod 4 of its row), then their fp16 scales
+ *                       ([row r8 < 8][block][r8, r8+8]).
  *                       The last N % 16 rows stay in GGML layout after the
  *                       slabs.
  *   xq (Q8_0, planar) : for R rows of K values, R*K int8 values ([r][k]),
@@ -262,13 +264,14 @@ qgemv_status qgemv_debug_block_isums(const void *W, qgemv_wlayout layout, const 
 qgemv_status qgemv_debug_stream_read(const void *src, size_t bytes, int method, int warps, int depth,
                                      int stage_bytes, unsigned long long *sink, qgemv_stream_t stream);
 
-/* Tuning: how the streaming kernel is launched.  ctas_per_sm = CTAs resident
- * per SM (1 = one CTA of up to 16 warps; 2 = two CTAs of 8 warps, T <= 2
- * only), waves = CTAs per SM slot in one launch (more, smaller CTAs let the
- * block scheduler hand more work to SMs that stream faster).  0 restores the
- * default for either.  Results do not depend on it (the summation order is
- * fixed by K).  Process-wide; affects launches enqueued afterwards. */
-qgemv_status qgemv_set_launch_shape(int ctas_per_sm, int waves);
+/* Tuning of the streaming kernel (0 restores the default for any of them;
+ * results never depend on it -- the summation order is fixed by K):
+ *   ctas_per_sm: CTAs resident per SM (1 = one CTA of up to 16 warps;
+ *                2 = two CTAs of 8 warps), waves: CTAs per SM slot in one
+ *                launch, mma_min_T: token count from which T > 1 runs on the
+ *                int8 tensor-core path (9 = never) instead of dp4a.
+ * Process-wide; affects launches enqueued afterwards. */
+qgemv_status qgemv_set_tuning(int ctas_per_sm, int waves, int mma_min_T);
 
 /* Read and clear the current device's status word: QGEMV_OK, or the first
  * asynchronous error a kernel recorded (QGEMV_ERR_TIMEOUT, QGEMV_ERR_BAD_ID)

@@ -208,9 +208,9 @@ struct StageCursor {
 // values after the phase combine and lane j == 0 writes.  MMA lanes (T > 1):
 // rows g and g + 8, tokens 2j and 2j + 1 -- the accumulator layout of
 // mma.m16n8k32 (element k: row g + 8 (k >> 1), token 2j + (k & 1)).
-template <int T>
+template <int T, bool MMA_>
 struct LaneOut {
-    static constexpr bool MMA = use_mma(T);
+    static constexpr bool MMA = MMA_;
     static constexpr int N = MMA ? 4 : 2 * T;
     __device__ static __forceinline__ int row(int k, int r8) { return MMA ? r8 + 8 * (k >> 1) : r8 + 8 * (k / T); }
     __device__ static __forceinline__ int tok(int k, int j) { return MMA ? 2 * j + (k & 1) : k % T; }
@@ -257,8 +257,9 @@ __device__ __forceinline__ void segment_from_stage(const uint8_t *stage, int s, 
         const int nbq = min(QUAD, nbs - QUAD * qq);
         if (j < nbq) {
             const uint8_t *q = stage + qq * QUAD_BYTES;
-            const uint4 n0 = *reinterpret_cast<const uint4 *>(q + (r8 * nbq + j) * 16);
-            const uint4 n1 = *reinterpret_cast<const uint4 *>(q + ((r8 + 8) * nbq + j) * 16);
+            const int c = quad_chunk(j, r8, nbq);  // rows r8 and r8 + 8 share the rotation
+            const uint4 n0 = *reinterpret_cast<const uint4 *>(q + (r8 * nbq + c) * 16);
+            const uint4 n1 = *reinterpret_cast<const uint4 *>(q + ((r8 + 8) * nbq + c) * 16);
             const unsigned sc = *reinterpret_cast<const unsigned *>(q + 256 * nbq + (r8 * nbq + j) * 4);
             fma_block<T>(n0, n1, h2f(sc), h2f(sc >> 16), SEG_BLOCKS * s + QUAD * qq + j, xv, acc);
         }
@@ -271,7 +272,7 @@ template <int T>
 __device__ __forceinline__ void segment_full_from_stage(const uint8_t *stage, int s, int r8, int j,
                                                         const XqView &xv, float (&acc)[2][T])
 {
-    const int lo = (r8 * QUAD + j) * 16;
+    const int lo = (r8 * QUAD + quad_chunk(j, r8, QUAD)) * 16;
     uint4 n0[4], n1[4];
     unsigned sc[4];
 #pragma unroll
@@ -377,8 +378,9 @@ __device__ __forceinline__ void mma_segment_from_stage(const uint8_t *stage, boo
             unsigned wg[4], wg8[4], sc[4];
 #pragma unroll
             for (int jq = 0; jq < 4; ++jq) {
-                wg[jq] = *reinterpret_cast<const unsigned *>(q + (g * QUAD + jq) * 16 + 4 * j);
-                wg8[jq] = *reinterpret_cast<const unsigned *>(q + ((g + 8) * QUAD + jq) * 16 + 4 * j);
+                const int c = quad_chunk(jq, g, QUAD);
+                wg[jq] = *reinterpret_cast<const unsigned *>(q + (g * QUAD + c) * 16 + 4 * j);
+                wg8[jq] = *reinterpret_cast<const unsigned *>(q + ((g + 8) * QUAD + c) * 16 + 4 * j);
                 sc[jq] = *reinterpret_cast<const unsigned *>(q + 256 * QUAD + (g * QUAD + jq) * 4);
             }
 #pragma unroll
@@ -395,8 +397,9 @@ __device__ __forceinline__ void mma_segment_from_stage(const uint8_t *stage, boo
 #pragma unroll
         for (int jq = 0; jq < 4; ++jq)
             if (jq < nbq) {  // warp-uniform
-                const unsigned wg = *reinterpret_cast<const unsigned *>(q + (g * nbq + jq) * 16 + 4 * j);
-                const unsigned wg8 = *reinterpret_cast<const unsigned *>(q + ((g + 8) * nbq + jq) * 16 + 4 * j);
+                const int c = quad_chunk(jq, g, nbq);
+                const unsigned wg = *reinterpret_cast<const unsigned *>(q + (g * nbq + c) * 16 + 4 * j);
+                const unsigned wg8 = *reinterpret_cast<const unsigned *>(q + ((g + 8) * nbq + c) * 16 + 4 * j);
                 const unsigned sc = *reinterpret_cast<const unsigned *>(q + 256 * nbq + (g * nbq + jq) * 4);
                 mma_block<T>(wg, wg8, sc, SEG_BLOCKS * s + QUAD * qq + jq, g, j, xv, acc[jq]);
             }
@@ -442,13 +445,13 @@ __device__ __forceinline__ void mma_segment_from_ggml(const uint8_t *rows_base, 
 // ------------------------------------------------------------------ either path
 
 // The ordered sum of one segment for this lane's outputs.
-template <int T>
+template <int T, bool MMA>
 __device__ __forceinline__ void segment_sum(bool from_stage, const uint8_t *stage, const uint8_t *rows_base, int rows,
                                             int s, int nb, int r8, int j, const XqView &xv,
-                                            float (&P)[LaneOut<T>::N])
+                                            float (&P)[LaneOut<T, MMA>::N])
 {
     const bool full = SEG_BLOCKS * (s + 1) <= nb;
-    if constexpr (use_mma(T)) {
+    if constexpr (MMA) {
         float acc[4][4];
 #pragma unroll
         for (int p = 0; p < 4; ++p)
@@ -485,10 +488,10 @@ __device__ __forceinline__ void segment_sum(bool from_stage, const uint8_t *stag
 // Builds one run's activation image in shared memory after its copy landed:
 // per block and token the folded constant and d_x / 16 (MMA path: tokens
 // past T get a constant that yields exactly 0).
-template <int T>
+template <int T, bool MMA>
 __device__ __forceinline__ void build_fold_constants(uint8_t *img, int K, int tid, int nthreads)
 {
-    const XqLayout L = xq_layout(T, K);
+    const XqLayout L = xq_layout(T, K, MMA);
     const int nb = K / QK;
     const int8_t *xq = reinterpret_cast<const int8_t *>(img);
     const unsigned short *xd = reinterpret_cast<const unsigned short *>(img + L.off_d);
@@ -506,11 +509,11 @@ __device__ __forceinline__ void build_fold_constants(uint8_t *img, int K, int ti
 
 // Copies one run's activations (planar Q8_0, T rows of K) into an image;
 // one copy per token row on the MMA path (padded rows).  Returns the bytes.
-template <int T>
+template <int T, bool MMA>
 __device__ __forceinline__ unsigned copy_activations(uint8_t *img, const uint8_t *src, int K, unsigned dbytes,
                                                      uint64_t *bar, uint64_t pol)
 {
-    const XqLayout L = xq_layout(T, K);
+    const XqLayout L = xq_layout(T, K, MMA);
     if (L.xstride == K) {
         bulk_g2s(img, src, static_cast<unsigned>(T * K), bar, pol);
     } else {
@@ -521,8 +524,10 @@ __device__ __forceinline__ unsigned copy_activations(uint8_t *img, const uint8_t
     return static_cast<unsigned>(T * K) + dbytes;
 }
 
-// Warps per CTA a T-token kernel may use (both paths fit 128 registers).
-__host__ __device__ constexpr int max_warps_for(int) { return NWARPS_MAX; }
+// Warps per CTA a T-token kernel may use: 16 (128 registers per thread),
+// except the dp4a path above two tokens, whose per-token accumulators need
+// more registers (8 warps).
+__host__ __device__ constexpr int max_warps_for(int T, bool mma) { return (mma || T <= 2) ? NWARPS_MAX : 8; }
 
 // ------------------------------------------------------------------ balanced mode
 //
@@ -704,11 +709,11 @@ struct Ring {
 
 // Write this lane's finished outputs (rows below `rows`) and fold them into
 // the argmax keys.
-template <int T, bool ARGMAX>
+template <int T, bool MMA, bool ARGMAX>
 __device__ __forceinline__ void store_outputs(float *ye, int N, int row0, int rows, int r8, int j,
-                                              const float (&yv)[LaneOut<T>::N], unsigned long long (&best)[T])
+                                              const float (&yv)[LaneOut<T, MMA>::N], unsigned long long (&best)[T])
 {
-    using LO = LaneOut<T>;
+    using LO = LaneOut<T, MMA>;
 #pragma unroll
     for (int k = 0; k < LO::N; ++k) {
         const int lr = LO::row(k, r8), t = LO::tok(k, j);
@@ -741,17 +746,17 @@ __device__ __forceinline__ bool wait_flag(volatile int *flag, volatile int *abor
     return true;
 }
 
-template <int T, int MAXG, bool ARGMAX>
-__global__ void __launch_bounds__(max_warps_for(T) * 32, 1) qgemv_stream_kernel(const __grid_constant__ Params<MAXG> P)
+template <int T, int MAXG, bool ARGMAX, bool MMA>
+__global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_kernel(const __grid_constant__ Params<MAXG> P)
 {
-    using LO = LaneOut<T>;
+    using LO = LaneOut<T, MMA>;
     constexpr int NO = LO::N;
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_abort;
     __shared__ int s_last;
     __shared__ int s_nruns;  // > 0: balanced mode with this many runs
     __shared__ int s_stages;
-    __shared__ unsigned long long s_best[max_warps_for(T) * T];
+    __shared__ unsigned long long s_best[max_warps_for(T, MMA) * T];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int nw = P.nwarps, nthreads = nw * 32;
@@ -816,7 +821,7 @@ __global__ void __launch_bounds__(max_warps_for(T) * 32, 1) qgemv_stream_kernel(
             R.nslabs = g.nslabs;
             R.xq_off = xoff;
             R.bad = bad;
-            xoff += xq_layout(T, g.K).bytes;
+            xoff += xq_layout(T, g.K, MMA).bytes;
             stages += R.nstages;
             nseg_max = max(nseg_max, g.nseg);
             ++nr;
@@ -888,7 +893,7 @@ __global__ void __launch_bounds__(max_warps_for(T) * 32, 1) qgemv_stream_kernel(
                 const RunInfo &R = runs[r];
                 const Group &g = P.g[R.gi];
                 const unsigned dbytes = static_cast<unsigned>(g.xq_bytes - T * R.K);
-                copy_activations<T>(smem + R.xq_off, g.xq + static_cast<long long>(R.e) * g.xq_stride, R.K, dbytes,
+                copy_activations<T, MMA>(smem + R.xq_off, g.xq + static_cast<long long>(R.e) * g.xq_stride, R.K, dbytes,
                                     xbar, pol_x);
             }
         }
@@ -896,7 +901,7 @@ __global__ void __launch_bounds__(max_warps_for(T) * 32, 1) qgemv_stream_kernel(
         xphase ^= 1u;
         if (xok) x_unconfirmed = false;
         if (xok)
-            for (int r = 0; r < nruns; ++r) build_fold_constants<T>(smem + runs[r].xq_off, runs[r].K, tid, nthreads);
+            for (int r = 0; r < nruns; ++r) build_fold_constants<T, MMA>(smem + runs[r].xq_off, runs[r].K, tid, nthreads);
         __syncthreads();
 
         // compute, one visit (the segments of one slab inside one interval) at a time
@@ -913,7 +918,7 @@ __global__ void __launch_bounds__(max_warps_for(T) * 32, 1) qgemv_stream_kernel(
             const int nb = w.nb;
             const int rows = tail_item ? P.g[R.gi].tail_rows : min(SLAB_ROWS, R.N - li * SLAB_ROWS);
             const uint8_t *rows_base = w.Wi + static_cast<long long>(li) * SLAB_ROWS * nb * Q4_BYTES;
-            const XqLayout L = xq_layout(T, R.K);
+            const XqLayout L = xq_layout(T, R.K, MMA);
             const XqView xv{reinterpret_cast<const int8_t *>(smem + R.xq_off), L.xstride,
                             reinterpret_cast<const int2 *>(smem + R.xq_off + L.off_cd), L.cdw};
             float yv[NO];
@@ -938,13 +943,13 @@ __global__ void __launch_bounds__(max_warps_for(T) * 32, 1) qgemv_stream_kernel(
                     // nothing is read for an out-of-range expert id
                 } else if (direct) {
                     if (ok) {
-                        segment_sum<T>(false, nullptr, rows_base, rows, sg, nb, r8, j, xv, Pk);
+                        segment_sum<T, MMA>(false, nullptr, rows_base, rows, sg, nb, r8, j, xv, Pk);
                         have = true;
                     }
                 } else {
                     if (ok) ok = mbar_wait_bounded(&ring.bar[ring.slot], ring.phase, abort_flag, P.status, WAIT_LIMIT_NS);
                     if (ok) {
-                        segment_sum<T>(true, ring.stage(), nullptr, 0, sg, nb, r8, j, xv, Pk);
+                        segment_sum<T, MMA>(true, ring.stage(), nullptr, 0, sg, nb, r8, j, xv, Pk);
                         have = true;
                     }
                     __syncwarp();
@@ -972,7 +977,7 @@ __global__ void __launch_bounds__(max_warps_for(T) * 32, 1) qgemv_stream_kernel(
                 __syncwarp();
                 if (lane == 0) hflag[warp] = 1;
             } else if (!w.bad) {
-                store_outputs<T, ARGMAX>(R.y, R.N, li * SLAB_ROWS, rows, r8, j, yv, best);
+                store_outputs<T, MMA, ARGMAX>(R.y, R.N, li * SLAB_ROWS, rows, r8, j, yv, best);
             } else if (lane == 0) {
                 atomicCAS(P.status, 0u, ST_BAD_ID);
             }
@@ -995,7 +1000,7 @@ __global__ void __launch_bounds__(max_warps_for(T) * 32, 1) qgemv_stream_kernel(
             const Group &g = P.g[gi_hint];
             const int K = g.K, nb = g.nb, N = g.N;
             const int e_run = static_cast<int>(ra - g.item_begin) / g.items_per_inst;
-            const XqLayout L = xq_layout(T, K);
+            const XqLayout L = xq_layout(T, K, MMA);
             const XqView xv{reinterpret_cast<const int8_t *>(smem), L.xstride,
                             reinterpret_cast<const int2 *>(smem + L.off_cd), L.cdw};
 
@@ -1005,12 +1010,12 @@ __global__ void __launch_bounds__(max_warps_for(T) * 32, 1) qgemv_stream_kernel(
                 fence_proxy_async_smem();
                 const unsigned dbytes = static_cast<unsigned>(g.xq_bytes - T * K);
                 mbar_arrive_expect_tx(xbar, static_cast<unsigned>(T * K) + dbytes);
-                copy_activations<T>(smem, g.xq + static_cast<long long>(e_run) * g.xq_stride, K, dbytes, xbar, pol_x);
+                copy_activations<T, MMA>(smem, g.xq + static_cast<long long>(e_run) * g.xq_stride, K, dbytes, xbar, pol_x);
             }
             const bool xok = mbar_wait_bounded(xbar, xphase, abort_flag, P.status, WAIT_LIMIT_NS);
             if (xok) x_unconfirmed = false;
             xphase ^= 1u;
-            if (xok) build_fold_constants<T>(smem, K, tid, nthreads);
+            if (xok) build_fold_constants<T, MMA>(smem, K, tid, nthreads);
             __syncthreads();
 
             for (long long it = ra + warp; it < rb; it += nw) {
@@ -1033,14 +1038,14 @@ __global__ void __launch_bounds__(max_warps_for(T) * 32, 1) qgemv_stream_kernel(
                     bool have = false;
                     if (direct) {
                         if (xok) {
-                            segment_sum<T>(false, nullptr, rows_base, inf.rows, sg, nb, r8, j, xv, Pk);
+                            segment_sum<T, MMA>(false, nullptr, rows_base, inf.rows, sg, nb, r8, j, xv, Pk);
                             have = true;
                         }
                     } else {
                         const bool ok = mbar_wait_bounded(&ring.bar[ring.slot], ring.phase, abort_flag, P.status,
                                                           WAIT_LIMIT_NS);
                         if (ok && xok) {
-                            segment_sum<T>(true, ring.stage(), nullptr, 0, sg, nb, r8, j, xv, Pk);
+                            segment_sum<T, MMA>(true, ring.stage(), nullptr, 0, sg, nb, r8, j, xv, Pk);
                             have = true;
                         }
                         __syncwarp();
@@ -1095,7 +1100,7 @@ __global__ void __launch_bounds__(max_warps_for(T) * 32, 1) qgemv_stream_kernel(
                         if (lane == 0) *cnt = 0u;
                     }
                 } else {
-                    store_outputs<T, ARGMAX>(ye, N, row0, inf.rows, r8, j, yv, best);
+                    store_outputs<T, MMA, ARGMAX>(ye, N, row0, inf.rows, r8, j, yv, best);
                 }
             }
             ra = rb;

@@ -2,7 +2,10 @@
 #include "launch_stream.cuh"
 
 namespace qg {
-template cudaError_t launch_stream<3, MAXG_SMALL, false>(const Params<MAXG_SMALL> &, int, size_t, cudaStream_t, bool);
-template cudaError_t launch_stream<3, MAXG_SMALL, true>(const Params<MAXG_SMALL> &, int, size_t, cudaStream_t, bool);
-template cudaError_t launch_stream<3, MAXG_SEQ, false>(const Params<MAXG_SEQ> &, int, size_t, cudaStream_t, bool);
+template cudaError_t launch_stream<3, MAXG_SMALL, false, false>(const Params<MAXG_SMALL> &, int, size_t, cudaStream_t, bool);
+template cudaError_t launch_stream<3, MAXG_SMALL, true, false>(const Params<MAXG_SMALL> &, int, size_t, cudaStream_t, bool);
+template cudaError_t launch_stream<3, MAXG_SEQ, false, false>(const Params<MAXG_SEQ> &, int, size_t, cudaStream_t, bool);
+template cudaError_t launch_stream<3, MAXG_SMALL, false, true>(const Params<MAXG_SMALL> &, int, size_t, cudaStream_t, bool);
+template cudaError_t launch_stream<3, MAXG_SMALL, true, true>(const Params<MAXG_SMALL> &, int, size_t, cudaStream_t, bool);
+template cudaError_t launch_stream<3, MAXG_SEQ, false, true>(const Params<MAXG_SEQ> &, int, size_t, cudaStream_t, bool);
 }  // namespace qg

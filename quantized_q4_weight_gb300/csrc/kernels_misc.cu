@@ -94,7 +94,8 @@ cudaError_t launch_quantize_list(const QuantList &L, cudaStream_t st)
 //
 // Packed layout (see include/qgemv.h): slab s of rows [16s, 16s+16) holds
 // quads q of nbq = min(4, nb - 4q) blocks at s * 288 * nb + 1152 * q:
-// nibbles [r][jq][16 bytes], then fp16 scales [r % 8][jq][r / 8].  Rows past
+// nibbles [r][chunk][16 bytes] with block jq in chunk quad_chunk(jq, r, nbq),
+// then fp16 scales [r % 8][jq][r / 8].  Rows past
 // the last full slab keep their GGML position, so the byte offset of their
 // blocks is the same in both layouts.
 
@@ -105,7 +106,7 @@ __device__ __forceinline__ void packed_offsets(long long row, int b, int nb, lon
     const int q = b / QUAD, jq = b - q * QUAD;
     const int nbq = min(QUAD, nb - q * QUAD);
     const long long base = s * static_cast<long long>(SLAB_COL_BYTES) * nb + static_cast<long long>(q) * QUAD_BYTES;
-    nib_off = base + (r * nbq + jq) * 16;
+    nib_off = base + (r * nbq + quad_chunk(jq, r, nbq)) * 16;
     sc_off = base + 256 * nbq + ((r % 8) * nbq + jq) * 4 + (r / 8) * 2;
 }
 

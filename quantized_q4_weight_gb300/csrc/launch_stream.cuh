@@ -9,10 +9,10 @@
 
 namespace qg {
 
-template <int T, int MAXG, bool ARGMAX>
+template <int T, int MAXG, bool ARGMAX, bool MMA>
 cudaError_t launch_stream(const Params<MAXG> &P, int grid, size_t smem, cudaStream_t st, bool pdl)
 {
-    auto kern = qgemv_stream_kernel<T, MAXG, ARGMAX>;
+    auto kern = qgemv_stream_kernel<T, MAXG, ARGMAX, MMA>;
     // The dynamic shared-memory limit is a per-device function attribute:
     // raise it once per device to the largest size any launch asks for.
     static std::atomic<unsigned long long> raised{0};

@@ -33,6 +33,15 @@ struct DevInfo {
 // 8 warps for T <= 2) and waves of CTAs per launch.  More, smaller CTAs let
 // the block scheduler give more work to SMs that stream faster.
 std::atomic<int> g_ctas_per_sm{0}, g_waves{0};
+// Token counts from which the int8 tensor-core path is used (0 = default).
+std::atomic<int> g_mma_min_T{0};
+constexpr int kDefaultMmaMinT = 2;
+
+inline bool mma_for(int T)
+{
+    const int m = g_mma_min_T.load(std::memory_order_relaxed);
+    return T >= 2 && T >= (m >= 2 ? m : kDefaultMmaMinT);
+}
 
 std::mutex g_dev_mu;
 DevInfo g_dev[kMaxDevices];
@@ -107,7 +116,7 @@ static_assert(CNT_AREA / 4 > SPLIT_SLAB_THRESHOLD, "split-K counters must fit th
 
 template <int MAXG>
 qgemv_status make_plan(const GroupSpec *gs, int n, int T, bool ggml, bool argmax, uint8_t *ws, int smem_limit,
-                       Plan<MAXG> &pl, int ctas_per_sm = 1)
+                       Plan<MAXG> &pl, int ctas_per_sm = 1, bool mma = false)
 {
     if (n < 1 || n > MAXG) return QGEMV_ERR_INTERNAL;
     Params<MAXG> &P = pl.P;
@@ -182,7 +191,7 @@ qgemv_status make_plan(const GroupSpec *gs, int n, int T, bool ggml, bool argmax
     // ([T][kmax] int8, fp16 scales, folded constants) and as many runs as fit
     // in the balanced mode.
     long long need_x = 0;  // the largest single-run activation image
-    for (int i = 0; i < n; ++i) need_x = std::max<long long>(need_x, xq_layout(T, P.g[i].K).bytes);
+    for (int i = 0; i < n; ++i) need_x = std::max<long long>(need_x, xq_layout(T, P.g[i].K, mma).bytes);
     P.off_d = 0;
     P.off_cd = 0;
     const long long tables = align_up(static_cast<long long>(MAX_RUNS) * sizeof(RunInfo), 128) +
@@ -193,7 +202,7 @@ qgemv_status make_plan(const GroupSpec *gs, int n, int T, bool ggml, bool argmax
     P.ring_depth = 0;
     // 2 stages per warp and the widest warp count that leaves room for the
     // activations; then 8 warps; then a single stage.
-    const int wide = ctas_per_sm > 1 ? 8 : max_warps_for(T);
+    const int wide = ctas_per_sm > 1 ? 8 : max_warps_for(T, mma);
     const int choices[3][2] = {{wide, 2}, {8, 2}, {8, 1}};
     for (const auto &c : choices) {
         const int nw = c[0], D = c[1];
@@ -220,19 +229,24 @@ qgemv_status make_plan(const GroupSpec *gs, int n, int T, bool ggml, bool argmax
 }
 
 template <int MAXG, bool ARGMAX>
-cudaError_t dispatch_T(const Params<MAXG> &P, int T, int grid, size_t smem, cudaStream_t st, bool pdl)
+cudaError_t dispatch_T(const Params<MAXG> &P, int T, bool mma, int grid, size_t smem, cudaStream_t st, bool pdl)
 {
+#define QG_CASE(t)                                                                                         \
+    case t:                                                                                                \
+        return mma ? launch_stream<t, MAXG, ARGMAX, true>(P, grid, smem, st, pdl)                          \
+                   : launch_stream<t, MAXG, ARGMAX, false>(P, grid, smem, st, pdl);
     switch (T) {
-    case 1: return launch_stream<1, MAXG, ARGMAX>(P, grid, smem, st, pdl);
-    case 2: return launch_stream<2, MAXG, ARGMAX>(P, grid, smem, st, pdl);
-    case 3: return launch_stream<3, MAXG, ARGMAX>(P, grid, smem, st, pdl);
-    case 4: return launch_stream<4, MAXG, ARGMAX>(P, grid, smem, st, pdl);
-    case 5: return launch_stream<5, MAXG, ARGMAX>(P, grid, smem, st, pdl);
-    case 6: return launch_stream<6, MAXG, ARGMAX>(P, grid, smem, st, pdl);
-    case 7: return launch_stream<7, MAXG, ARGMAX>(P, grid, smem, st, pdl);
-    case 8: return launch_stream<8, MAXG, ARGMAX>(P, grid, smem, st, pdl);
+    case 1: return launch_stream<1, MAXG, ARGMAX, false>(P, grid, smem, st, pdl);
+    QG_CASE(2)
+    QG_CASE(3)
+    QG_CASE(4)
+    QG_CASE(5)
+    QG_CASE(6)
+    QG_CASE(7)
+    QG_CASE(8)
     default: return cudaErrorInvalidValue;
     }
+#undef QG_CASE
 }
 
 // CTAs per SM for a T-token launch, and the dynamic shared-memory budget of
@@ -240,6 +254,7 @@ cudaError_t dispatch_T(const Params<MAXG> &P, int T, int grid, size_t smem, cuda
 inline int ctas_per_sm_for(int T, bool sequence)
 {
     const int c = g_ctas_per_sm.load(std::memory_order_relaxed);
+    if (!mma_for(T) && T > 2) return 1;  // 8 warps of wide accumulators fill the register file
     if (c >= 1 && c <= 2) return c;
     return sequence ? 2 : 1;  // measured: long lists gain from two CTAs per SM, single matrices do not
 }
@@ -254,10 +269,11 @@ template <int MAXG>
 qgemv_status plan_launch(const GroupSpec *gs, int n, int T, bool ggml, bool argmax, uint8_t *ws, const DevInfo &d,
                          int &cps, Plan<MAXG> &pl)
 {
-    qgemv_status s = make_plan<MAXG>(gs, n, T, ggml, argmax, ws, smem_budget(d, cps), pl, cps);
+    const bool mma = mma_for(T);
+    qgemv_status s = make_plan<MAXG>(gs, n, T, ggml, argmax, ws, smem_budget(d, cps), pl, cps, mma);
     if (s == QGEMV_ERR_UNSUPPORTED && cps > 1) {
         cps = 1;
-        s = make_plan<MAXG>(gs, n, T, ggml, argmax, ws, smem_budget(d, cps), pl, cps);
+        s = make_plan<MAXG>(gs, n, T, ggml, argmax, ws, smem_budget(d, cps), pl, cps, mma);
     }
     return s;
 }
@@ -315,8 +331,8 @@ qgemv_status run_single(const void *W, qgemv_wlayout layout, const void *xq, flo
     pl.P.status = dev.status;
     pl.P.am_idx = reinterpret_cast<long long *>(idx);
     const int grid = grid_for(dev, cps);
-    const cudaError_t e = argmax ? dispatch_T<MAXG_SMALL, true>(pl.P, T, grid, pl.smem, st, pdl)
-                                 : dispatch_T<MAXG_SMALL, false>(pl.P, T, grid, pl.smem, st, pdl);
+    const cudaError_t e = argmax ? dispatch_T<MAXG_SMALL, true>(pl.P, T, mma_for(T), grid, pl.smem, st, pdl)
+                                 : dispatch_T<MAXG_SMALL, false>(pl.P, T, mma_for(T), grid, pl.smem, st, pdl);
     return e == cudaSuccess ? QGEMV_OK : QGEMV_ERR_CUDA;
 }
 
@@ -537,7 +553,7 @@ static qgemv_status launch_seq(const qgemv_seq_item *items, const float *const *
             ql->total_blocks = blocks;
             if (launch_quantize_list(*ql, st) != cudaSuccess) return QGEMV_ERR_CUDA;
         }
-        if (dispatch_T<MAXG_SEQ, false>(pl->P, T, grid, pl->smem, st, xs != nullptr) != cudaSuccess)
+        if (dispatch_T<MAXG_SEQ, false>(pl->P, T, mma_for(T), grid, pl->smem, st, xs != nullptr) != cudaSuccess)
             return QGEMV_ERR_CUDA;
     }
     return QGEMV_OK;
@@ -673,7 +689,7 @@ qgemv_status qgemv_q4_0_gather(const qgemv_gather_matrix *mats, int n_mats, cons
     pl.P.ids = ids;
     pl.P.n_experts = n_experts;
     const int grid = grid_for(dev, cps);
-    return dispatch_T<MAXG_SMALL, false>(pl.P, T, grid, pl.smem, reinterpret_cast<cudaStream_t>(stream), false) ==
+    return dispatch_T<MAXG_SMALL, false>(pl.P, T, mma_for(T), grid, pl.smem, reinterpret_cast<cudaStream_t>(stream), false) ==
                    cudaSuccess
                ? QGEMV_OK
                : QGEMV_ERR_CUDA;
@@ -710,11 +726,13 @@ qgemv_status qgemv_debug_stream_read(const void *src, size_t bytes, int method, 
                : QGEMV_ERR_CUDA;
 }
 
-qgemv_status qgemv_set_launch_shape(int ctas_per_sm, int waves)
+qgemv_status qgemv_set_tuning(int ctas_per_sm, int waves, int mma_min_T)
 {
-    if (ctas_per_sm < 0 || ctas_per_sm > 2 || waves < 0 || waves > 6) return QGEMV_ERR_INVALID_ARG;
+    if (ctas_per_sm < 0 || ctas_per_sm > 2 || waves < 0 || waves > 6 || mma_min_T < 0 || mma_min_T > 9)
+        return QGEMV_ERR_INVALID_ARG;
     g_ctas_per_sm.store(ctas_per_sm);
     g_waves.store(waves);
+    g_mma_min_T.store(mma_min_T);
     return QGEMV_OK;
 }
 

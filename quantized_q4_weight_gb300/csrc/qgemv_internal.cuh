@@ -207,13 +207,18 @@ __device__ __forceinline__ void mbar_drain(uint64_t *bar, unsigned parity)
 
 __device__ __forceinline__ int roundup16_dev(int v) { return (v + 15) & ~15; }
 
-// T > 1 token columns run on int8 tensor cores (mma.sync m16n8k32, tokens as
-// the N dimension); one token runs on dp4a.
-__host__ __device__ constexpr bool use_mma(int T) { return T >= 2; }
+// Position of block jq's 16 nibble bytes among the nbq chunks of row r in a
+// quad tile.  Full quads rotate by r / 2, so that both the one-token lanes
+// (16-byte loads of one block, rows r and r + 8) and the tensor-core lanes
+// (word j of all four blocks) hit distinct shared-memory banks.
+__host__ __device__ __forceinline__ int quad_chunk(int jq, int r, int nbq)
+{
+    return nbq == QUAD ? ((jq + (r >> 1)) & 3) : jq;
+}
 
 // Shared-memory image of one GEMV's activations: T rows of K int8 (rows
-// padded on the MMA path so that the eight token rows fall in distinct
-// banks), the fp16 scales as copied, then per block and token the folded
+// padded on the tensor-core (MMA) path so that the eight token rows fall in
+// distinct banks), the fp16 scales as copied, then per block and token the folded
 // constant and d_x / 16 ({int, float} pairs, [block][T or 8]).
 struct XqLayout {
     int xstride;  // bytes between token rows
@@ -223,18 +228,18 @@ struct XqLayout {
     int bytes;    // whole image, 128-byte multiple
 };
 
-__host__ __device__ inline XqLayout xq_layout(int T, int K)
+__host__ __device__ inline XqLayout xq_layout(int T, int K, bool mma)
 {
     const int nb = K / QK;
     XqLayout L;
     L.xstride = K;
-    if (use_mma(T)) {
+    if (mma) {
         const int kw = K / 4;                    // words per row
         L.xstride = K + 4 * ((36 - (kw & 31)) & 31);  // words per row = 4 (mod 32)
     }
     L.off_d = T * L.xstride;
     L.off_cd = (L.off_d + 2 * T * nb + 15) & ~15;
-    L.cdw = use_mma(T) ? 8 : T;
+    L.cdw = mma ? 8 : T;
     L.bytes = (L.off_cd + 8 * L.cdw * nb + 127) & ~127;
     return L;
 }

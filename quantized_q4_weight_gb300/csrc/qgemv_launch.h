@@ -36,8 +36,8 @@ cudaError_t launch_isums(const void *W, bool packed, const void *xq, int32_t *is
                          cudaStream_t st);
 
 // The streaming GEMV kernel, one instantiation per (T, parameter-block size,
-// argmax).  Defined in gemv_t<T>.cu.
-template <int T, int MAXG, bool ARGMAX>
+// argmax, tensor-core path).  Defined in gemv_t<T>.cu.
+template <int T, int MAXG, bool ARGMAX, bool MMA>
 cudaError_t launch_stream(const Params<MAXG> &P, int grid, size_t smem, cudaStream_t st, bool pdl);
 
 }  // namespace qg

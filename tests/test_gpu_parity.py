@@ -99,7 +99,8 @@ def test_pack_roundtrip_and_layout(orc, N, K):
             for r in range(16):
                 for jq in range(nbq):
                     b = 4 * qd + jq
-                    o = qb + (r * nbq + jq) * 16
+                    c = ((jq + (r >> 1)) & 3) if nbq == 4 else jq     # full quads rotate by r // 2
+                    o = qb + (r * nbq + c) * 16
                     assert np.array_equal(got[o:o + 16], blk[16 * s + r, b, 2:])
                     so = qb + 256 * nbq + ((r % 8) * nbq + jq) * 4 + (r // 8) * 2
                     assert np.array_equal(got[so:so + 2], blk[16 * s + r, b, :2])
@@ -389,3 +390,26 @@ def test_seq_f32_equals_quantize_then_seq(orc):
     assert q.device_status() == 0
     for a, b in zip(ys_f, ys_q):
         assert torch.equal(a.cpu().view(torch.int32), b.cpu().view(torch.int32))
+
+
+@pytest.mark.parametrize("N,K", [(40, 1536), (17, 544), (300, 2080), (33, 8960)])
+@pytest.mark.parametrize("T", [2, 3, 8])
+def test_dp4a_and_tensor_core_paths_bit_identical(orc, N, K, T):
+    """T > 1 runs on the int8 tensor-core path or on dp4a (a tuning choice);
+    both must give the same bits, and the split / unsplit launches too."""
+    Wg, Wp = weights(600 + N + K, N, K, q.W_PACKED)
+    x, xd, xq = quantized(650 + N + T, T, K)
+    outs = []
+    try:
+        for mma_min in (9, 2):
+            q.set_tuning(0, 0, mma_min)
+            outs.append(q.gemv(Wp, q.W_PACKED, xq, N, K, T, ws_for(N, K, T)).cpu())
+            items = q.seq_items([(Wp, xq, torch.empty((T, N), dtype=torch.float32, device=DEV), N, K)
+                                 for _ in range(2100 // max(1, N // 16) + 1)])
+            q.gemv_seq(items, q.W_PACKED, T, q.new_workspace(q.seq_workspace_bytes(items, T)))
+            torch.cuda.synchronize()
+    finally:
+        q.set_tuning(0, 0, 0)
+    assert torch.equal(outs[0].view(torch.int32), outs[1].view(torch.int32))
+    y64, S = orc.gemv(Wg, N, K, orc.quantize(x), T)
+    check_close(outs[1].numpy(), y64, S, f"paths N={N} K={K} T={T}")
