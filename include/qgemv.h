@@ -269,7 +269,8 @@ qgemv_status qgemv_debug_stream_read(const void *src, size_t bytes, int method, 
  *   ctas_per_sm: CTAs resident per SM (1 = one CTA of up to 16 warps;
  *                2 = two CTAs of 8 warps), waves: CTAs per SM slot in one
  *                launch, mma_min_T: token count from which T > 1 runs on the
- *                int8 tensor-core path (9 = never) instead of dp4a.
+ *                f16 tensor-core path (mma.sync m16n8k16 over exact
+ *                integer operands; default 5, 9 = never) instead of dp4a.
  * Process-wide; affects launches enqueued afterwards. */
 qgemv_status qgemv_set_tuning(int ctas_per_sm, int waves, int mma_min_T);
 

@@ -207,7 +207,7 @@ struct StageCursor {
 // r8 + 8 of the slab, every token; the four lanes of a row pair hold equal
 // values after the phase combine and lane j == 0 writes.  MMA lanes (T > 1):
 // rows g and g + 8, tokens 2j and 2j + 1 -- the accumulator layout of
-// mma.m16n8k32 (element k: row g + 8 (k >> 1), token 2j + (k & 1)).
+// mma.m16n8k16 (element k: row g + 8 (k >> 1), token 2j + (k & 1)).
 template <int T, bool MMA_>
 struct LaneOut {
     static constexpr bool MMA = MMA_;
@@ -220,7 +220,7 @@ struct LaneOut {
 struct XqView {
     const int8_t *q;   // token rows at q + t * xstride
     int xstride;
-    const int2 *cd;    // [block][cdw] {folded constant, d_x / 16}
+    const int2 *cd;    // per block: cdw {folded constant, activation scale} pairs (MMA: token-pair order)
     int cdw;
 };
 
@@ -327,43 +327,240 @@ __device__ __forceinline__ void combine_phases(float (&acc)[2][T])
 
 // ------------------------------------------------------------------ MMA path (T > 1)
 //
-// One mma.sync.m16n8k32 (u8 x s8 -> s32) per block forms the 16 x 8 integer
-// block sums (16 rows of the slab, 8 token columns, zero past T).  Lane
-// (g, j) supplies word j of rows g and g + 8 (elements 4j..4j+3 in the low
-// nibbles, 16+4j..16+4j+3 in the high nibbles, both masked as 16 n) and
-// activation words j and 4 + j of token g; the accumulator starts at the
-// folded constant, so the result is MAGIC + 16 isum as on the dp4a path.
-// The lane keeps one fp32 sum per block phase (b % 4) and output, and the
-// same fused multiply-adds in the same order as a dp4a lane would.
+// Two mma.sync.m16n8k16 (f16 x f16 -> f32) per block form the 16 x 8 block
+// sums (16 rows of the slab, 8 token columns, zero past T).  Every operand is
+// a small integer (or an integer / 16) held exactly in f16, and every partial
+// sum is an integer below 2^22, so the fp32 accumulator holds the exact isum.
+//
+// Lane (g, j) supplies word j of rows g and g + 8 (bytes 4j..4j+3: elements
+// 4j..4j+3 in the low nibbles, 16+4j..16+4j+3 in the high nibbles) and
+// activation words j and 4 + j of token g.  The k index of the first MMA
+// runs over the low-nibble elements in the order 4j, 4j+2 (k = 2j, 2j+1) and
+// 4j+1, 4j+3 (k = 2j+8, 2j+9); the second MMA the same over the high nibbles.
+//   low nibbles:  A = 1024 + n   (one LOP3: n | 0x6400),      B = q
+//   high nibbles: A = 1024 + 16 n (one LOP3: 16n | 0x6400),   B = q / 16
+// so the MMAs add isum + 1032 sum(q_lo) + 72 sum(q_hi); the accumulator
+// starts at C = -(1032 sum(q_lo) + 72 sum(q_hi)) (per token and block) and
+// ends at isum.  Activations arrive as f16 1024 + (q xor 0x80) (one LOP3)
+// and one f16x2 add (or fma by 1/16) recovers q (or q / 16) exactly.
+// The lane keeps one fp32 sum per block phase (b % 4) and output and adds
+// (d_w * d_x) * isum with one fused multiply-add: the dp4a lanes' product
+// (d_w * (d_x / 16)) * (16 isum) is the same real number, rounded the same.
 
-__device__ __forceinline__ void mma_u8s8(int (&d)[4], unsigned a0, unsigned a1, unsigned a2, unsigned a3,
-                                         unsigned b0, unsigned b1)
+__device__ __forceinline__ void mma_f16(float (&d)[4], unsigned a0, unsigned a1, unsigned a2, unsigned a3,
+                                        unsigned b0, unsigned b1)
 {
-    asm volatile(
-        "mma.sync.aligned.m16n8k32.row.col.s32.u8.s8.s32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
-        : "+r"(d[0]), "+r"(d[1]), "+r"(d[2]), "+r"(d[3])
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ unsigned hadd2_u(unsigned a, unsigned b)
+{
+    unsigned d;
+    asm("add.rn.f16x2 %0, %1, %2;" : "=r"(d) : "r"(a), "r"(b));
+    return d;
+}
+
+__device__ __forceinline__ unsigned hfma2_u(unsigned a, unsigned b, unsigned c)
+{
+    unsigned d;
+    asm("fma.rn.f16x2 %0, %1, %2, %3;" : "=r"(d) : "r"(a), "r"(b), "r"(c));
+    return d;
+}
+
+constexpr unsigned H2_1024 = 0x64006400u;      // f16x2 (1024, 1024)
+constexpr unsigned H2_Q_BIAS = 0x64806480u;    // f16x2 1152: 1024 + (q xor 0x80) = 1152 + q
+constexpr unsigned H2_NEG_1152 = 0xE480E480u;  // f16x2 (-1152, -1152)
+constexpr unsigned H2_SIXTEENTH = 0x2C002C00u; // f16x2 (1/16, 1/16)
+constexpr unsigned H2_NEG_72 = 0xD480D480u;    // f16x2 (-72, -72): (1152 + q) / 16 - 72 = q / 16
+
+// Activation bytes 0, 2 (even) or 1, 3 (odd) of a word of the biased image
+// (bytes q xor 0x80) as f16x2 1024 + (q xor 0x80) = 1152 + q.
+__device__ __forceinline__ unsigned act_even(unsigned w) { return __byte_perm(w, 0x64646464u, 0x4240); }
+__device__ __forceinline__ unsigned act_odd(unsigned w) { return __byte_perm(w, 0x64646464u, 0x4341); }
+
+// d0 += c0, d1 += c1 (add.rn.f32x2).
+__device__ __forceinline__ void fadd2(float &d0, float &d1, float c0, float c1)
+{
+    asm("{\n\t.reg .b64 ra, rc;\n\t"
+        "mov.b64 ra, {%0, %1};\n\t"
+        "mov.b64 rc, {%2, %3};\n\t"
+        "add.rn.f32x2 ra, ra, rc;\n\t"
+        "mov.b64 {%0, %1}, ra;\n\t}"
+        : "+f"(d0), "+f"(d1)
+        : "f"(c0), "f"(c1));
+}
+
+// acc0 += s0 * d0, acc1 += s1 * d1: one fma.rn.f32x2 (two IEEE fused
+// multiply-adds, rounded as two fma.rn.f32 would be).
+__device__ __forceinline__ void ffma2(float &a0, float &a1, float s0, float s1, float d0, float d1)
+{
+    asm("{\n\t.reg .b64 ra, rs, rd;\n\t"
+        "mov.b64 ra, {%0, %1};\n\t"
+        "mov.b64 rs, {%2, %3};\n\t"
+        "mov.b64 rd, {%4, %5};\n\t"
+        "fma.rn.f32x2 ra, rs, rd, ra;\n\t"
+        "mov.b64 {%0, %1}, ra;\n\t}"
+        : "+f"(a0), "+f"(a1)
+        : "f"(s0), "f"(s1), "f"(d0), "f"(d1));
+}
+
+// Both fp16 halves of a word as fp32 (exact).
+__device__ __forceinline__ void h2f2(unsigned w, float &lo, float &hi)
+{
+    asm("{\n\t.reg .b16 l, h;\n\t"
+        "mov.b32 {l, h}, %2;\n\t"
+        "cvt.f32.f16 %0, l;\n\t"
+        "cvt.f32.f16 %1, h;\n\t}"
+        : "=f"(lo), "=f"(hi)
+        : "r"(w));
+}
+
+// Four 8 x 8 b16 matrices from shared memory; lane l gives the address of
+// row l & 7 of matrix l >> 3 and receives word l & 3 of row l >> 2 of each.
+__device__ __forceinline__ void ldsm_x4(unsigned &r0, unsigned &r1, unsigned &r2, unsigned &r3, uint32_t addr)
+{
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+                 : "r"(addr));
+}
+
+__device__ __forceinline__ float4 lds_f4(uint32_t addr)
+{
+    float4 v;
+    asm volatile("ld.shared.v4.f32 {%0, %1, %2, %3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w) : "r"(addr));
+    return v;
+}
+
+__device__ __forceinline__ uint4 lds_u4(uint32_t addr)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(addr));
+    return v;
+}
+
+// One block for this lane's four outputs from its words: weight word j of
+// rows g and g + 8 (wg, wg8), biased activation words j and 4 + j of token g
+// (ql, qh), the rows' fp16 scales (sc) and the block constants
+// {C(2j), C(2j+1), d_x(2j), d_x(2j+1)}.
+__device__ __forceinline__ void mma_block_words(unsigned wg, unsigned wg8, unsigned ql, unsigned qh, unsigned sc,
+                                                const float4 &cd, float (&acc)[4])
+{
+    const unsigned bl0 = hadd2_u(act_even(ql), H2_NEG_1152);
+    const unsigned bl1 = hadd2_u(act_odd(ql), H2_NEG_1152);
+    const unsigned bh0 = hfma2_u(act_even(qh), H2_SIXTEENTH, H2_NEG_72);
+    const unsigned bh1 = hfma2_u(act_odd(qh), H2_SIXTEENTH, H2_NEG_72);
+    const unsigned g1 = wg >> 8, g9 = wg8 >> 8;
+    float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+    mma_f16(d, (wg & 0x000F000Fu) | H2_1024, (wg8 & 0x000F000Fu) | H2_1024, (g1 & 0x000F000Fu) | H2_1024,
+            (g9 & 0x000F000Fu) | H2_1024, bl0, bl1);
+    mma_f16(d, (wg & 0x00F000F0u) | H2_1024, (wg8 & 0x00F000F0u) | H2_1024, (g1 & 0x00F000F0u) | H2_1024,
+            (g9 & 0x00F000F0u) | H2_1024, bh0, bh1);
+    fadd2(d[0], d[1], cd.x, cd.y);  // exact: integers below 2^23
+    fadd2(d[2], d[3], cd.x, cd.y);
+    float dw0, dw1;
+    h2f2(sc, dw0, dw1);
+    ffma2(acc[0], acc[1], __fmul_rn(dw0, cd.z), __fmul_rn(dw0, cd.w), d[0], d[1]);
+    ffma2(acc[2], acc[3], __fmul_rn(dw1, cd.z), __fmul_rn(dw1, cd.w), d[2], d[3]);
+}
+
+// The block's constants for tokens 2j and 2j + 1: {C(2j), C(2j+1), d_x(2j), d_x(2j+1)}.
+__device__ __forceinline__ float4 mma_block_consts(const XqView &xv, int b, int j)
+{
+    return *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(xv.cd) + b * 16 + 4 * j);
 }
 
 template <int T>
 __device__ __forceinline__ void mma_block(unsigned wg, unsigned wg8, unsigned sc, int b, int g, int j,
                                           const XqView &xv, float (&acc)[4])
 {
-    unsigned b0 = 0, b1 = 0;
-    if (g < T) {
-        const unsigned *xr = reinterpret_cast<const unsigned *>(xv.q + g * xv.xstride + b * QK);
-        b0 = xr[j];
-        b1 = xr[4 + j];
+    // Token columns past T read token T - 1: a column of B only reaches its
+    // own outputs, which no lane stores.
+    const int tg = T == 8 ? g : min(g, T - 1);
+    const unsigned *xr = reinterpret_cast<const unsigned *>(xv.q + tg * xv.xstride + b * QK);
+    mma_block_words(wg, wg8, xr[j], xr[4 + j], sc, mma_block_consts(xv, b, j), acc);
+}
+
+// A full segment from a stage in the packed layout, with ldmatrix: per quad
+// one x4 load brings weight word j of rows g and g + 8 of two blocks, one
+// more the other two blocks, and two more the activation words of the four
+// blocks.  Lane l names, for the weights, row (l & 7) + 8 ((l >> 3) & 1) of
+// block l >> 4 (+ 2 in the second load); for the activations, token
+// min(l & 7, T - 1) of block l >> 4 (+ 2), bytes 16 ((l >> 3) & 1) onwards.
+// The rotation keeps each group of eight 16-byte rows in distinct banks.
+// Warps per CTA a T-token kernel may use: 16 (128 registers per thread),
+// except the dp4a path above two tokens and the MMA path above four, whose
+// per-token accumulators or pipelined operands want more registers (8 warps,
+// up to 255 registers).
+__host__ __device__ constexpr int max_warps_for(int T, bool mma) { return (mma ? T <= 4 : T <= 2) ? NWARPS_MAX : 8; }
+
+// The operands of one quad of a full segment (see mma_segment_full_ldsm).
+struct MmaQuad {
+    unsigned w[8], x[8];
+    uint4 sc;
+    float4 cd[4];
+};
+
+__device__ __forceinline__ void mma_quad_load(MmaQuad &o, uint32_t a1, uint32_t a2, uint32_t asc, uint32_t xa, uint32_t ca,
+                                              int qq)
+{
+    ldsm_x4(o.w[0], o.w[1], o.w[2], o.w[3], a1 + qq * QUAD_BYTES);
+    ldsm_x4(o.w[4], o.w[5], o.w[6], o.w[7], a2 + qq * QUAD_BYTES);
+    ldsm_x4(o.x[0], o.x[1], o.x[2], o.x[3], xa + qq * QUAD * QK);
+    ldsm_x4(o.x[4], o.x[5], o.x[6], o.x[7], xa + qq * QUAD * QK + 2 * QK);
+    o.sc = lds_u4(asc + qq * QUAD_BYTES);
+#pragma unroll
+    for (int jq = 0; jq < QUAD; ++jq) o.cd[jq] = lds_f4(ca + (qq * QUAD + jq) * 64);
+}
+
+__device__ __forceinline__ void mma_quad_compute(const MmaQuad &o, float (&acc)[4][4])
+{
+    mma_block_words(o.w[0], o.w[1], o.x[0], o.x[1], o.sc.x, o.cd[0], acc[0]);
+    mma_block_words(o.w[2], o.w[3], o.x[2], o.x[3], o.sc.y, o.cd[1], acc[1]);
+    mma_block_words(o.w[4], o.w[5], o.x[4], o.x[5], o.sc.z, o.cd[2], acc[2]);
+    mma_block_words(o.w[6], o.w[7], o.x[6], o.x[7], o.sc.w, o.cd[3], acc[3]);
+}
+
+// A full segment from a stage in the packed layout, with ldmatrix: per quad
+// one x4 load brings weight word j of rows g and g + 8 of two blocks, one
+// more the other two blocks, and two more the activation words of the four
+// blocks.  Lane l names, for the weights, row (l & 7) + 8 ((l >> 3) & 1) of
+// block l >> 4 (+ 2 in the second load); for the activations, token
+// min(l & 7, T - 1) of block l >> 4 (+ 2), bytes 16 ((l >> 3) & 1) onwards.
+// The rotation keeps each group of eight 16-byte rows in distinct banks.
+// With the larger register budget (8 warps) the next quad's operands load
+// while the current quad computes.
+template <int T>
+__device__ __forceinline__ void mma_segment_full_ldsm(const uint8_t *stage, int s, int g, int j, const XqView &xv,
+                                                      float (&acc)[4][4])
+{
+    const int lane = threadIdx.x & 31;
+    const int m = lane >> 3, rr = lane & 7;
+    const int row = rr + 8 * (m & 1), rot = rr >> 1;
+    const uint32_t st = smem_addr(stage);
+    const uint32_t a1 = st + (row * QUAD + (((m >> 1) + rot) & 3)) * 16;
+    const uint32_t a2 = st + (row * QUAD + (((m >> 1) + 2 + rot) & 3)) * 16;
+    const uint32_t asc = st + 256 * QUAD + g * 16;
+    const int tok = T == 8 ? rr : min(rr, T - 1);
+    const uint32_t xa = smem_addr(xv.q + tok * xv.xstride + SEG_BLOCKS * QK * s + (m >> 1) * QK + (m & 1) * 16);
+    const uint32_t ca = smem_addr(reinterpret_cast<const float *>(xv.cd) + SEG_BLOCKS * 16 * s + 4 * j);
+    if constexpr (max_warps_for(T, true) <= 8) {
+        MmaQuad o[2];
+        mma_quad_load(o[0], a1, a2, asc, xa, ca, 0);
+#pragma unroll
+        for (int qq = 0; qq < SEG_BLOCKS / QUAD; ++qq) {
+            if (qq + 1 < SEG_BLOCKS / QUAD) mma_quad_load(o[(qq + 1) & 1], a1, a2, asc, xa, ca, qq + 1);
+            mma_quad_compute(o[qq & 1], acc);
+        }
+    } else {
+#pragma unroll 1
+        for (int qq = 0; qq < SEG_BLOCKS / QUAD; ++qq) {
+            MmaQuad o;
+            mma_quad_load(o, a1, a2, asc, xa, ca, qq);
+            mma_quad_compute(o, acc);
+        }
     }
-    const int4 cd = *reinterpret_cast<const int4 *>(xv.cd + b * 8 + 2 * j);  // tokens 2j, 2j + 1
-    int d[4] = {cd.x, cd.z, cd.x, cd.z};
-    mma_u8s8(d, (wg << 4) & 0xF0F0F0F0u, (wg8 << 4) & 0xF0F0F0F0u, wg & 0xF0F0F0F0u, wg8 & 0xF0F0F0F0u, b0, b1);
-    const float dw0 = h2f(sc), dw1 = h2f(sc >> 16);
-    const float dx0 = __int_as_float(cd.y), dx1 = __int_as_float(cd.w);
-    acc[0] = __fmaf_rn(__fmul_rn(dw0, dx0), magic_to_float(d[0]), acc[0]);
-    acc[1] = __fmaf_rn(__fmul_rn(dw0, dx1), magic_to_float(d[1]), acc[1]);
-    acc[2] = __fmaf_rn(__fmul_rn(dw1, dx0), magic_to_float(d[2]), acc[2]);
-    acc[3] = __fmaf_rn(__fmul_rn(dw1, dx1), magic_to_float(d[3]), acc[3]);
 }
 
 // One segment from a stage; `full` segments (16 blocks) take the branch-free form.
@@ -372,21 +569,7 @@ __device__ __forceinline__ void mma_segment_from_stage(const uint8_t *stage, boo
                                                        const XqView &xv, float (&acc)[4][4])
 {
     if (full) {
-#pragma unroll 1
-        for (int qq = 0; qq < 4; ++qq) {  // one quad's loads in flight at a time (register budget)
-            const uint8_t *q = stage + qq * QUAD_BYTES;
-            unsigned wg[4], wg8[4], sc[4];
-#pragma unroll
-            for (int jq = 0; jq < 4; ++jq) {
-                const int c = quad_chunk(jq, g, QUAD);
-                wg[jq] = *reinterpret_cast<const unsigned *>(q + (g * QUAD + c) * 16 + 4 * j);
-                wg8[jq] = *reinterpret_cast<const unsigned *>(q + ((g + 8) * QUAD + c) * 16 + 4 * j);
-                sc[jq] = *reinterpret_cast<const unsigned *>(q + 256 * QUAD + (g * QUAD + jq) * 4);
-            }
-#pragma unroll
-            for (int jq = 0; jq < 4; ++jq)
-                mma_block<T>(wg[jq], wg8[jq], sc[jq], SEG_BLOCKS * s + QUAD * qq + jq, g, j, xv, acc[jq]);
-        }
+        mma_segment_full_ldsm<T>(stage, s, g, j, xv, acc);
         return;
     }
     const int nbs = min(SEG_BLOCKS, nb - SEG_BLOCKS * s);
@@ -486,21 +669,51 @@ __device__ __forceinline__ void segment_sum(bool from_stage, const uint8_t *stag
 }
 
 // Builds one run's activation image in shared memory after its copy landed:
-// per block and token the folded constant and d_x / 16 (MMA path: tokens
-// past T get a constant that yields exactly 0).
+// per block and token the folded constant and the activation scale.  dp4a
+// path: {MAGIC - 128 sum(q), d_x / 16} per token; MMA path: the activation
+// bytes are rewritten as q xor 0x80, and per token pair
+// (2p, 2p + 1) {C(2p), C(2p+1), d_x(2p), d_x(2p+1)} with C = -(1032 sum(q_lo)
+// + 72 sum(q_hi)) as fp32, and zeros for the token columns past T.
 template <int T, bool MMA>
 __device__ __forceinline__ void build_fold_constants(uint8_t *img, int K, int tid, int nthreads)
 {
     const XqLayout L = xq_layout(T, K, MMA);
     const int nb = K / QK;
     const int8_t *xq = reinterpret_cast<const int8_t *>(img);
+    int8_t *xq_w = reinterpret_cast<int8_t *>(img);
     const unsigned short *xd = reinterpret_cast<const unsigned short *>(img + L.off_d);
     int2 *cd = reinterpret_cast<int2 *>(img + L.off_cd);
     for (int i = tid; i < L.cdw * nb; i += nthreads) {
         const int b = i / L.cdw, t = i - b * L.cdw;
         if (t < T) {
             const uint4 *qp = reinterpret_cast<const uint4 *>(xq + t * L.xstride + b * QK);
-            cd[i] = make_int2(block_fold16_const(qp[0], qp[1]), __float_as_int(__fmul_rn(h2f(xd[t * nb + b]), 0.0625f)));
+            const float dx = h2f(xd[t * nb + b]);
+            if constexpr (MMA) {
+                const uint4 qa = qp[0], qb = qp[1];
+                uint4 *qw = reinterpret_cast<uint4 *>(xq_w + t * L.xstride + b * QK);
+                const unsigned flip = 0x80808080u;  // the MMA operands read q xor 0x80
+                qw[0] = make_uint4(qa.x ^ flip, qa.y ^ flip, qa.z ^ flip, qa.w ^ flip);
+                qw[1] = make_uint4(qb.x ^ flip, qb.y ^ flip, qb.z ^ flip, qb.w ^ flip);
+                const int ones = 0x01010101;
+                int slo = 0, shi = 0;
+                slo = dp4a_ss((int)qa.x, ones, slo);
+                slo = dp4a_ss((int)qa.y, ones, slo);
+                slo = dp4a_ss((int)qa.z, ones, slo);
+                slo = dp4a_ss((int)qa.w, ones, slo);
+                shi = dp4a_ss((int)qb.x, ones, shi);
+                shi = dp4a_ss((int)qb.y, ones, shi);
+                shi = dp4a_ss((int)qb.z, ones, shi);
+                shi = dp4a_ss((int)qb.w, ones, shi);
+                float *cp = reinterpret_cast<float *>(cd) + b * 16 + 4 * (t >> 1) + (t & 1);
+                cp[0] = static_cast<float>(-(1032 * slo + 72 * shi));
+                cp[2] = dx;
+            } else {
+                cd[i] = make_int2(block_fold16_const(qp[0], qp[1]), __float_as_int(__fmul_rn(dx, 0.0625f)));
+            }
+        } else if constexpr (MMA) {
+            float *cp = reinterpret_cast<float *>(cd) + b * 16 + 4 * (t >> 1) + (t & 1);
+            cp[0] = 0.0f;
+            cp[2] = 0.0f;
         } else {
             cd[i] = make_int2(MAGIC_I, 0);
         }
@@ -524,10 +737,6 @@ __device__ __forceinline__ unsigned copy_activations(uint8_t *img, const uint8_t
     return static_cast<unsigned>(T * K) + dbytes;
 }
 
-// Warps per CTA a T-token kernel may use: 16 (128 registers per thread),
-// except the dp4a path above two tokens, whose per-token accumulators need
-// more registers (8 warps).
-__host__ __device__ constexpr int max_warps_for(int T, bool mma) { return (mma || T <= 2) ? NWARPS_MAX : 8; }
 
 // ------------------------------------------------------------------ balanced mode
 //

@@ -33,9 +33,9 @@ struct DevInfo {
 // 8 warps for T <= 2) and waves of CTAs per launch.  More, smaller CTAs let
 // the block scheduler give more work to SMs that stream faster.
 std::atomic<int> g_ctas_per_sm{0}, g_waves{0};
-// Token counts from which the int8 tensor-core path is used (0 = default).
+// Token count from which T > 1 runs on the f16 tensor-core path (0 = default).
 std::atomic<int> g_mma_min_T{0};
-constexpr int kDefaultMmaMinT = 2;
+constexpr int kDefaultMmaMinT = 5;
 
 inline bool mma_for(int T)
 {

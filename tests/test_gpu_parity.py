@@ -404,12 +404,44 @@ def test_dp4a_and_tensor_core_paths_bit_identical(orc, N, K, T):
         for mma_min in (9, 2):
             q.set_tuning(0, 0, mma_min)
             outs.append(q.gemv(Wp, q.W_PACKED, xq, N, K, T, ws_for(N, K, T)).cpu())
-            items = q.seq_items([(Wp, xq, torch.empty((T, N), dtype=torch.float32, device=DEV), N, K)
-                                 for _ in range(2100 // max(1, N // 16) + 1)])
+            ys = [torch.empty((T, N), dtype=torch.float32, device=DEV) for _ in range(48)]
+            items = q.seq_items([(Wp, xq, y, N, K) for y in ys])
             q.gemv_seq(items, q.W_PACKED, T, q.new_workspace(q.seq_workspace_bytes(items, T)))
-            torch.cuda.synchronize()
+            outs += [y.cpu() for y in ys[::16]]
     finally:
         q.set_tuning(0, 0, 0)
-    assert torch.equal(outs[0].view(torch.int32), outs[1].view(torch.int32))
+    assert q.device_status() == 0
+    for o in outs[1:]:
+        assert torch.equal(outs[0].view(torch.int32), o.view(torch.int32))
     y64, S = orc.gemv(Wg, N, K, orc.quantize(x), T)
-    check_close(outs[1].numpy(), y64, S, f"paths N={N} K={K} T={T}")
+    check_close(outs[-1].numpy(), y64, S, f"paths N={N} K={K} T={T}")
+
+
+@pytest.mark.parametrize("T", [2, 8])
+def test_paths_at_extreme_magnitudes(orc, T):
+    """Nibbles all 0 or all 15 and activations all +-127 (same sign across a
+    block): the largest block sums and folded constants either path meets."""
+    N, K = 48, 1024
+    nb = K // 32
+    rng = np.random.default_rng(77)
+    Wg = np.zeros((N, nb, 18), np.uint8)
+    d = rng.uniform(1e-3, 1e-2, (N, nb)).astype(np.float16)
+    Wg[:, :, :2] = d.view(np.uint8).reshape(N, nb, 2)
+    Wg[:, :, 2:] = rng.choice(np.array([0x00, 0xFF, 0x0F, 0xF0], np.uint8), (N, nb))[:, :, None]
+    Wg = Wg.reshape(-1)
+    sign = rng.choice(np.array([-1.0, 1.0], np.float32), (T, nb))
+    x = np.repeat(sign, 32, axis=1).astype(np.float32)
+    xq = q.quantize_q8_0(torch.from_numpy(x).to(DEV), T, K)
+    Wp = q.pack_q4_0(to_dev(Wg), N, K)
+    outs = []
+    try:
+        for mma_min in (9, 2):
+            q.set_tuning(0, 0, mma_min)
+            for W, lay in ((Wp, q.W_PACKED), (to_dev(Wg), q.W_GGML)):
+                outs.append(q.gemv(W, lay, xq, N, K, T, ws_for(N, K, T)).cpu())
+    finally:
+        q.set_tuning(0, 0, 0)
+    for o in outs[1:]:
+        assert torch.equal(outs[0].view(torch.int32), o.view(torch.int32))
+    y64, S = orc.gemv(Wg, N, K, orc.quantize(x), T)
+    check_close(outs[0].numpy(), y64, S, f"extremes T={T}")
