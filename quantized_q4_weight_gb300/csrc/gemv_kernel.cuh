@@ -963,8 +963,9 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_abort;
     __shared__ int s_last;
-    __shared__ int s_nruns;  // > 0: balanced mode with this many runs
-    __shared__ int s_stages;
+    __shared__ int s_nruns;   // > 0: balanced mode with this many runs
+    __shared__ int s_ngroups; // groups of consecutive runs whose activations fit together
+    __shared__ int s_grp[MAX_RUNS + 1];  // first run of each group, then the run count
     __shared__ unsigned long long s_best[max_warps_for(T, MMA) * T];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -996,9 +997,12 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
     if (tid == 0) {
         s_abort = 0;
         mbar_init(xbar, 1);
-        // Run table for the balanced mode (thread 0 walks the CTA's runs).
-        int nr = 0, stages = 0, nseg_max = 0, xoff = 0;
+        // Run table for the balanced mode (thread 0 walks the CTA's runs),
+        // cut into groups of consecutive runs whose activation images fit the
+        // activation area together; each group's images start at offset 0.
+        int nr = 0, stages = 0, xoff = 0, ng = 0;
         bool fits = P.balanced_ok != 0;
+        s_grp[0] = 0;
         int gh = 0;
         for (long long ra = i0; ra < i1 && fits;) {
             const long long rb = run_end(P, ra, i1, gh);
@@ -1028,17 +1032,23 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
             R.K = g.K;
             R.N = g.N;
             R.nslabs = g.nslabs;
-            R.xq_off = xoff;
             R.bad = bad;
-            xoff += xq_layout(T, g.K, MMA).bytes;
+            const int xb = xq_layout(T, g.K, MMA).bytes;
+            if (xb > P.xq_area) fits = false;
+            if (nr > 0 && xoff + xb > P.xq_area) {  // close the group
+                s_grp[++ng] = nr;
+                xoff = 0;
+            }
+            R.xq_off = xoff;
+            xoff += xb;
             stages += R.nstages;
-            nseg_max = max(nseg_max, g.nseg);
             ++nr;
             ra = rb;
         }
-        if (xoff > P.xq_area || stages / nw < nseg_max || nr == 0) fits = false;
+        if (nr == 0) fits = false;
+        s_grp[++ng] = nr;
         s_nruns = fits ? nr : 0;
-        s_stages = stages;
+        s_ngroups = ng;
     }
     if (lane == 0)
         for (int d = 0; d < D; ++d) mbar_init(&ring.bar[d], 1);
@@ -1059,138 +1069,159 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
 
     if (nruns > 0) {
         // ================================================= balanced mode
-        const int S = s_stages;
-        const int a = static_cast<int>(static_cast<long long>(S) * warp / nw);
-        const int b = static_cast<int>(static_cast<long long>(S) * (warp + 1) / nw);
-        // boundary items: is stage p inside (not at the start of) an item?
-        auto item_start = [&](int p) {
-            int r = 0;
-            while (p >= runs[r].stage0 + runs[r].nstages) ++r;
-            return p - (p - runs[r].stage0) % runs[r].nseg;
-        };
-        int head_b = b, tail_e = a;
-        if (b < S && b > a) {
-            const int st = item_start(b);
-            if (st != b) head_b = st;  // [st, b) is the head of an item continued by warp + 1
-        }
-        if (a > 0 && a < b) {
-            const int st = item_start(a);
-            if (st != a) {
-                int r = 0;
-                while (a >= runs[r].stage0 + runs[r].nstages) ++r;
-                tail_e = st + runs[r].nseg;  // [a, tail_e) finishes an item begun by warp - 1
+        const int ngroups = s_ngroups;
+        for (int gidx = 0; gidx < ngroups; ++gidx) {
+            const int rg0 = s_grp[gidx], rg1 = s_grp[gidx + 1];
+            const int S0 = runs[rg0].stage0, S1 = runs[rg1 - 1].stage0 + runs[rg1 - 1].nstages;
+            const int S = S1 - S0;
+            // warps taking part: each must get at least one whole slab, so
+            // that a slab is shared by two warps at most (every run of the
+            // group holds whole slabs, so one warp always qualifies)
+            int nseg_max = 1;
+            for (int r = rg0; r < rg1; ++r) nseg_max = max(nseg_max, runs[r].nseg);
+            const int nwg = max(1, min(nw, S / nseg_max));
+            const int a = warp < nwg ? S0 + static_cast<int>(static_cast<long long>(S) * warp / nwg) : S1;
+            const int b = warp < nwg ? S0 + static_cast<int>(static_cast<long long>(S) * (warp + 1) / nwg) : S1;
+            // boundary items: is stage p inside (not at the start of) an item?
+            auto item_start = [&](int p) {
+                int r = rg0;
+                while (p >= runs[r].stage0 + runs[r].nstages) ++r;
+                return p - (p - runs[r].stage0) % runs[r].nseg;
+            };
+            int head_b = b, tail_e = a;
+            if (b < S1 && b > a) {
+                const int st = item_start(b);
+                if (st != b) head_b = st;  // [st, b) is the head of an item continued by warp + 1
             }
-        }
+            if (a > S0 && a < b) {
+                const int st = item_start(a);
+                if (st != a) {
+                    int r = rg0;
+                    while (a >= runs[r].stage0 + runs[r].nstages) ++r;
+                    tail_e = st + runs[r].nseg;  // [a, tail_e) finishes an item begun by warp - 1
+                }
+            }
 
-        // weights first (they do not depend on the preceding kernel)
-        Walker cur;
-        cur.init(runs, head_b, b, tail_e, head_b, a, tail_e);
-        cur.skip_untransferred(runs, ggml);
-        for (int d = 0; d < D && cur.valid; ++d) {
-            ring.issue(lane, d, cur.src(), cur.bytes(), pol_w);
-            cur.step(runs);
+            // weights first (they depend neither on the preceding kernel nor on
+            // the previous group); the ring is empty here, and its next slots
+            // in consumption order start at ring.slot
+            Walker cur;
+            cur.init(runs, head_b, b, tail_e, head_b, a, tail_e);
             cur.skip_untransferred(runs, ggml);
-        }
-        pdl_wait();
-        // every run's activations, one transaction count on one barrier
-        if (tid == 0 && !*abort_flag) {
-            unsigned tx = 0;
-            for (int r = 0; r < nruns; ++r) tx += static_cast<unsigned>(P.g[runs[r].gi].xq_bytes);
-            x_unconfirmed = true;
-            mbar_arrive_expect_tx(xbar, tx);
-            for (int r = 0; r < nruns; ++r) {
-                const RunInfo &R = runs[r];
-                const Group &g = P.g[R.gi];
-                const unsigned dbytes = static_cast<unsigned>(g.xq_bytes - T * R.K);
-                copy_activations<T, MMA>(smem + R.xq_off, g.xq + static_cast<long long>(R.e) * g.xq_stride, R.K, dbytes,
-                                    xbar, pol_x);
+            for (int d = 0; d < D && cur.valid; ++d) {
+                ring.issue(lane, (ring.slot + d) % D, cur.src(), cur.bytes(), pol_w);
+                cur.step(runs);
+                cur.skip_untransferred(runs, ggml);
             }
-        }
-        const bool xok = mbar_wait_bounded(xbar, 0, abort_flag, P.status, WAIT_LIMIT_NS);
-        xphase ^= 1u;
-        if (xok) x_unconfirmed = false;
-        if (xok)
-            for (int r = 0; r < nruns; ++r) build_fold_constants<T, MMA>(smem + runs[r].xq_off, runs[r].K, tid, nthreads);
-        __syncthreads();
+            if (gidx == 0) {
+                pdl_wait();
+            } else {
+                // every warp is done with the previous group's activations and
+                // hand-off sums; the whole CTA stops together after an abort
+                if (__syncthreads_or(*abort_flag)) break;
+                if (tid < nw) hflag[tid] = 0;
+            }
+            // the group's activations, one transaction count on one barrier
+            if (tid == 0 && !*abort_flag) {
+                unsigned tx = 0;
+                for (int r = rg0; r < rg1; ++r) tx += static_cast<unsigned>(P.g[runs[r].gi].xq_bytes);
+                x_unconfirmed = true;
+                fence_proxy_async_smem();
+                mbar_arrive_expect_tx(xbar, tx);
+                for (int r = rg0; r < rg1; ++r) {
+                    const RunInfo &R = runs[r];
+                    const Group &g = P.g[R.gi];
+                    const unsigned dbytes = static_cast<unsigned>(g.xq_bytes - T * R.K);
+                    copy_activations<T, MMA>(smem + R.xq_off, g.xq + static_cast<long long>(R.e) * g.xq_stride, R.K, dbytes,
+                                        xbar, pol_x);
+                }
+            }
+            const bool xok = mbar_wait_bounded(xbar, xphase, abort_flag, P.status, WAIT_LIMIT_NS);
+            xphase ^= 1u;
+            if (xok && tid == 0) x_unconfirmed = false;
+            if (xok)
+                for (int r = rg0; r < rg1; ++r) build_fold_constants<T, MMA>(smem + runs[r].xq_off, runs[r].K, tid, nthreads);
+            __syncthreads();
 
-        // compute, one visit (the segments of one slab inside one interval) at a time
-        Walker w;
-        w.init(runs, head_b, b, tail_e, head_b, a, tail_e);
-        bool ok = xok;
-        while (w.valid) {
-            const RunInfo &R = runs[w.r];
-            const int s_first = w.s;
-            const int seg_end = min(w.nseg, s_first + (w.kend - w.k));
-            const int li = w.first_local + w.ii;
-            const bool tail_item = li >= w.nslabs;
-            const bool direct = ggml || tail_item;
-            const int nb = w.nb;
-            const int rows = tail_item ? P.g[R.gi].tail_rows : min(SLAB_ROWS, R.N - li * SLAB_ROWS);
-            const uint8_t *rows_base = w.Wi + static_cast<long long>(li) * SLAB_ROWS * nb * Q4_BYTES;
-            const XqLayout L = xq_layout(T, R.K, MMA);
-            const XqView xv{reinterpret_cast<const int8_t *>(smem + R.xq_off), L.xstride,
-                            reinterpret_cast<const int2 *>(smem + R.xq_off + L.off_cd), L.cdw};
-            float yv[NO];
-#pragma unroll
-            for (int k = 0; k < NO; ++k) yv[k] = 0.0f;
-            if (s_first > 0) {
-                // tail of a slab begun by warp - 1: continue from its ordered sum
-                if (lane == 0) wait_flag(&hflag[warp - 1], abort_flag, P.status);
-                __syncwarp();
-                __threadfence_block();
-                const float *H = hbuf + (warp - 1) * T * 16;
-#pragma unroll
-                for (int k = 0; k < NO; ++k) {
-                    const int t = LO::tok(k, j);
-                    yv[k] = t < T ? H[t * 16 + LO::row(k, r8)] : 0.0f;
-                }
-            }
-            for (int sg = s_first; sg < seg_end; ++sg) {
-                float Pk[NO];
-                bool have = false;
-                if (w.bad) {
-                    // nothing is read for an out-of-range expert id
-                } else if (direct) {
-                    if (ok) {
-                        segment_sum<T, MMA>(false, nullptr, rows_base, rows, sg, nb, r8, j, xv, Pk);
-                        have = true;
-                    }
-                } else {
-                    if (ok) ok = mbar_wait_bounded(&ring.bar[ring.slot], ring.phase, abort_flag, P.status, WAIT_LIMIT_NS);
-                    if (ok) {
-                        segment_sum<T, MMA>(true, ring.stage(), nullptr, 0, sg, nb, r8, j, xv, Pk);
-                        have = true;
-                    }
+            // compute, one visit (the segments of one slab inside one interval) at a time
+            Walker w;
+            w.init(runs, head_b, b, tail_e, head_b, a, tail_e);
+            bool ok = xok;
+            while (w.valid) {
+                const RunInfo &R = runs[w.r];
+                const int s_first = w.s;
+                const int seg_end = min(w.nseg, s_first + (w.kend - w.k));
+                const int li = w.first_local + w.ii;
+                const bool tail_item = li >= w.nslabs;
+                const bool direct = ggml || tail_item;
+                const int nb = w.nb;
+                const int rows = tail_item ? P.g[R.gi].tail_rows : min(SLAB_ROWS, R.N - li * SLAB_ROWS);
+                const uint8_t *rows_base = w.Wi + static_cast<long long>(li) * SLAB_ROWS * nb * Q4_BYTES;
+                const XqLayout L = xq_layout(T, R.K, MMA);
+                const XqView xv{reinterpret_cast<const int8_t *>(smem + R.xq_off), L.xstride,
+                                reinterpret_cast<const int2 *>(smem + R.xq_off + L.off_cd), L.cdw};
+                float yv[NO];
+    #pragma unroll
+                for (int k = 0; k < NO; ++k) yv[k] = 0.0f;
+                if (s_first > 0) {
+                    // tail of a slab begun by warp - 1: continue from its ordered sum
+                    if (lane == 0) wait_flag(&hflag[warp - 1], abort_flag, P.status);
                     __syncwarp();
-                    if (cur.valid && ok) {  // refill the slot just consumed
-                        ring.issue(lane, ring.slot, cur.src(), cur.bytes(), pol_w);
-                        cur.step(runs);
-                        cur.skip_untransferred(runs, ggml);
+                    __threadfence_block();
+                    const float *H = hbuf + (warp - 1) * T * 16;
+    #pragma unroll
+                    for (int k = 0; k < NO; ++k) {
+                        const int t = LO::tok(k, j);
+                        yv[k] = t < T ? H[t * 16 + LO::row(k, r8)] : 0.0f;
                     }
-                    ring.pop();
                 }
-                if (!have) {
-#pragma unroll
-                    for (int k = 0; k < NO; ++k) Pk[k] = 0.0f;
+                for (int sg = s_first; sg < seg_end; ++sg) {
+                    float Pk[NO];
+                    bool have = false;
+                    if (w.bad) {
+                        // nothing is read for an out-of-range expert id
+                    } else if (direct) {
+                        if (ok) {
+                            segment_sum<T, MMA>(false, nullptr, rows_base, rows, sg, nb, r8, j, xv, Pk);
+                            have = true;
+                        }
+                    } else {
+                        if (ok) ok = mbar_wait_bounded(&ring.bar[ring.slot], ring.phase, abort_flag, P.status, WAIT_LIMIT_NS);
+                        if (ok) {
+                            segment_sum<T, MMA>(true, ring.stage(), nullptr, 0, sg, nb, r8, j, xv, Pk);
+                            have = true;
+                        }
+                        __syncwarp();
+                        if (cur.valid && ok) {  // refill the slot just consumed
+                            ring.issue(lane, ring.slot, cur.src(), cur.bytes(), pol_w);
+                            cur.step(runs);
+                            cur.skip_untransferred(runs, ggml);
+                        }
+                        ring.pop();
+                    }
+                    if (!have) {
+    #pragma unroll
+                        for (int k = 0; k < NO; ++k) Pk[k] = 0.0f;
+                    }
+    #pragma unroll
+                    for (int k = 0; k < NO; ++k) yv[k] = (sg == 0) ? Pk[k] : __fadd_rn(yv[k], Pk[k]);
                 }
-#pragma unroll
-                for (int k = 0; k < NO; ++k) yv[k] = (sg == 0) ? Pk[k] : __fadd_rn(yv[k], Pk[k]);
+                if (seg_end < w.nseg) {
+                    // head of a slab that warp + 1 finishes: leave the ordered sum
+                    float *H = hbuf + warp * T * 16;
+    #pragma unroll
+                    for (int k = 0; k < NO; ++k)
+                        if (LO::owner(k, j)) H[LO::tok(k, j) * 16 + LO::row(k, r8)] = yv[k];
+                    __threadfence_block();
+                    __syncwarp();
+                    if (lane == 0) hflag[warp] = 1;
+                } else if (!w.bad) {
+                    store_outputs<T, MMA, ARGMAX>(R.y, R.N, li * SLAB_ROWS, rows, r8, j, yv, best);
+                } else if (lane == 0) {
+                    atomicCAS(P.status, 0u, ST_BAD_ID);
+                }
+                w.next_item(runs);
             }
-            if (seg_end < w.nseg) {
-                // head of a slab that warp + 1 finishes: leave the ordered sum
-                float *H = hbuf + warp * T * 16;
-#pragma unroll
-                for (int k = 0; k < NO; ++k)
-                    if (LO::owner(k, j)) H[LO::tok(k, j) * 16 + LO::row(k, r8)] = yv[k];
-                __threadfence_block();
-                __syncwarp();
-                if (lane == 0) hflag[warp] = 1;
-            } else if (!w.bad) {
-                store_outputs<T, MMA, ARGMAX>(R.y, R.N, li * SLAB_ROWS, rows, r8, j, yv, best);
-            } else if (lane == 0) {
-                atomicCAS(P.status, 0u, ST_BAD_ID);
-            }
-            w.next_item(runs);
         }
     } else {
         // ================================================= run-synced mode
