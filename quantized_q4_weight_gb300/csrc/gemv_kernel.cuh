@@ -220,9 +220,31 @@ struct LaneOut {
 struct XqView {
     const int8_t *q;   // token rows at q + t * xstride
     int xstride;
-    const int2 *cd;    // per block: cdw {folded constant, activation scale} pairs (MMA: token-pair order)
+    const int2 *cd;    // dp4a: per block cdw {folded constant, d_x / 16}; MMA: CD_MMA_QUAD per 4 blocks
     int cdw;
+    // tensor-core path: f16 operand image (else int8); this lane's ldmatrix
+    // row offsets within a stage, and the shared-memory addresses of its
+    // activation rows and constants at block 0
+    int f16;
+    uint32_t oa1, oa2, osc, xa0, ca0;
 };
+
+// The tensor-core lane offsets of an activation image (see mma_segment_full_ldsm).
+template <int T>
+__device__ __forceinline__ void mma_lane_offsets(XqView &xv, int g, int j)
+{
+    const int lane = threadIdx.x & 31;
+    const int m = lane >> 3, rr = lane & 7;
+    const int row = rr + 8 * (m & 1), rot = rr >> 1;
+    xv.oa1 = (row * QUAD + (((m >> 1) + rot) & 3)) * 16;
+    xv.oa2 = (row * QUAD + (((m >> 1) + 2 + rot) & 3)) * 16;
+    xv.osc = 256 * QUAD + g * 16;
+    const int tok = T == 8 ? rr : min(rr, T - 1);
+    // int8 image: block l >> 4 (+ 2), bytes 16 ((l >> 3) & 1); f16 image:
+    // 16-byte chunk l >> 3 of the block's 64 bytes
+    xv.xa0 = smem_addr(xv.q + tok * xv.xstride + (xv.f16 ? m * 16 : (m >> 1) * QK + (m & 1) * 16));
+    xv.ca0 = smem_addr(xv.cd) + 16 * j;
+}
 
 // ------------------------------------------------------------------ dp4a path (T == 1)
 
@@ -339,12 +361,13 @@ __device__ __forceinline__ void combine_phases(float (&acc)[2][T])
 // 4j+1, 4j+3 (k = 2j+8, 2j+9); the second MMA the same over the high nibbles.
 //   low nibbles:  A = 1024 + n   (one LOP3: n | 0x6400),      B = q
 //   high nibbles: A = 1024 + 16 n (one LOP3: 16n | 0x6400),   B = q / 16
-// so the MMAs add isum + 1032 sum(q_lo) + 72 sum(q_hi); the accumulator
-// starts at C = -(1032 sum(q_lo) + 72 sum(q_hi)) (per token and block) and
-// ends at isum.  Activations arrive as f16 1024 + (q xor 0x80) (one LOP3)
-// and one f16x2 add (or fma by 1/16) recovers q (or q / 16) exactly.
-// The lane keeps one fp32 sum per block phase (b % 4) and output and adds
-// (d_w * d_x) * isum with one fused multiply-add: the dp4a lanes' product
+// so the MMAs add isum + 1032 sum(q_lo) + 72 sum(q_hi); the first MMA's
+// accumulator input is C = -(1032 sum(q_lo) + 72 sum(q_hi)) (per token and
+// block) and the second ends at isum.  Activations, stored as q xor 0x80,
+// become f16 1024 + (q xor 0x80) with one PRMT and one f16x2 add (or fma by
+// 1/16) recovers q (or q / 16) exactly.  The lane keeps one fp32 sum per
+// block phase (b % 4) and output and adds (d_w * d_x) * isum with one fused
+// multiply-add: d_w * d_x is exact in fp32, and the dp4a lanes' product
 // (d_w * (d_x / 16)) * (16 isum) is the same real number, rounded the same.
 
 __device__ __forceinline__ void mma_f16(float (&d)[4], unsigned a0, unsigned a1, unsigned a2, unsigned a3,
@@ -380,18 +403,6 @@ constexpr unsigned H2_NEG_72 = 0xD480D480u;    // f16x2 (-72, -72): (1152 + q) /
 __device__ __forceinline__ unsigned act_even(unsigned w) { return __byte_perm(w, 0x64646464u, 0x4240); }
 __device__ __forceinline__ unsigned act_odd(unsigned w) { return __byte_perm(w, 0x64646464u, 0x4341); }
 
-// d0 += c0, d1 += c1 (add.rn.f32x2).
-__device__ __forceinline__ void fadd2(float &d0, float &d1, float c0, float c1)
-{
-    asm("{\n\t.reg .b64 ra, rc;\n\t"
-        "mov.b64 ra, {%0, %1};\n\t"
-        "mov.b64 rc, {%2, %3};\n\t"
-        "add.rn.f32x2 ra, ra, rc;\n\t"
-        "mov.b64 {%0, %1}, ra;\n\t}"
-        : "+f"(d0), "+f"(d1)
-        : "f"(c0), "f"(c1));
-}
-
 // acc0 += s0 * d0, acc1 += s1 * d1: one fma.rn.f32x2 (two IEEE fused
 // multiply-adds, rounded as two fma.rn.f32 would be).
 __device__ __forceinline__ void ffma2(float &a0, float &a1, float s0, float s1, float d0, float d1)
@@ -406,15 +417,31 @@ __device__ __forceinline__ void ffma2(float &a0, float &a1, float s0, float s1, 
         : "f"(s0), "f"(s1), "f"(d0), "f"(d1));
 }
 
-// Both fp16 halves of a word as fp32 (exact).
-__device__ __forceinline__ void h2f2(unsigned w, float &lo, float &hi)
+// The four fp32 products of two fp16 pairs, w = {w0, w1}, x = {x0, x1}:
+// w0 x0, w0 x1, w1 x0, w1 x1.  Each product of two fp16 values is exact in
+// fp32; fma.rn.f32.f16 with a -0 addend returns it as fp32 multiplication
+// of the widened values would.
+__device__ __forceinline__ void h2_outer(unsigned w, unsigned x, float &p00, float &p01, float &p10, float &p11)
 {
-    asm("{\n\t.reg .b16 l, h;\n\t"
-        "mov.b32 {l, h}, %2;\n\t"
-        "cvt.f32.f16 %0, l;\n\t"
-        "cvt.f32.f16 %1, h;\n\t}"
-        : "=f"(lo), "=f"(hi)
-        : "r"(w));
+    asm("{\n\t.reg .b16 w0, w1, x0, x1;\n\t"
+        "mov.b32 {w0, w1}, %4;\n\t"
+        "mov.b32 {x0, x1}, %5;\n\t"
+        "fma.rn.f32.f16 %0, w0, x0, %6;\n\t"
+        "fma.rn.f32.f16 %1, w0, x1, %6;\n\t"
+        "fma.rn.f32.f16 %2, w1, x0, %6;\n\t"
+        "fma.rn.f32.f16 %3, w1, x1, %6;\n\t}"
+        : "=f"(p00), "=f"(p01), "=f"(p10), "=f"(p11)
+        : "r"(w), "r"(x), "f"(-0.0f));
+}
+
+// d = A B + C for one m16n8k16 tile with the accumulator start c.
+__device__ __forceinline__ void mma_f16_c(float (&d)[4], unsigned a0, unsigned a1, unsigned a2, unsigned a3,
+                                          unsigned b0, unsigned b1, const float4 &c)
+{
+    asm("mma.sync.aligned.m16n8k16.row.col.f32.f16.f16.f32 {%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, "
+        "{%10,%11,%12,%13};"
+        : "=f"(d[0]), "=f"(d[1]), "=f"(d[2]), "=f"(d[3])
+        : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1), "f"(c.x), "f"(c.y), "f"(c.z), "f"(c.w));
 }
 
 // Four 8 x 8 b16 matrices from shared memory; lane l gives the address of
@@ -440,35 +467,50 @@ __device__ __forceinline__ uint4 lds_u4(uint32_t addr)
     return v;
 }
 
-// One block for this lane's four outputs from its words: weight word j of
-// rows g and g + 8 (wg, wg8), biased activation words j and 4 + j of token g
-// (ql, qh), the rows' fp16 scales (sc) and the block constants
-// {C(2j), C(2j+1), d_x(2j), d_x(2j+1)}.
-__device__ __forceinline__ void mma_block_words(unsigned wg, unsigned wg8, unsigned ql, unsigned qh, unsigned sc,
-                                                const float4 &cd, float (&acc)[4])
+__device__ __forceinline__ unsigned lds_u32(uint32_t addr)
 {
-    const unsigned bl0 = hadd2_u(act_even(ql), H2_NEG_1152);
-    const unsigned bl1 = hadd2_u(act_odd(ql), H2_NEG_1152);
-    const unsigned bh0 = hfma2_u(act_even(qh), H2_SIXTEENTH, H2_NEG_72);
-    const unsigned bh1 = hfma2_u(act_odd(qh), H2_SIXTEENTH, H2_NEG_72);
-    const unsigned g1 = wg >> 8, g9 = wg8 >> 8;
-    float d[4] = {0.0f, 0.0f, 0.0f, 0.0f};
-    mma_f16(d, (wg & 0x000F000Fu) | H2_1024, (wg8 & 0x000F000Fu) | H2_1024, (g1 & 0x000F000Fu) | H2_1024,
-            (g9 & 0x000F000Fu) | H2_1024, bl0, bl1);
-    mma_f16(d, (wg & 0x00F000F0u) | H2_1024, (wg8 & 0x00F000F0u) | H2_1024, (g1 & 0x00F000F0u) | H2_1024,
-            (g9 & 0x00F000F0u) | H2_1024, bh0, bh1);
-    fadd2(d[0], d[1], cd.x, cd.y);  // exact: integers below 2^23
-    fadd2(d[2], d[3], cd.x, cd.y);
-    float dw0, dw1;
-    h2f2(sc, dw0, dw1);
-    ffma2(acc[0], acc[1], __fmul_rn(dw0, cd.z), __fmul_rn(dw0, cd.w), d[0], d[1]);
-    ffma2(acc[2], acc[3], __fmul_rn(dw1, cd.z), __fmul_rn(dw1, cd.w), d[2], d[3]);
+    unsigned v;
+    asm volatile("ld.shared.u32 %0, [%1];" : "=r"(v) : "r"(addr));
+    return v;
 }
 
-// The block's constants for tokens 2j and 2j + 1: {C(2j), C(2j+1), d_x(2j), d_x(2j+1)}.
-__device__ __forceinline__ float4 mma_block_consts(const XqView &xv, int b, int j)
+// One block for this lane's four outputs from its words: weight word j of
+// rows g and g + 8 (wg, wg8), biased activation words j and 4 + j of token g
+// (ql, qh), the rows' fp16 scales (sc), the accumulator start cq =
+// {C(2j), C(2j+1), C(2j), C(2j+1)} and the fp16 pair {d_x(2j), d_x(2j+1)}.
+// The same from the B registers of the two MMAs: (bl0, bl1) = {q} over the
+// low-nibble k order, (bh0, bh1) = {q / 16} over the high-nibble k order.
+__device__ __forceinline__ void mma_block_core(unsigned wg, unsigned wg8, unsigned bl0, unsigned bl1, unsigned bh0,
+                                               unsigned bh1, unsigned sc, const float4 &cq, unsigned dx, float (&acc)[4])
 {
-    return *reinterpret_cast<const float4 *>(reinterpret_cast<const float *>(xv.cd) + b * 16 + 4 * j);
+    const unsigned g1 = wg >> 8, g9 = wg8 >> 8;
+    float d[4];
+    mma_f16_c(d, (wg & 0x000F000Fu) | H2_1024, (wg8 & 0x000F000Fu) | H2_1024, (g1 & 0x000F000Fu) | H2_1024,
+              (g9 & 0x000F000Fu) | H2_1024, bl0, bl1, cq);
+    mma_f16(d, (wg & 0x00F000F0u) | H2_1024, (wg8 & 0x00F000F0u) | H2_1024, (g1 & 0x00F000F0u) | H2_1024,
+            (g9 & 0x00F000F0u) | H2_1024, bh0, bh1);
+    float s00, s01, s10, s11;  // (d_w d_x) for rows g, g + 8 and tokens 2j, 2j + 1
+    h2_outer(sc, dx, s00, s01, s10, s11);
+    ffma2(acc[0], acc[1], s00, s01, d[0], d[1]);
+    ffma2(acc[2], acc[3], s10, s11, d[2], d[3]);
+}
+
+__device__ __forceinline__ void mma_block_words(unsigned wg, unsigned wg8, unsigned ql, unsigned qh, unsigned sc,
+                                                const float4 &cq, unsigned dx, float (&acc)[4])
+{
+    mma_block_core(wg, wg8, hadd2_u(act_even(ql), H2_NEG_1152), hadd2_u(act_odd(ql), H2_NEG_1152),
+                   hfma2_u(act_even(qh), H2_SIXTEENTH, H2_NEG_72), hfma2_u(act_odd(qh), H2_SIXTEENTH, H2_NEG_72), sc,
+                   cq, dx, acc);
+}
+
+// Shared-memory addresses of block b's constants for lane j (token pair j).
+__device__ __forceinline__ uint32_t mma_cq_addr(const XqView &xv, int b)
+{
+    return xv.ca0 + (b >> 2) * CD_MMA_QUAD + (b & 3) * 64;
+}
+__device__ __forceinline__ uint32_t mma_dx_addr(const XqView &xv, int b, int j)
+{
+    return xv.ca0 - 16 * j + (b >> 2) * CD_MMA_QUAD + 256 + (j * 4 + (b & 3)) * 4;
 }
 
 template <int T>
@@ -478,48 +520,77 @@ __device__ __forceinline__ void mma_block(unsigned wg, unsigned wg8, unsigned sc
     // Token columns past T read token T - 1: a column of B only reaches its
     // own outputs, which no lane stores.
     const int tg = T == 8 ? g : min(g, T - 1);
-    const unsigned *xr = reinterpret_cast<const unsigned *>(xv.q + tg * xv.xstride + b * QK);
-    mma_block_words(wg, wg8, xr[j], xr[4 + j], sc, mma_block_consts(xv, b, j), acc);
+    const float4 cq = lds_f4(mma_cq_addr(xv, b));
+    const unsigned dx = lds_u32(mma_dx_addr(xv, b, j));
+    if (xv.f16) {
+        const unsigned *xr = reinterpret_cast<const unsigned *>(xv.q + tg * xv.xstride + b * 64);
+        mma_block_core(wg, wg8, xr[j], xr[4 + j], xr[8 + j], xr[12 + j], sc, cq, dx, acc);
+    } else {
+        const unsigned *xr = reinterpret_cast<const unsigned *>(xv.q + tg * xv.xstride + b * QK);
+        mma_block_words(wg, wg8, xr[j], xr[4 + j], sc, cq, dx, acc);
+    }
 }
 
-// A full segment from a stage in the packed layout, with ldmatrix: per quad
-// one x4 load brings weight word j of rows g and g + 8 of two blocks, one
-// more the other two blocks, and two more the activation words of the four
-// blocks.  Lane l names, for the weights, row (l & 7) + 8 ((l >> 3) & 1) of
-// block l >> 4 (+ 2 in the second load); for the activations, token
-// min(l & 7, T - 1) of block l >> 4 (+ 2), bytes 16 ((l >> 3) & 1) onwards.
-// The rotation keeps each group of eight 16-byte rows in distinct banks.
-// Warps per CTA a T-token kernel may use: 16 (128 registers per thread),
-// except the dp4a path above two tokens and the MMA path above four, whose
-// per-token accumulators or pipelined operands want more registers (8 warps,
-// up to 255 registers).
-__host__ __device__ constexpr int max_warps_for(int T, bool mma) { return (mma ? T <= 4 : T <= 2) ? NWARPS_MAX : 8; }
-
-// The operands of one quad of a full segment (see mma_segment_full_ldsm).
-struct MmaQuad {
+// The operands of one quad of a full segment (see mma_segment_full_ldsm):
+// the ldmatrix words (weights w, activations x) and the per-block constants.
+struct MmaWords {
     unsigned w[8], x[8];
-    uint4 sc;
-    float4 cd[4];
+};
+struct MmaConsts {
+    uint4 sc, dx;
+    float4 cq[4];
 };
 
-__device__ __forceinline__ void mma_quad_load(MmaQuad &o, uint32_t a1, uint32_t a2, uint32_t asc, uint32_t xa, uint32_t ca,
-                                              int qq)
+// Quad qq of the segment whose stage starts at shared address st and whose
+// first block is b0 (a multiple of 16).
+__device__ __forceinline__ void mma_quad_words(MmaWords &o, const XqView &xv, uint32_t st, int b0, int qq)
 {
-    ldsm_x4(o.w[0], o.w[1], o.w[2], o.w[3], a1 + qq * QUAD_BYTES);
-    ldsm_x4(o.w[4], o.w[5], o.w[6], o.w[7], a2 + qq * QUAD_BYTES);
-    ldsm_x4(o.x[0], o.x[1], o.x[2], o.x[3], xa + qq * QUAD * QK);
-    ldsm_x4(o.x[4], o.x[5], o.x[6], o.x[7], xa + qq * QUAD * QK + 2 * QK);
-    o.sc = lds_u4(asc + qq * QUAD_BYTES);
-#pragma unroll
-    for (int jq = 0; jq < QUAD; ++jq) o.cd[jq] = lds_f4(ca + (qq * QUAD + jq) * 64);
+    const uint32_t q = st + qq * QUAD_BYTES;
+    ldsm_x4(o.w[0], o.w[1], o.w[2], o.w[3], q + xv.oa1);
+    ldsm_x4(o.w[4], o.w[5], o.w[6], o.w[7], q + xv.oa2);
+    const uint32_t xa = xv.xa0 + (b0 + QUAD * qq) * QK;
+    ldsm_x4(o.x[0], o.x[1], o.x[2], o.x[3], xa);
+    ldsm_x4(o.x[4], o.x[5], o.x[6], o.x[7], xa + 2 * QK);
 }
 
-__device__ __forceinline__ void mma_quad_compute(const MmaQuad &o, float (&acc)[4][4])
+__device__ __forceinline__ void mma_quad_consts(MmaConsts &o, const XqView &xv, uint32_t st, int b0, int qq)
 {
-    mma_block_words(o.w[0], o.w[1], o.x[0], o.x[1], o.sc.x, o.cd[0], acc[0]);
-    mma_block_words(o.w[2], o.w[3], o.x[2], o.x[3], o.sc.y, o.cd[1], acc[1]);
-    mma_block_words(o.w[4], o.w[5], o.x[4], o.x[5], o.sc.z, o.cd[2], acc[2]);
-    mma_block_words(o.w[6], o.w[7], o.x[6], o.x[7], o.sc.w, o.cd[3], acc[3]);
+    o.sc = lds_u4(st + qq * QUAD_BYTES + xv.osc);
+    const uint32_t cq = xv.ca0 + (b0 / QUAD + qq) * CD_MMA_QUAD;
+#pragma unroll
+    for (int jq = 0; jq < QUAD; ++jq) o.cq[jq] = lds_f4(cq + jq * 64);
+    o.dx = lds_u4(cq + 256);  // ca0 includes 16 j: the pair's d_x for the quad's four blocks
+}
+
+// The weight words of quad qq only (f16 operand image).
+__device__ __forceinline__ void mma_quad_weights(MmaWords &o, const XqView &xv, uint32_t st, int qq)
+{
+    const uint32_t q = st + qq * QUAD_BYTES;
+    ldsm_x4(o.w[0], o.w[1], o.w[2], o.w[3], q + xv.oa1);
+    ldsm_x4(o.w[4], o.w[5], o.w[6], o.w[7], q + xv.oa2);
+}
+
+// One quad on the f16 operand image: one ldmatrix.x4 per block gives the
+// four B registers of its two MMAs (chunk c of the block's 64 bytes).
+__device__ __forceinline__ void mma_quad_compute_f16(const MmaWords &o, const MmaConsts &c, const XqView &xv, int bq,
+                                                     float (&acc)[4][4])
+{
+    const unsigned sc[4] = {c.sc.x, c.sc.y, c.sc.z, c.sc.w};
+    const unsigned dx[4] = {c.dx.x, c.dx.y, c.dx.z, c.dx.w};
+#pragma unroll
+    for (int jq = 0; jq < QUAD; ++jq) {
+        unsigned x0, x1, x2, x3;
+        ldsm_x4(x0, x1, x2, x3, xv.xa0 + (bq + jq) * 64);
+        mma_block_core(o.w[2 * jq], o.w[2 * jq + 1], x0, x1, x2, x3, sc[jq], c.cq[jq], dx[jq], acc[jq]);
+    }
+}
+
+__device__ __forceinline__ void mma_quad_compute(const MmaWords &o, const MmaConsts &c, float (&acc)[4][4])
+{
+    mma_block_words(o.w[0], o.w[1], o.x[0], o.x[1], c.sc.x, c.cq[0], c.dx.x, acc[0]);
+    mma_block_words(o.w[2], o.w[3], o.x[2], o.x[3], c.sc.y, c.cq[1], c.dx.y, acc[1]);
+    mma_block_words(o.w[4], o.w[5], o.x[4], o.x[5], c.sc.z, c.cq[2], c.dx.z, acc[2]);
+    mma_block_words(o.w[6], o.w[7], o.x[6], o.x[7], c.sc.w, c.cq[3], c.dx.w, acc[3]);
 }
 
 // A full segment from a stage in the packed layout, with ldmatrix: per quad
@@ -529,37 +600,31 @@ __device__ __forceinline__ void mma_quad_compute(const MmaQuad &o, float (&acc)[
 // block l >> 4 (+ 2 in the second load); for the activations, token
 // min(l & 7, T - 1) of block l >> 4 (+ 2), bytes 16 ((l >> 3) & 1) onwards.
 // The rotation keeps each group of eight 16-byte rows in distinct banks.
-// With the larger register budget (8 warps) the next quad's operands load
-// while the current quad computes.
+// On the f16 operand image one x4 load per block gives its B registers.
 template <int T>
-__device__ __forceinline__ void mma_segment_full_ldsm(const uint8_t *stage, int s, int g, int j, const XqView &xv,
+__device__ __forceinline__ void mma_segment_full_ldsm(const uint8_t *stage, int s, const XqView &xv,
                                                       float (&acc)[4][4])
 {
-    const int lane = threadIdx.x & 31;
-    const int m = lane >> 3, rr = lane & 7;
-    const int row = rr + 8 * (m & 1), rot = rr >> 1;
     const uint32_t st = smem_addr(stage);
-    const uint32_t a1 = st + (row * QUAD + (((m >> 1) + rot) & 3)) * 16;
-    const uint32_t a2 = st + (row * QUAD + (((m >> 1) + 2 + rot) & 3)) * 16;
-    const uint32_t asc = st + 256 * QUAD + g * 16;
-    const int tok = T == 8 ? rr : min(rr, T - 1);
-    const uint32_t xa = smem_addr(xv.q + tok * xv.xstride + SEG_BLOCKS * QK * s + (m >> 1) * QK + (m & 1) * 16);
-    const uint32_t ca = smem_addr(reinterpret_cast<const float *>(xv.cd) + SEG_BLOCKS * 16 * s + 4 * j);
-    if constexpr (max_warps_for(T, true) <= 8) {
-        MmaQuad o[2];
-        mma_quad_load(o[0], a1, a2, asc, xa, ca, 0);
-#pragma unroll
-        for (int qq = 0; qq < SEG_BLOCKS / QUAD; ++qq) {
-            if (qq + 1 < SEG_BLOCKS / QUAD) mma_quad_load(o[(qq + 1) & 1], a1, a2, asc, xa, ca, qq + 1);
-            mma_quad_compute(o[qq & 1], acc);
-        }
-    } else {
+    const int b0 = SEG_BLOCKS * s;
+    if (xv.f16) {
 #pragma unroll 1
         for (int qq = 0; qq < SEG_BLOCKS / QUAD; ++qq) {
-            MmaQuad o;
-            mma_quad_load(o, a1, a2, asc, xa, ca, qq);
-            mma_quad_compute(o, acc);
+            MmaWords w;
+            MmaConsts c;
+            mma_quad_weights(w, xv, st, qq);
+            mma_quad_consts(c, xv, st, b0, qq);
+            mma_quad_compute_f16(w, c, xv, b0 + QUAD * qq, acc);
         }
+        return;
+    }
+#pragma unroll 1
+    for (int qq = 0; qq < SEG_BLOCKS / QUAD; ++qq) {
+        MmaWords w;
+        MmaConsts c;
+        mma_quad_words(w, xv, st, b0, qq);
+        mma_quad_consts(c, xv, st, b0, qq);
+        mma_quad_compute(w, c, acc);
     }
 }
 
@@ -569,7 +634,7 @@ __device__ __forceinline__ void mma_segment_from_stage(const uint8_t *stage, boo
                                                        const XqView &xv, float (&acc)[4][4])
 {
     if (full) {
-        mma_segment_full_ldsm<T>(stage, s, g, j, xv, acc);
+        mma_segment_full_ldsm<T>(stage, s, xv, acc);
         return;
     }
     const int nbs = min(SEG_BLOCKS, nb - SEG_BLOCKS * s);
@@ -668,12 +733,23 @@ __device__ __forceinline__ void segment_sum(bool from_stage, const uint8_t *stag
     }
 }
 
+// Tensor-core constants of block b, token t: C into both slots of the
+// pair's accumulator start, the raw fp16 d_x into the pair's d_x word.
+__device__ __forceinline__ void mma_store_consts(uint8_t *cd, int b, int t, float C, unsigned short dx)
+{
+    uint8_t *q = cd + (b >> 2) * CD_MMA_QUAD;
+    float *cq = reinterpret_cast<float *>(q + (b & 3) * 64 + (t >> 1) * 16);
+    cq[t & 1] = C;
+    cq[2 + (t & 1)] = C;
+    reinterpret_cast<unsigned short *>(q + 256 + ((t >> 1) * 4 + (b & 3)) * 4)[t & 1] = dx;
+}
+
 // Builds one run's activation image in shared memory after its copy landed:
 // per block and token the folded constant and the activation scale.  dp4a
 // path: {MAGIC - 128 sum(q), d_x / 16} per token; MMA path: the activation
-// bytes are rewritten as q xor 0x80, and per token pair
-// (2p, 2p + 1) {C(2p), C(2p+1), d_x(2p), d_x(2p+1)} with C = -(1032 sum(q_lo)
-// + 72 sum(q_hi)) as fp32, and zeros for the token columns past T.
+// bytes are rewritten as q xor 0x80, and each token's accumulator start
+// C = -(1032 sum(q_lo) + 72 sum(q_hi)) (fp32) and fp16 d_x go to the
+// CD_MMA_QUAD layout, with zeros for the token columns past T.
 template <int T, bool MMA>
 __device__ __forceinline__ void build_fold_constants(uint8_t *img, int K, int tid, int nthreads)
 {
@@ -704,18 +780,65 @@ __device__ __forceinline__ void build_fold_constants(uint8_t *img, int K, int ti
                 shi = dp4a_ss((int)qb.y, ones, shi);
                 shi = dp4a_ss((int)qb.z, ones, shi);
                 shi = dp4a_ss((int)qb.w, ones, shi);
-                float *cp = reinterpret_cast<float *>(cd) + b * 16 + 4 * (t >> 1) + (t & 1);
-                cp[0] = static_cast<float>(-(1032 * slo + 72 * shi));
-                cp[2] = dx;
+                mma_store_consts(img + L.off_cd, b, t, static_cast<float>(-(1032 * slo + 72 * shi)), xd[t * nb + b]);
             } else {
                 cd[i] = make_int2(block_fold16_const(qp[0], qp[1]), __float_as_int(__fmul_rn(dx, 0.0625f)));
             }
         } else if constexpr (MMA) {
-            float *cp = reinterpret_cast<float *>(cd) + b * 16 + 4 * (t >> 1) + (t & 1);
-            cp[0] = 0.0f;
-            cp[2] = 0.0f;
+            mma_store_consts(img + L.off_cd, b, t, 0.0f, 0);
         } else {
             cd[i] = make_int2(MAGIC_I, 0);
+        }
+    }
+}
+
+// Builds one run's f16 operand image (tensor-core path, small images)
+// straight from the planar Q8_0 activations in global memory: per token row
+// and block 64 bytes, the chunks {q[e(k)] : k = 0..7}, {q[e(k)] : k = 8..15},
+// {q[16 + e(k)] / 16 : k = 0..7}, {q[16 + e(k)] / 16 : k = 8..15} with
+// e(2i) = 4i, e(2i+1) = 4i+2, e(2i+8) = 4i+1, e(2i+9) = 4i+3 (the MMA k
+// order of the weight words), plus the constants of build_fold_constants.
+// Every value is an integer, or one over 16, held exactly in f16.
+template <int T>
+__device__ __forceinline__ void build_f16_image(uint8_t *img, const uint8_t *src, int K, int tid, int nthreads)
+{
+    const XqLayout L = xq_layout(T, K, true);
+    const int nb = K / QK;
+    const unsigned short *xd = reinterpret_cast<const unsigned short *>(src + T * K);
+    for (int i = tid; i < 8 * nb; i += nthreads) {
+        const int t = i / nb, b = i - t * nb;
+        if (t < T) {
+            const uint4 *qp = reinterpret_cast<const uint4 *>(src + static_cast<long long>(t) * K + b * QK);
+            const uint4 qa = __ldcg(qp), qb = __ldcg(qp + 1);
+            const int8_t *qlo = reinterpret_cast<const int8_t *>(&qa);
+            const int8_t *qhi = reinterpret_cast<const int8_t *>(&qb);
+            unsigned w[16];
+#pragma unroll
+            for (int k = 0; k < 16; k += 2) {
+                const int i0 = 4 * ((k & 7) >> 1) + (k >> 3);  // e(k); e(k + 1) = e(k) + 2
+                const __half2 lo = __floats2half2_rn(static_cast<float>(qlo[i0]), static_cast<float>(qlo[i0 + 2]));
+                const __half2 hi = __floats2half2_rn(static_cast<float>(qhi[i0]) * 0.0625f,
+                                                     static_cast<float>(qhi[i0 + 2]) * 0.0625f);
+                w[k >> 1] = *reinterpret_cast<const unsigned *>(&lo);
+                w[8 + (k >> 1)] = *reinterpret_cast<const unsigned *>(&hi);
+            }
+            uint4 *dst = reinterpret_cast<uint4 *>(img + t * L.xstride + b * 64);
+#pragma unroll
+            for (int c = 0; c < 4; ++c) dst[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);
+            const int ones = 0x01010101;
+            int slo = 0, shi = 0;
+            slo = dp4a_ss((int)qa.x, ones, slo);
+            slo = dp4a_ss((int)qa.y, ones, slo);
+            slo = dp4a_ss((int)qa.z, ones, slo);
+            slo = dp4a_ss((int)qa.w, ones, slo);
+            shi = dp4a_ss((int)qb.x, ones, shi);
+            shi = dp4a_ss((int)qb.y, ones, shi);
+            shi = dp4a_ss((int)qb.z, ones, shi);
+            shi = dp4a_ss((int)qb.w, ones, shi);
+            mma_store_consts(img + L.off_cd, b, t, static_cast<float>(-(1032 * slo + 72 * shi)),
+                             __ldcg(xd + static_cast<long long>(t) * nb + b));
+        } else {
+            mma_store_consts(img + L.off_cd, b, t, 0.0f, 0);
         }
     }
 }
@@ -737,6 +860,11 @@ __device__ __forceinline__ unsigned copy_activations(uint8_t *img, const uint8_t
     return static_cast<unsigned>(T * K) + dbytes;
 }
 
+
+// Warps per CTA a T-token kernel may use: 16 (128 registers per thread),
+// except the dp4a path above two tokens, whose per-token accumulators need
+// more registers (8 warps).
+__host__ __device__ constexpr int max_warps_for(int T, bool mma) { return (mma || T <= 2) ? NWARPS_MAX : 8; }
 
 // ------------------------------------------------------------------ balanced mode
 //
@@ -1123,14 +1251,16 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
             }
             // the group's activations, one transaction count on one barrier
             if (tid == 0 && !*abort_flag) {
-                unsigned tx = 0;
-                for (int r = rg0; r < rg1; ++r) tx += static_cast<unsigned>(P.g[runs[r].gi].xq_bytes);
+                unsigned tx = 0;  // f16 operand images are built from global memory instead
+                for (int r = rg0; r < rg1; ++r)
+                    if (!xq_layout(T, runs[r].K, MMA).f16) tx += static_cast<unsigned>(P.g[runs[r].gi].xq_bytes);
                 x_unconfirmed = true;
                 fence_proxy_async_smem();
                 mbar_arrive_expect_tx(xbar, tx);
                 for (int r = rg0; r < rg1; ++r) {
                     const RunInfo &R = runs[r];
                     const Group &g = P.g[R.gi];
+                    if (xq_layout(T, R.K, MMA).f16) continue;
                     const unsigned dbytes = static_cast<unsigned>(g.xq_bytes - T * R.K);
                     copy_activations<T, MMA>(smem + R.xq_off, g.xq + static_cast<long long>(R.e) * g.xq_stride, R.K, dbytes,
                                         xbar, pol_x);
@@ -1140,7 +1270,16 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
             xphase ^= 1u;
             if (xok && tid == 0) x_unconfirmed = false;
             if (xok)
-                for (int r = rg0; r < rg1; ++r) build_fold_constants<T, MMA>(smem + runs[r].xq_off, runs[r].K, tid, nthreads);
+                for (int r = rg0; r < rg1; ++r) {
+                    const RunInfo &R = runs[r];
+                    if (MMA && xq_layout(T, R.K, MMA).f16) {
+                        const Group &g = P.g[R.gi];
+                        build_f16_image<T>(smem + R.xq_off, g.xq + static_cast<long long>(R.e) * g.xq_stride, R.K, tid,
+                                           nthreads);
+                    } else {
+                        build_fold_constants<T, MMA>(smem + R.xq_off, R.K, tid, nthreads);
+                    }
+                }
             __syncthreads();
 
             // compute, one visit (the segments of one slab inside one interval) at a time
@@ -1158,8 +1297,12 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
                 const int rows = tail_item ? P.g[R.gi].tail_rows : min(SLAB_ROWS, R.N - li * SLAB_ROWS);
                 const uint8_t *rows_base = w.Wi + static_cast<long long>(li) * SLAB_ROWS * nb * Q4_BYTES;
                 const XqLayout L = xq_layout(T, R.K, MMA);
-                const XqView xv{reinterpret_cast<const int8_t *>(smem + R.xq_off), L.xstride,
-                                reinterpret_cast<const int2 *>(smem + R.xq_off + L.off_cd), L.cdw};
+                XqView xv{reinterpret_cast<const int8_t *>(smem + R.xq_off), L.xstride,
+                          reinterpret_cast<const int2 *>(smem + R.xq_off + L.off_cd), L.cdw};
+                if constexpr (MMA) {
+                    xv.f16 = L.f16;
+                    mma_lane_offsets<T>(xv, r8, j);
+                }
                 float yv[NO];
     #pragma unroll
                 for (int k = 0; k < NO; ++k) yv[k] = 0.0f;
@@ -1241,21 +1384,35 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
             const int K = g.K, nb = g.nb, N = g.N;
             const int e_run = static_cast<int>(ra - g.item_begin) / g.items_per_inst;
             const XqLayout L = xq_layout(T, K, MMA);
-            const XqView xv{reinterpret_cast<const int8_t *>(smem), L.xstride,
-                            reinterpret_cast<const int2 *>(smem + L.off_cd), L.cdw};
+            XqView xv{reinterpret_cast<const int8_t *>(smem), L.xstride,
+                      reinterpret_cast<const int2 *>(smem + L.off_cd), L.cdw};
+            if constexpr (MMA) {
+                xv.f16 = L.f16;
+                mma_lane_offsets<T>(xv, r8, j);
+            }
 
             __syncthreads();
             if (tid == 0 && !*abort_flag) {
                 x_unconfirmed = true;
                 fence_proxy_async_smem();
                 const unsigned dbytes = static_cast<unsigned>(g.xq_bytes - T * K);
-                mbar_arrive_expect_tx(xbar, static_cast<unsigned>(T * K) + dbytes);
-                copy_activations<T, MMA>(smem, g.xq + static_cast<long long>(e_run) * g.xq_stride, K, dbytes, xbar, pol_x);
+                if (L.f16) {  // built from global memory below
+                    mbar_arrive_expect_tx(xbar, 0);
+                } else {
+                    mbar_arrive_expect_tx(xbar, static_cast<unsigned>(T * K) + dbytes);
+                    copy_activations<T, MMA>(smem, g.xq + static_cast<long long>(e_run) * g.xq_stride, K, dbytes, xbar,
+                                             pol_x);
+                }
             }
             const bool xok = mbar_wait_bounded(xbar, xphase, abort_flag, P.status, WAIT_LIMIT_NS);
             if (xok) x_unconfirmed = false;
             xphase ^= 1u;
-            if (xok) build_fold_constants<T, MMA>(smem, K, tid, nthreads);
+            if (xok) {
+                if (MMA && L.f16)
+                    build_f16_image<T>(smem, g.xq + static_cast<long long>(e_run) * g.xq_stride, K, tid, nthreads);
+                else
+                    build_fold_constants<T, MMA>(smem, K, tid, nthreads);
+            }
             __syncthreads();
 
             for (long long it = ra + warp; it < rb; it += nw) {

@@ -201,9 +201,10 @@ qgemv_status make_plan(const GroupSpec *gs, int n, int T, bool ggml, bool argmax
         if (P.g[i].split > 1) P.balanced_ok = 0;
     P.ring_depth = 0;
     // 2 stages per warp and the widest warp count that leaves room for the
-    // activations; then 8 warps; then a single stage.
+    // largest activation image; then, on the tensor-core path (whose warps
+    // are compute-bound), the widest count at one stage; then 8 warps.
     const int wide = ctas_per_sm > 1 ? 8 : max_warps_for(T, mma);
-    const int choices[3][2] = {{wide, 2}, {8, 2}, {8, 1}};
+    const int choices[4][2] = {{wide, 2}, {mma ? wide : 8, mma ? 1 : 2}, {8, 2}, {8, 1}};
     for (const auto &c : choices) {
         const int nw = c[0], D = c[1];
         const long long bars = align_up(8ll * (nw * D + 1), 128);

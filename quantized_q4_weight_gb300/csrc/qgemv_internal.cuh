@@ -220,11 +220,22 @@ __host__ __device__ __forceinline__ int quad_chunk(int jq, int r, int nbq)
 // padded on the tensor-core (MMA) path so that the eight token rows fall in
 // distinct banks), the fp16 scales as copied, then per block and token the folded
 // constant and d_x / 16 ({int, float} pairs, [block][T or 8]).
+// Tensor-core path constants per 4 blocks: for each block and token pair p
+// the accumulator start {C(2p), C(2p+1), C(2p), C(2p+1)} (4 x 4 x 16 bytes),
+// then the fp16 d_x pairs {d_x(2p), d_x(2p+1)} ordered [pair][block] (64 bytes).
+constexpr int CD_MMA_QUAD = 320;
+
+// Tensor-core path activation images up to this size hold the B operand
+// ready-made in f16 (64 bytes per token and block); larger ones hold the
+// int8 activations, converted by each warp as it goes.
+constexpr int MMA_F16_IMAGE_MAX = 40960;
+
 struct XqLayout {
+    int f16;      // tensor-core path: f16 operand image (else int8)
     int xstride;  // bytes between token rows
     int off_d;    // fp16 scales
     int off_cd;   // folded constants
-    int cdw;      // tokens per block in the constants (T, or 8 on the MMA path)
+    int cdw;      // tokens per block in the dp4a constants (T)
     int bytes;    // whole image, 128-byte multiple
 };
 
@@ -232,6 +243,21 @@ __host__ __device__ inline XqLayout xq_layout(int T, int K, bool mma)
 {
     const int nb = K / QK;
     XqLayout L;
+    L.f16 = 0;
+    if (mma) {
+        // f16 operand rows of 64 bytes per block; a row stride of 16 (mod 128)
+        // bytes puts the same block of eight token rows in distinct banks
+        const int xs = 64 * nb + ((nb & 1) ? 80 : 16);
+        if (static_cast<long long>(T) * xs <= MMA_F16_IMAGE_MAX) {
+            L.f16 = 1;
+            L.xstride = xs;
+            L.off_d = T * xs;  // no fp16 scales: the image is built from global memory
+            L.off_cd = L.off_d;
+            L.cdw = 8;
+            L.bytes = (L.off_cd + CD_MMA_QUAD * ((nb + QUAD - 1) / QUAD) + 127) & ~127;
+            return L;
+        }
+    }
     L.xstride = K;
     if (mma) {
         const int kw = K / 4;                    // words per row
@@ -240,7 +266,9 @@ __host__ __device__ inline XqLayout xq_layout(int T, int K, bool mma)
     L.off_d = T * L.xstride;
     L.off_cd = (L.off_d + 2 * T * nb + 15) & ~15;
     L.cdw = mma ? 8 : T;
-    L.bytes = (L.off_cd + 8 * L.cdw * nb + 127) & ~127;
+    // dp4a: 8 bytes per token and block; MMA: 320 bytes per 4 blocks
+    const int cd_bytes = mma ? CD_MMA_QUAD * ((nb + QUAD - 1) / QUAD) : 8 * L.cdw * nb;
+    L.bytes = (L.off_cd + cd_bytes + 127) & ~127;
     return L;
 }
 
