@@ -91,13 +91,11 @@ __device__ __forceinline__ ItemInfo decode_item(const Params<MAXG> &P, long long
 // First item whose (virtual) start byte is >= X.  Items are laid out in the
 // byte space as: slab s, segment part p at s * slab_bytes + seg0 * SEG_BYTES;
 // the tail after the slabs.
-template <int MAXG>
-__device__ long long first_item_at_or_after(const Params<MAXG> &P, long long X)
+// The first item whose weights start at or after byte X of the launch, for
+// the group g that holds X (g.byte_begin <= X <= the next group's byte_begin;
+// X below the launch's total).
+__device__ __forceinline__ long long first_item_in_group(const Group &g, long long X)
 {
-    if (X >= P.total_bytes) return P.total_items;
-    int gi = 0;
-    while (gi + 1 < P.ngroups && P.g[gi + 1].byte_begin <= X) ++gi;
-    const Group &g = P.g[gi];
     const long long local = X - g.byte_begin;
     const long long e = local / g.inst_bytes;
     const long long rem = local - e * g.inst_bytes;
@@ -117,6 +115,8 @@ __device__ long long first_item_at_or_after(const Params<MAXG> &P, long long X)
     if (rem == slabs_bytes) return base + static_cast<long long>(g.nslabs) * g.split;
     return base + g.items_per_inst;
 }
+
+
 
 // End of the run (same group and instance) that contains item i, clipped to i1.
 template <int MAXG>
@@ -879,6 +879,7 @@ __host__ __device__ constexpr int max_warps_for(int T, bool mma) { return (mma |
 // whole slabs, its boundary tail.
 
 constexpr int MAX_RUNS = 32;
+static_assert(GCACHE_GROUPS >= MAX_RUNS, "a balanced CTA's groups must fit the descriptor cache");
 
 struct RunInfo {
     const uint8_t *Wi;  // instance weights (expert resolved)
@@ -1094,6 +1095,8 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
     __shared__ int s_nruns;   // > 0: balanced mode with this many runs
     __shared__ int s_ngroups; // groups of consecutive runs whose activations fit together
     __shared__ int s_grp[MAX_RUNS + 1];  // first run of each group, then the run count
+    __shared__ int s_g0, s_g1;           // launch groups holding the CTA's first and last byte
+    __shared__ long long s_i0, s_i1;     // the CTA's item range
     __shared__ unsigned long long s_best[max_warps_for(T, MMA) * T];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -1119,22 +1122,55 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
 
     const long long b0 = P.total_bytes * blockIdx.x / gridDim.x;
     const long long b1 = P.total_bytes * (blockIdx.x + 1) / gridDim.x;
-    const long long i0 = first_item_at_or_after(P, b0);
-    const long long i1 = first_item_at_or_after(P, b1);
+
+    // The groups holding this CTA's first and last byte (from the host's
+    // table: the first byte of the next range lies in group cta_g0[c + 1],
+    // and the last byte of this one there too unless that group starts
+    // exactly at the boundary), then those groups' descriptors copied to
+    // shared memory by every thread in parallel.
+    Group *gcache = reinterpret_cast<Group *>(smem + P.off_gcache);
+    if (tid == 0) {
+        const int ga = P.cta_g0[blockIdx.x];
+        int gb = P.cta_g0[blockIdx.x + 1];
+        if (b1 < P.total_bytes && gb > ga && P.g[gb].byte_begin >= b1) --gb;
+        s_g0 = ga;
+        s_g1 = gb;
+    }
+    __syncthreads();
+    const int g0 = s_g0, g1 = s_g1;
+    const int ngc = min(g1 - g0 + 1, GCACHE_GROUPS);
+    {
+        static_assert(sizeof(Group) % 8 == 0, "group descriptors are copied in 8-byte words");
+        const unsigned long long *src = reinterpret_cast<const unsigned long long *>(&P.g[g0]);
+        unsigned long long *dst = reinterpret_cast<unsigned long long *>(gcache);
+        const int words = ngc * static_cast<int>(sizeof(Group) / 8);
+        for (int wd = tid; wd < words; wd += nthreads) dst[wd] = src[wd];
+    }
+    __syncthreads();
 
     if (tid == 0) {
         s_abort = 0;
         mbar_init(xbar, 1);
+        s_i0 = b0 >= P.total_bytes ? P.total_items : first_item_in_group(gcache[0], b0);
+        s_i1 = b1 >= P.total_bytes ? P.total_items
+                                   : first_item_in_group(g1 - g0 < ngc ? gcache[g1 - g0] : P.g[g1], b1);
+    }
+    __syncthreads();
+    const long long i0 = s_i0, i1 = s_i1;
+
+    if (tid == 0) {
         // Run table for the balanced mode (thread 0 walks the CTA's runs),
         // cut into groups of consecutive runs whose activation images fit the
         // activation area together; each group's images start at offset 0.
         int nr = 0, stages = 0, xoff = 0, ng = 0;
-        bool fits = P.balanced_ok != 0;
+        bool fits = P.balanced_ok != 0 && g1 - g0 < ngc;  // a longer span has more runs than MAX_RUNS
         s_grp[0] = 0;
-        int gh = 0;
+        int gh = g0;
         for (long long ra = i0; ra < i1 && fits;) {
-            const long long rb = run_end(P, ra, i1, gh);
-            const Group &g = P.g[gh];
+            while (gh + 1 <= g1 && gcache[gh + 1 - g0].item_begin <= ra) ++gh;
+            const Group &g = gcache[gh - g0];
+            const int ra_inst = static_cast<int>(ra - g.item_begin) / g.items_per_inst;
+            const long long rb = min(i1, g.item_begin + static_cast<long long>(ra_inst + 1) * g.items_per_inst);
             if (nr == MAX_RUNS) {
                 fits = false;
                 break;
@@ -1530,11 +1566,24 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
         if (tid == 0) s_last = (atomicAdd(P.am_cnt, 1u) == gridDim.x - 1) ? 1 : 0;
         __syncthreads();
         if (s_last) {
+            // every CTA's candidates, one per thread, then a warp and a CTA maximum
             __threadfence();
+#pragma unroll
+            for (int t = 0; t < T; ++t) {
+                unsigned long long m = 0ull;
+                for (unsigned c = tid; c < gridDim.x; c += nthreads)
+                    m = max(m, __ldcg(P.am_cand + static_cast<long long>(c) * T + t));
+#pragma unroll
+                for (int off = 16; off > 0; off >>= 1) {
+                    const unsigned long long o = __shfl_xor_sync(0xFFFFFFFFu, m, off);
+                    m = o > m ? o : m;
+                }
+                if (lane == 0) s_best[warp * T + t] = m;
+            }
+            __syncthreads();
             if (tid < T) {
                 unsigned long long m = 0ull;
-                for (unsigned c = 0; c < gridDim.x; ++c)
-                    m = max(m, __ldcg(P.am_cand + static_cast<long long>(c) * T + tid));
+                for (int w = 0; w < nw; ++w) m = max(m, s_best[w * T + tid]);
                 P.am_idx[tid] = static_cast<long long>(0xFFFFFFFFull - (m & 0xFFFFFFFFull));
             }
             if (tid == 0) *P.am_cnt = 0u;

@@ -195,7 +195,8 @@ qgemv_status make_plan(const GroupSpec *gs, int n, int T, bool ggml, bool argmax
     P.off_d = 0;
     P.off_cd = 0;
     const long long tables = align_up(static_cast<long long>(MAX_RUNS) * sizeof(RunInfo), 128) +
-                             align_up(static_cast<long long>(NWARPS_MAX) * T * 16 * 4, 128) + 128;
+                             align_up(static_cast<long long>(NWARPS_MAX) * T * 16 * 4, 128) + 128 +
+                             align_up(static_cast<long long>(GCACHE_GROUPS) * sizeof(Group), 128);
     P.balanced_ok = 1;
     for (int i = 0; i < n; ++i)
         if (P.g[i].split > 1) P.balanced_ok = 0;
@@ -218,6 +219,7 @@ qgemv_status make_plan(const GroupSpec *gs, int n, int T, bool ggml, bool argmax
             P.off_runs = static_cast<int>(xa);
             P.off_hbuf = static_cast<int>(xa + align_up(static_cast<long long>(MAX_RUNS) * sizeof(RunInfo), 128));
             P.off_hflag = static_cast<int>(P.off_hbuf + align_up(static_cast<long long>(NWARPS_MAX) * T * 16 * 4, 128));
+            P.off_gcache = P.off_hflag + 128;
             P.off_bar = static_cast<int>(xa + tables);
             P.off_ring = static_cast<int>(xa + tables + bars);
             pl.smem = static_cast<size_t>(xa + tables + bars + rings);
@@ -279,6 +281,21 @@ qgemv_status plan_launch(const GroupSpec *gs, int n, int T, bool ggml, bool argm
     return s;
 }
 
+// Group holding the first byte of each CTA's range (and of the range after
+// the last one), so that the kernel's prologue reads two descriptors instead
+// of searching the list.
+template <int MAXG>
+void set_cta_groups(Params<MAXG> &P, int grid)
+{
+    int gi = 0;
+    for (int c = 0; c <= grid; ++c) {
+        long long b = P.total_bytes * c / grid;
+        if (b >= P.total_bytes) b = P.total_bytes - 1;
+        while (gi + 1 < P.ngroups && P.g[gi + 1].byte_begin <= b) ++gi;
+        P.cta_g0[c] = static_cast<unsigned char>(gi);
+    }
+}
+
 inline int grid_for(const DevInfo &d, int ctas_per_sm)
 {
     const int w = g_waves.load(std::memory_order_relaxed);
@@ -332,6 +349,7 @@ qgemv_status run_single(const void *W, qgemv_wlayout layout, const void *xq, flo
     pl.P.status = dev.status;
     pl.P.am_idx = reinterpret_cast<long long *>(idx);
     const int grid = grid_for(dev, cps);
+    set_cta_groups(pl.P, grid);
     const cudaError_t e = argmax ? dispatch_T<MAXG_SMALL, true>(pl.P, T, mma_for(T), grid, pl.smem, st, pdl)
                                  : dispatch_T<MAXG_SMALL, false>(pl.P, T, mma_for(T), grid, pl.smem, st, pdl);
     return e == cudaSuccess ? QGEMV_OK : QGEMV_ERR_CUDA;
@@ -542,6 +560,7 @@ static qgemv_status launch_seq(const qgemv_seq_item *items, const float *const *
         if (s != QGEMV_OK) return s;
         if (static_cast<long long>(ws_bytes) < pl->ws_bytes) return QGEMV_ERR_WORKSPACE;
         pl->P.status = dev.status;
+        set_cta_groups(pl->P, grid);
         if (xs) {
             ql->n = cn;
             long long blocks = 0;
@@ -690,6 +709,7 @@ qgemv_status qgemv_q4_0_gather(const qgemv_gather_matrix *mats, int n_mats, cons
     pl.P.ids = ids;
     pl.P.n_experts = n_experts;
     const int grid = grid_for(dev, cps);
+    set_cta_groups(pl.P, grid);
     return dispatch_T<MAXG_SMALL, false>(pl.P, T, mma_for(T), grid, pl.smem, reinterpret_cast<cudaStream_t>(stream), false) ==
                    cudaSuccess
                ? QGEMV_OK

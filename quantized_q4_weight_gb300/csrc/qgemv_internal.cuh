@@ -62,6 +62,8 @@ struct Params {
     int kmax, nbmax;        // largest K / blocks per row over the groups
     int off_d, off_cd, off_bar, off_ring;  // dynamic shared-memory layout
     int off_runs, off_hbuf, off_hflag;     //   (balanced-mode tables)
+    int off_gcache;                        //   (group descriptors of the CTA's range)
+    unsigned char cta_g0[MAX_GRID + 1];    // group holding the first byte of CTA c's range
     int xq_area;            // bytes at offset 0 for activations
     int balanced_ok;        // every group unsplit: CTAs may balance by stages
     const int *ids;         // gather: slot -> expert id (nullptr: slot index)
@@ -75,7 +77,10 @@ struct Params {
 };
 
 constexpr int MAXG_SMALL = 4;
+constexpr int GCACHE_GROUPS = 34;  // launch groups a CTA caches in shared memory (MAX_RUNS + 2)
 constexpr int MAXG_SEQ = 224;  // keeps the parameter block under the 32 KB kernel-parameter limit
+static_assert(MAXG_SEQ <= 256, "CTA start groups are stored as bytes");
+static_assert(sizeof(Params<MAXG_SEQ>) <= 32764, "kernel parameters are limited to 32764 bytes");
 
 // ------------------------------------------------------------------ PTX helpers
 
