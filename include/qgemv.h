@@ -270,9 +270,11 @@ qgemv_status qgemv_debug_stream_read(const void *src, size_t bytes, int method, 
  *                2 = two CTAs of 8 warps), waves: CTAs per SM slot in one
  *                launch, mma_min_T: token count from which T > 1 runs on the
  *                f16 tensor-core path (mma.sync m16n8k16 over exact
- *                integer operands; default 5, 9 = never) instead of dp4a.
+ *                integer operands; default 5, 9 = never) instead of dp4a,
+ *   ring_depth:  weight stages in flight per warp (1..6; default 3 for one
+ *                token, else 2), used where the activations leave room.
  * Process-wide; affects launches enqueued afterwards. */
-qgemv_status qgemv_set_tuning(int ctas_per_sm, int waves, int mma_min_T);
+qgemv_status qgemv_set_tuning(int ctas_per_sm, int waves, int mma_min_T, int ring_depth);
 
 /* Read and clear the current device's status word: QGEMV_OK, or the first
  * asynchronous error a kernel recorded (QGEMV_ERR_TIMEOUT, QGEMV_ERR_BAD_ID)

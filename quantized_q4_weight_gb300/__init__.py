@@ -71,7 +71,7 @@ _SIGS = {
     "qgemv_q4_0_gather": ([ctypes.POINTER(GatherMatrix), _I32, _VP, _I32, _I32, _I32, _I32, _VP, _SZ, _VP], _I32),
     "qgemv_debug_block_isums": ([_VP, _I32, _VP, _VP, _I64, _I64, _I32, _VP], _I32),
     "qgemv_debug_stream_read": ([_VP, _SZ, _I32, _I32, _I32, _I32, _VP, _VP], _I32),
-    "qgemv_set_tuning": ([_I32, _I32, _I32], _I32),
+    "qgemv_set_tuning": ([_I32, _I32, _I32, _I32], _I32),
     "qgemv_device_status": ([ctypes.POINTER(ctypes.c_int)], _I32),
 }
 
@@ -242,9 +242,9 @@ def stream_read(src, method: int, warps: int, depth: int, stage_bytes: int, sink
                                          stage_bytes, _ptr(sink), _stream(stream)), "qgemv_debug_stream_read")
 
 
-def set_tuning(ctas_per_sm: int = 0, waves: int = 0, mma_min_T: int = 0):
+def set_tuning(ctas_per_sm: int = 0, waves: int = 0, mma_min_T: int = 0, ring_depth: int = 0):
     """Tuning of the streaming kernel (0 = default for each); results are unchanged."""
-    _check(lib().qgemv_set_tuning(ctas_per_sm, waves, mma_min_T), "qgemv_set_tuning")
+    _check(lib().qgemv_set_tuning(ctas_per_sm, waves, mma_min_T, ring_depth), "qgemv_set_tuning")
 
 
 def device_status() -> int:

@@ -1099,20 +1099,37 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
     __shared__ long long s_i0, s_i1;     // the CTA's item range
     __shared__ unsigned long long s_best[max_warps_for(T, MMA) * T];
 
+    __shared__ ParamHead H;              // the scalar launch parameters
+
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    const int nw = P.nwarps, nthreads = nw * 32;
+    // One round of parallel parameter reads: the scalar header into shared
+    // memory, and from the host's table the group holding this CTA's first
+    // byte and the one holding the next range's first byte.
+    {
+        static_assert(sizeof(ParamHead) % 8 == 0, "the header is copied in 8-byte words");
+        constexpr int HW = static_cast<int>(sizeof(ParamHead) / 8);
+        if (tid < HW)
+            reinterpret_cast<unsigned long long *>(&H)[tid] =
+                reinterpret_cast<const unsigned long long *>(static_cast<const ParamHead *>(&P))[tid];
+        else if (tid == HW)
+            s_g0 = P.cta_g0[blockIdx.x];
+        else if (tid == HW + 1)
+            s_g1 = P.cta_g0[blockIdx.x + 1];
+    }
+    __syncthreads();
+    const int nw = H.nwarps, nthreads = nw * 32;
     const int r8 = lane >> 2, j = lane & 3;
-    const int D = P.ring_depth;
-    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + P.off_bar);
+    const int D = H.ring_depth;
+    uint64_t *bars = reinterpret_cast<uint64_t *>(smem + H.off_bar);
     uint64_t *xbar = bars + nw * D;
-    RunInfo *runs = reinterpret_cast<RunInfo *>(smem + P.off_runs);
-    float *hbuf = reinterpret_cast<float *>(smem + P.off_hbuf);          // [nw][T][16]
-    volatile int *hflag = reinterpret_cast<volatile int *>(smem + P.off_hflag);
+    RunInfo *runs = reinterpret_cast<RunInfo *>(smem + H.off_runs);
+    float *hbuf = reinterpret_cast<float *>(smem + H.off_hbuf);          // [nw][T][16]
+    volatile int *hflag = reinterpret_cast<volatile int *>(smem + H.off_hflag);
     volatile int *abort_flag = &s_abort;
-    const bool ggml = P.ggml != 0;
+    const bool ggml = H.ggml != 0;
 
     Ring ring;
-    ring.base = smem + P.off_ring + static_cast<size_t>(warp) * D * SEG_BYTES;
+    ring.base = smem + H.off_ring + static_cast<size_t>(warp) * D * SEG_BYTES;
     ring.bar = bars + warp * D;
     ring.D = D;
     ring.slot = 0;
@@ -1120,25 +1137,15 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
     ring.issued = 0;
     ring.consumed = 0;
 
-    const long long b0 = P.total_bytes * blockIdx.x / gridDim.x;
-    const long long b1 = P.total_bytes * (blockIdx.x + 1) / gridDim.x;
+    const long long b0 = H.total_bytes * blockIdx.x / gridDim.x;
+    const long long b1 = H.total_bytes * (blockIdx.x + 1) / gridDim.x;
 
-    // The groups holding this CTA's first and last byte (from the host's
-    // table: the first byte of the next range lies in group cta_g0[c + 1],
-    // and the last byte of this one there too unless that group starts
-    // exactly at the boundary), then those groups' descriptors copied to
-    // shared memory by every thread in parallel.
-    Group *gcache = reinterpret_cast<Group *>(smem + P.off_gcache);
-    if (tid == 0) {
-        const int ga = P.cta_g0[blockIdx.x];
-        int gb = P.cta_g0[blockIdx.x + 1];
-        if (b1 < P.total_bytes && gb > ga && P.g[gb].byte_begin >= b1) --gb;
-        s_g0 = ga;
-        s_g1 = gb;
-    }
-    __syncthreads();
-    const int g0 = s_g0, g1 = s_g1;
-    const int ngc = min(g1 - g0 + 1, GCACHE_GROUPS);
+    // The descriptors of the groups from g0 to gn, copied to shared memory by
+    // every thread in parallel; this range's last byte lies in gn unless gn
+    // starts exactly at b1.
+    Group *gcache = reinterpret_cast<Group *>(smem + H.off_gcache);
+    const int g0 = s_g0, gn = s_g1;
+    const int ngc = min(gn - g0 + 1, GCACHE_GROUPS);
     {
         static_assert(sizeof(Group) % 8 == 0, "group descriptors are copied in 8-byte words");
         const unsigned long long *src = reinterpret_cast<const unsigned long long *>(&P.g[g0]);
@@ -1147,12 +1154,14 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
         for (int wd = tid; wd < words; wd += nthreads) dst[wd] = src[wd];
     }
     __syncthreads();
+    const Group &gnd = gn - g0 < ngc ? gcache[gn - g0] : P.g[gn];
+    const int g1 = (b1 < H.total_bytes && gn > g0 && gnd.byte_begin >= b1) ? gn - 1 : gn;
 
     if (tid == 0) {
         s_abort = 0;
         mbar_init(xbar, 1);
-        s_i0 = b0 >= P.total_bytes ? P.total_items : first_item_in_group(gcache[0], b0);
-        s_i1 = b1 >= P.total_bytes ? P.total_items
+        s_i0 = b0 >= H.total_bytes ? H.total_items : first_item_in_group(gcache[0], b0);
+        s_i1 = b1 >= H.total_bytes ? H.total_items
                                    : first_item_in_group(g1 - g0 < ngc ? gcache[g1 - g0] : P.g[g1], b1);
     }
     __syncthreads();
@@ -1163,7 +1172,7 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
         // cut into groups of consecutive runs whose activation images fit the
         // activation area together; each group's images start at offset 0.
         int nr = 0, stages = 0, xoff = 0, ng = 0;
-        bool fits = P.balanced_ok != 0 && g1 - g0 < ngc;  // a longer span has more runs than MAX_RUNS
+        bool fits = H.balanced_ok != 0 && g1 - g0 < ngc;  // a longer span has more runs than MAX_RUNS
         s_grp[0] = 0;
         int gh = g0;
         for (long long ra = i0; ra < i1 && fits;) {
@@ -1178,9 +1187,9 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
             const int local = static_cast<int>(ra - g.item_begin);
             const int e = local / g.items_per_inst;
             int expert = e, bad = 0;
-            if (P.ids != nullptr) {
-                expert = __ldg(P.ids + e);
-                bad = (expert < 0 || expert >= P.n_experts) ? 1 : 0;
+            if (H.ids != nullptr) {
+                expert = __ldg(H.ids + e);
+                bad = (expert < 0 || expert >= H.n_experts) ? 1 : 0;
                 if (bad) expert = 0;
             }
             RunInfo &R = runs[nr];
@@ -1198,8 +1207,8 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
             R.nslabs = g.nslabs;
             R.bad = bad;
             const int xb = xq_layout(T, g.K, MMA).bytes;
-            if (xb > P.xq_area) fits = false;
-            if (nr > 0 && xoff + xb > P.xq_area) {  // close the group
+            if (xb > H.xq_area) fits = false;
+            if (nr > 0 && xoff + xb > H.xq_area) {  // close the group
                 s_grp[++ng] = nr;
                 xoff = 0;
             }
@@ -1233,6 +1242,7 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
 
     if (nruns > 0) {
         // ================================================= balanced mode
+        // (the run's groups g0..g1 are all in the descriptor cache)
         const int ngroups = s_ngroups;
         for (int gidx = 0; gidx < ngroups; ++gidx) {
             const int rg0 = s_grp[gidx], rg1 = s_grp[gidx + 1];
@@ -1289,27 +1299,27 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
             if (tid == 0 && !*abort_flag) {
                 unsigned tx = 0;  // f16 operand images are built from global memory instead
                 for (int r = rg0; r < rg1; ++r)
-                    if (!xq_layout(T, runs[r].K, MMA).f16) tx += static_cast<unsigned>(P.g[runs[r].gi].xq_bytes);
+                    if (!xq_layout(T, runs[r].K, MMA).f16) tx += static_cast<unsigned>(gcache[runs[r].gi - g0].xq_bytes);
                 x_unconfirmed = true;
                 fence_proxy_async_smem();
                 mbar_arrive_expect_tx(xbar, tx);
                 for (int r = rg0; r < rg1; ++r) {
                     const RunInfo &R = runs[r];
-                    const Group &g = P.g[R.gi];
+                    const Group &g = gcache[R.gi - g0];
                     if (xq_layout(T, R.K, MMA).f16) continue;
                     const unsigned dbytes = static_cast<unsigned>(g.xq_bytes - T * R.K);
                     copy_activations<T, MMA>(smem + R.xq_off, g.xq + static_cast<long long>(R.e) * g.xq_stride, R.K, dbytes,
                                         xbar, pol_x);
                 }
             }
-            const bool xok = mbar_wait_bounded(xbar, xphase, abort_flag, P.status, WAIT_LIMIT_NS);
+            const bool xok = mbar_wait_bounded(xbar, xphase, abort_flag, H.status, WAIT_LIMIT_NS);
             xphase ^= 1u;
             if (xok && tid == 0) x_unconfirmed = false;
             if (xok)
                 for (int r = rg0; r < rg1; ++r) {
                     const RunInfo &R = runs[r];
                     if (MMA && xq_layout(T, R.K, MMA).f16) {
-                        const Group &g = P.g[R.gi];
+                        const Group &g = gcache[R.gi - g0];
                         build_f16_image<T>(smem + R.xq_off, g.xq + static_cast<long long>(R.e) * g.xq_stride, R.K, tid,
                                            nthreads);
                     } else {
@@ -1330,7 +1340,7 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
                 const bool tail_item = li >= w.nslabs;
                 const bool direct = ggml || tail_item;
                 const int nb = w.nb;
-                const int rows = tail_item ? P.g[R.gi].tail_rows : min(SLAB_ROWS, R.N - li * SLAB_ROWS);
+                const int rows = tail_item ? gcache[R.gi - g0].tail_rows : min(SLAB_ROWS, R.N - li * SLAB_ROWS);
                 const uint8_t *rows_base = w.Wi + static_cast<long long>(li) * SLAB_ROWS * nb * Q4_BYTES;
                 const XqLayout L = xq_layout(T, R.K, MMA);
                 XqView xv{reinterpret_cast<const int8_t *>(smem + R.xq_off), L.xstride,
@@ -1344,7 +1354,7 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
                 for (int k = 0; k < NO; ++k) yv[k] = 0.0f;
                 if (s_first > 0) {
                     // tail of a slab begun by warp - 1: continue from its ordered sum
-                    if (lane == 0) wait_flag(&hflag[warp - 1], abort_flag, P.status);
+                    if (lane == 0) wait_flag(&hflag[warp - 1], abort_flag, H.status);
                     __syncwarp();
                     __threadfence_block();
                     const float *H = hbuf + (warp - 1) * T * 16;
@@ -1365,7 +1375,7 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
                             have = true;
                         }
                     } else {
-                        if (ok) ok = mbar_wait_bounded(&ring.bar[ring.slot], ring.phase, abort_flag, P.status, WAIT_LIMIT_NS);
+                        if (ok) ok = mbar_wait_bounded(&ring.bar[ring.slot], ring.phase, abort_flag, H.status, WAIT_LIMIT_NS);
                         if (ok) {
                             segment_sum<T, MMA>(true, ring.stage(), nullptr, 0, sg, nb, r8, j, xv, Pk);
                             have = true;
@@ -1397,7 +1407,7 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
                 } else if (!w.bad) {
                     store_outputs<T, MMA, ARGMAX>(R.y, R.N, li * SLAB_ROWS, rows, r8, j, yv, best);
                 } else if (lane == 0) {
-                    atomicCAS(P.status, 0u, ST_BAD_ID);
+                    atomicCAS(H.status, 0u, ST_BAD_ID);
                 }
                 w.next_item(runs);
             }
@@ -1440,7 +1450,7 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
                                              pol_x);
                 }
             }
-            const bool xok = mbar_wait_bounded(xbar, xphase, abort_flag, P.status, WAIT_LIMIT_NS);
+            const bool xok = mbar_wait_bounded(xbar, xphase, abort_flag, H.status, WAIT_LIMIT_NS);
             if (xok) x_unconfirmed = false;
             xphase ^= 1u;
             if (xok) {
@@ -1454,7 +1464,7 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
             for (long long it = ra + warp; it < rb; it += nw) {
                 const ItemInfo inf = decode_item(P, it, gi_item);
                 if (inf.bad) {
-                    if (lane == 0) atomicCAS(P.status, 0u, ST_BAD_ID);
+                    if (lane == 0) atomicCAS(H.status, 0u, ST_BAD_ID);
                     continue;
                 }
                 const bool direct = ggml || inf.kind != 0;
@@ -1475,7 +1485,7 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
                             have = true;
                         }
                     } else {
-                        const bool ok = mbar_wait_bounded(&ring.bar[ring.slot], ring.phase, abort_flag, P.status,
+                        const bool ok = mbar_wait_bounded(&ring.bar[ring.slot], ring.phase, abort_flag, H.status,
                                                           WAIT_LIMIT_NS);
                         if (ok && xok) {
                             segment_sum<T, MMA>(true, ring.stage(), nullptr, 0, sg, nb, r8, j, xv, Pk);
@@ -1559,11 +1569,11 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
         if (tid < T) {
             unsigned long long m = 0ull;
             for (int w = 0; w < nw; ++w) m = max(m, s_best[w * T + tid]);
-            P.am_cand[static_cast<long long>(blockIdx.x) * T + tid] = m;
+            H.am_cand[static_cast<long long>(blockIdx.x) * T + tid] = m;
+            __threadfence();  // the candidate is visible before the arrival below
         }
-        __threadfence();
         __syncthreads();
-        if (tid == 0) s_last = (atomicAdd(P.am_cnt, 1u) == gridDim.x - 1) ? 1 : 0;
+        if (tid == 0) s_last = (atomicAdd(H.am_cnt, 1u) == gridDim.x - 1) ? 1 : 0;
         __syncthreads();
         if (s_last) {
             // every CTA's candidates, one per thread, then a warp and a CTA maximum
@@ -1572,7 +1582,7 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
             for (int t = 0; t < T; ++t) {
                 unsigned long long m = 0ull;
                 for (unsigned c = tid; c < gridDim.x; c += nthreads)
-                    m = max(m, __ldcg(P.am_cand + static_cast<long long>(c) * T + t));
+                    m = max(m, __ldcg(H.am_cand + static_cast<long long>(c) * T + t));
 #pragma unroll
                 for (int off = 16; off > 0; off >>= 1) {
                     const unsigned long long o = __shfl_xor_sync(0xFFFFFFFFu, m, off);
@@ -1584,9 +1594,9 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
             if (tid < T) {
                 unsigned long long m = 0ull;
                 for (int w = 0; w < nw; ++w) m = max(m, s_best[w * T + tid]);
-                P.am_idx[tid] = static_cast<long long>(0xFFFFFFFFull - (m & 0xFFFFFFFFull));
+                H.am_idx[tid] = static_cast<long long>(0xFFFFFFFFull - (m & 0xFFFFFFFFull));
             }
-            if (tid == 0) *P.am_cnt = 0u;
+            if (tid == 0) *H.am_cnt = 0u;
         }
     }
 }

@@ -32,7 +32,7 @@ struct DevInfo {
 // Launch shape of the streaming kernel: CTAs resident per SM (1, or 2 of
 // 8 warps for T <= 2) and waves of CTAs per launch.  More, smaller CTAs let
 // the block scheduler give more work to SMs that stream faster.
-std::atomic<int> g_ctas_per_sm{0}, g_waves{0};
+std::atomic<int> g_ctas_per_sm{0}, g_waves{0}, g_ring_depth{0};
 // Token count from which T > 1 runs on the f16 tensor-core path (0 = default).
 std::atomic<int> g_mma_min_T{0};
 constexpr int kDefaultMmaMinT = 5;
@@ -205,7 +205,9 @@ qgemv_status make_plan(const GroupSpec *gs, int n, int T, bool ggml, bool argmax
     // largest activation image; then, on the tensor-core path (whose warps
     // are compute-bound), the widest count at one stage; then 8 warps.
     const int wide = ctas_per_sm > 1 ? 8 : max_warps_for(T, mma);
-    const int choices[4][2] = {{wide, 2}, {mma ? wide : 8, mma ? 1 : 2}, {8, 2}, {8, 1}};
+    const int rd = g_ring_depth.load(std::memory_order_relaxed);
+    const int D0 = rd > 0 ? rd : (!mma && T == 1 ? 3 : 2);  // measured defaults
+    const int choices[5][2] = {{wide, D0}, {mma ? wide : 8, mma ? 1 : D0}, {8, D0}, {8, 2}, {8, 1}};
     for (const auto &c : choices) {
         const int nw = c[0], D = c[1];
         const long long bars = align_up(8ll * (nw * D + 1), 128);
@@ -259,7 +261,8 @@ inline int ctas_per_sm_for(int T, bool sequence)
     const int c = g_ctas_per_sm.load(std::memory_order_relaxed);
     if (!mma_for(T) && T > 2) return 1;  // 8 warps of wide accumulators fill the register file
     if (c >= 1 && c <= 2) return c;
-    return sequence ? 2 : 1;  // measured: long lists gain from two CTAs per SM, single matrices do not
+    (void)sequence;  // measured: one CTA per SM with three stages per warp beats two CTAs of 8 warps
+    return 1;
 }
 inline int smem_budget(const DevInfo &d, int ctas_per_sm)
 {
@@ -747,13 +750,15 @@ qgemv_status qgemv_debug_stream_read(const void *src, size_t bytes, int method, 
                : QGEMV_ERR_CUDA;
 }
 
-qgemv_status qgemv_set_tuning(int ctas_per_sm, int waves, int mma_min_T)
+qgemv_status qgemv_set_tuning(int ctas_per_sm, int waves, int mma_min_T, int ring_depth)
 {
-    if (ctas_per_sm < 0 || ctas_per_sm > 2 || waves < 0 || waves > 6 || mma_min_T < 0 || mma_min_T > 9)
+    if (ctas_per_sm < 0 || ctas_per_sm > 2 || waves < 0 || waves > 6 || mma_min_T < 0 || mma_min_T > 9 ||
+        ring_depth < 0 || ring_depth > MAX_RING)
         return QGEMV_ERR_INVALID_ARG;
     g_ctas_per_sm.store(ctas_per_sm);
     g_waves.store(waves);
     g_mma_min_T.store(mma_min_T);
+    g_ring_depth.store(ring_depth);
     return QGEMV_OK;
 }
 

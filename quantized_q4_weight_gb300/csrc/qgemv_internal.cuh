@@ -53,8 +53,8 @@ struct Group {
     float *part;                      // split-K partials [count][nslabs][nseg][T][16]
 };
 
-template <int MAXG>
-struct Params {
+// Scalar launch parameters (copied to shared memory at kernel entry).
+struct ParamHead {
     int ngroups;
     int ggml;               // weights in GGML layout (no TMA staging)
     int nwarps;             // warps per CTA (blockDim.x / 32)
@@ -63,7 +63,6 @@ struct Params {
     int off_d, off_cd, off_bar, off_ring;  // dynamic shared-memory layout
     int off_runs, off_hbuf, off_hflag;     //   (balanced-mode tables)
     int off_gcache;                        //   (group descriptors of the CTA's range)
-    unsigned char cta_g0[MAX_GRID + 1];    // group holding the first byte of CTA c's range
     int xq_area;            // bytes at offset 0 for activations
     int balanced_ok;        // every group unsplit: CTAs may balance by stages
     const int *ids;         // gather: slot -> expert id (nullptr: slot index)
@@ -73,7 +72,12 @@ struct Params {
     unsigned *am_cnt;             // argmax: CTA arrival counter
     long long *am_idx;            // argmax: result [T]
     unsigned *status;             // per-device status word
+};
+
+template <int MAXG>
+struct Params : ParamHead {
     Group g[MAXG];
+    unsigned char cta_g0[MAX_GRID + 1];  // group holding the first byte of CTA c's range
 };
 
 constexpr int MAXG_SMALL = 4;

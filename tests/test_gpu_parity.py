@@ -445,3 +445,24 @@ def test_paths_at_extreme_magnitudes(orc, T):
         assert torch.equal(outs[0].view(torch.int32), o.view(torch.int32))
     y64, S = orc.gemv(Wg, N, K, orc.quantize(x), T)
     check_close(outs[0].numpy(), y64, S, f"extremes T={T}")
+
+
+@pytest.mark.parametrize("ring_depth", [1, 3, 6])
+def test_ring_depth_leaves_results_unchanged(orc, ring_depth):
+    """The weight-stage depth per warp is a tuning knob only: same bits."""
+    N, K, T = 300, 2080, 1
+    Wg, Wp = weights(900 + ring_depth, N, K, q.W_PACKED)
+    x, xd, xq = quantized(901, T, K)
+    ref = q.gemv(Wp, q.W_PACKED, xq, N, K, T, ws_for(N, K, T)).cpu()
+    ys = [torch.empty((T, N), dtype=torch.float32, device=DEV) for _ in range(40)]
+    items = q.seq_items([(Wp, xq, y, N, K) for y in ys])
+    try:
+        q.set_tuning(0, 0, 0, ring_depth)
+        got = q.gemv(Wp, q.W_PACKED, xq, N, K, T, ws_for(N, K, T)).cpu()
+        q.gemv_seq(items, q.W_PACKED, T, q.new_workspace(q.seq_workspace_bytes(items, T)))
+        torch.cuda.synchronize()
+    finally:
+        q.set_tuning(0, 0, 0, 0)
+    assert q.device_status() == 0
+    for o in [got] + [y.cpu() for y in ys[::13]]:
+        assert torch.equal(ref.view(torch.int32), o.view(torch.int32))
