@@ -141,9 +141,10 @@ qgemv_status qgemv_q4_0(const void *W, qgemv_wlayout layout, const void *xq, flo
                         int64_t N, int64_t K, int T, void *ws, size_t ws_bytes,
                         qgemv_stream_t stream);
 
-/* Same as qgemv_q4_0 with fp32 input x[T][K]: the activations are quantised
- * into the workspace first (a separate kernel, chained with programmatic
- * dependent launch so the GEMV's weight stream starts while it runs). */
+/* Same as qgemv_q4_0 with fp32 input x[T][K] (4-byte aligned): the GEMV
+ * kernel quantises the activations itself (Q8_0, the same bytes as
+ * qgemv_quantize_q8_0) while it builds its shared-memory copy of them; one
+ * launch, which streams weights before it reads x. */
 qgemv_status qgemv_q4_0_f32(const void *W, qgemv_wlayout layout, const float *x, float *y,
                             int64_t N, int64_t K, int T, void *ws, size_t ws_bytes,
                             qgemv_stream_t stream);
@@ -211,11 +212,12 @@ typedef struct {
 /* Workspace bytes for qgemv_q4_0_seq_f32 on this list (0 if invalid). */
 size_t qgemv_seq_f32_workspace_bytes(const qgemv_seq_f32_item *items, int n, int T);
 
-/* qgemv_q4_0_seq with fp32 inputs: every item's activations are quantised
- * (Q8_0, as qgemv_quantize_q8_0) into the workspace by one launch, and the
- * GEMV launch follows with programmatic dependent launch, so its weight
- * stream starts while the quantiser runs (minfer README M15: the activation
- * is quantised once, then the weights stream). */
+/* qgemv_q4_0_seq with fp32 inputs x[T][K] (4-byte aligned): the GEMV kernel
+ * quantises each item's activations (Q8_0, the same bytes as
+ * qgemv_quantize_q8_0) while it builds its shared-memory copy of them, so a
+ * sequence is one launch per 224 items, streaming weights before it reads x
+ * (minfer README M15: the activation is quantised once, then the weights
+ * stream).  The workspace is the sequence's own (no activation area). */
 qgemv_status qgemv_q4_0_seq_f32(const qgemv_seq_f32_item *items, int n, qgemv_wlayout layout, int T,
                                 void *ws, size_t ws_bytes, qgemv_stream_t stream);
 

@@ -792,24 +792,94 @@ __device__ __forceinline__ void build_fold_constants(uint8_t *img, int K, int ti
     }
 }
 
+// One block of 32 fp32 activations quantised to Q8_0 by one thread, with the
+// warp quantiser's steps (the maximum is exact in any order, so the bytes are
+// the same): the codes as two uint4 (elements 0..15, 16..31) and the fp16
+// scale.  vec: x is 16-byte aligned.
+__device__ __forceinline__ void q8_block_thread(const float *x, bool vec, uint4 &qa, uint4 &qb, unsigned short &dh)
+{
+    float v[QK];
+    if (vec) {
+#pragma unroll
+        for (int i = 0; i < QK / 4; ++i) {
+            const float4 f = __ldcg(reinterpret_cast<const float4 *>(x) + i);
+            v[4 * i] = f.x;
+            v[4 * i + 1] = f.y;
+            v[4 * i + 2] = f.z;
+            v[4 * i + 3] = f.w;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < QK; ++i) v[i] = __ldcg(x + i);
+    }
+    float amax = fabsf(v[0]);
+#pragma unroll
+    for (int i = 1; i < QK; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    float d, id;
+    q8_scale(amax, d, id);
+    unsigned w[QK / 4];
+#pragma unroll
+    for (int k = 0; k < QK / 4; ++k)
+        w[k] = (static_cast<unsigned>(q8_code(v[4 * k], id)) & 0xFFu) |
+               ((static_cast<unsigned>(q8_code(v[4 * k + 1], id)) & 0xFFu) << 8) |
+               ((static_cast<unsigned>(q8_code(v[4 * k + 2], id)) & 0xFFu) << 16) |
+               ((static_cast<unsigned>(q8_code(v[4 * k + 3], id)) & 0xFFu) << 24);
+    qa = make_uint4(w[0], w[1], w[2], w[3]);
+    qb = make_uint4(w[4], w[5], w[6], w[7]);
+    dh = q8_half(d);
+}
+
+// One run's int8 activation image quantised in the kernel from fp32
+// activations x[T][K] in global memory: the bytes a copy of the planar Q8_0
+// activations would bring (codes at row t * xstride, fp16 scales at off_d).
+template <int T, bool MMA>
+__device__ __forceinline__ void quantize_image(uint8_t *img, const float *x, int K, int tid, int nthreads)
+{
+    const XqLayout L = xq_layout(T, K, MMA);
+    const int nb = K / QK;
+    const bool vec = (reinterpret_cast<uintptr_t>(x) & 15) == 0;
+    unsigned short *xd = reinterpret_cast<unsigned short *>(img + L.off_d);
+    for (int i = tid; i < T * nb; i += nthreads) {
+        const int t = i / nb, b = i - t * nb;
+        uint4 qa, qb;
+        unsigned short dh;
+        q8_block_thread(x + static_cast<long long>(t) * K + b * QK, vec, qa, qb, dh);
+        uint4 *dst = reinterpret_cast<uint4 *>(img + t * L.xstride + b * QK);
+        dst[0] = qa;
+        dst[1] = qb;
+        xd[t * nb + b] = dh;
+    }
+}
+
 // Builds one run's f16 operand image (tensor-core path, small images)
-// straight from the planar Q8_0 activations in global memory: per token row
+// straight from the planar Q8_0 activations in global memory (F32: from fp32
+// activations, quantised here by q8_block_thread): per token row
 // and block 64 bytes, the chunks {q[e(k)] : k = 0..7}, {q[e(k)] : k = 8..15},
 // {q[16 + e(k)] / 16 : k = 0..7}, {q[16 + e(k)] / 16 : k = 8..15} with
 // e(2i) = 4i, e(2i+1) = 4i+2, e(2i+8) = 4i+1, e(2i+9) = 4i+3 (the MMA k
 // order of the weight words), plus the constants of build_fold_constants.
 // Every value is an integer, or one over 16, held exactly in f16.
-template <int T>
+template <int T, bool F32>
 __device__ __forceinline__ void build_f16_image(uint8_t *img, const uint8_t *src, int K, int tid, int nthreads)
 {
     const XqLayout L = xq_layout(T, K, true);
     const int nb = K / QK;
     const unsigned short *xd = reinterpret_cast<const unsigned short *>(src + T * K);
+    const bool vec = (reinterpret_cast<uintptr_t>(src) & 15) == 0;
     for (int i = tid; i < 8 * nb; i += nthreads) {
         const int t = i / nb, b = i - t * nb;
         if (t < T) {
-            const uint4 *qp = reinterpret_cast<const uint4 *>(src + static_cast<long long>(t) * K + b * QK);
-            const uint4 qa = __ldcg(qp), qb = __ldcg(qp + 1);
+            uint4 qa, qb;
+            unsigned short dh;
+            if constexpr (F32) {
+                q8_block_thread(reinterpret_cast<const float *>(src) + static_cast<long long>(t) * K + b * QK, vec, qa, qb,
+                                dh);
+            } else {
+                const uint4 *qp = reinterpret_cast<const uint4 *>(src + static_cast<long long>(t) * K + b * QK);
+                qa = __ldcg(qp);
+                qb = __ldcg(qp + 1);
+                dh = __ldcg(xd + static_cast<long long>(t) * nb + b);
+            }
             const int8_t *qlo = reinterpret_cast<const int8_t *>(&qa);
             const int8_t *qhi = reinterpret_cast<const int8_t *>(&qb);
             unsigned w[16];
@@ -835,8 +905,7 @@ __device__ __forceinline__ void build_f16_image(uint8_t *img, const uint8_t *src
             shi = dp4a_ss((int)qb.y, ones, shi);
             shi = dp4a_ss((int)qb.z, ones, shi);
             shi = dp4a_ss((int)qb.w, ones, shi);
-            mma_store_consts(img + L.off_cd, b, t, static_cast<float>(-(1032 * slo + 72 * shi)),
-                             __ldcg(xd + static_cast<long long>(t) * nb + b));
+            mma_store_consts(img + L.off_cd, b, t, static_cast<float>(-(1032 * slo + 72 * shi)), dh);
         } else {
             mma_store_consts(img + L.off_cd, b, t, 0.0f, 0);
         }
@@ -1127,6 +1196,7 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
     volatile int *hflag = reinterpret_cast<volatile int *>(smem + H.off_hflag);
     volatile int *abort_flag = &s_abort;
     const bool ggml = H.ggml != 0;
+    const bool f32in = H.xf32 != 0;  // activations arrive as fp32 and are quantised here
 
     Ring ring;
     ring.base = smem + H.off_ring + static_cast<size_t>(warp) * D * SEG_BYTES;
@@ -1297,16 +1367,18 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
             }
             // the group's activations, one transaction count on one barrier
             if (tid == 0 && !*abort_flag) {
-                unsigned tx = 0;  // f16 operand images are built from global memory instead
+                // f16 operand images and fp32 activations are read from global memory instead
+                unsigned tx = 0;
                 for (int r = rg0; r < rg1; ++r)
-                    if (!xq_layout(T, runs[r].K, MMA).f16) tx += static_cast<unsigned>(gcache[runs[r].gi - g0].xq_bytes);
+                    if (!f32in && !xq_layout(T, runs[r].K, MMA).f16)
+                        tx += static_cast<unsigned>(gcache[runs[r].gi - g0].xq_bytes);
                 x_unconfirmed = true;
                 fence_proxy_async_smem();
                 mbar_arrive_expect_tx(xbar, tx);
                 for (int r = rg0; r < rg1; ++r) {
                     const RunInfo &R = runs[r];
                     const Group &g = gcache[R.gi - g0];
-                    if (xq_layout(T, R.K, MMA).f16) continue;
+                    if (f32in || xq_layout(T, R.K, MMA).f16) continue;
                     const unsigned dbytes = static_cast<unsigned>(g.xq_bytes - T * R.K);
                     copy_activations<T, MMA>(smem + R.xq_off, g.xq + static_cast<long long>(R.e) * g.xq_stride, R.K, dbytes,
                                         xbar, pol_x);
@@ -1315,13 +1387,28 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
             const bool xok = mbar_wait_bounded(xbar, xphase, abort_flag, H.status, WAIT_LIMIT_NS);
             xphase ^= 1u;
             if (xok && tid == 0) x_unconfirmed = false;
+            if (f32in) {  // int8 images quantised here from the fp32 activations
+                if (xok)
+                    for (int r = rg0; r < rg1; ++r) {
+                        const RunInfo &R = runs[r];
+                        if (MMA && xq_layout(T, R.K, MMA).f16) continue;
+                        const Group &g = gcache[R.gi - g0];
+                        quantize_image<T, MMA>(smem + R.xq_off,
+                                               reinterpret_cast<const float *>(g.xq + static_cast<long long>(R.e) * g.xq_stride),
+                                               R.K, tid, nthreads);
+                    }
+                __syncthreads();
+            }
             if (xok)
                 for (int r = rg0; r < rg1; ++r) {
                     const RunInfo &R = runs[r];
                     if (MMA && xq_layout(T, R.K, MMA).f16) {
                         const Group &g = gcache[R.gi - g0];
-                        build_f16_image<T>(smem + R.xq_off, g.xq + static_cast<long long>(R.e) * g.xq_stride, R.K, tid,
-                                           nthreads);
+                        const uint8_t *src = g.xq + static_cast<long long>(R.e) * g.xq_stride;
+                        if (f32in)
+                            build_f16_image<T, true>(smem + R.xq_off, src, R.K, tid, nthreads);
+                        else
+                            build_f16_image<T, false>(smem + R.xq_off, src, R.K, tid, nthreads);
                     } else {
                         build_fold_constants<T, MMA>(smem + R.xq_off, R.K, tid, nthreads);
                     }
@@ -1442,7 +1529,7 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
                 x_unconfirmed = true;
                 fence_proxy_async_smem();
                 const unsigned dbytes = static_cast<unsigned>(g.xq_bytes - T * K);
-                if (L.f16) {  // built from global memory below
+                if (L.f16 || f32in) {  // built from global memory below
                     mbar_arrive_expect_tx(xbar, 0);
                 } else {
                     mbar_arrive_expect_tx(xbar, static_cast<unsigned>(T * K) + dbytes);
@@ -1453,11 +1540,21 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
             const bool xok = mbar_wait_bounded(xbar, xphase, abort_flag, H.status, WAIT_LIMIT_NS);
             if (xok) x_unconfirmed = false;
             xphase ^= 1u;
+            const uint8_t *xsrc = g.xq + static_cast<long long>(e_run) * g.xq_stride;
+            if (f32in) {  // int8 image quantised here from the fp32 activations
+                if (xok && !(MMA && L.f16))
+                    quantize_image<T, MMA>(smem, reinterpret_cast<const float *>(xsrc), K, tid, nthreads);
+                __syncthreads();
+            }
             if (xok) {
-                if (MMA && L.f16)
-                    build_f16_image<T>(smem, g.xq + static_cast<long long>(e_run) * g.xq_stride, K, tid, nthreads);
-                else
+                if (MMA && L.f16) {
+                    if (f32in)
+                        build_f16_image<T, true>(smem, xsrc, K, tid, nthreads);
+                    else
+                        build_f16_image<T, false>(smem, xsrc, K, tid, nthreads);
+                } else {
                     build_fold_constants<T, MMA>(smem, K, tid, nthreads);
+                }
             }
             __syncthreads();
 

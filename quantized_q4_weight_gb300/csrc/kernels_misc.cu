@@ -22,12 +22,11 @@ __device__ __forceinline__ void quantize_block_warp(const float *__restrict__ x,
     float amax = fabsf(v);
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
-    const float d = __fdiv_rn(amax, 127.0f);
-    const float id = (d != 0.0f) ? __fdiv_rn(1.0f, d) : 0.0f;
-    const float q = roundf(__fmul_rn(v, id));
-    dst[static_cast<long long>(r) * K + b * QK + lane] = static_cast<uint8_t>(static_cast<int8_t>(static_cast<int>(q)));
+    float d, id;
+    q8_scale(amax, d, id);
+    dst[static_cast<long long>(r) * K + b * QK + lane] = static_cast<uint8_t>(static_cast<int8_t>(q8_code(v, id)));
     if (lane == 0) {
-        const unsigned short dh = __half_as_ushort(__float2half_rn(d));
+        const unsigned short dh = q8_half(d);
         reinterpret_cast<unsigned short *>(dst + static_cast<long long>(R) * K)[rem] = dh;
     }
     if (rem == 0) {  // zero the padding after the scales
@@ -61,34 +60,6 @@ cudaError_t launch_quantize(const float *x, void *xq, int R, long long K, int ba
     return cudaGetLastError();
 }
 
-// A list of activation vectors (one per GEMV of a sequence) in one launch:
-// warp -> global block -> item by binary search over the block prefixes.
-__global__ void __launch_bounds__(256) quantize_list_kernel(const __grid_constant__ QuantList L)
-{
-    pdl_launch_dependents();
-    pdl_wait();
-    const int lane = threadIdx.x & 31;
-    for (long long gb = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; gb < L.total_blocks;
-         gb += (static_cast<long long>(gridDim.x) * blockDim.x) >> 5) {
-        int lo = 0, hi = L.n - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (L.it[mid].block0 <= gb) lo = mid;
-            else hi = mid - 1;
-        }
-        const QuantItem &it = L.it[lo];
-        quantize_block_warp(it.x, it.xq, it.R, it.K, gb - it.block0, it.xq_bytes, lane);
-    }
-}
-
-cudaError_t launch_quantize_list(const QuantList &L, cudaStream_t st)
-{
-    long long grid = (L.total_blocks + 7) / 8;
-    if (grid > 65535) grid = 65535;
-    if (grid < 1) grid = 1;
-    quantize_list_kernel<<<static_cast<unsigned>(grid), 256, 0, st>>>(L);
-    return cudaGetLastError();
-}
 
 // ------------------------------------------------------------ pack / unpack
 //

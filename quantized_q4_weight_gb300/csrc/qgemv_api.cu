@@ -338,7 +338,8 @@ long long single_ws_bytes(long long N, long long K, int T, bool with_xq, long lo
 }
 
 qgemv_status run_single(const void *W, qgemv_wlayout layout, const void *xq, float *y, long long *idx, long long N,
-                        long long K, int T, void *ws, size_t ws_bytes, cudaStream_t st, bool argmax, bool pdl)
+                        long long K, int T, void *ws, size_t ws_bytes, cudaStream_t st, bool argmax, bool pdl,
+                        bool xf32 = false)
 {
     DevInfo dev;
     qgemv_status s = device_info(dev);
@@ -350,6 +351,7 @@ qgemv_status run_single(const void *W, qgemv_wlayout layout, const void *xq, flo
     if (s != QGEMV_OK) return s;
     if (static_cast<long long>(ws_bytes) < pl.ws_bytes) return QGEMV_ERR_WORKSPACE;
     pl.P.status = dev.status;
+    pl.P.xf32 = xf32 ? 1 : 0;
     pl.P.am_idx = reinterpret_cast<long long *>(idx);
     const int grid = grid_for(dev, cps);
     set_cta_groups(pl.P, grid);
@@ -453,17 +455,14 @@ qgemv_status qgemv_q4_0_f32(const void *W, qgemv_wlayout layout, const float *x,
     if (!y) return QGEMV_ERR_INVALID_ARG;
     if (!aligned(x, 4)) return QGEMV_ERR_MISALIGNED;
     if (!ws) return QGEMV_ERR_WORKSPACE;
-    long long xq_off = 0;
-    const long long need = single_ws_bytes(N, K, T, true, &xq_off);
+    const long long need = single_ws_bytes(N, K, T, false, nullptr);
     if (static_cast<long long>(ws_bytes) < need) return QGEMV_ERR_WORKSPACE;
     if (overlap(range(y, 4ll * T * N), range(ws, need)) || overlap(range(x, 4ll * T * K), range(ws, need)))
         return QGEMV_ERR_INVALID_ARG;
-    uint8_t *xq = static_cast<uint8_t *>(ws) + xq_off;
-    const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
-    if (launch_quantize(x, xq, T, K, 1, st) != cudaSuccess) return QGEMV_ERR_CUDA;
-    // The GEMV only reads what the quantiser writes after griddepcontrol.wait,
-    // so it may start (and stream weights) while the quantiser runs.
-    return run_single(W, layout, xq, y, nullptr, N, K, T, ws, static_cast<size_t>(xq_off), st, false, true);
+    // The kernel quantises x itself, after griddepcontrol.wait, so it may
+    // start (and stream weights) while the kernel that produced x finishes.
+    return run_single(W, layout, x, y, nullptr, N, K, T, ws, static_cast<size_t>(need),
+                      reinterpret_cast<cudaStream_t>(stream), false, true, true);
 }
 
 qgemv_status qgemv_q4_0_argmax(const void *W, qgemv_wlayout layout, const void *xq, float *y_or_null, int64_t *idx,
@@ -503,7 +502,7 @@ size_t qgemv_seq_workspace_bytes(const qgemv_seq_item *items, int n, int T)
 }
 
 static qgemv_status check_seq(const qgemv_seq_item *items, int n, qgemv_wlayout layout, int T, void *ws,
-                              size_t ws_bytes)
+                              size_t ws_bytes, bool xf32 = false)
 {
     if (!items || n < 1 || T < 1 || T > 8) return QGEMV_ERR_INVALID_ARG;
     if (layout != QGEMV_W_GGML && layout != QGEMV_W_PACKED) return QGEMV_ERR_INVALID_ARG;
@@ -521,10 +520,10 @@ static qgemv_status check_seq(const qgemv_seq_item *items, int n, qgemv_wlayout 
     for (int i = 0; i < n; ++i) {
         const qgemv_seq_item &a = items[i];
         if (!shape_ok(a.N, a.K) || !a.W || !a.xq || !a.y) return QGEMV_ERR_INVALID_ARG;
-        if (!aligned(a.W, layout == QGEMV_W_PACKED ? 16 : 2) || !aligned(a.xq, 16) || !aligned(a.y, 4))
+        if (!aligned(a.W, layout == QGEMV_W_PACKED ? 16 : 2) || !aligned(a.xq, xf32 ? 4 : 16) || !aligned(a.y, 4))
             return QGEMV_ERR_MISALIGNED;
         v.push_back(Tagged{range(a.W, 18ll * a.N * (a.K / QK)), false});
-        v.push_back(Tagged{range(a.xq, xq_bytes_host(T, a.K)), false});
+        v.push_back(Tagged{range(a.xq, xf32 ? 4ll * T * a.K : xq_bytes_host(T, a.K)), false});
         v.push_back(Tagged{range(a.y, 4ll * T * a.N), true});
     }
     std::sort(v.begin(), v.end(), [](const Tagged &x, const Tagged &y) { return x.r.lo < y.r.lo; });
@@ -538,18 +537,17 @@ static qgemv_status check_seq(const qgemv_seq_item *items, int n, qgemv_wlayout 
 }
 
 // The launches of a sequence (checked): one persistent GEMV launch per
-// MAXG_SEQ items; with fp32 inputs, each preceded by one quantiser launch
-// that writes the activations into `xq_ws` (the GEMV is then chained with
-// programmatic dependent launch).
-static qgemv_status launch_seq(const qgemv_seq_item *items, const float *const *xs, int n, qgemv_wlayout layout,
-                               int T, void *ws, size_t ws_bytes, cudaStream_t st)
+// MAXG_SEQ items.  xf32: the items' activations are fp32 x[T][K], quantised
+// inside the GEMV kernel (launched with programmatic dependent launch: it
+// streams weights before the preceding kernel's outputs are read).
+static qgemv_status launch_seq(const qgemv_seq_item *items, int n, qgemv_wlayout layout, int T, void *ws,
+                               size_t ws_bytes, cudaStream_t st, bool xf32)
 {
     DevInfo dev;
     qgemv_status s = device_info(dev);
     if (s != QGEMV_OK) return s;
     std::vector<GroupSpec> gs(MAXG_SEQ);
     std::unique_ptr<Plan<MAXG_SEQ>> pl(new Plan<MAXG_SEQ>());
-    std::unique_ptr<QuantList> ql(xs ? new QuantList() : nullptr);
     for (int c0 = 0; c0 < n; c0 += MAXG_SEQ) {
         const int cn = (n - c0) < MAXG_SEQ ? (n - c0) : MAXG_SEQ;
         for (int i = 0; i < cn; ++i) {
@@ -563,20 +561,9 @@ static qgemv_status launch_seq(const qgemv_seq_item *items, const float *const *
         if (s != QGEMV_OK) return s;
         if (static_cast<long long>(ws_bytes) < pl->ws_bytes) return QGEMV_ERR_WORKSPACE;
         pl->P.status = dev.status;
+        pl->P.xf32 = xf32 ? 1 : 0;
         set_cta_groups(pl->P, grid);
-        if (xs) {
-            ql->n = cn;
-            long long blocks = 0;
-            for (int i = 0; i < cn; ++i) {
-                const qgemv_seq_item &it = items[c0 + i];
-                ql->it[i] = QuantItem{xs[c0 + i], static_cast<uint8_t *>(const_cast<void *>(it.xq)), T,
-                                      static_cast<int>(it.K), xq_bytes_host(T, it.K), blocks};
-                blocks += static_cast<long long>(T) * (it.K / QK);
-            }
-            ql->total_blocks = blocks;
-            if (launch_quantize_list(*ql, st) != cudaSuccess) return QGEMV_ERR_CUDA;
-        }
-        if (dispatch_T<MAXG_SEQ, false>(pl->P, T, mma_for(T), grid, pl->smem, st, xs != nullptr) != cudaSuccess)
+        if (dispatch_T<MAXG_SEQ, false>(pl->P, T, mma_for(T), grid, pl->smem, st, xf32) != cudaSuccess)
             return QGEMV_ERR_CUDA;
     }
     return QGEMV_OK;
@@ -587,62 +574,38 @@ qgemv_status qgemv_q4_0_seq(const qgemv_seq_item *items, int n, qgemv_wlayout la
 {
     const qgemv_status s = check_seq(items, n, layout, T, ws, ws_bytes);
     if (s != QGEMV_OK) return s;
-    return launch_seq(items, nullptr, n, layout, T, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream));
+    return launch_seq(items, n, layout, T, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream), false);
 }
 
-// Workspace of the fp32-input sequence: the sequence's own, then each item's
-// quantised activations (256-byte aligned).
-static long long seq_f32_layout(const qgemv_seq_f32_item *items, int n, int T, std::vector<long long> *xq_off)
+// The fp32-input sequence as a sequence whose activation pointers are the
+// fp32 inputs (the kernel quantises them; no workspace for activations).
+static bool seq_f32_items(const qgemv_seq_f32_item *items, int n, std::vector<qgemv_seq_item> &sq)
 {
-    std::vector<qgemv_seq_item> tmp(n);
+    sq.resize(n);
     for (int i = 0; i < n; ++i) {
-        if (!shape_ok(items[i].N, items[i].K)) return 0;
-        tmp[i] = qgemv_seq_item{items[i].W, nullptr, items[i].y, items[i].N, items[i].K};
+        if (!shape_ok(items[i].N, items[i].K)) return false;
+        sq[i] = qgemv_seq_item{items[i].W, items[i].x, items[i].y, items[i].N, items[i].K};
     }
-    long long off = static_cast<long long>(qgemv_seq_workspace_bytes(tmp.data(), n, T));
-    if (off == 0) return 0;
-    off = align_up(off, 256);
-    for (int i = 0; i < n; ++i) {
-        if (xq_off) xq_off->push_back(off);
-        off = align_up(off + xq_bytes_host(T, items[i].K), 256);
-    }
-    return off;
+    return true;
 }
 
 size_t qgemv_seq_f32_workspace_bytes(const qgemv_seq_f32_item *items, int n, int T)
 {
     if (!items || n < 1 || T < 1 || T > 8) return 0;
-    return static_cast<size_t>(seq_f32_layout(items, n, T, nullptr));
+    std::vector<qgemv_seq_item> sq;
+    if (!seq_f32_items(items, n, sq)) return 0;
+    return qgemv_seq_workspace_bytes(sq.data(), n, T);
 }
 
 qgemv_status qgemv_q4_0_seq_f32(const qgemv_seq_f32_item *items, int n, qgemv_wlayout layout, int T, void *ws,
                                 size_t ws_bytes, qgemv_stream_t stream)
 {
     if (!items || n < 1 || T < 1 || T > 8) return QGEMV_ERR_INVALID_ARG;
-    if (!ws) return QGEMV_ERR_WORKSPACE;
-    std::vector<long long> xq_off;
-    const long long need = seq_f32_layout(items, n, T, &xq_off);
-    if (need == 0) return QGEMV_ERR_INVALID_ARG;
-    if (static_cast<long long>(ws_bytes) < need) return QGEMV_ERR_WORKSPACE;
-    std::vector<qgemv_seq_item> sq(n);
-    std::vector<const float *> xs(n);
-    const Range rw = range(ws, need);
-    for (int i = 0; i < n; ++i) {
-        const qgemv_seq_f32_item &a = items[i];
-        if (!a.x) return QGEMV_ERR_INVALID_ARG;
-        if (!aligned(a.x, 4)) return QGEMV_ERR_MISALIGNED;
-        if (overlap(range(a.x, 4ll * T * a.K), rw)) return QGEMV_ERR_INVALID_ARG;
-        for (int k = 0; k < n; ++k)
-            if (a.y && overlap(range(a.y, 4ll * T * a.N), range(items[k].x, 4ll * T * items[k].K)))
-                return QGEMV_ERR_INVALID_ARG;
-        sq[i] = qgemv_seq_item{a.W, static_cast<uint8_t *>(ws) + xq_off[i], a.y, a.N, a.K};
-        xs[i] = a.x;
-    }
-    // the sequence's own workspace ends where the activations begin
-    qgemv_status s = check_seq(sq.data(), n, layout, T, ws, static_cast<size_t>(xq_off[0]));
+    std::vector<qgemv_seq_item> sq;
+    if (!seq_f32_items(items, n, sq)) return QGEMV_ERR_INVALID_ARG;
+    const qgemv_status s = check_seq(sq.data(), n, layout, T, ws, ws_bytes, true);
     if (s != QGEMV_OK) return s;
-    return launch_seq(sq.data(), xs.data(), n, layout, T, ws, static_cast<size_t>(xq_off[0]),
-                      reinterpret_cast<cudaStream_t>(stream));
+    return launch_seq(sq.data(), n, layout, T, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream), true);
 }
 
 static qgemv_status gather_specs(const qgemv_gather_matrix *mats, int n_mats, int n_ids, int T, GroupSpec *gs)

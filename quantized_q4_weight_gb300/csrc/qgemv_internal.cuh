@@ -67,6 +67,7 @@ struct ParamHead {
     int balanced_ok;        // every group unsplit: CTAs may balance by stages
     const int *ids;         // gather: slot -> expert id (nullptr: slot index)
     int n_experts;
+    int xf32;               // the groups' activations are fp32 [T][K], quantised in the kernel
     long long total_bytes, total_items;
     unsigned long long *am_cand;  // argmax: [gridDim][T] candidate keys
     unsigned *am_cnt;             // argmax: CTA arrival counter
@@ -280,6 +281,17 @@ __host__ __device__ inline XqLayout xq_layout(int T, int K, bool mma)
     L.bytes = (L.off_cd + cd_bytes + 127) & ~127;
     return L;
 }
+
+// Q8_0 steps shared by every quantiser: d = amax / 127 (IEEE division),
+// 1/d from the fp32 d (0 when d = 0), q = roundf(x * (1/d)) -- halfway cases
+// away from zero -- and d stored as fp16, round to nearest even.
+__device__ __forceinline__ void q8_scale(float amax, float &d, float &id)
+{
+    d = __fdiv_rn(amax, 127.0f);
+    id = (d != 0.0f) ? __fdiv_rn(1.0f, d) : 0.0f;
+}
+__device__ __forceinline__ int q8_code(float v, float id) { return static_cast<int>(roundf(__fmul_rn(v, id))); }
+__device__ __forceinline__ unsigned short q8_half(float d) { return __half_as_ushort(__float2half_rn(d)); }
 
 // fp16 bits -> fp32 (exact).
 __device__ __forceinline__ float h2f(unsigned bits16)

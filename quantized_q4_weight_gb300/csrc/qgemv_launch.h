@@ -16,19 +16,6 @@ inline long long xq_bytes_host(long long R, long long K) { return R * K + roundu
 
 cudaError_t launch_quantize(const float *x, void *xq, int R, long long K, int batch, cudaStream_t st);
 
-struct QuantItem {
-    const float *x;      // fp32 [R][K]
-    uint8_t *xq;         // planar Q8_0 of R rows
-    int R, K;
-    long long xq_bytes;
-    long long block0;    // first global block of this item
-};
-struct QuantList {
-    int n;
-    long long total_blocks;
-    QuantItem it[MAXG_SEQ];
-};
-cudaError_t launch_quantize_list(const QuantList &L, cudaStream_t st);
 cudaError_t launch_stream_bench(const void *src, long long bytes, int method, int warps, int depth, int stage_bytes,
                                 unsigned long long *out, unsigned *status, int sms, cudaStream_t st);
 cudaError_t launch_pack(const void *src, void *dst, long long N, long long K, bool to_packed, cudaStream_t st);

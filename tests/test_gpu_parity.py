@@ -466,3 +466,31 @@ def test_ring_depth_leaves_results_unchanged(orc, ring_depth):
     assert q.device_status() == 0
     for o in [got] + [y.cpu() for y in ys[::13]]:
         assert torch.equal(ref.view(torch.int32), o.view(torch.int32))
+
+
+@pytest.mark.parametrize("T,K", [(1, 1536), (3, 544), (8, 1536), (8, 8960)])
+@pytest.mark.parametrize("offset", [0, 1])
+def test_fp32_entry_points_quantise_in_kernel(orc, T, K, offset):
+    """The fp32 calls quantise inside the GEMV kernel: the same bits as the
+    standalone quantiser followed by the quantised-input call, with x
+    16-byte aligned (offset 0) or only 4-byte aligned (offset 1 float).
+    T = 8 covers the tensor-core path with an f16 (K = 1536) and an int8
+    (K = 8960) activation image."""
+    N = 200
+    Wg, Wp = weights(1000 + T + K, N, K, q.W_PACKED)
+    x = synth.activations(1100 + T + K, T, K)
+    buf = torch.zeros(T * K + 4, dtype=torch.float32, device=DEV)
+    xd = buf[offset:offset + T * K].view(T, K)
+    xd.copy_(torch.from_numpy(x))
+    xq = q.quantize_q8_0(xd.contiguous(), T, K)
+    ref = q.gemv(Wp, q.W_PACKED, xq, N, K, T, ws_for(N, K, T)).cpu()
+    got = q.gemv_f32(Wp, q.W_PACKED, xd, N, K, T, ws_for(N, K, T)).cpu()
+    ys = [torch.empty((T, N), dtype=torch.float32, device=DEV) for _ in range(3)]
+    items = q.seq_f32_items([(Wp, xd, y, N, K) for y in ys])
+    q.gemv_seq_f32(items, q.W_PACKED, T, q.new_workspace(q.seq_f32_workspace_bytes(items, T)))
+    torch.cuda.synchronize()
+    assert q.device_status() == 0
+    for o in [got] + [y.cpu() for y in ys]:
+        assert torch.equal(ref.view(torch.int32), o.view(torch.int32))
+    y64, S = orc.gemv(Wg, N, K, orc.quantize(x), T)
+    check_close(got.numpy(), y64, S, f"fp32 in-kernel quantise T={T} K={K}")
