@@ -54,9 +54,17 @@
  * exception crosses the ABI.  Calls are thread-safe; two calls that share a
  * workspace must not overlap on the GPU.
  *
+ * Launch order.  The GEMV calls (all but the gather) launch with
+ * programmatic dependent launch: a GEMV kernel may start, and read the
+ * weights W, while the preceding kernel in the stream is still running, if
+ * that kernel allows it (griddepcontrol.launch_dependents); activations,
+ * outputs and workspace are touched only after the preceding kernel has
+ * completed.  So W must not be written by a preceding kernel that allows
+ * early launch before its writes are done (the library's own kernels that
+ * allow it never write weights).
+ *
  * Workspace.  Calls that take (ws, ws_bytes) use it for split-K partial
- * sums, completion counters, argmax candidates and (for fp32-input calls)
- * the quantised activations.  The matching *_workspace_bytes query gives the
+ * sums, completion counters and argmax candidates.  The matching *_workspace_bytes query gives the
  * size (device-independent, at least 16 KB).  Its first 16 KB hold
  * completion counters and must be zero-filled once before the first use
  * (e.g. cudaMemsetAsync); every call that completes without a device-status

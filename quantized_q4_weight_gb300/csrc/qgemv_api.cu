@@ -324,17 +324,14 @@ qgemv_status check_single(const void *W, qgemv_wlayout layout, const void *xin, 
     return QGEMV_OK;
 }
 
-long long single_ws_bytes(long long N, long long K, int T, bool with_xq, long long *xq_off)
+long long single_ws_bytes(long long N, long long K, int T)
 {
     GroupSpec gs{nullptr, 0, nullptr, 0, nullptr, 0, N, K, 1};
     Plan<MAXG_SMALL> pl;
     make_plan<MAXG_SMALL>(&gs, 1, T, false, true, nullptr, 0, pl);
     Plan<MAXG_SMALL> pg;  // the GGML layout splits its partial slab too
     make_plan<MAXG_SMALL>(&gs, 1, T, true, true, nullptr, 0, pg);
-    long long b = pl.ws_bytes > pg.ws_bytes ? pl.ws_bytes : pg.ws_bytes;
-    if (xq_off) *xq_off = b;
-    if (with_xq) b += align_up(xq_bytes_host(T, K), 256);
-    return b;
+    return pl.ws_bytes > pg.ws_bytes ? pl.ws_bytes : pg.ws_bytes;
 }
 
 qgemv_status run_single(const void *W, qgemv_wlayout layout, const void *xq, float *y, long long *idx, long long N,
@@ -431,7 +428,7 @@ qgemv_status qgemv_quantize_q8_0(const float *x, void *xq, int R, int64_t K, int
 size_t qgemv_workspace_bytes(int64_t N, int64_t K, int T)
 {
     if (!shape_ok(N, K) || T < 1 || T > 8) return 0;
-    return static_cast<size_t>(single_ws_bytes(N, K, T, true, nullptr));
+    return static_cast<size_t>(single_ws_bytes(N, K, T));
 }
 
 qgemv_status qgemv_q4_0(const void *W, qgemv_wlayout layout, const void *xq, float *y, int64_t N, int64_t K, int T,
@@ -444,7 +441,7 @@ qgemv_status qgemv_q4_0(const void *W, qgemv_wlayout layout, const void *xq, flo
     if (!ws) return QGEMV_ERR_WORKSPACE;
     if (overlap(range(y, 4ll * T * N), range(ws, static_cast<long long>(ws_bytes)))) return QGEMV_ERR_INVALID_ARG;
     return run_single(W, layout, xq, y, nullptr, N, K, T, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream), false,
-                      false);
+                      true);
 }
 
 qgemv_status qgemv_q4_0_f32(const void *W, qgemv_wlayout layout, const float *x, float *y, int64_t N, int64_t K,
@@ -455,7 +452,7 @@ qgemv_status qgemv_q4_0_f32(const void *W, qgemv_wlayout layout, const float *x,
     if (!y) return QGEMV_ERR_INVALID_ARG;
     if (!aligned(x, 4)) return QGEMV_ERR_MISALIGNED;
     if (!ws) return QGEMV_ERR_WORKSPACE;
-    const long long need = single_ws_bytes(N, K, T, false, nullptr);
+    const long long need = single_ws_bytes(N, K, T);
     if (static_cast<long long>(ws_bytes) < need) return QGEMV_ERR_WORKSPACE;
     if (overlap(range(y, 4ll * T * N), range(ws, need)) || overlap(range(x, 4ll * T * K), range(ws, need)))
         return QGEMV_ERR_INVALID_ARG;
@@ -477,7 +474,7 @@ qgemv_status qgemv_q4_0_argmax(const void *W, qgemv_wlayout layout, const void *
     if (overlap(range(idx, 8ll * T), rw) || (y_or_null && overlap(range(y_or_null, 4ll * T * N), rw)))
         return QGEMV_ERR_INVALID_ARG;
     return run_single(W, layout, xq, y_or_null, reinterpret_cast<long long *>(idx), N, K, T, ws, ws_bytes,
-                      reinterpret_cast<cudaStream_t>(stream), true, false);
+                      reinterpret_cast<cudaStream_t>(stream), true, true);
 }
 
 size_t qgemv_seq_workspace_bytes(const qgemv_seq_item *items, int n, int T)
@@ -538,8 +535,7 @@ static qgemv_status check_seq(const qgemv_seq_item *items, int n, qgemv_wlayout 
 
 // The launches of a sequence (checked): one persistent GEMV launch per
 // MAXG_SEQ items.  xf32: the items' activations are fp32 x[T][K], quantised
-// inside the GEMV kernel (launched with programmatic dependent launch: it
-// streams weights before the preceding kernel's outputs are read).
+// inside the GEMV kernel.
 static qgemv_status launch_seq(const qgemv_seq_item *items, int n, qgemv_wlayout layout, int T, void *ws,
                                size_t ws_bytes, cudaStream_t st, bool xf32)
 {
@@ -563,7 +559,7 @@ static qgemv_status launch_seq(const qgemv_seq_item *items, int n, qgemv_wlayout
         pl->P.status = dev.status;
         pl->P.xf32 = xf32 ? 1 : 0;
         set_cta_groups(pl->P, grid);
-        if (dispatch_T<MAXG_SEQ, false>(pl->P, T, mma_for(T), grid, pl->smem, st, xf32) != cudaSuccess)
+        if (dispatch_T<MAXG_SEQ, false>(pl->P, T, mma_for(T), grid, pl->smem, st, true) != cudaSuccess)
             return QGEMV_ERR_CUDA;
     }
     return QGEMV_OK;
@@ -766,7 +762,7 @@ extern "C" qgemv_status qgemv_q4_0_argmax_noalloc(const void *W, qgemv_wlayout l
                                                   qgemv_stream_t stream)
 {
     if (!shape_ok(N, K) || T < 1 || T > 8) return QGEMV_ERR_INVALID_ARG;
-    if (single_ws_bytes(N, K, T, false, nullptr) > kNoAllocScratchBytes) return QGEMV_ERR_UNSUPPORTED;
+    if (single_ws_bytes(N, K, T) > kNoAllocScratchBytes) return QGEMV_ERR_UNSUPPORTED;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QGEMV_ERR_CUDA;
     void *scratch = nullptr;
