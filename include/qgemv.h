@@ -138,8 +138,9 @@ qgemv_status qgemv_unpack_q4_0(const void *w_packed, void *w_ggml, int64_t N, in
 qgemv_status qgemv_quantize_q8_0(const float *x, void *xq, int R, int64_t K, int batch,
                                  qgemv_stream_t stream);
 
-/* Workspace bytes for qgemv_q4_0, qgemv_q4_0_f32 and qgemv_q4_0_argmax on
- * an N x K matrix with T tokens (0 for an invalid shape). */
+/* Workspace bytes for qgemv_q4_0, qgemv_q4_0_f32, qgemv_q4_0_argmax and
+ * qgemv_q4_0_argmax_f32 on an N x K matrix with T tokens (0 for an invalid
+ * shape). */
 size_t qgemv_workspace_bytes(int64_t N, int64_t K, int T);
 
 /* y[T][N] = W . x for T pre-quantised token columns (xq, planar Q8_0 of T
@@ -165,6 +166,13 @@ qgemv_status qgemv_q4_0_f32(const void *W, qgemv_wlayout layout, const float *x,
 qgemv_status qgemv_q4_0_argmax(const void *W, qgemv_wlayout layout, const void *xq,
                                float *y_or_null, int64_t *idx, int64_t N, int64_t K, int T,
                                void *ws, size_t ws_bytes, qgemv_stream_t stream);
+
+/* qgemv_q4_0_argmax with fp32 input x[T][K] (4-byte aligned), quantised
+ * inside the kernel as in qgemv_q4_0_f32: one launch for the lm_head of a
+ * decode step.  Same workspace as qgemv_q4_0_argmax. */
+qgemv_status qgemv_q4_0_argmax_f32(const void *W, qgemv_wlayout layout, const float *x, float *y_or_null,
+                                   int64_t *idx, int64_t N, int64_t K, int T, void *ws, size_t ws_bytes,
+                                   qgemv_stream_t stream);
 
 /* Allocation-free variant of qgemv_q4_0_argmax (the paper has no
  * counterpart; this is a convenience of this library).  For callers that
@@ -281,8 +289,9 @@ qgemv_status qgemv_debug_stream_read(const void *src, size_t bytes, int method, 
  *                launch, mma_min_T: token count from which T > 1 runs on the
  *                f16 tensor-core path (mma.sync m16n8k16 over exact
  *                integer operands; default 5, 9 = never) instead of dp4a,
- *   ring_depth:  weight stages in flight per warp (1..6; default 3 for one
- *                token, else 2), used where the activations leave room.
+ *   ring_depth:  weight stages in flight per warp (1..6; default 3 for
+ *                one-token sequences, else 2), used where the activations
+ *                leave room.
  * Process-wide; affects launches enqueued afterwards. */
 qgemv_status qgemv_set_tuning(int ctas_per_sm, int waves, int mma_min_T, int ring_depth);
 

@@ -62,6 +62,7 @@ _SIGS = {
     "qgemv_q4_0": ([_VP, _I32, _VP, _VP, _I64, _I64, _I32, _VP, _SZ, _VP], _I32),
     "qgemv_q4_0_f32": ([_VP, _I32, _VP, _VP, _I64, _I64, _I32, _VP, _SZ, _VP], _I32),
     "qgemv_q4_0_argmax": ([_VP, _I32, _VP, _VP, _VP, _I64, _I64, _I32, _VP, _SZ, _VP], _I32),
+    "qgemv_q4_0_argmax_f32": ([_VP, _I32, _VP, _VP, _VP, _I64, _I64, _I32, _VP, _SZ, _VP], _I32),
     "qgemv_q4_0_argmax_noalloc": ([_VP, _I32, _VP, _VP, _VP, _I64, _I64, _I32, _VP], _I32),
     "qgemv_seq_workspace_bytes": ([ctypes.POINTER(SeqItem), _I32, _I32], _SZ),
     "qgemv_q4_0_seq": ([ctypes.POINTER(SeqItem), _I32, _I32, _I32, _VP, _SZ, _VP], _I32),
@@ -172,6 +173,14 @@ def gemv_argmax(W, layout: int, xq, N: int, K: int, T: int, ws, y=None, idx=None
     idx = idx if idx is not None else torch.empty(T, dtype=torch.int64, device=W.device)
     _check(lib().qgemv_q4_0_argmax(_ptr(W), layout, _ptr(xq), _ptr(y), _ptr(idx), N, K, T, _ptr(ws), ws.numel(),
                                    _stream(stream)), "qgemv_q4_0_argmax")
+    return idx
+
+
+def gemv_argmax_f32(W, layout: int, x, N: int, K: int, T: int, ws, y=None, idx=None, stream=None):
+    """Argmax of W . x over rows for fp32 x[T][K] (quantised inside the kernel)."""
+    idx = idx if idx is not None else torch.empty(T, dtype=torch.int64, device=W.device)
+    _check(lib().qgemv_q4_0_argmax_f32(_ptr(W), layout, _ptr(x), _ptr(y), _ptr(idx), N, K, T, _ptr(ws), ws.numel(),
+                                       _stream(stream)), "qgemv_q4_0_argmax_f32")
     return idx
 
 

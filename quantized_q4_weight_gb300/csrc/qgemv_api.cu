@@ -206,7 +206,9 @@ qgemv_status make_plan(const GroupSpec *gs, int n, int T, bool ggml, bool argmax
     // are compute-bound), the widest count at one stage; then 8 warps.
     const int wide = ctas_per_sm > 1 ? 8 : max_warps_for(T, mma);
     const int rd = g_ring_depth.load(std::memory_order_relaxed);
-    const int D0 = rd > 0 ? rd : (!mma && T == 1 ? 3 : 2);  // measured defaults
+    // measured defaults: three stages per warp pay off for long one-token
+    // sequences only (layer sets); single matrices, lm_head and gathers run two
+    const int D0 = rd > 0 ? rd : (!mma && T == 1 && MAXG == MAXG_SEQ ? 3 : 2);
     const int choices[5][2] = {{wide, D0}, {mma ? wide : 8, mma ? 1 : D0}, {8, D0}, {8, 2}, {8, 1}};
     for (const auto &c : choices) {
         const int nw = c[0], D = c[1];
@@ -462,19 +464,37 @@ qgemv_status qgemv_q4_0_f32(const void *W, qgemv_wlayout layout, const float *x,
                       reinterpret_cast<cudaStream_t>(stream), false, true, true);
 }
 
-qgemv_status qgemv_q4_0_argmax(const void *W, qgemv_wlayout layout, const void *xq, float *y_or_null, int64_t *idx,
-                               int64_t N, int64_t K, int T, void *ws, size_t ws_bytes, qgemv_stream_t stream)
+// The argmax calls: quantised (xq) or fp32 (x, xf32) activations.
+static qgemv_status argmax_call(const void *W, qgemv_wlayout layout, const void *xin, bool xf32, float *y_or_null,
+                                int64_t *idx, int64_t N, int64_t K, int T, void *ws, size_t ws_bytes,
+                                qgemv_stream_t stream)
 {
-    qgemv_status s = check_single(W, layout, xq, shape_ok(N, K) ? xq_bytes_host(T, K) : 0, y_or_null, N, K, T, ws);
+    const long long xin_bytes = !shape_ok(N, K) ? 0 : xf32 ? 4ll * T * K : xq_bytes_host(T, K);
+    qgemv_status s = check_single(W, layout, xin, xin_bytes, y_or_null, N, K, T, ws);
     if (s != QGEMV_OK) return s;
     if (!idx) return QGEMV_ERR_INVALID_ARG;
-    if (!aligned(xq, 16) || !aligned(idx, 8)) return QGEMV_ERR_MISALIGNED;
+    if (!aligned(xin, xf32 ? 4 : 16) || !aligned(idx, 8)) return QGEMV_ERR_MISALIGNED;
     if (!ws) return QGEMV_ERR_WORKSPACE;
     const Range rw = range(ws, static_cast<long long>(ws_bytes));
     if (overlap(range(idx, 8ll * T), rw) || (y_or_null && overlap(range(y_or_null, 4ll * T * N), rw)))
         return QGEMV_ERR_INVALID_ARG;
-    return run_single(W, layout, xq, y_or_null, reinterpret_cast<long long *>(idx), N, K, T, ws, ws_bytes,
-                      reinterpret_cast<cudaStream_t>(stream), true, true);
+    if (xf32 && (overlap(range(xin, xin_bytes), rw) || overlap(range(xin, xin_bytes), range(idx, 8ll * T))))
+        return QGEMV_ERR_INVALID_ARG;
+    return run_single(W, layout, xin, y_or_null, reinterpret_cast<long long *>(idx), N, K, T, ws, ws_bytes,
+                      reinterpret_cast<cudaStream_t>(stream), true, true, xf32);
+}
+
+qgemv_status qgemv_q4_0_argmax(const void *W, qgemv_wlayout layout, const void *xq, float *y_or_null, int64_t *idx,
+                               int64_t N, int64_t K, int T, void *ws, size_t ws_bytes, qgemv_stream_t stream)
+{
+    return argmax_call(W, layout, xq, false, y_or_null, idx, N, K, T, ws, ws_bytes, stream);
+}
+
+qgemv_status qgemv_q4_0_argmax_f32(const void *W, qgemv_wlayout layout, const float *x, float *y_or_null,
+                                   int64_t *idx, int64_t N, int64_t K, int T, void *ws, size_t ws_bytes,
+                                   qgemv_stream_t stream)
+{
+    return argmax_call(W, layout, x, true, y_or_null, idx, N, K, T, ws, ws_bytes, stream);
 }
 
 size_t qgemv_seq_workspace_bytes(const qgemv_seq_item *items, int n, int T)

@@ -494,3 +494,23 @@ def test_fp32_entry_points_quantise_in_kernel(orc, T, K, offset):
         assert torch.equal(ref.view(torch.int32), o.view(torch.int32))
     y64, S = orc.gemv(Wg, N, K, orc.quantize(x), T)
     check_close(got.numpy(), y64, S, f"fp32 in-kernel quantise T={T} K={K}")
+
+
+@pytest.mark.parametrize("T", [1, 8])
+def test_argmax_f32_matches_quantised_argmax(orc, T):
+    """The fp32-input argmax quantises in the kernel: same index and same y
+    bits as quantising first."""
+    N, K = 5000, 1536
+    Wg, Wp = weights(1200 + T, N, K, q.W_PACKED)
+    x = synth.activations(1201 + T, T, K)
+    xd = torch.from_numpy(x).to(DEV)
+    xq = q.quantize_q8_0(xd, T, K)
+    y0 = torch.empty((T, N), dtype=torch.float32, device=DEV)
+    y1 = torch.empty((T, N), dtype=torch.float32, device=DEV)
+    i0 = q.gemv_argmax(Wp, q.W_PACKED, xq, N, K, T, ws_for(N, K, T), y=y0).cpu()
+    i1 = q.gemv_argmax_f32(Wp, q.W_PACKED, xd, N, K, T, ws_for(N, K, T), y=y1).cpu()
+    assert q.device_status() == 0
+    assert torch.equal(i0, i1)
+    assert torch.equal(y0.cpu().view(torch.int32), y1.cpu().view(torch.int32))
+    for t in range(T):
+        assert int(i1[t]) == orc.argmax_f32(y1[t].cpu().numpy())
