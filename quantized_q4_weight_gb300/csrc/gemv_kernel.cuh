@@ -403,6 +403,23 @@ constexpr unsigned H2_NEG_72 = 0xD480D480u;    // f16x2 (-72, -72): (1152 + q) /
 __device__ __forceinline__ unsigned act_even(unsigned w) { return __byte_perm(w, 0x64646464u, 0x4240); }
 __device__ __forceinline__ unsigned act_odd(unsigned w) { return __byte_perm(w, 0x64646464u, 0x4341); }
 
+// d0 += c0, d1 += c1: one add.rn.f32x2 (two IEEE additions).
+__device__ __forceinline__ void fadd2(float &d0, float &d1, float c0, float c1)
+{
+    asm("{\n\t.reg .b64 ra, rc;\n\t"
+        "mov.b64 ra, {%0, %1};\n\t"
+        "mov.b64 rc, {%2, %3};\n\t"
+        "add.rn.f32x2 ra, ra, rc;\n\t"
+        "mov.b64 {%0, %1}, ra;\n\t}"
+        : "+f"(d0), "+f"(d1)
+        : "f"(c0), "f"(c1));
+}
+
+// 2^24: w >> 8 as the high word of w * 2^24, an integer multiply (FMA pipe)
+// rather than a shift (ALU pipe, the busier one on the tensor-core path).
+// A constant-bank value, so the compiler keeps the multiply.
+__constant__ unsigned c_shr8_mul = 1u << 24;
+
 // acc0 += s0 * d0, acc1 += s1 * d1: one fma.rn.f32x2 (two IEEE fused
 // multiply-adds, rounded as two fma.rn.f32 would be).
 __device__ __forceinline__ void ffma2(float &a0, float &a1, float s0, float s1, float d0, float d1)
@@ -483,7 +500,7 @@ __device__ __forceinline__ unsigned lds_u32(uint32_t addr)
 __device__ __forceinline__ void mma_block_core(unsigned wg, unsigned wg8, unsigned bl0, unsigned bl1, unsigned bh0,
                                                unsigned bh1, unsigned sc, const float4 &cq, unsigned dx, float (&acc)[4])
 {
-    const unsigned g1 = wg >> 8, g9 = wg8 >> 8;
+    const unsigned g1 = __umulhi(wg, c_shr8_mul), g9 = __umulhi(wg8, c_shr8_mul);  // wg >> 8, wg8 >> 8
     float d[4];
     mma_f16_c(d, (wg & 0x000F000Fu) | H2_1024, (wg8 & 0x000F000Fu) | H2_1024, (g1 & 0x000F000Fu) | H2_1024,
               (g9 & 0x000F000Fu) | H2_1024, bl0, bl1, cq);
@@ -710,7 +727,14 @@ __device__ __forceinline__ void segment_sum(bool from_stage, const uint8_t *stag
         else
             mma_segment_from_ggml<T>(rows_base, rows, s, nb, r8, j, xv, acc);
 #pragma unroll
-        for (int k = 0; k < 4; ++k) P[k] = __fadd_rn(__fadd_rn(acc[0][k], acc[1][k]), __fadd_rn(acc[2][k], acc[3][k]));
+        for (int k = 0; k < 4; k += 2) {  // (s0 + s1) + (s2 + s3), two outputs per add.rn.f32x2
+            float u0 = acc[0][k], u1 = acc[0][k + 1], v0 = acc[2][k], v1 = acc[2][k + 1];
+            fadd2(u0, u1, acc[1][k], acc[1][k + 1]);
+            fadd2(v0, v1, acc[3][k], acc[3][k + 1]);
+            fadd2(u0, u1, v0, v1);
+            P[k] = u0;
+            P[k + 1] = u1;
+        }
     } else {
         float acc[2][T];
 #pragma unroll
