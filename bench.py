@@ -232,20 +232,25 @@ def build_moe(T, seed, dev, sets=4, n_experts=256, top_k=8, d_model=2048, d_ff=5
     wl.yg = torch.empty((n_ids, T, d_ff), dtype=torch.float32, device=dev)
     wl.yu = torch.empty((n_ids, T, d_ff), dtype=torch.float32, device=dev)
     wl.yd = torch.empty((n_ids, T, d_model), dtype=torch.float32, device=dev)
-    wl.gm = []
+    wl.gm, wl.gf = [], []
     for s in range(sets):
         Wgt, Wup, Wdn = wl.sets[s]
         wl.gm.append(q.gather_mats([
             (Wgt, q.q4_0_bytes(d_ff, d_model), wl.xq_in, 0, wl.yg, T * d_ff, d_ff, d_model),
             (Wup, q.q4_0_bytes(d_ff, d_model), wl.xq_in, 0, wl.yu, T * d_ff, d_ff, d_model),
             (Wdn, q.q4_0_bytes(d_model, d_ff), wl.xq_dn, xd, wl.yd, T * d_model, d_model, d_ff)]))
-    wl.ws = q.new_workspace(q.gather_workspace_bytes(wl.gm[0], n_ids, T), dev)
+        wl.gf.append(q.gather_f32_mats([
+            (Wgt, q.q4_0_bytes(d_ff, d_model), wl.x_in, 0, wl.yg, T * d_ff, d_ff, d_model),
+            (Wup, q.q4_0_bytes(d_ff, d_model), wl.x_in, 0, wl.yu, T * d_ff, d_ff, d_model),
+            (Wdn, q.q4_0_bytes(d_model, d_ff), wl.x_dn, 4 * T * d_ff, wl.yd, T * d_model, d_model, d_ff)]))
+    wl.ws = q.new_workspace(max(q.gather_workspace_bytes(wl.gm[0], n_ids, T),
+                                q.gather_f32_workspace_bytes(wl.gf[0], n_ids, T)), dev)
     per_tok = n_ids * (2 * q.q4_0_bytes(d_ff, d_model) + q.q4_0_bytes(d_model, d_ff))
     wl.w_bytes = per_tok
     wl.x_bytes = 4 * T * (d_model + n_ids * d_ff)
     wl.y_bytes = 4 * T * n_ids * (2 * d_ff + d_model)
     wl.xq_bytes = xg + n_ids * xd
-    wl.n_gemv, wl.launches, wl.tok = 3 * n_ids, 3, 0
+    wl.n_gemv, wl.launches, wl.tok = 3 * n_ids, 1, 0
     wl.n_experts, wl.n_ids = ne, n_ids
 
     def quantize(stream=None):
@@ -257,10 +262,12 @@ def build_moe(T, seed, dev, sets=4, n_experts=256, top_k=8, d_model=2048, d_ff=5
         q.gemv_gather(wl.gm[s], wl.ids[wl.tok % 64], ne, q.W_PACKED, T, wl.ws, stream=stream)
         wl.tok += 1
 
-    def step(stream=None):
-        quantize(stream)
-        kernel(stream)
+    def step(stream=None):  # fp32 inputs, quantised inside the one gather launch
+        s = wl.tok % sets
+        q.gemv_gather_f32(wl.gf[s], wl.ids[wl.tok % 64], ne, q.W_PACKED, T, wl.ws, stream=stream)
+        wl.tok += 1
 
+    quantize()  # the kernel-only launches' inputs
     wl.quantize = quantize
     wl.step, wl.kernel = step, kernel
     wl.inputs, wl.outputs = [wl.x_in, wl.x_dn], [wl.yg, wl.yu, wl.yd]
@@ -403,14 +410,36 @@ def _oracle_inputs(workload: str):
     return _ORACLE_INPUTS[workload]
 
 
-def oracle_sample(workload: str, budget_s: float = 12.0, min_s: float = 3.0):
+def cpu_model() -> str:
+    """The host CPU's model name, as /proc/cpuinfo or lscpu report it."""
+    try:
+        out = subprocess.run(["lscpu"], capture_output=True, text=True, timeout=10).stdout
+        for line in out.splitlines():
+            if line.strip().startswith("Model name:"):
+                return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    try:
+        with open("/proc/cpuinfo") as f:
+            for line in f:
+                if line.lower().startswith("model name"):
+                    return line.split(":", 1)[1].strip()
+    except Exception:
+        pass
+    import platform
+    return platform.processor() or platform.machine()
+
+
+def oracle_sample(workload: str, budget_s: float = 12.0, min_s: float = 3.0, threads: int | None = None):
     """Time the CPU oracle as it stands (Q8_0 quantisation, per-block int32
     sums, fp64 accumulation; OpenMP over rows) on a bounded sample of one step
-    of the workload.  Returns (GB/s under the GPU's byte accounting, threads,
-    description of the sample)."""
+    of the workload, on all cores or on `threads` threads.  Returns (GB/s
+    under the GPU's byte accounting, threads, description of the sample)."""
     import oracle
     oracle.build()
     o = oracle.load()
+    if threads:
+        o.set_threads(threads)
     T, data = _oracle_inputs(workload)
     done_bytes, t_total, n_done = 0, 0.0, 0
     while True:
@@ -431,6 +460,30 @@ def oracle_sample(workload: str, budget_s: float = 12.0, min_s: float = 3.0):
 
 
 # ============================================================ main
+
+def own_stream_gbs(dev, nbytes: int = 4 << 30) -> float:
+    """The library's own read-only stream (TMA, 16 warps x 2 x 4608-byte
+    stages per SM) over one 4 GiB buffer: the achievable HBM read rate of the
+    GEMV's access pattern, measured in this run (best of 5 launches)."""
+    import torch
+    q = _q()
+    buf = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    sink = torch.zeros(1, dtype=torch.int64, device=dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(2):
+        q.stream_read(buf, 0, 16, 2, 4608, sink)
+    best = float("inf")
+    for _ in range(5):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        q.stream_read(buf, 0, 16, 2, 4608, sink)
+        b.record(stream)
+        torch.cuda.synchronize()
+        best = min(best, a.elapsed_time(b))
+    del buf
+    torch.cuda.empty_cache()
+    return nbytes / (best * 1e-3) / 1e9
+
 
 def slowest_rank_ms(ms: float, world: int) -> float:
     """Replicas only: every rank runs the same workload; the job's step time
@@ -506,6 +559,7 @@ def main(argv=None):
     _build.build()
     q = _q()
 
+    own_stream = own_stream_gbs(dev)
     spec = synth.WORKLOADS[args.workload]
     Ts = [args.T] if args.T else list(spec.get("Ts", [spec.get("T", 1)]))
     results = {}
@@ -513,6 +567,10 @@ def main(argv=None):
         results[T] = measure(args, build_workload(args.workload, dev, T=T, layers=args.layers), dev, world, rank)
         torch.cuda.empty_cache()
     head = results[Ts[0]]
+    for r in results.values():
+        r["config"]["own_stream_gbs"] = round(own_stream, 1)
+        r["config"]["pct_of_own_stream"] = round(100 * r["value"] / world / own_stream, 2)
+        r["roofline"]["frac_of_own_stream"] = round(r["roofline"]["achieved"] / own_stream, 4)
     if rank == 0:
         if len(Ts) > 1:
             base = results[Ts[0]]["ms_per_step"]
@@ -520,9 +578,11 @@ def main(argv=None):
                                                    "cost_vs_T1": round(r["ms_per_step"] / base, 4)}
                                          for T, r in results.items()}
         if not args.no_cpu_baseline:
-            v, cores, desc = oracle_sample(args.workload)
+            v1, _, desc1 = oracle_sample(args.workload, budget_s=4.0, min_s=2.0, threads=1)
+            v, cores, desc = oracle_sample(args.workload, threads=os.cpu_count() or 1)
             head["cpu_baseline"] = {"value": round(v, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
-                                    "sample": desc}
+                                    "sample": desc, "single_thread_value": round(v1, 4),
+                                    "single_thread_sample": desc1, "cpu": cpu_model()}
         print(json.dumps(head), flush=True)
     if world > 1:
         import torch.distributed as tdist
@@ -565,6 +625,34 @@ def measure(args, wl: Workload, dev, world, rank):
     torch.cuda.synchronize()
     clk = clocks.stop()
     gemv_ms = k0.elapsed_time(k1) / K
+    # ---- the same kernel loop captured in a CUDA graph (median of 7 replays)
+    graph_ms = None
+    try:
+        R = 20
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(stream)
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.stream(side):
+            wl.kernel()
+            torch.cuda.synchronize()
+            with torch.cuda.graph(g):
+                for _ in range(R):
+                    wl.kernel()
+        stream.wait_stream(side)
+        g.replay()
+        torch.cuda.synchronize()
+        reps = []
+        for _ in range(7):
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            g.replay()
+            b.record(stream)
+            torch.cuda.synchronize()
+            reps.append(a.elapsed_time(b) / R)
+        graph_ms = statistics.median(reps)
+        del g
+    except Exception:
+        graph_ms = None
     ms = slowest_rank_ms(ms, world)
     assert q.device_status() == 0
 
@@ -597,6 +685,7 @@ def measure(args, wl: Workload, dev, world, rank):
     achieved = wl.gemv_kernel_bytes / (gemv_ms * 1e-3) / 1e9
     cfg = dict(wl.config)
     cfg.update({"us_per_gemv": round(ms * 1e3 / wl.n_gemv, 3), "gemv_kernel_ms": round(gemv_ms, 5),
+                "gemv_kernel_graph_ms": None if graph_ms is None else round(graph_ms, 5),
                 "pct_of_hbm_peak": round(100 * gbs / world / peak, 2), "peak_kind": peak_kind,
                 "pct_of_8TBs": round(100 * gbs / world / 8000.0, 2), "step_bytes": wl.step_bytes})
     return {

@@ -265,6 +265,28 @@ qgemv_status qgemv_q4_0_gather(const qgemv_gather_matrix *mats, int n_mats, cons
                                int n_ids, int n_experts, qgemv_wlayout layout, int T, void *ws,
                                size_t ws_bytes, qgemv_stream_t stream);
 
+/* A gather matrix with fp32 activations: slot s reads x + s * x_stride
+ * (bytes; 0 = shared by all slots), fp32 [T][K], 4-byte aligned. */
+typedef struct {
+    const void *W;
+    int64_t expert_stride;
+    const float *x;
+    int64_t x_stride;
+    float *y;
+    int64_t y_stride;
+    int64_t N;
+    int64_t K;
+} qgemv_gather_f32_matrix;
+
+/* Workspace bytes for qgemv_q4_0_gather_f32 (0 if invalid). */
+size_t qgemv_gather_f32_workspace_bytes(const qgemv_gather_f32_matrix *mats, int n_mats, int n_ids, int T);
+
+/* qgemv_q4_0_gather with fp32 activations, quantised inside the kernel (the
+ * same bytes as qgemv_quantize_q8_0): a routed-expert step is one launch. */
+qgemv_status qgemv_q4_0_gather_f32(const qgemv_gather_f32_matrix *mats, int n_mats, const int32_t *ids,
+                                   int n_ids, int n_experts, qgemv_wlayout layout, int T, void *ws,
+                                   size_t ws_bytes, qgemv_stream_t stream);
+
 /* Test hook: the exact per-block integer sums the GEMV kernels form,
  * isums[T][N][K/32] int32 (device), from the same unpack / int8-dot code. */
 qgemv_status qgemv_debug_block_isums(const void *W, qgemv_wlayout layout, const void *xq,

@@ -80,9 +80,15 @@ class Oracle:
         L.orc_argmax_f64.argtypes = [_f64p, ctypes.c_int64]
         L.orc_argmax_f64.restype = ctypes.c_int64
         L.orc_num_threads.restype = ctypes.c_int
+        L.orc_set_threads.argtypes = [ctypes.c_int]
+        L.orc_set_threads.restype = ctypes.c_int
         L.orc_mutant.restype = ctypes.c_int
         L.orc_range_violations.restype = ctypes.c_long
         self.L = L
+
+    def set_threads(self, n: int) -> int:
+        """Threads of the row loops (timing only; results do not depend on it)."""
+        return int(self.L.orc_set_threads(int(n)))
 
     # -- binary16
     def half_to_float(self, h: int) -> float:

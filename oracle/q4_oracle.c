@@ -320,4 +320,16 @@ int orc_num_threads(void)
 #endif
 }
 
+/* Threads of the row loops from now on (n >= 1); returns the new count. */
+int orc_set_threads(int n)
+{
+#ifdef _OPENMP
+    if (n >= 1) omp_set_num_threads(n);
+    return omp_get_max_threads();
+#else
+    (void)n;
+    return 1;
+#endif
+}
+
 int orc_mutant(void) { return ORC_MUTANT; }

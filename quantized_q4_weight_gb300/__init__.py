@@ -47,6 +47,12 @@ class GatherMatrix(ctypes.Structure):
                 ("N", ctypes.c_int64), ("K", ctypes.c_int64)]
 
 
+class GatherF32Matrix(ctypes.Structure):
+    _fields_ = [("W", ctypes.c_void_p), ("expert_stride", ctypes.c_int64), ("x", ctypes.c_void_p),
+                ("x_stride", ctypes.c_int64), ("y", ctypes.c_void_p), ("y_stride", ctypes.c_int64),
+                ("N", ctypes.c_int64), ("K", ctypes.c_int64)]
+
+
 _lib = None
 
 _VP, _I64, _I32, _SZ = ctypes.c_void_p, ctypes.c_int64, ctypes.c_int, ctypes.c_size_t
@@ -70,6 +76,9 @@ _SIGS = {
     "qgemv_q4_0_seq_f32": ([ctypes.POINTER(SeqF32Item), _I32, _I32, _I32, _VP, _SZ, _VP], _I32),
     "qgemv_gather_workspace_bytes": ([ctypes.POINTER(GatherMatrix), _I32, _I32, _I32], _SZ),
     "qgemv_q4_0_gather": ([ctypes.POINTER(GatherMatrix), _I32, _VP, _I32, _I32, _I32, _I32, _VP, _SZ, _VP], _I32),
+    "qgemv_gather_f32_workspace_bytes": ([ctypes.POINTER(GatherF32Matrix), _I32, _I32, _I32], _SZ),
+    "qgemv_q4_0_gather_f32": ([ctypes.POINTER(GatherF32Matrix), _I32, _VP, _I32, _I32, _I32, _I32, _VP, _SZ, _VP],
+                              _I32),
     "qgemv_debug_block_isums": ([_VP, _I32, _VP, _VP, _I64, _I64, _I32, _VP], _I32),
     "qgemv_debug_stream_read": ([_VP, _SZ, _I32, _I32, _I32, _I32, _VP, _VP], _I32),
     "qgemv_set_tuning": ([_I32, _I32, _I32, _I32], _I32),
@@ -236,6 +245,24 @@ def gather_workspace_bytes(mats: ctypes.Array, n_ids: int, T: int) -> int:
 def gemv_gather(mats: ctypes.Array, ids, n_experts: int, layout: int, T: int, ws, stream=None):
     _check(lib().qgemv_q4_0_gather(mats, len(mats), _ptr(ids), ids.numel(), n_experts, layout, T, _ptr(ws),
                                    ws.numel(), _stream(stream)), "qgemv_q4_0_gather")
+
+
+def gather_f32_mats(entries) -> ctypes.Array:
+    """entries: (W, expert_stride_bytes, x, x_stride_bytes, y, y_stride_floats, N, K), x fp32."""
+    entries = list(entries)
+    arr = (GatherF32Matrix * len(entries))()
+    for i, (W, ws_, x, xs, y, ys, N, K) in enumerate(entries):
+        arr[i] = GatherF32Matrix(W.data_ptr(), ws_, x.data_ptr(), xs, y.data_ptr(), ys, N, K)
+    return arr
+
+
+def gather_f32_workspace_bytes(mats: ctypes.Array, n_ids: int, T: int) -> int:
+    return int(lib().qgemv_gather_f32_workspace_bytes(mats, len(mats), n_ids, T))
+
+
+def gemv_gather_f32(mats: ctypes.Array, ids, n_experts: int, layout: int, T: int, ws, stream=None):
+    _check(lib().qgemv_q4_0_gather_f32(mats, len(mats), _ptr(ids), ids.numel(), n_experts, layout, T, _ptr(ws),
+                                       ws.numel(), _stream(stream)), "qgemv_q4_0_gather_f32")
 
 
 def block_isums(W, layout: int, xq, N: int, K: int, T: int, stream=None) -> torch.Tensor:

@@ -624,32 +624,72 @@ qgemv_status qgemv_q4_0_seq_f32(const qgemv_seq_f32_item *items, int n, qgemv_wl
     return launch_seq(sq.data(), n, layout, T, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream), true);
 }
 
-static qgemv_status gather_specs(const qgemv_gather_matrix *mats, int n_mats, int n_ids, int T, GroupSpec *gs)
+extern "C++" {
+// One gather matrix, quantised (xq) or fp32 (x) activations alike.
+struct GatherIn {
+    const void *W;
+    long long expert_stride;
+    const void *x;  // planar Q8_0, or fp32 [T][K] on the fp32 call
+    long long x_stride;
+    float *y;
+    long long y_stride;
+    long long N, K;
+};
+
+static GatherIn gather_in(const qgemv_gather_matrix &a)
+{
+    return GatherIn{a.W, a.expert_stride, a.xq, a.xq_stride, a.y, a.y_stride, a.N, a.K};
+}
+static GatherIn gather_in(const qgemv_gather_f32_matrix &a)
+{
+    return GatherIn{a.W, a.expert_stride, a.x, a.x_stride, a.y, a.y_stride, a.N, a.K};
+}
+
+static qgemv_status gather_specs(const GatherIn *mats, int n_mats, int n_ids, int T, GroupSpec *gs)
 {
     if (!mats || n_mats < 1 || n_mats > MAXG_SMALL || n_ids < 1 || T < 1 || T > 8) return QGEMV_ERR_INVALID_ARG;
     for (int m = 0; m < n_mats; ++m) {
-        const qgemv_gather_matrix &a = mats[m];
+        const GatherIn &a = mats[m];
         if (!shape_ok(a.N, a.K)) return QGEMV_ERR_INVALID_ARG;
         if (n_ids > 1 && a.y_stride < static_cast<long long>(T) * a.N) return QGEMV_ERR_INVALID_ARG;
-        if (a.expert_stride < 0 || a.xq_stride < 0) return QGEMV_ERR_INVALID_ARG;
-        gs[m] = GroupSpec{a.W, a.expert_stride, a.xq, a.xq_stride, a.y, a.y_stride, a.N, a.K, n_ids};
+        if (a.expert_stride < 0 || a.x_stride < 0) return QGEMV_ERR_INVALID_ARG;
+        gs[m] = GroupSpec{a.W, a.expert_stride, a.x, a.x_stride, a.y, a.y_stride, a.N, a.K, n_ids};
     }
     return QGEMV_OK;
 }
 
-size_t qgemv_gather_workspace_bytes(const qgemv_gather_matrix *mats, int n_mats, int n_ids, int T)
+template <class M>
+static size_t gather_ws(const M *mats, int n_mats, int n_ids, int T)
 {
+    if (!mats || n_mats < 1 || n_mats > MAXG_SMALL) return 0;
+    GatherIn in[MAXG_SMALL];
+    for (int m = 0; m < n_mats; ++m) in[m] = gather_in(mats[m]);
     GroupSpec gs[MAXG_SMALL];
-    if (gather_specs(mats, n_mats, n_ids, T, gs) != QGEMV_OK) return 0;
+    if (gather_specs(in, n_mats, n_ids, T, gs) != QGEMV_OK) return 0;
     Plan<MAXG_SMALL> a, b;
     make_plan<MAXG_SMALL>(gs, n_mats, T, false, false, nullptr, 0, a);
     make_plan<MAXG_SMALL>(gs, n_mats, T, true, false, nullptr, 0, b);
     return static_cast<size_t>(a.ws_bytes > b.ws_bytes ? a.ws_bytes : b.ws_bytes);
 }
 
-qgemv_status qgemv_q4_0_gather(const qgemv_gather_matrix *mats, int n_mats, const int32_t *ids, int n_ids,
-                               int n_experts, qgemv_wlayout layout, int T, void *ws, size_t ws_bytes,
-                               qgemv_stream_t stream)
+}  // extern "C++"
+
+size_t qgemv_gather_workspace_bytes(const qgemv_gather_matrix *mats, int n_mats, int n_ids, int T)
+{
+    return gather_ws(mats, n_mats, n_ids, T);
+}
+
+size_t qgemv_gather_f32_workspace_bytes(const qgemv_gather_f32_matrix *mats, int n_mats, int n_ids, int T)
+{
+    return gather_ws(mats, n_mats, n_ids, T);
+}
+
+// The gather calls (checked here).  xf32: activations are fp32 x[T][K],
+// quantised inside the kernel.  No dependent-launch overlap: the run table
+// reads the expert ids, which the preceding kernel may write.
+static qgemv_status gather_call(const GatherIn *mats, int n_mats, const int32_t *ids, int n_ids, int n_experts,
+                                qgemv_wlayout layout, int T, void *ws, size_t ws_bytes, qgemv_stream_t stream,
+                                bool xf32)
 {
     GroupSpec gs[MAXG_SMALL];
     qgemv_status s = gather_specs(mats, n_mats, n_ids, T, gs);
@@ -660,20 +700,21 @@ qgemv_status qgemv_q4_0_gather(const qgemv_gather_matrix *mats, int n_mats, cons
     if (!ws) return QGEMV_ERR_WORKSPACE;
     if (!aligned(ws, 256)) return QGEMV_ERR_MISALIGNED;
     const Range rw = range(ws, static_cast<long long>(ws_bytes));
+    const long long xa = xf32 ? 4 : 16;
     for (int m = 0; m < n_mats; ++m) {
-        const qgemv_gather_matrix &a = mats[m];
-        if (!a.W || !a.xq || !a.y) return QGEMV_ERR_INVALID_ARG;
+        const GatherIn &a = mats[m];
+        if (!a.W || !a.x || !a.y) return QGEMV_ERR_INVALID_ARG;
         const size_t wa = layout == QGEMV_W_PACKED ? 16 : 2;
-        if (!aligned(a.W, wa) || a.expert_stride % static_cast<long long>(wa) != 0 || !aligned(a.xq, 16) ||
-            a.xq_stride % 16 != 0 || !aligned(a.y, 4))
+        if (!aligned(a.W, wa) || a.expert_stride % static_cast<long long>(wa) != 0 || !aligned(a.x, xa) ||
+            a.x_stride % xa != 0 || !aligned(a.y, 4))
             return QGEMV_ERR_MISALIGNED;
         const Range ry = range(a.y, 4ll * ((n_ids - 1) * a.y_stride + static_cast<long long>(T) * a.N));
         if (overlap(ry, rw)) return QGEMV_ERR_INVALID_ARG;
         for (int k = 0; k < n_mats; ++k) {
-            const qgemv_gather_matrix &b = mats[k];
+            const GatherIn &b = mats[k];
             const long long wb = (n_experts - 1) * b.expert_stride + 18ll * b.N * (b.K / QK);
-            const long long xb = (n_ids - 1) * b.xq_stride + xq_bytes_host(T, b.K);
-            if (overlap(ry, range(b.W, wb)) || overlap(ry, range(b.xq, xb))) return QGEMV_ERR_INVALID_ARG;
+            const long long xb = (n_ids - 1) * b.x_stride + (xf32 ? 4ll * T * b.K : xq_bytes_host(T, b.K));
+            if (overlap(ry, range(b.W, wb)) || overlap(ry, range(b.x, xb))) return QGEMV_ERR_INVALID_ARG;
             if (k != m && overlap(ry, range(b.y, 4ll * ((n_ids - 1) * b.y_stride + static_cast<long long>(T) * b.N))))
                 return QGEMV_ERR_INVALID_ARG;
         }
@@ -690,12 +731,33 @@ qgemv_status qgemv_q4_0_gather(const qgemv_gather_matrix *mats, int n_mats, cons
     pl.P.status = dev.status;
     pl.P.ids = ids;
     pl.P.n_experts = n_experts;
+    pl.P.xf32 = xf32 ? 1 : 0;
     const int grid = grid_for(dev, cps);
     set_cta_groups(pl.P, grid);
     return dispatch_T<MAXG_SMALL, false>(pl.P, T, mma_for(T), grid, pl.smem, reinterpret_cast<cudaStream_t>(stream), false) ==
                    cudaSuccess
                ? QGEMV_OK
                : QGEMV_ERR_CUDA;
+}
+
+qgemv_status qgemv_q4_0_gather(const qgemv_gather_matrix *mats, int n_mats, const int32_t *ids, int n_ids,
+                               int n_experts, qgemv_wlayout layout, int T, void *ws, size_t ws_bytes,
+                               qgemv_stream_t stream)
+{
+    if (!mats || n_mats < 1 || n_mats > MAXG_SMALL) return QGEMV_ERR_INVALID_ARG;
+    GatherIn in[MAXG_SMALL];
+    for (int m = 0; m < n_mats; ++m) in[m] = gather_in(mats[m]);
+    return gather_call(in, n_mats, ids, n_ids, n_experts, layout, T, ws, ws_bytes, stream, false);
+}
+
+qgemv_status qgemv_q4_0_gather_f32(const qgemv_gather_f32_matrix *mats, int n_mats, const int32_t *ids, int n_ids,
+                                   int n_experts, qgemv_wlayout layout, int T, void *ws, size_t ws_bytes,
+                                   qgemv_stream_t stream)
+{
+    if (!mats || n_mats < 1 || n_mats > MAXG_SMALL) return QGEMV_ERR_INVALID_ARG;
+    GatherIn in[MAXG_SMALL];
+    for (int m = 0; m < n_mats; ++m) in[m] = gather_in(mats[m]);
+    return gather_call(in, n_mats, ids, n_ids, n_experts, layout, T, ws, ws_bytes, stream, true);
 }
 
 qgemv_status qgemv_debug_block_isums(const void *W, qgemv_wlayout layout, const void *xq, int32_t *isums, int64_t N,

@@ -514,3 +514,40 @@ def test_argmax_f32_matches_quantised_argmax(orc, T):
     assert torch.equal(y0.cpu().view(torch.int32), y1.cpu().view(torch.int32))
     for t in range(T):
         assert int(i1[t]) == orc.argmax_f32(y1[t].cpu().numpy())
+
+
+def test_gather_f32_matches_quantised_gather(orc):
+    """The fp32 gather quantises inside the kernel: same bits as quantising
+    the shared input and the per-slot inputs first."""
+    T, n_exp, n_ids = 1, 6, 4
+    N1, K1, N2, K2 = 96, 512, 512, 256
+    shapes = [(N1, K1), (N2, K2)]
+    W = []
+    for m, (N, K) in enumerate(shapes):
+        per = q.q4_0_bytes(N, K)
+        buf = torch.empty(n_exp * per, dtype=torch.uint8, device=DEV)
+        for e in range(n_exp):
+            buf[e * per:(e + 1) * per] = q.pack_q4_0(to_dev(synth.q4_0_weights(1300 + m, N, K, stream=(e,))), N, K)
+        W.append(buf)
+    x1 = torch.from_numpy(synth.activations(1310, T, K1)).to(DEV)
+    x2 = torch.from_numpy(synth.activations(1311, n_ids * T, K2)).to(DEV)
+    xq1 = q.quantize_q8_0(x1, T, K1)
+    xq2 = q.quantize_q8_0(x2, T, K2, batch=n_ids)
+    ids = torch.tensor([3, 0, 5, 3], dtype=torch.int32, device=DEV)
+    outs = []
+    for f32 in (False, True):
+        y1 = torch.empty((n_ids, T, N1), dtype=torch.float32, device=DEV)
+        y2 = torch.empty((n_ids, T, N2), dtype=torch.float32, device=DEV)
+        if f32:
+            mats = q.gather_f32_mats([(W[0], q.q4_0_bytes(N1, K1), x1, 0, y1, T * N1, N1, K1),
+                                      (W[1], q.q4_0_bytes(N2, K2), x2, 4 * T * K2, y2, T * N2, N2, K2)])
+            q.gemv_gather_f32(mats, ids, n_exp, q.W_PACKED, T, q.new_workspace(q.gather_f32_workspace_bytes(mats, n_ids, T)))
+        else:
+            mats = q.gather_mats([(W[0], q.q4_0_bytes(N1, K1), xq1, 0, y1, T * N1, N1, K1),
+                                  (W[1], q.q4_0_bytes(N2, K2), xq2, q.xq_bytes(T, K2), y2, T * N2, N2, K2)])
+            q.gemv_gather(mats, ids, n_exp, q.W_PACKED, T, q.new_workspace(q.gather_workspace_bytes(mats, n_ids, T)))
+        torch.cuda.synchronize()
+        outs.append((y1.cpu(), y2.cpu()))
+    assert q.device_status() == 0
+    for a, b in zip(outs[0], outs[1]):
+        assert torch.equal(a.view(torch.int32), b.view(torch.int32))
