@@ -113,3 +113,31 @@ def test_other_calls_reject_bad_arguments(L):
     assert L.qgemv_q4_0_gather(mats, 1, FAKE + (1 << 31), 2, 4, 1, 1, FAKE + (1 << 30), 4096, s) == 1  # y_stride < T*N
     assert L.qgemv_q4_0_gather(mats, 1, None, 1, 4, 1, 1, FAKE + (1 << 30), 4096, s) == 1
     assert L.qgemv_debug_block_isums(FAKE, 1, FAKE, None, 16, 64, 1, s) == 1
+
+
+def test_fp32_calls_reject_bad_arguments(L):
+    """The fp32-input calls check their own input ranges: alignment (4 bytes),
+    null pointers, and outputs that overlap the fp32 inputs or the workspace."""
+    s = None
+    ws = FAKE + (1 << 30)
+    x = FAKE + (1 << 28)
+    # argmax_f32: missing idx, misaligned x, y overlapping x
+    assert L.qgemv_q4_0_argmax_f32(FAKE, 1, x, None, None, 64, 64, 1, ws, 4096, s) == 1
+    assert L.qgemv_q4_0_argmax_f32(FAKE, 1, x + 2, None, FAKE + (1 << 29), 64, 64, 1, ws, 4096, s) == 2
+    assert L.qgemv_q4_0_argmax_f32(FAKE, 1, x, x + 4, FAKE + (1 << 29), 64, 64, 1, ws, 4096, s) == 1
+    # gemv_f32: x only needs 4-byte alignment, y overlapping the workspace is refused
+    assert L.qgemv_q4_0_f32(FAKE, 1, x + 2, FAKE + (1 << 29), 64, 64, 1, ws, 1 << 20, s) == 2
+    assert L.qgemv_q4_0_f32(FAKE, 1, x, ws + 256, 64, 64, 1, ws, 1 << 20, s) == 1
+    # seq_f32: an output overlapping another item's fp32 input
+    items = (q.SeqF32Item * 2)(q.SeqF32Item(FAKE, x, FAKE + (1 << 29), 64, 64),
+                               q.SeqF32Item(FAKE, x + 4096, x, 64, 64))
+    assert L.qgemv_q4_0_seq_f32(items, 2, 1, 1, ws, 1 << 20, s) == 1
+    items2 = (q.SeqF32Item * 1)(q.SeqF32Item(FAKE, x + 2, FAKE + (1 << 29), 64, 64))
+    assert L.qgemv_q4_0_seq_f32(items2, 1, 1, 1, ws, 1 << 20, s) == 2
+    # gather_f32: misaligned x stride, y_stride below T * N
+    mats = (q.GatherF32Matrix * 1)(q.GatherF32Matrix(FAKE, 4608, x, 6, FAKE + (1 << 29), 64, 64, 128))
+    assert L.qgemv_q4_0_gather_f32(mats, 1, FAKE + (1 << 31), 2, 4, 1, 1, ws, 4096, s) == 2
+    mats2 = (q.GatherF32Matrix * 1)(q.GatherF32Matrix(FAKE, 4608, x, 512, FAKE + (1 << 29), 10, 64, 128))
+    assert L.qgemv_q4_0_gather_f32(mats2, 1, FAKE + (1 << 31), 2, 4, 1, 1, ws, 4096, s) == 1
+    assert L.qgemv_gather_f32_workspace_bytes(mats2, 1, 2, 1) == 0
+    assert L.qgemv_seq_f32_workspace_bytes(items, 2, 1) >= 16384

@@ -551,3 +551,31 @@ def test_gather_f32_matches_quantised_gather(orc):
     assert q.device_status() == 0
     for a, b in zip(outs[0], outs[1]):
         assert torch.equal(a.view(torch.int32), b.view(torch.int32))
+
+
+@pytest.mark.parametrize("f32", [False, True])
+def test_seq_longer_than_one_launch(orc, f32):
+    """More items than one launch takes (224): the library splits the list;
+    every item equals its single call, bit for bit."""
+    n, T = 230, 2
+    shapes = [(16 + (i % 5), 32 * (1 + i % 4)) for i in range(n)]
+    Ws, xs, xqs, ys, refs = [], [], [], [], []
+    for i, (N, K) in enumerate(shapes):
+        Wg, Wp = weights(2000 + i, N, K, q.W_PACKED)
+        x = torch.from_numpy(synth.activations(3000 + i, T, K)).to(DEV)
+        xq = q.quantize_q8_0(x, T, K)
+        Ws.append(Wp)
+        xs.append(x)
+        xqs.append(xq)
+        ys.append(torch.empty((T, N), dtype=torch.float32, device=DEV))
+        refs.append(q.gemv(Wp, q.W_PACKED, xq, N, K, T, ws_for(N, K, T)).cpu())
+    if f32:
+        items = q.seq_f32_items([(Ws[i], xs[i], ys[i], N, K) for i, (N, K) in enumerate(shapes)])
+        q.gemv_seq_f32(items, q.W_PACKED, T, q.new_workspace(q.seq_f32_workspace_bytes(items, T)))
+    else:
+        items = q.seq_items([(Ws[i], xqs[i], ys[i], N, K) for i, (N, K) in enumerate(shapes)])
+        q.gemv_seq(items, q.W_PACKED, T, q.new_workspace(q.seq_workspace_bytes(items, T)))
+    torch.cuda.synchronize()
+    assert q.device_status() == 0
+    for i in range(n):
+        assert torch.equal(refs[i].view(torch.int32), ys[i].cpu().view(torch.int32)), i
