@@ -1,27 +1,32 @@
 // gemv_kernel.cuh -- the weight-streaming Q4_0 x Q8_0 GEMV kernel.
 //
-// One persistent CTA per SM, 8 warps.  A launch covers a list of GEMVs
-// ("groups" x "instances"); their work is cut into items -- one 16-row slab
-// over all of K, or (split-K) over one 16-block segment of K -- and the items
-// are dealt to CTAs as contiguous ranges of equal weight bytes.  Inside a CTA
-// the items of each (group, instance) run go round-robin to the warps.
+// One persistent CTA per SM (16 warps, or 8 where registers or shared memory
+// ask for it).  A launch covers a list of GEMVs ("groups" x "instances");
+// their work is cut into items -- one 16-row slab over all of K, or
+// (split-K) over one 16-block segment of K -- and the items are dealt to
+// CTAs as contiguous ranges of equal weight bytes.  Inside a CTA the runs
+// (items of one group instance) are cut into groups whose activations fit
+// shared memory together, and each group's stages are split evenly over the
+// warps (balanced mode); split-K launches process runs in turn instead.
 //
 // Weight bytes reach shared memory through 1-D bulk asynchronous copies
 // (TMA, cp.async.bulk) into a per-warp ring of stages (one stage = one
 // 16-block segment of a slab = 4608 bytes), each completing on its own
 // mbarrier; the next stage is issued as soon as a slot is consumed, so every
-// warp keeps ring_depth stages in flight.  The activations of the current
-// run (planar Q8_0) are copied into shared memory once per CTA, together with
-// each block's folded-offset constant and fp32 scale.
+// warp keeps ring_depth stages in flight.  The activations of a run are
+// copied into shared memory once per CTA (or quantised there from fp32),
+// together with each block's folded-offset constant and scale.
 //
-// Lane mapping (minfer README M15 repacks rows into groups so a warp reads
-// contiguous bytes; here 16-row slabs): lane = 4 * r8 + j handles rows r8 and
-// r8 + 8 of the slab and the blocks b with b % 4 == j.  Per block it unpacks
-// the nibbles with two masks (M9: SIMD nibble masking), forms the exact
-// integer block sum with dp4a and the folded -8 offset (M9), and accumulates
-// (d_w * d_x) * isum with one fp32 fused multiply-add.  At the end of a
-// segment the four phases are combined by a fixed two-level shuffle tree;
-// segments are added in order.  The order depends only on K (include/qgemv.h).
+// One-token lanes (dp4a path; minfer README M15 repacks rows into groups so
+// a warp reads contiguous bytes, here 16-row slabs): lane = 4 * r8 + j
+// handles rows r8 and r8 + 8 of the slab and the blocks b with b % 4 == j.
+// Per block it unpacks the nibbles with two masks (M9: SIMD nibble masking),
+// forms the exact integer block sum with dp4a and the folded -8 offset (M9),
+// and accumulates (d_w * d_x) * isum with one fp32 fused multiply-add.  At
+// the end of a segment the four phases are combined by a fixed two-level
+// shuffle tree; segments are added in order.  Several tokens on the tensor
+// cores (see "MMA path") keep the same order.  The order depends only on K
+// (include/qgemv.h).
 //
 // Every wait on an asynchronous copy is bounded (see mbar_wait_bounded); a
 // CTA that gives up records a status word, stops issuing copies, drains the

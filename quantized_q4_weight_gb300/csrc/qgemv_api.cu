@@ -29,9 +29,9 @@ struct DevInfo {
     unsigned *status = nullptr;
 };
 
-// Launch shape of the streaming kernel: CTAs resident per SM (1, or 2 of
-// 8 warps for T <= 2) and waves of CTAs per launch.  More, smaller CTAs let
-// the block scheduler give more work to SMs that stream faster.
+// Launch shape of the streaming kernel (0 = default): CTAs resident per SM
+// (1: one CTA of up to 16 warps; 2: two CTAs of 8 warps), waves of CTAs per
+// launch and weight stages per warp.  Results never depend on them.
 std::atomic<int> g_ctas_per_sm{0}, g_waves{0}, g_ring_depth{0};
 // Token count from which T > 1 runs on the f16 tensor-core path (0 = default).
 std::atomic<int> g_mma_min_T{0};
