@@ -4,7 +4,8 @@
 // ask for it).  A launch covers a list of GEMVs ("groups" x "instances");
 // their work is cut into items -- one 16-row slab over all of K, or
 // (split-K) over one 16-block segment of K -- and the items are dealt to
-// CTAs as contiguous ranges of equal weight bytes.  Inside a CTA the runs
+// CTAs as contiguous ranges of equal weighted bytes (a byte of a group
+// whose per-block work costs more counts more).  Inside a CTA the runs
 // (items of one group instance) are cut into groups whose activations fit
 // shared memory together, and each group's stages are split evenly over the
 // warps (balanced mode); split-K launches process runs in turn instead.
@@ -93,26 +94,26 @@ __device__ __forceinline__ ItemInfo decode_item(const Params<MAXG> &P, long long
     return it;
 }
 
-// First item whose (virtual) start byte is >= X.  Items are laid out in the
-// byte space as: slab s, segment part p at s * slab_bytes + seg0 * SEG_BYTES;
-// the tail after the slabs.
-// The first item whose weights start at or after byte X of the launch, for
-// the group g that holds X (g.byte_begin <= X <= the next group's byte_begin;
-// X below the launch's total).
+// The first item whose weights start at or after position X of the launch's
+// weighted byte space (each group's bytes times its cost), for the group g
+// that holds X (g.cost_begin <= X <= the next group's cost_begin; X below the
+// launch's total).  Within an instance, slab s and its segment part p start at
+// (s * slab_bytes + p * spp * SEG_BYTES) * cost; the tail follows the slabs.
 __device__ __forceinline__ long long first_item_in_group(const Group &g, long long X)
 {
-    const long long local = X - g.byte_begin;
-    const long long e = local / g.inst_bytes;
-    const long long rem = local - e * g.inst_bytes;
+    const long long local = X - g.cost_begin;
+    const long long inst = g.inst_bytes * g.cost, slab = g.slab_bytes * g.cost;
+    const long long e = local / inst;
+    const long long rem = local - e * inst;
     const long long base = g.item_begin + e * g.items_per_inst;
     if (rem == 0) return base;
-    const long long slabs_bytes = static_cast<long long>(g.nslabs) * g.slab_bytes;
+    const long long slabs_bytes = static_cast<long long>(g.nslabs) * slab;
     if (rem < slabs_bytes) {
-        const long long s = rem / g.slab_bytes;
-        const long long r2 = rem - s * g.slab_bytes;
+        const long long s = rem / slab;
+        const long long r2 = rem - s * slab;
         if (r2 == 0) return base + s * g.split;
         const int spp = (g.nseg + g.split - 1) / g.split;
-        const long long pb = static_cast<long long>(spp) * SEG_BYTES;
+        const long long pb = static_cast<long long>(spp) * SEG_BYTES * g.cost;
         const long long p = (r2 + pb - 1) / pb;
         if (p >= g.split) return base + (s + 1) * g.split;
         return base + s * g.split + p;
@@ -960,9 +961,10 @@ __device__ __forceinline__ unsigned copy_activations(uint8_t *img, const uint8_t
 
 
 // Warps per CTA a T-token kernel may use: 16 (128 registers per thread),
-// except the dp4a path above two tokens, whose per-token accumulators need
-// more registers (8 warps).
-__host__ __device__ constexpr int max_warps_for(int T, bool mma) { return (mma || T <= 2) ? NWARPS_MAX : 8; }
+// except the dp4a path above four tokens, whose per-token accumulators need
+// more registers (8 warps).  Measured at three and four tokens: 16 warps at
+// 128 registers, with a few spilled words, beat 8 warps without spills.
+__host__ __device__ constexpr int max_warps_for(int T, bool mma) { return (mma || T <= 4) ? NWARPS_MAX : 8; }
 
 // ------------------------------------------------------------------ balanced mode
 //
@@ -1236,8 +1238,8 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
     ring.issued = 0;
     ring.consumed = 0;
 
-    const long long b0 = H.total_bytes * blockIdx.x / gridDim.x;
-    const long long b1 = H.total_bytes * (blockIdx.x + 1) / gridDim.x;
+    const long long b0 = H.total_cost * blockIdx.x / gridDim.x;
+    const long long b1 = H.total_cost * (blockIdx.x + 1) / gridDim.x;
 
     // The descriptors of the groups from g0 to gn, copied to shared memory by
     // every thread in parallel; this range's last byte lies in gn unless gn
@@ -1254,13 +1256,13 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
     }
     __syncthreads();
     const Group &gnd = gn - g0 < ngc ? gcache[gn - g0] : P.g[gn];
-    const int g1 = (b1 < H.total_bytes && gn > g0 && gnd.byte_begin >= b1) ? gn - 1 : gn;
+    const int g1 = (b1 < H.total_cost && gn > g0 && gnd.cost_begin >= b1) ? gn - 1 : gn;
 
     if (tid == 0) {
         s_abort = 0;
         mbar_init(xbar, 1);
-        s_i0 = b0 >= H.total_bytes ? H.total_items : first_item_in_group(gcache[0], b0);
-        s_i1 = b1 >= H.total_bytes ? H.total_items
+        s_i0 = b0 >= H.total_cost ? H.total_items : first_item_in_group(gcache[0], b0);
+        s_i1 = b1 >= H.total_cost ? H.total_items
                                    : first_item_in_group(g1 - g0 < ngc ? gcache[g1 - g0] : P.g[g1], b1);
     }
     __syncthreads();

@@ -114,6 +114,17 @@ struct Plan {
 constexpr long long CNT_AREA = 16384;
 static_assert(CNT_AREA / 4 > SPLIT_SLAB_THRESHOLD, "split-K counters must fit the counter area");
 
+// Partition weight of one weight byte of a group, in sixteenths, so that
+// CTAs get equal time rather than equal bytes where the per-block work
+// differs: on the tensor-core path (compute-bound) a group whose activations
+// take the int8 image, too large for the f16 operand image, converts them to
+// f16 in every warp and block; measured at about 1.125 times the time per
+// byte of an f16-image group.  The partition never changes a result.
+inline int partition_cost(int T, int K, bool mma)
+{
+    return mma && !xq_layout(T, K, true).f16 ? 18 : 16;
+}
+
 template <int MAXG>
 qgemv_status make_plan(const GroupSpec *gs, int n, int T, bool ggml, bool argmax, uint8_t *ws, int smem_limit,
                        Plan<MAXG> &pl, int ctas_per_sm = 1, bool mma = false)
@@ -137,7 +148,7 @@ qgemv_status make_plan(const GroupSpec *gs, int n, int T, bool ggml, bool argmax
         P.am_cand = ws ? reinterpret_cast<unsigned long long *>(ws + off) : nullptr;
         off = align_up(off + static_cast<long long>(MAX_GRID) * T * 8, 256);
     }
-    long long bytes = 0, items = 0;
+    long long cost = 0, items = 0;
     int kmax = 0, nbmax = 0;
     for (int i = 0; i < n; ++i) {
         Group &g = P.g[i];
@@ -165,9 +176,10 @@ qgemv_status make_plan(const GroupSpec *gs, int n, int T, bool ggml, bool argmax
         g.xq_bytes = static_cast<int>(xq_bytes_host(T, g.K));
         g.slab_bytes = static_cast<long long>(SLAB_COL_BYTES) * g.nb;
         g.inst_bytes = g.nslabs * g.slab_bytes + static_cast<long long>(g.tail_rows) * g.nb * Q4_BYTES;
-        g.byte_begin = bytes;
-        g.item_begin = items;
-        bytes += g.inst_bytes * g.count;
+        g.cost = partition_cost(T, g.K, mma);
+        g.cost_begin = cost;
+        g.item_begin = static_cast<int>(items);
+        cost += g.inst_bytes * g.count * g.cost;
         items += static_cast<long long>(g.items_per_inst) * g.count;
         if (g.split > 1) {
             const long long nc = static_cast<long long>(g.count) * g.nslabs;
@@ -180,7 +192,7 @@ qgemv_status make_plan(const GroupSpec *gs, int n, int T, bool ggml, bool argmax
         if (g.K > kmax) kmax = g.K;
         if (g.nb > nbmax) nbmax = g.nb;
     }
-    P.total_bytes = bytes;
+    P.total_cost = cost;
     P.total_items = items;
     P.kmax = kmax;
     P.nbmax = nbmax;
@@ -261,7 +273,7 @@ cudaError_t dispatch_T(const Params<MAXG> &P, int T, bool mma, int grid, size_t 
 inline int ctas_per_sm_for(int T, bool sequence)
 {
     const int c = g_ctas_per_sm.load(std::memory_order_relaxed);
-    if (!mma_for(T) && T > 2) return 1;  // 8 warps of wide accumulators fill the register file
+    if (!mma_for(T) && T > 4) return 1;  // 8 warps of wide accumulators fill the register file
     if (c >= 1 && c <= 2) return c;
     (void)sequence;  // measured: one CTA per SM with three stages per warp beats two CTAs of 8 warps
     return 1;
@@ -294,9 +306,9 @@ void set_cta_groups(Params<MAXG> &P, int grid)
 {
     int gi = 0;
     for (int c = 0; c <= grid; ++c) {
-        long long b = P.total_bytes * c / grid;
-        if (b >= P.total_bytes) b = P.total_bytes - 1;
-        while (gi + 1 < P.ngroups && P.g[gi + 1].byte_begin <= b) ++gi;
+        long long b = P.total_cost * c / grid;
+        if (b >= P.total_cost) b = P.total_cost - 1;
+        while (gi + 1 < P.ngroups && P.g[gi + 1].cost_begin <= b) ++gi;
         P.cta_g0[c] = static_cast<unsigned char>(gi);
     }
 }

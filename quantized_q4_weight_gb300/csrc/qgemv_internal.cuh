@@ -48,7 +48,9 @@ struct Group {
     int xq_bytes;                     // planar Q8_0 bytes per slot (T rows)
     long long inst_bytes;             // 18 * N * nb
     long long slab_bytes;             // 288 * nb
-    long long byte_begin, item_begin; // prefixes over the launch
+    long long cost_begin;             // prefix of the launch's weighted bytes (the CTA partition)
+    int item_begin;                   // prefix of the launch's items (a launch has < 2^31 items)
+    int cost;                         // partition weight of one weight byte, in sixteenths
     unsigned *cnt;                    // split-K arrival counters [count][nslabs]
     float *part;                      // split-K partials [count][nslabs][nseg][T][16]
 };
@@ -68,7 +70,7 @@ struct ParamHead {
     const int *ids;         // gather: slot -> expert id (nullptr: slot index)
     int n_experts;
     int xf32;               // the groups' activations are fp32 [T][K], quantised in the kernel
-    long long total_bytes, total_items;
+    long long total_cost, total_items;  // weighted bytes, items of the launch
     unsigned long long *am_cand;  // argmax: [gridDim][T] candidate keys
     unsigned *am_cnt;             // argmax: CTA arrival counter
     long long *am_idx;            // argmax: result [T]
