@@ -356,25 +356,30 @@ __device__ __forceinline__ void combine_phases(float (&acc)[2][T])
 // ------------------------------------------------------------------ MMA path (T > 1)
 //
 // Two mma.sync.m16n8k16 (f16 x f16 -> f32) per block form the 16 x 8 block
-// sums (16 rows of the slab, 8 token columns, zero past T).  Every operand is
-// a small integer (or an integer / 16) held exactly in f16, and every partial
-// sum is an integer below 2^22, so the fp32 accumulator holds the exact isum.
+// sums (16 rows of the slab, 8 token columns, zero past T), scaled by 2^-24.
+// Every operand is exact in f16: the nibbles enter as f16 subnormals (the
+// masked bits themselves, n 2^-24 or 16 n 2^-24), the activations as small
+// integers or integers / 16.  Every product and partial sum is a multiple of
+// 2^-24 below 2^-8, so the fp32 accumulator holds isum 2^-24 exactly.
 //
 // Lane (g, j) supplies word j of rows g and g + 8 (bytes 4j..4j+3: elements
 // 4j..4j+3 in the low nibbles, 16+4j..16+4j+3 in the high nibbles) and
 // activation words j and 4 + j of token g.  The k index of the first MMA
 // runs over the low-nibble elements in the order 4j, 4j+2 (k = 2j, 2j+1) and
 // 4j+1, 4j+3 (k = 2j+8, 2j+9); the second MMA the same over the high nibbles.
-//   low nibbles:  A = 1024 + n   (one LOP3: n | 0x6400),      B = q
-//   high nibbles: A = 1024 + 16 n (one LOP3: 16n | 0x6400),   B = q / 16
-// so the MMAs add isum + 1032 sum(q_lo) + 72 sum(q_hi); the first MMA's
-// accumulator input is C = -(1032 sum(q_lo) + 72 sum(q_hi)) (per token and
-// block) and the second ends at isum.  Activations, stored as q xor 0x80,
-// become f16 1024 + (q xor 0x80) with one PRMT and one f16x2 add (or fma by
-// 1/16) recovers q (or q / 16) exactly.  The lane keeps one fp32 sum per
-// block phase (b % 4) and output and adds (d_w * d_x) * isum with one fused
-// multiply-add: d_w * d_x is exact in fp32, and the dp4a lanes' product
-// (d_w * (d_x / 16)) * (16 isum) is the same real number, rounded the same.
+//   low nibbles:  A = n 2^-24    (one AND: w & 0x000F000F),   B = q
+//   high nibbles: A = 16 n 2^-24 (one AND: w & 0x00F000F0),   B = q / 16
+// so the MMAs add (sum n q) 2^-24; the first MMA's accumulator input is the
+// folded offset C = -8 sum(q) 2^-24 (per token and block) and the second
+// ends at isum 2^-24.  Activations, stored as q xor 0x80, become f16
+// 1024 + (q xor 0x80) with one PRMT, and one f16x2 add (or fma by 1/16)
+// recovers q (or q / 16) exactly.  The lane keeps one fp32 sum per block
+// phase (b % 4) and output and adds (d_w * d_x) * (isum 2^-24) with one
+// fused multiply-add: d_w * d_x is exact in fp32.  Every value of the
+// accumulation is a multiple of 2^-72 (or zero), far above the fp32
+// subnormal range, so each rounding is that of the unscaled sum scaled by
+// 2^-24; the segment sum is scaled back by 2^24 (exact).  The result is the
+// dp4a lanes' (d_w * (d_x / 16)) * (16 isum), rounded the same.
 
 __device__ __forceinline__ void mma_f16(float (&d)[4], unsigned a0, unsigned a1, unsigned a2, unsigned a3,
                                         unsigned b0, unsigned b1)
@@ -398,7 +403,8 @@ __device__ __forceinline__ unsigned hfma2_u(unsigned a, unsigned b, unsigned c)
     return d;
 }
 
-constexpr unsigned H2_1024 = 0x64006400u;      // f16x2 (1024, 1024)
+constexpr float MMA_SCALE = 5.9604644775390625e-8f;  // 2^-24
+constexpr float MMA_UNSCALE = 16777216.0f;           // 2^24
 constexpr unsigned H2_Q_BIAS = 0x64806480u;    // f16x2 1152: 1024 + (q xor 0x80) = 1152 + q
 constexpr unsigned H2_NEG_1152 = 0xE480E480u;  // f16x2 (-1152, -1152)
 constexpr unsigned H2_SIXTEENTH = 0x2C002C00u; // f16x2 (1/16, 1/16)
@@ -508,10 +514,8 @@ __device__ __forceinline__ void mma_block_core(unsigned wg, unsigned wg8, unsign
 {
     const unsigned g1 = __umulhi(wg, c_shr8_mul), g9 = __umulhi(wg8, c_shr8_mul);  // wg >> 8, wg8 >> 8
     float d[4];
-    mma_f16_c(d, (wg & 0x000F000Fu) | H2_1024, (wg8 & 0x000F000Fu) | H2_1024, (g1 & 0x000F000Fu) | H2_1024,
-              (g9 & 0x000F000Fu) | H2_1024, bl0, bl1, cq);
-    mma_f16(d, (wg & 0x00F000F0u) | H2_1024, (wg8 & 0x00F000F0u) | H2_1024, (g1 & 0x00F000F0u) | H2_1024,
-            (g9 & 0x00F000F0u) | H2_1024, bh0, bh1);
+    mma_f16_c(d, wg & 0x000F000Fu, wg8 & 0x000F000Fu, g1 & 0x000F000Fu, g9 & 0x000F000Fu, bl0, bl1, cq);
+    mma_f16(d, wg & 0x00F000F0u, wg8 & 0x00F000F0u, g1 & 0x00F000F0u, g9 & 0x00F000F0u, bh0, bh1);
     float s00, s01, s10, s11;  // (d_w d_x) for rows g, g + 8 and tokens 2j, 2j + 1
     h2_outer(sc, dx, s00, s01, s10, s11);
     ffma2(acc[0], acc[1], s00, s01, d[0], d[1]);
@@ -738,8 +742,8 @@ __device__ __forceinline__ void segment_sum(bool from_stage, const uint8_t *stag
             fadd2(u0, u1, acc[1][k], acc[1][k + 1]);
             fadd2(v0, v1, acc[3][k], acc[3][k + 1]);
             fadd2(u0, u1, v0, v1);
-            P[k] = u0;
-            P[k + 1] = u1;
+            P[k] = __fmul_rn(u0, MMA_UNSCALE);  // exact: back from the 2^-24 scale
+            P[k + 1] = __fmul_rn(u1, MMA_UNSCALE);
         }
     } else {
         float acc[2][T];
@@ -763,6 +767,13 @@ __device__ __forceinline__ void segment_sum(bool from_stage, const uint8_t *stag
     }
 }
 
+// The tensor-core accumulator start of one token's block: the folded
+// offset -8 sum(q), at the 2^-24 scale of the subnormal nibble operands.
+__device__ __forceinline__ float mma_fold_const(int sum_q)
+{
+    return __fmul_rn(static_cast<float>(-8 * sum_q), MMA_SCALE);  // exact: |8 sum(q)| < 2^15
+}
+
 // Tensor-core constants of block b, token t: C into both slots of the
 // pair's accumulator start, the raw fp16 d_x into the pair's d_x word.
 __device__ __forceinline__ void mma_store_consts(uint8_t *cd, int b, int t, float C, unsigned short dx)
@@ -778,7 +789,7 @@ __device__ __forceinline__ void mma_store_consts(uint8_t *cd, int b, int t, floa
 // per block and token the folded constant and the activation scale.  dp4a
 // path: {MAGIC - 128 sum(q), d_x / 16} per token; MMA path: the activation
 // bytes are rewritten as q xor 0x80, and each token's accumulator start
-// C = -(1032 sum(q_lo) + 72 sum(q_hi)) (fp32) and fp16 d_x go to the
+// C = -8 sum(q) 2^-24 (fp32, mma_fold_const) and fp16 d_x go to the
 // CD_MMA_QUAD layout, with zeros for the token columns past T.
 template <int T, bool MMA>
 __device__ __forceinline__ void build_fold_constants(uint8_t *img, int K, int tid, int nthreads)
@@ -810,7 +821,7 @@ __device__ __forceinline__ void build_fold_constants(uint8_t *img, int K, int ti
                 shi = dp4a_ss((int)qb.y, ones, shi);
                 shi = dp4a_ss((int)qb.z, ones, shi);
                 shi = dp4a_ss((int)qb.w, ones, shi);
-                mma_store_consts(img + L.off_cd, b, t, static_cast<float>(-(1032 * slo + 72 * shi)), xd[t * nb + b]);
+                mma_store_consts(img + L.off_cd, b, t, mma_fold_const(slo + shi), xd[t * nb + b]);
             } else {
                 cd[i] = make_int2(block_fold16_const(qp[0], qp[1]), __float_as_int(__fmul_rn(dx, 0.0625f)));
             }
@@ -935,7 +946,7 @@ __device__ __forceinline__ void build_f16_image(uint8_t *img, const uint8_t *src
             shi = dp4a_ss((int)qb.y, ones, shi);
             shi = dp4a_ss((int)qb.z, ones, shi);
             shi = dp4a_ss((int)qb.w, ones, shi);
-            mma_store_consts(img + L.off_cd, b, t, static_cast<float>(-(1032 * slo + 72 * shi)), dh);
+            mma_store_consts(img + L.off_cd, b, t, mma_fold_const(slo + shi), dh);
         } else {
             mma_store_consts(img + L.off_cd, b, t, 0.0f, 0);
         }
