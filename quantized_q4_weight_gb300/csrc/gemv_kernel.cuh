@@ -94,33 +94,6 @@ __device__ __forceinline__ ItemInfo decode_item(const Params<MAXG> &P, long long
     return it;
 }
 
-// The first item whose weights start at or after position X of the launch's
-// weighted byte space (each group's bytes times its cost), for the group g
-// that holds X (g.cost_begin <= X <= the next group's cost_begin; X below the
-// launch's total).  Within an instance, slab s and its segment part p start at
-// (s * slab_bytes + p * spp * SEG_BYTES) * cost; the tail follows the slabs.
-__device__ __forceinline__ long long first_item_in_group(const Group &g, long long X)
-{
-    const long long local = X - g.cost_begin;
-    const long long inst = g.inst_bytes * g.cost, slab = g.slab_bytes * g.cost;
-    const long long e = local / inst;
-    const long long rem = local - e * inst;
-    const long long base = g.item_begin + e * g.items_per_inst;
-    if (rem == 0) return base;
-    const long long slabs_bytes = static_cast<long long>(g.nslabs) * slab;
-    if (rem < slabs_bytes) {
-        const long long s = rem / slab;
-        const long long r2 = rem - s * slab;
-        if (r2 == 0) return base + s * g.split;
-        const int spp = (g.nseg + g.split - 1) / g.split;
-        const long long pb = static_cast<long long>(spp) * SEG_BYTES * g.cost;
-        const long long p = (r2 + pb - 1) / pb;
-        if (p >= g.split) return base + (s + 1) * g.split;
-        return base + s * g.split + p;
-    }
-    if (rem == slabs_bytes) return base + static_cast<long long>(g.nslabs) * g.split;
-    return base + g.items_per_inst;
-}
 
 
 
@@ -1206,26 +1179,36 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
     __shared__ int s_nruns;   // > 0: balanced mode with this many runs
     __shared__ int s_ngroups; // groups of consecutive runs whose activations fit together
     __shared__ int s_grp[MAX_RUNS + 1];  // first run of each group, then the run count
-    __shared__ int s_g0, s_g1;           // launch groups holding the CTA's first and last byte
     __shared__ long long s_i0, s_i1;     // the CTA's item range
     __shared__ unsigned long long s_best[max_warps_for(T, MMA) * T];
 
     __shared__ ParamHead H;              // the scalar launch parameters
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    // One round of parallel parameter reads: the scalar header into shared
-    // memory, and from the host's table the group holding this CTA's first
-    // byte and the one holding the next range's first byte.
+    // One round of parallel parameter reads into shared memory: the scalar
+    // header, this CTA's item range from the host's table, and the
+    // descriptors of the launch groups from g0 (holding the range's first
+    // item) to gn (holding the next range's first item; the range ends in gn
+    // or before it).
+    const int g0 = P.cta_g0[blockIdx.x], gn = P.cta_g0[blockIdx.x + 1];
+    const int ngc = min(gn - g0 + 1, GCACHE_GROUPS);
+    Group *gcache = reinterpret_cast<Group *>(smem + P.off_gcache);
     {
         static_assert(sizeof(ParamHead) % 8 == 0, "the header is copied in 8-byte words");
+        static_assert(sizeof(Group) % 8 == 0, "group descriptors are copied in 8-byte words");
         constexpr int HW = static_cast<int>(sizeof(ParamHead) / 8);
         if (tid < HW)
             reinterpret_cast<unsigned long long *>(&H)[tid] =
                 reinterpret_cast<const unsigned long long *>(static_cast<const ParamHead *>(&P))[tid];
-        else if (tid == HW)
-            s_g0 = P.cta_g0[blockIdx.x];
-        else if (tid == HW + 1)
-            s_g1 = P.cta_g0[blockIdx.x + 1];
+        const unsigned long long *src = reinterpret_cast<const unsigned long long *>(&P.g[g0]);
+        unsigned long long *dst = reinterpret_cast<unsigned long long *>(gcache);
+        const int words = ngc * static_cast<int>(sizeof(Group) / 8);
+        for (int wd = tid; wd < words; wd += blockDim.x) dst[wd] = src[wd];
+        if (tid == blockDim.x - 1) {
+            s_i0 = P.cta_i0[blockIdx.x];
+            s_i1 = P.cta_i0[blockIdx.x + 1];
+            s_abort = 0;
+        }
     }
     __syncthreads();
     const int nw = H.nwarps, nthreads = nw * 32;
@@ -1249,46 +1232,19 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
     ring.issued = 0;
     ring.consumed = 0;
 
-    const long long b0 = H.total_cost * blockIdx.x / gridDim.x;
-    const long long b1 = H.total_cost * (blockIdx.x + 1) / gridDim.x;
-
-    // The descriptors of the groups from g0 to gn, copied to shared memory by
-    // every thread in parallel; this range's last byte lies in gn unless gn
-    // starts exactly at b1.
-    Group *gcache = reinterpret_cast<Group *>(smem + H.off_gcache);
-    const int g0 = s_g0, gn = s_g1;
-    const int ngc = min(gn - g0 + 1, GCACHE_GROUPS);
-    {
-        static_assert(sizeof(Group) % 8 == 0, "group descriptors are copied in 8-byte words");
-        const unsigned long long *src = reinterpret_cast<const unsigned long long *>(&P.g[g0]);
-        unsigned long long *dst = reinterpret_cast<unsigned long long *>(gcache);
-        const int words = ngc * static_cast<int>(sizeof(Group) / 8);
-        for (int wd = tid; wd < words; wd += nthreads) dst[wd] = src[wd];
-    }
-    __syncthreads();
-    const Group &gnd = gn - g0 < ngc ? gcache[gn - g0] : P.g[gn];
-    const int g1 = (b1 < H.total_cost && gn > g0 && gnd.cost_begin >= b1) ? gn - 1 : gn;
-
-    if (tid == 0) {
-        s_abort = 0;
-        mbar_init(xbar, 1);
-        s_i0 = b0 >= H.total_cost ? H.total_items : first_item_in_group(gcache[0], b0);
-        s_i1 = b1 >= H.total_cost ? H.total_items
-                                   : first_item_in_group(g1 - g0 < ngc ? gcache[g1 - g0] : P.g[g1], b1);
-    }
-    __syncthreads();
     const long long i0 = s_i0, i1 = s_i1;
 
     if (tid == 0) {
+        mbar_init(xbar, 1);
         // Run table for the balanced mode (thread 0 walks the CTA's runs),
         // cut into groups of consecutive runs whose activation images fit the
         // activation area together; each group's images start at offset 0.
         int nr = 0, stages = 0, xoff = 0, ng = 0;
-        bool fits = H.balanced_ok != 0 && g1 - g0 < ngc;  // a longer span has more runs than MAX_RUNS
+        bool fits = H.balanced_ok != 0 && gn - g0 < ngc;  // a longer span has more runs than MAX_RUNS
         s_grp[0] = 0;
         int gh = g0;
         for (long long ra = i0; ra < i1 && fits;) {
-            while (gh + 1 <= g1 && gcache[gh + 1 - g0].item_begin <= ra) ++gh;
+            while (gh + 1 <= gn && gcache[gh + 1 - g0].item_begin <= ra) ++gh;
             const Group &g = gcache[gh - g0];
             const int ra_inst = static_cast<int>(ra - g.item_begin) / g.items_per_inst;
             const long long rb = min(i1, g.item_begin + static_cast<long long>(ra_inst + 1) * g.items_per_inst);
@@ -1354,7 +1310,7 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
 
     if (nruns > 0) {
         // ================================================= balanced mode
-        // (the run's groups g0..g1 are all in the descriptor cache)
+        // (the run's groups g0..gn are all in the descriptor cache)
         const int ngroups = s_ngroups;
         for (int gidx = 0; gidx < ngroups; ++gidx) {
             const int rg0 = s_grp[gidx], rg1 = s_grp[gidx + 1];
@@ -1366,8 +1322,8 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
             int nseg_max = 1;
             for (int r = rg0; r < rg1; ++r) nseg_max = max(nseg_max, runs[r].nseg);
             const int nwg = max(1, min(nw, S / nseg_max));
-            const int a = warp < nwg ? S0 + static_cast<int>(static_cast<long long>(S) * warp / nwg) : S1;
-            const int b = warp < nwg ? S0 + static_cast<int>(static_cast<long long>(S) * (warp + 1) / nwg) : S1;
+            const int a = warp < nwg ? S0 + static_cast<int>(static_cast<unsigned>(S) * warp / nwg) : S1;
+            const int b = warp < nwg ? S0 + static_cast<int>(static_cast<unsigned>(S) * (warp + 1) / nwg) : S1;
             // boundary items: is stage p inside (not at the start of) an item?
             auto item_start = [&](int p) {
                 int r = rg0;

@@ -298,18 +298,48 @@ qgemv_status plan_launch(const GroupSpec *gs, int n, int T, bool ggml, bool argm
     return s;
 }
 
-// Group holding the first byte of each CTA's range (and of the range after
-// the last one), so that the kernel's prologue reads two descriptors instead
-// of searching the list.
+// The first item whose weights start at or after position X of the launch's
+// weighted byte space (each group's bytes times its cost), for the group g
+// that holds X (g.cost_begin <= X <= the next group's cost_begin; X below the
+// launch's total).  Within an instance, slab s and its segment part p start at
+// (s * slab_bytes + p * spp * SEG_BYTES) * cost; the tail follows the slabs.
+inline long long first_item_in_group(const Group &g, long long X)
+{
+    const long long local = X - g.cost_begin;
+    const long long inst = g.inst_bytes * g.cost, slab = g.slab_bytes * g.cost;
+    const long long e = local / inst;
+    const long long rem = local - e * inst;
+    const long long base = g.item_begin + e * g.items_per_inst;
+    if (rem == 0) return base;
+    const long long slabs_bytes = static_cast<long long>(g.nslabs) * slab;
+    if (rem < slabs_bytes) {
+        const long long s = rem / slab;
+        const long long r2 = rem - s * slab;
+        if (r2 == 0) return base + s * g.split;
+        const int spp = (g.nseg + g.split - 1) / g.split;
+        const long long pb = static_cast<long long>(spp) * SEG_BYTES * g.cost;
+        const long long p = (r2 + pb - 1) / pb;
+        if (p >= g.split) return base + (s + 1) * g.split;
+        return base + s * g.split + p;
+    }
+    if (rem == slabs_bytes) return base + static_cast<long long>(g.nslabs) * g.split;
+    return base + g.items_per_inst;
+}
+
+// Each CTA's range of the launch's weighted bytes, [total c / grid,
+// total (c + 1) / grid), as items: the first item of every range (and the
+// launch's item count after the last one), and the group holding that item,
+// so that the kernel's prologue reads its range and descriptors in one round.
 template <int MAXG>
 void set_cta_groups(Params<MAXG> &P, int grid)
 {
     int gi = 0;
     for (int c = 0; c <= grid; ++c) {
-        long long b = P.total_cost * c / grid;
-        if (b >= P.total_cost) b = P.total_cost - 1;
+        const long long x = P.total_cost * c / grid;
+        const long long b = x >= P.total_cost ? P.total_cost - 1 : x;
         while (gi + 1 < P.ngroups && P.g[gi + 1].cost_begin <= b) ++gi;
         P.cta_g0[c] = static_cast<unsigned char>(gi);
+        P.cta_i0[c] = static_cast<int>(x >= P.total_cost ? P.total_items : first_item_in_group(P.g[gi], x));
     }
 }
 

@@ -80,12 +80,13 @@ struct ParamHead {
 template <int MAXG>
 struct Params : ParamHead {
     Group g[MAXG];
-    unsigned char cta_g0[MAX_GRID + 1];  // group holding the first byte of CTA c's range
+    unsigned char cta_g0[MAX_GRID + 1];  // group holding the first item of CTA c's range
+    int cta_i0[MAX_GRID + 1];            // first item of CTA c's range (cta_i0[grid]: the launch's items)
 };
 
 constexpr int MAXG_SMALL = 4;
 constexpr int GCACHE_GROUPS = 34;  // launch groups a CTA caches in shared memory (MAX_RUNS + 2)
-constexpr int MAXG_SEQ = 224;  // keeps the parameter block under the 32 KB kernel-parameter limit
+constexpr int MAXG_SEQ = 200;  // keeps the parameter block under the 32 KB kernel-parameter limit
 static_assert(MAXG_SEQ <= 256, "CTA start groups are stored as bytes");
 static_assert(sizeof(Params<MAXG_SEQ>) <= 32764, "kernel parameters are limited to 32764 bytes");
 
