@@ -209,7 +209,7 @@ typedef struct {
 size_t qgemv_seq_workspace_bytes(const qgemv_seq_item *items, int n, int T);
 
 /* Run n GEMVs (host array `items`, read during the call only) in list order
- * in one persistent launch per 224 items (minfer README M15: one persistent
+ * in one persistent launch per 200 items (minfer README M15: one persistent
  * kernel streams every matrix of the token and keeps DRAM busy).  Every
  * item's inputs must be ready when the call is enqueued: no item may read
  * another item's y.  All items share T and the layout. */
@@ -231,7 +231,7 @@ size_t qgemv_seq_f32_workspace_bytes(const qgemv_seq_f32_item *items, int n, int
 /* qgemv_q4_0_seq with fp32 inputs x[T][K] (4-byte aligned): the GEMV kernel
  * quantises each item's activations (Q8_0, the same bytes as
  * qgemv_quantize_q8_0) while it builds its shared-memory copy of them, so a
- * sequence is one launch per 224 items, streaming weights before it reads x
+ * sequence is one launch per 200 items, streaming weights before it reads x
  * (minfer README M15: the activation is quantised once, then the weights
  * stream).  The workspace is the sequence's own (no activation area). */
 qgemv_status qgemv_q4_0_seq_f32(const qgemv_seq_f32_item *items, int n, qgemv_wlayout layout, int T,

@@ -555,7 +555,7 @@ def test_gather_f32_matches_quantised_gather(orc):
 
 @pytest.mark.parametrize("f32", [False, True])
 def test_seq_longer_than_one_launch(orc, f32):
-    """More items than one launch takes (224): the library splits the list;
+    """More items than one launch takes (200): the library splits the list;
     every item equals its single call, bit for bit."""
     n, T = 230, 2
     shapes = [(16 + (i % 5), 32 * (1 + i % 4)) for i in range(n)]
