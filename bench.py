@@ -633,10 +633,11 @@ def measure(args, wl: Workload, dev, world, rank):
     clocks = ClockSampler(torch.cuda.current_device())
     if world > 1:
         torch.distributed.barrier()
-    l2_flush.fill_(1)
-    torch.cuda.synchronize()
     clocks.start()
     time.sleep(0.3)
+    # the flush is the last work before the timed steps, on the same stream:
+    # no idle gap (and no clock ramp) between it and the first timed step
+    l2_flush.fill_(1)
     t_start.record(stream)
     if g_steps is not None:
         g_steps.replay()

@@ -844,10 +844,74 @@ __device__ __forceinline__ void q8_block_thread(const float *x, bool vec, uint4 
 }
 
 // One run's int8 activation image quantised in the kernel from fp32
-// activations x[T][K] in global memory: the bytes a copy of the planar Q8_0
-// activations would bring (codes at row t * xstride, fp16 scales at off_d).
+// activations x[T][K] in global memory, with its per-block constants, in one
+// pass, for images of at most nthreads / 8 blocks: the bytes a copy of the
+// planar Q8_0 activations followed by build_fold_constants would leave (codes
+// at row t * xstride -- rewritten as q xor 0x80 on the tensor-core path --
+// fp16 scales at off_d, constants at off_cd).  Eight consecutive threads take
+// one block, four values each; the block maximum and the code sum are
+// combined with shuffles inside the eight-lane group (the maximum is exact in
+// any order, so every byte equals the standalone quantiser's).  nthreads is a
+// multiple of 32, so each group lies in one warp.
 template <int T, bool MMA>
-__device__ __forceinline__ void quantize_image(uint8_t *img, const float *x, int K, int tid, int nthreads)
+__device__ __forceinline__ void quantize_image_small(uint8_t *img, const float *x, int K, int tid, int nthreads)
+{
+    const XqLayout L = xq_layout(T, K, MMA);
+    const int nb = K / QK;
+    const bool act = tid < T * nb * 8;  // eight-lane groups are wholly in or out
+    const int blk = (act ? tid : 0) >> 3, sub = tid & 7;
+    const int t = blk / nb, b = blk - t * nb;
+    const float *xp = x + static_cast<long long>(t) * K + b * QK + 4 * sub;
+    float4 v = make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+    if (act) {
+        if ((reinterpret_cast<uintptr_t>(x) & 15) == 0) {
+            v = __ldcg(reinterpret_cast<const float4 *>(xp));
+        } else {
+            v.x = __ldcg(xp);
+            v.y = __ldcg(xp + 1);
+            v.z = __ldcg(xp + 2);
+            v.w = __ldcg(xp + 3);
+        }
+    }
+    float amax = fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w)));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 1));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 2));
+    amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, 4));
+    float d, id;
+    q8_scale(amax, d, id);
+    const int c0 = q8_code(v.x, id), c1 = q8_code(v.y, id), c2 = q8_code(v.z, id), c3 = q8_code(v.w, id);
+    int sq = c0 + c1 + c2 + c3;
+    sq += __shfl_xor_sync(0xFFFFFFFFu, sq, 1);
+    sq += __shfl_xor_sync(0xFFFFFFFFu, sq, 2);
+    sq += __shfl_xor_sync(0xFFFFFFFFu, sq, 4);
+    if (act) {
+        unsigned w = (static_cast<unsigned>(c0) & 0xFFu) | ((static_cast<unsigned>(c1) & 0xFFu) << 8) |
+                     ((static_cast<unsigned>(c2) & 0xFFu) << 16) | ((static_cast<unsigned>(c3) & 0xFFu) << 24);
+        if (MMA) w ^= 0x80808080u;  // the MMA operands read q xor 0x80
+        *reinterpret_cast<unsigned *>(img + t * L.xstride + b * QK + 4 * sub) = w;
+        if (sub == 0) {
+            const unsigned short dh = q8_half(d);
+            reinterpret_cast<unsigned short *>(img + L.off_d)[t * nb + b] = dh;
+            if constexpr (MMA)
+                mma_store_consts(img + L.off_cd, b, t, mma_fold_const(sq), dh);
+            else
+                reinterpret_cast<int2 *>(img + L.off_cd)[b * L.cdw + t] =
+                    make_int2(MAGIC_I - 128 * sq, __float_as_int(__fmul_rn(h2f(dh), 0.0625f)));
+        }
+    }
+    if constexpr (MMA && T < 8)  // token columns past T: zero constants
+        for (int i = tid; i < (8 - T) * nb; i += nthreads) {
+            const int bb = i / (8 - T), tt = T + (i - bb * (8 - T));
+            mma_store_consts(img + L.off_cd, bb, tt, 0.0f, 0);
+        }
+}
+
+// The codes and scales of one run's int8 activation image quantised in the
+// kernel from fp32 activations x[T][K] in global memory, one block per
+// thread: the bytes a copy of the planar Q8_0 activations would bring (codes
+// at row t * xstride, fp16 scales at off_d); build_fold_constants follows.
+template <int T, bool MMA>
+__device__ __forceinline__ void quantize_image_codes(uint8_t *img, const float *x, int K, int tid, int nthreads)
 {
     const XqLayout L = xq_layout(T, K, MMA);
     const int nb = K / QK;
@@ -862,6 +926,22 @@ __device__ __forceinline__ void quantize_image(uint8_t *img, const float *x, int
         dst[0] = qa;
         dst[1] = qb;
         xd[t * nb + b] = dh;
+    }
+}
+
+// One run's int8 activation image (codes, scales and constants) quantised
+// in the kernel from fp32 activations: small images in one pass of eight
+// threads per block, larger ones one block per thread and then the
+// constants.  The bytes are the same either way.
+template <int T, bool MMA>
+__device__ __forceinline__ void quantize_image(uint8_t *img, const float *x, int K, int tid, int nthreads)
+{
+    if (T * (K / QK) * 8 <= nthreads) {
+        quantize_image_small<T, MMA>(img, x, K, tid, nthreads);
+    } else {
+        quantize_image_codes<T, MMA>(img, x, K, tid, nthreads);
+        __syncthreads();
+        build_fold_constants<T, MMA>(img, K, tid, nthreads);
     }
 }
 
@@ -963,6 +1043,8 @@ __host__ __device__ constexpr int max_warps_for(int T, bool mma) { return (mma |
 // whole slabs, its boundary tail.
 
 constexpr int MAX_RUNS = 32;
+constexpr long long WARM_L2_BYTES = 262144;  // L2 warm-up per CTA (bytes)
+constexpr int WARM_L2_PIECE = 16384;
 static_assert(GCACHE_GROUPS >= MAX_RUNS, "a balanced CTA's groups must fit the descriptor cache");
 
 struct RunInfo {
@@ -1190,7 +1272,10 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
     // descriptors of the launch groups from g0 (holding the range's first
     // item) to gn (holding the next range's first item; the range ends in gn
     // or before it).
-    const int g0 = P.cta_g0[blockIdx.x], gn = P.cta_g0[blockIdx.x + 1];
+    // (one-group launches skip the table: their descriptor loads then start
+    // in the same round as the header's)
+    const bool one = P.ngroups == 1;
+    const int g0 = one ? 0 : P.cta_g0[blockIdx.x], gn = one ? 0 : P.cta_g0[blockIdx.x + 1];
     const int ngc = min(gn - g0 + 1, GCACHE_GROUPS);
     Group *gcache = reinterpret_cast<Group *>(smem + P.off_gcache);
     {
@@ -1211,6 +1296,21 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
         }
     }
     __syncthreads();
+    // Warm-up: warp 0 asks L2 for the first bytes of this CTA's weights (in
+    // its first group, packed slabs only) in 16 KB pieces, so that HBM works
+    // while the prologue and the activations are prepared and the first
+    // stage copies find their bytes in L2.  Bounded by the group's slabs.
+    if (warp == 0 && !H.ggml) {
+        const Group &g = gcache[0];
+        const long long li0 = s_i0 - g.item_begin;
+        const long long li1 = gn == g0 ? s_i1 - g.item_begin : static_cast<long long>(g.items_per_inst) * g.count;
+        if (g.split == 1 && g.count == 1 && li0 < g.nslabs && li1 > li0) {
+            const long long lo = li0 * g.slab_bytes, hi = (li1 < g.nslabs ? li1 : g.nslabs) * g.slab_bytes;
+            const long long end = hi - lo > WARM_L2_BYTES ? lo + WARM_L2_BYTES : hi;
+            for (long long c = lo + static_cast<long long>(lane) * WARM_L2_PIECE; c < end; c += 32ll * WARM_L2_PIECE)
+                bulk_prefetch_l2(g.W + c, static_cast<unsigned>(min(static_cast<long long>(WARM_L2_PIECE), end - c)));
+        }
+    }
     const int nw = H.nwarps, nthreads = nw * 32;
     const int r8 = lane >> 2, j = lane & 3;
     const int D = H.ring_depth;
@@ -1385,28 +1485,18 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
             const bool xok = mbar_wait_bounded(xbar, xphase, abort_flag, H.status, WAIT_LIMIT_NS);
             xphase ^= 1u;
             if (xok && tid == 0) x_unconfirmed = false;
-            if (f32in) {  // int8 images quantised here from the fp32 activations
-                if (xok)
-                    for (int r = rg0; r < rg1; ++r) {
-                        const RunInfo &R = runs[r];
-                        if (MMA && xq_layout(T, R.K, MMA).f16) continue;
-                        const Group &g = gcache[R.gi - g0];
-                        quantize_image<T, MMA>(smem + R.xq_off,
-                                               reinterpret_cast<const float *>(g.xq + static_cast<long long>(R.e) * g.xq_stride),
-                                               R.K, tid, nthreads);
-                    }
-                __syncthreads();
-            }
             if (xok)
                 for (int r = rg0; r < rg1; ++r) {
                     const RunInfo &R = runs[r];
+                    const Group &g = gcache[R.gi - g0];
+                    const uint8_t *src = g.xq + static_cast<long long>(R.e) * g.xq_stride;
                     if (MMA && xq_layout(T, R.K, MMA).f16) {
-                        const Group &g = gcache[R.gi - g0];
-                        const uint8_t *src = g.xq + static_cast<long long>(R.e) * g.xq_stride;
                         if (f32in)
                             build_f16_image<T, true>(smem + R.xq_off, src, R.K, tid, nthreads);
                         else
                             build_f16_image<T, false>(smem + R.xq_off, src, R.K, tid, nthreads);
+                    } else if (f32in) {  // int8 image quantised here from the fp32 activations
+                        quantize_image<T, MMA>(smem + R.xq_off, reinterpret_cast<const float *>(src), R.K, tid, nthreads);
                     } else {
                         build_fold_constants<T, MMA>(smem + R.xq_off, R.K, tid, nthreads);
                     }
@@ -1539,17 +1629,14 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
             if (xok) x_unconfirmed = false;
             xphase ^= 1u;
             const uint8_t *xsrc = g.xq + static_cast<long long>(e_run) * g.xq_stride;
-            if (f32in) {  // int8 image quantised here from the fp32 activations
-                if (xok && !(MMA && L.f16))
-                    quantize_image<T, MMA>(smem, reinterpret_cast<const float *>(xsrc), K, tid, nthreads);
-                __syncthreads();
-            }
             if (xok) {
                 if (MMA && L.f16) {
                     if (f32in)
                         build_f16_image<T, true>(smem, xsrc, K, tid, nthreads);
                     else
                         build_f16_image<T, false>(smem, xsrc, K, tid, nthreads);
+                } else if (f32in) {  // int8 image quantised here from the fp32 activations
+                    quantize_image<T, MMA>(smem, reinterpret_cast<const float *>(xsrc), K, tid, nthreads);
                 } else {
                     build_fold_constants<T, MMA>(smem, K, tid, nthreads);
                 }

@@ -208,7 +208,7 @@ qgemv_status make_plan(const GroupSpec *gs, int n, int T, bool ggml, bool argmax
     P.off_cd = 0;
     const long long tables = align_up(static_cast<long long>(MAX_RUNS) * sizeof(RunInfo), 128) +
                              align_up(static_cast<long long>(NWARPS_MAX) * T * 16 * 4, 128) + 128 +
-                             align_up(static_cast<long long>(GCACHE_GROUPS) * sizeof(Group), 128);
+                             align_up(static_cast<long long>(std::min(GCACHE_GROUPS, n)) * sizeof(Group), 128);
     P.balanced_ok = 1;
     for (int i = 0; i < n; ++i)
         if (P.g[i].split > 1) P.balanced_ok = 0;
