@@ -79,6 +79,12 @@ class Oracle:
         L.orc_argmax_f32.restype = ctypes.c_int64
         L.orc_argmax_f64.argtypes = [_f64p, ctypes.c_int64]
         L.orc_argmax_f64.restype = ctypes.c_int64
+        L.orc_top2_f32.argtypes = [_f32p, ctypes.c_int64, _i64p]
+        L.orc_top2_f32.restype = None
+        L.orc_top2_f64.argtypes = [_f64p, ctypes.c_int64, _i64p]
+        L.orc_top2_f64.restype = None
+        L.orc_verify_commit.argtypes = [_i64p, _i64p, ctypes.c_int]
+        L.orc_verify_commit.restype = ctypes.c_int
         L.orc_num_threads.restype = ctypes.c_int
         L.orc_set_threads.argtypes = [ctypes.c_int]
         L.orc_set_threads.restype = ctypes.c_int
@@ -154,6 +160,27 @@ class Oracle:
     def argmax_f64(self, y: np.ndarray) -> int:
         y = np.ascontiguousarray(y, np.float64)
         return int(self.L.orc_argmax_f64(_p(y, _f64p), y.size))
+
+    def top2_f32(self, y: np.ndarray):
+        """(best, second) row indices of fp32 y (second = -1 when y has one row)."""
+        y = np.ascontiguousarray(y, np.float32)
+        out = np.empty(2, np.int64)
+        self.L.orc_top2_f32(_p(y, _f32p), y.size, out.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)))
+        return int(out[0]), int(out[1])
+
+    def top2_f64(self, y: np.ndarray):
+        y = np.ascontiguousarray(y, np.float64)
+        out = np.empty(2, np.int64)
+        self.L.orc_top2_f64(_p(y, _f64p), y.size, out.ctypes.data_as(ctypes.POINTER(ctypes.c_int64)))
+        return int(out[0]), int(out[1])
+
+    def verify_commit(self, tokens, pred) -> int:
+        """Committed predictions of one verify step (1..T)."""
+        tk = np.ascontiguousarray(tokens, np.int64)
+        pr = np.ascontiguousarray(pred, np.int64)
+        assert tk.size == pr.size >= 1
+        P = ctypes.POINTER(ctypes.c_int64)
+        return int(self.L.orc_verify_commit(tk.ctypes.data_as(P), pr.ctypes.data_as(P), tk.size))
 
     def num_threads(self) -> int:
         return int(self.L.orc_num_threads())

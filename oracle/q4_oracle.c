@@ -34,6 +34,7 @@
  *  - x * (1/d) is one fp32 multiply, rounded to nearest even.
  *  - amax = 0 gives d = 0, 1/d := 0, all q = 0.
  *  - argmax: lowest index among equal maxima, equality by IEEE == (so -0 == +0).
+ *  - top-2: the second is the argmax of the rows other than the first.
  *
  * ORC_MUTANT (compile-time, default 0) plants one known mistake; the test
  * suite builds each mutant and checks that its pins reject it.
@@ -307,6 +308,55 @@ int64_t orc_argmax_f64(const double *y, int64_t N)
         if (y[i] > y[best])
             best = i;
     return best;
+}
+
+/* ------------------------------------------------ top-2 and the commit rule */
+
+/* The two best rows of y: idx[0] is the argmax (lowest index among equal
+ * maxima); idx[1] is the argmax of the remaining rows, with the same rules
+ * (minfer README M19 keeps the top-2 margin of every step).  idx[1] = -1
+ * when N < 2. */
+void orc_top2_f32(const float *y, int64_t N, int64_t idx[2])
+{
+    idx[0] = orc_argmax_f32(y, N);
+    idx[1] = -1;
+    for (int64_t i = 0; i < N; i++) {
+        if (i == idx[0]) continue;
+#if ORC_MUTANT == 11
+        if (idx[1] < 0 || y[i] >= y[idx[1]])    /* MUTANT: second ties to highest index */
+#else
+        if (idx[1] < 0 || y[i] > y[idx[1]])
+#endif
+            idx[1] = i;
+    }
+}
+
+void orc_top2_f64(const double *y, int64_t N, int64_t idx[2])
+{
+    idx[0] = orc_argmax_f64(y, N);
+    idx[1] = -1;
+    for (int64_t i = 0; i < N; i++) {
+        if (i == idx[0]) continue;
+        if (idx[1] < 0 || y[i] > y[idx[1]]) idx[1] = i;
+    }
+}
+
+/* The lossless verify rule (minfer README M17): a verify step runs the
+ * current token and its drafts, tokens[0] = current, tokens[1..T-1] =
+ * drafts; pred[t] is the greedy prediction after tokens[0..t].  The step
+ * commits pred[0], then pred[t] for each t >= 1 while every draft so far
+ * equalled the prediction before it (tokens[t] == pred[t-1]), up to and
+ * including the first prediction that disagrees with its draft.  Returns
+ * the number of committed predictions, 1..T. */
+int orc_verify_commit(const int64_t *tokens, const int64_t *pred, int T)
+{
+    int n = 1;
+#if ORC_MUTANT == 12
+    while (n < T && tokens[n] == pred[n]) n++;  /* MUTANT: draft compared with its own prediction */
+#else
+    while (n < T && tokens[n] == pred[n - 1]) n++;
+#endif
+    return n;
 }
 
 /* ------------------------------------------------------------------ misc */

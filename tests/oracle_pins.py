@@ -291,4 +291,77 @@ def pin_argmax_rules(o):
     assert o.argmax_f64(np.array([2.0, 5.0, 5.0], np.float64)) == 1
 
 
+# ------------------------------------------------------------------ top-2
+
+def _top2_by_sort(y):
+    """The first two rows in (larger value, lower index) order, by a library
+    sort; Python compares -0.0 == 0.0, so the tie rule is IEEE equality."""
+    order = sorted(range(len(y)), key=lambda i: (-float(y[i]), i))
+    return order[0], (order[1] if len(order) > 1 else -1)
+
+
+def pin_top2_rules(o):
+    assert o.top2_f32(np.array([1, 3, 3, 2], np.float32)) == (1, 2)
+    assert o.top2_f32(np.array([4, 1, 3, 3], np.float32)) == (0, 2)
+    assert o.top2_f32(np.array([-0.0, 0.0, -1.0], np.float32)) == (0, 1)
+    assert o.top2_f32(np.array([0.0, -1.0, -0.0], np.float32)) == (0, 2)
+    assert o.top2_f32(np.array([2.5], np.float32)) == (0, -1)
+    assert o.top2_f32(np.zeros(9, np.float32)) == (0, 1)
+    assert o.top2_f32(np.array([-5.0, -2.0, -9.0, -2.0], np.float32)) == (1, 3)
+    assert o.top2_f64(np.array([2.0, 5.0, 5.0, 7.0], np.float64)) == (3, 1)
+
+
+def pin_top2_against_sort(o):
+    rng = np.random.default_rng(62)
+    for n in (2, 3, 17, 1000):
+        for _ in range(20):
+            # few distinct values, so ties are frequent; some zeros of both signs
+            y = rng.integers(-3, 4, n).astype(np.float32)
+            y[rng.random(n) < 0.2] = -0.0
+            assert o.top2_f32(y) == _top2_by_sort(y)
+            y64 = y.astype(np.float64) * 0.5
+            assert o.top2_f64(y64) == _top2_by_sort(y64)
+
+
+# ------------------------------------------------------------------ verify-commit
+
+def pin_verify_commit_hand_cases(o):
+    # tokens = [current, draft1, draft2, draft3]; pred[t] follows tokens[0..t]
+    pred = [7, 9, 11, 4]
+    assert o.verify_commit([5, 7, 9, 11], pred) == 4    # every draft right: all four commit
+    assert o.verify_commit([5, 8, 9, 11], pred) == 1    # first draft wrong: pred[0] only
+    assert o.verify_commit([5, 7, 10, 11], pred) == 2   # second wrong: pred[0], pred[1]
+    assert o.verify_commit([5, 7, 0, 11], pred) == 2    # a later match after a miss does not count
+    assert o.verify_commit([5], [7]) == 1               # plain decode step
+
+
+def pin_verify_commit_is_lossless(o):
+    """The committed tokens are exactly what plain greedy decoding emits, and
+    as many as the drafts allow (a toy deterministic model stands in for the
+    lm_head: next token = a hash of the whole prefix)."""
+    def nxt(prefix):
+        h = 1469598103934665603
+        for tok in prefix:
+            h = ((h ^ tok) * 1099511628211) % (1 << 61)
+        return h % 13
+
+    rng = np.random.default_rng(63)
+    for _ in range(300):
+        prefix = [int(v) for v in rng.integers(0, 13, rng.integers(1, 6))]
+        greedy = []
+        for _ in range(8):
+            greedy.append(nxt(prefix + greedy))
+        T = int(rng.integers(1, 9))
+        # drafts: the greedy continuation with some tokens replaced
+        drafts = [g if rng.random() < 0.7 else int(rng.integers(0, 13)) for g in greedy[:T - 1]]
+        tokens = [prefix[-1]] + drafts
+        pred = [nxt(prefix + drafts[:t]) for t in range(T)]
+        n = o.verify_commit(tokens, pred)
+        assert pred[:n] == greedy[:n]
+        right = 0
+        while right < T - 1 and drafts[right] == greedy[right]:
+            right += 1
+        assert n == right + 1
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

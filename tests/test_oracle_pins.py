@@ -21,8 +21,9 @@ def test_pin(orc, pin):
 #  4 inverse scale from the fp16 d, 5 activation scale dropped,
 #  6 wrong activation block index, 7 signed instead of absolute max,
 #  8 truncating fp16 encode, 9 argmax ties to the highest index,
-#  10 transposed output.
-MUTANTS = list(range(1, 11))
+#  10 transposed output, 11 top-2 second ties to the highest index,
+#  12 verify rule comparing a draft with its own prediction.
+MUTANTS = list(range(1, 13))
 
 
 @pytest.fixture(scope="module")
