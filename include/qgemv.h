@@ -174,6 +174,42 @@ qgemv_status qgemv_q4_0_argmax_f32(const void *W, qgemv_wlayout layout, const fl
                                    int64_t *idx, int64_t N, int64_t K, int T, void *ws, size_t ws_bytes,
                                    qgemv_stream_t stream);
 
+/* lm_head GEMV with the two best rows per token (minfer README M19: the
+ * step keeps each token's top-2 margin; top-2 merging is associative, so the
+ * result does not depend on the merge order).  idx2 (int64 [T][2], device)
+ * and val2 (fp32 [T][2], device) receive, per token t:
+ *   idx2[t][0], val2[t][0]: the row qgemv_q4_0_argmax returns, and its output;
+ *   idx2[t][1], val2[t][1]: the argmax of the other rows (lowest index among
+ *     equal outputs, -0 == +0), and its output;
+ * so val2[t][0] - val2[t][1] >= 0 is the token's margin.  Values are y's
+ * exactly, except that -0 is returned as +0.  With N == 1 the second row is
+ * -1 and its value -infinity.  y_or_null as in qgemv_q4_0_argmax.  idx2 and
+ * val2 must not overlap each other, y or the workspace.  Workspace: as
+ * qgemv_q4_0_argmax (qgemv_workspace_bytes). */
+qgemv_status qgemv_q4_0_top2(const void *W, qgemv_wlayout layout, const void *xq,
+                             float *y_or_null, int64_t *idx2, float *val2, int64_t N, int64_t K,
+                             int T, void *ws, size_t ws_bytes, qgemv_stream_t stream);
+
+/* qgemv_q4_0_top2 with fp32 input x[T][K] (4-byte aligned), quantised inside
+ * the kernel: one launch for the lm_head of a verify step. */
+qgemv_status qgemv_q4_0_top2_f32(const void *W, qgemv_wlayout layout, const float *x,
+                                 float *y_or_null, int64_t *idx2, float *val2, int64_t N,
+                                 int64_t K, int T, void *ws, size_t ws_bytes,
+                                 qgemv_stream_t stream);
+
+/* The lossless verify rule of speculative greedy decoding (minfer README
+ * M17: a verify step runs [current, draft_1..draft_K] and commits up to and
+ * including the first prediction that disagrees with its draft).
+ * tokens (int64 [T], device): tokens[0] is the step's current token,
+ * tokens[1..T-1] its drafts; pred (int64, device): pred[t * pred_stride]
+ * is the greedy prediction after tokens[0..t] (pred_stride 1 for idx from
+ * qgemv_q4_0_argmax, 2 for the first rows of qgemv_q4_0_top2's idx2).  Writes to *n_commit (int32, device) the number of committed
+ * predictions, 1 + the length of the leading run of t with
+ * tokens[t + 1] == pred[t]; the committed tokens are pred[0..n-1].
+ * 1 <= T <= 32.  One single-warp launch on `stream`; no workspace. */
+qgemv_status qgemv_verify_commit(const int64_t *tokens, const int64_t *pred, int pred_stride,
+                                 int T, int32_t *n_commit, qgemv_stream_t stream);
+
 /* Allocation-free variant of qgemv_q4_0_argmax (the paper has no
  * counterpart; this is a convenience of this library).  For callers that
  * cannot allocate device memory where they run the lm_head -- a plugin that

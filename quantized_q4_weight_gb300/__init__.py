@@ -70,6 +70,9 @@ _SIGS = {
     "qgemv_q4_0_argmax": ([_VP, _I32, _VP, _VP, _VP, _I64, _I64, _I32, _VP, _SZ, _VP], _I32),
     "qgemv_q4_0_argmax_f32": ([_VP, _I32, _VP, _VP, _VP, _I64, _I64, _I32, _VP, _SZ, _VP], _I32),
     "qgemv_q4_0_argmax_noalloc": ([_VP, _I32, _VP, _VP, _VP, _I64, _I64, _I32, _VP], _I32),
+    "qgemv_q4_0_top2": ([_VP, _I32, _VP, _VP, _VP, _VP, _I64, _I64, _I32, _VP, _SZ, _VP], _I32),
+    "qgemv_q4_0_top2_f32": ([_VP, _I32, _VP, _VP, _VP, _VP, _I64, _I64, _I32, _VP, _SZ, _VP], _I32),
+    "qgemv_verify_commit": ([_VP, _VP, _I32, _I32, _VP, _VP], _I32),
     "qgemv_seq_workspace_bytes": ([ctypes.POINTER(SeqItem), _I32, _I32], _SZ),
     "qgemv_q4_0_seq": ([ctypes.POINTER(SeqItem), _I32, _I32, _I32, _VP, _SZ, _VP], _I32),
     "qgemv_seq_f32_workspace_bytes": ([ctypes.POINTER(SeqF32Item), _I32, _I32], _SZ),
@@ -191,6 +194,37 @@ def gemv_argmax_f32(W, layout: int, x, N: int, K: int, T: int, ws, y=None, idx=N
     _check(lib().qgemv_q4_0_argmax_f32(_ptr(W), layout, _ptr(x), _ptr(y), _ptr(idx), N, K, T, _ptr(ws), ws.numel(),
                                        _stream(stream)), "qgemv_q4_0_argmax_f32")
     return idx
+
+
+def gemv_top2(W, layout: int, xq, N: int, K: int, T: int, ws, y=None, idx2=None, val2=None, stream=None):
+    """The two best rows per token and their outputs: (idx2 int64 [T][2], val2 fp32 [T][2])."""
+    idx2 = idx2 if idx2 is not None else torch.empty((T, 2), dtype=torch.int64, device=W.device)
+    val2 = val2 if val2 is not None else torch.empty((T, 2), dtype=torch.float32, device=W.device)
+    _check(lib().qgemv_q4_0_top2(_ptr(W), layout, _ptr(xq), _ptr(y), _ptr(idx2), _ptr(val2), N, K, T, _ptr(ws),
+                                 ws.numel(), _stream(stream)), "qgemv_q4_0_top2")
+    return idx2, val2
+
+
+def gemv_top2_f32(W, layout: int, x, N: int, K: int, T: int, ws, y=None, idx2=None, val2=None, stream=None):
+    """gemv_top2 for fp32 x[T][K] (quantised inside the kernel)."""
+    idx2 = idx2 if idx2 is not None else torch.empty((T, 2), dtype=torch.int64, device=W.device)
+    val2 = val2 if val2 is not None else torch.empty((T, 2), dtype=torch.float32, device=W.device)
+    _check(lib().qgemv_q4_0_top2_f32(_ptr(W), layout, _ptr(x), _ptr(y), _ptr(idx2), _ptr(val2), N, K, T, _ptr(ws),
+                                     ws.numel(), _stream(stream)), "qgemv_q4_0_top2_f32")
+    return idx2, val2
+
+
+def verify_commit(tokens, pred, n_commit=None, stream=None):
+    """Committed predictions of one verify step (int32 device scalar): tokens[0]
+    is the current token, tokens[1:] the drafts, pred[t] the prediction after
+    tokens[:t+1] (int64 device tensors; pred may be a strided column such as
+    idx2[:, 0] of gemv_top2)."""
+    T = tokens.numel()
+    assert pred.dim() == 1 and pred.numel() == T and tokens.is_contiguous()
+    n_commit = n_commit if n_commit is not None else torch.empty(1, dtype=torch.int32, device=tokens.device)
+    _check(lib().qgemv_verify_commit(_ptr(tokens), ctypes.c_void_p(pred.data_ptr()), pred.stride(0), T,
+                                     _ptr(n_commit), _stream(stream)), "qgemv_verify_commit")
+    return n_commit
 
 
 def seq_items(entries) -> ctypes.Array:

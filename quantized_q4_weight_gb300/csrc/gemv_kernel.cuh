@@ -1211,26 +1211,73 @@ struct Ring {
     }
 };
 
+// Top-2 of distinct 64-bit keys (0 = none): push one key, or merge another
+// pair.  Merging is associative and exact, so every order of merges gives
+// the same pair.
+__device__ __forceinline__ void top2_push(unsigned long long &b1, unsigned long long &b2, unsigned long long key)
+{
+    const unsigned long long lo = b1 < key ? b1 : key;
+    b1 = b1 < key ? key : b1;
+    b2 = b2 < lo ? lo : b2;
+}
+__device__ __forceinline__ void top2_merge(unsigned long long &b1, unsigned long long &b2, unsigned long long c1,
+                                           unsigned long long c2)
+{
+    top2_push(b1, b2, c1);
+    b2 = b2 < c2 ? c2 : b2;
+}
+__device__ __forceinline__ void top2_warp(unsigned long long &b1, unsigned long long &b2)
+{
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) {
+        const unsigned long long o1 = __shfl_xor_sync(0xFFFFFFFFu, b1, off);
+        const unsigned long long o2 = __shfl_xor_sync(0xFFFFFFFFu, b2, off);
+        top2_merge(b1, b2, o1, o2);
+    }
+}
+
+// Row and value of a key (argmax_key's inverse; -0 came in as +0).
+__device__ __forceinline__ long long key_row(unsigned long long k)
+{
+    return k ? static_cast<long long>(0xFFFFFFFFull - (k & 0xFFFFFFFFull)) : -1ll;
+}
+__device__ __forceinline__ float key_value(unsigned long long k)
+{
+    if (!k) return -__int_as_float(0x7F800000);
+    const unsigned u = static_cast<unsigned>(k >> 32);
+    return __uint_as_float((u & 0x80000000u) ? (u & 0x7FFFFFFFu) : ~u);
+}
+
+// A lane's two best keys for the tokens it tracks.  Lane (r8, j) tracks the
+// tokens t with jt(t) == j: on the tensor-core path the tokens it computes,
+// 2j and 2j + 1; on the dp4a path, where the four lanes of a row pair hold
+// the same outputs, t = j, j + 4.  Slot indices are compile-time constants.
+template <int T, bool MMA>
+struct Top2Lane {
+    static constexpr int S = MMA ? 2 : (T + 3) / 4;
+    __host__ __device__ static constexpr int jt(int t) { return MMA ? t >> 1 : t & 3; }
+    __host__ __device__ static constexpr int slot(int t) { return MMA ? t & 1 : t >> 2; }
+    __host__ __device__ static constexpr int token(int sl, int j) { return MMA ? 2 * j + sl : 4 * sl + j; }
+    unsigned long long b1[S], b2[S];
+};
+
 // Write this lane's finished outputs (rows below `rows`) and fold them into
-// the argmax keys.
+// the top-2 keys of their tokens.
 template <int T, bool MMA, bool ARGMAX>
 __device__ __forceinline__ void store_outputs(float *ye, int N, int row0, int rows, int r8, int j,
-                                              const float (&yv)[LaneOut<T, MMA>::N], unsigned long long (&best)[T])
+                                              const float (&yv)[LaneOut<T, MMA>::N], Top2Lane<T, MMA> &st)
 {
     using LO = LaneOut<T, MMA>;
+    using TL2 = Top2Lane<T, MMA>;
 #pragma unroll
     for (int k = 0; k < LO::N; ++k) {
         const int lr = LO::row(k, r8), t = LO::tok(k, j);
-        if (LO::owner(k, j) && lr < rows) {
-            const int row = row0 + lr;
-            if (ye != nullptr) ye[static_cast<long long>(t) * N + row] = yv[k];
-            if (ARGMAX) {
-                const unsigned long long key = argmax_key(yv[k], static_cast<unsigned>(row));
-#pragma unroll
-                for (int u = 0; u < T; ++u)  // static indices: no local memory
-                    if (u == t) best[u] = max(best[u], key);
-            }
-        }
+        if (lr >= rows) continue;
+        if (LO::owner(k, j) && ye != nullptr) ye[static_cast<long long>(t) * N + row0 + lr] = yv[k];
+        // static slot: (k & 1) on the tensor-core path, (k % T) / 4 on dp4a
+        const int sl = MMA ? (k & 1) : ((k % T) >> 2);
+        if (ARGMAX && t < T && (MMA || TL2::jt(k % T) == j))
+            top2_push(st.b1[sl], st.b2[sl], argmax_key(yv[k], static_cast<unsigned>(row0 + lr)));
     }
 }
 
@@ -1262,7 +1309,7 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
     __shared__ int s_ngroups; // groups of consecutive runs whose activations fit together
     __shared__ int s_grp[MAX_RUNS + 1];  // first run of each group, then the run count
     __shared__ long long s_i0, s_i1;     // the CTA's item range
-    __shared__ unsigned long long s_best[max_warps_for(T, MMA) * T];
+    __shared__ unsigned long long s_best[ARGMAX ? max_warps_for(T, MMA) * T * 2 : 1];  // [warp][t][2]
 
     __shared__ ParamHead H;              // the scalar launch parameters
 
@@ -1402,9 +1449,9 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
     const uint64_t pol_x = l2_policy_evict_last();
     const int nruns = s_nruns;
 
-    unsigned long long best[T];
+    Top2Lane<T, MMA> st;  // the lane's two best keys per token (argmax launches)
 #pragma unroll
-    for (int t = 0; t < T; ++t) best[t] = 0ull;
+    for (int sl = 0; sl < Top2Lane<T, MMA>::S; ++sl) st.b1[sl] = st.b2[sl] = 0ull;
     bool x_unconfirmed = false;  // thread 0: an activation copy was issued but not seen complete
     unsigned xphase = 0;
 
@@ -1580,7 +1627,7 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
                     __syncwarp();
                     if (lane == 0) hflag[warp] = 1;
                 } else if (!w.bad) {
-                    store_outputs<T, MMA, ARGMAX>(R.y, R.N, li * SLAB_ROWS, rows, r8, j, yv, best);
+                    store_outputs<T, MMA, ARGMAX>(R.y, R.N, li * SLAB_ROWS, rows, r8, j, yv, st);
                 } else if (lane == 0) {
                     atomicCAS(H.status, 0u, ST_BAD_ID);
                 }
@@ -1710,6 +1757,9 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
                         __threadfence();
                         const float *pb =
                             g.part + (static_cast<long long>(inf.e) * g.nslabs + inf.slab) * g.nseg * T * 16;
+                        unsigned long long kt[ARGMAX ? T : 1];  // this lane's row's key per token
+#pragma unroll
+                        for (int t = 0; t < (ARGMAX ? T : 1); ++t) kt[t] = 0ull;
                         if (lane < inf.rows) {
                             const int row = row0 + lane;
 #pragma unroll
@@ -1718,14 +1768,23 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
                                 for (int s2 = 1; s2 < g.nseg; ++s2)
                                     v = __fadd_rn(v, __ldcg(pb + (s2 * T + t) * 16 + lane));
                                 if (ye != nullptr) ye[static_cast<long long>(t) * N + row] = v;
-                                if (ARGMAX) best[t] = max(best[t], argmax_key(v, static_cast<unsigned>(row)));
+                                if (ARGMAX) kt[ARGMAX ? t : 0] = argmax_key(v, static_cast<unsigned>(row));
+                            }
+                        }
+                        if constexpr (ARGMAX) {
+                            using TL2 = Top2Lane<T, MMA>;
+#pragma unroll
+                            for (int t = 0; t < T; ++t) {  // the warp's pair, into a lane that tracks t
+                                unsigned long long a1 = kt[t], a2 = 0ull;
+                                top2_warp(a1, a2);
+                                if (lane == TL2::jt(t)) top2_merge(st.b1[TL2::slot(t)], st.b2[TL2::slot(t)], a1, a2);
                             }
                         }
                         __syncwarp();
                         if (lane == 0) *cnt = 0u;
                     }
                 } else {
-                    store_outputs<T, MMA, ARGMAX>(ye, N, row0, inf.rows, r8, j, yv, best);
+                    store_outputs<T, MMA, ARGMAX>(ye, N, row0, inf.rows, r8, j, yv, st);
                 }
             }
             ra = rb;
@@ -1737,46 +1796,61 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
     if (x_unconfirmed) mbar_drain(xbar, xphase ^ 1u);
 
     if (ARGMAX) {
+        // top-2 per token: lanes with the same j (lane bits 2..4 are r8), then
+        // warps, then this CTA's candidate pair
 #pragma unroll
-        for (int t = 0; t < T; ++t) {
-            unsigned long long v = best[t];
+        for (int sl = 0; sl < Top2Lane<T, MMA>::S; ++sl) {
+            unsigned long long v1 = st.b1[sl], v2 = st.b2[sl];
 #pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                const unsigned long long o = __shfl_xor_sync(0xFFFFFFFFu, v, off);
-                v = o > v ? o : v;
+            for (int off = 4; off < 32; off <<= 1) {
+                const unsigned long long o1 = __shfl_xor_sync(0xFFFFFFFFu, v1, off);
+                const unsigned long long o2 = __shfl_xor_sync(0xFFFFFFFFu, v2, off);
+                top2_merge(v1, v2, o1, o2);
             }
-            if (lane == 0) s_best[warp * T + t] = v;
+            const int t = Top2Lane<T, MMA>::token(sl, lane);
+            if (lane < 4 && t < T) {
+                s_best[(warp * T + t) * 2] = v1;
+                s_best[(warp * T + t) * 2 + 1] = v2;
+            }
         }
         __syncthreads();
         if (tid < T) {
-            unsigned long long m = 0ull;
-            for (int w = 0; w < nw; ++w) m = max(m, s_best[w * T + tid]);
-            H.am_cand[static_cast<long long>(blockIdx.x) * T + tid] = m;
-            __threadfence();  // the candidate is visible before the arrival below
+            unsigned long long m1 = 0ull, m2 = 0ull;
+            for (int w = 0; w < nw; ++w) top2_merge(m1, m2, s_best[(w * T + tid) * 2], s_best[(w * T + tid) * 2 + 1]);
+            H.am_cand[(static_cast<long long>(blockIdx.x) * T + tid) * 2] = m1;
+            H.am_cand[(static_cast<long long>(blockIdx.x) * T + tid) * 2 + 1] = m2;
+            __threadfence();  // the candidates are visible before the arrival below
         }
         __syncthreads();
         if (tid == 0) s_last = (atomicAdd(H.am_cnt, 1u) == gridDim.x - 1) ? 1 : 0;
         __syncthreads();
         if (s_last) {
-            // every CTA's candidates, one per thread, then a warp and a CTA maximum
+            // every CTA's candidate pair, one per thread, then a warp and a CTA merge
             __threadfence();
 #pragma unroll
             for (int t = 0; t < T; ++t) {
-                unsigned long long m = 0ull;
+                unsigned long long m1 = 0ull, m2 = 0ull;
                 for (unsigned c = tid; c < gridDim.x; c += nthreads)
-                    m = max(m, __ldcg(H.am_cand + static_cast<long long>(c) * T + t));
-#pragma unroll
-                for (int off = 16; off > 0; off >>= 1) {
-                    const unsigned long long o = __shfl_xor_sync(0xFFFFFFFFu, m, off);
-                    m = o > m ? o : m;
+                    top2_merge(m1, m2, __ldcg(H.am_cand + (static_cast<long long>(c) * T + t) * 2),
+                               __ldcg(H.am_cand + (static_cast<long long>(c) * T + t) * 2 + 1));
+                top2_warp(m1, m2);
+                if (lane == 0) {
+                    s_best[(warp * T + t) * 2] = m1;
+                    s_best[(warp * T + t) * 2 + 1] = m2;
                 }
-                if (lane == 0) s_best[warp * T + t] = m;
             }
             __syncthreads();
             if (tid < T) {
-                unsigned long long m = 0ull;
-                for (int w = 0; w < nw; ++w) m = max(m, s_best[w * T + tid]);
-                H.am_idx[tid] = static_cast<long long>(0xFFFFFFFFull - (m & 0xFFFFFFFFull));
+                unsigned long long m1 = 0ull, m2 = 0ull;
+                for (int w = 0; w < nw; ++w)
+                    top2_merge(m1, m2, s_best[(w * T + tid) * 2], s_best[(w * T + tid) * 2 + 1]);
+                if (H.am_idx != nullptr) H.am_idx[tid] = key_row(m1);
+                if (H.am_idx2 != nullptr) {
+                    H.am_idx2[2 * tid] = key_row(m1);
+                    H.am_idx2[2 * tid + 1] = key_row(m2);
+                    H.am_val2[2 * tid] = key_value(m1);
+                    H.am_val2[2 * tid + 1] = key_value(m2);
+                }
             }
             if (tid == 0) *H.am_cnt = 0u;
         }

@@ -176,4 +176,26 @@ cudaError_t launch_isums(const void *W, bool packed, const void *xq, int32_t *is
     return cudaGetLastError();
 }
 
+// The lossless verify rule (minfer README M17): tokens[0] is the step's
+// current token, tokens[1..T-1] its drafts, pred[t] the greedy prediction
+// after tokens[0..t] (at pred[t * pred_stride]).  The step commits pred[0] and each later prediction
+// while every draft so far equalled the prediction before it: n = 1 + the
+// length of the leading run of t with tokens[t + 1] == pred[t].  One warp.
+__global__ void __launch_bounds__(32) verify_commit_kernel(const long long *__restrict__ tokens,
+                                                           const long long *__restrict__ pred, int pred_stride,
+                                                           int T, int32_t *__restrict__ n_commit)
+{
+    const int t = threadIdx.x;
+    const bool match = t + 1 < T && tokens[t + 1] == pred[static_cast<long long>(t) * pred_stride];
+    const unsigned m = __ballot_sync(0xFFFFFFFFu, match);
+    if (t == 0) *n_commit = __ffs(~m);  // bit T-1 of m is clear, so n <= T
+}
+
+cudaError_t launch_verify_commit(const long long *tokens, const long long *pred, int pred_stride, int T,
+                                 int32_t *n_commit, cudaStream_t st)
+{
+    verify_commit_kernel<<<1, 32, 0, st>>>(tokens, pred, pred_stride, T, n_commit);
+    return cudaGetLastError();
+}
+
 }  // namespace qg

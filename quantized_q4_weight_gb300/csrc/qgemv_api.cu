@@ -146,7 +146,7 @@ qgemv_status make_plan(const GroupSpec *gs, int n, int T, bool ggml, bool argmax
     if (argmax) {
         P.am_cnt = ws ? reinterpret_cast<unsigned *>(ws) : nullptr;
         P.am_cand = ws ? reinterpret_cast<unsigned long long *>(ws + off) : nullptr;
-        off = align_up(off + static_cast<long long>(MAX_GRID) * T * 8, 256);
+        off = align_up(off + static_cast<long long>(MAX_GRID) * T * 16, 256);  // a key pair per CTA and token
     }
     long long cost = 0, items = 0;
     int kmax = 0, nbmax = 0;
@@ -290,10 +290,12 @@ qgemv_status plan_launch(const GroupSpec *gs, int n, int T, bool ggml, bool argm
                          int &cps, Plan<MAXG> &pl)
 {
     const bool mma = mma_for(T);
-    qgemv_status s = make_plan<MAXG>(gs, n, T, ggml, argmax, ws, smem_budget(d, cps), pl, cps, mma);
+    // argmax kernels hold [warps][T][2] key pairs in static shared memory (up to 2 KB)
+    const int extra = argmax ? 1024 : 0;
+    qgemv_status s = make_plan<MAXG>(gs, n, T, ggml, argmax, ws, smem_budget(d, cps) - extra, pl, cps, mma);
     if (s == QGEMV_ERR_UNSUPPORTED && cps > 1) {
         cps = 1;
-        s = make_plan<MAXG>(gs, n, T, ggml, argmax, ws, smem_budget(d, cps), pl, cps, mma);
+        s = make_plan<MAXG>(gs, n, T, ggml, argmax, ws, smem_budget(d, cps) - extra, pl, cps, mma);
     }
     return s;
 }
@@ -380,7 +382,7 @@ long long single_ws_bytes(long long N, long long K, int T)
 
 qgemv_status run_single(const void *W, qgemv_wlayout layout, const void *xq, float *y, long long *idx, long long N,
                         long long K, int T, void *ws, size_t ws_bytes, cudaStream_t st, bool argmax, bool pdl,
-                        bool xf32 = false)
+                        bool xf32 = false, long long *idx2 = nullptr, float *val2 = nullptr)
 {
     DevInfo dev;
     qgemv_status s = device_info(dev);
@@ -394,6 +396,8 @@ qgemv_status run_single(const void *W, qgemv_wlayout layout, const void *xq, flo
     pl.P.status = dev.status;
     pl.P.xf32 = xf32 ? 1 : 0;
     pl.P.am_idx = reinterpret_cast<long long *>(idx);
+    pl.P.am_idx2 = idx2;
+    pl.P.am_val2 = val2;
     const int grid = grid_for(dev, cps);
     set_cta_groups(pl.P, grid);
     const cudaError_t e = argmax ? dispatch_T<MAXG_SMALL, true>(pl.P, T, mma_for(T), grid, pl.smem, st, pdl)
@@ -537,6 +541,59 @@ qgemv_status qgemv_q4_0_argmax_f32(const void *W, qgemv_wlayout layout, const fl
                                    qgemv_stream_t stream)
 {
     return argmax_call(W, layout, x, true, y_or_null, idx, N, K, T, ws, ws_bytes, stream);
+}
+
+// The top-2 calls: the argmax calls' checks, with the [T][2] row and value
+// outputs in place of idx.
+static qgemv_status top2_call(const void *W, qgemv_wlayout layout, const void *xin, bool xf32, float *y_or_null,
+                              int64_t *idx2, float *val2, int64_t N, int64_t K, int T, void *ws, size_t ws_bytes,
+                              qgemv_stream_t stream)
+{
+    const long long xin_bytes = !shape_ok(N, K) ? 0 : xf32 ? 4ll * T * K : xq_bytes_host(T, K);
+    qgemv_status s = check_single(W, layout, xin, xin_bytes, y_or_null, N, K, T, ws);
+    if (s != QGEMV_OK) return s;
+    if (!idx2 || !val2) return QGEMV_ERR_INVALID_ARG;
+    if (!aligned(xin, xf32 ? 4 : 16) || !aligned(idx2, 8) || !aligned(val2, 4)) return QGEMV_ERR_MISALIGNED;
+    if (!ws) return QGEMV_ERR_WORKSPACE;
+    const Range rw = range(ws, static_cast<long long>(ws_bytes));
+    const Range ri = range(idx2, 16ll * T), rv = range(val2, 8ll * T);
+    if (overlap(ri, rw) || overlap(rv, rw) || overlap(ri, rv)) return QGEMV_ERR_INVALID_ARG;
+    if (y_or_null) {
+        const Range ry = range(y_or_null, 4ll * T * N);
+        if (overlap(ry, rw) || overlap(ry, ri) || overlap(ry, rv)) return QGEMV_ERR_INVALID_ARG;
+    }
+    if (xf32) {
+        const Range rx = range(xin, xin_bytes);
+        if (overlap(rx, rw) || overlap(rx, ri) || overlap(rx, rv)) return QGEMV_ERR_INVALID_ARG;
+    }
+    return run_single(W, layout, xin, y_or_null, nullptr, N, K, T, ws, ws_bytes,
+                      reinterpret_cast<cudaStream_t>(stream), true, true, xf32, reinterpret_cast<long long *>(idx2),
+                      val2);
+}
+
+qgemv_status qgemv_q4_0_top2(const void *W, qgemv_wlayout layout, const void *xq, float *y_or_null, int64_t *idx2,
+                             float *val2, int64_t N, int64_t K, int T, void *ws, size_t ws_bytes,
+                             qgemv_stream_t stream)
+{
+    return top2_call(W, layout, xq, false, y_or_null, idx2, val2, N, K, T, ws, ws_bytes, stream);
+}
+
+qgemv_status qgemv_q4_0_top2_f32(const void *W, qgemv_wlayout layout, const float *x, float *y_or_null,
+                                 int64_t *idx2, float *val2, int64_t N, int64_t K, int T, void *ws, size_t ws_bytes,
+                                 qgemv_stream_t stream)
+{
+    return top2_call(W, layout, x, true, y_or_null, idx2, val2, N, K, T, ws, ws_bytes, stream);
+}
+
+qgemv_status qgemv_verify_commit(const int64_t *tokens, const int64_t *pred, int pred_stride, int T,
+                                 int32_t *n_commit, qgemv_stream_t stream)
+{
+    if (T < 1 || T > 32 || pred_stride < 1 || !tokens || !pred || !n_commit) return QGEMV_ERR_INVALID_ARG;
+    if (!aligned(tokens, 8) || !aligned(pred, 8) || !aligned(n_commit, 4)) return QGEMV_ERR_MISALIGNED;
+    return launch_verify_commit(reinterpret_cast<const long long *>(tokens), reinterpret_cast<const long long *>(pred),
+                                pred_stride, T, n_commit, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? QGEMV_OK
+               : QGEMV_ERR_CUDA;
 }
 
 size_t qgemv_seq_workspace_bytes(const qgemv_seq_item *items, int n, int T)

@@ -73,7 +73,9 @@ struct ParamHead {
     long long total_cost, total_items;  // weighted bytes, items of the launch
     unsigned long long *am_cand;  // argmax: [gridDim][T] candidate keys
     unsigned *am_cnt;             // argmax: CTA arrival counter
-    long long *am_idx;            // argmax: result [T]
+    long long *am_idx;            // argmax: result [T] (or nullptr)
+    long long *am_idx2;           // top-2: rows [T][2] (or nullptr)
+    float *am_val2;               // top-2: values [T][2] (with am_idx2)
     unsigned *status;             // per-device status word
 };
 

@@ -21,6 +21,8 @@ cudaError_t launch_stream_bench(const void *src, long long bytes, int method, in
 cudaError_t launch_pack(const void *src, void *dst, long long N, long long K, bool to_packed, cudaStream_t st);
 cudaError_t launch_isums(const void *W, bool packed, const void *xq, int32_t *isums, long long N, long long K, int T,
                          cudaStream_t st);
+cudaError_t launch_verify_commit(const long long *tokens, const long long *pred, int pred_stride, int T,
+                                 int32_t *n_commit, cudaStream_t st);
 
 // The streaming GEMV kernel, one instantiation per (T, parameter-block size,
 // argmax, tensor-core path).  Defined in gemv_t<T>.cu.

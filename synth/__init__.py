@@ -100,6 +100,9 @@ WORKLOADS = {
     "qwen2.5-1.5b_layerset": dict(kind="seq", layer=QWEN25_1P5B_LAYER, layers=28, T=1, seed=1000),
     # lm_head 151936x1536 with fused argmax, 4 weight copies in rotation
     "lm_head_argmax": dict(kind="argmax", N=151936, K=1536, T=1, copies=4, seed=2000),
+    # lm_head verify step: 8 positions (current token + 7 drafts), top-2 rows
+    # per position, then the commit rule; 4 weight copies in rotation
+    "lm_head_top2_verify": dict(kind="verify", N=151936, K=1536, T=8, copies=4, seed=2100),
     # 36-layer Qwen2.5-3B-shaped layer set, T in {1,2,4,8}
     "qwen2.5-3b_verify": dict(kind="seq", layer=QWEN25_3B_LAYER, layers=36, Ts=(1, 2, 4, 8), seed=3000),
     # MoE: 256 experts (gate/up 512x2048, down 2048x512), top-8 + 1 shared, T=1
