@@ -79,6 +79,10 @@ class Oracle:
         L.orc_argmax_f32.restype = ctypes.c_int64
         L.orc_argmax_f64.argtypes = [_f64p, ctypes.c_int64]
         L.orc_argmax_f64.restype = ctypes.c_int64
+        L.orc_block_isum_q8.argtypes = [_u8p, _u8p]
+        L.orc_block_isum_q8.restype = ctypes.c_int32
+        L.orc_block_isums_q8.argtypes = [_u8p, ctypes.c_int64, ctypes.c_int64, _u8p, ctypes.c_int, _i32p]
+        L.orc_gemv_q8_f64.argtypes = [_u8p, ctypes.c_int64, ctypes.c_int64, _u8p, ctypes.c_int, _f64p, _f64p]
         L.orc_top2_f32.argtypes = [_f32p, ctypes.c_int64, _i64p]
         L.orc_top2_f32.restype = None
         L.orc_top2_f64.argtypes = [_f64p, ctypes.c_int64, _i64p]
@@ -150,6 +154,28 @@ class Oracle:
         S = np.empty((T, rows.size), np.float64)
         self.L.orc_gemv_rows_f64(_p(W, _u8p), N, K, _p(xq, _u8p), T, _p(rows, _i64p), rows.size,
                                  _p(y, _f64p), _p(S, _f64p))
+        return y, S
+
+    # -- Q8_0 weights
+    def block_isum_q8(self, wblk: np.ndarray, xblk: np.ndarray) -> int:
+        wblk = np.ascontiguousarray(wblk, np.uint8)
+        xblk = np.ascontiguousarray(xblk, np.uint8)
+        return int(self.L.orc_block_isum_q8(_p(wblk, _u8p), _p(xblk, _u8p)))
+
+    def block_isums_q8(self, W: np.ndarray, N: int, K: int, xq: np.ndarray, T: int) -> np.ndarray:
+        W = np.ascontiguousarray(W, np.uint8)
+        xq = np.ascontiguousarray(xq, np.uint8)
+        out = np.empty((T, N, K // 32), np.int32)
+        self.L.orc_block_isums_q8(_p(W, _u8p), N, K, _p(xq, _u8p), T, _p(out, _i32p))
+        return out
+
+    def gemv_q8(self, W: np.ndarray, N: int, K: int, xq: np.ndarray, T: int):
+        """Q8_0 weights (GGML blocks [N][nb][34]) -> (y64 [T, N], S [T, N]) in fp64."""
+        W = np.ascontiguousarray(W, np.uint8)
+        xq = np.ascontiguousarray(xq, np.uint8)
+        y = np.empty((T, N), np.float64)
+        S = np.empty((T, N), np.float64)
+        self.L.orc_gemv_q8_f64(_p(W, _u8p), N, K, _p(xq, _u8p), T, _p(y, _f64p), _p(S, _f64p))
         return y, S
 
     # -- argmax

@@ -284,6 +284,60 @@ void orc_gemv_rows_f64(const uint8_t *W, int64_t N, int64_t K, const uint8_t *xq
                      &S[(int64_t)t * nrows + r]);
 }
 
+/* ---------------------------------------------------------- Q8_0 weights */
+/* A second weight format on the same path (minfer README "How it works":
+ * gemv_q8_dp4a, int8 weights with int8 activations; M14: the lm_head held
+ * as Q8_0): a weight block is the Q8_0 block itself, fp16 d then 32 int8 q,
+ * and the weight is q * d (no offset). */
+
+/* isum = sum_j w_j * q_j over one block, exact int32 (|isum| <= 32*127*127). */
+int32_t orc_block_isum_q8(const uint8_t *wblk, const uint8_t *xblk)
+{
+    const int8_t *w = (const int8_t *)(wblk + 2);
+    const int8_t *q = (const int8_t *)(xblk + 2);
+    int32_t s = 0;
+    for (int j = 0; j < QK; j++)
+#if ORC_MUTANT == 13
+        s += (int32_t)(uint8_t)w[j] * q[j];     /* MUTANT: weights read as unsigned */
+#else
+        s += (int32_t)w[j] * q[j];
+#endif
+    return s;
+}
+
+/* isums [T][N][nb] for W (GGML Q8_0, [N][nb][34]) and xq (GGML Q8_0). */
+void orc_block_isums_q8(const uint8_t *W, int64_t N, int64_t K, const uint8_t *xq, int T, int32_t *isums)
+{
+    int64_t nb = K / QK;
+    for (int t = 0; t < T; t++)
+        for (int64_t i = 0; i < N; i++)
+            for (int64_t b = 0; b < nb; b++)
+                isums[((int64_t)t * N + i) * nb + b] =
+                    orc_block_isum_q8(W + (i * nb + b) * Q8_0_BYTES, xq_block(xq, nb, t, b));
+}
+
+/* y64, S: [T][N], as orc_gemv_f64 with Q8_0 weight blocks. */
+void orc_gemv_q8_f64(const uint8_t *W, int64_t N, int64_t K, const uint8_t *xq, int T, double *y64, double *S)
+{
+    int64_t nb = K / QK;
+    for (int t = 0; t < T; t++) {
+#pragma omp parallel for schedule(static)
+        for (int64_t i = 0; i < N; i++) {
+            double acc = 0.0, mag = 0.0;
+            for (int64_t b = 0; b < nb; b++) {
+                const uint8_t *wblk = W + (i * nb + b) * Q8_0_BYTES;
+                const uint8_t *xblk = xq_block(xq, nb, t, b);
+                double term = (double)orc_half_to_float(rd16(wblk)) * (double)orc_half_to_float(rd16(xblk)) *
+                              (double)orc_block_isum_q8(wblk, xblk);
+                acc += term;
+                mag += fabs(term);
+            }
+            y64[(int64_t)t * N + i] = acc;
+            S[(int64_t)t * N + i] = mag;
+        }
+    }
+}
+
 /* --------------------------------------------------------------- argmax */
 
 /* Lowest index i with y[i] maximal; equality is IEEE == (-0 == +0). */

@@ -48,6 +48,19 @@ def q4_0_weights(seed: int, N: int, K: int, stream: tuple = ()) -> np.ndarray:
     return blocks.reshape(N, nb * Q4_0_BLOCK_BYTES)
 
 
+def q8_0_weights(seed: int, N: int, K: int, stream: tuple = ()) -> np.ndarray:
+    """Random Q8_0 weight matrix in GGML row-major block layout, uint8 [N, K/32*34]:
+    fp16 scales as for Q4_0, int8 values uniform on [-127, 127]."""
+    assert K % QK == 0 and N >= 0
+    nb = K // QK
+    rng = _rng(seed, 4, *stream)
+    blocks = np.empty((N, nb, 34), dtype=np.uint8)
+    scales = rng.uniform(SCALE_LO, SCALE_HI, size=(N, nb)).astype(np.float16)
+    blocks[:, :, 0:2] = scales.astype("<f2").view(np.uint8).reshape(N, nb, 2)
+    blocks[:, :, 2:] = rng.integers(-127, 128, size=(N, nb, 32)).astype(np.int8).view(np.uint8)
+    return blocks.reshape(N, nb * 34)
+
+
 def activations(seed: int, T: int, K: int, stream: tuple = ()) -> np.ndarray:
     """fp32 [T, K]: N(0,1) with 1 % of entries scaled by 20."""
     rng = _rng(seed, 2, *stream)

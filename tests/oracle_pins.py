@@ -291,6 +291,75 @@ def pin_argmax_rules(o):
     assert o.argmax_f64(np.array([2.0, 5.0, 5.0], np.float64)) == 1
 
 
+# ------------------------------------------------------------------ Q8_0 weights
+
+def _q8w_bytes(d_bits: int, w) -> np.ndarray:
+    """One 34-byte Q8_0 weight block: fp16 d (little-endian), then 32 int8."""
+    return np.concatenate([np.array([d_bits & 0xFF, d_bits >> 8], np.uint8),
+                           np.asarray(w, np.int8).view(np.uint8)])
+
+
+def pin_q8w_hand_block(o):
+    # weights: w0 = 3, w1 = -2, w31 = 127, rest 0; activations q0 = 10, q1 = 7,
+    # q31 = -127, rest 0: isum = 30 - 14 - 16129 = -16113 (worked by hand)
+    w = np.zeros(32, np.int8); w[0], w[1], w[31] = 3, -2, 127
+    qx = np.zeros(32, np.int8); qx[0], qx[1], qx[31] = 10, 7, -127
+    wb, xb = _q8w_bytes(0x3800, w), _xq_bytes(0x3C00, qx)          # d_w = 0.5, d_x = 1
+    assert o.block_isum_q8(wb, xb) == -16113
+    y, S = o.gemv_q8(wb, 1, 32, xb, 1)
+    assert y[0, 0] == -8056.5 and S[0, 0] == 8056.5
+
+
+def pin_q8w_closed_forms_and_range(o):
+    K, nb = 1536, 48
+    for c in (-128, -127, -1, 0, 1, 127):
+        W = np.tile(_q8w_bytes(0x3C00, np.full(32, c, np.int8)), nb)   # d_w = 1
+        x = np.full((1, K), 127.0, np.float32)                         # every q = 127, d_x = 1
+        xq = o.quantize(x)
+        y, _ = o.gemv_q8(W, 1, K, xq, 1)
+        assert y[0, 0] == nb * 32 * 127 * c
+        assert o.block_isum_q8(W[:34], xq.reshape(-1, 34)[0]) == 32 * 127 * c
+    # the range extreme: -128 * -127 * 32
+    xb = _xq_bytes(0x3C00, np.full(32, -127, np.int8))
+    assert o.block_isum_q8(_q8w_bytes(0x3C00, np.full(32, -128, np.int8)), xb) == 520192
+
+
+def pin_q8w_from_q4_blocks(o):
+    """A Q4_0 block rewritten as Q8_0 weights (w = n - 8, same d) gives the
+    same integer sums and outputs as the Q4_0 path (pinned separately)."""
+    N, K, T = 7, 256, 3
+    import synth
+    W4 = synth.q4_0_weights(81, N, K).reshape(N, K // 32, 18)
+    lo, hi = W4[:, :, 2:] & 0x0F, W4[:, :, 2:] >> 4
+    n = np.concatenate([lo, hi], axis=2).astype(np.int16)            # elements 0..15, 16..31
+    W8 = np.empty((N, K // 32, 34), np.uint8)
+    W8[:, :, :2] = W4[:, :, :2]
+    W8[:, :, 2:] = (n - 8).astype(np.int8).view(np.uint8)
+    xq = o.quantize(synth.activations(82, T, K))
+    assert np.array_equal(o.block_isums_q8(W8.reshape(N, -1), N, K, xq, T),
+                          o.block_isums(W4.reshape(N, -1), N, K, xq, T))
+    y8, S8 = o.gemv_q8(W8.reshape(N, -1), N, K, xq, T)
+    y4, S4 = o.gemv(W4.reshape(N, -1), N, K, xq, T)
+    assert np.array_equal(y8, y4) and np.array_equal(S8, S4)
+
+
+def pin_q8w_bruteforce_dequant_dot(o):
+    import synth
+    rng = np.random.default_rng(83)
+    for _ in range(10):
+        N, K, T = int(rng.integers(1, 40)), 32 * int(rng.integers(1, 9)), int(rng.integers(1, 9))
+        W = synth.q8_0_weights(int(rng.integers(1 << 30)), N, K)
+        x = synth.activations(int(rng.integers(1 << 30)), T, K)
+        xq = o.quantize(x)
+        blk = W.reshape(N, K // 32, 34)
+        dw = blk[:, :, :2].copy().view("<f2").astype(np.float64)[:, :, 0]
+        wf = blk[:, :, 2:].view(np.int8).astype(np.float64) * dw[:, :, None]
+        xf = _dequant_x_f64(xq, T, K)
+        ref = xf @ wf.reshape(N, K).T
+        y, S = o.gemv_q8(W, N, K, xq, T)
+        assert np.all(np.abs(y - ref) <= 1e-12 * np.maximum(S, 1e-30))
+
+
 # ------------------------------------------------------------------ top-2
 
 def _top2_by_sort(y):

@@ -22,8 +22,9 @@ def test_pin(orc, pin):
 #  6 wrong activation block index, 7 signed instead of absolute max,
 #  8 truncating fp16 encode, 9 argmax ties to the highest index,
 #  10 transposed output, 11 top-2 second ties to the highest index,
-#  12 verify rule comparing a draft with its own prediction.
-MUTANTS = list(range(1, 13))
+#  12 verify rule comparing a draft with its own prediction,
+#  13 Q8_0 weights read as unsigned.
+MUTANTS = list(range(1, 14))
 
 
 @pytest.fixture(scope="module")
