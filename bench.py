@@ -56,6 +56,7 @@ class Workload:
         self.n_gemv = 0
         self.launches = 0         # kernels of ours per step
         self.host = {}            # optional host copies for parity checks
+        self.kernel_name = "qgemv_stream_kernel"  # the step's streaming kernel
         self.config = {}
 
     @property
@@ -200,9 +201,52 @@ def build_verify(T, seed, dev, copies=4, keep_host=False, N=151936, K=1536):
 
     wl.step, wl.kernel, wl.dominant = step, kernel, dominant
     wl.dominant_bytes = wl.w_bytes + wl.x_bytes + 24 * T
+    wl.other_launch = "the step's other launch is the one-warp commit rule"
     wl.inputs, wl.outputs = [wl.x, wl.tokens], [wl.idx2, wl.val2, wl.n_commit]
     wl.config = {"workload": "lm_head_top2_verify", "N": N, "K": K, "T": T, "copies": copies,
                  "step": "top-2 lm_head GEMV on fp32 x (quantised in the kernel), then the commit rule",
+                 "l2_defeat": f"{copies} weight copies in rotation ({copies * wl.w_bytes / 1e6:.0f} MB)"}
+    return wl
+
+
+def build_q8(T, seed, dev, copies=2, keep_host=False, N=151936, K=1536):
+    """The lm_head held as Q8_0 weights: one step quantises x and runs the
+    Q8_0-weight GEMV (two launches); copies rotate so reads hit HBM."""
+    import torch
+    q = _q()
+    wl = Workload("q8_lm_head", T)
+    wl.W = []
+    for c in range(copies):
+        Wg = synth.q8_0_weights(seed, N, K, stream=(c,))
+        if keep_host:
+            wl.host[c] = Wg
+        Wd = torch.from_numpy(Wg.reshape(-1)).to(dev)
+        wl.W.append(q.pack_q8_0(Wd, N, K))
+        del Wd
+    wl.x = torch.from_numpy(synth.activations(seed, T, K)).to(dev)
+    wl.xqb = q.quantize_q8_0(wl.x, T, K)
+    wl.y = torch.empty((T, N), dtype=torch.float32, device=dev)
+    wl.ws = q.new_workspace(q.q8_0_workspace_bytes(N, K, T), dev)
+    wl.w_bytes = q.q8_0_bytes(N, K)
+    wl.x_bytes, wl.y_bytes, wl.xq_bytes = 4 * T * K, 4 * T * N, q.xq_bytes(T, K)
+    wl.n_gemv, wl.launches = 1, 2
+    wl.copy = 0
+
+    def kernel(stream=None):
+        q.gemv_q8_0(wl.W[wl.copy], wl.xqb, N, K, T, wl.ws, y=wl.y, stream=stream)
+        wl.copy = (wl.copy + 1) % copies
+
+    def step(stream=None):
+        q.quantize_q8_0(wl.x, T, K, out=wl.xqb, stream=stream)
+        kernel(stream)
+
+    wl.step, wl.kernel, wl.dominant = step, kernel, kernel
+    wl.dominant_bytes = wl.w_bytes + wl.xq_bytes + wl.y_bytes
+    wl.other_launch = "the step's other launch is the activation quantiser"
+    wl.kernel_name = "q8_gemv_kernel"
+    wl.inputs, wl.outputs = [wl.x], [wl.y]
+    wl.config = {"workload": "q8_lm_head", "N": N, "K": K, "T": T, "copies": copies, "weights": "Q8_0",
+                 "step": "Q8_0 quantiser launch, then the Q8_0-weight GEMV launch",
                  "l2_defeat": f"{copies} weight copies in rotation ({copies * wl.w_bytes / 1e6:.0f} MB)"}
     return wl
 
@@ -326,6 +370,8 @@ def build_workload(name: str, dev, T: int | None = None, keep_host: bool = False
         return build_lm_head(T or spec["T"], spec["seed"], dev, spec["copies"], keep_host, spec["N"], spec["K"])
     if spec["kind"] == "verify":
         return build_verify(T or spec["T"], spec["seed"], dev, spec["copies"], keep_host, spec["N"], spec["K"])
+    if spec["kind"] == "q8":
+        return build_q8(T or spec["T"], spec["seed"], dev, spec["copies"], keep_host, spec["N"], spec["K"])
     if spec["kind"] == "single":
         return build_single(T or spec["T"], spec["seed"], dev, keep_host=keep_host, N=spec["N"], K=spec["K"])
     if spec["kind"] == "moe":
@@ -440,13 +486,14 @@ def _oracle_inputs(workload: str):
         if spec["kind"] == "seq":
             T = 1
             mats = synth.layer_set(spec["layer"], spec["layers"])
-        elif spec["kind"] in ("argmax", "single", "verify"):
+        elif spec["kind"] in ("argmax", "single", "verify", "q8"):
             T, mats = spec["T"], [("w", spec["N"], spec["K"])]
         else:
             T = 1
             mats = [("gate", spec["d_ff"], spec["d_model"]), ("up", spec["d_ff"], spec["d_model"]),
                     ("down", spec["d_model"], spec["d_ff"])] * (spec["top_k"] + 1)
-        data = [(N, K, synth.q4_0_weights(spec["seed"], N, K, stream=(i,)),
+        gen = synth.q8_0_weights if spec["kind"] == "q8" else synth.q4_0_weights
+        data = [(N, K, gen(spec["seed"], N, K, stream=(i,)),
                  synth.activations(spec["seed"], T, K, stream=(i,))) for i, (_, N, K) in enumerate(mats)]
         _ORACLE_INPUTS[workload] = (T, data)
     return _ORACLE_INPUTS[workload]
@@ -483,12 +530,13 @@ def oracle_sample(workload: str, budget_s: float = 12.0, min_s: float = 3.0, thr
     if threads:
         o.set_threads(threads)
     T, data = _oracle_inputs(workload)
+    gemv = o.gemv_q8 if synth.WORKLOADS[workload]["kind"] == "q8" else o.gemv
     done_bytes, t_total, n_done = 0, 0.0, 0
     while True:
         for N, K, Wg, x in data:
             t0 = time.perf_counter()
             xq = o.quantize(x)
-            o.gemv(Wg, N, K, xq, T)
+            gemv(Wg, N, K, xq, T)
             t_total += time.perf_counter() - t0
             done_bytes += Wg.nbytes + 4 * T * K + 4 * T * N
             n_done += 1
@@ -785,7 +833,7 @@ def measure(args, wl: Workload, dev, world, rank):
         torch.cuda.synchronize()
         dom_ms, dom_bytes = a.elapsed_time(b) / K, wl.dominant_bytes
         dom_timing = ("the step's GEMV launch alone, K launches back to back between two events on the "
-                      "launching stream (the step's other launch is the one-warp commit rule)")
+                      "launching stream (" + wl.other_launch + ")")
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
     achieved_preq = wl.gemv_kernel_bytes / (gemv_ms * 1e-3) / 1e9
     cfg = dict(wl.config)
@@ -807,7 +855,7 @@ def measure(args, wl: Workload, dev, world, rank):
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 2), "peak": peak, "unit": "GB/s",
                      "frac": round(achieved / peak, 4), "traffic": traffic_record(wl.name, wl.T),
-                     "kernel": "qgemv_stream_kernel", "algorithmic_bytes_per_launch": dom_bytes,
+                     "kernel": wl.kernel_name, "algorithmic_bytes_per_launch": dom_bytes,
                      "ms_per_launch": round(dom_ms, 5), "timing": dom_timing,
                      "preq_input": {
                          "achieved": round(achieved_preq, 2), "frac": round(achieved_preq / peak, 4),

@@ -197,6 +197,41 @@ qgemv_status qgemv_q4_0_top2_f32(const void *W, qgemv_wlayout layout, const floa
                                  int64_t K, int T, void *ws, size_t ws_bytes,
                                  qgemv_stream_t stream);
 
+/* ---- Q8_0 weights: a second weight format on the same path (minfer README
+ * "How it works": gemv_q8_dp4a, int8 weights with int8 activations; M14: the
+ * lm_head held as Q8_0).  A weight block is 34 bytes, fp16 d then 32 int8 q,
+ * and the weight is q * d.  GGML layout: row-major [N][K/32] blocks. */
+
+/* One-time repack of a GGML Q8_0 matrix into the device layout (same byte
+ * count, 34 * N * K/32): 16-row slabs of 8-block stages, each row's 16-byte
+ * chunks of codes placed so that the GEMV's lanes read conflict-free, then the
+ * stage's fp16 scales; the N % 16 tail rows stay in GGML layout after the
+ * slabs.  w_packed 16-byte aligned, not overlapping w_ggml.  The inverse is
+ * qgemv_unpack_q8_0. */
+qgemv_status qgemv_pack_q8_0(const void *w_ggml, void *w_packed, int64_t N, int64_t K,
+                             qgemv_stream_t stream);
+qgemv_status qgemv_unpack_q8_0(const void *w_packed, void *w_ggml, int64_t N, int64_t K,
+                               qgemv_stream_t stream);
+
+/* Workspace bytes for qgemv_q8_0 (0 when the launch needs none; 0 also for
+ * an invalid shape). */
+size_t qgemv_q8_0_workspace_bytes(int64_t N, int64_t K, int T);
+
+/* y[T][N] = W . x for packed Q8_0 weights W and planar Q8_0 activations xq
+ * (T rows, as qgemv_quantize_q8_0 writes them).  Per block the int32 sum
+ * sum w q is exact; (d_w d_x) isum is accumulated in fp32 in a fixed order that
+ * depends on K only: per row, the blocks of each 8-block stage in two
+ * interleaved halves (even, odd blocks) summed in increasing order from +0,
+ * the halves added, then the stage sums added in order.  Outputs are
+ * bit-identical for every T and launch shape.  W, xq 16-byte aligned; y
+ * 4-byte aligned and not overlapping W, xq or ws.  Returns
+ * QGEMV_ERR_UNSUPPORTED when T * K activation bytes (plus their scales and
+ * one weight stage per warp) exceed shared memory (about T * K <= 150000),
+ * QGEMV_ERR_WORKSPACE when ws is smaller than qgemv_q8_0_workspace_bytes.
+ * The workspace must be zero-filled before its first use and is left zeroed. */
+qgemv_status qgemv_q8_0(const void *W, const void *xq, float *y, int64_t N, int64_t K, int T,
+                        void *ws, size_t ws_bytes, qgemv_stream_t stream);
+
 /* The lossless verify rule of speculative greedy decoding (minfer README
  * M17: a verify step runs [current, draft_1..draft_K] and commits up to and
  * including the first prediction that disagrees with its draft).

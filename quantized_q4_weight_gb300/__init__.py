@@ -73,6 +73,10 @@ _SIGS = {
     "qgemv_q4_0_top2": ([_VP, _I32, _VP, _VP, _VP, _VP, _I64, _I64, _I32, _VP, _SZ, _VP], _I32),
     "qgemv_q4_0_top2_f32": ([_VP, _I32, _VP, _VP, _VP, _VP, _I64, _I64, _I32, _VP, _SZ, _VP], _I32),
     "qgemv_verify_commit": ([_VP, _VP, _I32, _I32, _VP, _VP], _I32),
+    "qgemv_pack_q8_0": ([_VP, _VP, _I64, _I64, _VP], _I32),
+    "qgemv_unpack_q8_0": ([_VP, _VP, _I64, _I64, _VP], _I32),
+    "qgemv_q8_0_workspace_bytes": ([_I64, _I64, _I32], _SZ),
+    "qgemv_q8_0": ([_VP, _VP, _VP, _I64, _I64, _I32, _VP, _SZ, _VP], _I32),
     "qgemv_seq_workspace_bytes": ([ctypes.POINTER(SeqItem), _I32, _I32], _SZ),
     "qgemv_q4_0_seq": ([ctypes.POINTER(SeqItem), _I32, _I32, _I32, _VP, _SZ, _VP], _I32),
     "qgemv_seq_f32_workspace_bytes": ([ctypes.POINTER(SeqF32Item), _I32, _I32], _SZ),
@@ -225,6 +229,35 @@ def verify_commit(tokens, pred, n_commit=None, stream=None):
     _check(lib().qgemv_verify_commit(_ptr(tokens), ctypes.c_void_p(pred.data_ptr()), pred.stride(0), T,
                                      _ptr(n_commit), _stream(stream)), "qgemv_verify_commit")
     return n_commit
+
+
+def q8_0_bytes(N: int, K: int) -> int:
+    return 34 * N * (K // QK)
+
+
+def pack_q8_0(w_ggml: torch.Tensor, N: int, K: int, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """GGML Q8_0 weights (uint8 [34 N K/32]) -> the device layout (same bytes)."""
+    out = out if out is not None else torch.empty(q8_0_bytes(N, K), dtype=torch.uint8, device=w_ggml.device)
+    _check(lib().qgemv_pack_q8_0(_ptr(w_ggml), _ptr(out), N, K, _stream(stream)), "qgemv_pack_q8_0")
+    return out
+
+
+def unpack_q8_0(w_packed: torch.Tensor, N: int, K: int, out: torch.Tensor | None = None, stream=None):
+    out = out if out is not None else torch.empty(q8_0_bytes(N, K), dtype=torch.uint8, device=w_packed.device)
+    _check(lib().qgemv_unpack_q8_0(_ptr(w_packed), _ptr(out), N, K, _stream(stream)), "qgemv_unpack_q8_0")
+    return out
+
+
+def q8_0_workspace_bytes(N: int, K: int, T: int) -> int:
+    return int(lib().qgemv_q8_0_workspace_bytes(N, K, T))
+
+
+def gemv_q8_0(W, xq, N: int, K: int, T: int, ws=None, y=None, stream=None) -> torch.Tensor:
+    """y[T][N] for packed Q8_0 weights and planar Q8_0 activations."""
+    y = y if y is not None else torch.empty((T, N), dtype=torch.float32, device=W.device)
+    _check(lib().qgemv_q8_0(_ptr(W), _ptr(xq), _ptr(y), N, K, T, _ptr(ws), 0 if ws is None else ws.numel(),
+                            _stream(stream)), "qgemv_q8_0")
+    return y
 
 
 def seq_items(entries) -> ctypes.Array:

@@ -585,6 +585,64 @@ qgemv_status qgemv_q4_0_top2_f32(const void *W, qgemv_wlayout layout, const floa
     return top2_call(W, layout, x, true, y_or_null, idx2, val2, N, K, T, ws, ws_bytes, stream);
 }
 
+// ------------------------------------------------------------ Q8_0 weights
+
+qgemv_status qgemv_pack_q8_0(const void *w_ggml, void *w_packed, int64_t N, int64_t K, qgemv_stream_t stream)
+{
+    if (!shape_ok(N, K) || !w_ggml || !w_packed) return QGEMV_ERR_INVALID_ARG;
+    if (!aligned(w_packed, 16)) return QGEMV_ERR_MISALIGNED;
+    if (overlap(range(w_ggml, 34ll * N * (K / QK)), range(w_packed, 34ll * N * (K / QK)))) return QGEMV_ERR_INVALID_ARG;
+    return launch_q8_pack(w_ggml, w_packed, N, K, true, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? QGEMV_OK
+               : QGEMV_ERR_CUDA;
+}
+
+qgemv_status qgemv_unpack_q8_0(const void *w_packed, void *w_ggml, int64_t N, int64_t K, qgemv_stream_t stream)
+{
+    if (!shape_ok(N, K) || !w_ggml || !w_packed) return QGEMV_ERR_INVALID_ARG;
+    if (!aligned(w_packed, 16)) return QGEMV_ERR_MISALIGNED;
+    if (overlap(range(w_ggml, 34ll * N * (K / QK)), range(w_packed, 34ll * N * (K / QK)))) return QGEMV_ERR_INVALID_ARG;
+    return launch_q8_pack(w_packed, w_ggml, N, K, false, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? QGEMV_OK
+               : QGEMV_ERR_CUDA;
+}
+
+size_t qgemv_q8_0_workspace_bytes(int64_t N, int64_t K, int T)
+{
+    if (!shape_ok(N, K) || T < 1 || T > 8) return 0;
+    DevInfo dev;
+    int sms = 152, budget = 230400;
+    if (device_info(dev) == QGEMV_OK) {
+        sms = dev.sms;
+        budget = dev.smem_optin - 2048;
+    }
+    long long need = 0;
+    int uns = 0;
+    launch_q8(nullptr, nullptr, nullptr, N, K, T, nullptr, 0, false, sms, budget, nullptr, nullptr, &need, &uns);
+    return static_cast<size_t>(need);
+}
+
+qgemv_status qgemv_q8_0(const void *W, const void *xq, float *y, int64_t N, int64_t K, int T, void *ws,
+                        size_t ws_bytes, qgemv_stream_t stream)
+{
+    if (!shape_ok(N, K) || T < 1 || T > 8 || !W || !xq || !y) return QGEMV_ERR_INVALID_ARG;
+    if (!aligned(W, 16) || !aligned(xq, 16) || !aligned(y, 4) || (ws && !aligned(ws, 256))) return QGEMV_ERR_MISALIGNED;
+    const Range ry = range(y, 4ll * T * N);
+    if (overlap(ry, range(W, 34ll * N * (K / QK))) || overlap(ry, range(xq, xq_bytes_host(T, K))) ||
+        (ws && overlap(ry, range(ws, static_cast<long long>(ws_bytes)))))
+        return QGEMV_ERR_INVALID_ARG;
+    DevInfo dev;
+    qgemv_status s = device_info(dev);
+    if (s != QGEMV_OK) return s;
+    long long need = 0;
+    int uns = 0;
+    const cudaError_t e = launch_q8(W, xq, y, N, K, T, ws, static_cast<long long>(ws_bytes), true, dev.sms,
+                                    dev.smem_optin - 2048, dev.status, reinterpret_cast<cudaStream_t>(stream), &need,
+                                    &uns);
+    if (uns) return uns == 1 ? QGEMV_ERR_UNSUPPORTED : QGEMV_ERR_WORKSPACE;
+    return e == cudaSuccess ? QGEMV_OK : QGEMV_ERR_CUDA;
+}
+
 qgemv_status qgemv_verify_commit(const int64_t *tokens, const int64_t *pred, int pred_stride, int T,
                                  int32_t *n_commit, qgemv_stream_t stream)
 {

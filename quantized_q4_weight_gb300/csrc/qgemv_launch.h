@@ -21,6 +21,13 @@ cudaError_t launch_stream_bench(const void *src, long long bytes, int method, in
 cudaError_t launch_pack(const void *src, void *dst, long long N, long long K, bool to_packed, cudaStream_t st);
 cudaError_t launch_isums(const void *W, bool packed, const void *xq, int32_t *isums, long long N, long long K, int T,
                          cudaStream_t st);
+cudaError_t launch_q8_pack(const void *src, void *dst, long long N, long long K, bool to_packed, cudaStream_t st);
+// Q8_0-weight GEMV (q8_kernel.cu): plans, and launches when do_launch.
+// *ws_need: workspace bytes; *unsupported: 1 the activations do not fit
+// shared memory, 2 the workspace is missing or too small (nothing launched).
+cudaError_t launch_q8(const void *W, const void *xq, float *y, long long N, long long K, int T, void *ws,
+                      long long ws_bytes, bool do_launch, int sms, int smem_budget, unsigned *status,
+                      cudaStream_t st, long long *ws_need, int *unsupported);
 cudaError_t launch_verify_commit(const long long *tokens, const long long *pred, int pred_stride, int T,
                                  int32_t *n_commit, cudaStream_t st);
 

@@ -116,6 +116,8 @@ WORKLOADS = {
     # lm_head verify step: 8 positions (current token + 7 drafts), top-2 rows
     # per position, then the commit rule; 4 weight copies in rotation
     "lm_head_top2_verify": dict(kind="verify", N=151936, K=1536, T=8, copies=4, seed=2100),
+    # the lm_head held as Q8_0 weights (248 MB per copy), T=1, 2 copies in rotation
+    "q8_lm_head": dict(kind="q8", N=151936, K=1536, T=1, copies=2, seed=2200),
     # 36-layer Qwen2.5-3B-shaped layer set, T in {1,2,4,8}
     "qwen2.5-3b_verify": dict(kind="seq", layer=QWEN25_3B_LAYER, layers=36, Ts=(1, 2, 4, 8), seed=3000),
     # MoE: 256 experts (gate/up 512x2048, down 2048x512), top-8 + 1 shared, T=1
