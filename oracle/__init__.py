@@ -83,6 +83,9 @@ class Oracle:
         L.orc_block_isum_q8.restype = ctypes.c_int32
         L.orc_block_isums_q8.argtypes = [_u8p, ctypes.c_int64, ctypes.c_int64, _u8p, ctypes.c_int, _i32p]
         L.orc_gemv_q8_f64.argtypes = [_u8p, ctypes.c_int64, ctypes.c_int64, _u8p, ctypes.c_int, _f64p, _f64p]
+        L.orc_exp_f32_n.argtypes = [_f32p, ctypes.c_int64, _f32p]
+        L.orc_silu_f32_n.argtypes = [_f32p, ctypes.c_int64, _f32p]
+        L.orc_silu_mul_quantize.argtypes = [_f32p, _f32p, ctypes.c_int, ctypes.c_int64, _u8p, _f32p]
         L.orc_top2_f32.argtypes = [_f32p, ctypes.c_int64, _i64p]
         L.orc_top2_f32.restype = None
         L.orc_top2_f64.argtypes = [_f64p, ctypes.c_int64, _i64p]
@@ -177,6 +180,29 @@ class Oracle:
         S = np.empty((T, N), np.float64)
         self.L.orc_gemv_q8_f64(_p(W, _u8p), N, K, _p(xq, _u8p), T, _p(y, _f64p), _p(S, _f64p))
         return y, S
+
+    # -- FFN chain
+    def exp_f32(self, x: np.ndarray) -> np.ndarray:
+        x = np.ascontiguousarray(x, np.float32)
+        out = np.empty_like(x)
+        self.L.orc_exp_f32_n(_p(x, _f32p), x.size, _p(out, _f32p))
+        return out
+
+    def silu_f32(self, x: np.ndarray) -> np.ndarray:
+        x = np.ascontiguousarray(x, np.float32)
+        out = np.empty_like(x)
+        self.L.orc_silu_f32_n(_p(x, _f32p), x.size, _p(out, _f32p))
+        return out
+
+    def silu_mul_quantize(self, g: np.ndarray, u: np.ndarray):
+        """g, u fp32 [T, F] -> (Q8_0 blocks of SiLU(g) * u [T, F/32, 34], the fp32 h [T, F])."""
+        g = np.ascontiguousarray(g, np.float32)
+        u = np.ascontiguousarray(u, np.float32)
+        T, F = g.shape
+        hq = np.empty((T, F // 32, 34), np.uint8)
+        h = np.empty((T, F), np.float32)
+        self.L.orc_silu_mul_quantize(_p(g, _f32p), _p(u, _f32p), T, F, _p(hq, _u8p), _p(h, _f32p))
+        return hq, h
 
     # -- argmax
     def argmax_f32(self, y: np.ndarray) -> int:

@@ -364,6 +364,74 @@ int64_t orc_argmax_f64(const double *y, int64_t N)
     return best;
 }
 
+/* ------------------------------------------------------------- FFN chain */
+/* The decode FFN around the GEMVs (minfer README M15: one persistent kernel
+ * runs every layer; colibri qwen36 docs: gate and up share one pass over the
+ * activation): h = SiLU(g) * u with SiLU(g) = g / (1 + exp(-g)), then h is
+ * quantised to Q8_0 for the down projection.  Every step is fp32, rounded to
+ * nearest even, in the order written, so that the kernel's fp32 values and
+ * codes can match exactly.
+ *
+ * exp by Cody and Waite's method (W. J. Cody, W. Waite, "Software Manual for
+ * the Elementary Functions", 1980): x = k ln2 + r with k = rint(x log2 e) and
+ * ln 2 split into a short head (exact k * head) and a tail, so r is formed
+ * almost exactly; exp(r) by its Taylor series to r^7/7! in Horner form
+ * (|r| <= ln2/2, truncation below 2^-27 relative); then the exact scale 2^k.
+ * x is clamped to [-87, 88] so that 2^k stays a normal float. */
+#define ORC_LOG2E 1.44269504088896340736f
+#define ORC_LN2_HI 0.693145751953125f          /* 0x3F317200: 13 significant bits */
+#define ORC_LN2_LO 1.42860682030941723212e-6f  /* ln 2 - ORC_LN2_HI */
+
+float orc_exp_f32(float x)
+{
+    if (x > 88.0f) x = 88.0f;
+    if (x < -87.0f) x = -87.0f;
+    float k = rintf(x * ORC_LOG2E);
+    float r = fmaf(-k, ORC_LN2_HI, x);
+    r = fmaf(-k, ORC_LN2_LO, r);
+    float p = 1.0f / 5040.0f;
+    p = fmaf(p, r, 1.0f / 720.0f);
+    p = fmaf(p, r, 1.0f / 120.0f);
+    p = fmaf(p, r, 1.0f / 24.0f);
+    p = fmaf(p, r, 1.0f / 6.0f);
+    p = fmaf(p, r, 0.5f);
+    p = fmaf(p, r, 1.0f);
+    p = fmaf(p, r, 1.0f);
+    union { uint32_t u; float f; } sc;
+    sc.u = (uint32_t)((int)k + 127) << 23;
+    return p * sc.f;
+}
+
+float orc_silu_f32(float g)
+{
+#if ORC_MUTANT == 14
+    return g / (1.0f + orc_exp_f32(g));         /* MUTANT: exp(+g) */
+#else
+    return g / (1.0f + orc_exp_f32(-g));
+#endif
+}
+
+void orc_exp_f32_n(const float *x, int64_t n, float *out)
+{
+    for (int64_t i = 0; i < n; i++) out[i] = orc_exp_f32(x[i]);
+}
+
+void orc_silu_f32_n(const float *x, int64_t n, float *out)
+{
+    for (int64_t i = 0; i < n; i++) out[i] = orc_silu_f32(x[i]);
+}
+
+/* h[t][j] = SiLU(g[t][j]) * u[t][j] (fp32 [T][F]), quantised to Q8_0 blocks
+ * [T][F/32][34] as orc_quantize_q8_0 does. */
+void orc_silu_mul_quantize(const float *g, const float *u, int T, int64_t F, uint8_t *hq, float *h_out)
+{
+    float *h = (float *)malloc(sizeof(float) * (size_t)T * (size_t)F);
+    for (int64_t i = 0; i < (int64_t)T * F; i++) h[i] = orc_silu_f32(g[i]) * u[i];
+    orc_quantize_q8_0(h, T, F, hq);
+    if (h_out) memcpy(h_out, h, sizeof(float) * (size_t)T * (size_t)F);
+    free(h);
+}
+
 /* ------------------------------------------------ top-2 and the commit rule */
 
 /* The two best rows of y: idx[0] is the argmax (lowest index among equal

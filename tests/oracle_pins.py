@@ -360,6 +360,48 @@ def pin_q8w_bruteforce_dequant_dot(o):
         assert np.all(np.abs(y - ref) <= 1e-12 * np.maximum(S, 1e-30))
 
 
+# ------------------------------------------------------------------ FFN chain
+
+def pin_exp_against_libm(o):
+    """Cody-Waite exp against numpy's fp64 exp: within 2 ulp over [-87, 88]."""
+    x = np.linspace(-87.0, 88.0, 400001).astype(np.float32)
+    x = np.concatenate([x, np.array([0.0, -0.0, 1e-8, -1e-8, 0.5, -0.5], np.float32)])
+    e = o.exp_f32(x).astype(np.float64)
+    ref = np.exp(x.astype(np.float64))
+    ulp = np.spacing(ref.astype(np.float32)).astype(np.float64)
+    assert np.all(np.abs(e - ref) <= 2 * ulp)
+    assert o.exp_f32(np.array([0.0], np.float32))[0] == 1.0
+    assert np.all(np.diff(o.exp_f32(np.sort(x))) >= 0)        # monotone
+
+
+def pin_silu_identities(o):
+    g = np.linspace(-40.0, 40.0, 100001).astype(np.float32)
+    s, sm = o.silu_f32(g).astype(np.float64), o.silu_f32(-g).astype(np.float64)
+    ref = g.astype(np.float64) / (1.0 + np.exp(-g.astype(np.float64)))
+    assert np.all(np.abs(s - ref) <= 4 * np.spacing(np.abs(ref).astype(np.float32)) + 1e-30)
+    # silu(g) - silu(-g) = g
+    assert np.all(np.abs((s - sm) - g) <= 8 * np.spacing(np.abs(g)) + 1e-30)
+    assert o.silu_f32(np.array([0.0], np.float32))[0] == 0.0
+
+
+def pin_silu_mul_quantize_against_fp64(o):
+    """Dequantised codes of SiLU(g) * u within half a quantisation step (plus
+    the fp32 rounding of h) of the fp64 value; token-major blocks."""
+    rng = np.random.default_rng(91)
+    T, F = 3, 512
+    g = (rng.standard_normal((T, F)) * 3).astype(np.float32)
+    u = rng.standard_normal((T, F)).astype(np.float32)
+    hq, h = o.silu_mul_quantize(g, u)
+    h64 = g.astype(np.float64) / (1.0 + np.exp(-g.astype(np.float64))) * u
+    assert np.all(np.abs(h - h64) <= 8 * np.spacing(np.abs(h64).astype(np.float32)) + 1e-30)
+    d = hq[:, :, 0:2].copy().view("<f2").astype(np.float64)          # [T, F/32, 1]
+    q = hq[:, :, 2:].view(np.int8).astype(np.float64)
+    deq = (q * d).reshape(T, F)
+    step = np.repeat(d[:, :, 0], 32, axis=1)
+    assert np.all(np.abs(deq - h64) <= 0.5 * step * (1 + 1e-3) + 1e-3 * np.abs(h64) + 1e-12)
+    assert np.array_equal(hq, o.quantize(h))                          # the quantiser of x, applied to h
+
+
 # ------------------------------------------------------------------ top-2
 
 def _top2_by_sort(y):
