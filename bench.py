@@ -209,6 +209,43 @@ def build_verify(T, seed, dev, copies=4, keep_host=False, N=151936, K=1536):
     return wl
 
 
+def build_ffn(T, seed, dev, layers=28, d_model=1536, d_ff=8960, keep_host=False):
+    """The decode FFN of every layer: per layer one qgemv_q4_0_ffn call (gate
+    and up in one launch on the same fp32 x, the SiLU * up quantiser, down),
+    each layer with its own seeded weights and x."""
+    import torch
+    q = _q()
+    wl = Workload("qwen2.5-1.5b_ffn", T)
+    wl.Wg, wl.Wu, wl.Wd, wl.xs, wl.ys = [], [], [], [], []
+    for l in range(layers):
+        for lst, (N, K, k) in zip((wl.Wg, wl.Wu, wl.Wd), ((d_ff, d_model, 0), (d_ff, d_model, 1), (d_model, d_ff, 2))):
+            Wg = synth.q4_0_weights(seed, N, K, stream=(l, k))
+            lst.append(_upload_packed(q, torch, Wg, N, K, dev))
+            wl.w_bytes += Wg.nbytes
+        wl.xs.append(torch.from_numpy(synth.activations(seed, T, d_model, stream=(l,))).to(dev))
+        wl.ys.append(torch.empty((T, d_model), dtype=torch.float32, device=dev))
+    wl.ws = q.new_workspace(q.ffn_workspace_bytes(d_model, d_ff, T), dev)
+    wl.x_bytes = 4 * T * d_model * layers
+    wl.y_bytes = 4 * T * d_model * layers
+    wl.xq_bytes = (2 * q.xq_bytes(T, d_model) + q.xq_bytes(T, d_ff)) * layers
+    wl.n_gemv, wl.launches = 3 * layers, 3 * layers
+
+    def step(stream=None):
+        for l in range(layers):
+            q.ffn(wl.Wg[l], wl.Wu[l], wl.Wd[l], q.W_PACKED, wl.xs[l], d_model, d_ff, T, wl.ws, y=wl.ys[l],
+                  stream=stream)
+
+    wl.step, wl.kernel, wl.dominant = step, step, step
+    wl.dominant_bytes = wl.w_bytes + wl.x_bytes + wl.y_bytes
+    wl.other_launch = ("the whole step: per layer the gate/up and down streaming launches and the SiLU * up "
+                       "quantiser, whose bytes are 0.2 % of the step's")
+    wl.inputs, wl.outputs = list(wl.xs), list(wl.ys)
+    wl.config = {"workload": "qwen2.5-1.5b_ffn", "layers": layers, "d_model": d_model, "d_ff": d_ff, "T": T,
+                 "weight_bytes": wl.w_bytes, "step": "per layer: gate+up launch, SiLU(gate)*up to Q8_0, down launch",
+                 "l2_defeat": "weights larger than the 126 MB L2, each streamed once per step"}
+    return wl
+
+
 def build_q8(T, seed, dev, copies=2, keep_host=False, N=151936, K=1536):
     """The lm_head held as Q8_0 weights: one step quantises x and runs the
     Q8_0-weight GEMV (two launches); copies rotate so reads hit HBM."""
@@ -370,6 +407,9 @@ def build_workload(name: str, dev, T: int | None = None, keep_host: bool = False
         return build_lm_head(T or spec["T"], spec["seed"], dev, spec["copies"], keep_host, spec["N"], spec["K"])
     if spec["kind"] == "verify":
         return build_verify(T or spec["T"], spec["seed"], dev, spec["copies"], keep_host, spec["N"], spec["K"])
+    if spec["kind"] == "ffn":
+        return build_ffn(T or spec["T"], spec["seed"], dev, layers or spec["layers"], spec["d_model"], spec["d_ff"],
+                         keep_host)
     if spec["kind"] == "q8":
         return build_q8(T or spec["T"], spec["seed"], dev, spec["copies"], keep_host, spec["N"], spec["K"])
     if spec["kind"] == "single":
@@ -488,6 +528,10 @@ def _oracle_inputs(workload: str):
             mats = synth.layer_set(spec["layer"], spec["layers"])
         elif spec["kind"] in ("argmax", "single", "verify", "q8"):
             T, mats = spec["T"], [("w", spec["N"], spec["K"])]
+        elif spec["kind"] == "ffn":
+            T = spec["T"]
+            mats = [("gate", spec["d_ff"], spec["d_model"]), ("up", spec["d_ff"], spec["d_model"]),
+                    ("down", spec["d_model"], spec["d_ff"])] * spec["layers"]
         else:
             T = 1
             mats = [("gate", spec["d_ff"], spec["d_model"]), ("up", spec["d_ff"], spec["d_model"]),

@@ -232,6 +232,32 @@ size_t qgemv_q8_0_workspace_bytes(int64_t N, int64_t K, int T);
 qgemv_status qgemv_q8_0(const void *W, const void *xq, float *y, int64_t N, int64_t K, int T,
                         void *ws, size_t ws_bytes, qgemv_stream_t stream);
 
+/* ---- The FFN of a decode step (minfer README M15: the whole layer runs
+ * around its GEMVs; colibri qwen36 docs: gate and up share one pass over the
+ * activation):  y = W_down . Q8_0(SiLU(W_gate . x) * (W_up . x)).
+ * Three launches on `stream`, chained by programmatic dependent launch:
+ *   1. gate and up, one sequence launch over the same fp32 x[T][d_model]
+ *      (quantised inside the kernel; outputs g, u fp32 [T][d_ff] in ws);
+ *   2. h = SiLU(g) * u with SiLU(g) = g / (1 + exp(-g)), exp by Cody and
+ *      Waite's method (split ln 2, Taylor series to r^7/7!, exact 2^k), every
+ *      step an fp32 operation rounded to nearest in a fixed order; h is
+ *      quantised to planar Q8_0 exactly as qgemv_quantize_q8_0 would;
+ *   3. the down projection (d_model x d_ff) on those codes into y[T][d_model].
+ * W_gate, W_up: d_ff x d_model; W_down: d_model x d_ff; all in `layout`.
+ * ws: qgemv_ffn_workspace_bytes(d_model, d_ff, T) bytes, 256-byte aligned,
+ * zero-filled before its first use (left so).  y must not overlap x, W_down
+ * or ws. */
+size_t qgemv_ffn_workspace_bytes(int64_t d_model, int64_t d_ff, int T);
+qgemv_status qgemv_q4_0_ffn(const void *W_gate, const void *W_up, const void *W_down, qgemv_wlayout layout,
+                            const float *x, float *y, int64_t d_model, int64_t d_ff, int T,
+                            void *ws, size_t ws_bytes, qgemv_stream_t stream);
+
+/* Test hook: step 2 of qgemv_q4_0_ffn alone.  g, u fp32 [T][F]; hq receives
+ * T rows of F int8 codes then the [T][F/32] fp16 scales (16-byte aligned,
+ * qgemv_xq_bytes(T, F) bytes). */
+qgemv_status qgemv_debug_silu_mul_q8(const float *g, const float *u, void *hq, int T, int64_t F,
+                                     qgemv_stream_t stream);
+
 /* The lossless verify rule of speculative greedy decoding (minfer README
  * M17: a verify step runs [current, draft_1..draft_K] and commits up to and
  * including the first prediction that disagrees with its draft).

@@ -73,6 +73,9 @@ _SIGS = {
     "qgemv_q4_0_top2": ([_VP, _I32, _VP, _VP, _VP, _VP, _I64, _I64, _I32, _VP, _SZ, _VP], _I32),
     "qgemv_q4_0_top2_f32": ([_VP, _I32, _VP, _VP, _VP, _VP, _I64, _I64, _I32, _VP, _SZ, _VP], _I32),
     "qgemv_verify_commit": ([_VP, _VP, _I32, _I32, _VP, _VP], _I32),
+    "qgemv_ffn_workspace_bytes": ([_I64, _I64, _I32], _SZ),
+    "qgemv_q4_0_ffn": ([_VP, _VP, _VP, _I32, _VP, _VP, _I64, _I64, _I32, _VP, _SZ, _VP], _I32),
+    "qgemv_debug_silu_mul_q8": ([_VP, _VP, _VP, _I32, _I64, _VP], _I32),
     "qgemv_pack_q8_0": ([_VP, _VP, _I64, _I64, _VP], _I32),
     "qgemv_unpack_q8_0": ([_VP, _VP, _I64, _I64, _VP], _I32),
     "qgemv_q8_0_workspace_bytes": ([_I64, _I64, _I32], _SZ),
@@ -229,6 +232,25 @@ def verify_commit(tokens, pred, n_commit=None, stream=None):
     _check(lib().qgemv_verify_commit(_ptr(tokens), ctypes.c_void_p(pred.data_ptr()), pred.stride(0), T,
                                      _ptr(n_commit), _stream(stream)), "qgemv_verify_commit")
     return n_commit
+
+
+def ffn_workspace_bytes(d_model: int, d_ff: int, T: int) -> int:
+    return int(lib().qgemv_ffn_workspace_bytes(d_model, d_ff, T))
+
+
+def ffn(W_gate, W_up, W_down, layout: int, x, d_model: int, d_ff: int, T: int, ws, y=None, stream=None):
+    """y[T][d_model] = W_down . Q8_0(SiLU(W_gate . x) * (W_up . x)) for fp32 x[T][d_model]."""
+    y = y if y is not None else torch.empty((T, d_model), dtype=torch.float32, device=x.device)
+    _check(lib().qgemv_q4_0_ffn(_ptr(W_gate), _ptr(W_up), _ptr(W_down), layout, _ptr(x), _ptr(y), d_model, d_ff, T,
+                                _ptr(ws), ws.numel(), _stream(stream)), "qgemv_q4_0_ffn")
+    return y
+
+
+def silu_mul_q8(g, u, T: int, F: int, hq=None, stream=None):
+    """Test hook: planar Q8_0 codes of SiLU(g) * u (g, u fp32 [T][F])."""
+    hq = hq if hq is not None else torch.empty(xq_bytes(T, F), dtype=torch.uint8, device=g.device)
+    _check(lib().qgemv_debug_silu_mul_q8(_ptr(g), _ptr(u), _ptr(hq), T, F, _stream(stream)), "qgemv_debug_silu_mul_q8")
+    return hq
 
 
 def q8_0_bytes(N: int, K: int) -> int:

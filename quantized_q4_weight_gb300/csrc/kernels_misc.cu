@@ -176,6 +176,84 @@ cudaError_t launch_isums(const void *W, bool packed, const void *xq, int32_t *is
     return cudaGetLastError();
 }
 
+// ------------------------------------------------------------ FFN step
+//
+// h = SiLU(g) * u, quantised to planar Q8_0 for the down projection (minfer
+// README M15: the FFN between the GEMVs of a decode step).  exp by Cody and
+// Waite's method (W. J. Cody, W. Waite, "Software Manual for the Elementary
+// Functions", 1980): x = k ln2 + r, k = rint(x log2 e), ln 2 split into a
+// head whose products with k are exact and a tail; exp(r) by its Taylor
+// series to r^7/7! in Horner form; the exact scale 2^k.  x is clamped to
+// [-87, 88].  Every operation is an explicitly rounded fp32 one, in the
+// order written, so the values (and so the codes) are a fixed function of
+// g and u.
+__device__ __forceinline__ float ffn_exp(float x)
+{
+    x = fminf(fmaxf(x, -87.0f), 88.0f);
+    const float k = rintf(__fmul_rn(x, 1.44269504088896340736f));
+    float r = __fmaf_rn(-k, 0.693145751953125f, x);   // ln 2 head: 13 significant bits
+    r = __fmaf_rn(-k, 1.42860682030941723212e-6f, r);  // ln 2 - head
+    float p = 1.0f / 5040.0f;
+    p = __fmaf_rn(p, r, 1.0f / 720.0f);
+    p = __fmaf_rn(p, r, 1.0f / 120.0f);
+    p = __fmaf_rn(p, r, 1.0f / 24.0f);
+    p = __fmaf_rn(p, r, 1.0f / 6.0f);
+    p = __fmaf_rn(p, r, 0.5f);
+    p = __fmaf_rn(p, r, 1.0f);
+    p = __fmaf_rn(p, r, 1.0f);
+    return __fmul_rn(p, __int_as_float((static_cast<int>(k) + 127) << 23));
+}
+
+__device__ __forceinline__ float ffn_silu(float g) { return __fdiv_rn(g, __fadd_rn(1.0f, ffn_exp(-g))); }
+
+// One warp per block of 32: h for lane j, the block maximum by shuffles, then
+// the Q8_0 steps of the activation quantiser.  hq: T rows of F codes, then
+// [T][F/32] fp16 scales, zero-padded like qgemv_quantize_q8_0's output.
+__global__ void __launch_bounds__(256) silu_mul_q8_kernel(const float *__restrict__ g, const float *__restrict__ u,
+                                                          uint8_t *__restrict__ hq, int T, int F, long long nblocks,
+                                                          long long hq_bytes)
+{
+    pdl_wait();
+    pdl_launch_dependents();
+    const int lane = threadIdx.x & 31;
+    const int nb = F / QK;
+    for (long long blk = (blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x) >> 5; blk < nblocks;
+         blk += (static_cast<long long>(gridDim.x) * blockDim.x) >> 5) {
+        const int t = static_cast<int>(blk / nb), b = static_cast<int>(blk - static_cast<long long>(t) * nb);
+        const long long e = static_cast<long long>(t) * F + b * QK + lane;
+        const float h = __fmul_rn(ffn_silu(__ldg(g + e)), __ldg(u + e));
+        float amax = fabsf(h);
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
+        float d, id;
+        q8_scale(amax, d, id);
+        hq[e] = static_cast<uint8_t>(static_cast<int8_t>(q8_code(h, id)));
+        if (lane == 0) reinterpret_cast<unsigned short *>(hq + static_cast<long long>(T) * F)[blk] = q8_half(d);
+        if (blk == 0) {  // zero the padding after the scales
+            const long long used = static_cast<long long>(T) * F + 2ll * T * nb;
+            if (used + lane < hq_bytes) hq[used + lane] = 0;
+        }
+    }
+}
+
+cudaError_t launch_silu_mul_q8(const float *g, const float *u, void *hq, int T, long long F, bool pdl, cudaStream_t st)
+{
+    const long long nblocks = static_cast<long long>(T) * (F / QK);
+    long long grid = (nblocks + 7) / 8;
+    if (grid > 65535) grid = 65535;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    return cudaLaunchKernelEx(&cfg, silu_mul_q8_kernel, g, u, static_cast<uint8_t *>(hq), T, static_cast<int>(F),
+                              nblocks, static_cast<long long>(xq_bytes_host(T, F)));
+}
+
 // The lossless verify rule (minfer README M17): tokens[0] is the step's
 // current token, tokens[1..T-1] its drafts, pred[t] the greedy prediction
 // after tokens[0..t] (at pred[t * pred_stride]).  The step commits pred[0] and each later prediction

@@ -643,6 +643,68 @@ qgemv_status qgemv_q8_0(const void *W, const void *xq, float *y, int64_t N, int6
     return e == cudaSuccess ? QGEMV_OK : QGEMV_ERR_CUDA;
 }
 
+// ------------------------------------------------------------ FFN step
+
+// Workspace of qgemv_q4_0_ffn: [gate/up sequence][g][u][h codes][down call],
+// each part 256-byte aligned; off[0..4] the parts' offsets.  0: bad shape.
+static long long ffn_parts(int64_t d_model, int64_t d_ff, int T, long long off[5])
+{
+    if (!shape_ok(d_ff, d_model) || !shape_ok(d_model, d_ff) || T < 1 || T > 8) return 0;
+    const qgemv_seq_item it[2] = {{nullptr, nullptr, nullptr, d_ff, d_model}, {nullptr, nullptr, nullptr, d_ff, d_model}};
+    off[0] = 0;
+    off[1] = align_up(static_cast<long long>(qgemv_seq_workspace_bytes(it, 2, T)), 256);
+    off[2] = off[1] + align_up(4ll * T * d_ff, 256);
+    off[3] = off[2] + align_up(4ll * T * d_ff, 256);
+    off[4] = off[3] + align_up(xq_bytes_host(T, d_ff), 256);
+    return off[4] + align_up(static_cast<long long>(qgemv_workspace_bytes(d_model, d_ff, T)), 256);
+}
+
+size_t qgemv_ffn_workspace_bytes(int64_t d_model, int64_t d_ff, int T)
+{
+    long long off[5];
+    return static_cast<size_t>(ffn_parts(d_model, d_ff, T, off));
+}
+
+qgemv_status qgemv_debug_silu_mul_q8(const float *g, const float *u, void *hq, int T, int64_t F, qgemv_stream_t stream)
+{
+    if (T < 1 || T > 8 || !shape_ok(1, F) || !g || !u || !hq) return QGEMV_ERR_INVALID_ARG;
+    if (!aligned(g, 4) || !aligned(u, 4) || !aligned(hq, 16)) return QGEMV_ERR_MISALIGNED;
+    const Range rh = range(hq, xq_bytes_host(T, F));
+    if (overlap(rh, range(g, 4ll * T * F)) || overlap(rh, range(u, 4ll * T * F))) return QGEMV_ERR_INVALID_ARG;
+    return launch_silu_mul_q8(g, u, hq, T, F, false, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? QGEMV_OK
+               : QGEMV_ERR_CUDA;
+}
+
+qgemv_status qgemv_q4_0_ffn(const void *W_gate, const void *W_up, const void *W_down, qgemv_wlayout layout,
+                            const float *x, float *y, int64_t d_model, int64_t d_ff, int T, void *ws,
+                            size_t ws_bytes, qgemv_stream_t stream)
+{
+    long long off[5];
+    const long long need = ffn_parts(d_model, d_ff, T, off);
+    if (need == 0 || !W_gate || !W_up || !W_down || !x || !y) return QGEMV_ERR_INVALID_ARG;
+    if (layout != QGEMV_W_GGML && layout != QGEMV_W_PACKED) return QGEMV_ERR_INVALID_ARG;
+    if (!aligned(x, 4) || !aligned(y, 4)) return QGEMV_ERR_MISALIGNED;
+    if (!ws) return QGEMV_ERR_WORKSPACE;
+    if (!aligned(ws, 256)) return QGEMV_ERR_MISALIGNED;
+    if (static_cast<long long>(ws_bytes) < need) return QGEMV_ERR_WORKSPACE;
+    const Range ry = range(y, 4ll * T * d_model), rw = range(ws, need);
+    if (overlap(ry, rw) || overlap(ry, range(x, 4ll * T * d_model)) || overlap(range(x, 4ll * T * d_model), rw) ||
+        overlap(ry, range(W_down, 18ll * d_model * (d_ff / QK))))
+        return QGEMV_ERR_INVALID_ARG;
+    uint8_t *w = static_cast<uint8_t *>(ws);
+    float *g = reinterpret_cast<float *>(w + off[1]);
+    float *u = reinterpret_cast<float *>(w + off[2]);
+    void *hq = w + off[3];
+    // gate and up: one sequence launch over the same fp32 x (quantised in the kernel)
+    const qgemv_seq_f32_item gu[2] = {{W_gate, x, g, d_ff, d_model}, {W_up, x, u, d_ff, d_model}};
+    qgemv_status s = qgemv_q4_0_seq_f32(gu, 2, layout, T, w + off[0], static_cast<size_t>(off[1]), stream);
+    if (s != QGEMV_OK) return s;
+    if (launch_silu_mul_q8(g, u, hq, T, d_ff, true, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
+        return QGEMV_ERR_CUDA;
+    return qgemv_q4_0(W_down, layout, hq, y, d_model, d_ff, T, w + off[4], static_cast<size_t>(need - off[4]), stream);
+}
+
 qgemv_status qgemv_verify_commit(const int64_t *tokens, const int64_t *pred, int pred_stride, int T,
                                  int32_t *n_commit, qgemv_stream_t stream)
 {

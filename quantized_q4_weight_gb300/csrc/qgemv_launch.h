@@ -28,6 +28,7 @@ cudaError_t launch_q8_pack(const void *src, void *dst, long long N, long long K,
 cudaError_t launch_q8(const void *W, const void *xq, float *y, long long N, long long K, int T, void *ws,
                       long long ws_bytes, bool do_launch, int sms, int smem_budget, unsigned *status,
                       cudaStream_t st, long long *ws_need, int *unsupported);
+cudaError_t launch_silu_mul_q8(const float *g, const float *u, void *hq, int T, long long F, bool pdl, cudaStream_t st);
 cudaError_t launch_verify_commit(const long long *tokens, const long long *pred, int pred_stride, int T,
                                  int32_t *n_commit, cudaStream_t st);
 

@@ -116,6 +116,9 @@ WORKLOADS = {
     # lm_head verify step: 8 positions (current token + 7 drafts), top-2 rows
     # per position, then the commit rule; 4 weight copies in rotation
     "lm_head_top2_verify": dict(kind="verify", N=151936, K=1536, T=8, copies=4, seed=2100),
+    # the decode FFN of the 28 Qwen2.5-1.5B layers: gate and up 8960x1536 on
+    # the same x, SiLU(gate) * up quantised to Q8_0, down 1536x8960; T=1
+    "qwen2.5-1.5b_ffn": dict(kind="ffn", d_model=1536, d_ff=8960, layers=28, T=1, seed=5000),
     # the lm_head held as Q8_0 weights (248 MB per copy), T=1, 2 copies in rotation
     "q8_lm_head": dict(kind="q8", N=151936, K=1536, T=1, copies=2, seed=2200),
     # 36-layer Qwen2.5-3B-shaped layer set, T in {1,2,4,8}
