@@ -171,8 +171,8 @@ def build_lm_head(T, seed, dev, copies=4, keep_host=False, N=151936, K=1536):
 
 def build_verify(T, seed, dev, copies=4, keep_host=False, N=151936, K=1536):
     """A speculative verify step on the lm_head: T positions (the current
-    token and T-1 drafts) through the fp32-input top-2 GEMV, then the commit
-    rule on the first rows.  Two launches per step."""
+    token and T-1 drafts) through the fp32-input top-2 GEMV, with the commit
+    rule on the first rows applied by the same launch."""
     import torch
     q = _q()
     wl = build_lm_head(T, seed, dev, copies, keep_host, N, K)
@@ -183,28 +183,22 @@ def build_verify(T, seed, dev, copies=4, keep_host=False, N=151936, K=1536):
     rng = np.random.default_rng(seed + 7)          # seeded synthetic drafts
     wl.tokens = torch.from_numpy(rng.integers(0, N, T).astype(np.int64)).to(dev)
     wl.y_bytes = 24 * T + 4                         # idx2, val2, committed count
-    wl.launches = 2
+    wl.launches = 1
     wl.copy = 0
 
     def kernel(stream=None):
         q.gemv_top2(wl.W[wl.copy], q.W_PACKED, wl.xqb, N, K, T, wl.ws, idx2=wl.idx2, val2=wl.val2, stream=stream)
         wl.copy = (wl.copy + 1) % copies
 
-    def step(stream=None):
-        q.gemv_top2_f32(wl.W[wl.copy], q.W_PACKED, wl.x, N, K, T, wl.ws, idx2=wl.idx2, val2=wl.val2, stream=stream)
-        q.verify_commit(wl.tokens, wl.idx2[:, 0], n_commit=wl.n_commit, stream=stream)
+    def step(stream=None):  # one launch: top-2 rows and the commit rule
+        q.verify_f32(wl.W[wl.copy], q.W_PACKED, wl.x, wl.tokens, N, K, T, wl.ws, idx2=wl.idx2, val2=wl.val2,
+                     n_commit=wl.n_commit, stream=stream)
         wl.copy = (wl.copy + 1) % copies
 
-    def dominant(stream=None):  # the step's streaming launch (fp32 x, top-2 out)
-        q.gemv_top2_f32(wl.W[wl.copy], q.W_PACKED, wl.x, N, K, T, wl.ws, idx2=wl.idx2, val2=wl.val2, stream=stream)
-        wl.copy = (wl.copy + 1) % copies
-
-    wl.step, wl.kernel, wl.dominant = step, kernel, dominant
-    wl.dominant_bytes = wl.w_bytes + wl.x_bytes + 24 * T
-    wl.other_launch = "the step's other launch is the one-warp commit rule"
+    wl.step, wl.kernel = step, kernel
     wl.inputs, wl.outputs = [wl.x, wl.tokens], [wl.idx2, wl.val2, wl.n_commit]
     wl.config = {"workload": "lm_head_top2_verify", "N": N, "K": K, "T": T, "copies": copies,
-                 "step": "top-2 lm_head GEMV on fp32 x (quantised in the kernel), then the commit rule",
+                 "step": "top-2 lm_head GEMV on fp32 x (quantised in the kernel) and the commit rule, one launch",
                  "l2_defeat": f"{copies} weight copies in rotation ({copies * wl.w_bytes / 1e6:.0f} MB)"}
     return wl
 

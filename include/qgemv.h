@@ -258,6 +258,17 @@ qgemv_status qgemv_q4_0_ffn(const void *W_gate, const void *W_up, const void *W_
 qgemv_status qgemv_debug_silu_mul_q8(const float *g, const float *u, void *hq, int T, int64_t F,
                                      qgemv_stream_t stream);
 
+/* A whole verify step in one launch: qgemv_q4_0_top2_f32 (without logits)
+ * followed by the verify rule on its first rows, applied by the kernel's
+ * last CTA after the final merge: *n_commit receives what
+ * qgemv_verify_commit(tokens, idx2, 2, T, n_commit) would write.  tokens
+ * (int64 [T], device) as in qgemv_verify_commit; n_commit (int32, device)
+ * must not overlap the other buffers. */
+qgemv_status qgemv_q4_0_verify_f32(const void *W, qgemv_wlayout layout, const float *x,
+                                   const int64_t *tokens, int64_t *idx2, float *val2,
+                                   int32_t *n_commit, int64_t N, int64_t K, int T, void *ws,
+                                   size_t ws_bytes, qgemv_stream_t stream);
+
 /* The lossless verify rule of speculative greedy decoding (minfer README
  * M17: a verify step runs [current, draft_1..draft_K] and commits up to and
  * including the first prediction that disagrees with its draft).

@@ -73,6 +73,7 @@ _SIGS = {
     "qgemv_q4_0_top2": ([_VP, _I32, _VP, _VP, _VP, _VP, _I64, _I64, _I32, _VP, _SZ, _VP], _I32),
     "qgemv_q4_0_top2_f32": ([_VP, _I32, _VP, _VP, _VP, _VP, _I64, _I64, _I32, _VP, _SZ, _VP], _I32),
     "qgemv_verify_commit": ([_VP, _VP, _I32, _I32, _VP, _VP], _I32),
+    "qgemv_q4_0_verify_f32": ([_VP, _I32, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I32, _VP, _SZ, _VP], _I32),
     "qgemv_ffn_workspace_bytes": ([_I64, _I64, _I32], _SZ),
     "qgemv_q4_0_ffn": ([_VP, _VP, _VP, _I32, _VP, _VP, _I64, _I64, _I32, _VP, _SZ, _VP], _I32),
     "qgemv_debug_silu_mul_q8": ([_VP, _VP, _VP, _I32, _I64, _VP], _I32),
@@ -219,6 +220,18 @@ def gemv_top2_f32(W, layout: int, x, N: int, K: int, T: int, ws, y=None, idx2=No
     _check(lib().qgemv_q4_0_top2_f32(_ptr(W), layout, _ptr(x), _ptr(y), _ptr(idx2), _ptr(val2), N, K, T, _ptr(ws),
                                      ws.numel(), _stream(stream)), "qgemv_q4_0_top2_f32")
     return idx2, val2
+
+
+def verify_f32(W, layout: int, x, tokens, N: int, K: int, T: int, ws, idx2=None, val2=None, n_commit=None,
+               stream=None):
+    """A verify step in one launch: the top-2 rows of W . x per position and the
+    committed count of the verify rule on (tokens, idx2[:, 0])."""
+    idx2 = idx2 if idx2 is not None else torch.empty((T, 2), dtype=torch.int64, device=W.device)
+    val2 = val2 if val2 is not None else torch.empty((T, 2), dtype=torch.float32, device=W.device)
+    n_commit = n_commit if n_commit is not None else torch.empty(1, dtype=torch.int32, device=W.device)
+    _check(lib().qgemv_q4_0_verify_f32(_ptr(W), layout, _ptr(x), _ptr(tokens), _ptr(idx2), _ptr(val2), _ptr(n_commit),
+                                       N, K, T, _ptr(ws), ws.numel(), _stream(stream)), "qgemv_q4_0_verify_f32")
+    return idx2, val2, n_commit
 
 
 def verify_commit(tokens, pred, n_commit=None, stream=None):

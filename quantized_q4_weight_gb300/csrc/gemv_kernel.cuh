@@ -1310,6 +1310,7 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
     __shared__ int s_grp[MAX_RUNS + 1];  // first run of each group, then the run count
     __shared__ long long s_i0, s_i1;     // the CTA's item range
     __shared__ unsigned long long s_best[ARGMAX ? max_warps_for(T, MMA) * T * 2 : 1];  // [warp][t][2]
+    __shared__ long long s_pred[ARGMAX ? T : 1];  // verify: the step's predictions
 
     __shared__ ParamHead H;              // the scalar launch parameters
 
@@ -1850,6 +1851,17 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
                     H.am_idx2[2 * tid + 1] = key_row(m2);
                     H.am_val2[2 * tid] = key_value(m1);
                     H.am_val2[2 * tid + 1] = key_value(m2);
+                }
+                if (H.vc_tokens != nullptr) s_pred[tid] = key_row(m1);
+            }
+            if (H.vc_tokens != nullptr) {
+                // the verify rule on this step's predictions (minfer README M17): commit
+                // pred[0] and each later one while every draft equalled the prediction before it
+                __syncthreads();
+                if (tid == 0) {
+                    int n = 1;
+                    while (n < T && H.vc_tokens[n] == s_pred[n - 1]) ++n;
+                    *H.vc_n = n;
                 }
             }
             if (tid == 0) *H.am_cnt = 0u;

@@ -382,7 +382,8 @@ long long single_ws_bytes(long long N, long long K, int T)
 
 qgemv_status run_single(const void *W, qgemv_wlayout layout, const void *xq, float *y, long long *idx, long long N,
                         long long K, int T, void *ws, size_t ws_bytes, cudaStream_t st, bool argmax, bool pdl,
-                        bool xf32 = false, long long *idx2 = nullptr, float *val2 = nullptr)
+                        bool xf32 = false, long long *idx2 = nullptr, float *val2 = nullptr,
+                        const long long *vc_tokens = nullptr, int *vc_n = nullptr)
 {
     DevInfo dev;
     qgemv_status s = device_info(dev);
@@ -398,6 +399,8 @@ qgemv_status run_single(const void *W, qgemv_wlayout layout, const void *xq, flo
     pl.P.am_idx = reinterpret_cast<long long *>(idx);
     pl.P.am_idx2 = idx2;
     pl.P.am_val2 = val2;
+    pl.P.vc_tokens = vc_tokens;
+    pl.P.vc_n = vc_n;
     const int grid = grid_for(dev, cps);
     set_cta_groups(pl.P, grid);
     const cudaError_t e = argmax ? dispatch_T<MAXG_SMALL, true>(pl.P, T, mma_for(T), grid, pl.smem, st, pdl)
@@ -547,7 +550,7 @@ qgemv_status qgemv_q4_0_argmax_f32(const void *W, qgemv_wlayout layout, const fl
 // outputs in place of idx.
 static qgemv_status top2_call(const void *W, qgemv_wlayout layout, const void *xin, bool xf32, float *y_or_null,
                               int64_t *idx2, float *val2, int64_t N, int64_t K, int T, void *ws, size_t ws_bytes,
-                              qgemv_stream_t stream)
+                              qgemv_stream_t stream, const int64_t *tokens = nullptr, int32_t *n_commit = nullptr)
 {
     const long long xin_bytes = !shape_ok(N, K) ? 0 : xf32 ? 4ll * T * K : xq_bytes_host(T, K);
     qgemv_status s = check_single(W, layout, xin, xin_bytes, y_or_null, N, K, T, ws);
@@ -566,9 +569,17 @@ static qgemv_status top2_call(const void *W, qgemv_wlayout layout, const void *x
         const Range rx = range(xin, xin_bytes);
         if (overlap(rx, rw) || overlap(rx, ri) || overlap(rx, rv)) return QGEMV_ERR_INVALID_ARG;
     }
+    if (tokens || n_commit) {
+        if (!tokens || !n_commit) return QGEMV_ERR_INVALID_ARG;
+        if (!aligned(tokens, 8) || !aligned(n_commit, 4)) return QGEMV_ERR_MISALIGNED;
+        const Range rn = range(n_commit, 4);
+        if (overlap(rn, rw) || overlap(rn, ri) || overlap(rn, rv) || overlap(rn, range(tokens, 8ll * T)) ||
+            (y_or_null && overlap(rn, range(y_or_null, 4ll * T * N))))
+            return QGEMV_ERR_INVALID_ARG;
+    }
     return run_single(W, layout, xin, y_or_null, nullptr, N, K, T, ws, ws_bytes,
                       reinterpret_cast<cudaStream_t>(stream), true, true, xf32, reinterpret_cast<long long *>(idx2),
-                      val2);
+                      val2, reinterpret_cast<const long long *>(tokens), n_commit);
 }
 
 qgemv_status qgemv_q4_0_top2(const void *W, qgemv_wlayout layout, const void *xq, float *y_or_null, int64_t *idx2,
@@ -703,6 +714,13 @@ qgemv_status qgemv_q4_0_ffn(const void *W_gate, const void *W_up, const void *W_
     if (launch_silu_mul_q8(g, u, hq, T, d_ff, true, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return QGEMV_ERR_CUDA;
     return qgemv_q4_0(W_down, layout, hq, y, d_model, d_ff, T, w + off[4], static_cast<size_t>(need - off[4]), stream);
+}
+
+qgemv_status qgemv_q4_0_verify_f32(const void *W, qgemv_wlayout layout, const float *x, const int64_t *tokens,
+                                  int64_t *idx2, float *val2, int32_t *n_commit, int64_t N, int64_t K, int T,
+                                  void *ws, size_t ws_bytes, qgemv_stream_t stream)
+{
+    return top2_call(W, layout, x, true, nullptr, idx2, val2, N, K, T, ws, ws_bytes, stream, tokens, n_commit);
 }
 
 qgemv_status qgemv_verify_commit(const int64_t *tokens, const int64_t *pred, int pred_stride, int T,

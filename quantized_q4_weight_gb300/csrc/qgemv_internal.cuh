@@ -76,6 +76,8 @@ struct ParamHead {
     long long *am_idx;            // argmax: result [T] (or nullptr)
     long long *am_idx2;           // top-2: rows [T][2] (or nullptr)
     float *am_val2;               // top-2: values [T][2] (with am_idx2)
+    const long long *vc_tokens;   // verify: the step's tokens [T] (or nullptr)
+    int *vc_n;                    // verify: committed predictions (with vc_tokens)
     unsigned *status;             // per-device status word
 };
 

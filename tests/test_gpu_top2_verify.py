@@ -189,3 +189,25 @@ def test_verify_step_on_the_lm_head(orc):
         assert int(n.item()) == (k + 1 if k + 1 < T else T)
         assert int(n.item()) == orc.verify_commit(tokens.cpu().numpy(), pred.cpu().numpy())
     assert torch.all(val2[:, 0] >= val2[:, 1])
+
+
+@pytest.mark.parametrize("T", [1, 3, 8])
+def test_verify_in_one_launch(orc, T):
+    """qgemv_q4_0_verify_f32 (top-2 and the rule in one launch) gives the
+    rows, values and committed count of top2_f32 followed by verify_commit."""
+    N, K = 20000, 1536
+    Wg, W, x, xd, xq = setup(90 + T, N, K, T)
+    ws = ws_for(N, K, T)
+    i_ref, v_ref = q.gemv_top2_f32(W, q.W_PACKED, xd, N, K, T, ws)
+    pred = i_ref[:, 0].contiguous()
+    n_ref = torch.empty(1, dtype=torch.int32, device=DEV)
+    for k in range(T):
+        tokens = torch.cat([torch.tensor([5], dtype=torch.int64, device=DEV), pred[:-1]])
+        if k + 1 < T:
+            tokens[k + 1] = (pred[k] + 7) % N            # the draft after position k disagrees
+        i2, v2, n = q.verify_f32(W, q.W_PACKED, xd, tokens, N, K, T, ws)
+        q.verify_commit(tokens, pred, n_commit=n_ref)
+        assert torch.equal(i2.cpu(), i_ref.cpu())
+        assert torch.equal(v2.cpu().view(torch.int32), v_ref.cpu().view(torch.int32))
+        assert int(n.item()) == int(n_ref.item()) == orc.verify_commit(tokens.cpu().numpy(), pred.cpu().numpy())
+    assert q.device_status() == 0
