@@ -313,7 +313,11 @@ typedef struct {
     int64_t K;
 } qgemv_seq_item;
 
-/* Workspace bytes for qgemv_q4_0_seq on this list (0 if invalid). */
+/* Workspace bytes for qgemv_q4_0_seq on this list (0 if invalid).  From
+ * T = 5 on (tensor-core path) this includes one region of segment sums per
+ * CTA of this device, which lets all warps of a CTA share a matrix piece of
+ * fewer slabs than warps; a workspace with fewer regions (down to the 16 KB
+ * counter area that an unsplit list needs) gives the same bits, more slowly. */
 size_t qgemv_seq_workspace_bytes(const qgemv_seq_item *items, int n, int T);
 
 /* Run n GEMVs (host array `items`, read during the call only) in list order

@@ -1313,6 +1313,9 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
     __shared__ long long s_pred[ARGMAX ? T : 1];  // verify: the step's predictions
 
     __shared__ ParamHead H;              // the scalar launch parameters
+    // small groups spread over all warps: sequence launches on the
+    // tensor-core path only (the int8 path's groups are rarely that small)
+    constexpr bool SMALL_GROUPS = MMA && !ARGMAX && MAXG == MAXG_SEQ;
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     // One round of parallel parameter reads into shared memory: the scalar
@@ -1469,7 +1472,17 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
             // group holds whole slabs, so one warp always qualifies)
             int nseg_max = 1;
             for (int r = rg0; r < rg1; ++r) nseg_max = max(nseg_max, runs[r].nseg);
-            const int nwg = max(1, min(nw, S / nseg_max));
+            // a small group (one run of fewer whole slabs than warps, e.g. a
+            // few slabs of a projection whose activations need shared memory
+            // alone): every warp takes an equal range of its stages, writes
+            // each segment sum to this CTA's workspace region, and after a
+            // barrier the CTA adds them per output in segment order
+            const bool small_grp = SMALL_GROUPS && !ggml && H.sg_part != nullptr && static_cast<int>(blockIdx.x) < H.sg_ctas &&
+                                   rg1 - rg0 == 1 &&
+                                   runs[rg0].nstages < nw * runs[rg0].nseg && !runs[rg0].bad &&
+                                   runs[rg0].first_local + runs[rg0].nstages / runs[rg0].nseg <= runs[rg0].nslabs &&
+                                   runs[rg0].nstages * T * 16 <= H.sg_stride;
+            const int nwg = small_grp ? min(nw, S) : max(1, min(nw, S / nseg_max));
             const int a = warp < nwg ? S0 + static_cast<int>(static_cast<unsigned>(S) * warp / nwg) : S1;
             const int b = warp < nwg ? S0 + static_cast<int>(static_cast<unsigned>(S) * (warp + 1) / nwg) : S1;
             // boundary items: is stage p inside (not at the start of) an item?
@@ -1479,11 +1492,11 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
                 return p - (p - runs[r].stage0) % runs[r].nseg;
             };
             int head_b = b, tail_e = a;
-            if (b < S1 && b > a) {
+            if (!small_grp && b < S1 && b > a) {
                 const int st = item_start(b);
                 if (st != b) head_b = st;  // [st, b) is the head of an item continued by warp + 1
             }
-            if (a > S0 && a < b) {
+            if (!small_grp && a > S0 && a < b) {
                 const int st = item_start(a);
                 if (st != a) {
                     int r = rg0;
@@ -1575,7 +1588,7 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
                 float yv[NO];
     #pragma unroll
                 for (int k = 0; k < NO; ++k) yv[k] = 0.0f;
-                if (s_first > 0) {
+                if (s_first > 0 && !small_grp) {
                     // tail of a slab begun by warp - 1: continue from its ordered sum
                     if (lane == 0) wait_flag(&hflag[warp - 1], abort_flag, H.status);
                     __syncwarp();
@@ -1615,10 +1628,22 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
     #pragma unroll
                         for (int k = 0; k < NO; ++k) Pk[k] = 0.0f;
                     }
+                    if (small_grp) {  // the segment sum, for the CTA's ordered fold below
+                        // (the region's base is re-read from shared memory: no register holds it)
+                        float *pb = *reinterpret_cast<float *volatile *>(&H.sg_part) +
+                                    static_cast<long long>(blockIdx.x) * H.sg_stride +
+                                    ((li - w.first_local) * w.nseg + sg) * T * 16;
+    #pragma unroll
+                        for (int k = 0; k < NO; ++k)
+                            if (LO::owner(k, j)) pb[LO::tok(k, j) * 16 + LO::row(k, r8)] = Pk[k];
+                        continue;
+                    }
     #pragma unroll
                     for (int k = 0; k < NO; ++k) yv[k] = (sg == 0) ? Pk[k] : __fadd_rn(yv[k], Pk[k]);
                 }
-                if (seg_end < w.nseg) {
+                if (small_grp) {
+                    // outputs come from the fold after the group
+                } else if (seg_end < w.nseg) {
                     // head of a slab that warp + 1 finishes: leave the ordered sum
                     float *H = hbuf + warp * T * 16;
     #pragma unroll
@@ -1633,6 +1658,21 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
                     atomicCAS(H.status, 0u, ST_BAD_ID);
                 }
                 w.next_item(runs);
+            }
+            if (small_grp) {
+                // every segment sum of the group is written: add them per
+                // output (slab, token, row) in segment order
+                __syncthreads();
+                const RunInfo &R = runs[rg0];
+                const int nsl = R.nstages / R.nseg;
+                const float *pr = H.sg_part + static_cast<long long>(blockIdx.x) * H.sg_stride;
+                for (int o = tid; o < nsl * T * 16; o += nthreads) {
+                    const int sl = o / (T * 16), t = (o / 16) % T, row = o % 16;
+                    const float *p = pr + static_cast<long long>(sl) * R.nseg * T * 16 + t * 16 + row;
+                    float v = p[0];
+                    for (int sg = 1; sg < R.nseg; ++sg) v = __fadd_rn(v, p[static_cast<long long>(sg) * T * 16]);
+                    R.y[static_cast<long long>(t) * R.N + (R.first_local + sl) * SLAB_ROWS + row] = v;
+                }
             }
         }
     } else {

@@ -734,6 +734,28 @@ qgemv_status qgemv_verify_commit(const int64_t *tokens, const int64_t *pred, int
                : QGEMV_ERR_CUDA;
 }
 
+// Small groups of a tensor-core sequence launch (a CTA's share of one
+// matrix, fewer whole slabs than warps, alone in shared memory) are spread
+// over all warps when the workspace holds a region of segment sums for the
+// CTA: up to
+// NWARPS_MAX - 1 slabs of the launch's longest rows.  Without it they run one
+// slab per warp; the results are the same bits either way.
+inline long long sg_stride_floats(const GroupSpec *gs, int n, int T)
+{
+    long long nseg_max = 1;
+    for (int i = 0; i < n; ++i) nseg_max = std::max(nseg_max, (gs[i].K / QK + SEG_BLOCKS - 1) / SEG_BLOCKS);
+    return (NWARPS_MAX - 1) * nseg_max * T * 16;
+}
+
+// CTAs of a sequence launch given a small-group region by the workspace size
+// below: the grid on this device, else one CTA on each of 152 SMs.
+inline long long sg_ctas_hint(int T)
+{
+    DevInfo dev;
+    if (device_info(dev) != QGEMV_OK) return 152;
+    return grid_for(dev, ctas_per_sm_for(T, true));
+}
+
 size_t qgemv_seq_workspace_bytes(const qgemv_seq_item *items, int n, int T)
 {
     if (!items || n < 1 || T < 1 || T > 8) return 0;
@@ -749,7 +771,8 @@ size_t qgemv_seq_workspace_bytes(const qgemv_seq_item *items, int n, int T)
         std::unique_ptr<Plan<MAXG_SEQ>> pa(new Plan<MAXG_SEQ>()), pb(new Plan<MAXG_SEQ>());
         make_plan<MAXG_SEQ>(gs.data(), cn, T, false, false, nullptr, 0, *pa);
         make_plan<MAXG_SEQ>(gs.data(), cn, T, true, false, nullptr, 0, *pb);
-        const long long b = pa->ws_bytes > pb->ws_bytes ? pa->ws_bytes : pb->ws_bytes;
+        long long b = pa->ws_bytes > pb->ws_bytes ? pa->ws_bytes : pb->ws_bytes;
+        if (pa->P.balanced_ok && mma_for(T)) b = align_up(b, 256) + sg_ctas_hint(T) * sg_stride_floats(gs.data(), cn, T) * 4;
         if (b > total) total = b;  // consecutive launches reuse the workspace
     }
     return static_cast<size_t>(total);
@@ -815,6 +838,16 @@ static qgemv_status launch_seq(const qgemv_seq_item *items, int n, qgemv_wlayout
         if (static_cast<long long>(ws_bytes) < pl->ws_bytes) return QGEMV_ERR_WORKSPACE;
         pl->P.status = dev.status;
         pl->P.xf32 = xf32 ? 1 : 0;
+        if (pl->P.balanced_ok && layout != QGEMV_W_GGML && mma_for(T)) {
+            const long long off = align_up(pl->ws_bytes, 256), stride = sg_stride_floats(gs.data(), cn, T);
+            const long long room = static_cast<long long>(ws_bytes) - off;
+            const long long nc = room > 0 ? std::min<long long>(grid, room / (stride * 4)) : 0;
+            if (nc > 0 && stride <= INT32_MAX) {
+                pl->P.sg_part = reinterpret_cast<float *>(static_cast<uint8_t *>(ws) + off);
+                pl->P.sg_stride = static_cast<int>(stride);
+                pl->P.sg_ctas = static_cast<int>(nc);
+            }
+        }
         set_cta_groups(pl->P, grid);
         if (dispatch_T<MAXG_SEQ, false>(pl->P, T, mma_for(T), grid, pl->smem, st, true) != cudaSuccess)
             return QGEMV_ERR_CUDA;

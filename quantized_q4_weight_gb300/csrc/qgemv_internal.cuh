@@ -76,6 +76,9 @@ struct ParamHead {
     long long *am_idx;            // argmax: result [T] (or nullptr)
     long long *am_idx2;           // top-2: rows [T][2] (or nullptr)
     float *am_val2;               // top-2: values [T][2] (with am_idx2)
+    float *sg_part;               // small groups: per-CTA segment sums (or nullptr)
+    int sg_stride;                //   floats per CTA region
+    int sg_ctas;                  //   CTAs 0..sg_ctas-1 have a region
     const long long *vc_tokens;   // verify: the step's tokens [T] (or nullptr)
     int *vc_n;                    // verify: committed predictions (with vc_tokens)
     unsigned *status;             // per-device status word

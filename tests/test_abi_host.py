@@ -70,7 +70,13 @@ def test_workspace_queries(L):
     assert L.qgemv_workspace_bytes(1536, 30, 1) == 0
     assert L.qgemv_workspace_bytes(1536, 64, 9) == 0
     items = (q.SeqItem * 2)(q.SeqItem(16, 4096, 8192, 40000, 1536), q.SeqItem(32, 4096, 8192, 1536, 8960))
+    # the counter area; on the tensor-core path (T >= 5) a small-group region
+    # of segment sums for each of the 152 CTAs (no device here):
+    # 15 slabs x 18 segments (K = 8960) x T x 16 rows
     assert L.qgemv_seq_workspace_bytes(items, 2, 1) == 16384
+    assert L.qgemv_seq_workspace_bytes(items, 2, 4) == 16384
+    for T in (5, 8):
+        assert L.qgemv_seq_workspace_bytes(items, 2, T) == 16384 + 152 * 15 * 18 * T * 16 * 4
     assert L.qgemv_seq_workspace_bytes(items, 0, 1) == 0
 
 

@@ -369,6 +369,44 @@ def test_seq_balanced_mode_bit_identical(orc, layout, T):
         check_close(yref.numpy()[:, rows], y64, S, f"balanced N={N} K={K}")
 
 
+@pytest.mark.parametrize("T", [5, 6, 8])
+def test_seq_small_groups_bit_identical(orc, T):
+    """Layer lists whose long-row projections need the activation area alone
+    leave CTAs with groups of a few slabs, which all warps of a tensor-core
+    launch share when the workspace holds the CTAs' segment-sum regions.  The bits must equal the
+    single calls with the full workspace, with regions for a third of the
+    CTAs, and with none."""
+    shapes = [(2048, 2048), (256, 2048), (2048, 11008), (11008, 2048), (2048, 11008), (1536, 8960)] * 4
+    entries, refs, cache = [], [], {}
+    for N, K in shapes:
+        if (N, K) not in cache:
+            Wg, W = weights(700 + N + K, N, K, q.W_PACKED)
+            x, xd, xq = quantized(800 + N + K + T, T, K)
+            yref = q.gemv(W, q.W_PACKED, xq, N, K, T, ws_for(N, K, T)).cpu()
+            cache[(N, K)] = (Wg, W, x, xq, yref)
+        Wg, W, x, xq, yref = cache[(N, K)]
+        entries.append((W, xq, torch.empty((T, N), dtype=torch.float32, device=DEV), N, K))
+        refs.append(((N, K), yref))
+    items = q.seq_items(entries)
+    full = q.seq_workspace_bytes(items, T)
+    base = 16384                                   # the counter area: all an unsplit list needs
+    assert full > base
+    for size in (full, base + (full - base) // 3, base):
+        ws = q.new_workspace(size)
+        for e in entries:
+            e[2].fill_(float("nan"))
+        q.gemv_seq(items, q.W_PACKED, T, ws)
+        torch.cuda.synchronize()
+        assert q.device_status() == 0
+        for (W, xq, y, N, K), (key, yref) in zip(entries, refs):
+            assert torch.equal(y.cpu().view(torch.int32), yref.view(torch.int32)), (key, size)
+    rng = np.random.default_rng(70 + T)
+    for (N, K), (Wg, W, x, xq, yref) in cache.items():
+        rows = np.unique(rng.integers(0, N, 8))
+        y64, S = orc.gemv_rows(Wg, N, K, orc.quantize(x), T, rows)
+        check_close(yref.numpy()[:, rows], y64, S, f"small groups N={N} K={K}")
+
+
 def test_seq_f32_equals_quantize_then_seq(orc):
     shapes = [(2048, 1536), (17, 544), (1536, 8960), (100, 2080)] * 40
     T = 2
