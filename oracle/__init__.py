@@ -91,6 +91,9 @@ class Oracle:
         L.orc_top2_f64.argtypes = [_f64p, ctypes.c_int64, _i64p]
         L.orc_top2_f64.restype = None
         L.orc_verify_commit.argtypes = [_i64p, _i64p, ctypes.c_int]
+        L.orc_quantize_block_q4_0.argtypes = [_f32p, _u8p]
+        L.orc_requant_f32_q4_0.argtypes = [_f32p, ctypes.c_int64, ctypes.c_int64, _u8p]
+        L.orc_requant_q8_0_q4_0.argtypes = [_u8p, ctypes.c_int64, ctypes.c_int64, _u8p]
         L.orc_verify_commit.restype = ctypes.c_int
         L.orc_num_threads.restype = ctypes.c_int
         L.orc_set_threads.argtypes = [ctypes.c_int]
@@ -233,6 +236,27 @@ class Oracle:
         assert tk.size == pr.size >= 1
         P = ctypes.POINTER(ctypes.c_int64)
         return int(self.L.orc_verify_commit(tk.ctypes.data_as(P), pr.ctypes.data_as(P), tk.size))
+
+    def quantize_block_q4_0(self, x: np.ndarray) -> np.ndarray:
+        """One block of 32 fp32 values -> its 18 Q4_0 bytes."""
+        x = np.ascontiguousarray(x, dtype=np.float32).reshape(32)
+        out = np.empty(18, np.uint8)
+        self.L.orc_quantize_block_q4_0(_p(x, _f32p), _p(out, _u8p))
+        return out
+
+    def requant_f32_q4_0(self, w: np.ndarray, N: int, K: int) -> np.ndarray:
+        """fp32 w[N][K] -> GGML Q4_0 bytes [N][K/32 * 18]."""
+        w = np.ascontiguousarray(w, dtype=np.float32).reshape(N, K)
+        out = np.empty((N, K // 32 * 18), np.uint8)
+        self.L.orc_requant_f32_q4_0(_p(w, _f32p), N, K, _p(out, _u8p))
+        return out
+
+    def requant_q8_0_q4_0(self, w: np.ndarray, N: int, K: int) -> np.ndarray:
+        """GGML Q8_0 bytes [N][K/32 * 34] -> GGML Q4_0 bytes [N][K/32 * 18]."""
+        w = np.ascontiguousarray(w, dtype=np.uint8).reshape(N, K // 32 * 34)
+        out = np.empty((N, K // 32 * 18), np.uint8)
+        self.L.orc_requant_q8_0_q4_0(_p(w, _u8p), N, K, _p(out, _u8p))
+        return out
 
     def num_threads(self) -> int:
         return int(self.L.orc_num_threads())

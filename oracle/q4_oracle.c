@@ -481,6 +481,85 @@ int orc_verify_commit(const int64_t *tokens, const int64_t *pred, int T)
     return n;
 }
 
+/* ------------------------------------------ Q4_0 requantisation at load */
+
+/* Weights requantised to Q4_0 blocks at load (minfer README M14: the
+ * lm_head requantised from Q8_0 to q4_0, 248 MB to 131 MB; M18: the Q8_0
+ * head of the smallest model requantised to q4_0 at load).  The pages fix
+ * the block format, not its encoder; the reading here is the encoder of the
+ * GGML q4_0 format the pages' models ship in:
+ *  - m = the block's element of largest magnitude (the first on ties; a
+ *    block of zeros gives m = +0);
+ *  - d = m / -8 in fp32, so that m is code 0 (value -8d) and the code range
+ *    0..15 covers [-8d, 7d];
+ *  - 1/d from the fp32 d (0 when d = 0);
+ *  - code n = min(15, floor(x * (1/d) + 8.5)): one fp32 multiply and one
+ *    fp32 add, each rounded to nearest even (x * (1/d) lies in [-8, 8] up
+ *    to rounding, so the sum is at least 0.49...);
+ *  - d stored as fp16, round to nearest even.
+ * Non-finite inputs give unspecified codes (NaN elements code 0 here). */
+void orc_quantize_block_q4_0(const float *x, uint8_t *blk)
+{
+    float amax = 0.0f, m = 0.0f;
+    for (int j = 0; j < QK; j++) {
+        float a = fabsf(x[j]);
+        if (a > amax) {
+            amax = a;
+#if ORC_MUTANT == 15
+            m = a;                              /* MUTANT: the magnitude, not the signed value */
+#else
+            m = x[j];
+#endif
+        }
+    }
+    float d = m / -8.0f;
+    float id = (d != 0.0f) ? 1.0f / d : 0.0f;
+    uint16_t dh = orc_float_to_half_rn(d);
+    blk[0] = (uint8_t)(dh & 0xFF);
+    blk[1] = (uint8_t)(dh >> 8);
+    int n[QK];
+    for (int j = 0; j < QK; j++) {
+        float v = x[j] * id;
+#if ORC_MUTANT == 16
+        float s = v + 8.0f;                     /* MUTANT: rounds down instead of to nearest */
+#else
+        float s = v + 8.5f;
+#endif
+        int c = (s >= 0.0f) ? (int)floorf(s) : 0;  /* s >= 0 unless NaN */
+        if (c > 15) c = 15;
+        n[j] = c;
+    }
+    for (int j = 0; j < 16; j++) blk[2 + j] = (uint8_t)(n[j] | (n[j + 16] << 4));
+}
+
+/* w fp32 [N][K] -> GGML Q4_0 blocks [N][K/32][18]. */
+void orc_requant_f32_q4_0(const float *w, int64_t N, int64_t K, uint8_t *out)
+{
+    int64_t nb = N * (K / QK);
+    for (int64_t b = 0; b < nb; b++) orc_quantize_block_q4_0(w + b * QK, out + b * Q4_0_BYTES);
+}
+
+/* GGML Q8_0 weight blocks [N][K/32][34] -> GGML Q4_0 blocks [N][K/32][18]:
+ * each block decoded to fp32 (q * d, exact: an 8-bit integer times an
+ * 11-bit significand), then encoded as above. */
+void orc_requant_q8_0_q4_0(const uint8_t *w, int64_t N, int64_t K, uint8_t *out)
+{
+    int64_t nb = N * (K / QK);
+    for (int64_t b = 0; b < nb; b++) {
+        const uint8_t *src = w + b * Q8_0_BYTES;
+        float d = orc_half_to_float(rd16(src));
+        float x[QK];
+        for (int j = 0; j < QK; j++) {
+#if ORC_MUTANT == 17
+            x[j] = (float)src[2 + j] * d;       /* MUTANT: codes read as unsigned */
+#else
+            x[j] = (float)(int8_t)src[2 + j] * d;
+#endif
+        }
+        orc_quantize_block_q4_0(x, out + b * Q4_0_BYTES);
+    }
+}
+
 /* ------------------------------------------------------------------ misc */
 
 int orc_num_threads(void)

@@ -475,4 +475,115 @@ def pin_verify_commit_is_lossless(o):
         assert n == right + 1
 
 
+# --------------------------------------------- Q4_0 requantisation at load
+# The encoder (reading: the GGML q4_0 encoder; minfer README M14 and M18
+# requantise heads to q4_0 at load) must invert the block format's decoder
+# on every block it can represent, keep its error within half a step, place
+# the block's extreme at code 0, and commute with power-of-two scaling.
+
+def _q4_decode(blk: np.ndarray) -> np.ndarray:
+    """fp64 values of one 18-byte Q4_0 block, from the format's definition."""
+    d = float(blk[:2].view(np.float16)[0])
+    n = np.concatenate([blk[2:] & 0x0F, blk[2:] >> 4]).astype(np.float64)
+    return (n - 8.0) * d, n.astype(int), d
+
+
+def _q4_block(d_bits: int, n) -> np.ndarray:
+    n = np.asarray(n, np.uint8)
+    return np.concatenate([np.array([d_bits & 0xFF, d_bits >> 8], np.uint8), (n[:16] | (n[16:] << 4)).astype(np.uint8)])
+
+
+def pin_q4enc_hand_blocks(o):
+    # Worked by hand.  A: the first element of largest magnitude is x[3] = 8,
+    # so d = 8 / -8 = -1 (fp16 0xBC00) and 1/d = -1; codes floor(-x + 8.5):
+    # 8 -> 0, -8 -> 16 -> clamped 15, -4 -> 12, 2 -> 6, 3.75 -> 4, 0 -> 8.
+    x = np.zeros(32, np.float32)
+    x[[0, 1, 2, 3, 9]] = [-4.0, 2.0, 3.75, 8.0, -8.0]
+    n = [8] * 32
+    n[0], n[1], n[2], n[3], n[9] = 12, 6, 4, 0, 15
+    assert np.array_equal(o.quantize_block_q4_0(x), _q4_block(0xBC00, n))
+    # B: the tie goes the other way (x[3] = -8 first), so d = 1 (0x3C00):
+    # codes floor(x + 8.5): -8 -> 0, 8 -> 15, -4 -> 4, 2 -> 10, 3.75 -> 12.
+    x[3], x[9] = -8.0, 8.0
+    n[0], n[1], n[2], n[3], n[9] = 4, 10, 12, 0, 15
+    assert np.array_equal(o.quantize_block_q4_0(x), _q4_block(0x3C00, n))
+
+
+def pin_q4enc_round_trip(o):
+    """Every block holding code 0 (its unique extreme value -8d) decodes to
+    fp32 values that encode back to the same 18 bytes."""
+    rng = np.random.default_rng(1410)
+    for i in range(600):
+        mag = rng.choice([rng.uniform(1e-3, 4.0), rng.uniform(6e-8, 6e-5), rng.uniform(1.0, 8000.0)])
+        d16 = np.float16(mag * rng.choice([-1.0, 1.0]))
+        if d16 == 0:
+            continue
+        n = rng.integers(0, 16, 32)
+        n[rng.integers(0, 32, rng.integers(1, 4))] = 0
+        blk = _q4_block(int(np.array([d16]).view(np.uint16)[0]), n)
+        vals, _, _ = _q4_decode(blk)
+        x = vals.astype(np.float32)
+        assert np.array_equal(x.astype(np.float64), vals)          # exact in fp32
+        assert np.array_equal(o.quantize_block_q4_0(x), blk), i
+
+
+def pin_q4enc_error_and_extreme(o):
+    rng = np.random.default_rng(1411)
+    for i in range(400):
+        x = (rng.standard_normal(32) * rng.choice([1e-3, 0.05, 1.0, 30.0])).astype(np.float32)
+        if i % 3 == 0:
+            x[rng.integers(0, 32)] *= 6.0                              # an outlier
+        if i % 5 == 0:
+            x[rng.integers(0, 32)] = -x[np.argmax(np.abs(x))]          # the extreme's opposite
+        vals, n, d = _q4_decode(o.quantize_block_q4_0(x))
+        x64 = x.astype(np.float64)
+        first = int(np.argmax(np.abs(x64)))                            # first of the largest magnitude
+        assert n[first] == 0
+        assert abs(d - (-x64[first] / 8.0)) <= 2.0 ** -11 * abs(x64[first] / 8.0)
+        err = np.abs(x64 - vals)
+        step = abs(d) * (1.0 + 2.0 ** -10)
+        assert np.all(err[n < 15] <= 0.5045 * step), i
+        assert np.all(err[n == 15] <= 1.0045 * step), i
+
+
+def pin_q4enc_zero_and_power_of_two_scaling(o):
+    vals, n, d = _q4_decode(o.quantize_block_q4_0(np.zeros(32, np.float32)))
+    assert d == 0.0 and np.all(n == 8) and np.all(vals == 0.0)
+    rng = np.random.default_rng(1412)
+    for i in range(100):
+        x = rng.standard_normal(32).astype(np.float32)
+        base = o.quantize_block_q4_0(x)
+        for k in (-6, -1, 3, 9):
+            sc = o.quantize_block_q4_0((x * np.float32(2.0 ** k)).astype(np.float32))
+            assert np.array_equal(sc[2:], base[2:]), (i, k)
+            d0 = float(base[:2].view(np.float16)[0])
+            assert float(sc[:2].view(np.float16)[0]) == d0 * 2.0 ** k
+
+
+def pin_q8_to_q4_exact_blocks(o):
+    """Q8_0 blocks whose codes are (n - 8) * s for an integer s requantise to
+    Q4_0 codes n with d = s * d8 (exact in fp32), stored as numpy's fp16."""
+    rng = np.random.default_rng(1413)
+    N, K = 3, 256
+    nb = K // 32
+    q8 = np.empty((N, nb, 34), np.uint8)
+    expect = np.empty((N, nb, 18), np.uint8)
+    for r in range(N):
+        for b in range(nb):
+            n = rng.integers(0, 16, 32)
+            n[rng.integers(0, 32)] = 0
+            s = int(rng.integers(1, 16))
+            d8 = np.float16(rng.uniform(1e-4, 0.5) * rng.choice([-1.0, 1.0]))
+            q8[r, b, :2] = np.array([d8]).view(np.uint8)
+            q8[r, b, 2:] = ((n - 8) * s).astype(np.int8).view(np.uint8)
+            dq = np.float16(np.float32(s) * np.float32(d8))
+            expect[r, b] = _q4_block(int(np.array([dq]).view(np.uint16)[0]), n)
+    got = o.requant_q8_0_q4_0(q8.reshape(N, -1), N, K)
+    assert np.array_equal(got.reshape(N, nb, 18), expect)
+    # and the fp32 entry point agrees block for block on the decoded values
+    x = (q8[:, :, 2:].view(np.int8).astype(np.float32) *
+         q8[:, :, :2].copy().view(np.float16).astype(np.float32)).reshape(N, K)
+    assert np.array_equal(o.requant_f32_q4_0(x, N, K), got)
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -23,8 +23,10 @@ def test_pin(orc, pin):
 #  8 truncating fp16 encode, 9 argmax ties to the highest index,
 #  10 transposed output, 11 top-2 second ties to the highest index,
 #  12 verify rule comparing a draft with its own prediction,
-#  13 Q8_0 weights read as unsigned, 14 SiLU with exp(+g).
-MUTANTS = list(range(1, 15))
+#  13 Q8_0 weights read as unsigned, 14 SiLU with exp(+g),
+#  15 Q4_0 encoder scale from the magnitude, 16 Q4_0 codes rounded down,
+#  17 Q8_0 weights read as unsigned when requantised to Q4_0.
+MUTANTS = list(range(1, 18))
 
 
 @pytest.fixture(scope="module")
