@@ -497,7 +497,10 @@ int orc_verify_commit(const int64_t *tokens, const int64_t *pred, int T)
  *    fp32 add, each rounded to nearest even (x * (1/d) lies in [-8, 8] up
  *    to rounding, so the sum is at least 0.49...);
  *  - d stored as fp16, round to nearest even.
- * Non-finite inputs give unspecified codes (NaN elements code 0 here). */
+ * When d is so small (an fp32 subnormal) that 1/d overflows to infinity,
+ * the same operations give codes 0 (x < 0), 15 (x > 0) and 0 (x = 0, a NaN
+ * sum), the clamp taken before the conversion.  Non-finite inputs give
+ * unspecified codes. */
 void orc_quantize_block_q4_0(const float *x, uint8_t *blk)
 {
     float amax = 0.0f, m = 0.0f;
@@ -525,8 +528,9 @@ void orc_quantize_block_q4_0(const float *x, uint8_t *blk)
 #else
         float s = v + 8.5f;
 #endif
-        int c = (s >= 0.0f) ? (int)floorf(s) : 0;  /* s >= 0 unless NaN */
-        if (c > 15) c = 15;
+        /* min(15, floor(s)), taken so that an infinite s (1/d overflows when
+         * d is an fp32 subnormal) gives 15 or 0 and a NaN gives 0 */
+        int c = (s >= 15.0f) ? 15 : (s >= 0.0f) ? (int)floorf(s) : 0;
         n[j] = c;
     }
     for (int j = 0; j < 16; j++) blk[2 + j] = (uint8_t)(n[j] | (n[j + 16] << 4));

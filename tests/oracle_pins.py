@@ -507,6 +507,15 @@ def pin_q4enc_hand_blocks(o):
     x[3], x[9] = -8.0, 8.0
     n[0], n[1], n[2], n[3], n[9] = 4, 10, 12, 0, 15
     assert np.array_equal(o.quantize_block_q4_0(x), _q4_block(0x3C00, n))
+    # C: m = -1.6e-39 (an fp32 subnormal), d = m / -8 about 2e-40, whose
+    # reciprocal (5e39) overflows to +inf; x * inf + 8.5 is -inf for x < 0
+    # (code 0), +inf for x > 0 (code 15) and NaN for x = 0 (code 0); d
+    # underflows to fp16 +0.
+    x = np.zeros(32, np.float32)
+    x[0], x[1] = np.float32(-1.6e-39), np.float32(1e-40)
+    n = [0] * 32
+    n[1] = 15
+    assert np.array_equal(o.quantize_block_q4_0(x), _q4_block(0x0000, n))
 
 
 def pin_q4enc_round_trip(o):
