@@ -282,6 +282,38 @@ def build_q8(T, seed, dev, copies=2, keep_host=False, N=151936, K=1536):
     return wl
 
 
+def build_requant(T, seed, dev, copies=2, keep_host=False, N=151936, K=1536):
+    """Load-time requantisation of the Q8_0 lm_head to Q4_0 blocks (one
+    launch per step); two source copies rotate so reads hit HBM."""
+    import torch
+    q = _q()
+    wl = Workload("lm_head_requant_q8", T)
+    wl.W = []
+    for c in range(copies):
+        Wg = synth.q8_0_weights(seed, N, K, stream=(c,))
+        if keep_host:
+            wl.host[c] = Wg
+        wl.W.append(torch.from_numpy(Wg.reshape(-1)).to(dev))
+    wl.out = torch.empty(q.q4_0_bytes(N, K), dtype=torch.uint8, device=dev)
+    wl.w_bytes, wl.y_bytes = q.q8_0_bytes(N, K), q.q4_0_bytes(N, K)   # read, written
+    wl.n_gemv, wl.launches = 1, 1
+    wl.copy = 0
+
+    def step(stream=None):
+        q.requant_q8_0_q4_0(wl.W[wl.copy], N, K, out=wl.out, stream=stream)
+        wl.copy = (wl.copy + 1) % copies
+
+    wl.step, wl.kernel = step, step
+    wl.kernel_name = "requant_q4_0_staged"
+    wl.dtype = "fp32 encoder arithmetic (Q8_0 in, Q4_0 out)"
+    wl.data = "synthetic (seeded; Q8_0 codes uniform on [-127, 127], fp16 scales U[1e-3,4e-3])"
+    wl.inputs, wl.outputs = [wl.W[0]], [wl.out]
+    wl.config = {"workload": "lm_head_requant_q8", "N": N, "K": K, "copies": copies,
+                 "bytes": "Q8_0 read + Q4_0 written per step; us_per_gemv is us per requantisation",
+                 "l2_defeat": f"{copies} source copies in rotation ({copies * wl.w_bytes / 1e6:.0f} MB)"}
+    return wl
+
+
 def build_single(T, seed, dev, copies=400, N=1536, K=1536, keep_host=False):
     import torch
     q = _q()
@@ -406,6 +438,8 @@ def build_workload(name: str, dev, T: int | None = None, keep_host: bool = False
                          keep_host)
     if spec["kind"] == "q8":
         return build_q8(T or spec["T"], spec["seed"], dev, spec["copies"], keep_host, spec["N"], spec["K"])
+    if spec["kind"] == "requant":
+        return build_requant(T or spec["T"], spec["seed"], dev, spec["copies"], keep_host, spec["N"], spec["K"])
     if spec["kind"] == "single":
         return build_single(T or spec["T"], spec["seed"], dev, keep_host=keep_host, N=spec["N"], K=spec["K"])
     if spec["kind"] == "moe":
@@ -520,7 +554,7 @@ def _oracle_inputs(workload: str):
         if spec["kind"] == "seq":
             T = 1
             mats = synth.layer_set(spec["layer"], spec["layers"])
-        elif spec["kind"] in ("argmax", "single", "verify", "q8"):
+        elif spec["kind"] in ("argmax", "single", "verify", "q8", "requant"):
             T, mats = spec["T"], [("w", spec["N"], spec["K"])]
         elif spec["kind"] == "ffn":
             T = spec["T"]
@@ -530,7 +564,7 @@ def _oracle_inputs(workload: str):
             T = 1
             mats = [("gate", spec["d_ff"], spec["d_model"]), ("up", spec["d_ff"], spec["d_model"]),
                     ("down", spec["d_model"], spec["d_ff"])] * (spec["top_k"] + 1)
-        gen = synth.q8_0_weights if spec["kind"] == "q8" else synth.q4_0_weights
+        gen = synth.q8_0_weights if spec["kind"] in ("q8", "requant") else synth.q4_0_weights
         data = [(N, K, gen(spec["seed"], N, K, stream=(i,)),
                  synth.activations(spec["seed"], T, K, stream=(i,))) for i, (_, N, K) in enumerate(mats)]
         _ORACLE_INPUTS[workload] = (T, data)
@@ -568,6 +602,8 @@ def oracle_sample(workload: str, budget_s: float = 12.0, min_s: float = 3.0, thr
     if threads:
         o.set_threads(threads)
     T, data = _oracle_inputs(workload)
+    if synth.WORKLOADS[workload]["kind"] == "requant":
+        return _oracle_requant_sample(o, data, budget_s, min_s)
     gemv = o.gemv_q8 if synth.WORKLOADS[workload]["kind"] == "q8" else o.gemv
     done_bytes, t_total, n_done = 0, 0.0, 0
     while True:
@@ -585,6 +621,26 @@ def oracle_sample(workload: str, budget_s: float = 12.0, min_s: float = 3.0, thr
     return (done_bytes / t_total / 1e9, o.num_threads(),
             f"{n_done} GEMVs ({n_done / len(data):.2f} steps of {len(data)} GEMVs, {done_bytes / 1e6:.0f} MB), "
             f"T={T}, {t_total:.1f} s of oracle time")
+
+
+def _oracle_requant_sample(o, data, budget_s, min_s):
+    """The oracle's Q8_0 -> Q4_0 requantisation (one thread: the oracle's
+    encoder loop has no OpenMP) over row slices of the lm_head."""
+    N, K, Wg, _ = data[0]
+    rows = 8192
+    done_bytes, t_total, n_done = 0, 0.0, 0
+    while t_total < budget_s:
+        r0 = (n_done * rows) % N
+        r1 = min(N, r0 + rows)
+        t0 = time.perf_counter()
+        o.requant_q8_0_q4_0(Wg[r0:r1], r1 - r0, K)
+        t_total += time.perf_counter() - t0
+        done_bytes += (r1 - r0) * (K // 32) * (34 + 18)
+        n_done += 1
+        if t_total >= budget_s:
+            break
+    return (done_bytes / t_total / 1e9, 1,
+            f"{n_done} slices of {rows} rows ({done_bytes / 1e6:.0f} MB read + written), {t_total:.1f} s of oracle time")
 
 
 # ============================================================ main
@@ -886,8 +942,10 @@ def measure(args, wl: Workload, dev, world, rank):
     return {
         "metric": METRIC, "value": round(gbs, 3), "unit": UNIT, "n_gpus": world, "steps": K,
         "warmup": args.warmup, "ms_per_step": round(ms, 5), "higher_is_better": True, "scaling": "weak",
-        "vs_baseline": None, "dtype": "int8 x uint4 -> int32 block sums, fp32 accumulation",
-        "data": "synthetic (seeded; Q4_0 nibbles uniform, fp16 scales U[1e-3,4e-3], x N(0,1) with 1% x20)",
+        "vs_baseline": None,
+        "dtype": getattr(wl, "dtype", "int8 x uint4 -> int32 block sums, fp32 accumulation"),
+        "data": getattr(wl, "data", "synthetic (seeded; Q4_0 nibbles uniform, fp16 scales U[1e-3,4e-3], "
+                                    "x N(0,1) with 1% x20)"),
         "config": cfg,
         "e2e": {"value": round(wl.step_bytes / (e2e_ms * 1e-3) / 1e9 * world, 3), "unit": UNIT,
                 "ms_per_step": round(e2e_ms, 5), "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},

@@ -213,6 +213,28 @@ qgemv_status qgemv_pack_q8_0(const void *w_ggml, void *w_packed, int64_t N, int6
 qgemv_status qgemv_unpack_q8_0(const void *w_packed, void *w_ggml, int64_t N, int64_t K,
                                qgemv_stream_t stream);
 
+/* ---- Requantisation to Q4_0 at load (minfer README M14: the lm_head
+ * requantised from Q8_0 to q4_0, 248 MB to 131 MB; M18: Q8_0 heads
+ * requantised to q4_0 when the model loads).  The pages give no encoder;
+ * these use GGML's q4_0 encoder, per block of 32 values x:
+ *   m = the first element of largest |x| (+0 for a block of zeros),
+ *   d = m / -8 in fp32 (m is code 0), id = 1/d (0 when d = 0),
+ *   code_j = min(15, floor(x_j * id + 8.5)), multiply and add each rounded
+ *   to nearest even; d stored as fp16 (round to nearest even).
+ * Output: GGML Q4_0 blocks [N][K/32][18] (pack with qgemv_pack_q4_0 for the
+ * GEMV).  A block whose d is an fp32 subnormal (1/d overflows) gets codes
+ * 0 for x < 0, 15 for x > 0 and 0 for x = 0.  Values must be finite: a
+ * block holding an inf or NaN gets unspecified bytes.  Inputs are not modified; output must not overlap them.
+ * Enqueued on `stream`, no synchronisation. */
+
+/* fp32 w[N][K] (row-major, 4-byte aligned) -> Q4_0 (2-byte aligned). */
+qgemv_status qgemv_requant_f32_q4_0(const float *w, void *w_q4, int64_t N, int64_t K,
+                                    qgemv_stream_t stream);
+/* GGML Q8_0 weight blocks [N][K/32][34] (2-byte aligned; values q * d,
+ * exact in fp32) -> Q4_0 (2-byte aligned). */
+qgemv_status qgemv_requant_q8_0_q4_0(const void *w_q8, void *w_q4, int64_t N, int64_t K,
+                                     qgemv_stream_t stream);
+
 /* Workspace bytes for qgemv_q8_0 (0 when the launch needs none; 0 also for
  * an invalid shape). */
 size_t qgemv_q8_0_workspace_bytes(int64_t N, int64_t K, int T);

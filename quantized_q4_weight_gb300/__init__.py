@@ -79,6 +79,8 @@ _SIGS = {
     "qgemv_debug_silu_mul_q8": ([_VP, _VP, _VP, _I32, _I64, _VP], _I32),
     "qgemv_pack_q8_0": ([_VP, _VP, _I64, _I64, _VP], _I32),
     "qgemv_unpack_q8_0": ([_VP, _VP, _I64, _I64, _VP], _I32),
+    "qgemv_requant_f32_q4_0": ([_VP, _VP, _I64, _I64, _VP], _I32),
+    "qgemv_requant_q8_0_q4_0": ([_VP, _VP, _I64, _I64, _VP], _I32),
     "qgemv_q8_0_workspace_bytes": ([_I64, _I64, _I32], _SZ),
     "qgemv_q8_0": ([_VP, _VP, _VP, _I64, _I64, _I32, _VP, _SZ, _VP], _I32),
     "qgemv_seq_workspace_bytes": ([ctypes.POINTER(SeqItem), _I32, _I32], _SZ),
@@ -280,6 +282,20 @@ def pack_q8_0(w_ggml: torch.Tensor, N: int, K: int, out: torch.Tensor | None = N
 def unpack_q8_0(w_packed: torch.Tensor, N: int, K: int, out: torch.Tensor | None = None, stream=None):
     out = out if out is not None else torch.empty(q8_0_bytes(N, K), dtype=torch.uint8, device=w_packed.device)
     _check(lib().qgemv_unpack_q8_0(_ptr(w_packed), _ptr(out), N, K, _stream(stream)), "qgemv_unpack_q8_0")
+    return out
+
+
+def requant_f32_q4_0(w: torch.Tensor, N: int, K: int, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """fp32 weights [N][K] -> GGML Q4_0 blocks (uint8 [18 N K/32]), GGML's q4_0 encoder."""
+    out = out if out is not None else torch.empty(q4_0_bytes(N, K), dtype=torch.uint8, device=w.device)
+    _check(lib().qgemv_requant_f32_q4_0(_ptr(w), _ptr(out), N, K, _stream(stream)), "qgemv_requant_f32_q4_0")
+    return out
+
+
+def requant_q8_0_q4_0(w_q8: torch.Tensor, N: int, K: int, out: torch.Tensor | None = None, stream=None):
+    """GGML Q8_0 weights (uint8 [34 N K/32]) -> GGML Q4_0 blocks (uint8 [18 N K/32])."""
+    out = out if out is not None else torch.empty(q4_0_bytes(N, K), dtype=torch.uint8, device=w_q8.device)
+    _check(lib().qgemv_requant_q8_0_q4_0(_ptr(w_q8), _ptr(out), N, K, _stream(stream)), "qgemv_requant_q8_0_q4_0")
     return out
 
 

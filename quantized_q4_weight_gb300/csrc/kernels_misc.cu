@@ -276,4 +276,201 @@ cudaError_t launch_verify_commit(const long long *tokens, const long long *pred,
     return cudaGetLastError();
 }
 
+// Weights requantised to GGML Q4_0 blocks at load (minfer README M14 and
+// M18: heads requantised to q4_0 when the model is loaded).  The encoder is
+// GGML's q4_0 one: m = the block's first element of largest magnitude (+0
+// for a block of zeros), d = m / -8 in fp32 (m becomes code 0), 1/d from
+// that d (0 when d = 0), code min(15, floor(x * (1/d) + 8.5)) with the
+// multiply and the add each rounded to nearest, d stored as fp16.  From Q8_0
+// blocks the values are q * d8 (exact in fp32).
+//
+// The conversion units (int <-> float, floor) run at a quarter of the FP32
+// rate, and three per element made the Q8_0 encoder bound by them.  Both
+// conversions are done in the FP32 pipe instead, exactly:
+//  - int8 q -> float: the float with bits 0x4B000000 | (q + 128) is
+//    2^23 + q + 128, so subtracting 2^23 + 128 leaves q;
+//  - floor(s) for 0 <= s <= 15: 2^23 + s rounded toward minus infinity is
+//    2^23 + floor(s) (the spacing of floats at 2^23 is 1), whose low four
+//    bits are floor(s).
+__device__ __forceinline__ float q8_code_to_float(unsigned byte)
+{
+    return __fsub_rn(__uint_as_float(0x4B000000u | (byte ^ 0x80u)), 8388736.0f);
+}
+
+// One block of 32 values -> its 18 bytes as nine two-byte words: d, then
+// byte j = code j | code j+16 << 4.
+__device__ __forceinline__ void q4_encode_block(const float (&x)[QK], unsigned short (&o)[9])
+{
+    float amax = 0.0f, m = 0.0f;
+#pragma unroll
+    for (int j = 0; j < QK; ++j) {
+        const float a = fabsf(x[j]);
+        if (a > amax) {
+            amax = a;
+            m = x[j];
+        }
+    }
+    const float d = __fdiv_rn(m, -8.0f);
+    const float id = d != 0.0f ? __frcp_rn(d) : 0.0f;
+    int c[QK];
+#pragma unroll
+    for (int j = 0; j < QK; ++j) {
+        // min(15, floor(s)) with s first clamped to [0, 15]: an infinite s
+        // (1/d overflows for an fp32-subnormal d) gives 15 or 0, a NaN
+        // (0 * inf) gives 0 (fmaxf returns the number)
+        const float sj = __fadd_rn(__fmul_rn(x[j], id), 8.5f);
+        const float cl = fminf(fmaxf(sj, 0.0f), 15.0f);
+        c[j] = static_cast<int>(__float_as_uint(__fadd_rd(cl, 8388608.0f)) & 0xFu);
+    }
+    o[0] = __half_as_ushort(__float2half_rn(d));
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+        o[1 + i] = static_cast<unsigned short>((c[2 * i] | (c[2 * i + 16] << 4)) |
+                                               ((c[2 * i + 1] | (c[2 * i + 17] << 4)) << 8));
+}
+
+// One thread per block, all of its loads issued before any use, blocks in a
+// grid-stride loop (unaligned sources, and the blocks after the last whole
+// chunk of the staged kernel below).  VEC: the fp32 source is 16-byte
+// aligned (float4 loads).
+template <bool FROM_Q8, bool VEC>
+__global__ void __launch_bounds__(256) requant_q4_0_kernel(const void *__restrict__ src, uint8_t *__restrict__ dst,
+                                                           long long nblocks)
+{
+    const long long step = static_cast<long long>(gridDim.x) * blockDim.x;
+    for (long long blk = blockIdx.x * static_cast<long long>(blockDim.x) + threadIdx.x; blk < nblocks; blk += step) {
+        float x[QK];
+        if constexpr (FROM_Q8) {
+            // 34 bytes at an even offset: 17 two-byte loads
+            const unsigned short *s =
+                reinterpret_cast<const unsigned short *>(static_cast<const uint8_t *>(src) + blk * 34);
+            unsigned short h[17];
+#pragma unroll
+            for (int i = 0; i < 17; ++i) h[i] = __ldg(s + i);
+            const float d8 = __half2float(__ushort_as_half(h[0]));
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                x[2 * i] = __fmul_rn(q8_code_to_float(h[1 + i] & 0xFFu), d8);
+                x[2 * i + 1] = __fmul_rn(q8_code_to_float(h[1 + i] >> 8), d8);
+            }
+        } else if constexpr (VEC) {
+            const float4 *s = reinterpret_cast<const float4 *>(static_cast<const float *>(src) + blk * QK);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                const float4 v = __ldg(s + i);
+                x[4 * i] = v.x;
+                x[4 * i + 1] = v.y;
+                x[4 * i + 2] = v.z;
+                x[4 * i + 3] = v.w;
+            }
+        } else {
+            const float *s = static_cast<const float *>(src) + blk * QK;
+#pragma unroll
+            for (int j = 0; j < QK; ++j) x[j] = __ldg(s + j);
+        }
+        unsigned short o[9];
+        q4_encode_block(x, o);
+        unsigned short *out = reinterpret_cast<unsigned short *>(dst + blk * 18);
+#pragma unroll
+        for (int i = 0; i < 9; ++i) out[i] = o[i];
+    }
+}
+
+// The same encoder over chunks of 256 blocks staged through shared memory,
+// so that global memory sees only coalesced 16-byte loads and stores (source
+// and destination 16-byte aligned; whole chunks only).  fp32 chunks are
+// stored transposed, element j of block b at word j * 257 + b: the staging
+// stores of one 16-byte load and the per-thread reads of one element then
+// fall in distinct banks.  Q8_0 chunks stay as they are (34-byte blocks,
+// read as two-byte words: at most two threads per bank).
+constexpr int RQ_CHUNK = 256;
+
+template <bool FROM_Q8>
+__global__ void __launch_bounds__(RQ_CHUNK) requant_q4_0_staged(const uint8_t *__restrict__ src,
+                                                                uint8_t *__restrict__ dst, long long nchunks)
+{
+    constexpr int IN_BYTES = FROM_Q8 ? 34 * RQ_CHUNK : QK * 257 * 4;  // staging area
+    constexpr int IN_LOADS = (FROM_Q8 ? 34 : 128) * RQ_CHUNK / 16;     // 16-byte loads per chunk
+    constexpr int OUT_STORES = 18 * RQ_CHUNK / 16;
+    __shared__ __align__(16) uint8_t s_in[IN_BYTES];
+    __shared__ __align__(16) uint8_t s_out[18 * RQ_CHUNK];
+    const int tid = threadIdx.x;
+    for (long long ch = blockIdx.x; ch < nchunks; ch += gridDim.x) {
+        const int4 *g = reinterpret_cast<const int4 *>(src + ch * (IN_LOADS * 16ll));
+        if constexpr (FROM_Q8) {
+            for (int i = tid; i < IN_LOADS; i += RQ_CHUNK) reinterpret_cast<int4 *>(s_in)[i] = __ldg(g + i);
+        } else {
+            float *t = reinterpret_cast<float *>(s_in);
+            for (int i = tid; i < IN_LOADS; i += RQ_CHUNK) {
+                const float4 v = __ldg(reinterpret_cast<const float4 *>(g) + i);
+                const int b = i >> 3, j = (i & 7) * 4;  // block, first element
+                t[j * 257 + b] = v.x;
+                t[(j + 1) * 257 + b] = v.y;
+                t[(j + 2) * 257 + b] = v.z;
+                t[(j + 3) * 257 + b] = v.w;
+            }
+        }
+        __syncthreads();
+        float x[QK];
+        if constexpr (FROM_Q8) {
+            const unsigned short *h = reinterpret_cast<const unsigned short *>(s_in + tid * 34);
+            const float d8 = __half2float(__ushort_as_half(h[0]));
+#pragma unroll
+            for (int i = 0; i < 16; ++i) {
+                const unsigned w = h[1 + i];
+                x[2 * i] = __fmul_rn(q8_code_to_float(w & 0xFFu), d8);
+                x[2 * i + 1] = __fmul_rn(q8_code_to_float(w >> 8), d8);
+            }
+        } else {
+            const float *t = reinterpret_cast<const float *>(s_in);
+#pragma unroll
+            for (int j = 0; j < QK; ++j) x[j] = t[j * 257 + tid];
+        }
+        unsigned short o[9];
+        q4_encode_block(x, o);
+        unsigned short *so = reinterpret_cast<unsigned short *>(s_out + tid * 18);
+#pragma unroll
+        for (int i = 0; i < 9; ++i) so[i] = o[i];
+        __syncthreads();
+        int4 *go = reinterpret_cast<int4 *>(dst + ch * (OUT_STORES * 16ll));
+        for (int i = tid; i < OUT_STORES; i += RQ_CHUNK) go[i] = reinterpret_cast<const int4 *>(s_out)[i];
+        // the next chunk's staging stores wait for these reads at its first barrier;
+        // its s_out writes come after that barrier too
+    }
+}
+
+cudaError_t launch_requant_q4_0(const void *src, bool from_q8, void *dst, long long nblocks, cudaStream_t st)
+{
+    const uint8_t *s8 = static_cast<const uint8_t *>(src);
+    uint8_t *o = static_cast<uint8_t *>(dst);
+    const bool aligned16 = ((reinterpret_cast<uintptr_t>(src) | reinterpret_cast<uintptr_t>(dst)) & 15) == 0;
+    long long done = 0;
+    if (aligned16 && nblocks >= RQ_CHUNK) {
+        const long long nchunks = nblocks / RQ_CHUNK;
+        // resident CTAs: 8 per SM (Q8_0, 13 KB of shared memory each) or 5 (fp32, 37 KB)
+        long long grid = nchunks < 152ll * 8 * 16 ? nchunks : 152ll * 8 * 16;
+        if (from_q8)
+            requant_q4_0_staged<true><<<static_cast<unsigned>(grid), RQ_CHUNK, 0, st>>>(s8, o, nchunks);
+        else
+            requant_q4_0_staged<false><<<static_cast<unsigned>(grid), RQ_CHUNK, 0, st>>>(s8, o, nchunks);
+        done = nchunks * RQ_CHUNK;
+        const cudaError_t e = cudaGetLastError();
+        if (e != cudaSuccess || done == nblocks) return e;
+    }
+    // the rest (or everything, unaligned): one thread per block
+    const long long rest = nblocks - done;
+    const void *s = s8 + done * (from_q8 ? 34 : 128);
+    o += done * 18;
+    long long grid = (rest + 255) / 256;
+    if (grid > (1 << 20)) grid = 1 << 20;
+    const dim3 g(static_cast<unsigned>(grid));
+    if (from_q8)
+        requant_q4_0_kernel<true, false><<<g, 256, 0, st>>>(s, o, rest);
+    else if ((reinterpret_cast<uintptr_t>(s) & 15) == 0)
+        requant_q4_0_kernel<false, true><<<g, 256, 0, st>>>(s, o, rest);
+    else
+        requant_q4_0_kernel<false, false><<<g, 256, 0, st>>>(s, o, rest);
+    return cudaGetLastError();
+}
+
 }  // namespace qg

@@ -608,6 +608,26 @@ qgemv_status qgemv_pack_q8_0(const void *w_ggml, void *w_packed, int64_t N, int6
                : QGEMV_ERR_CUDA;
 }
 
+qgemv_status qgemv_requant_f32_q4_0(const float *w, void *w_q4, int64_t N, int64_t K, qgemv_stream_t stream)
+{
+    if (!shape_ok(N, K) || !w || !w_q4) return QGEMV_ERR_INVALID_ARG;
+    if (!aligned(w, 4) || !aligned(w_q4, 2)) return QGEMV_ERR_MISALIGNED;
+    if (overlap(range(w, 4ll * N * K), range(w_q4, 18ll * N * (K / QK)))) return QGEMV_ERR_INVALID_ARG;
+    return launch_requant_q4_0(w, false, w_q4, N * (K / QK), reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? QGEMV_OK
+               : QGEMV_ERR_CUDA;
+}
+
+qgemv_status qgemv_requant_q8_0_q4_0(const void *w_q8, void *w_q4, int64_t N, int64_t K, qgemv_stream_t stream)
+{
+    if (!shape_ok(N, K) || !w_q8 || !w_q4) return QGEMV_ERR_INVALID_ARG;
+    if (!aligned(w_q8, 2) || !aligned(w_q4, 2)) return QGEMV_ERR_MISALIGNED;
+    if (overlap(range(w_q8, 34ll * N * (K / QK)), range(w_q4, 18ll * N * (K / QK)))) return QGEMV_ERR_INVALID_ARG;
+    return launch_requant_q4_0(w_q8, true, w_q4, N * (K / QK), reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? QGEMV_OK
+               : QGEMV_ERR_CUDA;
+}
+
 qgemv_status qgemv_unpack_q8_0(const void *w_packed, void *w_ggml, int64_t N, int64_t K, qgemv_stream_t stream)
 {
     if (!shape_ok(N, K) || !w_ggml || !w_packed) return QGEMV_ERR_INVALID_ARG;

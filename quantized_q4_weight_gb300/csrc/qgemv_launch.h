@@ -29,6 +29,9 @@ cudaError_t launch_q8(const void *W, const void *xq, float *y, long long N, long
                       long long ws_bytes, bool do_launch, int sms, int smem_budget, unsigned *status,
                       cudaStream_t st, long long *ws_need, int *unsupported);
 cudaError_t launch_silu_mul_q8(const float *g, const float *u, void *hq, int T, long long F, bool pdl, cudaStream_t st);
+// Requantisation to GGML Q4_0 blocks (kernels_misc.cu): nblocks blocks of
+// fp32 [32] (from_q8 false) or GGML Q8_0 (from_q8 true) into 18-byte blocks.
+cudaError_t launch_requant_q4_0(const void *src, bool from_q8, void *dst, long long nblocks, cudaStream_t st);
 cudaError_t launch_verify_commit(const long long *tokens, const long long *pred, int pred_stride, int T,
                                  int32_t *n_commit, cudaStream_t st);
 

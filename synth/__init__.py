@@ -61,6 +61,17 @@ def q8_0_weights(seed: int, N: int, K: int, stream: tuple = ()) -> np.ndarray:
     return blocks.reshape(N, nb * 34)
 
 
+def f32_weights(seed: int, N: int, K: int, stream: tuple = ()) -> np.ndarray:
+    """fp32 weight matrix [N, K] before quantisation: N(0, s_r^2) per row r,
+    s_r log-uniform on [0.005, 0.1], with 1 % of entries scaled by 20."""
+    rng = _rng(seed, 5, *stream)
+    s = np.exp(rng.uniform(np.log(0.005), np.log(0.1), size=(N, 1)))
+    w = rng.standard_normal(size=(N, K)) * s
+    mask = rng.random(size=(N, K)) < OUTLIER_P
+    w[mask] *= OUTLIER_MUL
+    return w.astype(np.float32)
+
+
 def activations(seed: int, T: int, K: int, stream: tuple = ()) -> np.ndarray:
     """fp32 [T, K]: N(0,1) with 1 % of entries scaled by 20."""
     rng = _rng(seed, 2, *stream)
@@ -121,6 +132,8 @@ WORKLOADS = {
     "qwen2.5-1.5b_ffn": dict(kind="ffn", d_model=1536, d_ff=8960, layers=28, T=1, seed=5000),
     # the lm_head held as Q8_0 weights (248 MB per copy), T=1, 2 copies in rotation
     "q8_lm_head": dict(kind="q8", N=151936, K=1536, T=1, copies=2, seed=2200),
+    # load-time requantisation of that Q8_0 lm_head to Q4_0
+    "lm_head_requant_q8": dict(kind="requant", N=151936, K=1536, T=1, copies=2, seed=2300),
     # 36-layer Qwen2.5-3B-shaped layer set, T in {1,2,4,8}
     "qwen2.5-3b_verify": dict(kind="seq", layer=QWEN25_3B_LAYER, layers=36, Ts=(1, 2, 4, 8), seed=3000),
     # MoE: 256 experts (gate/up 512x2048, down 2048x512), top-8 + 1 shared, T=1

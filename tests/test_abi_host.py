@@ -119,6 +119,16 @@ def test_other_calls_reject_bad_arguments(L):
     assert L.qgemv_q4_0_gather(mats, 1, FAKE + (1 << 31), 2, 4, 1, 1, FAKE + (1 << 30), 4096, s) == 1  # y_stride < T*N
     assert L.qgemv_q4_0_gather(mats, 1, None, 1, 4, 1, 1, FAKE + (1 << 30), 4096, s) == 1
     assert L.qgemv_debug_block_isums(FAKE, 1, FAKE, None, 16, 64, 1, s) == 1
+    # requantisation: shapes, null pointers, alignment, output over the input
+    out = FAKE + (1 << 30)
+    assert L.qgemv_requant_f32_q4_0(FAKE, out, 16, 48, s) == 1
+    assert L.qgemv_requant_f32_q4_0(None, out, 16, 64, s) == 1
+    assert L.qgemv_requant_f32_q4_0(FAKE + 2, out, 16, 64, s) == 2
+    assert L.qgemv_requant_f32_q4_0(FAKE, out + 1, 16, 64, s) == 2
+    assert L.qgemv_requant_f32_q4_0(FAKE, FAKE + 4 * 16 * 64 - 2, 16, 64, s) == 1
+    assert L.qgemv_requant_q8_0_q4_0(FAKE + 1, out, 16, 64, s) == 2
+    assert L.qgemv_requant_q8_0_q4_0(FAKE, FAKE + 34 * 16 * 2 - 18, 16, 64, s) == 1
+    assert L.qgemv_requant_q8_0_q4_0(FAKE, out, 0, 64, s) == 1
 
 
 def test_fp32_calls_reject_bad_arguments(L):
