@@ -92,6 +92,8 @@ class Oracle:
         L.orc_top2_f64.restype = None
         L.orc_verify_commit.argtypes = [_i64p, _i64p, ctypes.c_int]
         L.orc_quantize_block_q4_0.argtypes = [_f32p, _u8p]
+        L.orc_gemv_ep_f64.argtypes = [_u8p, ctypes.c_int64, ctypes.c_int64, _u8p, ctypes.c_int, _f32p, _f32p,
+                                      _f64p, _f64p]
         L.orc_requant_f32_q4_0.argtypes = [_f32p, ctypes.c_int64, ctypes.c_int64, _u8p]
         L.orc_requant_q8_0_q4_0.argtypes = [_u8p, ctypes.c_int64, ctypes.c_int64, _u8p]
         L.orc_verify_commit.restype = ctypes.c_int
@@ -236,6 +238,18 @@ class Oracle:
         assert tk.size == pr.size >= 1
         P = ctypes.POINTER(ctypes.c_int64)
         return int(self.L.orc_verify_commit(tk.ctypes.data_as(P), pr.ctypes.data_as(P), tk.size))
+
+    def gemv_ep(self, W: np.ndarray, N: int, K: int, xq: np.ndarray, T: int, bias=None, res=None):
+        """-> (y64, S) [T, N] of W.x + bias[N] + res[T, N] (either may be None)."""
+        W = np.ascontiguousarray(W, np.uint8)
+        xq = np.ascontiguousarray(xq, np.uint8)
+        b = None if bias is None else np.ascontiguousarray(bias, np.float32).reshape(N)
+        r = None if res is None else np.ascontiguousarray(res, np.float32).reshape(T, N)
+        y = np.empty((T, N), np.float64)
+        S = np.empty((T, N), np.float64)
+        self.L.orc_gemv_ep_f64(_p(W, _u8p), N, K, _p(xq, _u8p), T, None if b is None else _p(b, _f32p),
+                               None if r is None else _p(r, _f32p), _p(y, _f64p), _p(S, _f64p))
+        return y, S
 
     def quantize_block_q4_0(self, x: np.ndarray) -> np.ndarray:
         """One block of 32 fp32 values -> its 18 Q4_0 bytes."""

@@ -272,6 +272,33 @@ void orc_gemv_f64(const uint8_t *W, int64_t N, int64_t K, const uint8_t *xq, int
     }
 }
 
+/* The sequence epilogue (minfer README M19: the QKV bias and the residual
+ * adds run in the GEMVs' epilogues): y64[t][i] = (W.x)[t][i] + bias[i] +
+ * res[t][i] in fp64, either term absent when its pointer is NULL; S gains
+ * |bias[i]| + |res[t][i]|, the scale of the two fp32 adds' rounding. */
+void orc_gemv_ep_f64(const uint8_t *W, int64_t N, int64_t K, const uint8_t *xq, int T,
+                     const float *bias, const float *res, double *y64, double *S)
+{
+    orc_gemv_f64(W, N, K, xq, T, y64, S);
+    for (int t = 0; t < T; t++)
+        for (int64_t i = 0; i < N; i++) {
+            int64_t o = (int64_t)t * N + i;
+            if (bias) {
+                y64[o] += (double)bias[i];
+                S[o] += fabs((double)bias[i]);
+            }
+            if (res) {
+#if ORC_MUTANT == 18
+                double r = (double)res[i];              /* MUTANT: residual of token 0 for every token */
+#else
+                double r = (double)res[o];
+#endif
+                y64[o] += r;
+                S[o] += fabs(r);
+            }
+        }
+}
+
 /* Selected rows only: y64, S are [T][nrows]. */
 void orc_gemv_rows_f64(const uint8_t *W, int64_t N, int64_t K, const uint8_t *xq, int T,
                        const int64_t *rows, int64_t nrows, double *y64, double *S)

@@ -595,4 +595,30 @@ def pin_q8_to_q4_exact_blocks(o):
     assert np.array_equal(o.requant_f32_q4_0(x, N, K), got)
 
 
+# ---------------------------------------------------- sequence epilogue
+# y = W.x + bias + residual (minfer README M19: bias and residual adds in the
+# GEMVs' epilogues).  Zero-scale weight blocks make W.x exactly 0, so the
+# output is the bias plus the residual, exactly (both fp32, their fp64 sum
+# exact); without the terms the output is the plain GEMV's.
+
+def pin_epilogue_closed_forms(o):
+    rng = np.random.default_rng(1500)
+    N, K, T = 40, 96, 3
+    W = synth.q4_0_weights(1501, N, K).reshape(N, K // 32, 18).copy()
+    W[:, :, 0:2] = 0                                            # d = +0: every weight is 0
+    x = rng.standard_normal((T, K)).astype(np.float32)
+    xq = o.quantize(x)
+    bias = rng.standard_normal(N).astype(np.float32)
+    res = rng.standard_normal((T, N)).astype(np.float32)
+    y, S = o.gemv_ep(W.reshape(N, -1), N, K, xq, T, bias, res)
+    assert np.array_equal(y, bias.astype(np.float64)[None, :] + res.astype(np.float64))
+    assert np.array_equal(S, np.abs(bias.astype(np.float64))[None, :] + np.abs(res.astype(np.float64)))
+    yb, _ = o.gemv_ep(W.reshape(N, -1), N, K, xq, T, bias, None)
+    assert np.array_equal(yb, np.broadcast_to(bias.astype(np.float64), (T, N)))
+    Wr = synth.q4_0_weights(1502, N, K)
+    y0, S0 = o.gemv(Wr, N, K, xq, T)
+    y1, S1 = o.gemv_ep(Wr, N, K, xq, T, None, None)
+    assert np.array_equal(y0, y1) and np.array_equal(S0, S1)
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

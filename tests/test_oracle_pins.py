@@ -25,8 +25,9 @@ def test_pin(orc, pin):
 #  12 verify rule comparing a draft with its own prediction,
 #  13 Q8_0 weights read as unsigned, 14 SiLU with exp(+g),
 #  15 Q4_0 encoder scale from the magnitude, 16 Q4_0 codes rounded down,
-#  17 Q8_0 weights read as unsigned when requantised to Q4_0.
-MUTANTS = list(range(1, 18))
+#  17 Q8_0 weights read as unsigned when requantised to Q4_0,
+#  18 the epilogue's residual of token 0 used for every token.
+MUTANTS = list(range(1, 19))
 
 
 @pytest.fixture(scope="module")
