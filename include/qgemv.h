@@ -359,6 +359,30 @@ typedef struct {
     int64_t K;
 } qgemv_seq_f32_item;
 
+/* ---- Sequences with an output epilogue (minfer README M19: the QKV bias
+ * and the residual adds are the GEMVs' epilogues in the pages' decode step):
+ *   y[t][i] = (W.x[t])[i] + bias[i] + residual[t][i]
+ * with the GEMV value computed exactly as by qgemv_q4_0_seq (the same bits),
+ * then the two fp32 adds, each rounded to nearest, in that order; either
+ * term may be NULL.  x is planar Q8_0 (x_f32 = 0) or fp32 [T][K] quantised
+ * inside the kernel (x_f32 = 1).  bias [N] and residual [T][N] are 4-byte
+ * aligned inputs; residual may be y itself (y += W.x + bias in place) but
+ * must not otherwise overlap any output. */
+typedef struct {
+    const void *W;
+    const void *x;
+    float *y;
+    int64_t N;
+    int64_t K;
+    const float *bias;
+    const float *residual;
+} qgemv_seq_ep_item;
+
+/* Workspace bytes for qgemv_q4_0_seq_ep on this list (0 if invalid). */
+size_t qgemv_seq_ep_workspace_bytes(const qgemv_seq_ep_item *items, int n, int T, int x_f32);
+qgemv_status qgemv_q4_0_seq_ep(const qgemv_seq_ep_item *items, int n, qgemv_wlayout layout, int T, int x_f32,
+                               void *ws, size_t ws_bytes, qgemv_stream_t stream);
+
 /* Workspace bytes for qgemv_q4_0_seq_f32 on this list (0 if invalid). */
 size_t qgemv_seq_f32_workspace_bytes(const qgemv_seq_f32_item *items, int n, int T);
 

@@ -41,6 +41,12 @@ class SeqF32Item(ctypes.Structure):
                 ("N", ctypes.c_int64), ("K", ctypes.c_int64)]
 
 
+class SeqEpItem(ctypes.Structure):
+    _fields_ = [("W", ctypes.c_void_p), ("x", ctypes.c_void_p), ("y", ctypes.c_void_p),
+                ("N", ctypes.c_int64), ("K", ctypes.c_int64), ("bias", ctypes.c_void_p),
+                ("residual", ctypes.c_void_p)]
+
+
 class GatherMatrix(ctypes.Structure):
     _fields_ = [("W", ctypes.c_void_p), ("expert_stride", ctypes.c_int64), ("xq", ctypes.c_void_p),
                 ("xq_stride", ctypes.c_int64), ("y", ctypes.c_void_p), ("y_stride", ctypes.c_int64),
@@ -87,6 +93,8 @@ _SIGS = {
     "qgemv_q4_0_seq": ([ctypes.POINTER(SeqItem), _I32, _I32, _I32, _VP, _SZ, _VP], _I32),
     "qgemv_seq_f32_workspace_bytes": ([ctypes.POINTER(SeqF32Item), _I32, _I32], _SZ),
     "qgemv_q4_0_seq_f32": ([ctypes.POINTER(SeqF32Item), _I32, _I32, _I32, _VP, _SZ, _VP], _I32),
+    "qgemv_seq_ep_workspace_bytes": ([ctypes.POINTER(SeqEpItem), _I32, _I32, _I32], _SZ),
+    "qgemv_q4_0_seq_ep": ([ctypes.POINTER(SeqEpItem), _I32, _I32, _I32, _I32, _VP, _SZ, _VP], _I32),
     "qgemv_gather_workspace_bytes": ([ctypes.POINTER(GatherMatrix), _I32, _I32, _I32], _SZ),
     "qgemv_q4_0_gather": ([ctypes.POINTER(GatherMatrix), _I32, _VP, _I32, _I32, _I32, _I32, _VP, _SZ, _VP], _I32),
     "qgemv_gather_f32_workspace_bytes": ([ctypes.POINTER(GatherF32Matrix), _I32, _I32, _I32], _SZ),
@@ -345,6 +353,28 @@ def seq_f32_workspace_bytes(items: ctypes.Array, T: int) -> int:
 def gemv_seq_f32(items: ctypes.Array, layout: int, T: int, ws, stream=None):
     _check(lib().qgemv_q4_0_seq_f32(items, len(items), layout, T, _ptr(ws), ws.numel(), _stream(stream)),
            "qgemv_q4_0_seq_f32")
+
+
+def seq_ep_items(entries) -> ctypes.Array:
+    """entries: iterable of (W, x, y, N, K, bias, residual) with CUDA tensors;
+    x planar Q8_0 or fp32 [T, K] (the call's x_f32 says which); bias [N] and
+    residual [T, N] fp32 or None (residual may be y)."""
+    entries = list(entries)
+    arr = (SeqEpItem * len(entries))()
+    for i, (W, x, y, N, K, b, r) in enumerate(entries):
+        arr[i] = SeqEpItem(W.data_ptr(), x.data_ptr(), y.data_ptr(), N, K,
+                           None if b is None else b.data_ptr(), None if r is None else r.data_ptr())
+    return arr
+
+
+def seq_ep_workspace_bytes(items: ctypes.Array, T: int, x_f32: bool = False) -> int:
+    return int(lib().qgemv_seq_ep_workspace_bytes(items, len(items), T, int(x_f32)))
+
+
+def gemv_seq_ep(items: ctypes.Array, layout: int, T: int, ws, x_f32: bool = False, stream=None):
+    """y = W . x + bias + residual for every item, in one launch per 200 items."""
+    _check(lib().qgemv_q4_0_seq_ep(items, len(items), layout, T, int(x_f32), _ptr(ws), ws.numel(), _stream(stream)),
+           "qgemv_q4_0_seq_ep")
 
 
 def gather_mats(entries) -> ctypes.Array:

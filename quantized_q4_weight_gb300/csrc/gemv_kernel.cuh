@@ -1261,11 +1261,24 @@ struct Top2Lane {
     unsigned long long b1[S], b2[S];
 };
 
+// The output epilogue of a sequence launch (minfer README M19: the QKV bias
+// and the residual adds run in the GEMV's epilogue): y = (v + bias[row]) +
+// residual[t][row], each add an fp32 operation rounded to nearest; either
+// term may be absent.  The residual is read with a plain load: it may be y
+// itself, read and then written by this thread.
+__device__ __forceinline__ float apply_epilogue(float v, const float *bias, const float *res, long long yi, int row)
+{
+    if (bias != nullptr) v = __fadd_rn(v, __ldg(bias + row));
+    if (res != nullptr) v = __fadd_rn(v, res[yi]);
+    return v;
+}
+
 // Write this lane's finished outputs (rows below `rows`) and fold them into
-// the top-2 keys of their tokens.
+// the top-2 keys of their tokens.  bias / res: the sequence epilogue (or nullptr).
 template <int T, bool MMA, bool ARGMAX>
 __device__ __forceinline__ void store_outputs(float *ye, int N, int row0, int rows, int r8, int j,
-                                              const float (&yv)[LaneOut<T, MMA>::N], Top2Lane<T, MMA> &st)
+                                              const float (&yv)[LaneOut<T, MMA>::N], Top2Lane<T, MMA> &st,
+                                              const float *bias = nullptr, const float *res = nullptr)
 {
     using LO = LaneOut<T, MMA>;
     using TL2 = Top2Lane<T, MMA>;
@@ -1273,7 +1286,10 @@ __device__ __forceinline__ void store_outputs(float *ye, int N, int row0, int ro
     for (int k = 0; k < LO::N; ++k) {
         const int lr = LO::row(k, r8), t = LO::tok(k, j);
         if (lr >= rows) continue;
-        if (LO::owner(k, j) && ye != nullptr) ye[static_cast<long long>(t) * N + row0 + lr] = yv[k];
+        if (LO::owner(k, j) && ye != nullptr) {
+            const long long yi = static_cast<long long>(t) * N + row0 + lr;
+            ye[yi] = ARGMAX ? yv[k] : apply_epilogue(yv[k], bias, res, yi, row0 + lr);
+        }
         // static slot: (k & 1) on the tensor-core path, (k % T) / 4 on dp4a
         const int sl = MMA ? (k & 1) : ((k % T) >> 2);
         if (ARGMAX && t < T && (MMA || TL2::jt(k % T) == j))
@@ -1297,7 +1313,7 @@ __device__ __forceinline__ bool wait_flag(volatile int *flag, volatile int *abor
     return true;
 }
 
-template <int T, int MAXG, bool ARGMAX, bool MMA>
+template <int T, int MAXG, bool ARGMAX, bool MMA, bool EPI>
 __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_kernel(const __grid_constant__ Params<MAXG> P)
 {
     using LO = LaneOut<T, MMA>;
@@ -1653,7 +1669,9 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
                     __syncwarp();
                     if (lane == 0) hflag[warp] = 1;
                 } else if (!w.bad) {
-                    store_outputs<T, MMA, ARGMAX>(R.y, R.N, li * SLAB_ROWS, rows, r8, j, yv, st);
+                    const Group &gg = gcache[R.gi - g0];
+                    store_outputs<T, MMA, ARGMAX>(R.y, R.N, li * SLAB_ROWS, rows, r8, j, yv, st,
+                                                  EPI ? gg.bias : nullptr, EPI ? gg.res : nullptr);
                 } else if (lane == 0) {
                     atomicCAS(H.status, 0u, ST_BAD_ID);
                 }
@@ -1671,7 +1689,13 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
                     const float *p = pr + static_cast<long long>(sl) * R.nseg * T * 16 + t * 16 + row;
                     float v = p[0];
                     for (int sg = 1; sg < R.nseg; ++sg) v = __fadd_rn(v, p[static_cast<long long>(sg) * T * 16]);
-                    R.y[static_cast<long long>(t) * R.N + (R.first_local + sl) * SLAB_ROWS + row] = v;
+                    const int orow = (R.first_local + sl) * SLAB_ROWS + row;
+                    const long long yi = static_cast<long long>(t) * R.N + orow;
+                    if constexpr (EPI) {
+                        const Group &gg = gcache[R.gi - g0];
+                        v = apply_epilogue(v, gg.bias, gg.res, yi, orow);
+                    }
+                    R.y[yi] = v;
                 }
             }
         }
@@ -1808,7 +1832,10 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
                                 float v = __ldcg(pb + t * 16 + lane);
                                 for (int s2 = 1; s2 < g.nseg; ++s2)
                                     v = __fadd_rn(v, __ldcg(pb + (s2 * T + t) * 16 + lane));
-                                if (ye != nullptr) ye[static_cast<long long>(t) * N + row] = v;
+                                if (ye != nullptr) {
+                                    const long long yi = static_cast<long long>(t) * N + row;
+                                    ye[yi] = EPI ? apply_epilogue(v, g.bias, g.res, yi, row) : v;
+                                }
                                 if (ARGMAX) kt[ARGMAX ? t : 0] = argmax_key(v, static_cast<unsigned>(row));
                             }
                         }
@@ -1825,7 +1852,8 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
                         if (lane == 0) *cnt = 0u;
                     }
                 } else {
-                    store_outputs<T, MMA, ARGMAX>(ye, N, row0, inf.rows, r8, j, yv, st);
+                    store_outputs<T, MMA, ARGMAX>(ye, N, row0, inf.rows, r8, j, yv, st, EPI ? g.bias : nullptr,
+                                                  EPI ? g.res : nullptr);
                 }
             }
             ra = rb;

@@ -5,4 +5,6 @@ namespace qg {
 template cudaError_t launch_stream<1, MAXG_SMALL, false, false>(const Params<MAXG_SMALL> &, int, size_t, cudaStream_t, bool);
 template cudaError_t launch_stream<1, MAXG_SMALL, true, false>(const Params<MAXG_SMALL> &, int, size_t, cudaStream_t, bool);
 template cudaError_t launch_stream<1, MAXG_SEQ, false, false>(const Params<MAXG_SEQ> &, int, size_t, cudaStream_t, bool);
+// the sequence epilogue, on the default path for T = 1 (dp4a)
+template cudaError_t launch_stream<1, MAXG_SEQ, false, false, true>(const Params<MAXG_SEQ> &, int, size_t, cudaStream_t, bool);
 }  // namespace qg

@@ -8,4 +8,6 @@ template cudaError_t launch_stream<5, MAXG_SEQ, false, false>(const Params<MAXG_
 template cudaError_t launch_stream<5, MAXG_SMALL, false, true>(const Params<MAXG_SMALL> &, int, size_t, cudaStream_t, bool);
 template cudaError_t launch_stream<5, MAXG_SMALL, true, true>(const Params<MAXG_SMALL> &, int, size_t, cudaStream_t, bool);
 template cudaError_t launch_stream<5, MAXG_SEQ, false, true>(const Params<MAXG_SEQ> &, int, size_t, cudaStream_t, bool);
+// the sequence epilogue, on the default path for T = 5 (tensor cores)
+template cudaError_t launch_stream<5, MAXG_SEQ, false, true, true>(const Params<MAXG_SEQ> &, int, size_t, cudaStream_t, bool);
 }  // namespace qg

@@ -9,10 +9,10 @@
 
 namespace qg {
 
-template <int T, int MAXG, bool ARGMAX, bool MMA>
+template <int T, int MAXG, bool ARGMAX, bool MMA, bool EPI>
 cudaError_t launch_stream(const Params<MAXG> &P, int grid, size_t smem, cudaStream_t st, bool pdl)
 {
-    auto kern = qgemv_stream_kernel<T, MAXG, ARGMAX, MMA>;
+    auto kern = qgemv_stream_kernel<T, MAXG, ARGMAX, MMA, EPI>;
     // The dynamic shared-memory limit is a per-device function attribute:
     // raise it once per device to the largest size any launch asks for.
     static std::atomic<unsigned long long> raised{0};

@@ -95,6 +95,8 @@ struct GroupSpec {
     long long y_stride;
     long long N, K;
     int count;
+    const float *bias = nullptr;  // sequence epilogue: bias[N] (count 1 only)
+    const float *res = nullptr;   // sequence epilogue: residual[T][N] (count 1 only; may be y)
 };
 
 // Launch plan: the kernel parameter block (without device pointers into the
@@ -159,6 +161,13 @@ qgemv_status make_plan(const GroupSpec *gs, int n, int T, bool ggml, bool argmax
         g.xq_stride = s.xq_stride;
         g.y = s.y;
         g.y_stride = s.y_stride;
+        if (s.bias != nullptr || s.res != nullptr) {
+            // a sequence item (one instance): the stride words carry the epilogue
+            if (s.count != 1 || s.w_stride != 0 || s.y_stride != 0) return QGEMV_ERR_INTERNAL;
+            g.bias = s.bias;
+            g.res = s.res;
+            P.epilogue = 1;
+        }
         g.N = static_cast<int>(s.N);
         g.K = static_cast<int>(s.K);
         g.count = s.count;
@@ -266,6 +275,25 @@ cudaError_t dispatch_T(const Params<MAXG> &P, int T, bool mma, int grid, size_t 
     default: return cudaErrorInvalidValue;
     }
 #undef QG_CASE
+}
+
+// Sequence launches with the output epilogue: compiled for each T's default
+// path only (dp4a below five tokens, tensor cores from five); a launch on the
+// other path (moved by qgemv_set_tuning) is refused with cudaErrorNotSupported.
+cudaError_t dispatch_ep(const Params<MAXG_SEQ> &P, int T, bool mma, int grid, size_t smem, cudaStream_t st)
+{
+    if (mma != (T >= kDefaultMmaMinT)) return cudaErrorNotSupported;
+    switch (T) {
+    case 1: return launch_stream<1, MAXG_SEQ, false, false, true>(P, grid, smem, st, true);
+    case 2: return launch_stream<2, MAXG_SEQ, false, false, true>(P, grid, smem, st, true);
+    case 3: return launch_stream<3, MAXG_SEQ, false, false, true>(P, grid, smem, st, true);
+    case 4: return launch_stream<4, MAXG_SEQ, false, false, true>(P, grid, smem, st, true);
+    case 5: return launch_stream<5, MAXG_SEQ, false, true, true>(P, grid, smem, st, true);
+    case 6: return launch_stream<6, MAXG_SEQ, false, true, true>(P, grid, smem, st, true);
+    case 7: return launch_stream<7, MAXG_SEQ, false, true, true>(P, grid, smem, st, true);
+    case 8: return launch_stream<8, MAXG_SEQ, false, true, true>(P, grid, smem, st, true);
+    default: return cudaErrorInvalidValue;
+    }
 }
 
 // CTAs per SM for a T-token launch, and the dynamic shared-memory budget of
@@ -799,7 +827,8 @@ size_t qgemv_seq_workspace_bytes(const qgemv_seq_item *items, int n, int T)
 }
 
 static qgemv_status check_seq(const qgemv_seq_item *items, int n, qgemv_wlayout layout, int T, void *ws,
-                              size_t ws_bytes, bool xf32 = false)
+                              size_t ws_bytes, bool xf32 = false, const float *const *bias = nullptr,
+                              const float *const *res = nullptr)
 {
     if (!items || n < 1 || T < 1 || T > 8) return QGEMV_ERR_INVALID_ARG;
     if (layout != QGEMV_W_GGML && layout != QGEMV_W_PACKED) return QGEMV_ERR_INVALID_ARG;
@@ -822,6 +851,15 @@ static qgemv_status check_seq(const qgemv_seq_item *items, int n, qgemv_wlayout 
         v.push_back(Tagged{range(a.W, 18ll * a.N * (a.K / QK)), false});
         v.push_back(Tagged{range(a.xq, xf32 ? 4ll * T * a.K : xq_bytes_host(T, a.K)), false});
         v.push_back(Tagged{range(a.y, 4ll * T * a.N), true});
+        // epilogue inputs: a residual equal to y is read in place (same element, same thread)
+        if (bias && bias[i]) {
+            if (!aligned(bias[i], 4)) return QGEMV_ERR_MISALIGNED;
+            v.push_back(Tagged{range(bias[i], 4ll * a.N), false});
+        }
+        if (res && res[i] && res[i] != a.y) {
+            if (!aligned(res[i], 4)) return QGEMV_ERR_MISALIGNED;
+            v.push_back(Tagged{range(res[i], 4ll * T * a.N), false});
+        }
     }
     std::sort(v.begin(), v.end(), [](const Tagged &x, const Tagged &y) { return x.r.lo < y.r.lo; });
     uintptr_t hi_any = 0, hi_out = 0;
@@ -837,7 +875,8 @@ static qgemv_status check_seq(const qgemv_seq_item *items, int n, qgemv_wlayout 
 // MAXG_SEQ items.  xf32: the items' activations are fp32 x[T][K], quantised
 // inside the GEMV kernel.
 static qgemv_status launch_seq(const qgemv_seq_item *items, int n, qgemv_wlayout layout, int T, void *ws,
-                               size_t ws_bytes, cudaStream_t st, bool xf32)
+                               size_t ws_bytes, cudaStream_t st, bool xf32, const float *const *bias = nullptr,
+                               const float *const *res = nullptr)
 {
     DevInfo dev;
     qgemv_status s = device_info(dev);
@@ -849,6 +888,8 @@ static qgemv_status launch_seq(const qgemv_seq_item *items, int n, qgemv_wlayout
         for (int i = 0; i < cn; ++i) {
             const qgemv_seq_item &it = items[c0 + i];
             gs[i] = GroupSpec{it.W, 0, it.xq, 0, it.y, 0, it.N, it.K, 1};
+            gs[i].bias = bias ? bias[c0 + i] : nullptr;
+            gs[i].res = res ? res[c0 + i] : nullptr;
         }
         int cps = ctas_per_sm_for(T, true);
         s = plan_launch<MAXG_SEQ>(gs.data(), cn, T, layout == QGEMV_W_GGML, false, static_cast<uint8_t *>(ws), dev,
@@ -869,8 +910,13 @@ static qgemv_status launch_seq(const qgemv_seq_item *items, int n, qgemv_wlayout
             }
         }
         set_cta_groups(pl->P, grid);
-        if (dispatch_T<MAXG_SEQ, false>(pl->P, T, mma_for(T), grid, pl->smem, st, true) != cudaSuccess)
+        if (pl->P.epilogue) {
+            const cudaError_t e = dispatch_ep(pl->P, T, mma_for(T), grid, pl->smem, st);
+            if (e == cudaErrorNotSupported) return QGEMV_ERR_UNSUPPORTED;
+            if (e != cudaSuccess) return QGEMV_ERR_CUDA;
+        } else if (dispatch_T<MAXG_SEQ, false>(pl->P, T, mma_for(T), grid, pl->smem, st, true) != cudaSuccess) {
             return QGEMV_ERR_CUDA;
+        }
     }
     return QGEMV_OK;
 }
@@ -912,6 +958,44 @@ qgemv_status qgemv_q4_0_seq_f32(const qgemv_seq_f32_item *items, int n, qgemv_wl
     const qgemv_status s = check_seq(sq.data(), n, layout, T, ws, ws_bytes, true);
     if (s != QGEMV_OK) return s;
     return launch_seq(sq.data(), n, layout, T, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream), true);
+}
+
+static bool seq_ep_items(const qgemv_seq_ep_item *items, int n, std::vector<qgemv_seq_item> &sq,
+                         std::vector<const float *> &bias, std::vector<const float *> &res)
+{
+    sq.resize(n);
+    bias.resize(n);
+    res.resize(n);
+    for (int i = 0; i < n; ++i) {
+        if (!shape_ok(items[i].N, items[i].K)) return false;
+        sq[i] = qgemv_seq_item{items[i].W, items[i].x, items[i].y, items[i].N, items[i].K};
+        bias[i] = items[i].bias;
+        res[i] = items[i].residual;
+    }
+    return true;
+}
+
+size_t qgemv_seq_ep_workspace_bytes(const qgemv_seq_ep_item *items, int n, int T, int x_f32)
+{
+    (void)x_f32;  // the same plans either way
+    if (!items || n < 1 || T < 1 || T > 8) return 0;
+    std::vector<qgemv_seq_item> sq;
+    std::vector<const float *> bias, res;
+    if (!seq_ep_items(items, n, sq, bias, res)) return 0;
+    return qgemv_seq_workspace_bytes(sq.data(), n, T);
+}
+
+qgemv_status qgemv_q4_0_seq_ep(const qgemv_seq_ep_item *items, int n, qgemv_wlayout layout, int T, int x_f32,
+                               void *ws, size_t ws_bytes, qgemv_stream_t stream)
+{
+    if (!items || n < 1 || T < 1 || T > 8 || (x_f32 != 0 && x_f32 != 1)) return QGEMV_ERR_INVALID_ARG;
+    std::vector<qgemv_seq_item> sq;
+    std::vector<const float *> bias, res;
+    if (!seq_ep_items(items, n, sq, bias, res)) return QGEMV_ERR_INVALID_ARG;
+    const qgemv_status s = check_seq(sq.data(), n, layout, T, ws, ws_bytes, x_f32 != 0, bias.data(), res.data());
+    if (s != QGEMV_OK) return s;
+    return launch_seq(sq.data(), n, layout, T, ws, ws_bytes, reinterpret_cast<cudaStream_t>(stream), x_f32 != 0,
+                      bias.data(), res.data());
 }
 
 extern "C++" {

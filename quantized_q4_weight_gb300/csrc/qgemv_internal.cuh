@@ -37,11 +37,20 @@ constexpr unsigned ST_BAD_ID = 7;
 // of a routed-expert gather (count = slots).
 struct Group {
     const uint8_t *W;       // instance 0 weights (packed or GGML)
-    long long w_stride;     // bytes between instances (experts)
+    // The instance strides mean something only in gathers (count > 1 or
+    // expert ids); a launch with ParamHead::epilogue set is a sequence of
+    // single instances and reads the same words as its epilogue pointers.
+    union {
+        long long w_stride;  // gathers: bytes between instances (experts)
+        const float *bias;   // epilogue launches: bias[N] added to y (or nullptr)
+    };
     const uint8_t *xq;      // planar Q8_0 of slot 0
     long long xq_stride;    // bytes between slots (0: shared)
     float *y;               // y[T][N] of slot 0
-    long long y_stride;     // floats between slots
+    union {
+        long long y_stride;  // gathers: floats between slots
+        const float *res;    // epilogue launches: residual[T][N] added after the bias (or nullptr; may be y)
+    };
     int N, K, count, split;
     int nb, nseg, nslabs, tail_rows;  // nslabs: slab items (GGML: ceil(N/16)); tail: packed N%16
     int items_per_inst;               // nslabs * split + (tail_rows > 0)
@@ -76,6 +85,8 @@ struct ParamHead {
     long long *am_idx;            // argmax: result [T] (or nullptr)
     long long *am_idx2;           // top-2: rows [T][2] (or nullptr)
     float *am_val2;               // top-2: values [T][2] (with am_idx2)
+    int epilogue;                 // groups carry bias / residual pointers (sequences only)
+    int epilogue_unused;
     float *sg_part;               // small groups: per-CTA segment sums (or nullptr)
     int sg_stride;                //   floats per CTA region
     int sg_ctas;                  //   CTAs 0..sg_ctas-1 have a region

@@ -37,7 +37,8 @@ cudaError_t launch_verify_commit(const long long *tokens, const long long *pred,
 
 // The streaming GEMV kernel, one instantiation per (T, parameter-block size,
 // argmax, tensor-core path).  Defined in gemv_t<T>.cu.
-template <int T, int MAXG, bool ARGMAX, bool MMA>
+// EPI: the sequence output epilogue (bias, residual) is compiled in.
+template <int T, int MAXG, bool ARGMAX, bool MMA, bool EPI = false>
 cudaError_t launch_stream(const Params<MAXG> &P, int grid, size_t smem, cudaStream_t st, bool pdl);
 
 }  // namespace qg
