@@ -81,9 +81,10 @@ def _upload_packed(q, torch, Wg, N, K, dev):
     return Wp
 
 
-def build_layerset(name, layer, layers, T, seed, dev, keep_host=False):
+def build_layerset(name, layer, layers, T, seed, dev, keep_host=False, epilogue=False):
     """Layer set in order.  One step = one fp32-input sequence call (one
-    persistent launch that also quantises the activations)."""
+    persistent launch that also quantises the activations).  epilogue: qkv
+    adds a bias [N], o and down add a residual [T][N] (seeded inputs)."""
     import torch
     q = _q()
     wl = Workload(name, T)
@@ -113,23 +114,51 @@ def build_layerset(name, layer, layers, T, seed, dev, keep_host=False):
         wl.x_bytes += 4 * T * K
         wl.y_bytes += 4 * T * N
         wl.xq_bytes += q.xq_bytes(T, K)
-    wl.items_f32 = q.seq_f32_items([(wl.W[i], wl.x[i], wl.y[i], N, K) for i, (_, N, K) in enumerate(mats)])
-    wl.items_xq = q.seq_items([(wl.W[i], wl.xq[i], wl.y[i], N, K) for i, (_, N, K) in enumerate(mats)])
-    wl.ws = q.new_workspace(q.seq_f32_workspace_bytes(wl.items_f32, T), dev)
-    wl.ws_xq = q.new_workspace(q.seq_workspace_bytes(wl.items_xq, T), dev)
     wl.mats = mats
     wl.launches = 1
+    wl.inputs, wl.outputs = [wl.x_all], [wl.y_all]
+    if not epilogue:
+        wl.items_f32 = q.seq_f32_items([(wl.W[i], wl.x[i], wl.y[i], N, K) for i, (_, N, K) in enumerate(mats)])
+        wl.items_xq = q.seq_items([(wl.W[i], wl.xq[i], wl.y[i], N, K) for i, (_, N, K) in enumerate(mats)])
+        wl.ws = q.new_workspace(q.seq_f32_workspace_bytes(wl.items_f32, T), dev)
+        wl.ws_xq = q.new_workspace(q.seq_workspace_bytes(wl.items_xq, T), dev)
 
-    def step(stream=None):
-        q.gemv_seq_f32(wl.items_f32, q.W_PACKED, T, wl.ws, stream=stream)
+        def step(stream=None):
+            q.gemv_seq_f32(wl.items_f32, q.W_PACKED, T, wl.ws, stream=stream)
 
-    def kernel(stream=None):
-        q.gemv_seq(wl.items_xq, q.W_PACKED, T, wl.ws_xq, stream=stream)
+        def kernel(stream=None):
+            q.gemv_seq(wl.items_xq, q.W_PACKED, T, wl.ws_xq, stream=stream)
+    else:
+        bias, res = [None] * len(mats), [None] * len(mats)
+        for i, (nm, N, K) in enumerate(mats):
+            rng = np.random.default_rng([seed, 7, i])
+            if nm.endswith(".qkv"):
+                bias[i] = torch.from_numpy(rng.standard_normal(N).astype(np.float32)).to(dev)
+                wl.x_bytes += 4 * N
+                wl.xq_bytes += 4 * N
+            elif nm.endswith(".o") or nm.endswith(".down"):
+                res[i] = torch.from_numpy(rng.standard_normal((T, N)).astype(np.float32)).to(dev)
+                wl.x_bytes += 4 * T * N
+                wl.xq_bytes += 4 * T * N
+        wl.bias, wl.res = bias, res
+        wl.items_f32 = q.seq_ep_items([(wl.W[i], wl.x[i], wl.y[i], N, K, bias[i], res[i])
+                                       for i, (_, N, K) in enumerate(mats)])
+        wl.items_xq = q.seq_ep_items([(wl.W[i], wl.xq[i], wl.y[i], N, K, bias[i], res[i])
+                                      for i, (_, N, K) in enumerate(mats)])
+        wl.ws = q.new_workspace(q.seq_ep_workspace_bytes(wl.items_f32, T, True), dev)
+        wl.ws_xq = q.new_workspace(q.seq_ep_workspace_bytes(wl.items_xq, T, False), dev)
+        wl.inputs = [wl.x_all] + [b for b in bias if b is not None] + [r for r in res if r is not None]
+
+        def step(stream=None):
+            q.gemv_seq_ep(wl.items_f32, q.W_PACKED, T, wl.ws, x_f32=True, stream=stream)
+
+        def kernel(stream=None):
+            q.gemv_seq_ep(wl.items_xq, q.W_PACKED, T, wl.ws_xq, x_f32=False, stream=stream)
 
     wl.step, wl.kernel = step, kernel
-    wl.inputs, wl.outputs = [wl.x_all], [wl.y_all]
     wl.config = {"workload": name, "layers": layers, "gemvs": len(mats), "T": T,
                  "weight_bytes": wl.w_bytes,
+                 "epilogue": "bias on qkv, residual on o and down (read as inputs)" if epilogue else None,
                  "l2_defeat": "weights larger than the 126 MB L2, each streamed once per step"}
     return wl
 
@@ -428,7 +457,8 @@ def build_workload(name: str, dev, T: int | None = None, keep_host: bool = False
     spec = synth.WORKLOADS[name]
     if spec["kind"] == "seq":
         T = T or spec.get("T", 1)
-        return build_layerset(name, spec["layer"], layers or spec["layers"], T, spec["seed"], dev, keep_host)
+        return build_layerset(name, spec["layer"], layers or spec["layers"], T, spec["seed"], dev, keep_host,
+                              spec.get("epilogue", False))
     if spec["kind"] == "argmax":
         return build_lm_head(T or spec["T"], spec["seed"], dev, spec["copies"], keep_host, spec["N"], spec["K"])
     if spec["kind"] == "verify":

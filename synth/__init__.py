@@ -122,6 +122,9 @@ WORKLOADS = {
     "single_1536": dict(kind="single", N=1536, K=1536, T=1, seed=0),
     # 28-layer Qwen2.5-1.5B-shaped layer set, T=1, in layer order
     "qwen2.5-1.5b_layerset": dict(kind="seq", layer=QWEN25_1P5B_LAYER, layers=28, T=1, seed=1000),
+    # the same with the decode step's epilogues: bias on qkv, a residual added to o and down
+    "qwen2.5-1.5b_layerset_ep": dict(kind="seq", layer=QWEN25_1P5B_LAYER, layers=28, T=1, seed=1000,
+                                     epilogue=True),
     # lm_head 151936x1536 with fused argmax, 4 weight copies in rotation
     "lm_head_argmax": dict(kind="argmax", N=151936, K=1536, T=1, copies=4, seed=2000),
     # lm_head verify step: 8 positions (current token + 7 drafts), top-2 rows

@@ -50,6 +50,33 @@ def test_layer_sets_sampled(orc, name, T):
         check_close(y_step[i][:, rows], y64, S, f"{name} {nm}")
 
 
+def test_layer_set_epilogue_full(orc):
+    """The 28-layer set with its epilogues (qkv bias, o and down residuals) as
+    bench.py times it: every GEMV's y equals the plain sequence's y plus the
+    bias and the residual (torch's fp32 adds), and the first layer's outputs
+    are within the bound of the oracle's fp64 W.x + bias + residual."""
+    wl = bench.build_workload("qwen2.5-1.5b_layerset_ep", DEV, keep_host=True)
+    wl.step()
+    torch.cuda.synchronize()
+    assert q.device_status() == 0
+    y_ep = [host(y).copy() for y in wl.y]
+    plain = q.seq_f32_items([(wl.W[i], wl.x[i], wl.y[i], N, K) for i, (_, N, K) in enumerate(wl.mats)])
+    q.gemv_seq_f32(plain, q.W_PACKED, wl.T, q.new_workspace(q.seq_f32_workspace_bytes(plain, wl.T)))
+    torch.cuda.synchronize()
+    for i, (nm, N, K) in enumerate(wl.mats):
+        want = wl.y[i]
+        if wl.bias[i] is not None:
+            want = want + wl.bias[i][None, :]
+        if wl.res[i] is not None:
+            want = want + wl.res[i]
+        assert np.array_equal(y_ep[i].view(np.int32), host(want).view(np.int32)), nm
+        if i < 5:
+            b = None if wl.bias[i] is None else host(wl.bias[i])
+            r = None if wl.res[i] is None else host(wl.res[i])
+            y64, S = orc.gemv_ep(wl.host[i], N, K, orc.quantize(host(wl.x[i])), wl.T, b, r)
+            check_close(y_ep[i], y64, S, f"epilogue {nm}")
+
+
 def test_lm_head_argmax_full(orc):
     wl = bench.build_workload("lm_head_argmax", DEV, keep_host=True)
     y = torch.empty((wl.T, wl.N), dtype=torch.float32, device=DEV)
