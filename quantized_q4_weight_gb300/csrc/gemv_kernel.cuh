@@ -1297,6 +1297,43 @@ __device__ __forceinline__ void store_outputs(float *ye, int N, int row0, int ro
     }
 }
 
+// The epilogue's terms of this lane's outputs, loaded when a visit starts so
+// that their latency hides behind the visit's segments (a load at the store
+// stalls the streaming warp once per slab).  Absent terms are not loaded.
+template <int T, bool MMA>
+__device__ __forceinline__ void load_epilogue(const float *bias, const float *res, int N, int row0, int rows, int r8,
+                                              int j, bool stores, float (&eb)[LaneOut<T, MMA>::N],
+                                              float (&er)[LaneOut<T, MMA>::N])
+{
+    using LO = LaneOut<T, MMA>;
+#pragma unroll
+    for (int k = 0; k < LO::N; ++k) {
+        const int lr = LO::row(k, r8), t = LO::tok(k, j);
+        const bool own = stores && LO::owner(k, j) && lr < rows;
+        eb[k] = (own && bias != nullptr) ? __ldg(bias + row0 + lr) : 0.0f;
+        er[k] = (own && res != nullptr) ? res[static_cast<long long>(t) * N + row0 + lr] : 0.0f;
+    }
+}
+
+// store_outputs with the epilogue terms already loaded (non-argmax launches).
+template <int T, bool MMA>
+__device__ __forceinline__ void store_outputs_ep(float *ye, int N, int row0, int rows, int r8, int j,
+                                                 const float (&yv)[LaneOut<T, MMA>::N],
+                                                 const float (&eb)[LaneOut<T, MMA>::N],
+                                                 const float (&er)[LaneOut<T, MMA>::N], bool has_b, bool has_r)
+{
+    using LO = LaneOut<T, MMA>;
+#pragma unroll
+    for (int k = 0; k < LO::N; ++k) {
+        const int lr = LO::row(k, r8), t = LO::tok(k, j);
+        if (lr >= rows || !LO::owner(k, j)) continue;
+        float v = yv[k];
+        if (has_b) v = __fadd_rn(v, eb[k]);
+        if (has_r) v = __fadd_rn(v, er[k]);
+        ye[static_cast<long long>(t) * N + row0 + lr] = v;
+    }
+}
+
 // Bounded spin on a shared-memory flag written by another warp of the CTA.
 __device__ __forceinline__ bool wait_flag(volatile int *flag, volatile int *abort_flag, unsigned *status)
 {
@@ -1604,6 +1641,16 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
                 float yv[NO];
     #pragma unroll
                 for (int k = 0; k < NO; ++k) yv[k] = 0.0f;
+                float eb[EPI ? NO : 1], er[EPI ? NO : 1];
+                const float *ep_bias = nullptr, *ep_res = nullptr;
+                if constexpr (EPI) {
+                    // this warp stores the slab's outputs: fetch the epilogue's terms now
+                    const Group &gg = gcache[R.gi - g0];
+                    ep_bias = gg.bias;
+                    ep_res = gg.res;
+                    load_epilogue<T, MMA>(ep_bias, ep_res, R.N, li * SLAB_ROWS, rows, r8, j,
+                                          !small_grp && seg_end == w.nseg && !w.bad, eb, er);
+                }
                 if (s_first > 0 && !small_grp) {
                     // tail of a slab begun by warp - 1: continue from its ordered sum
                     if (lane == 0) wait_flag(&hflag[warp - 1], abort_flag, H.status);
@@ -1669,9 +1716,11 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
                     __syncwarp();
                     if (lane == 0) hflag[warp] = 1;
                 } else if (!w.bad) {
-                    const Group &gg = gcache[R.gi - g0];
-                    store_outputs<T, MMA, ARGMAX>(R.y, R.N, li * SLAB_ROWS, rows, r8, j, yv, st,
-                                                  EPI ? gg.bias : nullptr, EPI ? gg.res : nullptr);
+                    if constexpr (EPI)
+                        store_outputs_ep<T, MMA>(R.y, R.N, li * SLAB_ROWS, rows, r8, j, yv, eb, er, ep_bias != nullptr,
+                                                 ep_res != nullptr);
+                    else
+                        store_outputs<T, MMA, ARGMAX>(R.y, R.N, li * SLAB_ROWS, rows, r8, j, yv, st);
                 } else if (lane == 0) {
                     atomicCAS(H.status, 0u, ST_BAD_ID);
                 }
