@@ -793,7 +793,7 @@ def main(argv=None):
                                          for T, r in results.items()}
         if not args.no_cpu_baseline:
             v1, _, desc1 = oracle_sample(args.workload, budget_s=4.0, min_s=2.0, threads=1)
-            v, cores, desc = oracle_sample(args.workload, threads=os.cpu_count() or 1)
+            v, cores, desc = oracle_sample(args.workload, min_s=10.0, threads=os.cpu_count() or 1)
             head["cpu_baseline"] = {"value": round(v, 4), "unit": UNIT, "cores": cores, "kind": "oracle",
                                     "sample": desc, "single_thread_value": round(v1, 4),
                                     "single_thread_sample": desc1, "cpu": cpu_model()}
