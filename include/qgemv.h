@@ -274,6 +274,18 @@ qgemv_status qgemv_q4_0_ffn(const void *W_gate, const void *W_up, const void *W_
                             const float *x, float *y, int64_t d_model, int64_t d_ff, int T,
                             void *ws, size_t ws_bytes, qgemv_stream_t stream);
 
+/* The same chain with a residual added to the down projection's output
+ * (the decode step's FFN block: y = residual + W_down . h; minfer README
+ * M19).  The down launch is a one-item sequence with the residual epilogue:
+ * y = (W_down . h) + residual[t][i], one fp32 add after the same GEMV bits.
+ * residual [T][d_model] fp32, 4-byte aligned; it may be y itself, and must
+ * otherwise not overlap y or the workspace.  The workspace is
+ * qgemv_ffn_workspace_bytes, as for qgemv_q4_0_ffn. */
+qgemv_status qgemv_q4_0_ffn_residual(const void *W_gate, const void *W_up, const void *W_down,
+                                     qgemv_wlayout layout, const float *x, const float *residual, float *y,
+                                     int64_t d_model, int64_t d_ff, int T, void *ws, size_t ws_bytes,
+                                     qgemv_stream_t stream);
+
 /* Test hook: step 2 of qgemv_q4_0_ffn alone.  g, u fp32 [T][F]; hq receives
  * T rows of F int8 codes then the [T][F/32] fp16 scales (16-byte aligned,
  * qgemv_xq_bytes(T, F) bytes). */

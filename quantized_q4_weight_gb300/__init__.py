@@ -82,6 +82,7 @@ _SIGS = {
     "qgemv_q4_0_verify_f32": ([_VP, _I32, _VP, _VP, _VP, _VP, _VP, _I64, _I64, _I32, _VP, _SZ, _VP], _I32),
     "qgemv_ffn_workspace_bytes": ([_I64, _I64, _I32], _SZ),
     "qgemv_q4_0_ffn": ([_VP, _VP, _VP, _I32, _VP, _VP, _I64, _I64, _I32, _VP, _SZ, _VP], _I32),
+    "qgemv_q4_0_ffn_residual": ([_VP, _VP, _VP, _I32, _VP, _VP, _VP, _I64, _I64, _I32, _VP, _SZ, _VP], _I32),
     "qgemv_debug_silu_mul_q8": ([_VP, _VP, _VP, _I32, _I64, _VP], _I32),
     "qgemv_pack_q8_0": ([_VP, _VP, _I64, _I64, _VP], _I32),
     "qgemv_unpack_q8_0": ([_VP, _VP, _I64, _I64, _VP], _I32),
@@ -266,6 +267,16 @@ def ffn(W_gate, W_up, W_down, layout: int, x, d_model: int, d_ff: int, T: int, w
     y = y if y is not None else torch.empty((T, d_model), dtype=torch.float32, device=x.device)
     _check(lib().qgemv_q4_0_ffn(_ptr(W_gate), _ptr(W_up), _ptr(W_down), layout, _ptr(x), _ptr(y), d_model, d_ff, T,
                                 _ptr(ws), ws.numel(), _stream(stream)), "qgemv_q4_0_ffn")
+    return y
+
+
+def ffn_residual(W_gate, W_up, W_down, layout: int, x, residual, d_model: int, d_ff: int, T: int, ws, y=None,
+                 stream=None):
+    """y = residual + W_down . Q8_0(SiLU(W_gate . x) * (W_up . x)); residual may be y."""
+    y = y if y is not None else torch.empty((T, d_model), dtype=torch.float32, device=x.device)
+    _check(lib().qgemv_q4_0_ffn_residual(_ptr(W_gate), _ptr(W_up), _ptr(W_down), layout, _ptr(x), _ptr(residual),
+                                         _ptr(y), d_model, d_ff, T, _ptr(ws), ws.numel(), _stream(stream)),
+           "qgemv_q4_0_ffn_residual")
     return y
 
 

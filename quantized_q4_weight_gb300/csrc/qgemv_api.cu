@@ -715,7 +715,11 @@ static long long ffn_parts(int64_t d_model, int64_t d_ff, int T, long long off[5
     off[2] = off[1] + align_up(4ll * T * d_ff, 256);
     off[3] = off[2] + align_up(4ll * T * d_ff, 256);
     off[4] = off[3] + align_up(xq_bytes_host(T, d_ff), 256);
-    return off[4] + align_up(static_cast<long long>(qgemv_workspace_bytes(d_model, d_ff, T)), 256);
+    // down: a single call, or a one-item sequence with the residual epilogue
+    const qgemv_seq_item dn[1] = {{nullptr, nullptr, nullptr, d_model, d_ff}};
+    const long long d1 = static_cast<long long>(qgemv_workspace_bytes(d_model, d_ff, T));
+    const long long d2 = static_cast<long long>(qgemv_seq_workspace_bytes(dn, 1, T));
+    return off[4] + align_up(d1 > d2 ? d1 : d2, 256);
 }
 
 size_t qgemv_ffn_workspace_bytes(int64_t d_model, int64_t d_ff, int T)
@@ -735,9 +739,31 @@ qgemv_status qgemv_debug_silu_mul_q8(const float *g, const float *u, void *hq, i
                : QGEMV_ERR_CUDA;
 }
 
+static qgemv_status ffn_chain(const void *W_gate, const void *W_up, const void *W_down, qgemv_wlayout layout,
+                              const float *x, const float *residual, float *y, int64_t d_model, int64_t d_ff, int T,
+                              void *ws, size_t ws_bytes, qgemv_stream_t stream);
+static qgemv_status launch_seq(const qgemv_seq_item *items, int n, qgemv_wlayout layout, int T, void *ws,
+                               size_t ws_bytes, cudaStream_t st, bool xf32, const float *const *bias,
+                               const float *const *res);
+
 qgemv_status qgemv_q4_0_ffn(const void *W_gate, const void *W_up, const void *W_down, qgemv_wlayout layout,
                             const float *x, float *y, int64_t d_model, int64_t d_ff, int T, void *ws,
                             size_t ws_bytes, qgemv_stream_t stream)
+{
+    return ffn_chain(W_gate, W_up, W_down, layout, x, nullptr, y, d_model, d_ff, T, ws, ws_bytes, stream);
+}
+
+qgemv_status qgemv_q4_0_ffn_residual(const void *W_gate, const void *W_up, const void *W_down, qgemv_wlayout layout,
+                                     const float *x, const float *residual, float *y, int64_t d_model, int64_t d_ff,
+                                     int T, void *ws, size_t ws_bytes, qgemv_stream_t stream)
+{
+    if (!residual) return QGEMV_ERR_INVALID_ARG;
+    return ffn_chain(W_gate, W_up, W_down, layout, x, residual, y, d_model, d_ff, T, ws, ws_bytes, stream);
+}
+
+static qgemv_status ffn_chain(const void *W_gate, const void *W_up, const void *W_down, qgemv_wlayout layout,
+                              const float *x, const float *residual, float *y, int64_t d_model, int64_t d_ff, int T,
+                              void *ws, size_t ws_bytes, qgemv_stream_t stream)
 {
     long long off[5];
     const long long need = ffn_parts(d_model, d_ff, T, off);
@@ -751,6 +777,11 @@ qgemv_status qgemv_q4_0_ffn(const void *W_gate, const void *W_up, const void *W_
     if (overlap(ry, rw) || overlap(ry, range(x, 4ll * T * d_model)) || overlap(range(x, 4ll * T * d_model), rw) ||
         overlap(ry, range(W_down, 18ll * d_model * (d_ff / QK))))
         return QGEMV_ERR_INVALID_ARG;
+    if (residual) {  // may be y itself; otherwise it overlaps nothing the chain writes
+        if (!aligned(residual, 4)) return QGEMV_ERR_MISALIGNED;
+        const Range rr = range(residual, 4ll * T * d_model);
+        if (residual != y && (overlap(rr, ry) || overlap(rr, rw))) return QGEMV_ERR_INVALID_ARG;
+    }
     uint8_t *w = static_cast<uint8_t *>(ws);
     float *g = reinterpret_cast<float *>(w + off[1]);
     float *u = reinterpret_cast<float *>(w + off[2]);
@@ -761,7 +792,15 @@ qgemv_status qgemv_q4_0_ffn(const void *W_gate, const void *W_up, const void *W_
     if (s != QGEMV_OK) return s;
     if (launch_silu_mul_q8(g, u, hq, T, d_ff, true, reinterpret_cast<cudaStream_t>(stream)) != cudaSuccess)
         return QGEMV_ERR_CUDA;
-    return qgemv_q4_0(W_down, layout, hq, y, d_model, d_ff, T, w + off[4], static_cast<size_t>(need - off[4]), stream);
+    if (!residual)
+        return qgemv_q4_0(W_down, layout, hq, y, d_model, d_ff, T, w + off[4], static_cast<size_t>(need - off[4]),
+                          stream);
+    // down with the residual epilogue: a one-item sequence launch
+    const qgemv_seq_item dn[1] = {{W_down, hq, y, d_model, d_ff}};
+    const float *const bias[1] = {nullptr};
+    const float *const res[1] = {residual};
+    return launch_seq(dn, 1, layout, T, w + off[4], static_cast<size_t>(need - off[4]),
+                      reinterpret_cast<cudaStream_t>(stream), false, bias, res);
 }
 
 qgemv_status qgemv_q4_0_verify_f32(const void *W, qgemv_wlayout layout, const float *x, const int64_t *tokens,

@@ -85,6 +85,37 @@ def test_ffn_chain(orc, d_model, d_ff, T):
     assert q.device_status() == 0
 
 
+@pytest.mark.parametrize("d_model,d_ff,T", [(1536, 8960, 1), (2048, 11008, 8), (256, 512, 5)])
+def test_ffn_residual(orc, d_model, d_ff, T):
+    """The chain with a residual on down: y equals the plain chain's y plus
+    the residual (one fp32 add), separate and in place; within the bound of
+    the oracle's fp64 down projection plus the residual."""
+    seed = 900 + d_model + T
+    Wg_ggml = synth.q4_0_weights(seed, d_ff, d_model)
+    Wd_ggml = synth.q4_0_weights(seed + 2, d_model, d_ff)
+    Wg = q.pack_q4_0(to_dev(Wg_ggml), d_ff, d_model)
+    Wu = q.pack_q4_0(to_dev(synth.q4_0_weights(seed + 1, d_ff, d_model)), d_ff, d_model)
+    Wd = q.pack_q4_0(to_dev(Wd_ggml), d_model, d_ff)
+    xd = torch.from_numpy(synth.activations(seed + 3, T, d_model)).to(DEV)
+    r = torch.from_numpy(synth.activations(seed + 4, T, d_model)).to(DEV)
+    ws = q.new_workspace(q.ffn_workspace_bytes(d_model, d_ff, T))
+    y0 = q.ffn(Wg, Wu, Wd, q.W_PACKED, xd, d_model, d_ff, T, ws)
+    y1 = q.ffn_residual(Wg, Wu, Wd, q.W_PACKED, xd, r, d_model, d_ff, T, ws)
+    want = (y0 + r).cpu()
+    assert torch.equal(y1.cpu().view(torch.int32), want.view(torch.int32))
+    h = r.clone()                                                  # in place: h += FFN(x)
+    q.ffn_residual(Wg, Wu, Wd, q.W_PACKED, xd, h, d_model, d_ff, T, ws, y=h)
+    assert torch.equal(h.cpu().view(torch.int32), want.view(torch.int32))
+    # against the oracle: the codes of the GPU's own gate and up, then fp64 down + residual
+    g = q.gemv_f32(Wg, q.W_PACKED, xd, d_ff, d_model, T, q.new_workspace(q.workspace_bytes(d_ff, d_model, T)))
+    u = q.gemv_f32(Wu, q.W_PACKED, xd, d_ff, d_model, T, q.new_workspace(q.workspace_bytes(d_ff, d_model, T)))
+    ref_hq, _ = orc.silu_mul_quantize(g.cpu().numpy(), u.cpu().numpy())
+    y64, S = orc.gemv_ep(Wd_ggml, d_model, d_ff, ref_hq, T, None, r.cpu().numpy())
+    err = np.abs(y1.cpu().numpy().astype(np.float64) - y64)
+    assert np.all(err <= oracle.tolerance(S))
+    assert q.device_status() == 0
+
+
 def test_ffn_errors():
     d_model, d_ff, T = 256, 512, 2
     W = torch.zeros(q.q4_0_bytes(d_ff, d_model), dtype=torch.uint8, device=DEV)
@@ -96,4 +127,14 @@ def test_ffn_errors():
     ws = q.new_workspace(need)
     with pytest.raises(q.QgemvError, match="INVALID_ARG"):   # y inside the workspace
         q.ffn(W, W, W, q.W_PACKED, x, d_model, d_ff, T, ws, y=ws[:4 * T * d_model].view(torch.float32).view(T, d_model))
+    assert q.device_status() == 0
+    r = torch.zeros((T, d_model), dtype=torch.float32, device=DEV)
+    y = torch.zeros((T, d_model), dtype=torch.float32, device=DEV)
+    with pytest.raises(q.QgemvError, match="INVALID_ARG"):   # residual over the workspace
+        q.ffn_residual(W, W, W, q.W_PACKED, x, ws[:4 * T * d_model].view(torch.float32).view(T, d_model), d_model,
+                       d_ff, T, ws, y=y)
+    with pytest.raises(q.QgemvError, match="INVALID_ARG"):   # residual shifted over y
+        yy = torch.zeros(T * d_model + 1, dtype=torch.float32, device=DEV)
+        q.ffn_residual(W, W, W, q.W_PACKED, x, yy[1:].view(T, d_model), d_model, d_ff, T, ws,
+                       y=yy[:T * d_model].view(T, d_model))
     assert q.device_status() == 0
