@@ -25,7 +25,7 @@ constexpr int NWARPS_MAX = 16;        // consumer warps per CTA (one CTA per SM)
 constexpr int NTHREADS_MAX = NWARPS_MAX * 32;
 constexpr int MAX_RING = 6;           // pipeline stages per warp, upper bound
 constexpr int MAX_GRID = 1024;        // argmax candidate slots
-constexpr int SPLIT_SLAB_THRESHOLD = 1024;  // split K only when a launch has fewer slabs (measured)
+constexpr int SPLIT_SLAB_THRESHOLD = 608;  // split K below four slabs per CTA of a 152-SM grid (measured)
 constexpr int MAGIC_I = 0x4B400000;   // bits of 12582912.0f = 1.5 * 2^23
 constexpr float MAGIC_F = 12582912.0f;
 

@@ -336,7 +336,7 @@ def test_workspace_left_zeroed_and_reusable(orc):
 @pytest.mark.parametrize("layout", [q.W_PACKED, q.W_GGML])
 @pytest.mark.parametrize("T", [1, 3, 8])
 def test_seq_balanced_mode_bit_identical(orc, layout, T):
-    """Lists with 1024 slabs or more run unsplit, with CTAs balanced by
+    """Lists with 608 slabs or more run unsplit, with CTAs balanced by
     16-block stages (slabs cut between warps); the bits must equal the single
     calls (which split K) and stay within the bound of the oracle."""
     shapes = [(2048, 1536), (1000, 2080), (1536, 8960), (17, 544), (301, 1024), (64, 11008), (8960, 1536)] * 3
