@@ -63,9 +63,12 @@ def test_noalloc_matches_workspace_entry_point(orc, N, K, T):
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch(orc):
-    # 2000 slabs of 16 rows with K = 16384 at T = 8 would need ~33 MB of partial sums
-    N, K, T = 32000, 16384, 8
-    W = torch.empty(16, dtype=torch.uint8, device=DEV)
-    y = torch.empty(16, dtype=torch.float32, device=DEV)
+    # 600 slabs of 16 rows (split K) with K = 16384 at T = 8 need 9.8 MB of
+    # partial sums, beyond the 4 MiB scratch.  Every buffer has its full size,
+    # so that the call could run safely if it were accepted.
+    N, K, T = 9600, 16384, 8
+    W = torch.zeros(q.q4_0_bytes(N, K), dtype=torch.uint8, device=DEV)
+    xq = torch.zeros(q.xq_bytes(T, K), dtype=torch.uint8, device=DEV)
+    y = torch.empty((T, N), dtype=torch.float32, device=DEV)
     idx = torch.empty(T, dtype=torch.int64, device=DEV)
-    assert noalloc(W, W, y, idx, N, K, T) == 3                     # QGEMV_ERR_UNSUPPORTED
+    assert noalloc(W, xq, y, idx, N, K, T) == 3                    # QGEMV_ERR_UNSUPPORTED
