@@ -489,10 +489,22 @@ def peaks():
         return 6800.0, "fallback"
 
 
-def kernel_source_hash() -> str:
+# The sources each measured kernel is built from, with the host planning
+# code that sizes its launches: a traffic record stays valid while they do.
+_COMMON_SOURCES = ["qgemv_internal.cuh", "qgemv_launch.h", "qgemv_api.cu"]
+KERNEL_SOURCES = {
+    "qgemv_stream_kernel": ["gemv_kernel.cuh", "launch_stream.cuh"] + [f"gemv_t{t}.cu" for t in range(1, 9)],
+    "q8_gemv_kernel": ["q8_kernel.cu"],
+    "requant_q4_0_staged": ["kernels_misc.cu"],
+}
+
+
+def kernel_source_hash(kernel: str | None = None) -> str:
+    """Hash of one kernel's sources (all of csrc when the kernel is unknown)."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "quantized_q4_weight_gb300", "csrc")
-    for fn in sorted(os.listdir(csrc)):
+    files = sorted(KERNEL_SOURCES[kernel] + _COMMON_SOURCES) if kernel in KERNEL_SOURCES else sorted(os.listdir(csrc))
+    for fn in files:
         with open(os.path.join(csrc, fn), "rb") as f:
             h.update(fn.encode() + f.read())
     return h.hexdigest()[:16]
@@ -506,7 +518,7 @@ def traffic_record(workload: str, T: int):
         with open(p) as f:
             rec = json.load(f)
         r = rec.get(f"{workload}/T{T}")
-        if r and r.get("kernel_hash") == kernel_source_hash():
+        if r and r.get("kernel_hash") == kernel_source_hash(r.get("kernel")):
             return r.get("dram_bytes_per_launch")
     except Exception:
         pass
