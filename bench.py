@@ -333,7 +333,7 @@ def build_requant(T, seed, dev, copies=2, keep_host=False, N=151936, K=1536):
         wl.copy = (wl.copy + 1) % copies
 
     wl.step, wl.kernel = step, step
-    wl.kernel_name = "requant_q4_0_staged"
+    wl.kernel_name = "requant_q4_0_staged_q8"
     wl.dtype = "fp32 encoder arithmetic (Q8_0 in, Q4_0 out)"
     wl.data = "synthetic (seeded; Q8_0 codes uniform on [-127, 127], fp16 scales U[1e-3,4e-3])"
     wl.inputs, wl.outputs = [wl.W[0]], [wl.out]
@@ -495,7 +495,7 @@ _COMMON_SOURCES = ["qgemv_internal.cuh", "qgemv_launch.h", "qgemv_api.cu"]
 KERNEL_SOURCES = {
     "qgemv_stream_kernel": ["gemv_kernel.cuh", "launch_stream.cuh"] + [f"gemv_t{t}.cu" for t in range(1, 9)],
     "q8_gemv_kernel": ["q8_kernel.cu"],
-    "requant_q4_0_staged": ["kernels_misc.cu"],
+    "requant_q4_0_staged_q8": ["kernels_misc.cu"],
 }
 
 

@@ -385,6 +385,63 @@ __global__ void __launch_bounds__(256) requant_q4_0_kernel(const void *__restric
 // read as two-byte words: at most two threads per bank).
 constexpr int RQ_CHUNK = 256;
 
+// Q8_0 chunks: two staging buffers filled by cp.async, the next chunk's
+// copies issued before the current chunk is encoded (a grid of a few CTAs
+// per SM walks the chunks), so that the copies overlap the encoder.
+__device__ __forceinline__ void rq_issue_q8_chunk(uint8_t *s, const uint8_t *g, int tid)
+{
+    for (int i = tid; i < 34 * RQ_CHUNK / 16; i += RQ_CHUNK)
+        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_addr(s + 16 * i)), "l"(g + 16 * i)
+                     : "memory");
+    asm volatile("cp.async.commit_group;" ::: "memory");
+}
+
+__device__ __forceinline__ void rq_encode_q8_chunk(const uint8_t *s_in, uint8_t *s_out, int tid)
+{
+    float x[QK];
+    const unsigned short *h = reinterpret_cast<const unsigned short *>(s_in + tid * 34);
+    const float d8 = __half2float(__ushort_as_half(h[0]));
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+        const unsigned w = h[1 + i];
+        x[2 * i] = __fmul_rn(q8_code_to_float(w & 0xFFu), d8);
+        x[2 * i + 1] = __fmul_rn(q8_code_to_float(w >> 8), d8);
+    }
+    unsigned short o[9];
+    q4_encode_block(x, o);
+    unsigned short *so = reinterpret_cast<unsigned short *>(s_out + tid * 18);
+#pragma unroll
+    for (int i = 0; i < 9; ++i) so[i] = o[i];
+}
+
+__global__ void __launch_bounds__(RQ_CHUNK) requant_q4_0_staged_q8(const uint8_t *__restrict__ src,
+                                                                   uint8_t *__restrict__ dst, long long nchunks)
+{
+    __shared__ __align__(16) uint8_t s_in[2][34 * RQ_CHUNK];
+    __shared__ __align__(16) uint8_t s_out[18 * RQ_CHUNK];
+    const int tid = threadIdx.x;
+    long long ch = blockIdx.x;
+    int buf = 0;
+    if (ch < nchunks) rq_issue_q8_chunk(s_in[0], src + ch * (34ll * RQ_CHUNK), tid);
+    for (; ch < nchunks; ch += gridDim.x) {
+        const long long nx = ch + gridDim.x;
+        if (nx < nchunks) {
+            // s_in[buf ^ 1] was last read before the previous chunk's second barrier
+            rq_issue_q8_chunk(s_in[buf ^ 1], src + nx * (34ll * RQ_CHUNK), tid);
+            asm volatile("cp.async.wait_group 1;" ::: "memory");  // this chunk's group is complete
+        } else {
+            asm volatile("cp.async.wait_group 0;" ::: "memory");
+        }
+        __syncthreads();
+        rq_encode_q8_chunk(s_in[buf], s_out, tid);
+        __syncthreads();
+        int4 *go = reinterpret_cast<int4 *>(dst + ch * (18ll * RQ_CHUNK));
+        for (int i = tid; i < 18 * RQ_CHUNK / 16; i += RQ_CHUNK) go[i] = reinterpret_cast<const int4 *>(s_out)[i];
+        buf ^= 1;
+        // s_out is written again only after the next chunk's first barrier
+    }
+}
+
 template <bool FROM_Q8>
 __global__ void __launch_bounds__(RQ_CHUNK) requant_q4_0_staged(const uint8_t *__restrict__ src,
                                                                 uint8_t *__restrict__ dst, long long nchunks)
@@ -447,10 +504,12 @@ cudaError_t launch_requant_q4_0(const void *src, bool from_q8, void *dst, long l
     long long done = 0;
     if (aligned16 && nblocks >= RQ_CHUNK) {
         const long long nchunks = nblocks / RQ_CHUNK;
-        // resident CTAs: 8 per SM (Q8_0, 13 KB of shared memory each) or 5 (fp32, 37 KB)
+        // fp32: 5 resident CTAs per SM (37 KB of shared memory each), many waves; Q8_0:
+        // four CTAs per SM of the 152-SM grid walk the chunks with the next one in flight
         long long grid = nchunks < 152ll * 8 * 16 ? nchunks : 152ll * 8 * 16;
         if (from_q8)
-            requant_q4_0_staged<true><<<static_cast<unsigned>(grid), RQ_CHUNK, 0, st>>>(s8, o, nchunks);
+            requant_q4_0_staged_q8<<<static_cast<unsigned>(nchunks < 152ll * 4 ? nchunks : 152ll * 4), RQ_CHUNK, 0,
+                                     st>>>(s8, o, nchunks);
         else
             requant_q4_0_staged<false><<<static_cast<unsigned>(grid), RQ_CHUNK, 0, st>>>(s8, o, nchunks);
         done = nchunks * RQ_CHUNK;
