@@ -35,6 +35,10 @@
  *  - amax = 0 gives d = 0, 1/d := 0, all q = 0.
  *  - argmax: lowest index among equal maxima, equality by IEEE == (so -0 == +0).
  *  - top-2: the second is the argmax of the rows other than the first.
+ *  - Q4_0 encoder (requantisation at load): GGML's q4_0 encoder (see the
+ *    section below).
+ *  - sequence epilogue: y = W.x + bias + residual, the two terms added
+ *    after the GEMV value.
  *
  * ORC_MUTANT (compile-time, default 0) plants one known mistake; the test
  * suite builds each mutant and checks that its pins reject it.
