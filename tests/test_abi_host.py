@@ -129,6 +129,22 @@ def test_other_calls_reject_bad_arguments(L):
     assert L.qgemv_requant_q8_0_q4_0(FAKE + 1, out, 16, 64, s) == 2
     assert L.qgemv_requant_q8_0_q4_0(FAKE, FAKE + 34 * 16 * 2 - 18, 16, 64, s) == 1
     assert L.qgemv_requant_q8_0_q4_0(FAKE, out, 0, 64, s) == 1
+    # sequences with the epilogue: x_f32 flag, misaligned bias, residual over another output
+    ep = (q.SeqEpItem * 2)(q.SeqEpItem(FAKE, FAKE + (1 << 28), FAKE + (1 << 29), 64, 64, None, None),
+                           q.SeqEpItem(FAKE, FAKE + (1 << 28), FAKE + (1 << 29) + 4096, 64, 64, None, None))
+    ws = FAKE + (1 << 30)
+    assert L.qgemv_q4_0_seq_ep(ep, 2, 1, 1, 2, ws, 1 << 20, s) == 1
+    ep[0].bias = FAKE + (1 << 27) + 2
+    assert L.qgemv_q4_0_seq_ep(ep, 2, 1, 1, 0, ws, 1 << 20, s) == 2
+    ep[0].bias = None
+    ep[0].residual = FAKE + (1 << 29) + 4096                          # item 1's output
+    assert L.qgemv_q4_0_seq_ep(ep, 2, 1, 1, 0, ws, 1 << 20, s) == 1
+    # the FFN chain with a residual: misaligned, or over the workspace
+    need = L.qgemv_ffn_workspace_bytes(256, 512, 2)
+    x, y = FAKE + (1 << 28), FAKE + (1 << 29)
+    assert L.qgemv_q4_0_ffn_residual(FAKE, FAKE, FAKE, 1, x, None, y, 256, 512, 2, ws, need, s) == 1
+    assert L.qgemv_q4_0_ffn_residual(FAKE, FAKE, FAKE, 1, x, y + 4098, y, 256, 512, 2, ws, need, s) == 2
+    assert L.qgemv_q4_0_ffn_residual(FAKE, FAKE, FAKE, 1, x, ws + 256, y, 256, 512, 2, ws, need, s) == 1
 
 
 def test_fp32_calls_reject_bad_arguments(L):
