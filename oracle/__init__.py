@@ -92,6 +92,9 @@ class Oracle:
         L.orc_top2_f64.restype = None
         L.orc_verify_commit.argtypes = [_i64p, _i64p, ctypes.c_int]
         L.orc_quantize_block_q4_0.argtypes = [_f32p, _u8p]
+        L.orc_quantize_vec_i8.argtypes = [_f32p, ctypes.c_int, ctypes.c_int64, _i8p, _f32p]
+        L.orc_gemv_gs64_f64.argtypes = [_u8p, _f32p, ctypes.c_int64, ctypes.c_int64, _i8p, _f32p, ctypes.c_int,
+                                        _f64p, _f64p]
         L.orc_gemv_ep_f64.argtypes = [_u8p, ctypes.c_int64, ctypes.c_int64, _u8p, ctypes.c_int, _f32p, _f32p,
                                       _f64p, _f64p]
         L.orc_requant_f32_q4_0.argtypes = [_f32p, ctypes.c_int64, ctypes.c_int64, _u8p]
@@ -249,6 +252,29 @@ class Oracle:
         S = np.empty((T, N), np.float64)
         self.L.orc_gemv_ep_f64(_p(W, _u8p), N, K, _p(xq, _u8p), T, None if b is None else _p(b, _f32p),
                                None if r is None else _p(r, _f32p), _p(y, _f64p), _p(S, _f64p))
+        return y, S
+
+    def quantize_vec_i8(self, x: np.ndarray):
+        """fp32 x [T, K] -> (q int8 [T, K], s fp32 [T]): one scale per vector."""
+        x = np.ascontiguousarray(x, np.float32)
+        T, K = x.shape
+        q = np.empty((T, K), np.int8)
+        s = np.empty(T, np.float32)
+        self.L.orc_quantize_vec_i8(_p(x, _f32p), T, K, _p(q, _i8p), _p(s, _f32p))
+        return q, s
+
+    def gemv_gs64(self, Wq: np.ndarray, Ws: np.ndarray, N: int, K: int, q: np.ndarray, s: np.ndarray):
+        """gs64 planar int4 weights (nibbles [N][K/64][32], fp32 scales [N][K/64])
+        against per-vector int8 activations -> (y64, S) [T, N]."""
+        Wq = np.ascontiguousarray(Wq, np.uint8)
+        Ws = np.ascontiguousarray(Ws, np.float32)
+        q = np.ascontiguousarray(q, np.int8)
+        s = np.ascontiguousarray(s, np.float32)
+        T = q.shape[0]
+        y = np.empty((T, N), np.float64)
+        S = np.empty((T, N), np.float64)
+        self.L.orc_gemv_gs64_f64(_p(Wq, _u8p), _p(Ws, _f32p), N, K, _p(q, _i8p), _p(s, _f32p), T,
+                                 _p(y, _f64p), _p(S, _f64p))
         return y, S
 
     def quantize_block_q4_0(self, x: np.ndarray) -> np.ndarray:

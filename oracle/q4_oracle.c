@@ -512,6 +512,82 @@ int orc_verify_commit(const int64_t *tokens, const int64_t *pred, int T)
     return n;
 }
 
+/* ------------------------------------ gs64 planar int4, per-vector int8 */
+
+/* A variant format (colibri qwen36 docs: the gs64 container and its planar
+ * repack; the dense int8 IDOT activation contract).  Readings where the
+ * pages are silent:
+ *  - a gs64 group is 64 weights in 32 bytes: byte j (j < 32) holds element
+ *    j in its low nibble and element j + 32 in its high nibble (so one AND
+ *    and one shift give the two halves in order), and the weight is
+ *    (n - 8) * s with one fp32 scale s per group, as Q4_0's offset;
+ *  - the activation is quantised once per vector: s_x = amax / 127 over the
+ *    whole row of K values (fp32, not rounded to fp16), 1/s_x from it (0 when
+ *    amax = 0), q = round-half-away(x * (1/s_x)) as int8;
+ *  - y = sum_g s_w[g] * s_x * isum_g, isum_g the exact int32 sum over the
+ *    group, formed here in fp64 (every product exact). */
+
+/* x fp32 [T][K] -> q int8 [T][K], s [T]. */
+void orc_quantize_vec_i8(const float *x, int T, int64_t K, int8_t *q, float *s)
+{
+    for (int t = 0; t < T; t++) {
+        const float *xr = x + (int64_t)t * K;
+        float amax = 0.0f;
+#if ORC_MUTANT == 20
+        for (int64_t k = 0; k < (K < 32 ? K : 32); k++) {   /* MUTANT: the first block's maximum only */
+#else
+        for (int64_t k = 0; k < K; k++) {
+#endif
+            float a = fabsf(xr[k]);
+            if (a > amax) amax = a;
+        }
+        float d = amax / 127.0f;
+        float id = (d != 0.0f) ? 1.0f / d : 0.0f;
+        s[t] = d;
+        for (int64_t k = 0; k < K; k++) {
+            float r = roundf(xr[k] * id);
+            if (r > 127.0f) r = 127.0f;             /* unreachable for finite x */
+            if (r < -127.0f) r = -127.0f;
+            q[(int64_t)t * K + k] = (int8_t)r;
+        }
+    }
+}
+
+/* Nibble of element e (0..63) of a 32-byte gs64 group. */
+static int gs64_nibble(const uint8_t *grp, int e)
+{
+#if ORC_MUTANT == 19
+    return e % 2 == 0 ? (grp[e / 2] & 0x0F) : (grp[e / 2] >> 4);   /* MUTANT: GGML-style pairs */
+#else
+    return e < 32 ? (grp[e] & 0x0F) : (grp[e - 32] >> 4);
+#endif
+}
+
+/* W nibbles [N][K/64][32], scales [N][K/64] fp32; q int8 [T][K], s [T]:
+ * y64 = sum_g ws * s * isum_g, S = sum_g |same term|, both [T][N]. */
+void orc_gemv_gs64_f64(const uint8_t *Wq, const float *Ws, int64_t N, int64_t K, const int8_t *q,
+                       const float *s, int T, double *y64, double *S)
+{
+    int64_t ng = K / 64;
+    for (int t = 0; t < T; t++) {
+#pragma omp parallel for schedule(static)
+        for (int64_t i = 0; i < N; i++) {
+            double acc = 0.0, sc = 0.0;
+            for (int64_t g = 0; g < ng; g++) {
+                const uint8_t *grp = Wq + (i * ng + g) * 32;
+                const int8_t *qg = q + (int64_t)t * K + g * 64;
+                int32_t isum = 0;
+                for (int e = 0; e < 64; e++) isum += (gs64_nibble(grp, e) - 8) * (int32_t)qg[e];
+                double term = (double)Ws[i * ng + g] * (double)s[t] * (double)isum;
+                acc += term;
+                sc += fabs(term);
+            }
+            y64[(int64_t)t * N + i] = acc;
+            S[(int64_t)t * N + i] = sc;
+        }
+    }
+}
+
 /* ------------------------------------------ Q4_0 requantisation at load */
 
 /* Weights requantised to Q4_0 blocks at load (minfer README M14: the

@@ -621,4 +621,61 @@ def pin_epilogue_closed_forms(o):
     assert np.array_equal(y0, y1) and np.array_equal(S0, S1)
 
 
+# ------------------------------------ gs64 planar int4, per-vector int8
+# (colibri qwen36 docs: 64-weight groups with one scale, repacked so that one
+# AND and one shift give a group's two halves in order; activations
+# quantised once per vector with amax / 127.)
+
+def _gs64_decode_f64(Wq, Ws, N, K):
+    """fp64 weights [N][K] from the layout's definition: byte j of a group
+    holds element j (low nibble) and element j + 32 (high nibble)."""
+    g = Wq.reshape(N, K // 64, 32)
+    n = np.concatenate([g & 0x0F, g >> 4], axis=2).astype(np.float64)     # [N][G][64]
+    return ((n - 8.0) * Ws.reshape(N, K // 64, 1).astype(np.float64)).reshape(N, K)
+
+
+def pin_gs64_hand_group(o):
+    # one group: every code 8 (weight 0) except element 33 = 15 (weight 7 s);
+    # element 33 is the high nibble of byte 1.  q = 1 everywhere but q[33] = 5:
+    # isum = 7 * 5 = 35, y = s_w * s_x * 35 exactly.
+    Wq = np.full((1, 32), 0x88, np.uint8)
+    Wq[0, 1] = 0xF8
+    Ws = np.array([[0.375]], np.float32)
+    q = np.ones((1, 64), np.int8)
+    q[0, 33] = 5
+    y, S = o.gemv_gs64(Wq, Ws, 1, 64, q, np.array([2.0], np.float32))
+    assert y[0, 0] == 0.375 * 2.0 * 35 and S[0, 0] == abs(y[0, 0])
+
+
+def pin_gs64_bruteforce(o):
+    rng = np.random.default_rng(1600)
+    for N, K, T in [(3, 64, 1), (5, 256, 3), (2, 640, 2)]:
+        Wq = rng.integers(0, 256, (N, K // 64 * 32)).astype(np.uint8)
+        Ws = rng.uniform(-0.02, 0.02, (N, K // 64)).astype(np.float32)
+        q = rng.integers(-127, 128, (T, K)).astype(np.int8)
+        s = rng.uniform(1e-3, 1e-1, T).astype(np.float32)
+        y, _ = o.gemv_gs64(Wq, Ws, N, K, q, s)
+        ref = (q.astype(np.float64) * s.astype(np.float64)[:, None]) @ _gs64_decode_f64(Wq, Ws, N, K).T
+        assert np.allclose(y, ref, rtol=1e-12, atol=1e-15), (N, K, T)
+
+
+def pin_vec_i8_quantiser(o):
+    rng = np.random.default_rng(1601)
+    x = (rng.standard_normal((4, 1000)) * np.array([[1e-3], [1.0], [50.0], [3.0]])).astype(np.float32)
+    x[3, 500] = -40.0                                   # the extreme late in the vector
+    q, s = o.quantize_vec_i8(x)
+    for t in range(4):
+        a = int(np.argmax(np.abs(x[t])))
+        assert abs(int(q[t, a])) == 127 and np.sign(q[t, a]) == np.sign(x[t, a])
+        assert s[t] == np.float32(np.max(np.abs(x[t])) / np.float32(127.0))
+        err = np.abs(x[t].astype(np.float64) - q[t].astype(np.float64) * float(s[t]))
+        assert np.all(err <= 0.5 * float(s[t]) * (1 + 1e-5)), t
+    q2, s2 = o.quantize_vec_i8(-x)
+    assert np.array_equal(q2, -q) and np.array_equal(s2, s)
+    q3, s3 = o.quantize_vec_i8((x * np.float32(2.0 ** -5)).astype(np.float32))
+    assert np.array_equal(q3, q) and np.array_equal(s3, (s * np.float32(2.0 ** -5)).astype(np.float32))
+    qz, sz = o.quantize_vec_i8(np.zeros((1, 64), np.float32))
+    assert sz[0] == 0.0 and not qz.any()
+
+
 PINS = [v for k, v in sorted(globals().items()) if k.startswith("pin_")]

@@ -26,8 +26,10 @@ def test_pin(orc, pin):
 #  13 Q8_0 weights read as unsigned, 14 SiLU with exp(+g),
 #  15 Q4_0 encoder scale from the magnitude, 16 Q4_0 codes rounded down,
 #  17 Q8_0 weights read as unsigned when requantised to Q4_0,
-#  18 the epilogue's residual of token 0 used for every token.
-MUTANTS = list(range(1, 19))
+#  18 the epilogue's residual of token 0 used for every token,
+#  19 gs64 nibbles read as GGML-style pairs, 20 the per-vector activation
+#  scale from the first block's maximum only.
+MUTANTS = list(range(1, 21))
 
 
 @pytest.fixture(scope="module")
