@@ -324,11 +324,15 @@ qgemv_status qgemv_verify_commit(const int64_t *tokens, const int64_t *pred, int
  * takes no workspace: its scratch is one 4 MiB array in the library's own
  * device memory, held by every GPU that loads the library until the process
  * exits.  Arguments and results are those of qgemv_q4_0_argmax.
- *   - Shapes whose scratch would exceed 4 MiB (see qgemv_workspace_bytes
- *     minus the activation area) return QGEMV_ERR_UNSUPPORTED.
+ *   - Shapes with qgemv_workspace_bytes(N, K, T) > 4 MiB return
+ *     QGEMV_ERR_UNSUPPORTED.
+ *   - Every argument is checked before any CUDA call: a refused call
+ *     enqueues nothing.
  *   - The first call on a device looks up the array's device address (once
- *     per device, with that device current); make that first call before
- *     any stream capture.
+ *     per device, with that device current) and keeps it for the life of the
+ *     process; make that first call before any stream capture, and do not
+ *     use the call after a cudaDeviceReset of that device (the array then
+ *     moves, and the kept address is stale).
  *   - Every call shares the array and clears its counters at the start (an
  *     asynchronous memset on `stream`); calls that overlap on the GPU, from
  *     any stream or thread, race and give undefined results.
@@ -462,6 +466,18 @@ qgemv_status qgemv_q4_0_gather_f32(const qgemv_gather_f32_matrix *mats, int n_ma
 qgemv_status qgemv_debug_block_isums(const void *W, qgemv_wlayout layout, const void *xq,
                                      int32_t *isums, int64_t N, int64_t K, int T,
                                      qgemv_stream_t stream);
+
+/* Test hook: the same sums as the tensor-core (MMA) path forms them (minfer
+ * README M16: the batched path and the one-token path form identical
+ * per-block integer sums).  Per 16 rows and block, the nibbles enter two
+ * f16 MMAs as subnormal operands and the activations as q and q / 16,
+ * converted as the GEMV kernel converts them: f16_image = 1 from the f16
+ * operand words of small activation images, 0 from the int8 image's
+ * biased bytes; the accumulator starts from the folded offset -8 sum(q) and
+ * ends at isum * 2^-24, which the hook writes as int32.  Arguments and
+ * output layout as qgemv_debug_block_isums. */
+qgemv_status qgemv_debug_block_isums_tc(const void *W, qgemv_wlayout layout, const void *xq, int32_t *isums,
+                                        int64_t N, int64_t K, int T, int f16_image, qgemv_stream_t stream);
 
 /* Measurement hook: stream `bytes` of device memory from `src` once, with
  * no arithmetic, to measure the HBM read bandwidth an access pattern

@@ -29,7 +29,7 @@
  *    q = round-half-away-from-zero(x * (1/d)) as int8 (all zero if amax = 0).
  *    Byte layout: fp16 d then 32 int8 (34 bytes).
  *
- * Readings where the pages are silent (each also listed in the design notes):
+ * Readings where the pages are silent:
  *  - 1/d is taken from the fp32 d, before d is rounded to fp16.
  *  - x * (1/d) is one fp32 multiply, rounded to nearest even.
  *  - amax = 0 gives d = 0, 1/d := 0, all q = 0.

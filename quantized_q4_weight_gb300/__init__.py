@@ -102,6 +102,7 @@ _SIGS = {
     "qgemv_q4_0_gather_f32": ([ctypes.POINTER(GatherF32Matrix), _I32, _VP, _I32, _I32, _I32, _I32, _VP, _SZ, _VP],
                               _I32),
     "qgemv_debug_block_isums": ([_VP, _I32, _VP, _VP, _I64, _I64, _I32, _VP], _I32),
+    "qgemv_debug_block_isums_tc": ([_VP, _I32, _VP, _VP, _I64, _I64, _I32, _I32, _VP], _I32),
     "qgemv_debug_stream_read": ([_VP, _SZ, _I32, _I32, _I32, _I32, _VP, _VP], _I32),
     "qgemv_set_tuning": ([_I32, _I32, _I32, _I32], _I32),
     "qgemv_device_status": ([ctypes.POINTER(ctypes.c_int)], _I32),
@@ -428,6 +429,14 @@ def block_isums(W, layout: int, xq, N: int, K: int, T: int, stream=None) -> torc
     out = torch.empty((T, N, K // QK), dtype=torch.int32, device=W.device)
     _check(lib().qgemv_debug_block_isums(_ptr(W), layout, _ptr(xq), _ptr(out), N, K, T, _stream(stream)),
            "qgemv_debug_block_isums")
+    return out
+
+
+def block_isums_tc(W, layout: int, xq, N: int, K: int, T: int, f16_image: bool, stream=None) -> torch.Tensor:
+    """The tensor-core path's block sums (see qgemv_debug_block_isums_tc)."""
+    out = torch.empty((T, N, K // QK), dtype=torch.int32, device=W.device)
+    _check(lib().qgemv_debug_block_isums_tc(_ptr(W), layout, _ptr(xq), _ptr(out), N, K, T, 1 if f16_image else 0,
+                                            _stream(stream)), "qgemv_debug_block_isums_tc")
     return out
 
 

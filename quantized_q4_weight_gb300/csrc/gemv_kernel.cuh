@@ -482,25 +482,45 @@ __device__ __forceinline__ unsigned lds_u32(uint32_t addr)
 // {C(2j), C(2j+1), C(2j), C(2j+1)} and the fp16 pair {d_x(2j), d_x(2j+1)}.
 // The same from the B registers of the two MMAs: (bl0, bl1) = {q} over the
 // low-nibble k order, (bh0, bh1) = {q / 16} over the high-nibble k order.
+// The block sums alone: d[k] = isum 2^-24 (exact) for row g + 8 (k >> 1),
+// token 2j + (k & 1).  Two MMAs over the low and the high nibbles, the first
+// starting from the folded offset cq.
+__device__ __forceinline__ void mma_block_sums(unsigned wg, unsigned wg8, unsigned bl0, unsigned bl1, unsigned bh0,
+                                               unsigned bh1, const float4 &cq, float (&d)[4])
+{
+    const unsigned g1 = __umulhi(wg, c_shr8_mul), g9 = __umulhi(wg8, c_shr8_mul);  // wg >> 8, wg8 >> 8
+    mma_f16_c(d, wg & 0x000F000Fu, wg8 & 0x000F000Fu, g1 & 0x000F000Fu, g9 & 0x000F000Fu, bl0, bl1, cq);
+    mma_f16(d, wg & 0x00F000F0u, wg8 & 0x00F000F0u, g1 & 0x00F000F0u, g9 & 0x00F000F0u, bh0, bh1);
+}
+
 __device__ __forceinline__ void mma_block_core(unsigned wg, unsigned wg8, unsigned bl0, unsigned bl1, unsigned bh0,
                                                unsigned bh1, unsigned sc, const float4 &cq, unsigned dx, float (&acc)[4])
 {
-    const unsigned g1 = __umulhi(wg, c_shr8_mul), g9 = __umulhi(wg8, c_shr8_mul);  // wg >> 8, wg8 >> 8
     float d[4];
-    mma_f16_c(d, wg & 0x000F000Fu, wg8 & 0x000F000Fu, g1 & 0x000F000Fu, g9 & 0x000F000Fu, bl0, bl1, cq);
-    mma_f16(d, wg & 0x00F000F0u, wg8 & 0x00F000F0u, g1 & 0x00F000F0u, g9 & 0x00F000F0u, bh0, bh1);
+    mma_block_sums(wg, wg8, bl0, bl1, bh0, bh1, cq, d);
     float s00, s01, s10, s11;  // (d_w d_x) for rows g, g + 8 and tokens 2j, 2j + 1
     h2_outer(sc, dx, s00, s01, s10, s11);
     ffma2(acc[0], acc[1], s00, s01, d[0], d[1]);
     ffma2(acc[2], acc[3], s10, s11, d[2], d[3]);
 }
 
+// The B registers of the two MMAs from biased activation words (bytes
+// q xor 0x80): ql holds elements 4j..4j+3, qh elements 16+4j..16+4j+3.
+__device__ __forceinline__ void mma_b_from_biased(unsigned ql, unsigned qh, unsigned &bl0, unsigned &bl1,
+                                                  unsigned &bh0, unsigned &bh1)
+{
+    bl0 = hadd2_u(act_even(ql), H2_NEG_1152);
+    bl1 = hadd2_u(act_odd(ql), H2_NEG_1152);
+    bh0 = hfma2_u(act_even(qh), H2_SIXTEENTH, H2_NEG_72);
+    bh1 = hfma2_u(act_odd(qh), H2_SIXTEENTH, H2_NEG_72);
+}
+
 __device__ __forceinline__ void mma_block_words(unsigned wg, unsigned wg8, unsigned ql, unsigned qh, unsigned sc,
                                                 const float4 &cq, unsigned dx, float (&acc)[4])
 {
-    mma_block_core(wg, wg8, hadd2_u(act_even(ql), H2_NEG_1152), hadd2_u(act_odd(ql), H2_NEG_1152),
-                   hfma2_u(act_even(qh), H2_SIXTEENTH, H2_NEG_72), hfma2_u(act_odd(qh), H2_SIXTEENTH, H2_NEG_72), sc,
-                   cq, dx, acc);
+    unsigned bl0, bl1, bh0, bh1;
+    mma_b_from_biased(ql, qh, bl0, bl1, bh0, bh1);
+    mma_block_core(wg, wg8, bl0, bl1, bh0, bh1, sc, cq, dx, acc);
 }
 
 // Shared-memory addresses of block b's constants for lane j (token pair j).
@@ -945,6 +965,25 @@ __device__ __forceinline__ void quantize_image(uint8_t *img, const float *x, int
     }
 }
 
+// One token's block of the f16 operand image: from its codes (qa: elements
+// 0..15, qb: 16..31) the 16 words {q[e(k)] : k = 0..7}, {q[e(k)] : k =
+// 8..15}, {q[16 + e(k)] / 16 : k = 0..7}, {q[16 + e(k)] / 16 : k = 8..15}
+// (e as below), each value exact in f16.
+__device__ __forceinline__ void f16_block_words(const uint4 &qa, const uint4 &qb, unsigned (&w)[16])
+{
+    const int8_t *qlo = reinterpret_cast<const int8_t *>(&qa);
+    const int8_t *qhi = reinterpret_cast<const int8_t *>(&qb);
+#pragma unroll
+    for (int k = 0; k < 16; k += 2) {
+        const int i0 = 4 * ((k & 7) >> 1) + (k >> 3);  // e(k); e(k + 1) = e(k) + 2
+        const __half2 lo = __floats2half2_rn(static_cast<float>(qlo[i0]), static_cast<float>(qlo[i0 + 2]));
+        const __half2 hi = __floats2half2_rn(static_cast<float>(qhi[i0]) * 0.0625f,
+                                             static_cast<float>(qhi[i0 + 2]) * 0.0625f);
+        w[k >> 1] = *reinterpret_cast<const unsigned *>(&lo);
+        w[8 + (k >> 1)] = *reinterpret_cast<const unsigned *>(&hi);
+    }
+}
+
 // Builds one run's f16 operand image (tensor-core path, small images)
 // straight from the planar Q8_0 activations in global memory (F32: from fp32
 // activations, quantised here by q8_block_thread): per token row
@@ -974,18 +1013,8 @@ __device__ __forceinline__ void build_f16_image(uint8_t *img, const uint8_t *src
                 qb = __ldcg(qp + 1);
                 dh = __ldcg(xd + static_cast<long long>(t) * nb + b);
             }
-            const int8_t *qlo = reinterpret_cast<const int8_t *>(&qa);
-            const int8_t *qhi = reinterpret_cast<const int8_t *>(&qb);
             unsigned w[16];
-#pragma unroll
-            for (int k = 0; k < 16; k += 2) {
-                const int i0 = 4 * ((k & 7) >> 1) + (k >> 3);  // e(k); e(k + 1) = e(k) + 2
-                const __half2 lo = __floats2half2_rn(static_cast<float>(qlo[i0]), static_cast<float>(qlo[i0 + 2]));
-                const __half2 hi = __floats2half2_rn(static_cast<float>(qhi[i0]) * 0.0625f,
-                                                     static_cast<float>(qhi[i0 + 2]) * 0.0625f);
-                w[k >> 1] = *reinterpret_cast<const unsigned *>(&lo);
-                w[8 + (k >> 1)] = *reinterpret_cast<const unsigned *>(&hi);
-            }
+            f16_block_words(qa, qb, w);
             uint4 *dst = reinterpret_cast<uint4 *>(img + t * L.xstride + b * 64);
 #pragma unroll
             for (int c = 0; c < 4; ++c) dst[c] = make_uint4(w[4 * c], w[4 * c + 1], w[4 * c + 2], w[4 * c + 3]);

@@ -70,17 +70,6 @@ cudaError_t launch_quantize(const float *x, void *xq, int R, long long K, int ba
 // the last full slab keep their GGML position, so the byte offset of their
 // blocks is the same in both layouts.
 
-__device__ __forceinline__ void packed_offsets(long long row, int b, int nb, long long &nib_off, long long &sc_off)
-{
-    const long long s = row / SLAB_ROWS;
-    const int r = static_cast<int>(row - s * SLAB_ROWS);
-    const int q = b / QUAD, jq = b - q * QUAD;
-    const int nbq = min(QUAD, nb - q * QUAD);
-    const long long base = s * static_cast<long long>(SLAB_COL_BYTES) * nb + static_cast<long long>(q) * QUAD_BYTES;
-    nib_off = base + (r * nbq + quad_chunk(jq, r, nbq)) * 16;
-    sc_off = base + 256 * nbq + ((r % 8) * nbq + jq) * 4 + (r / 8) * 2;
-}
-
 __global__ void __launch_bounds__(256) pack_kernel(const uint8_t *__restrict__ src, uint8_t *__restrict__ dst,
                                                    long long N, int nb, bool to_packed)
 {

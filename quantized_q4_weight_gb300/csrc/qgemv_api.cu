@@ -541,22 +541,35 @@ qgemv_status qgemv_q4_0_f32(const void *W, qgemv_wlayout layout, const float *x,
                       reinterpret_cast<cudaStream_t>(stream), false, true, true);
 }
 
-// The argmax calls: quantised (xq) or fp32 (x, xf32) activations.
-static qgemv_status argmax_call(const void *W, qgemv_wlayout layout, const void *xin, bool xf32, float *y_or_null,
-                                int64_t *idx, int64_t N, int64_t K, int T, void *ws, size_t ws_bytes,
-                                qgemv_stream_t stream)
+// Argument checks of the argmax calls, host only (no CUDA call).  ws ==
+// nullptr: the library's own scratch, which no caller buffer can overlap.
+static qgemv_status argmax_check(const void *W, qgemv_wlayout layout, const void *xin, bool xf32,
+                                 const float *y_or_null, const int64_t *idx, int64_t N, int64_t K, int T,
+                                 const void *ws, size_t ws_bytes)
 {
     const long long xin_bytes = !shape_ok(N, K) ? 0 : xf32 ? 4ll * T * K : xq_bytes_host(T, K);
     qgemv_status s = check_single(W, layout, xin, xin_bytes, y_or_null, N, K, T, ws);
     if (s != QGEMV_OK) return s;
     if (!idx) return QGEMV_ERR_INVALID_ARG;
     if (!aligned(xin, xf32 ? 4 : 16) || !aligned(idx, 8)) return QGEMV_ERR_MISALIGNED;
-    if (!ws) return QGEMV_ERR_WORKSPACE;
+    if (y_or_null && overlap(range(idx, 8ll * T), range(y_or_null, 4ll * T * N))) return QGEMV_ERR_INVALID_ARG;
+    if (xf32 && overlap(range(xin, xin_bytes), range(idx, 8ll * T))) return QGEMV_ERR_INVALID_ARG;
+    if (!ws) return QGEMV_OK;
     const Range rw = range(ws, static_cast<long long>(ws_bytes));
     if (overlap(range(idx, 8ll * T), rw) || (y_or_null && overlap(range(y_or_null, 4ll * T * N), rw)))
         return QGEMV_ERR_INVALID_ARG;
-    if (xf32 && (overlap(range(xin, xin_bytes), rw) || overlap(range(xin, xin_bytes), range(idx, 8ll * T))))
-        return QGEMV_ERR_INVALID_ARG;
+    if (xf32 && overlap(range(xin, xin_bytes), rw)) return QGEMV_ERR_INVALID_ARG;
+    return QGEMV_OK;
+}
+
+// The argmax calls: quantised (xq) or fp32 (x, xf32) activations.
+static qgemv_status argmax_call(const void *W, qgemv_wlayout layout, const void *xin, bool xf32, float *y_or_null,
+                                int64_t *idx, int64_t N, int64_t K, int T, void *ws, size_t ws_bytes,
+                                qgemv_stream_t stream)
+{
+    const qgemv_status s = argmax_check(W, layout, xin, xf32, y_or_null, idx, N, K, T, ws, ws_bytes);
+    if (s != QGEMV_OK) return s;
+    if (!ws) return QGEMV_ERR_WORKSPACE;
     return run_single(W, layout, xin, y_or_null, reinterpret_cast<long long *>(idx), N, K, T, ws, ws_bytes,
                       reinterpret_cast<cudaStream_t>(stream), true, true, xf32);
 }
@@ -1186,6 +1199,20 @@ qgemv_status qgemv_debug_block_isums(const void *W, qgemv_wlayout layout, const 
                : QGEMV_ERR_CUDA;
 }
 
+qgemv_status qgemv_debug_block_isums_tc(const void *W, qgemv_wlayout layout, const void *xq, int32_t *isums,
+                                        int64_t N, int64_t K, int T, int f16_image, qgemv_stream_t stream)
+{
+    if (!shape_ok(N, K) || T < 1 || T > 8 || !W || !xq || !isums) return QGEMV_ERR_INVALID_ARG;
+    if (layout != QGEMV_W_GGML && layout != QGEMV_W_PACKED) return QGEMV_ERR_INVALID_ARG;
+    if (f16_image != 0 && f16_image != 1) return QGEMV_ERR_INVALID_ARG;
+    if (!aligned(W, layout == QGEMV_W_PACKED ? 16 : 2) || !aligned(xq, 16) || !aligned(isums, 4))
+        return QGEMV_ERR_MISALIGNED;
+    return launch_isums_tc(W, layout == QGEMV_W_PACKED, xq, isums, N, K, T, f16_image != 0,
+                           reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? QGEMV_OK
+               : QGEMV_ERR_CUDA;
+}
+
 qgemv_status qgemv_debug_stream_read(const void *src, size_t bytes, int method, int warps, int depth,
                                      int stage_bytes, unsigned long long *sink, qgemv_stream_t stream)
 {
@@ -1258,6 +1285,11 @@ extern "C" qgemv_status qgemv_q4_0_argmax_noalloc(const void *W, qgemv_wlayout l
 {
     if (!shape_ok(N, K) || T < 1 || T > 8) return QGEMV_ERR_INVALID_ARG;
     if (single_ws_bytes(N, K, T) > kNoAllocScratchBytes) return QGEMV_ERR_UNSUPPORTED;
+    // Every argument check first, on the host: a refused call makes no CUDA
+    // call and enqueues nothing (so it cannot clear the counters of a call
+    // still running on another stream).
+    const qgemv_status chk = argmax_check(W, layout, xq, false, y_or_null, idx, N, K, T, nullptr, 0);
+    if (chk != QGEMV_OK) return chk;
     int dev = 0;
     if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= kMaxDevices) return QGEMV_ERR_CUDA;
     void *scratch = nullptr;
@@ -1276,6 +1308,6 @@ extern "C" qgemv_status qgemv_q4_0_argmax_noalloc(const void *W, qgemv_wlayout l
     // counters must start at zero, so clear them on the caller's stream.
     const cudaStream_t st = reinterpret_cast<cudaStream_t>(stream);
     if (cudaMemsetAsync(scratch, 0, static_cast<size_t>(CNT_AREA), st) != cudaSuccess) return QGEMV_ERR_CUDA;
-    return qgemv_q4_0_argmax(W, layout, xq, y_or_null, idx, N, K, T, scratch,
-                             static_cast<size_t>(kNoAllocScratchBytes), stream);
+    return run_single(W, layout, xq, y_or_null, reinterpret_cast<long long *>(idx), N, K, T, scratch,
+                      static_cast<size_t>(kNoAllocScratchBytes), st, true, true);
 }

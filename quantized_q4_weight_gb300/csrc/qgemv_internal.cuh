@@ -254,6 +254,20 @@ __host__ __device__ __forceinline__ int quad_chunk(int jq, int r, int nbq)
     return nbq == QUAD ? ((jq + (r >> 1)) & 3) : jq;
 }
 
+// Byte offsets, in the packed layout, of block b of row `row` (a row of a
+// full slab): its 16 nibble bytes and its fp16 scale.
+__host__ __device__ __forceinline__ void packed_offsets(long long row, int b, int nb, long long &nib_off,
+                                                        long long &sc_off)
+{
+    const long long s = row / SLAB_ROWS;
+    const int r = static_cast<int>(row - s * SLAB_ROWS);
+    const int q = b / QUAD, jq = b - q * QUAD;
+    const int nbq = nb - q * QUAD < QUAD ? nb - q * QUAD : QUAD;
+    const long long base = s * static_cast<long long>(SLAB_COL_BYTES) * nb + static_cast<long long>(q) * QUAD_BYTES;
+    nib_off = base + (r * nbq + quad_chunk(jq, r, nbq)) * 16;
+    sc_off = base + 256 * nbq + ((r % 8) * nbq + jq) * 4 + (r / 8) * 2;
+}
+
 // Shared-memory image of one GEMV's activations: T rows of K int8 (rows
 // padded on the tensor-core (MMA) path so that the eight token rows fall in
 // distinct banks), the fp16 scales as copied, then per block and token the folded

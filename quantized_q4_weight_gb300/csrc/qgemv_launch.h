@@ -21,6 +21,10 @@ cudaError_t launch_stream_bench(const void *src, long long bytes, int method, in
 cudaError_t launch_pack(const void *src, void *dst, long long N, long long K, bool to_packed, cudaStream_t st);
 cudaError_t launch_isums(const void *W, bool packed, const void *xq, int32_t *isums, long long N, long long K, int T,
                          cudaStream_t st);
+// The tensor-core path's block sums (isums_tc.cu): f16_image selects the
+// operands of small activation images (built in f16) or of the int8 image.
+cudaError_t launch_isums_tc(const void *W, bool packed, const void *xq, int32_t *isums, long long N, long long K,
+                            int T, bool f16_image, cudaStream_t st);
 cudaError_t launch_q8_pack(const void *src, void *dst, long long N, long long K, bool to_packed, cudaStream_t st);
 // Q8_0-weight GEMV (q8_kernel.cu): plans, and launches when do_launch.
 // *ws_need: workspace bytes; *unsupported: 1 the activations do not fit

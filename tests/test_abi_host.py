@@ -173,3 +173,32 @@ def test_fp32_calls_reject_bad_arguments(L):
     assert L.qgemv_q4_0_gather_f32(mats2, 1, FAKE + (1 << 31), 2, 4, 1, 1, ws, 4096, s) == 1
     assert L.qgemv_gather_f32_workspace_bytes(mats2, 1, 2, 1) == 0
     assert L.qgemv_seq_f32_workspace_bytes(items, 2, 1) >= 16384
+
+
+def test_noalloc_refusals_before_any_cuda_call(L):
+    """The allocation-free argmax checks every argument on the host first:
+    these refusals make no CUDA call (so they also pass without a GPU)."""
+    s = None
+    W, xq, idx = FAKE, FAKE + (1 << 28), FAKE + (1 << 29)
+    f = L.qgemv_q4_0_argmax_noalloc
+    assert f(W, 1, xq, None, idx, 64, 64, 0, s) == 1              # T out of range
+    assert f(W, 1, xq, None, idx, 64, 64, 9, s) == 1
+    assert f(W, 1, xq, None, idx, 64, 100, 1, s) == 1             # K % 32 != 0
+    assert f(W, 1, xq, None, idx, 0, 64, 1, s) == 1
+    # split-K partials of 600 slabs x 512 blocks x 8 tokens: 9.8 MB > 4 MiB
+    assert f(None, 1, None, None, None, 9600, 16384, 8, s) == 3   # QGEMV_ERR_UNSUPPORTED
+    assert L.qgemv_workspace_bytes(9600, 16384, 8) > 4 << 20
+    assert f(None, 1, xq, None, idx, 64, 64, 1, s) == 1           # null weights
+    assert f(W, 1, xq, None, None, 64, 64, 1, s) == 1             # null idx
+    assert f(W, 1, xq + 4, None, idx, 64, 64, 1, s) == 2          # misaligned activations
+    assert f(W + 8, 1, xq, None, idx, 64, 64, 1, s) == 2          # packed weights need 16 bytes
+    assert f(W, 1, xq, idx - 8, idx, 64, 64, 1, s) == 1           # y over idx
+    assert f(W, 1, xq, W + 64, idx, 64, 64, 1, s) == 1            # y over the weights
+
+
+def test_tensor_core_isums_hook_rejects_bad_arguments(L):
+    s = None
+    assert L.qgemv_debug_block_isums_tc(FAKE, 1, FAKE, FAKE, 16, 64, 1, 2, s) == 1
+    assert L.qgemv_debug_block_isums_tc(FAKE, 1, FAKE, None, 16, 64, 1, 0, s) == 1
+    assert L.qgemv_debug_block_isums_tc(FAKE, 1, FAKE, FAKE, 16, 64, 9, 0, s) == 1
+    assert L.qgemv_debug_block_isums_tc(FAKE + 8, 1, FAKE, FAKE, 16, 64, 1, 0, s) == 2

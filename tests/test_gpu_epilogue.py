@@ -88,7 +88,10 @@ def test_seq_epilogue_errors():
     N, K, T = 64, 256, 2
     W = torch.zeros(q.q4_0_bytes(N, K), dtype=torch.uint8, device=DEV)
     xq = torch.zeros(q.xq_bytes(T, K), dtype=torch.uint8, device=DEV)
-    y = torch.zeros((T, N), device=DEV)
+    # y and its shifted residual are slices of one buffer, so that even an
+    # accepted call would stay inside an allocation
+    yy = torch.zeros(T * N + 1, device=DEV)
+    y = yy[:T * N].view(T, N)
     y2 = torch.zeros((T, N), device=DEV)
     buf = torch.zeros(4 * N + 4, device=DEV)
     ws = q.new_workspace(1 << 20)
@@ -103,7 +106,7 @@ def test_seq_epilogue_errors():
     bad_b[0].bias = buf.data_ptr() + 2                                    # misaligned bias
     assert call(bad_b) == 2
     part = q.seq_ep_items([(W, xq, y, N, K, None, y)])
-    part[0].residual = y.data_ptr() + 4                                   # residual shifted over y
+    part[0].residual = yy.data_ptr() + 4                                  # residual shifted over y
     assert call(part) == 1
     other = q.seq_ep_items([(W, xq, y, N, K, None, y2), (W, xq, y2, N, K, None, None)])
     assert call(other) == 1                                               # residual over another output

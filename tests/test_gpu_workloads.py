@@ -8,7 +8,7 @@ import torch
 import bench
 import oracle
 import quantized_q4_weight_gb300 as q
-from tests.gpu_util import check_close
+from tests.gpu_util import check_close, rank_vs_fp64, report_near_ties
 
 pytestmark = pytest.mark.gpu
 DEV = torch.device("cuda", 0)
@@ -27,7 +27,8 @@ def host(t: torch.Tensor) -> np.ndarray:
 
 
 @pytest.mark.parametrize("name,T", [("qwen2.5-1.5b_layerset", 1), ("qwen2.5-3b_verify", 8),
-                                    ("qwen2.5-3b_verify", 5), ("qwen2.5-3b_verify", 1)])
+                                    ("qwen2.5-3b_verify", 5), ("qwen2.5-3b_verify", 4),
+                                    ("qwen2.5-3b_verify", 2), ("qwen2.5-3b_verify", 1)])
 def test_layer_sets_sampled(orc, name, T):
     wl = bench.build_workload(name, DEV, T=T, keep_host=True)
     wl.step()                                   # fp32 inputs, one quantiser + one GEMV launch
@@ -80,6 +81,7 @@ def test_layer_set_epilogue_full(orc):
 def test_lm_head_argmax_full(orc):
     wl = bench.build_workload("lm_head_argmax", DEV, keep_host=True)
     y = torch.empty((wl.T, wl.N), dtype=torch.float32, device=DEV)
+    ties = tokens = 0
     for c in range(len(wl.W)):
         wl.copy = c
         wl.step()
@@ -91,9 +93,10 @@ def test_lm_head_argmax_full(orc):
         check_close(yh, y64, S, "lm_head")
         for t in range(wl.T):
             assert idx[t] == orc.argmax_f32(yh[t])
-            i64 = orc.argmax_f64(y64[t])
-            if idx[t] != i64:
-                assert abs(y64[t, idx[t]] - y64[t, i64]) <= oracle.tolerance(S[t, idx[t]]) + oracle.tolerance(S[t, i64])
+        ties += rank_vs_fp64(idx, [orc.argmax_f64(y64[t]) for t in range(wl.T)], y64, S, f"lm_head copy {c}",
+                             log=False)
+        tokens += wl.T
+    report_near_ties("lm_head 151936 x 1536, every copy", ties, tokens)
 
 
 def test_single_full(orc):

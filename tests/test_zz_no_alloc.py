@@ -60,6 +60,12 @@ def test_noalloc_matches_workspace_entry_point(orc, N, K, T):
         assert np.array_equal(idx.cpu().numpy(), idx_ref), call
         check_close(yh, y64, S, f"noalloc call {call}")
         assert np.array_equal(yh.view(np.int32), y_ref.view(np.int32)), call
+    # the usual lm_head use: no logits, the index only
+    idx = torch.full((T,), -1, dtype=torch.int64, device=DEV)
+    assert noalloc(W, xq, None, idx, N, K, T) == 0
+    torch.cuda.synchronize()
+    assert q.device_status() == 0
+    assert np.array_equal(idx.cpu().numpy(), idx_ref)
 
 
 def test_noalloc_rejects_shapes_beyond_its_scratch(orc):
