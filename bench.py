@@ -58,6 +58,7 @@ class Workload:
         self.host = {}            # optional host copies for parity checks
         self.kernel_name = "qgemv_stream_kernel"  # the step's streaming kernel
         self.config = {}
+        self.rotation = 1         # steps after which the step's inputs repeat
 
     @property
     def step_bytes(self) -> int:
@@ -81,10 +82,12 @@ def _upload_packed(q, torch, Wg, N, K, dev):
     return Wp
 
 
-def build_layerset(name, layer, layers, T, seed, dev, keep_host=False, epilogue=False):
+def build_layerset(name, layer, layers, T, seed, dev, keep_host=False, epilogue=False, reuse_W=None):
     """Layer set in order.  One step = one fp32-input sequence call (one
     persistent launch that also quantises the activations).  epilogue: qkv
-    adds a bias [N], o and down add a residual [T][N] (seeded inputs)."""
+    adds a bias [N], o and down add a residual [T][N] (seeded inputs).
+    reuse_W: the packed weights of an earlier build of the same set (another
+    T), used instead of generating them again."""
     import torch
     q = _q()
     wl = Workload(name, T)
@@ -105,12 +108,15 @@ def build_layerset(name, layer, layers, T, seed, dev, keep_host=False, epilogue=
     wl.y = [wl.y_all[ys_off[i]:ys_off[i] + T * N].view(T, N) for i, (_, N, K) in enumerate(mats)]
     wl.W, wl.xq = [], []
     for i, (nm, N, K) in enumerate(mats):
-        Wg = synth.q4_0_weights(seed, N, K, stream=(i,))
-        if keep_host:
-            wl.host[i] = Wg
-        wl.W.append(_upload_packed(q, torch, Wg, N, K, dev))
+        if reuse_W is not None:
+            wl.W.append(reuse_W[i])
+        else:
+            Wg = synth.q4_0_weights(seed, N, K, stream=(i,))
+            if keep_host:
+                wl.host[i] = Wg
+            wl.W.append(_upload_packed(q, torch, Wg, N, K, dev))
         wl.xq.append(q.quantize_q8_0(wl.x[i], T, K))
-        wl.w_bytes += Wg.nbytes
+        wl.w_bytes += q.q4_0_bytes(N, K)
         wl.x_bytes += 4 * T * K
         wl.y_bytes += 4 * T * N
         wl.xq_bytes += q.xq_bytes(T, K)
@@ -192,6 +198,7 @@ def build_lm_head(T, seed, dev, copies=4, keep_host=False, N=151936, K=1536):
         wl.copy = (wl.copy + 1) % copies
 
     wl.step, wl.kernel = step, kernel
+    wl.rotation = copies
     wl.inputs, wl.outputs = [wl.x], [wl.idx]
     wl.config = {"workload": "lm_head_argmax", "N": N, "K": K, "T": T, "copies": copies,
                  "l2_defeat": f"{copies} weight copies in rotation ({copies * wl.w_bytes / 1e6:.0f} MB)"}
@@ -371,6 +378,7 @@ def build_single(T, seed, dev, copies=400, N=1536, K=1536, keep_host=False):
         wl.copy = (wl.copy + 1) % copies
 
     wl.step, wl.kernel = step, kernel
+    wl.rotation = copies
     wl.inputs, wl.outputs = [wl.x], [wl.y]
     wl.config = {"workload": "single_1536", "N": N, "K": K, "T": T, "copies": copies,
                  "l2_defeat": f"{copies} weight copies in rotation"}
@@ -446,6 +454,7 @@ def build_moe(T, seed, dev, sets=4, n_experts=256, top_k=8, d_model=2048, d_ff=5
     quantize()  # the kernel-only launches' inputs
     wl.quantize = quantize
     wl.step, wl.kernel = step, kernel
+    wl.rotation = 64  # the seeded tokens' expert ids cycle every 64 steps (the 4 sets every 4)
     wl.inputs, wl.outputs = [wl.x_in, wl.x_dn], [wl.yg, wl.yu, wl.yd]
     wl.config = {"workload": "moe_top8_shared", "experts": n_experts, "top_k": top_k, "shared": 1, "T": T,
                  "sets": sets, "l2_defeat": f"{sets} expert sets in rotation ({sets * ne * 3 * q.q4_0_bytes(d_ff, d_model) / 1e9:.2f} GB)"}
@@ -453,12 +462,12 @@ def build_moe(T, seed, dev, sets=4, n_experts=256, top_k=8, d_model=2048, d_ff=5
 
 
 def build_workload(name: str, dev, T: int | None = None, keep_host: bool = False,
-                   layers: int | None = None) -> Workload:
+                   layers: int | None = None, reuse_W=None) -> Workload:
     spec = synth.WORKLOADS[name]
     if spec["kind"] == "seq":
         T = T or spec.get("T", 1)
         return build_layerset(name, spec["layer"], layers or spec["layers"], T, spec["seed"], dev, keep_host,
-                              spec.get("epilogue", False))
+                              spec.get("epilogue", False), reuse_W)
     if spec["kind"] == "argmax":
         return build_lm_head(T or spec["T"], spec["seed"], dev, spec["copies"], keep_host, spec["N"], spec["K"])
     if spec["kind"] == "verify":
@@ -769,6 +778,8 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--layers", type=int, default=None,
                     help="fewer layers of a layer-set workload (smaller profiling captures only)")
+    ap.add_argument("--no-workloads", action="store_true",
+                    help="skip the other configurations' records (the default workload at N=1 measures them)")
     args = ap.parse_args(argv)
     assert args.warmup >= 3, "at least 3 warm-up steps"
     if args.impl == "reference":
@@ -789,10 +800,18 @@ def main(argv=None):
     spec = synth.WORKLOADS[args.workload]
     Ts = [args.T] if args.T else list(spec.get("Ts", [spec.get("T", 1)]))
     results = {}
+    workloads = None
     for T in Ts:
-        results[T] = measure(args, build_workload(args.workload, dev, T=T, layers=args.layers), dev, world, rank)
+        wl = build_workload(args.workload, dev, T=T, layers=args.layers)
+        results[T] = measure(args, wl, dev, world, rank)
+        if (T == Ts[0] and world == 1 and args.workload == DEFAULT_WORKLOAD and not args.no_workloads
+                and args.layers is None):
+            workloads = measure_workloads(dev, wl)
+        del wl
         torch.cuda.empty_cache()
     head = results[Ts[0]]
+    if workloads is not None:
+        head["workloads"] = workloads
     for r in results.values():
         r["config"]["own_stream_gbs"] = round(own_stream, 1)
         r["config"]["pct_of_own_stream"] = round(100 * r["value"] / world / own_stream, 2)
@@ -814,6 +833,110 @@ def main(argv=None):
         import torch.distributed as tdist
         tdist.destroy_process_group()
     return 0
+
+
+# The other configurations of the metric, measured in the same run (one
+# record each in the line's "workloads" list): the single 1536 x 1536 GEMV,
+# the 28-layer Qwen2.5-1.5B set, the lm_head with argmax, the Qwen2.5-3B set
+# at T = 1, 2, 4, 8 and the routed-expert step.
+REPEAT_MIN_MS = 50.0   # each repeat times at least this much work
+REPEATS = 7
+GRAPH_CAP = 512        # steps captured in one graph (replayed as often as a repeat needs)
+
+
+def repeat_timing(torch, dev, stream, wl):
+    """Per-step device time of a workload: n steps captured once in a CUDA
+    graph (n a multiple of the workload's rotation, so that every replay
+    walks its weight copies in the same cyclic order and each copy comes
+    back only after the whole rotation), replayed k times inside each of
+    REPEATS timed repeats of at least REPEAT_MIN_MS.  Returns (median, min,
+    max) microseconds per step and the steps per repeat."""
+    for _ in range(3):
+        wl.step()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for _ in range(max(8, wl.rotation)):
+        wl.step()
+    b.record(stream)
+    torch.cuda.synchronize()
+    est_ms = a.elapsed_time(b) / max(8, wl.rotation)
+    rot = max(1, wl.rotation)
+    n = min(GRAPH_CAP, max(1, int(REPEAT_MIN_MS / est_ms) + 1))
+    n = max(rot, (n + rot - 1) // rot * rot)
+    g = capture_steps(torch, dev, stream, wl.step, n)
+    if g is None:
+        raise RuntimeError(f"{wl.name}: graph capture failed")
+    g.replay()
+    torch.cuda.synchronize()
+    k = max(1, int(REPEAT_MIN_MS / (n * est_ms)) + 1)
+    per = []
+    for _ in range(REPEATS):
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for _ in range(k):
+            g.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        per.append(a.elapsed_time(b) * 1e3 / (n * k))
+    del g
+    return statistics.median(per), min(per), max(per), n * k
+
+
+def workload_record(torch, dev, stream, wl, label: str, peak: float, base_us: float | None = None):
+    q = _q()
+    med, lo, hi, steps = repeat_timing(torch, dev, stream, wl)
+    assert q.device_status() == 0
+    gbs = wl.step_bytes / (med * 1e-6) / 1e9
+    rec = {"config": label, "workload": wl.name, "T": wl.T, "us_per_step": round(med, 3),
+           "us_min": round(lo, 3), "us_max": round(hi, 3), "repeats": REPEATS, "steps_per_repeat": steps,
+           "bytes_per_step": wl.step_bytes, "weight_bytes_per_step": wl.w_bytes,
+           "value": round(gbs, 2), "unit": UNIT, "frac_of_peak": round(gbs / peak, 4), "peak": peak,
+           "gemvs_per_step": wl.n_gemv, "us_per_gemv": round(med / wl.n_gemv, 3),
+           "traffic": traffic_record(wl.name, wl.T),
+           "l2_defeat": wl.config.get("l2_defeat")}
+    if base_us is not None:
+        rec["cost_vs_T1"] = round(med / base_us, 4)
+    return rec
+
+
+def measure_workloads(dev, head_wl):
+    """One record per configuration of the metric (see REPEAT_MIN_MS)."""
+    import torch
+    stream = torch.cuda.current_stream(dev)
+    peak, peak_kind = peaks()
+    clocks = ClockSampler(torch.cuda.current_device())
+    clocks.start()
+    recs = []
+    wl = build_workload("single_1536", dev)
+    recs.append(workload_record(torch, dev, stream, wl, "single 1536 x 1536, T=1, quantiser included", peak))
+    del wl
+    torch.cuda.empty_cache()
+    recs.append(workload_record(torch, dev, stream, head_wl,
+                                "Qwen2.5-1.5B 28-layer set, T=1 (the headline's workload)", peak))
+    wl = build_workload("lm_head_argmax", dev)
+    recs.append(workload_record(torch, dev, stream, wl, "lm_head 151936 x 1536 + argmax, T=1, 4 copies", peak))
+    del wl
+    torch.cuda.empty_cache()
+    W3, base = None, None
+    for T in (1, 2, 4, 8):
+        wl = build_workload("qwen2.5-3b_verify", dev, T=T, reuse_W=W3)
+        W3 = wl.W
+        r = workload_record(torch, dev, stream, wl, f"Qwen2.5-3B 36-layer set, T={T}", peak, base)
+        base = base or r["us_per_step"]
+        r["cost_vs_T1"] = round(r["us_per_step"] / base, 4)
+        recs.append(r)
+        del wl
+    del W3
+    torch.cuda.empty_cache()
+    wl = build_workload("moe_top8_shared", dev)
+    recs.append(workload_record(torch, dev, stream, wl, "MoE top-8 + shared expert, T=1, 4 expert sets", peak))
+    del wl
+    torch.cuda.empty_cache()
+    clk = clocks.stop()
+    return {"records": recs, "peak_kind": peak_kind, "clocks": clk,
+            "timed_as": f"{REPEATS} repeats, each >= {REPEAT_MIN_MS:.0f} ms of CUDA-graph replays of whole "
+                        f"rotations of the workload's weight copies; median, min and max per step"}
 
 
 def capture_steps(torch, dev, stream, fn, n: int):
