@@ -254,6 +254,58 @@ size_t qgemv_q8_0_workspace_bytes(int64_t N, int64_t K, int T);
 qgemv_status qgemv_q8_0(const void *W, const void *xq, float *y, int64_t N, int64_t K, int T,
                         void *ws, size_t ws_bytes, qgemv_stream_t stream);
 
+/* ---- Grouped int4 weights with per-vector int8 activations (colibri
+ * qwen36 docs: the gs64 container, one scale per group of 64 weights, its
+ * nibbles repacked once into a planar layout where one AND gives a group's
+ * first 32 elements in order and one shift the other 32; the dense int8 IDOT
+ * GEMV: the activation quantised to int8 once per call with one scale
+ * amax / 127, the integer sums exact and scaled afterwards).
+ * Row planes (host or device, the container's form):
+ *   wq     [N][K/64][32] bytes: byte j of a group holds element j (low
+ *          nibble) and element j + 32 (high nibble); weight = (n - 8) * s;
+ *   wscale [N][K/64] fp32: the groups' scales s.
+ * Activations: q int8 [T][K] and one fp32 scale s_x per token row.
+ * Output: y[t][i] = s_x[t] * sum_g s[i][g] * isum, isum the exact int32 sum
+ * over the group, accumulated in fp32 in a fixed order that depends on K
+ * only: per stage of 8 groups the even and the odd groups each summed in
+ * increasing order from +0 (one fused multiply-add of s * (16 isum) per
+ * group), the two added, the stage sums added in order, the total times
+ * 1/16, then times s_x; bit-identical for every T and launch shape.
+ * K % 64 == 0. */
+
+/* Bytes of the packed layout: 36 * N * K / 64 (0 for an invalid shape). */
+size_t qgemv_gs64_bytes(int64_t N, int64_t K);
+
+/* One-time repack of the row planes (device buffers) into the device layout:
+ * 16-row slabs of 8-group stages (4608 bytes), each row's 16-byte nibble
+ * chunks placed so the GEMV's lanes read shared memory conflict-free, then
+ * the stage's scales; the N % 16 tail rows follow, each as its nibbles then
+ * its scales.  wscale 4-byte aligned, w_packed 16-byte aligned (not
+ * overlapping the planes).  qgemv_unpack_gs64 is the inverse. */
+qgemv_status qgemv_pack_gs64(const void *wq, const float *wscale, void *w_packed, int64_t N, int64_t K,
+                             qgemv_stream_t stream);
+qgemv_status qgemv_unpack_gs64(const void *w_packed, void *wq, float *wscale, int64_t N, int64_t K,
+                               qgemv_stream_t stream);
+
+/* Per-vector int8 quantisation of R rows x[R][K] (fp32, 4-byte aligned):
+ * s[r] = amax / 127 over the whole row (fp32 IEEE division), 1/s from it
+ * (0 when amax = 0), q[r][k] = round-half-away(x * (1/s)) as int8.  One
+ * launch; q, s device buffers not overlapping x. */
+qgemv_status qgemv_quantize_vec_i8(const float *x, int8_t *q, float *s, int R, int64_t K, qgemv_stream_t stream);
+
+/* Workspace bytes for qgemv_gs64 (0 when the launch needs none; 0 also for
+ * an invalid shape).  Zero-filled before its first use, left zeroed. */
+size_t qgemv_gs64_workspace_bytes(int64_t N, int64_t K, int T);
+
+/* y[T][N] = W . x for packed gs64 weights W (16-byte aligned), activation
+ * codes q [T][K] (16-byte aligned) and scales s [T] (4-byte aligned); y
+ * 4-byte aligned, not overlapping W, q, s or ws.  Returns
+ * QGEMV_ERR_UNSUPPORTED when the T * K codes do not fit shared memory beside
+ * one weight stage per warp (about T * K <= 200000), QGEMV_ERR_WORKSPACE when
+ * ws is smaller than qgemv_gs64_workspace_bytes. */
+qgemv_status qgemv_gs64(const void *W, const int8_t *q, const float *s, float *y, int64_t N, int64_t K, int T,
+                        void *ws, size_t ws_bytes, qgemv_stream_t stream);
+
 /* ---- The FFN of a decode step (minfer README M15: the whole layer runs
  * around its GEMVs; colibri qwen36 docs: gate and up share one pass over the
  * activation):  y = W_down . Q8_0(SiLU(W_gate . x) * (W_up . x)).

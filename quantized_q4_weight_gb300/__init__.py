@@ -101,6 +101,12 @@ _SIGS = {
     "qgemv_gather_f32_workspace_bytes": ([ctypes.POINTER(GatherF32Matrix), _I32, _I32, _I32], _SZ),
     "qgemv_q4_0_gather_f32": ([ctypes.POINTER(GatherF32Matrix), _I32, _VP, _I32, _I32, _I32, _I32, _VP, _SZ, _VP],
                               _I32),
+    "qgemv_gs64_bytes": ([_I64, _I64], _SZ),
+    "qgemv_pack_gs64": ([_VP, _VP, _VP, _I64, _I64, _VP], _I32),
+    "qgemv_unpack_gs64": ([_VP, _VP, _VP, _I64, _I64, _VP], _I32),
+    "qgemv_quantize_vec_i8": ([_VP, _VP, _VP, _I32, _I64, _VP], _I32),
+    "qgemv_gs64_workspace_bytes": ([_I64, _I64, _I32], _SZ),
+    "qgemv_gs64": ([_VP, _VP, _VP, _VP, _I64, _I64, _I32, _VP, _SZ, _VP], _I32),
     "qgemv_debug_block_isums": ([_VP, _I32, _VP, _VP, _I64, _I64, _I32, _VP], _I32),
     "qgemv_debug_block_isums_tc": ([_VP, _I32, _VP, _VP, _I64, _I64, _I32, _I32, _VP], _I32),
     "qgemv_debug_stream_read": ([_VP, _SZ, _I32, _I32, _I32, _I32, _VP, _VP], _I32),
@@ -430,6 +436,44 @@ def block_isums(W, layout: int, xq, N: int, K: int, T: int, stream=None) -> torc
     _check(lib().qgemv_debug_block_isums(_ptr(W), layout, _ptr(xq), _ptr(out), N, K, T, _stream(stream)),
            "qgemv_debug_block_isums")
     return out
+
+
+def gs64_bytes(N: int, K: int) -> int:
+    return int(lib().qgemv_gs64_bytes(N, K))
+
+
+def pack_gs64(wq, wscale, N: int, K: int, stream=None) -> torch.Tensor:
+    """Row planes (nibbles [N][K/64][32] uint8, scales [N][K/64] fp32) -> packed device layout."""
+    out = torch.empty(gs64_bytes(N, K), dtype=torch.uint8, device=wq.device)
+    _check(lib().qgemv_pack_gs64(_ptr(wq), _ptr(wscale), _ptr(out), N, K, _stream(stream)), "qgemv_pack_gs64")
+    return out
+
+
+def unpack_gs64(W, N: int, K: int, stream=None):
+    wq = torch.empty((N, K // 64, 32), dtype=torch.uint8, device=W.device)
+    ws = torch.empty((N, K // 64), dtype=torch.float32, device=W.device)
+    _check(lib().qgemv_unpack_gs64(_ptr(W), _ptr(wq), _ptr(ws), N, K, _stream(stream)), "qgemv_unpack_gs64")
+    return wq, ws
+
+
+def quantize_vec_i8(x, R: int, K: int, stream=None):
+    """fp32 x [R][K] -> (int8 codes [R][K], fp32 scales [R]), one scale per row."""
+    q = torch.empty((R, K), dtype=torch.int8, device=x.device)
+    s = torch.empty(R, dtype=torch.float32, device=x.device)
+    _check(lib().qgemv_quantize_vec_i8(_ptr(x), _ptr(q), _ptr(s), R, K, _stream(stream)), "qgemv_quantize_vec_i8")
+    return q, s
+
+
+def gs64_workspace_bytes(N: int, K: int, T: int) -> int:
+    return int(lib().qgemv_gs64_workspace_bytes(N, K, T))
+
+
+def gemv_gs64(W, q, s, N: int, K: int, T: int, ws=None, y=None, stream=None) -> torch.Tensor:
+    if y is None:
+        y = torch.empty((T, N), dtype=torch.float32, device=W.device)
+    _check(lib().qgemv_gs64(_ptr(W), _ptr(q), _ptr(s), _ptr(y), N, K, T, _ptr(ws) if ws is not None else None,
+                            ws.numel() if ws is not None else 0, _stream(stream)), "qgemv_gs64")
+    return y
 
 
 def block_isums_tc(W, layout: int, xq, N: int, K: int, T: int, f16_image: bool, stream=None) -> torch.Tensor:

@@ -128,13 +128,6 @@ __device__ __forceinline__ int dp4a_ss8(const uint4 &w0, const uint4 &w1, const 
     return s;  // |s| <= 32 * 128 * 127 < 2^20
 }
 
-__device__ __forceinline__ uint4 lds128(uint32_t a)
-{
-    uint4 v;
-    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
-    return v;
-}
-
 // The lane's terms of one block for every token: acc[t] += (d_w d_x) isum.
 // isum enters fp32 exactly through the magic-number form (|isum| < 2^22).
 template <int T>

@@ -715,6 +715,92 @@ qgemv_status qgemv_q8_0(const void *W, const void *xq, float *y, int64_t N, int6
     return e == cudaSuccess ? QGEMV_OK : QGEMV_ERR_CUDA;
 }
 
+// ------------------------------------------------------------ gs64 int4 groups
+
+static bool gs64_shape_ok(long long N, long long K) { return shape_ok(N, K) && K % 64 == 0; }
+
+size_t qgemv_gs64_bytes(int64_t N, int64_t K)
+{
+    return gs64_shape_ok(N, K) ? static_cast<size_t>(36ll * N * (K / 64)) : 0;
+}
+
+qgemv_status qgemv_pack_gs64(const void *wq, const float *wscale, void *w_packed, int64_t N, int64_t K,
+                             qgemv_stream_t stream)
+{
+    if (!gs64_shape_ok(N, K) || !wq || !wscale || !w_packed) return QGEMV_ERR_INVALID_ARG;
+    if (!aligned(wscale, 4) || !aligned(w_packed, 16)) return QGEMV_ERR_MISALIGNED;
+    const Range rp = range(w_packed, 36ll * N * (K / 64));
+    if (overlap(rp, range(wq, 32ll * N * (K / 64))) || overlap(rp, range(wscale, 4ll * N * (K / 64))))
+        return QGEMV_ERR_INVALID_ARG;
+    return launch_gs64_pack(const_cast<void *>(wq), const_cast<float *>(wscale), w_packed, N, K, true,
+                            reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? QGEMV_OK
+               : QGEMV_ERR_CUDA;
+}
+
+qgemv_status qgemv_unpack_gs64(const void *w_packed, void *wq, float *wscale, int64_t N, int64_t K,
+                               qgemv_stream_t stream)
+{
+    if (!gs64_shape_ok(N, K) || !wq || !wscale || !w_packed) return QGEMV_ERR_INVALID_ARG;
+    if (!aligned(wscale, 4) || !aligned(w_packed, 16)) return QGEMV_ERR_MISALIGNED;
+    const Range rp = range(w_packed, 36ll * N * (K / 64)), rq = range(wq, 32ll * N * (K / 64)),
+                rs = range(wscale, 4ll * N * (K / 64));
+    if (overlap(rp, rq) || overlap(rp, rs) || overlap(rq, rs)) return QGEMV_ERR_INVALID_ARG;
+    return launch_gs64_pack(wq, wscale, const_cast<void *>(w_packed), N, K, false,
+                            reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? QGEMV_OK
+               : QGEMV_ERR_CUDA;
+}
+
+qgemv_status qgemv_quantize_vec_i8(const float *x, int8_t *q, float *s, int R, int64_t K, qgemv_stream_t stream)
+{
+    if (R < 1 || R > 65535 || K < 1 || K > (1ll << 24) || !x || !q || !s) return QGEMV_ERR_INVALID_ARG;
+    if (!aligned(x, 4) || !aligned(s, 4)) return QGEMV_ERR_MISALIGNED;
+    const Range rx = range(x, 4ll * R * K), rq = range(q, 1ll * R * K), rs = range(s, 4ll * R);
+    if (overlap(rx, rq) || overlap(rx, rs) || overlap(rq, rs)) return QGEMV_ERR_INVALID_ARG;
+    return launch_quantize_vec_i8(x, q, s, R, K, reinterpret_cast<cudaStream_t>(stream)) == cudaSuccess
+               ? QGEMV_OK
+               : QGEMV_ERR_CUDA;
+}
+
+size_t qgemv_gs64_workspace_bytes(int64_t N, int64_t K, int T)
+{
+    if (!gs64_shape_ok(N, K) || T < 1 || T > 8) return 0;
+    DevInfo dev;
+    int sms = 152, budget = 230400;
+    if (device_info(dev) == QGEMV_OK) {
+        sms = dev.sms;
+        budget = dev.smem_optin - 2048;
+    }
+    long long need = 0;
+    int uns = 0;
+    launch_gs64(nullptr, nullptr, nullptr, nullptr, N, K, T, nullptr, 0, false, sms, budget, nullptr, nullptr, &need,
+                &uns);
+    return static_cast<size_t>(need);
+}
+
+qgemv_status qgemv_gs64(const void *W, const int8_t *q, const float *s, float *y, int64_t N, int64_t K, int T,
+                        void *ws, size_t ws_bytes, qgemv_stream_t stream)
+{
+    if (!gs64_shape_ok(N, K) || T < 1 || T > 8 || !W || !q || !s || !y) return QGEMV_ERR_INVALID_ARG;
+    if (!aligned(W, 16) || !aligned(q, 16) || !aligned(s, 4) || !aligned(y, 4) || (ws && !aligned(ws, 256)))
+        return QGEMV_ERR_MISALIGNED;
+    const Range ry = range(y, 4ll * T * N);
+    if (overlap(ry, range(W, 36ll * N * (K / 64))) || overlap(ry, range(q, 1ll * T * K)) ||
+        overlap(ry, range(s, 4ll * T)) || (ws && overlap(ry, range(ws, static_cast<long long>(ws_bytes)))))
+        return QGEMV_ERR_INVALID_ARG;
+    DevInfo dev;
+    qgemv_status st = device_info(dev);
+    if (st != QGEMV_OK) return st;
+    long long need = 0;
+    int uns = 0;
+    const cudaError_t e = launch_gs64(W, q, s, y, N, K, T, ws, static_cast<long long>(ws_bytes), true, dev.sms,
+                                      dev.smem_optin - 2048, dev.status, reinterpret_cast<cudaStream_t>(stream),
+                                      &need, &uns);
+    if (uns) return uns == 1 ? QGEMV_ERR_UNSUPPORTED : QGEMV_ERR_WORKSPACE;
+    return e == cudaSuccess ? QGEMV_OK : QGEMV_ERR_CUDA;
+}
+
 // ------------------------------------------------------------ FFN step
 
 // Workspace of qgemv_q4_0_ffn: [gate/up sequence][g][u][h codes][down call],

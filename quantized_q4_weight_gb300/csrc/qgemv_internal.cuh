@@ -194,6 +194,14 @@ __device__ __forceinline__ uint64_t global_timer_ns()
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_launch_dependents() { asm volatile("griddepcontrol.launch_dependents;"); }
 
+// 16 bytes from shared memory (16-byte aligned shared address).
+__device__ __forceinline__ uint4 lds128(uint32_t a)
+{
+    uint4 v;
+    asm volatile("ld.shared.v4.u32 {%0, %1, %2, %3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w) : "r"(a));
+    return v;
+}
+
 // sum of 4 (unsigned byte of a) * (signed byte of b) + c.
 __device__ __forceinline__ int dp4a_us(unsigned a, int b, int c)
 {

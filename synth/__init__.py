@@ -20,6 +20,9 @@ Value recipe (the same for every workload):
     Token columns are independent.
   * Expert ids: k distinct ids out of n_experts per token (uniform subset,
     drawn without replacement).
+  * gs64 grouped int4 weights (64 weights per group in 32 nibble bytes, one
+    fp32 scale): nibble bytes uniform on 0..255, scales uniform real on
+    [1e-3, 4e-3] kept in fp32.
 """
 from __future__ import annotations
 
@@ -59,6 +62,19 @@ def q8_0_weights(seed: int, N: int, K: int, stream: tuple = ()) -> np.ndarray:
     blocks[:, :, 0:2] = scales.astype("<f2").view(np.uint8).reshape(N, nb, 2)
     blocks[:, :, 2:] = rng.integers(-127, 128, size=(N, nb, 32)).astype(np.int8).view(np.uint8)
     return blocks.reshape(N, nb * 34)
+
+
+def gs64_weights(seed: int, N: int, K: int, stream: tuple = ()):
+    """Random gs64 grouped int4 matrix as its two row planes: nibble bytes
+    uint8 [N, K/64, 32] (every byte uniform on 0..255, so every nibble is
+    uniform on 0..15) and fp32 group scales [N, K/64] uniform real on
+    [1e-3, 4e-3] (drawn in fp64, cast once)."""
+    assert K % 64 == 0 and N >= 0
+    ng = K // 64
+    rng = _rng(seed, 6, *stream)
+    wq = rng.integers(0, 256, size=(N, ng, 32), dtype=np.uint8)
+    ws = rng.uniform(SCALE_LO, SCALE_HI, size=(N, ng)).astype(np.float32)
+    return wq, ws
 
 
 def f32_weights(seed: int, N: int, K: int, stream: tuple = ()) -> np.ndarray:

@@ -202,3 +202,21 @@ def test_tensor_core_isums_hook_rejects_bad_arguments(L):
     assert L.qgemv_debug_block_isums_tc(FAKE, 1, FAKE, None, 16, 64, 1, 0, s) == 1
     assert L.qgemv_debug_block_isums_tc(FAKE, 1, FAKE, FAKE, 16, 64, 9, 0, s) == 1
     assert L.qgemv_debug_block_isums_tc(FAKE + 8, 1, FAKE, FAKE, 16, 64, 1, 0, s) == 2
+
+
+def test_gs64_calls_reject_bad_arguments(L):
+    s = None
+    assert L.qgemv_gs64_bytes(16, 96) == 0 and L.qgemv_gs64_bytes(16, 128) == 36 * 16 * 2
+    assert L.qgemv_gs64_workspace_bytes(16, 96, 1) == 0
+    W, qa, sa, y = FAKE, FAKE + (1 << 28), FAKE + (1 << 29), FAKE + (1 << 30)
+    assert L.qgemv_gs64(W, qa, sa, y, 64, 96, 1, None, 0, s) == 1            # K % 64 != 0
+    assert L.qgemv_gs64(W, qa, sa, y, 64, 128, 9, None, 0, s) == 1           # T out of range
+    assert L.qgemv_gs64(W + 8, qa, sa, y, 64, 128, 1, None, 0, s) == 2       # packed weights: 16 bytes
+    assert L.qgemv_gs64(W, qa + 4, sa, y, 64, 128, 1, None, 0, s) == 2       # codes: 16 bytes
+    assert L.qgemv_gs64(W, qa, sa, W + 64, 64, 128, 1, None, 0, s) == 1      # y over the weights
+    assert L.qgemv_gs64(W, qa, sa, qa + 16, 64, 128, 1, None, 0, s) == 1     # y over the codes
+    assert L.qgemv_pack_gs64(W, sa, W + 64, 16, 128, s) == 1                 # output over the nibbles
+    assert L.qgemv_pack_gs64(W, sa + 2, y, 16, 128, s) == 2
+    assert L.qgemv_quantize_vec_i8(W, qa, sa, 0, 64, s) == 1
+    assert L.qgemv_quantize_vec_i8(W, W + 16, sa, 1, 64, s) == 1             # codes over x
+    assert L.qgemv_quantize_vec_i8(W + 2, qa, sa, 1, 64, s) == 2
