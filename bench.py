@@ -318,6 +318,54 @@ def build_q8(T, seed, dev, copies=2, keep_host=False, N=151936, K=1536):
     return wl
 
 
+def build_gs64(T, seed, dev, copies=4, keep_host=False, N=151936, K=1536):
+    """A dense matrix of the lm_head's shape in the gs64 grouped int4 format
+    (colibri qwen36 docs: the dense trunk stored as int4 in groups of 64 with
+    one scale each): one step quantises x once per vector to int8 and runs
+    the gs64 GEMV (two launches); copies rotate so reads hit HBM."""
+    import torch
+    q = _q()
+    wl = Workload("gs64_lm_head", T)
+    wl.N, wl.K = N, K
+    wl.W = []
+    for c in range(copies):
+        wq, ws = synth.gs64_weights(seed, N, K, stream=(c,))
+        if keep_host:
+            wl.host[c] = (wq, ws)
+        wl.W.append(q.pack_gs64(torch.from_numpy(wq).to(dev), torch.from_numpy(ws).to(dev), N, K))
+    wl.x = torch.from_numpy(synth.activations(seed, T, K)).to(dev)
+    wl.qx, wl.sx = q.quantize_vec_i8(wl.x, T, K)
+    wl.y = torch.empty((T, N), dtype=torch.float32, device=dev)
+    wl.ws = q.new_workspace(q.gs64_workspace_bytes(N, K, T), dev)
+    wl.w_bytes = q.gs64_bytes(N, K)
+    wl.x_bytes, wl.y_bytes, wl.xq_bytes = 4 * T * K, 4 * T * N, T * K + 4 * T
+    wl.n_gemv, wl.launches = 1, 2
+    wl.copy = 0
+
+    def kernel(stream=None):
+        q.gemv_gs64(wl.W[wl.copy], wl.qx, wl.sx, N, K, T, wl.ws, y=wl.y, stream=stream)
+        wl.copy = (wl.copy + 1) % copies
+
+    def step(stream=None):
+        q.quantize_vec_i8_into(wl.x, wl.qx, wl.sx, T, K, stream=stream)
+        kernel(stream)
+
+    wl.step, wl.kernel, wl.dominant = step, kernel, kernel
+    wl.rotation = copies
+    wl.dominant_bytes = wl.w_bytes + wl.xq_bytes + wl.y_bytes
+    wl.other_launch = "the step's other launch is the per-vector int8 quantiser"
+    wl.kernel_name = "gs64_gemv_kernel"
+    wl.dtype = "uint4 x int8 -> int32 group sums, fp32 accumulation"
+    wl.data = ("synthetic (seeded; gs64 nibbles uniform, fp32 group scales U[1e-3,4e-3], "
+               "x N(0,1) with 1% x20)")
+    wl.inputs, wl.outputs = [wl.x], [wl.y]
+    wl.config = {"workload": "gs64_lm_head", "N": N, "K": K, "T": T, "copies": copies,
+                 "weights": "gs64 (64-weight groups, fp32 scale)",
+                 "step": "per-vector int8 quantiser launch, then the gs64 GEMV launch",
+                 "l2_defeat": f"{copies} weight copies in rotation ({copies * wl.w_bytes / 1e6:.0f} MB)"}
+    return wl
+
+
 def build_requant(T, seed, dev, copies=2, keep_host=False, N=151936, K=1536):
     """Load-time requantisation of the Q8_0 lm_head to Q4_0 blocks (one
     launch per step); two source copies rotate so reads hit HBM."""
@@ -477,6 +525,8 @@ def build_workload(name: str, dev, T: int | None = None, keep_host: bool = False
                          keep_host)
     if spec["kind"] == "q8":
         return build_q8(T or spec["T"], spec["seed"], dev, spec["copies"], keep_host, spec["N"], spec["K"])
+    if spec["kind"] == "gs64":
+        return build_gs64(T or spec["T"], spec["seed"], dev, spec["copies"], keep_host, spec["N"], spec["K"])
     if spec["kind"] == "requant":
         return build_requant(T or spec["T"], spec["seed"], dev, spec["copies"], keep_host, spec["N"], spec["K"])
     if spec["kind"] == "single":
@@ -505,6 +555,7 @@ KERNEL_SOURCES = {
     "qgemv_stream_kernel": ["gemv_kernel.cuh", "launch_stream.cuh"] + [f"gemv_t{t}.cu" for t in range(1, 9)],
     "q8_gemv_kernel": ["q8_kernel.cu"],
     "requant_q4_0_staged_q8": ["kernels_misc.cu"],
+    "gs64_gemv_kernel": ["gs64_kernel.cu"],
 }
 
 
@@ -605,7 +656,7 @@ def _oracle_inputs(workload: str):
         if spec["kind"] == "seq":
             T = 1
             mats = synth.layer_set(spec["layer"], spec["layers"])
-        elif spec["kind"] in ("argmax", "single", "verify", "q8", "requant"):
+        elif spec["kind"] in ("argmax", "single", "verify", "q8", "requant", "gs64"):
             T, mats = spec["T"], [("w", spec["N"], spec["K"])]
         elif spec["kind"] == "ffn":
             T = spec["T"]
@@ -615,6 +666,11 @@ def _oracle_inputs(workload: str):
             T = 1
             mats = [("gate", spec["d_ff"], spec["d_model"]), ("up", spec["d_ff"], spec["d_model"]),
                     ("down", spec["d_model"], spec["d_ff"])] * (spec["top_k"] + 1)
+        if spec["kind"] == "gs64":
+            _ORACLE_INPUTS[workload] = (T, [(N, K, synth.gs64_weights(spec["seed"], N, K, stream=(i,)),
+                                             synth.activations(spec["seed"], T, K, stream=(i,)))
+                                            for i, (_, N, K) in enumerate(mats)])
+            return _ORACLE_INPUTS[workload]
         gen = synth.q8_0_weights if spec["kind"] in ("q8", "requant") else synth.q4_0_weights
         data = [(N, K, gen(spec["seed"], N, K, stream=(i,)),
                  synth.activations(spec["seed"], T, K, stream=(i,))) for i, (_, N, K) in enumerate(mats)]
@@ -655,15 +711,21 @@ def oracle_sample(workload: str, budget_s: float = 12.0, min_s: float = 3.0, thr
     T, data = _oracle_inputs(workload)
     if synth.WORKLOADS[workload]["kind"] == "requant":
         return _oracle_requant_sample(o, data, budget_s, min_s)
-    gemv = o.gemv_q8 if synth.WORKLOADS[workload]["kind"] == "q8" else o.gemv
+    kind = synth.WORKLOADS[workload]["kind"]
+    gemv = o.gemv_q8 if kind == "q8" else o.gemv
     done_bytes, t_total, n_done = 0, 0.0, 0
     while True:
         for N, K, Wg, x in data:
             t0 = time.perf_counter()
-            xq = o.quantize(x)
-            gemv(Wg, N, K, xq, T)
+            if kind == "gs64":
+                o.gemv_gs64(Wg[0], Wg[1], N, K, *o.quantize_vec_i8(x))
+                wbytes = Wg[0].nbytes + Wg[1].nbytes
+            else:
+                xq = o.quantize(x)
+                gemv(Wg, N, K, xq, T)
+                wbytes = Wg.nbytes
             t_total += time.perf_counter() - t0
-            done_bytes += Wg.nbytes + 4 * T * K + 4 * T * N
+            done_bytes += wbytes + 4 * T * K + 4 * T * N
             n_done += 1
             if t_total >= budget_s:
                 break
@@ -931,6 +993,11 @@ def measure_workloads(dev, head_wl):
     torch.cuda.empty_cache()
     wl = build_workload("moe_top8_shared", dev)
     recs.append(workload_record(torch, dev, stream, wl, "MoE top-8 + shared expert, T=1, 4 expert sets", peak))
+    del wl
+    torch.cuda.empty_cache()
+    wl = build_workload("gs64_lm_head", dev)
+    recs.append(workload_record(torch, dev, stream, wl,
+                                "gs64 grouped int4, 151936 x 1536, per-vector int8 x, T=1, 4 copies", peak))
     del wl
     torch.cuda.empty_cache()
     clk = clocks.stop()

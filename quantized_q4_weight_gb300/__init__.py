@@ -464,6 +464,11 @@ def quantize_vec_i8(x, R: int, K: int, stream=None):
     return q, s
 
 
+def quantize_vec_i8_into(x, q, s, R: int, K: int, stream=None):
+    """quantize_vec_i8 into existing buffers."""
+    _check(lib().qgemv_quantize_vec_i8(_ptr(x), _ptr(q), _ptr(s), R, K, _stream(stream)), "qgemv_quantize_vec_i8")
+
+
 def gs64_workspace_bytes(N: int, K: int, T: int) -> int:
     return int(lib().qgemv_gs64_workspace_bytes(N, K, T))
 

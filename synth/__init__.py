@@ -151,6 +151,9 @@ WORKLOADS = {
     "qwen2.5-1.5b_ffn": dict(kind="ffn", d_model=1536, d_ff=8960, layers=28, T=1, seed=5000),
     # the lm_head held as Q8_0 weights (248 MB per copy), T=1, 2 copies in rotation
     "q8_lm_head": dict(kind="q8", N=151936, K=1536, T=1, copies=2, seed=2200),
+    # a dense matrix of the lm_head's shape in the gs64 grouped int4 format,
+    # per-vector int8 activations, T=1, 4 copies in rotation
+    "gs64_lm_head": dict(kind="gs64", N=151936, K=1536, T=1, copies=4, seed=2400),
     # load-time requantisation of that Q8_0 lm_head to Q4_0
     "lm_head_requant_q8": dict(kind="requant", N=151936, K=1536, T=1, copies=2, seed=2300),
     # 36-layer Qwen2.5-3B-shaped layer set, T in {1,2,4,8}

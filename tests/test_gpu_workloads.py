@@ -124,3 +124,19 @@ def test_moe_full(orc):
             xq = xin if m < 2 else orc.quantize(xdn[s:s + 1])
             y64, S = orc.gemv(wl.host[(m, int(e))], N, K, xq, 1)
             check_close(outs[m][s], y64, S, f"moe m={m} slot={s}")
+
+
+def test_gs64_lm_head_full(orc):
+    """The gs64 workload as bench.py times it (quantiser launch, then the
+    GEMV), every output of each weight copy against the oracle."""
+    wl = bench.build_workload("gs64_lm_head", DEV, keep_host=True)
+    for c in range(len(wl.W)):
+        wl.copy = c
+        wl.step()
+        torch.cuda.synchronize()
+        assert q.device_status() == 0
+        qr, sr = orc.quantize_vec_i8(host(wl.x))
+        assert np.array_equal(host(wl.qx), qr) and np.array_equal(host(wl.sx).view(np.int32), sr.view(np.int32))
+        wq, ws = wl.host[c]
+        y64, S = orc.gemv_gs64(wq, ws, wl.N, wl.K, qr, sr)
+        check_close(host(wl.y), y64, S, f"gs64 lm_head copy {c}")
