@@ -840,6 +840,8 @@ def main(argv=None):
     ap.add_argument("--e2e-steps", type=int, default=20)
     ap.add_argument("--layers", type=int, default=None,
                     help="fewer layers of a layer-set workload (smaller profiling captures only)")
+    ap.add_argument("--tc-min-tokens", type=int, default=0,
+                    help="token count from which packed sequences use the tcgen05 kernel (0 = library default, 9 = never)")
     ap.add_argument("--no-workloads", action="store_true",
                     help="skip the other configurations' records (the default workload at N=1 measures them)")
     args = ap.parse_args(argv)
@@ -857,6 +859,7 @@ def main(argv=None):
     from quantized_q4_weight_gb300 import _build
     _build.build()
     q = _q()
+    q.set_tc_min_T(args.tc_min_tokens)
 
     own_stream = own_stream_gbs(dev)
     spec = synth.WORKLOADS[args.workload]

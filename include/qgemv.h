@@ -555,6 +555,17 @@ qgemv_status qgemv_debug_stream_read(const void *src, size_t bytes, int method, 
  * Process-wide; affects launches enqueued afterwards. */
 qgemv_status qgemv_set_tuning(int ctas_per_sm, int waves, int mma_min_T, int ring_depth);
 
+/* Token count from which packed sequences (qgemv_q4_0_seq, _seq_f32)
+ * run on the tcgen05 tensor-core kernel (1..8; 9 = never, the default; 0
+ * restores the default).  The kernel is off by default because the
+ * mma.sync path measures faster on GB300 at every T.  It applies to launches without epilogues whose matrices all
+ * have N % 16 == 0 and K % 256 == 0 and whose workspace is as large as
+ * qgemv_seq_workspace_bytes (or _seq_f32_) returns while it is enabled;
+ * other launches keep the other kernels.  Results do not change: every path
+ * forms the same block sums and adds them in the same order.  fp32 inputs
+ * are quantised first, in one launch, into the workspace.  Process-wide. */
+qgemv_status qgemv_set_tc_min_tokens(int tc_min_T);
+
 /* Read and clear the current device's status word: QGEMV_OK, or the first
  * asynchronous error a kernel recorded (QGEMV_ERR_TIMEOUT, QGEMV_ERR_BAD_ID)
  * into *code_out.  Synchronises with the device (a query, not part of the

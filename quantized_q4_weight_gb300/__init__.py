@@ -111,6 +111,7 @@ _SIGS = {
     "qgemv_debug_block_isums_tc": ([_VP, _I32, _VP, _VP, _I64, _I64, _I32, _I32, _VP], _I32),
     "qgemv_debug_stream_read": ([_VP, _SZ, _I32, _I32, _I32, _I32, _VP, _VP], _I32),
     "qgemv_set_tuning": ([_I32, _I32, _I32, _I32], _I32),
+    "qgemv_set_tc_min_tokens": ([_I32], _I32),
     "qgemv_device_status": ([ctypes.POINTER(ctypes.c_int)], _I32),
 }
 
@@ -498,6 +499,11 @@ def stream_read(src, method: int, warps: int, depth: int, stage_bytes: int, sink
 def set_tuning(ctas_per_sm: int = 0, waves: int = 0, mma_min_T: int = 0, ring_depth: int = 0):
     """Tuning of the streaming kernel (0 = default for each); results are unchanged."""
     _check(lib().qgemv_set_tuning(ctas_per_sm, waves, mma_min_T, ring_depth), "qgemv_set_tuning")
+
+
+def set_tc_min_T(tc_min_T: int = 0):
+    """Token count from which packed sequences run on the tcgen05 kernel (0 = default: never; 1..8; 9 = never)."""
+    _check(lib().qgemv_set_tc_min_tokens(tc_min_T), "qgemv_set_tc_min_tokens")
 
 
 def device_status() -> int:

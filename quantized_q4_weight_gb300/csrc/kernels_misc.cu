@@ -1,5 +1,7 @@
 // kernels_misc.cu -- activation quantiser, weight pack / unpack and the
 // block-sum test hook.
+#include <cstring>
+
 #include "qgemv_launch.h"
 
 namespace qg {
@@ -47,6 +49,58 @@ __global__ void __launch_bounds__(256) quantize_q8_0_kernel(const float *__restr
         const long long bi = gb / per_batch;
         quantize_block_warp(x + bi * per_batch * QK, xq + bi * xq_bytes, R, K, gb - bi * per_batch, xq_bytes, lane);
     }
+}
+
+// A whole sequence's activations in one launch: item i's T rows of K[i]
+// fp32 values into its planar buffer, the same bytes as launch_quantize.
+struct QuantList {
+    int n, T;
+    const float *x[MAXG_SEQ];
+    uint8_t *xq[MAXG_SEQ];
+    int K[MAXG_SEQ];
+    long long block_begin[MAXG_SEQ + 1];  // prefix of T * K[i] / 32
+};
+
+__global__ void __launch_bounds__(256) quantize_list_kernel(const __grid_constant__ QuantList L)
+{
+    pdl_launch_dependents();
+    pdl_wait();
+    const int lane = threadIdx.x & 31;
+    int i = 0;
+    for (long long gb = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; gb < L.block_begin[L.n];
+         gb += (static_cast<long long>(gridDim.x) * blockDim.x) >> 5) {
+        while (L.block_begin[i + 1] <= gb) ++i;  // blocks are visited in increasing order per warp
+        const long long xqb = static_cast<long long>(L.T) * L.K[i] + ((2ll * L.T * (L.K[i] / QK) + 15) & ~15ll);
+        quantize_block_warp(L.x[i], L.xq[i], L.T, L.K[i], gb - L.block_begin[i], xqb, lane);
+    }
+}
+
+cudaError_t launch_quantize_list(const float *const *x, uint8_t *const *xq, const long long *K, int n, int T,
+                                 cudaStream_t st)
+{
+    if (n < 1 || n > MAXG_SEQ) return cudaErrorInvalidValue;
+    QuantList L;
+    memset(&L, 0, sizeof(L));
+    L.n = n;
+    L.T = T;
+    for (int i = 0; i < n; ++i) {
+        L.x[i] = x[i];
+        L.xq[i] = xq[i];
+        L.K[i] = static_cast<int>(K[i]);
+        L.block_begin[i + 1] = L.block_begin[i] + static_cast<long long>(T) * (K[i] / QK);
+    }
+    long long grid = (L.block_begin[n] + 7) / 8;
+    if (grid > 65535) grid = 65535;
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(static_cast<unsigned>(grid));
+    cfg.blockDim = dim3(256);
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, quantize_list_kernel, L);
 }
 
 cudaError_t launch_quantize(const float *x, void *xq, int R, long long K, int batch, cudaStream_t st)

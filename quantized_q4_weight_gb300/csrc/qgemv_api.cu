@@ -36,6 +36,17 @@ std::atomic<int> g_ctas_per_sm{0}, g_waves{0}, g_ring_depth{0};
 // Token count from which T > 1 runs on the f16 tensor-core path (0 = default).
 std::atomic<int> g_mma_min_T{0};
 constexpr int kDefaultMmaMinT = 5;
+// Token count from which packed sequences run on the tcgen05 kernel (0 =
+// default; 9 = never).  Off by default: on GB300 the mma.sync path is faster
+// at every T (3B 36-layer set, T = 8: 0.37 ms against 0.73 ms).
+std::atomic<int> g_tc_min_T{0};
+constexpr int kDefaultTcMinT = 9;
+
+inline bool tc_for(int T)
+{
+    const int m = g_tc_min_T.load(std::memory_order_relaxed);
+    return T >= (m >= 1 ? m : kDefaultTcMinT);
+}
 
 inline bool mma_for(int T)
 {
@@ -942,7 +953,38 @@ inline long long sg_ctas_hint(int T)
     return grid_for(dev, ctas_per_sm_for(T, true));
 }
 
-size_t qgemv_seq_workspace_bytes(const qgemv_seq_item *items, int n, int T)
+// The tcgen05 path of one launch's items (c0, cn): eligible or not, and its
+// workspace (with the quantised activations' area for fp32 inputs).
+static bool tc_chunk(const qgemv_seq_item *items, int c0, int cn, int T, qgemv_wlayout layout, std::vector<TcSpec> &sp)
+{
+    if (layout != QGEMV_W_PACKED || !tc_for(T)) return false;
+    sp.resize(cn);
+    for (int i = 0; i < cn; ++i) {
+        const qgemv_seq_item &it = items[c0 + i];
+        sp[i] = TcSpec{it.W, it.xq, it.y, it.N, it.K};
+    }
+    return tc_eligible(sp.data(), cn, T);
+}
+
+static long long tc_grid()
+{
+    DevInfo dev;
+    return device_info(dev) == QGEMV_OK ? dev.sms : 152;
+}
+
+static long long tc_chunk_ws(const std::vector<TcSpec> &sp, int T, bool xf32)
+{
+    long long b = align_up(tc_ws_bytes(sp.data(), static_cast<int>(sp.size()), static_cast<int>(tc_grid())), 256);
+    if (xf32)
+        for (const TcSpec &s : sp) b += align_up(xq_bytes_host(T, s.K), 256);
+    return b;
+}
+
+static size_t seq_ws(const qgemv_seq_item *items, int n, int T, bool xf32);
+
+size_t qgemv_seq_workspace_bytes(const qgemv_seq_item *items, int n, int T) { return seq_ws(items, n, T, false); }
+
+static size_t seq_ws(const qgemv_seq_item *items, int n, int T, bool xf32)
 {
     if (!items || n < 1 || T < 1 || T > 8) return 0;
     long long total = 0;
@@ -959,6 +1001,8 @@ size_t qgemv_seq_workspace_bytes(const qgemv_seq_item *items, int n, int T)
         make_plan<MAXG_SEQ>(gs.data(), cn, T, true, false, nullptr, 0, *pb);
         long long b = pa->ws_bytes > pb->ws_bytes ? pa->ws_bytes : pb->ws_bytes;
         if (pa->P.balanced_ok && mma_for(T)) b = align_up(b, 256) + sg_ctas_hint(T) * sg_stride_floats(gs.data(), cn, T) * 4;
+        std::vector<TcSpec> sp;
+        if (tc_chunk(items, c0, cn, T, QGEMV_W_PACKED, sp)) b = std::max(b, tc_chunk_ws(sp, T, xf32));
         if (b > total) total = b;  // consecutive launches reuse the workspace
     }
     return static_cast<size_t>(total);
@@ -1023,6 +1067,30 @@ static qgemv_status launch_seq(const qgemv_seq_item *items, int n, qgemv_wlayout
     std::unique_ptr<Plan<MAXG_SEQ>> pl(new Plan<MAXG_SEQ>());
     for (int c0 = 0; c0 < n; c0 += MAXG_SEQ) {
         const int cn = (n - c0) < MAXG_SEQ ? (n - c0) : MAXG_SEQ;
+        // the tcgen05 kernel (plain packed sequences whose workspace holds its
+        // sums; fp32 inputs are quantised first, into the workspace, in one launch)
+        std::vector<TcSpec> sp;
+        if (!bias && !res && tc_chunk(items, c0, cn, T, layout, sp) &&
+            static_cast<long long>(ws_bytes) >= tc_chunk_ws(sp, T, xf32)) {
+            uint8_t *w = static_cast<uint8_t *>(ws);
+            if (xf32) {
+                long long off = align_up(tc_ws_bytes(sp.data(), cn, dev.sms), 256);
+                std::vector<const float *> xs(cn);
+                std::vector<uint8_t *> xqs(cn);
+                std::vector<long long> ks(cn);
+                for (int i = 0; i < cn; ++i) {
+                    xs[i] = static_cast<const float *>(sp[i].xq);
+                    xqs[i] = w + off;
+                    ks[i] = sp[i].K;
+                    sp[i].xq = w + off;
+                    off += align_up(xq_bytes_host(T, sp[i].K), 256);
+                }
+                if (launch_quantize_list(xs.data(), xqs.data(), ks.data(), cn, T, st) != cudaSuccess)
+                    return QGEMV_ERR_CUDA;
+            }
+            if (launch_tc(sp.data(), cn, T, w, dev.sms, dev.status, st) != cudaSuccess) return QGEMV_ERR_CUDA;
+            continue;
+        }
         for (int i = 0; i < cn; ++i) {
             const qgemv_seq_item &it = items[c0 + i];
             gs[i] = GroupSpec{it.W, 0, it.xq, 0, it.y, 0, it.N, it.K, 1};
@@ -1084,7 +1152,7 @@ size_t qgemv_seq_f32_workspace_bytes(const qgemv_seq_f32_item *items, int n, int
     if (!items || n < 1 || T < 1 || T > 8) return 0;
     std::vector<qgemv_seq_item> sq;
     if (!seq_f32_items(items, n, sq)) return 0;
-    return qgemv_seq_workspace_bytes(sq.data(), n, T);
+    return seq_ws(sq.data(), n, T, true);
 }
 
 qgemv_status qgemv_q4_0_seq_f32(const qgemv_seq_f32_item *items, int n, qgemv_wlayout layout, int T, void *ws,
@@ -1326,6 +1394,13 @@ qgemv_status qgemv_set_tuning(int ctas_per_sm, int waves, int mma_min_T, int rin
     g_waves.store(waves);
     g_mma_min_T.store(mma_min_T);
     g_ring_depth.store(ring_depth);
+    return QGEMV_OK;
+}
+
+qgemv_status qgemv_set_tc_min_tokens(int tc_min_T)
+{
+    if (tc_min_T < 0 || tc_min_T > 9) return QGEMV_ERR_INVALID_ARG;
+    g_tc_min_T.store(tc_min_T);
     return QGEMV_OK;
 }
 

@@ -48,6 +48,25 @@ cudaError_t launch_requant_q4_0(const void *src, bool from_q8, void *dst, long l
 cudaError_t launch_verify_commit(const long long *tokens, const long long *pred, int pred_stride, int T,
                                  int32_t *n_commit, cudaStream_t st);
 
+// The few-token GEMV on tcgen05 tensor cores (gemv_tc.cu): a list of up to
+// MAXG_SEQ packed GEMVs with N % 16 == 0 and K % 256 == 0.  Workspace: warp
+// arrival counters in its first TC_CNT_BYTES (zero, and left zero), then the
+// segment sums of tiles shared by warp groups.
+struct TcSpec {
+    const void *W;
+    const void *xq;  // planar Q8_0 activations of T rows
+    float *y;
+    long long N, K;
+};
+constexpr long long TC_CNT_BYTES = 16384;
+bool tc_eligible(const TcSpec *s, int n, int T);
+long long tc_ws_bytes(const TcSpec *s, int n, int grid);
+cudaError_t launch_tc(const TcSpec *s, int n, int T, uint8_t *ws, int grid, unsigned *status, cudaStream_t st);
+// Q8_0 quantisation of n activation blocks x[i] (fp32 [T][K[i]]) into planar
+// buffers xq[i] (kernels_misc.cu): one launch for a whole sequence.
+cudaError_t launch_quantize_list(const float *const *x, uint8_t *const *xq, const long long *K, int n, int T,
+                                 cudaStream_t st);
+
 // The streaming GEMV kernel, one instantiation per (T, parameter-block size,
 // argmax, tensor-core path).  Defined in gemv_t<T>.cu.
 // EPI: the sequence output epilogue (bias, residual) is compiled in.

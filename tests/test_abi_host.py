@@ -77,6 +77,18 @@ def test_workspace_queries(L):
     assert L.qgemv_seq_workspace_bytes(items, 2, 4) == 16384
     for T in (5, 8):
         assert L.qgemv_seq_workspace_bytes(items, 2, T) == 16384 + 152 * 15 * 18 * T * 16 * 4
+    # with the tcgen05 kernel switched on, packed lists with N % 16 == 0 and
+    # K % 256 == 0 may run on it: 16 KB of counters, then for each of the
+    # 2 x 152 warp groups a slot of segment sums (18 segments x 8 x 128 rows)
+    tc = 16384 + 2 * 152 * 18 * 8 * 128 * 4
+    L.qgemv_set_tc_min_tokens(5)
+    try:
+        for T in (5, 8):
+            assert L.qgemv_seq_workspace_bytes(items, 2, T) == max(16384 + 152 * 15 * 18 * T * 16 * 4, tc)
+        assert L.qgemv_seq_workspace_bytes(items, 2, 4) == 16384
+    finally:
+        L.qgemv_set_tc_min_tokens(0)
+    assert L.qgemv_set_tc_min_tokens(10) == 1
     assert L.qgemv_seq_workspace_bytes(items, 0, 1) == 0
 
 
