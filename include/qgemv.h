@@ -309,7 +309,12 @@ qgemv_status qgemv_gs64(const void *W, const int8_t *q, const float *s, float *y
 /* ---- The FFN of a decode step (minfer README M15: the whole layer runs
  * around its GEMVs; colibri qwen36 docs: gate and up share one pass over the
  * activation):  y = W_down . Q8_0(SiLU(W_gate . x) * (W_up . x)).
- * Three launches on `stream`, chained by programmatic dependent launch:
+ * On packed weights with T <= 4 (d_model % 16 == 0, d_ff % 32 == 0) one
+ * cooperative launch runs all three steps (see qgemv_set_ffn_fused): it
+ * streams gate and up, writes h's Q8_0 codes, waits (bounded) until every
+ * CTA's share of h is written, and reduces the down projection, whose
+ * weights it has streamed meanwhile; otherwise three launches on `stream`,
+ * chained by programmatic dependent launch:
  *   1. gate and up, one sequence launch over the same fp32 x[T][d_model]
  *      (quantised inside the kernel; outputs g, u fp32 [T][d_ff] in ws);
  *   2. h = SiLU(g) * u with SiLU(g) = g / (1 + exp(-g)), exp by Cody and
@@ -554,6 +559,12 @@ qgemv_status qgemv_debug_stream_read(const void *src, size_t bytes, int method, 
  *                leave room.
  * Process-wide; affects launches enqueued afterwards. */
 qgemv_status qgemv_set_tuning(int ctas_per_sm, int waves, int mma_min_T, int ring_depth);
+
+/* qgemv_q4_0_ffn and qgemv_q4_0_ffn_residual as one fused launch (on = 1,
+ * the default) where it applies -- packed weights, T <= 4, d_model % 16 ==
+ * 0, d_ff % 32 == 0 -- or always as the three launches (on = 0).  Results
+ * do not change (the same steps in the same order).  Process-wide. */
+qgemv_status qgemv_set_ffn_fused(int on);
 
 /* Token count from which packed sequences (qgemv_q4_0_seq, _seq_f32)
  * run on the tcgen05 tensor-core kernel (1..8; 9 = never, the default; 0

@@ -112,6 +112,7 @@ _SIGS = {
     "qgemv_debug_stream_read": ([_VP, _SZ, _I32, _I32, _I32, _I32, _VP, _VP], _I32),
     "qgemv_set_tuning": ([_I32, _I32, _I32, _I32], _I32),
     "qgemv_set_tc_min_tokens": ([_I32], _I32),
+    "qgemv_set_ffn_fused": ([_I32], _I32),
     "qgemv_device_status": ([ctypes.POINTER(ctypes.c_int)], _I32),
 }
 
@@ -499,6 +500,11 @@ def stream_read(src, method: int, warps: int, depth: int, stage_bytes: int, sink
 def set_tuning(ctas_per_sm: int = 0, waves: int = 0, mma_min_T: int = 0, ring_depth: int = 0):
     """Tuning of the streaming kernel (0 = default for each); results are unchanged."""
     _check(lib().qgemv_set_tuning(ctas_per_sm, waves, mma_min_T, ring_depth), "qgemv_set_tuning")
+
+
+def set_ffn_fused(on: bool = True):
+    """The decode FFN step as one fused launch where it applies (else always three launches)."""
+    _check(lib().qgemv_set_ffn_fused(1 if on else 0), "qgemv_set_ffn_fused")
 
 
 def set_tc_min_T(tc_min_T: int = 0):

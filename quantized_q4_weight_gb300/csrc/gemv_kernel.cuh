@@ -1907,9 +1907,7 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
                             const int row = row0 + lane;
 #pragma unroll
                             for (int t = 0; t < T; ++t) {
-                                float v = __ldcg(pb + t * 16 + lane);
-                                for (int s2 = 1; s2 < g.nseg; ++s2)
-                                    v = __fadd_rn(v, __ldcg(pb + (s2 * T + t) * 16 + lane));
+                                const float v = ordered_sum_ldcg(pb + t * 16 + lane, g.nseg, T * 16);
                                 if (ye != nullptr) {
                                     const long long yi = static_cast<long long>(t) * N + row;
                                     ye[yi] = EPI ? apply_epilogue(v, g.bias, g.res, yi, row) : v;

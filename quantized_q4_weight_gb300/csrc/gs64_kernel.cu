@@ -431,9 +431,7 @@ __global__ void __launch_bounds__(NWARPS_MAX * 32, 1) gs64_gemv_kernel(const __g
 #pragma unroll
                 for (int t = 0; t < T; ++t) {
                     const float *pb = P.part + (static_cast<long long>(sl) * P.nstage * T + t) * SLAB_ROWS + r;
-                    float v = __ldcg(pb);
-                    for (int s2 = 1; s2 < P.nstage; ++s2)
-                        v = __fadd_rn(v, __ldcg(pb + static_cast<long long>(s2) * T * SLAB_ROWS));
+                    const float v = ordered_sum_ldcg(pb, P.nstage, static_cast<long long>(T) * SLAB_ROWS);
                     P.y[static_cast<long long>(t) * P.N + row] = g64_output(v, s_sx[t]);
                 }
             __syncwarp();

@@ -221,33 +221,8 @@ cudaError_t launch_isums(const void *W, bool packed, const void *xq, int32_t *is
 
 // ------------------------------------------------------------ FFN step
 //
-// h = SiLU(g) * u, quantised to planar Q8_0 for the down projection (minfer
-// README M15: the FFN between the GEMVs of a decode step).  exp by Cody and
-// Waite's method (W. J. Cody, W. Waite, "Software Manual for the Elementary
-// Functions", 1980): x = k ln2 + r, k = rint(x log2 e), ln 2 split into a
-// head whose products with k are exact and a tail; exp(r) by its Taylor
-// series to r^7/7! in Horner form; the exact scale 2^k.  x is clamped to
-// [-87, 88].  Every operation is an explicitly rounded fp32 one, in the
-// order written, so the values (and so the codes) are a fixed function of
-// g and u.
-__device__ __forceinline__ float ffn_exp(float x)
-{
-    x = fminf(fmaxf(x, -87.0f), 88.0f);
-    const float k = rintf(__fmul_rn(x, 1.44269504088896340736f));
-    float r = __fmaf_rn(-k, 0.693145751953125f, x);   // ln 2 head: 13 significant bits
-    r = __fmaf_rn(-k, 1.42860682030941723212e-6f, r);  // ln 2 - head
-    float p = 1.0f / 5040.0f;
-    p = __fmaf_rn(p, r, 1.0f / 720.0f);
-    p = __fmaf_rn(p, r, 1.0f / 120.0f);
-    p = __fmaf_rn(p, r, 1.0f / 24.0f);
-    p = __fmaf_rn(p, r, 1.0f / 6.0f);
-    p = __fmaf_rn(p, r, 0.5f);
-    p = __fmaf_rn(p, r, 1.0f);
-    p = __fmaf_rn(p, r, 1.0f);
-    return __fmul_rn(p, __int_as_float((static_cast<int>(k) + 127) << 23));
-}
-
-__device__ __forceinline__ float ffn_silu(float g) { return __fdiv_rn(g, __fadd_rn(1.0f, ffn_exp(-g))); }
+// h = SiLU(g) * u quantised to planar Q8_0 for the down projection: the
+// steps of ffn_exp / ffn_silu (qgemv_internal.cuh), then the Q8_0 steps.
 
 // One warp per block of 32: h for lane j, the block maximum by shuffles, then
 // the Q8_0 steps of the activation quantiser.  hq: T rows of F codes, then

@@ -42,6 +42,10 @@ constexpr int kDefaultMmaMinT = 5;
 std::atomic<int> g_tc_min_T{0};
 constexpr int kDefaultTcMinT = 9;
 
+// The decode FFN step as one fused launch where it applies (1) or always as
+// three launches (0).
+std::atomic<int> g_ffn_fused{1};
+
 inline bool tc_for(int T)
 {
     const int m = g_tc_min_T.load(std::memory_order_relaxed);
@@ -893,6 +897,23 @@ static qgemv_status ffn_chain(const void *W_gate, const void *W_up, const void *
         if (residual != y && (overlap(rr, ry) || overlap(rr, rw))) return QGEMV_ERR_INVALID_ARG;
     }
     uint8_t *w = static_cast<uint8_t *>(ws);
+    // one fused launch: h's codes where the chain keeps them, the down
+    // projection's segment sums in the down call's data area, counters in
+    // the workspace's zeroed counter area
+    if (layout == QGEMV_W_PACKED && g_ffn_fused.load(std::memory_order_relaxed)) {
+        DevInfo dev;
+        qgemv_status ds = device_info(dev);
+        if (ds != QGEMV_OK) return ds;
+        const long long nseg_dn = (d_ff / QK + SEG_BLOCKS - 1) / SEG_BLOCKS;
+        const long long part_bytes = (d_model / SLAB_ROWS) * nseg_dn * T * 16 * 4;
+        if (ffn_fused_fits(d_model, d_ff, T, dev.smem_optin - 2048) && off[4] + CNT_AREA + part_bytes <= need) {
+            const cudaError_t e =
+                launch_ffn_fused(W_gate, W_up, W_down, x, residual, y, d_model, d_ff, T, w + off[3],
+                                 reinterpret_cast<float *>(w + off[4] + CNT_AREA), reinterpret_cast<unsigned *>(w),
+                                 dev.sms, dev.smem_optin - 2048, dev.status, reinterpret_cast<cudaStream_t>(stream));
+            return e == cudaSuccess ? QGEMV_OK : QGEMV_ERR_CUDA;
+        }
+    }
     float *g = reinterpret_cast<float *>(w + off[1]);
     float *u = reinterpret_cast<float *>(w + off[2]);
     void *hq = w + off[3];
@@ -1394,6 +1415,13 @@ qgemv_status qgemv_set_tuning(int ctas_per_sm, int waves, int mma_min_T, int rin
     g_waves.store(waves);
     g_mma_min_T.store(mma_min_T);
     g_ring_depth.store(ring_depth);
+    return QGEMV_OK;
+}
+
+qgemv_status qgemv_set_ffn_fused(int on)
+{
+    if (on != 0 && on != 1) return QGEMV_ERR_INVALID_ARG;
+    g_ffn_fused.store(on);
     return QGEMV_OK;
 }
 

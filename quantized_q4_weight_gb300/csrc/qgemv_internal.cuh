@@ -343,6 +343,51 @@ __device__ __forceinline__ void q8_scale(float amax, float &d, float &id)
 __device__ __forceinline__ int q8_code(float v, float id) { return static_cast<int>(roundf(__fmul_rn(v, id))); }
 __device__ __forceinline__ unsigned short q8_half(float d) { return __half_as_ushort(__float2half_rn(d)); }
 
+// h = SiLU(g) * u, quantised to planar Q8_0 for the down projection (minfer
+// README M15: the FFN between the GEMVs of a decode step).  exp by Cody and
+// Waite's method (W. J. Cody, W. Waite, "Software Manual for the Elementary
+// Functions", 1980): x = k ln2 + r, k = rint(x log2 e), ln 2 split into a
+// head whose products with k are exact and a tail; exp(r) by its Taylor
+// series to r^7/7! in Horner form; the exact scale 2^k.  x is clamped to
+// [-87, 88].  Every operation is an explicitly rounded fp32 one, in the
+// order written, so the values (and so the codes) are a fixed function of
+// g and u.
+__device__ __forceinline__ float ffn_exp(float x)
+{
+    x = fminf(fmaxf(x, -87.0f), 88.0f);
+    const float k = rintf(__fmul_rn(x, 1.44269504088896340736f));
+    float r = __fmaf_rn(-k, 0.693145751953125f, x);   // ln 2 head: 13 significant bits
+    r = __fmaf_rn(-k, 1.42860682030941723212e-6f, r);  // ln 2 - head
+    float p = 1.0f / 5040.0f;
+    p = __fmaf_rn(p, r, 1.0f / 720.0f);
+    p = __fmaf_rn(p, r, 1.0f / 120.0f);
+    p = __fmaf_rn(p, r, 1.0f / 24.0f);
+    p = __fmaf_rn(p, r, 1.0f / 6.0f);
+    p = __fmaf_rn(p, r, 0.5f);
+    p = __fmaf_rn(p, r, 1.0f);
+    p = __fmaf_rn(p, r, 1.0f);
+    return __fmul_rn(p, __int_as_float((static_cast<int>(k) + 127) << 23));
+}
+
+__device__ __forceinline__ float ffn_silu(float g) { return __fdiv_rn(g, __fadd_rn(1.0f, ffn_exp(-g))); }
+
+// p[0] + p[stride] + ... + p[(n - 1) stride], added in index order from
+// p[0] (the fixed order of a split sum), loaded from L2 eight at a time so
+// that the loads' latencies overlap instead of adding up.
+__device__ __forceinline__ float ordered_sum_ldcg(const float *p, int n, long long stride)
+{
+    float v = __ldcg(p);
+    for (int i = 1; i < n; i += 8) {
+        float x[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) x[k] = i + k < n ? __ldcg(p + (i + k) * stride) : 0.0f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k)
+            if (i + k < n) v = __fadd_rn(v, x[k]);
+    }
+    return v;
+}
+
 // fp16 bits -> fp32 (exact).
 __device__ __forceinline__ float h2f(unsigned bits16)
 {

@@ -138,3 +138,37 @@ def test_ffn_errors():
         q.ffn_residual(W, W, W, q.W_PACKED, x, yy[1:].view(T, d_model), d_model, d_ff, T, ws,
                        y=yy[:T * d_model].view(T, d_model))
     assert q.device_status() == 0
+
+
+# the fused launch (T <= 4, packed) against the three launches: many h blocks
+# per CTA and fewer h blocks than CTAs, partial segments in both projections
+# (d_model = 96, d_ff = 8960 and 160), several rounds of h blocks (d_ff = 23 x
+# 32 x 152 > 4 per CTA), with and without the residual, repeated calls
+@pytest.mark.parametrize("d_model,d_ff,T", [(1536, 8960, 1), (1536, 8960, 4), (96, 160, 2), (2048, 11008, 3),
+                                           (512, 32 * 152 * 5, 1), (4096, 1024, 2)])
+def test_ffn_fused_matches_three_launches(orc, d_model, d_ff, T):
+    seed = 1000 + d_model + d_ff + T
+    Wg = q.pack_q4_0(to_dev(synth.q4_0_weights(seed, d_ff, d_model)), d_ff, d_model)
+    Wu = q.pack_q4_0(to_dev(synth.q4_0_weights(seed + 1, d_ff, d_model)), d_ff, d_model)
+    Wd = q.pack_q4_0(to_dev(synth.q4_0_weights(seed + 2, d_model, d_ff)), d_model, d_ff)
+    xd = torch.from_numpy(synth.activations(seed + 3, T, d_model)).to(DEV)
+    r = torch.from_numpy(synth.activations(seed + 4, T, d_model)).to(DEV)
+    ws = q.new_workspace(q.ffn_workspace_bytes(d_model, d_ff, T))
+    try:
+        q.set_ffn_fused(False)
+        y3 = q.ffn(Wg, Wu, Wd, q.W_PACKED, xd, d_model, d_ff, T, ws).cpu()
+        y3r = q.ffn_residual(Wg, Wu, Wd, q.W_PACKED, xd, r, d_model, d_ff, T, ws).cpu()
+        q.set_ffn_fused(True)
+        for _ in range(2):                                    # the counters are left at zero
+            y1 = q.ffn(Wg, Wu, Wd, q.W_PACKED, xd, d_model, d_ff, T, ws).cpu()
+            assert torch.equal(y1.view(torch.int32), y3.view(torch.int32))
+        y1r = q.ffn_residual(Wg, Wu, Wd, q.W_PACKED, xd, r, d_model, d_ff, T, ws).cpu()
+        assert torch.equal(y1r.view(torch.int32), y3r.view(torch.int32))
+        h = r.clone()                                         # in place: h += FFN(x)
+        q.ffn_residual(Wg, Wu, Wd, q.W_PACKED, xd, h, d_model, d_ff, T, ws, y=h)
+        assert torch.equal(h.cpu().view(torch.int32), y3r.view(torch.int32))
+    finally:
+        q.set_ffn_fused(True)
+    torch.cuda.synchronize()
+    assert q.device_status() == 0
+    assert int(ws[:16384].count_nonzero()) == 0
