@@ -4,20 +4,26 @@
 //     y = W_down . Q8_0(SiLU(W_gate . x) * (W_up . x))  [+ residual]
 //
 // One CTA per SM, launched cooperatively (all CTAs resident: the down
-// projection waits for every CTA's share of h).  Phase A: the h blocks (32
-// rows of d_ff: two gate slabs and two up slabs) are dealt to CTAs in turn;
-// four warps stream one block's four slabs, each CTA quantises x itself (the
-// standalone quantiser's bytes), and one warp per block forms h = SiLU(g) * u
-// and its Q8_0 codes (the steps of the three-launch chain's middle kernel) in
-// global memory, then counts the block done.  Phase B: the down projection's
-// (slab, segment) stages are dealt to CTAs in contiguous ranges, and inside
-// a CTA to the warps that phase A leaves idle first; each warp's ring holds
-// its stages from the start, so the down weights stream while phase A runs.
-// After a bounded wait for all h blocks, each CTA copies h's codes into
-// shared memory and every warp reduces its stages; the segment sums of a
-// slab are added in segment order by the last warp to finish one (atomic
-// counter), then the residual.  Every fp32 step is the one of the chain, in
-// the same order, so y is bit-identical to qgemv_q4_0_ffn's three launches.
+// projection waits for every CTA's share of h).  Work is dealt in weight
+// stages (one 16-block segment of one 16-row slab, 4608 bytes): a CTA's
+// stages are its phase-A stages, then its phase-B stages, and warp w of the
+// CTA streams every sixteenth of them through its own ring.
+//   Phase A: the h blocks (32 rows of d_ff: two gate slabs and two up
+//   slabs) are dealt to CTAs in turn; a block's 4 x nseg_up stages go to
+//   the warps, each writing its segment sums to shared memory.  Each CTA
+//   quantises x itself (the standalone quantiser's bytes).  One warp per
+//   block then adds every row's segment sums in segment order, forms
+//   h = SiLU(g) * u and its Q8_0 codes (the steps of the three-launch
+//   chain's middle kernel) in global memory, and counts the block done.
+//   Phase B: the down projection's slabs are dealt to CTAs in turn, a
+//   slab's nseg_dn stages to the warps; after a bounded wait for all h
+//   blocks each CTA copies h's codes into shared memory, every warp reduces
+//   its stages, and the slab's segment sums are added in segment order in
+//   shared memory, then the residual.
+// Every fp32 step is the one of the chain, in the same order, so y is
+// bit-identical to qgemv_q4_0_ffn's three launches.  Before the dependency
+// wait each warp asks L2 for its first stages, so the layer streams from
+// HBM while the CTA waits for its input.
 #include <algorithm>
 #include <atomic>
 #include <cstring>
@@ -29,9 +35,9 @@ namespace qg {
 
 constexpr int FF_WARPS = 16;
 constexpr int FF_THREADS = FF_WARPS * 32;
-constexpr int FF_RING = 2;    // weight stages in flight per warp
-constexpr int FF_HB = 4;      // h blocks a CTA works on at once (four warps each)
-constexpr int FF_CNT_WORDS = 4096;  // counters in the workspace's first 16 KB
+constexpr int FF_RING = 2;      // weight stages in flight per warp
+constexpr int FF_HB = 4;        // h blocks a CTA works on at once
+constexpr int FF_PREFETCH = 4;  // stages per warp requested into L2 beyond its ring at the start
 
 struct FfnParams {
     const uint8_t *Wg, *Wu, *Wd;  // packed weights
@@ -39,39 +45,45 @@ struct FfnParams {
     const float *res;             // [T][d_model] or nullptr
     float *y;                     // [T][d_model]
     uint8_t *hq;                  // planar Q8_0 of h: [T][d_ff] codes, then [T][d_ff / 32] fp16 scales
-    float *part;                  // down segment sums [nslab_dn][nseg_dn][T][16]
-    unsigned *cnt;                // [0] h blocks done, [1] CTAs past the wait, [2 + s] down slab s arrivals
+    unsigned *cnt;                // [0] h blocks done, [1] CTAs past the wait (both left at zero)
     unsigned *status;
     long long slab_up, slab_dn;   // bytes of one packed slab (288 nb)
     int d_model, d_ff;
     int nb_up, nb_dn, nseg_up, nseg_dn, nslab_dn;
     int nhb;                      // h blocks: d_ff / 32
-    int ndn;                      // down stages: nslab_dn * nseg_dn
-    int off_ring, off_bar, off_hbuf;  // shared memory: [activation area][hbuf][barriers][rings]
+    int off_part, off_bar, off_ring;  // shared memory: [activation area][segment sums][barriers][rings]
 };
 
-// The stages one warp consumes, in order: its phase-A slab items (round by
-// round, all segments of K = d_model each), then its phase-B stages (one
-// down (slab, segment) each).
+// The stages one warp consumes, in order: its phase-A stages round by round
+// (a round is up to FF_HB of the CTA's h blocks, stage a of a round being
+// (h block a / (4 nseg_up), slab (a / nseg_up) % 4, segment a % nseg_up)),
+// then its phase-B stages (stage b: the CTA's down slab b / nseg_dn,
+// segment b % nseg_dn); warp w takes the stages whose index is w modulo 16
+// in phase A and 15 - w in phase B, so that the warps with fewer phase-A
+// stages take the down stages first.
 struct FfWalk {
-    int phase;          // 0: A, 1: B, 2: done
-    int round, seg;     // A: round, segment of the current slab item
-    int k;              // B: index among the CTA's down stages
-    int nrounds, nhb_cta, dn0, dn1;
+    int phase;        // 0: A, 1: B, 2: done
+    int round, a, na; // A: round, stage in it, stages in it
+    int b;            // B: stage among the CTA's down stages
+    int nrounds, nhb_cta, nb_cta;
 
-    __device__ __forceinline__ bool a_item(int warp, int rnd) const { return FF_HB * rnd + (warp >> 2) < nhb_cta; }
+    __device__ __forceinline__ void start_round(const FfnParams &P)
+    {
+        na = min(FF_HB, nhb_cta - FF_HB * round) * 4 * P.nseg_up;
+    }
 
     __device__ __forceinline__ void settle(const FfnParams &P, int warp)
     {
-        while (phase == 0 && (round >= nrounds || !a_item(warp, round))) {
-            if (round >= nrounds) {
+        while (phase == 0 && a >= na) {
+            if (++round >= nrounds) {
                 phase = 1;
-                k = FF_WARPS - 1 - warp;  // this warp's first stage: items k with k % 16 == 15 - warp
+                b = FF_WARPS - 1 - warp;
                 break;
             }
-            ++round;
+            a = warp;
+            start_round(P);
         }
-        if (phase == 1 && dn0 + k >= dn1) phase = 2;
+        if (phase == 1 && b >= nb_cta) phase = 2;
     }
 
     __device__ __forceinline__ void init(const FfnParams &P, int warp)
@@ -79,47 +91,50 @@ struct FfWalk {
         const int G = gridDim.x, c = blockIdx.x;
         nhb_cta = c < P.nhb ? (P.nhb - c + G - 1) / G : 0;
         nrounds = (nhb_cta + FF_HB - 1) / FF_HB;
-        dn0 = static_cast<int>(static_cast<long long>(P.ndn) * c / G);
-        dn1 = static_cast<int>(static_cast<long long>(P.ndn) * (c + 1) / G);
+        nb_cta = (c < P.nslab_dn ? (P.nslab_dn - c + G - 1) / G : 0) * P.nseg_dn;
         phase = 0;
         round = 0;
-        seg = 0;
-        k = 0;
+        a = warp;
+        na = 0;
+        b = 0;
+        if (nrounds > 0) start_round(P);
         settle(P, warp);
     }
 
     __device__ __forceinline__ void advance(const FfnParams &P, int warp)
     {
         if (phase == 0) {
-            if (++seg < P.nseg_up) return;
-            seg = 0;
-            ++round;
+            a += FF_WARPS;
             settle(P, warp);
         } else if (phase == 1) {
-            k += FF_WARPS;
-            if (dn0 + k >= dn1) phase = 2;
+            b += FF_WARPS;
+            if (b >= nb_cta) phase = 2;
         }
     }
 
-    // The h block of this warp's phase-A item, and the item's slab and matrix.
-    __device__ __forceinline__ int hb(int warp) const { return blockIdx.x + gridDim.x * (FF_HB * round + (warp >> 2)); }
+    // the segment of the current stage
+    __device__ __forceinline__ int seg(const FfnParams &P) const
+    {
+        return phase == 0 ? a % P.nseg_up : b % P.nseg_dn;
+    }
 
-    __device__ __forceinline__ const uint8_t *src(const FfnParams &P, int warp) const
+    __device__ __forceinline__ const uint8_t *src(const FfnParams &P) const
     {
         if (phase == 0) {
-            const int slab = 2 * hb(warp) + (warp & 1);
-            const uint8_t *W = (warp & 2) ? P.Wu : P.Wg;
-            return W + static_cast<long long>(slab) * P.slab_up + static_cast<long long>(seg) * SEG_BYTES;
+            const int hl = a / (4 * P.nseg_up), m = (a / P.nseg_up) & 3, sg = a % P.nseg_up;
+            const int hb = blockIdx.x + gridDim.x * (FF_HB * round + hl);
+            const uint8_t *W = (m & 2) ? P.Wu : P.Wg;
+            return W + static_cast<long long>(2 * hb + (m & 1)) * P.slab_up + static_cast<long long>(sg) * SEG_BYTES;
         }
-        const int i = dn0 + k, s = i / P.nseg_dn, sg = i - s * P.nseg_dn;
-        return P.Wd + static_cast<long long>(s) * P.slab_dn + static_cast<long long>(sg) * SEG_BYTES;
+        const int si = b / P.nseg_dn, sg = b - si * P.nseg_dn;
+        return P.Wd + static_cast<long long>(blockIdx.x + gridDim.x * si) * P.slab_dn +
+               static_cast<long long>(sg) * SEG_BYTES;
     }
 
     __device__ __forceinline__ unsigned bytes(const FfnParams &P) const
     {
-        if (phase == 0) return static_cast<unsigned>(SLAB_COL_BYTES * min(SEG_BLOCKS, P.nb_up - SEG_BLOCKS * seg));
-        const int sg = (dn0 + k) % P.nseg_dn;
-        return static_cast<unsigned>(SLAB_COL_BYTES * min(SEG_BLOCKS, P.nb_dn - SEG_BLOCKS * sg));
+        const int sg = seg(P), nb = phase == 0 ? P.nb_up : P.nb_dn;
+        return static_cast<unsigned>(SLAB_COL_BYTES * min(SEG_BLOCKS, nb - SEG_BLOCKS * sg));
     }
 };
 
@@ -128,13 +143,15 @@ __global__ void __launch_bounds__(FF_THREADS, 1) ffn_fused_kernel(const __grid_c
 {
     extern __shared__ __align__(128) uint8_t smem[];
     __shared__ int s_abort;
+    __shared__ int s_go;
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     const int r8 = lane >> 2, j = lane & 3;
     using LO = LaneOut<T, false>;
     constexpr int NO = LO::N;
+    constexpr int TS = T * 16;  // floats of one stage's segment sums: [T][16 rows]
     uint64_t *bar = reinterpret_cast<uint64_t *>(smem + P.off_bar) + warp * FF_RING;
     uint8_t *ring = smem + P.off_ring + static_cast<size_t>(warp) * FF_RING * SEG_BYTES;
-    float *hbuf = reinterpret_cast<float *>(smem + P.off_hbuf);  // [FF_HB][2 (gate, up)][32 rows][T]
+    float *part = reinterpret_cast<float *>(smem + P.off_part);
     volatile int *abort_flag = &s_abort;
 
     if (tid == 0) s_abort = 0;
@@ -143,7 +160,7 @@ __global__ void __launch_bounds__(FF_THREADS, 1) ffn_fused_kernel(const __grid_c
     fence_mbar_init();
     __syncthreads();
 
-    // weights first: phase A's slabs and the down stages depend on no kernel
+    // the weights depend on no kernel: each warp's stages, in its order
     FfWalk fill, use;
     fill.init(P, warp);
     use = fill;
@@ -154,70 +171,91 @@ __global__ void __launch_bounds__(FF_THREADS, 1) ffn_fused_kernel(const __grid_c
         if (lane == 0) {
             fence_proxy_async_smem();
             mbar_arrive_expect_tx(&bar[into], fill.bytes(P));
-            bulk_g2s(ring + into * SEG_BYTES, fill.src(P, warp), fill.bytes(P), &bar[into], pol);
+            bulk_g2s(ring + into * SEG_BYTES, fill.src(P), fill.bytes(P), &bar[into], pol);
         }
         ++issued;
         fill.advance(P, warp);
     };
-    for (int d = 0; d < FF_RING && fill.phase < 2; ++d) issue(d);
-    // the next stage in this warp's order, once its copy has landed
+    // Before the dependency wait: x's lines, then every warp's first stages
+    // (its whole share of the layer in the usual shapes) are requested into
+    // L2, so HBM streams the layer while the CTA waits; the ring copies
+    // themselves start only once x is quantised, so that x's load does not
+    // queue behind a ring's worth of weight data returning to this SM.  (x
+    // may still be being written by the kernel before this one: a prefetch
+    // only moves lines into L2, which the writes update.  Only x's whole
+    // 16-byte units are prefetched, so nothing outside x is read.)
+    if (tid == 0) {
+        const uintptr_t a = reinterpret_cast<uintptr_t>(P.x);
+        const uintptr_t b = a + 4ull * T * P.d_model;
+        const uintptr_t a16 = (a + 15) & ~static_cast<uintptr_t>(15), b16 = b & ~static_cast<uintptr_t>(15);
+        if (b16 > a16) bulk_prefetch_l2(reinterpret_cast<const void *>(a16), static_cast<unsigned>(b16 - a16));
+    }
+    __syncwarp();
+    if (lane == 0) {
+        FfWalk pf = fill;
+        for (int d = 0; d < FF_RING + FF_PREFETCH && pf.phase < 2; ++d) {
+            bulk_prefetch_l2(pf.src(P), pf.bytes(P));
+            pf.advance(P, warp);
+        }
+    }
     bool ok = true;
-    auto take = [&]() -> const uint8_t * {
+    // The warp's next stage: waits for its copy, reduces it against the
+    // activation image xv into this lane's segment sums, frees the slot for
+    // the next fill, and stores the sums as part[idx][t][row].
+    auto stage = [&](const XqView &xv, int nb, bool live) {
+        const int sg = use.seg(P), idx = use.phase == 0 ? use.a : use.b;
         if (ok) {
             ok = mbar_wait_bounded(&bar[slot], phase_bit, abort_flag, P.status, WAIT_LIMIT_NS);
             waited += ok ? 1 : 0;
         }
-        return ring + slot * SEG_BYTES;
-    };
-    auto release = [&]() {
+        float Pk[NO];
+        if (ok && live)
+            segment_sum<T, false>(true, ring + slot * SEG_BYTES, nullptr, 0, sg, nb, r8, j, xv, Pk);
+        else
+#pragma unroll
+            for (int k2 = 0; k2 < NO; ++k2) Pk[k2] = 0.0f;
         __syncwarp();
         if (fill.phase < 2 && ok) issue(slot);
         if (++slot == FF_RING) {
             slot = 0;
             phase_bit ^= 1u;
         }
+        use.advance(P, warp);
+        float *pp = part + idx * TS;
+#pragma unroll
+        for (int k2 = 0; k2 < NO; ++k2)
+            if (LO::owner(k2, j)) pp[LO::tok(k2, j) * 16 + LO::row(k2, r8)] = Pk[k2];
     };
 
     // ---- phase A: x quantised in shared memory, then the h blocks
     pdl_wait();
     quantize_image<T, false>(smem, P.x, P.d_model, tid, FF_THREADS);
+    for (int d = 0; d < FF_RING && fill.phase < 2; ++d) issue(d);
     __syncthreads();
     {
         const XqLayout L = xq_layout(T, P.d_model, false);
         const XqView xv{reinterpret_cast<const int8_t *>(smem), L.xstride,
                         reinterpret_cast<const int2 *>(smem + L.off_cd), L.cdw};
         for (int rnd = 0; rnd < use.nrounds; ++rnd) {
-            if (use.phase == 0 && use.round == rnd) {
-                // this warp's slab item: all segments in order
-                float yv[NO];
-                for (int sg = 0; sg < P.nseg_up; ++sg) {
-                    float Pk[NO];
-                    const uint8_t *stg = take();
-                    if (ok)
-                        segment_sum<T, false>(true, stg, nullptr, 0, sg, P.nb_up, r8, j, xv, Pk);
-                    else
-#pragma unroll
-                        for (int k2 = 0; k2 < NO; ++k2) Pk[k2] = 0.0f;
-                    release();
-                    use.advance(P, warp);
-#pragma unroll
-                    for (int k2 = 0; k2 < NO; ++k2) yv[k2] = sg == 0 ? Pk[k2] : __fadd_rn(yv[k2], Pk[k2]);
-                }
-                // rows r8 and r8 + 8 of the slab, every token (lanes j == 0)
-                float *hb = hbuf + ((warp >> 2) * 2 + ((warp >> 1) & 1)) * 32 * T;
-#pragma unroll
-                for (int k2 = 0; k2 < NO; ++k2)
-                    if (LO::owner(k2, j)) hb[(16 * (warp & 1) + LO::row(k2, r8)) * T + LO::tok(k2, j)] = yv[k2];
-            }
+            while (use.phase == 0 && use.round == rnd) stage(xv, P.nb_up, true);
             __syncthreads();
-            // one warp per h block of the round: h = SiLU(g) * u, then Q8_0
+            // one warp per h block of the round: lane = row of the block
+            // (gate and up slab 2 hb + lane / 16, row lane % 16); each
+            // output's segment sums added in segment order, h = SiLU(g) * u,
+            // then Q8_0
             const int hbl = warp;
             if (hbl < FF_HB && FF_HB * rnd + hbl < use.nhb_cta) {
                 const int hbi = blockIdx.x + gridDim.x * (FF_HB * rnd + hbl);
-                const float *gb = hbuf + (hbl * 2) * 32 * T, *ub = gb + 32 * T;
+                const float *pg = part + (hbl * 4 + (lane >> 4)) * P.nseg_up * TS + (lane & 15);
+                const float *pu = pg + 2 * P.nseg_up * TS;
 #pragma unroll
                 for (int t = 0; t < T; ++t) {
-                    const float h = __fmul_rn(ffn_silu(gb[lane * T + t]), ub[lane * T + t]);
+                    float g = pg[t * 16], u = pu[t * 16];
+                    for (int sg = 1; sg < P.nseg_up; ++sg) {
+                        g = __fadd_rn(g, pg[sg * TS + t * 16]);
+                        u = __fadd_rn(u, pu[sg * TS + t * 16]);
+                    }
+                    const float h = __fmul_rn(ffn_silu(g), u);
                     float amax = fabsf(h);
 #pragma unroll
                     for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xFFFFFFFFu, amax, off));
@@ -229,16 +267,19 @@ __global__ void __launch_bounds__(FF_THREADS, 1) ffn_fused_kernel(const __grid_c
                         reinterpret_cast<unsigned short *>(P.hq + static_cast<long long>(T) * P.d_ff)[t * P.nhb + hbi] =
                             q8_half(d);
                 }
-                __threadfence();
-                __syncwarp();
-                if (lane == 0) atomicAdd(P.cnt, 1u);
             }
-            __syncthreads();  // hbuf is reused by the next round
+            __syncthreads();  // (the segment sums are reused by the next round)
+            // the round's h blocks are written: one fence makes the whole
+            // CTA's writes visible before they are counted
+            if (tid == 0) {
+                const int nr = min(FF_HB, use.nhb_cta - FF_HB * rnd);
+                __threadfence();
+                atomicAdd(P.cnt, static_cast<unsigned>(nr));
+            }
         }
     }
 
     // ---- every h block done (bounded wait by one thread per CTA)
-    __shared__ int s_go;
     if (tid == 0) {
         const uint64_t t0 = global_timer_ns();
         unsigned v = 0;
@@ -279,46 +320,27 @@ __global__ void __launch_bounds__(FF_THREADS, 1) ffn_fused_kernel(const __grid_c
         const XqLayout L = xq_layout(T, P.d_ff, false);
         const XqView xv{reinterpret_cast<const int8_t *>(smem), L.xstride,
                         reinterpret_cast<const int2 *>(smem + L.off_cd), L.cdw};
-        while (use.phase == 1) {
-            const int i = use.dn0 + use.k, s = i / P.nseg_dn, sg = i - s * P.nseg_dn;
-            float Pk[NO];
-            const uint8_t *stg = take();
-            if (ok && go)
-                segment_sum<T, false>(true, stg, nullptr, 0, sg, P.nb_dn, r8, j, xv, Pk);
-            else
-#pragma unroll
-                for (int k2 = 0; k2 < NO; ++k2) Pk[k2] = 0.0f;
-            release();
-            use.advance(P, warp);
-            if (!go) continue;
-            float *pb = P.part + (static_cast<long long>(s) * P.nseg_dn + sg) * T * 16;
-#pragma unroll
-            for (int k2 = 0; k2 < NO; ++k2)
-                if (LO::owner(k2, j)) pb[LO::tok(k2, j) * 16 + LO::row(k2, r8)] = Pk[k2];
-            // the last warp to finish a segment of slab s adds all of them in order
-            __threadfence();
-            __syncwarp();
-            unsigned old = 0;
-            if (lane == 0) old = atomicAdd(P.cnt + 2 + s, 1u);
-            old = __shfl_sync(0xFFFFFFFFu, old, 0);
-            if (old == static_cast<unsigned>(P.nseg_dn - 1)) {
-                __threadfence();
-                if (lane < 16) {
-                    const float *pr = P.part + static_cast<long long>(s) * P.nseg_dn * T * 16;
-                    const int row = s * 16 + lane;
-#pragma unroll
-                    for (int t = 0; t < T; ++t) {
-                        float v = ordered_sum_ldcg(pr + t * 16 + lane, P.nseg_dn, T * 16);
-                        const long long yi = static_cast<long long>(t) * P.d_model + row;
-                        if (P.res != nullptr) v = __fadd_rn(v, P.res[yi]);
-                        P.y[yi] = v;
-                    }
-                }
-                __syncwarp();
-                if (lane == 0) P.cnt[2 + s] = 0u;
-            }
-        }
+        while (use.phase == 1) stage(xv, P.nb_dn, go);
     }
+    __syncthreads();
+    // each output of the CTA's slabs: its segment sums in segment order, then the residual
+    if (go)
+        for (int i = tid; i < use.nb_cta / P.nseg_dn * TS; i += FF_THREADS) {
+            const int si = i / TS, rem = i - si * TS, t = rem >> 4, row = rem & 15;
+            const float *pp = part + si * P.nseg_dn * TS + rem;
+            float v = pp[0];
+            for (int sg = 1; sg < P.nseg_dn; sg += 8) {
+                float x8[8];
+#pragma unroll
+                for (int k = 0; k < 8; ++k) x8[k] = sg + k < P.nseg_dn ? pp[(sg + k) * TS] : 0.0f;
+#pragma unroll
+                for (int k = 0; k < 8; ++k)
+                    if (sg + k < P.nseg_dn) v = __fadd_rn(v, x8[k]);
+            }
+            const long long yi = static_cast<long long>(t) * P.d_model + (blockIdx.x + gridDim.x * si) * SLAB_ROWS + row;
+            if (P.res != nullptr) v = __fadd_rn(v, P.res[yi]);
+            P.y[yi] = v;
+        }
     // copies still in flight (only after an abort): wait for them, bounded;
     // fill i went to slot i % FF_RING, completing that slot's phase i / FF_RING
     for (int i = waited; i < issued; ++i) mbar_drain(&bar[i % FF_RING], static_cast<unsigned>((i / FF_RING) & 1));
@@ -328,26 +350,34 @@ __global__ void __launch_bounds__(FF_THREADS, 1) ffn_fused_kernel(const __grid_c
 
 bool ffn_fused_eligible(long long d_model, long long d_ff, int T)
 {
-    return T >= 1 && T <= 4 && d_model % SLAB_ROWS == 0 && d_ff % QK == 0 && d_model >= SLAB_ROWS && d_ff >= QK &&
-           2 + d_model / SLAB_ROWS <= FF_CNT_WORDS;
+    return T >= 1 && T <= 4 && d_model % SLAB_ROWS == 0 && d_ff % QK == 0 && d_model >= SLAB_ROWS && d_ff >= QK;
 }
 
 // Shared memory: the activation area (x's image in phase A, h's in phase
-// B), the h buffer, barriers, rings.
-static long long ffn_smem(long long d_model, long long d_ff, int T, int &off_hbuf, int &off_bar, int &off_ring)
+// B), the segment sums (a round's phase-A stages, or the CTA's down
+// stages), barriers, rings.
+static long long ffn_smem(long long d_model, long long d_ff, int T, int grid, int &off_part, int &off_bar,
+                          int &off_ring)
 {
     const long long xa = std::max(xq_layout(T, static_cast<int>(d_model), false).bytes,
                                   xq_layout(T, static_cast<int>(d_ff), false).bytes);
-    off_hbuf = static_cast<int>((xa + 127) / 128 * 128);
-    off_bar = off_hbuf + (FF_HB * 2 * 32 * T * 4 + 127) / 128 * 128;
+    const long long nb_up = d_model / QK, nb_dn = d_ff / QK;
+    const long long nseg_up = (nb_up + SEG_BLOCKS - 1) / SEG_BLOCKS, nseg_dn = (nb_dn + SEG_BLOCKS - 1) / SEG_BLOCKS;
+    const long long nhb = d_ff / QK, nslab = d_model / SLAB_ROWS;
+    const long long hb_round = std::min<long long>(FF_HB, (nhb + grid - 1) / grid);
+    const long long slabs_cta = (nslab + grid - 1) / grid;
+    const long long sums = std::max(hb_round * 4 * nseg_up, slabs_cta * nseg_dn) * T * 16 * 4;
+    off_part = static_cast<int>((xa + 127) / 128 * 128);
+    off_bar = off_part + static_cast<int>((sums + 127) / 128 * 128);
     off_ring = off_bar + (FF_WARPS * FF_RING * 8 + 127) / 128 * 128;
     return off_ring + static_cast<long long>(FF_WARPS) * FF_RING * SEG_BYTES;
 }
 
-bool ffn_fused_fits(long long d_model, long long d_ff, int T, int smem_budget)
+bool ffn_fused_fits(long long d_model, long long d_ff, int T, int grid, int smem_budget)
 {
+    if (!ffn_fused_eligible(d_model, d_ff, T) || grid < 1) return false;
     int a, b, c;
-    return ffn_fused_eligible(d_model, d_ff, T) && ffn_smem(d_model, d_ff, T, a, b, c) <= smem_budget;
+    return ffn_smem(d_model, d_ff, T, grid, a, b, c) <= smem_budget;
 }
 
 template <int T>
@@ -394,10 +424,10 @@ static cudaError_t launch_ffn_t(const FfnParams &P, int grid, size_t smem, cudaS
 }
 
 cudaError_t launch_ffn_fused(const void *Wg, const void *Wu, const void *Wd, const float *x, const float *res,
-                             float *y, long long d_model, long long d_ff, int T, uint8_t *hq, float *part,
-                             unsigned *cnt, int grid, int smem_budget, unsigned *status, cudaStream_t st)
+                             float *y, long long d_model, long long d_ff, int T, uint8_t *hq, unsigned *cnt, int grid,
+                             int smem_budget, unsigned *status, cudaStream_t st)
 {
-    if (!ffn_fused_eligible(d_model, d_ff, T)) return cudaErrorInvalidValue;
+    if (!ffn_fused_eligible(d_model, d_ff, T) || grid < 1) return cudaErrorInvalidValue;
     FfnParams P;
     memset(&P, 0, sizeof(P));
     P.Wg = static_cast<const uint8_t *>(Wg);
@@ -407,7 +437,6 @@ cudaError_t launch_ffn_fused(const void *Wg, const void *Wu, const void *Wd, con
     P.res = res;
     P.y = y;
     P.hq = hq;
-    P.part = part;
     P.cnt = cnt;
     P.status = status;
     P.d_model = static_cast<int>(d_model);
@@ -420,8 +449,7 @@ cudaError_t launch_ffn_fused(const void *Wg, const void *Wu, const void *Wd, con
     P.slab_up = static_cast<long long>(SLAB_COL_BYTES) * P.nb_up;
     P.slab_dn = static_cast<long long>(SLAB_COL_BYTES) * P.nb_dn;
     P.nhb = P.d_ff / QK;
-    P.ndn = P.nslab_dn * P.nseg_dn;
-    const long long smem = ffn_smem(d_model, d_ff, T, P.off_hbuf, P.off_bar, P.off_ring);
+    const long long smem = ffn_smem(d_model, d_ff, T, grid, P.off_part, P.off_bar, P.off_ring);
     if (smem > smem_budget) return cudaErrorInvalidValue;
     switch (T) {
     case 1: return launch_ffn_t<1>(P, grid, static_cast<size_t>(smem), st);

@@ -897,20 +897,17 @@ static qgemv_status ffn_chain(const void *W_gate, const void *W_up, const void *
         if (residual != y && (overlap(rr, ry) || overlap(rr, rw))) return QGEMV_ERR_INVALID_ARG;
     }
     uint8_t *w = static_cast<uint8_t *>(ws);
-    // one fused launch: h's codes where the chain keeps them, the down
-    // projection's segment sums in the down call's data area, counters in
+    // one fused launch: h's codes where the chain keeps them, counters in
     // the workspace's zeroed counter area
     if (layout == QGEMV_W_PACKED && g_ffn_fused.load(std::memory_order_relaxed)) {
         DevInfo dev;
         qgemv_status ds = device_info(dev);
         if (ds != QGEMV_OK) return ds;
-        const long long nseg_dn = (d_ff / QK + SEG_BLOCKS - 1) / SEG_BLOCKS;
-        const long long part_bytes = (d_model / SLAB_ROWS) * nseg_dn * T * 16 * 4;
-        if (ffn_fused_fits(d_model, d_ff, T, dev.smem_optin - 2048) && off[4] + CNT_AREA + part_bytes <= need) {
+        if (ffn_fused_fits(d_model, d_ff, T, dev.sms, dev.smem_optin - 2048)) {
             const cudaError_t e =
                 launch_ffn_fused(W_gate, W_up, W_down, x, residual, y, d_model, d_ff, T, w + off[3],
-                                 reinterpret_cast<float *>(w + off[4] + CNT_AREA), reinterpret_cast<unsigned *>(w),
-                                 dev.sms, dev.smem_optin - 2048, dev.status, reinterpret_cast<cudaStream_t>(stream));
+                                 reinterpret_cast<unsigned *>(w), dev.sms, dev.smem_optin - 2048, dev.status,
+                                 reinterpret_cast<cudaStream_t>(stream));
             return e == cudaSuccess ? QGEMV_OK : QGEMV_ERR_CUDA;
         }
     }

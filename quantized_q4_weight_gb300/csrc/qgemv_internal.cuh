@@ -372,17 +372,18 @@ __device__ __forceinline__ float ffn_exp(float x)
 __device__ __forceinline__ float ffn_silu(float g) { return __fdiv_rn(g, __fadd_rn(1.0f, ffn_exp(-g))); }
 
 // p[0] + p[stride] + ... + p[(n - 1) stride], added in index order from
-// p[0] (the fixed order of a split sum), loaded from L2 eight at a time so
-// that the loads' latencies overlap instead of adding up.
+// p[0] (the fixed order of a split sum), loaded from L2 B at a time so that
+// the loads' latencies overlap instead of adding up.
+template <int B = 8>
 __device__ __forceinline__ float ordered_sum_ldcg(const float *p, int n, long long stride)
 {
     float v = __ldcg(p);
-    for (int i = 1; i < n; i += 8) {
-        float x[8];
+    for (int i = 1; i < n; i += B) {
+        float x[B];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) x[k] = i + k < n ? __ldcg(p + (i + k) * stride) : 0.0f;
+        for (int k = 0; k < B; ++k) x[k] = i + k < n ? __ldcg(p + (i + k) * stride) : 0.0f;
 #pragma unroll
-        for (int k = 0; k < 8; ++k)
+        for (int k = 0; k < B; ++k)
             if (i + k < n) v = __fadd_rn(v, x[k]);
     }
     return v;

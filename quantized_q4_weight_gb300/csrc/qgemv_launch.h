@@ -68,14 +68,14 @@ cudaError_t launch_quantize_list(const float *const *x, uint8_t *const *xq, cons
                                  cudaStream_t st);
 
 // The decode FFN step in one cooperative launch (ffn_fused.cu), T <= 4,
-// packed weights, d_model % 16 == 0, d_ff % 32 == 0.  cnt: zeroed counters
-// (left zero): 2 + d_model / 16 words; hq: T * d_ff + 2 * T * d_ff / 32
-// bytes; part: (d_model / 16) * ceil(d_ff / 512) * T * 16 floats.
+// packed weights, d_model % 16 == 0, d_ff % 32 == 0, one CTA per SM of a
+// grid of `grid` CTAs.  cnt: two zeroed counters (left zero); hq: T * d_ff +
+// 2 * T * d_ff / 32 bytes.
 bool ffn_fused_eligible(long long d_model, long long d_ff, int T);
-bool ffn_fused_fits(long long d_model, long long d_ff, int T, int smem_budget);
+bool ffn_fused_fits(long long d_model, long long d_ff, int T, int grid, int smem_budget);
 cudaError_t launch_ffn_fused(const void *Wg, const void *Wu, const void *Wd, const float *x, const float *res,
-                             float *y, long long d_model, long long d_ff, int T, uint8_t *hq, float *part,
-                             unsigned *cnt, int grid, int smem_budget, unsigned *status, cudaStream_t st);
+                             float *y, long long d_model, long long d_ff, int T, uint8_t *hq, unsigned *cnt, int grid,
+                             int smem_budget, unsigned *status, cudaStream_t st);
 
 // The streaming GEMV kernel, one instantiation per (T, parameter-block size,
 // argmax, tensor-core path).  Defined in gemv_t<T>.cu.
