@@ -240,9 +240,10 @@ def build_verify(T, seed, dev, copies=4, keep_host=False, N=151936, K=1536):
 
 
 def build_ffn(T, seed, dev, layers=28, d_model=1536, d_ff=8960, keep_host=False):
-    """The decode FFN of every layer: per layer one qgemv_q4_0_ffn call (gate
-    and up in one launch on the same fp32 x, the SiLU * up quantiser, down),
-    each layer with its own seeded weights and x."""
+    """The decode FFN of every layer: per layer one qgemv_q4_0_ffn call (one
+    fused launch for T <= 4; otherwise gate and up in one launch on the same
+    fp32 x, the SiLU * up quantiser, down), each layer with its own seeded
+    weights and x."""
     import torch
     q = _q()
     wl = Workload("qwen2.5-1.5b_ffn", T)
@@ -258,7 +259,8 @@ def build_ffn(T, seed, dev, layers=28, d_model=1536, d_ff=8960, keep_host=False)
     wl.x_bytes = 4 * T * d_model * layers
     wl.y_bytes = 4 * T * d_model * layers
     wl.xq_bytes = (2 * q.xq_bytes(T, d_model) + q.xq_bytes(T, d_ff)) * layers
-    wl.n_gemv, wl.launches = 3 * layers, 3 * layers
+    fused = T <= 4  # one fused launch per layer; else gate/up, the SiLU step and down
+    wl.n_gemv, wl.launches = 3 * layers, (1 if fused else 3) * layers
 
     def step(stream=None):
         for l in range(layers):
@@ -267,11 +269,13 @@ def build_ffn(T, seed, dev, layers=28, d_model=1536, d_ff=8960, keep_host=False)
 
     wl.step, wl.kernel, wl.dominant = step, step, step
     wl.dominant_bytes = wl.w_bytes + wl.x_bytes + wl.y_bytes
-    wl.other_launch = ("the whole step: per layer the gate/up and down streaming launches and the SiLU * up "
-                       "quantiser, whose bytes are 0.2 % of the step's")
+    wl.other_launch = ("the whole step: per layer one fused launch (T <= 4), else the gate/up and down "
+                       "streaming launches and the SiLU * up quantiser")
     wl.inputs, wl.outputs = list(wl.xs), list(wl.ys)
     wl.config = {"workload": "qwen2.5-1.5b_ffn", "layers": layers, "d_model": d_model, "d_ff": d_ff, "T": T,
-                 "weight_bytes": wl.w_bytes, "step": "per layer: gate+up launch, SiLU(gate)*up to Q8_0, down launch",
+                 "weight_bytes": wl.w_bytes, "step": ("per layer one qgemv_q4_0_ffn call: " +
+                          ("one fused launch (gate+up, SiLU(gate)*up to Q8_0, down)" if fused else
+                           "gate+up launch, SiLU(gate)*up to Q8_0, down launch")),
                  "l2_defeat": "weights larger than the 126 MB L2, each streamed once per step"}
     return wl
 
@@ -321,8 +325,9 @@ def build_q8(T, seed, dev, copies=2, keep_host=False, N=151936, K=1536):
 def build_gs64(T, seed, dev, copies=4, keep_host=False, N=151936, K=1536):
     """A dense matrix of the lm_head's shape in the gs64 grouped int4 format
     (colibri qwen36 docs: the dense trunk stored as int4 in groups of 64 with
-    one scale each): one step quantises x once per vector to int8 and runs
-    the gs64 GEMV (two launches); copies rotate so reads hit HBM."""
+    one scale each): one step is one launch of the gs64 GEMV on fp32 x,
+    quantised once per vector to int8 inside the launch; copies rotate so
+    reads hit HBM."""
     import torch
     q = _q()
     wl = Workload("gs64_lm_head", T)
@@ -339,21 +344,19 @@ def build_gs64(T, seed, dev, copies=4, keep_host=False, N=151936, K=1536):
     wl.ws = q.new_workspace(q.gs64_workspace_bytes(N, K, T), dev)
     wl.w_bytes = q.gs64_bytes(N, K)
     wl.x_bytes, wl.y_bytes, wl.xq_bytes = 4 * T * K, 4 * T * N, T * K + 4 * T
-    wl.n_gemv, wl.launches = 1, 2
+    wl.n_gemv, wl.launches = 1, 1
     wl.copy = 0
 
-    def kernel(stream=None):
+    def kernel(stream=None):  # on pre-quantised activations
         q.gemv_gs64(wl.W[wl.copy], wl.qx, wl.sx, N, K, T, wl.ws, y=wl.y, stream=stream)
         wl.copy = (wl.copy + 1) % copies
 
-    def step(stream=None):
-        q.quantize_vec_i8_into(wl.x, wl.qx, wl.sx, T, K, stream=stream)
-        kernel(stream)
+    def step(stream=None):  # fp32 x, quantised inside the one GEMV launch
+        q.gemv_gs64_f32(wl.W[wl.copy], wl.x, N, K, T, wl.ws, y=wl.y, stream=stream)
+        wl.copy = (wl.copy + 1) % copies
 
-    wl.step, wl.kernel, wl.dominant = step, kernel, kernel
+    wl.step, wl.kernel = step, kernel
     wl.rotation = copies
-    wl.dominant_bytes = wl.w_bytes + wl.xq_bytes + wl.y_bytes
-    wl.other_launch = "the step's other launch is the per-vector int8 quantiser"
     wl.kernel_name = "gs64_gemv_kernel"
     wl.dtype = "uint4 x int8 -> int32 group sums, fp32 accumulation"
     wl.data = ("synthetic (seeded; gs64 nibbles uniform, fp32 group scales U[1e-3,4e-3], "
@@ -361,7 +364,7 @@ def build_gs64(T, seed, dev, copies=4, keep_host=False, N=151936, K=1536):
     wl.inputs, wl.outputs = [wl.x], [wl.y]
     wl.config = {"workload": "gs64_lm_head", "N": N, "K": K, "T": T, "copies": copies,
                  "weights": "gs64 (64-weight groups, fp32 scale)",
-                 "step": "per-vector int8 quantiser launch, then the gs64 GEMV launch",
+                 "step": "one gs64 GEMV launch on fp32 x (per-vector int8 quantisation inside it)",
                  "l2_defeat": f"{copies} weight copies in rotation ({copies * wl.w_bytes / 1e6:.0f} MB)"}
     return wl
 
@@ -998,9 +1001,15 @@ def measure_workloads(dev, head_wl):
     recs.append(workload_record(torch, dev, stream, wl, "MoE top-8 + shared expert, T=1, 4 expert sets", peak))
     del wl
     torch.cuda.empty_cache()
+    wl = build_workload("qwen2.5-1.5b_ffn", dev)
+    recs.append(workload_record(torch, dev, stream, wl,
+                                "decode FFN of 28 Qwen2.5-1.5B layers (one fused launch each), T=1", peak))
+    del wl
+    torch.cuda.empty_cache()
     wl = build_workload("gs64_lm_head", dev)
     recs.append(workload_record(torch, dev, stream, wl,
-                                "gs64 grouped int4, 151936 x 1536, per-vector int8 x, T=1, 4 copies", peak))
+                                "gs64 grouped int4, 151936 x 1536, fp32 x quantised per vector in the launch, "
+                                "T=1, 4 copies", peak))
     del wl
     torch.cuda.empty_cache()
     clk = clocks.stop()

@@ -306,6 +306,14 @@ size_t qgemv_gs64_workspace_bytes(int64_t N, int64_t K, int T);
 qgemv_status qgemv_gs64(const void *W, const int8_t *q, const float *s, float *y, int64_t N, int64_t K, int T,
                         void *ws, size_t ws_bytes, qgemv_stream_t stream);
 
+/* The same GEMV on fp32 activations x [T][K] (4-byte aligned), quantised
+ * inside the launch with qgemv_quantize_vec_i8's steps (each CTA forms the
+ * row maxima and the codes itself): y is bit-identical to
+ * qgemv_quantize_vec_i8 followed by qgemv_gs64, in one launch.  Workspace,
+ * limits and errors as qgemv_gs64; y must not overlap W, x or ws. */
+qgemv_status qgemv_gs64_f32(const void *W, const float *x, float *y, int64_t N, int64_t K, int T, void *ws,
+                            size_t ws_bytes, qgemv_stream_t stream);
+
 /* ---- The FFN of a decode step (minfer README M15: the whole layer runs
  * around its GEMVs; colibri qwen36 docs: gate and up share one pass over the
  * activation):  y = W_down . Q8_0(SiLU(W_gate . x) * (W_up . x)).

@@ -107,6 +107,7 @@ _SIGS = {
     "qgemv_quantize_vec_i8": ([_VP, _VP, _VP, _I32, _I64, _VP], _I32),
     "qgemv_gs64_workspace_bytes": ([_I64, _I64, _I32], _SZ),
     "qgemv_gs64": ([_VP, _VP, _VP, _VP, _I64, _I64, _I32, _VP, _SZ, _VP], _I32),
+    "qgemv_gs64_f32": ([_VP, _VP, _VP, _I64, _I64, _I32, _VP, _SZ, _VP], _I32),
     "qgemv_debug_block_isums": ([_VP, _I32, _VP, _VP, _I64, _I64, _I32, _VP], _I32),
     "qgemv_debug_block_isums_tc": ([_VP, _I32, _VP, _VP, _I64, _I64, _I32, _I32, _VP], _I32),
     "qgemv_debug_stream_read": ([_VP, _SZ, _I32, _I32, _I32, _I32, _VP, _VP], _I32),
@@ -480,6 +481,15 @@ def gemv_gs64(W, q, s, N: int, K: int, T: int, ws=None, y=None, stream=None) -> 
         y = torch.empty((T, N), dtype=torch.float32, device=W.device)
     _check(lib().qgemv_gs64(_ptr(W), _ptr(q), _ptr(s), _ptr(y), N, K, T, _ptr(ws) if ws is not None else None,
                             ws.numel() if ws is not None else 0, _stream(stream)), "qgemv_gs64")
+    return y
+
+
+def gemv_gs64_f32(W, x, N: int, K: int, T: int, ws=None, y=None, stream=None) -> torch.Tensor:
+    """gs64 GEMV on fp32 activations, quantised per vector inside the launch."""
+    if y is None:
+        y = torch.empty((T, N), dtype=torch.float32, device=W.device)
+    _check(lib().qgemv_gs64_f32(_ptr(W), _ptr(x), _ptr(y), N, K, T, _ptr(ws) if ws is not None else None,
+                                ws.numel() if ws is not None else 0, _stream(stream)), "qgemv_gs64_f32")
     return y
 
 

@@ -161,6 +161,7 @@ struct G64Params {
     const uint8_t *W;   // packed weights
     const int8_t *q;    // activation codes [T][K]
     const float *sx;    // activation scales [T]
+    const float *xf;    // or fp32 activations [T][K], quantised in the kernel (q, sx unused)
     float *y;           // [T][N]
     float *part;        // [nslabs][nstage][T][16] stage sums of slabs split over warps
     unsigned *cnt;      // [nslabs] arrival counters (left at zero)
@@ -251,6 +252,54 @@ __device__ __forceinline__ uint4 ldg_u4_a4(const uint8_t *p)
     return make_uint4(__ldg(w), __ldg(w + 1), __ldg(w + 2), __ldg(w + 3));
 }
 
+// The activation rows x[T][K] (fp32) quantised by this CTA into the code
+// image [T][K] and s_sx[T]: the steps of quantize_vec_i8_kernel (s =
+// amax / 127 over the row, 1/s from it, codes round-half-away(x * (1/s))).
+// The maximum is exact in any order, so codes and scales equal that
+// kernel's.  K % 64 == 0.
+template <int T>
+__device__ __forceinline__ void g64_quantize_rows(const float *x, int K, uint8_t *img, float *s_sx, int tid,
+                                                  int nthreads)
+{
+    __shared__ float s_red[T][NWARPS_MAX];
+    __shared__ float s_id[T];
+    const int warp = tid >> 5, lane = tid & 31, nw = nthreads >> 5;
+    const bool vec = (reinterpret_cast<uintptr_t>(x) & 15) == 0;
+    auto load4 = [&](long long i) -> float4 {
+        if (vec) return __ldcg(reinterpret_cast<const float4 *>(x + i));
+        return make_float4(__ldcg(x + i), __ldcg(x + i + 1), __ldcg(x + i + 2), __ldcg(x + i + 3));
+    };
+#pragma unroll
+    for (int t = 0; t < T; ++t) {
+        float m = 0.0f;
+        for (int k = 4 * tid; k < K; k += 4 * nthreads) {
+            const float4 v = load4(static_cast<long long>(t) * K + k);
+            m = fmaxf(m, fmaxf(fmaxf(fabsf(v.x), fabsf(v.y)), fmaxf(fabsf(v.z), fabsf(v.w))));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xFFFFFFFFu, m, o));
+        if (lane == 0) s_red[t][warp] = m;
+    }
+    __syncthreads();
+    if (tid < T) {
+        float m = 0.0f;
+        for (int w = 0; w < nw; ++w) m = fmaxf(m, s_red[tid][w]);
+        float d, id;
+        q8_scale(m, d, id);
+        s_sx[tid] = d;
+        s_id[tid] = id;
+    }
+    __syncthreads();
+    for (int i = 4 * tid; i < T * K; i += 4 * nthreads) {
+        const float id = s_id[i / K];
+        const float4 v = load4(i);
+        *reinterpret_cast<unsigned *>(img + i) =
+            (static_cast<unsigned>(q8_code(v.x, id)) & 0xFFu) | ((static_cast<unsigned>(q8_code(v.y, id)) & 0xFFu) << 8) |
+            ((static_cast<unsigned>(q8_code(v.z, id)) & 0xFFu) << 16) |
+            ((static_cast<unsigned>(q8_code(v.w, id)) & 0xFFu) << 24);
+    }
+}
+
 // y = (total / 16) * s_x: the output of one row and token.
 __device__ __forceinline__ float g64_output(float total, float sx) { return __fmul_rn(__fmul_rn(total, 0.0625f), sx); }
 
@@ -319,7 +368,9 @@ __global__ void __launch_bounds__(NWARPS_MAX * 32, 1) gs64_gemv_kernel(const __g
     // activations after the preceding kernel: the codes as given, then per
     // token and group the folded constant MAGIC - 128 sum(q)
     pdl_wait();
-    {
+    if (P.xf != nullptr) {
+        g64_quantize_rows<T>(P.xf, P.K, smem, s_sx, tid, nthreads);
+    } else {
         const uint4 *src = reinterpret_cast<const uint4 *>(P.q);
         uint4 *dst = reinterpret_cast<uint4 *>(smem);
         for (int i = tid; i < T * P.K / 16; i += nthreads) dst[i] = __ldcg(src + i);
@@ -483,14 +534,15 @@ cudaError_t launch_gs64_t(const G64Params &P, int grid, size_t smem, cudaStream_
     return cudaLaunchKernelEx(&cfg, kern, P);
 }
 
-cudaError_t launch_gs64(const void *W, const int8_t *q, const float *sx, float *y, long long N, long long K, int T,
-                        void *ws, long long ws_bytes, bool do_launch, int sms, int smem_budget, unsigned *status,
-                        cudaStream_t st, long long *ws_need, int *unsupported)
+cudaError_t launch_gs64(const void *W, const int8_t *q, const float *sx, const float *xf, float *y, long long N,
+                        long long K, int T, void *ws, long long ws_bytes, bool do_launch, int sms, int smem_budget,
+                        unsigned *status, cudaStream_t st, long long *ws_need, int *unsupported)
 {
     G64Params P = {};
     P.W = static_cast<const uint8_t *>(W);
     P.q = q;
     P.sx = sx;
+    P.xf = xf;
     P.y = y;
     P.status = status;
     P.N = N;

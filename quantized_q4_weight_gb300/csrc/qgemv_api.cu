@@ -789,8 +789,8 @@ size_t qgemv_gs64_workspace_bytes(int64_t N, int64_t K, int T)
     }
     long long need = 0;
     int uns = 0;
-    launch_gs64(nullptr, nullptr, nullptr, nullptr, N, K, T, nullptr, 0, false, sms, budget, nullptr, nullptr, &need,
-                &uns);
+    launch_gs64(nullptr, nullptr, nullptr, nullptr, nullptr, N, K, T, nullptr, 0, false, sms, budget, nullptr, nullptr,
+                &need, &uns);
     return static_cast<size_t>(need);
 }
 
@@ -809,9 +809,30 @@ qgemv_status qgemv_gs64(const void *W, const int8_t *q, const float *s, float *y
     if (st != QGEMV_OK) return st;
     long long need = 0;
     int uns = 0;
-    const cudaError_t e = launch_gs64(W, q, s, y, N, K, T, ws, static_cast<long long>(ws_bytes), true, dev.sms,
-                                      dev.smem_optin - 2048, dev.status, reinterpret_cast<cudaStream_t>(stream),
-                                      &need, &uns);
+    const cudaError_t e = launch_gs64(W, q, s, nullptr, y, N, K, T, ws, static_cast<long long>(ws_bytes), true,
+                                      dev.sms, dev.smem_optin - 2048, dev.status,
+                                      reinterpret_cast<cudaStream_t>(stream), &need, &uns);
+    if (uns) return uns == 1 ? QGEMV_ERR_UNSUPPORTED : QGEMV_ERR_WORKSPACE;
+    return e == cudaSuccess ? QGEMV_OK : QGEMV_ERR_CUDA;
+}
+
+qgemv_status qgemv_gs64_f32(const void *W, const float *x, float *y, int64_t N, int64_t K, int T, void *ws,
+                            size_t ws_bytes, qgemv_stream_t stream)
+{
+    if (!gs64_shape_ok(N, K) || T < 1 || T > 8 || !W || !x || !y) return QGEMV_ERR_INVALID_ARG;
+    if (!aligned(W, 16) || !aligned(x, 4) || !aligned(y, 4) || (ws && !aligned(ws, 256))) return QGEMV_ERR_MISALIGNED;
+    const Range ry = range(y, 4ll * T * N);
+    if (overlap(ry, range(W, 36ll * N * (K / 64))) || overlap(ry, range(x, 4ll * T * K)) ||
+        (ws && overlap(ry, range(ws, static_cast<long long>(ws_bytes)))))
+        return QGEMV_ERR_INVALID_ARG;
+    DevInfo dev;
+    qgemv_status st = device_info(dev);
+    if (st != QGEMV_OK) return st;
+    long long need = 0;
+    int uns = 0;
+    const cudaError_t e = launch_gs64(W, nullptr, nullptr, x, y, N, K, T, ws, static_cast<long long>(ws_bytes), true,
+                                      dev.sms, dev.smem_optin - 2048, dev.status,
+                                      reinterpret_cast<cudaStream_t>(stream), &need, &uns);
     if (uns) return uns == 1 ? QGEMV_ERR_UNSUPPORTED : QGEMV_ERR_WORKSPACE;
     return e == cudaSuccess ? QGEMV_OK : QGEMV_ERR_CUDA;
 }

@@ -38,9 +38,9 @@ cudaError_t launch_q8(const void *W, const void *xq, float *y, long long N, long
 cudaError_t launch_gs64_pack(void *wq, float *wsc, void *packed, long long N, long long K, bool to_packed,
                              cudaStream_t st);
 cudaError_t launch_quantize_vec_i8(const float *x, int8_t *q, float *s, int R, long long K, cudaStream_t st);
-cudaError_t launch_gs64(const void *W, const int8_t *q, const float *sx, float *y, long long N, long long K, int T,
-                        void *ws, long long ws_bytes, bool do_launch, int sms, int smem_budget, unsigned *status,
-                        cudaStream_t st, long long *ws_need, int *unsupported);
+cudaError_t launch_gs64(const void *W, const int8_t *q, const float *sx, const float *xf, float *y, long long N,
+                        long long K, int T, void *ws, long long ws_bytes, bool do_launch, int sms, int smem_budget,
+                        unsigned *status, cudaStream_t st, long long *ws_need, int *unsupported);
 cudaError_t launch_silu_mul_q8(const float *g, const float *u, void *hq, int T, long long F, bool pdl, cudaStream_t st);
 // Requantisation to GGML Q4_0 blocks (kernels_misc.cu): nblocks blocks of
 // fp32 [32] (from_q8 false) or GGML Q8_0 (from_q8 true) into 18-byte blocks.

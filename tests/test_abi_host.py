@@ -232,3 +232,11 @@ def test_gs64_calls_reject_bad_arguments(L):
     assert L.qgemv_quantize_vec_i8(W, qa, sa, 0, 64, s) == 1
     assert L.qgemv_quantize_vec_i8(W, W + 16, sa, 1, 64, s) == 1             # codes over x
     assert L.qgemv_quantize_vec_i8(W + 2, qa, sa, 1, 64, s) == 2
+    xa = FAKE + (1 << 31)
+    assert L.qgemv_gs64_f32(W, xa, y, 64, 96, 1, None, 0, s) == 1             # K % 64 != 0
+    assert L.qgemv_gs64_f32(W, xa, y, 64, 128, 0, None, 0, s) == 1            # T out of range
+    assert L.qgemv_gs64_f32(W, None, y, 64, 128, 1, None, 0, s) == 1          # no x
+    assert L.qgemv_gs64_f32(W, xa + 2, y, 64, 128, 1, None, 0, s) == 2        # x: 4 bytes
+    assert L.qgemv_gs64_f32(W + 8, xa, y, 64, 128, 1, None, 0, s) == 2        # packed weights: 16 bytes
+    assert L.qgemv_gs64_f32(W, xa, xa + 64, 64, 128, 1, None, 0, s) == 1      # y over x
+    assert L.qgemv_gs64_f32(W, xa, W + 64, 64, 128, 1, None, 0, s) == 1       # y over the weights

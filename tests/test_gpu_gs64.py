@@ -134,6 +134,52 @@ def test_gs64_bit_identical_across_T(orc, N, K):
         assert torch.equal(y1[0].view(torch.int32), y8[t].view(torch.int32)), t
 
 
+@pytest.mark.parametrize("N,K", [(512, 2048), (2048, 512), (17, 576), (33, 11008), (4099, 1536), (1, 64)])
+@pytest.mark.parametrize("T", [1, 3, 8])
+@pytest.mark.parametrize("shift", [0, 1])
+def test_gs64_f32_matches_two_launches(orc, N, K, T, shift):
+    """fp32 activations quantised inside the GEMV launch: y bit-identical to
+    the quantiser launch followed by the GEMV, and within the bound of the
+    oracle; shift = 1 puts x at a 4-byte (not 16-byte) boundary."""
+    wq, ws, W = packed(13 * N + K, N, K)
+    x = synth.activations(17 * N + K + T, T, K)
+    x[T - 1, K // 3] = -55.0                            # an extreme inside the last row
+    buf = torch.zeros(T * K + 4, dtype=torch.float32, device=DEV)
+    xd = buf[shift:shift + T * K].view(T, K)
+    xd.copy_(torch.from_numpy(x))
+    wsp = q.new_workspace(q.gs64_workspace_bytes(N, K, T))
+    qd, sd = q.quantize_vec_i8(xd, T, K)
+    y2 = q.gemv_gs64(W, qd, sd, N, K, T, wsp)
+    y1 = q.gemv_gs64_f32(W, xd, N, K, T, wsp)
+    y1b = q.gemv_gs64_f32(W, xd, N, K, T, wsp)          # the workspace left reusable
+    torch.cuda.synchronize()
+    assert q.device_status() == 0
+    assert torch.equal(y1.view(torch.int32), y2.view(torch.int32))
+    assert torch.equal(y1b.view(torch.int32), y2.view(torch.int32))
+    qr, sr = orc.quantize_vec_i8(x)
+    y64, S = orc.gemv_gs64(wq, ws, N, K, qr, sr)
+    check_close(y1.cpu().numpy(), y64, S, f"gs64 f32 N={N} K={K} T={T}")
+
+
+def test_gs64_f32_edge_rows(orc):
+    # a zero row (s = 0, all codes 0), a tiny one, exact halves, a huge value
+    N, K = 40, 256
+    wq, ws, W = packed(99, N, K)
+    x = np.zeros((4, K), np.float32)
+    x[1] = 1e-30
+    x[2, :5] = [127.0, 2.5, -2.5, 0.5, -0.5]
+    x[3, 7] = 3.0e38
+    xd = torch.from_numpy(x).to(DEV)
+    qd, sd = q.quantize_vec_i8(xd, 4, K)
+    y2 = q.gemv_gs64(W, qd, sd, N, K, 4)
+    y1 = q.gemv_gs64_f32(W, xd, N, K, 4)
+    torch.cuda.synchronize()
+    assert torch.equal(y1.view(torch.int32), y2.view(torch.int32))
+    assert not y1[0].any()
+    y64, S = orc.gemv_gs64(wq, ws, N, K, *orc.quantize_vec_i8(x))
+    check_close(y1.cpu().numpy(), y64, S, "gs64 f32 edge rows")
+
+
 def test_gs64_closed_forms(orc):
     # every nibble c, every scale s, every code q = 127 (x constant, s_x = x / 127):
     # y = s_x * (K / 64) * s * 64 * (c - 8) * 127, exact here
@@ -162,4 +208,7 @@ def test_gs64_errors():
         big = 1 << 19                                      # codes beyond shared memory
         q.gemv_gs64(torch.zeros(q.gs64_bytes(16, big), dtype=torch.uint8, device=DEV),
                     torch.zeros((8, big), dtype=torch.int8, device=DEV), torch.zeros(8, device=DEV), 16, big, 8)
+    buf = torch.zeros(T * N + T * K, dtype=torch.float32, device=DEV)
+    with pytest.raises(q.QgemvError, match="INVALID_ARG"):         # y over x
+        q.gemv_gs64_f32(W, buf[:T * K].view(T, K), N, K, T, y=buf[8:8 + T * N].view(T, N))
     assert q.device_status() == 0
