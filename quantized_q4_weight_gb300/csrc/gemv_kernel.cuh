@@ -1429,18 +1429,22 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
         }
     }
     __syncthreads();
-    // Warm-up: warp 0 asks L2 for the first bytes of this CTA's weights (in
-    // its first group, packed slabs only) in 16 KB pieces, so that HBM works
-    // while the prologue and the activations are prepared and the first
-    // stage copies find their bytes in L2.  Bounded by the group's slabs.
-    if (warp == 0 && !H.ggml) {
+    // Warm-up: the warps ask L2 for the first bytes of this CTA's weights (in
+    // its first group, packed slabs only) in 16 KB pieces, one piece per
+    // warp in turn (so that no warp, thread 0's least, waits on many
+    // prefetch issues before the run table), so that HBM works while the
+    // prologue and the activations are prepared and the first stage copies
+    // find their bytes in L2.  Bounded by the group's slabs.
+    if (lane == 0 && !H.ggml) {
         const Group &g = gcache[0];
         const long long li0 = s_i0 - g.item_begin;
         const long long li1 = gn == g0 ? s_i1 - g.item_begin : static_cast<long long>(g.items_per_inst) * g.count;
         if (g.split == 1 && g.count == 1 && li0 < g.nslabs && li1 > li0) {
             const long long lo = li0 * g.slab_bytes, hi = (li1 < g.nslabs ? li1 : g.nslabs) * g.slab_bytes;
             const long long end = hi - lo > WARM_L2_BYTES ? lo + WARM_L2_BYTES : hi;
-            for (long long c = lo + static_cast<long long>(lane) * WARM_L2_PIECE; c < end; c += 32ll * WARM_L2_PIECE)
+            const int nwp = static_cast<int>(blockDim.x >> 5);
+            for (long long c = lo + static_cast<long long>(nwp - 1 - warp) * WARM_L2_PIECE; c < end;
+                 c += static_cast<long long>(nwp) * WARM_L2_PIECE)
                 bulk_prefetch_l2(g.W + c, static_cast<unsigned>(min(static_cast<long long>(WARM_L2_PIECE), end - c)));
         }
     }
@@ -1959,17 +1963,32 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
             }
         }
         __syncthreads();
+        // the argmax alone (no top-2, no verify rule): each CTA folds its best
+        // key into a running maximum per token (exact in any order); the last
+        // CTA reads and clears it
+        const bool alone = H.am_idx2 == nullptr && H.vc_tokens == nullptr;
         if (tid < T) {
             unsigned long long m1 = 0ull, m2 = 0ull;
             for (int w = 0; w < nw; ++w) top2_merge(m1, m2, s_best[(w * T + tid) * 2], s_best[(w * T + tid) * 2 + 1]);
-            H.am_cand[(static_cast<long long>(blockIdx.x) * T + tid) * 2] = m1;
-            H.am_cand[(static_cast<long long>(blockIdx.x) * T + tid) * 2 + 1] = m2;
+            if (alone) {
+                if (m1) atomicMax(H.am_key + tid, m1);
+            } else {
+                H.am_cand[(static_cast<long long>(blockIdx.x) * T + tid) * 2] = m1;
+                H.am_cand[(static_cast<long long>(blockIdx.x) * T + tid) * 2 + 1] = m2;
+            }
             __threadfence();  // the candidates are visible before the arrival below
         }
         __syncthreads();
         if (tid == 0) s_last = (atomicAdd(H.am_cnt, 1u) == gridDim.x - 1) ? 1 : 0;
         __syncthreads();
-        if (s_last) {
+        if (s_last && alone) {
+            __threadfence();
+            if (tid < T) {
+                const unsigned long long k = atomicExch(H.am_key + tid, 0ull);
+                if (H.am_idx != nullptr) H.am_idx[tid] = key_row(k);
+            }
+            if (tid == 0) *H.am_cnt = 0u;
+        } else if (s_last) {
             // every CTA's candidate pair, one per thread, then a warp and a CTA merge
             __threadfence();
 #pragma unroll

@@ -129,6 +129,7 @@ struct Plan {
 // partials).  Counters are only ever used as counters and every completed
 // call leaves them at zero, so calls of any kind may share a workspace.
 constexpr long long CNT_AREA = 16384;
+constexpr long long AM_KEY_BYTES = 64;  // the last 64 bytes of the counter area: argmax running maxima [T]
 static_assert(CNT_AREA / 4 > SPLIT_SLAB_THRESHOLD, "split-K counters must fit the counter area");
 
 // Partition weight of one weight byte of a group, in sixteenths, so that
@@ -162,6 +163,7 @@ qgemv_status make_plan(const GroupSpec *gs, int n, int T, bool ggml, bool argmax
     long long cnt_off = 4;     // counters (argmax arrival counter at 0)
     if (argmax) {
         P.am_cnt = ws ? reinterpret_cast<unsigned *>(ws) : nullptr;
+        P.am_key = ws ? reinterpret_cast<unsigned long long *>(ws + CNT_AREA - AM_KEY_BYTES) : nullptr;
         P.am_cand = ws ? reinterpret_cast<unsigned long long *>(ws + off) : nullptr;
         off = align_up(off + static_cast<long long>(MAX_GRID) * T * 16, 256);  // a key pair per CTA and token
     }
@@ -209,7 +211,7 @@ qgemv_status make_plan(const GroupSpec *gs, int n, int T, bool ggml, bool argmax
             const long long nc = static_cast<long long>(g.count) * g.nslabs;
             g.cnt = ws ? reinterpret_cast<unsigned *>(ws + cnt_off) : nullptr;
             cnt_off += nc * 4;
-            if (cnt_off > CNT_AREA) return QGEMV_ERR_INTERNAL;
+            if (cnt_off > CNT_AREA - AM_KEY_BYTES) return QGEMV_ERR_INTERNAL;  // the argmax maxima end the area
             g.part = ws ? reinterpret_cast<float *>(ws + off) : nullptr;
             off = align_up(off + nc * g.nseg * T * 16 * 4, 256);
         }

@@ -81,6 +81,7 @@ struct ParamHead {
     int xf32;               // the groups' activations are fp32 [T][K], quantised in the kernel
     long long total_cost, total_items;  // weighted bytes, items of the launch
     unsigned long long *am_cand;  // argmax: [gridDim][T] candidate keys
+    unsigned long long *am_key;   // argmax alone: [T] running maxima (zero between launches)
     unsigned *am_cnt;             // argmax: CTA arrival counter
     long long *am_idx;            // argmax: result [T] (or nullptr)
     long long *am_idx2;           // top-2: rows [T][2] (or nullptr)
