@@ -54,12 +54,12 @@
  * exception crosses the ABI.  Calls are thread-safe; two calls that share a
  * workspace must not overlap on the GPU.
  *
- * Launch order.  The GEMV calls (all but the gather) launch with
- * programmatic dependent launch: a GEMV kernel may start, and read the
- * weights W, while the preceding kernel in the stream is still running, if
- * that kernel allows it (griddepcontrol.launch_dependents); activations,
- * outputs and workspace are touched only after the preceding kernel has
- * completed.  So W must not be written by a preceding kernel that allows
+ * Launch order.  The GEMV calls launch with programmatic dependent launch:
+ * a GEMV kernel may start, and read the weights W, while the preceding
+ * kernel in the stream is still running, if that kernel allows it
+ * (griddepcontrol.launch_dependents); activations, outputs, workspace and a
+ * gather's expert ids (and so the weights a gather reads) are touched only
+ * after the preceding kernel has completed.  So W must not be written by a preceding kernel that allows
  * early launch before its writes are done (the library's own kernels that
  * allow it never write weights).
  *

@@ -1429,6 +1429,10 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
         }
     }
     __syncthreads();
+    // A gather's expert ids may be written by the preceding kernel: its
+    // stage walkers and run table read them only after the dependency wait
+    // (everything above overlaps the preceding kernel's end).
+    if (H.ids != nullptr) pdl_wait();
     // Warm-up: the warps ask L2 for the first bytes of this CTA's weights (in
     // its first group, packed slabs only) in 16 KB pieces, one piece per
     // warp in turn (so that no warp, thread 0's least, waits on many

@@ -1306,8 +1306,9 @@ size_t qgemv_gather_f32_workspace_bytes(const qgemv_gather_f32_matrix *mats, int
 }
 
 // The gather calls (checked here).  xf32: activations are fp32 x[T][K],
-// quantised inside the kernel.  No dependent-launch overlap: the run table
-// reads the expert ids, which the preceding kernel may write.
+// quantised inside the kernel.  Launched with programmatic dependent launch:
+// the kernel reads the expert ids (which the preceding kernel may write)
+// only after its dependency wait.
 static qgemv_status gather_call(const GatherIn *mats, int n_mats, const int32_t *ids, int n_ids, int n_experts,
                                 qgemv_wlayout layout, int T, void *ws, size_t ws_bytes, qgemv_stream_t stream,
                                 bool xf32)
@@ -1355,7 +1356,7 @@ static qgemv_status gather_call(const GatherIn *mats, int n_mats, const int32_t 
     pl.P.xf32 = xf32 ? 1 : 0;
     const int grid = grid_for(dev, cps);
     set_cta_groups(pl.P, grid);
-    return dispatch_T<MAXG_SMALL, false>(pl.P, T, mma_for(T), grid, pl.smem, reinterpret_cast<cudaStream_t>(stream), false) ==
+    return dispatch_T<MAXG_SMALL, false>(pl.P, T, mma_for(T), grid, pl.smem, reinterpret_cast<cudaStream_t>(stream), true) ==
                    cudaSuccess
                ? QGEMV_OK
                : QGEMV_ERR_CUDA;
