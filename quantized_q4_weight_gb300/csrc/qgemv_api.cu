@@ -138,9 +138,18 @@ static_assert(CNT_AREA / 4 > SPLIT_SLAB_THRESHOLD, "split-K counters must fit th
 // take the int8 image, too large for the f16 operand image, converts them to
 // f16 in every warp and block; measured at about 1.125 times the time per
 // byte of an f16-image group.  The partition never changes a result.
+constexpr int PART_OVH_KB_MMA = 448;   // tensor-core path (T >= 5 by default)
+constexpr int PART_OVH_KB_DP4A = 176;  // dp4a path at three and four tokens
+
 inline int partition_cost(int T, int K, bool mma)
 {
     return mma && !xq_layout(T, K, true).f16 ? 18 : 16;
+}
+
+// The fixed partition cost of each GEMV a CTA meets, in KB of weights.
+inline int partition_overhead_kb(int T, bool mma)
+{
+    return mma ? PART_OVH_KB_MMA : (T >= 3 ? PART_OVH_KB_DP4A : 0);
 }
 
 template <int MAXG>
@@ -159,6 +168,13 @@ qgemv_status make_plan(const GroupSpec *gs, int n, int T, bool ggml, bool argmax
         total_slabs += nslabs * gs[i].count;
         (void)nb;
     }
+    // The partition's fixed cost of each group instance (each GEMV a CTA
+    // meets costs a group barrier and its activation image), from per-CTA
+    // timing probes of the 36-layer 3B set: about 12 us per GEMV at T = 8
+    // (the streaming time of ~448 KB), 5 us at T = 4 (~176 KB), and the
+    // int8-image groups weighted 18/16 per byte (more measured worse)
+    P.part_ovh_kb = partition_overhead_kb(T, mma);
+    const long long ovh = static_cast<long long>(P.part_ovh_kb) * 1024 * 16;
     long long off = CNT_AREA;  // data
     long long cnt_off = 4;     // counters (argmax arrival counter at 0)
     if (argmax) {
@@ -205,7 +221,7 @@ qgemv_status make_plan(const GroupSpec *gs, int n, int T, bool ggml, bool argmax
         g.cost = partition_cost(T, g.K, mma);
         g.cost_begin = cost;
         g.item_begin = static_cast<int>(items);
-        cost += g.inst_bytes * g.count * g.cost;
+        cost += (ovh + g.inst_bytes * g.cost) * g.count;
         items += static_cast<long long>(g.items_per_inst) * g.count;
         if (g.split > 1) {
             const long long nc = static_cast<long long>(g.count) * g.nslabs;
@@ -350,14 +366,16 @@ qgemv_status plan_launch(const GroupSpec *gs, int n, int T, bool ggml, bool argm
 // that holds X (g.cost_begin <= X <= the next group's cost_begin; X below the
 // launch's total).  Within an instance, slab s and its segment part p start at
 // (s * slab_bytes + p * spp * SEG_BYTES) * cost; the tail follows the slabs.
-inline long long first_item_in_group(const Group &g, long long X)
+// Each instance is preceded by a fixed cost ovh (its activations' set-up):
+// a position inside it maps to the instance's first item.
+inline long long first_item_in_group(const Group &g, long long X, long long ovh)
 {
     const long long local = X - g.cost_begin;
-    const long long inst = g.inst_bytes * g.cost, slab = g.slab_bytes * g.cost;
+    const long long inst = ovh + g.inst_bytes * g.cost, slab = g.slab_bytes * g.cost;
     const long long e = local / inst;
-    const long long rem = local - e * inst;
+    const long long rem = local - e * inst - ovh;
     const long long base = g.item_begin + e * g.items_per_inst;
-    if (rem == 0) return base;
+    if (rem <= 0) return base;
     const long long slabs_bytes = static_cast<long long>(g.nslabs) * slab;
     if (rem < slabs_bytes) {
         const long long s = rem / slab;
@@ -380,13 +398,14 @@ inline long long first_item_in_group(const Group &g, long long X)
 template <int MAXG>
 void set_cta_groups(Params<MAXG> &P, int grid)
 {
+    const long long ovh = static_cast<long long>(P.part_ovh_kb) * 1024 * 16;
     int gi = 0;
     for (int c = 0; c <= grid; ++c) {
         const long long x = P.total_cost * c / grid;
         const long long b = x >= P.total_cost ? P.total_cost - 1 : x;
         while (gi + 1 < P.ngroups && P.g[gi + 1].cost_begin <= b) ++gi;
         P.cta_g0[c] = static_cast<unsigned char>(gi);
-        P.cta_i0[c] = static_cast<int>(x >= P.total_cost ? P.total_items : first_item_in_group(P.g[gi], x));
+        P.cta_i0[c] = static_cast<int>(x >= P.total_cost ? P.total_items : first_item_in_group(P.g[gi], x, ovh));
     }
 }
 

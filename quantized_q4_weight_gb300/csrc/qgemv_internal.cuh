@@ -87,7 +87,7 @@ struct ParamHead {
     long long *am_idx2;           // top-2: rows [T][2] (or nullptr)
     float *am_val2;               // top-2: values [T][2] (with am_idx2)
     int epilogue;                 // groups carry bias / residual pointers (sequences only)
-    int epilogue_unused;
+    int part_ovh_kb;              // host partition only: fixed cost of each group instance, in KB of weights
     float *sg_part;               // small groups: per-CTA segment sums (or nullptr)
     int sg_stride;                //   floats per CTA region
     int sg_ctas;                  //   CTAs 0..sg_ctas-1 have a region
