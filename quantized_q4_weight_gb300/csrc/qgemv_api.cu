@@ -138,7 +138,7 @@ static_assert(CNT_AREA / 4 > SPLIT_SLAB_THRESHOLD, "split-K counters must fit th
 // take the int8 image, too large for the f16 operand image, converts them to
 // f16 in every warp and block; measured at about 1.125 times the time per
 // byte of an f16-image group.  The partition never changes a result.
-constexpr int PART_OVH_KB_MMA = 448;   // tensor-core path (T >= 5 by default)
+constexpr int PART_OVH_KB_MMA = 256;   // tensor-core path (T >= 5 by default)
 constexpr int PART_OVH_KB_DP4A = 176;  // dp4a path at three and four tokens
 
 inline int partition_cost(int T, int K, bool mma)
@@ -169,10 +169,12 @@ qgemv_status make_plan(const GroupSpec *gs, int n, int T, bool ggml, bool argmax
         (void)nb;
     }
     // The partition's fixed cost of each group instance (each GEMV a CTA
-    // meets costs a group barrier and its activation image), from per-CTA
-    // timing probes of the 36-layer 3B set: about 12 us per GEMV at T = 8
-    // (the streaming time of ~448 KB), 5 us at T = 4 (~176 KB), and the
-    // int8-image groups weighted 18/16 per byte (more measured worse)
+    // meets costs a group barrier and its activation image).  Per-CTA timing
+    // probes of the 36-layer 3B set fitted about 12 us per GEMV at T = 8 and
+    // 5 us at T = 4 beyond the per-byte costs; the step times of a sweep of
+    // the charge (0, 128, 256, 448, 704 KB at T = 8) were best at 256 KB,
+    // and 176 KB at T = 4 beat none.  The int8-image groups stay at 18/16
+    // per byte (20/16 measured worse).
     P.part_ovh_kb = partition_overhead_kb(T, mma);
     const long long ovh = static_cast<long long>(P.part_ovh_kb) * 1024 * 16;
     long long off = CNT_AREA;  // data
