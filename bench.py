@@ -559,6 +559,7 @@ KERNEL_SOURCES = {
     "q8_gemv_kernel": ["q8_kernel.cu"],
     "requant_q4_0_staged_q8": ["kernels_misc.cu"],
     "gs64_gemv_kernel": ["gs64_kernel.cu"],
+    "ffn_fused_kernel": ["ffn_fused.cu", "gemv_kernel.cuh"],
 }
 
 
