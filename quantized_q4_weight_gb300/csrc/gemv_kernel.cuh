@@ -1607,7 +1607,7 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
                 cur.skip_untransferred(runs, ggml);
             }
             if (gidx == 0) {
-                pdl_wait();
+                if (H.ids == nullptr) pdl_wait();  // (a gather waited before its run table)
             } else {
                 // every warp is done with the previous group's activations and
                 // hand-off sums; the whole CTA stops together after an abort
@@ -1794,7 +1794,7 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
             ring.issue(lane, d, cur.src(P), cur.bytes(P), pol_w);
             cur.advance(P, warp);
         }
-        pdl_wait();
+        if (H.ids == nullptr) pdl_wait();  // (a gather waited before its stage walkers)
 
         int gi_hint = 0, gi_item = 0;
         for (long long ra = i0; ra < i1;) {
