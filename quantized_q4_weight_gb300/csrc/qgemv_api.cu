@@ -140,6 +140,7 @@ static_assert(CNT_AREA / 4 > SPLIT_SLAB_THRESHOLD, "split-K counters must fit th
 // byte of an f16-image group.  The partition never changes a result.
 constexpr int PART_OVH_KB_MMA = 256;   // tensor-core path (T >= 5 by default)
 constexpr int PART_OVH_KB_DP4A = 176;  // dp4a path at three and four tokens
+constexpr int PART_OVH_KB_FEW = 96;    // dp4a path at one and two tokens
 
 inline int partition_cost(int T, int K, bool mma)
 {
@@ -149,7 +150,7 @@ inline int partition_cost(int T, int K, bool mma)
 // The fixed partition cost of each GEMV a CTA meets, in KB of weights.
 inline int partition_overhead_kb(int T, bool mma)
 {
-    return mma ? PART_OVH_KB_MMA : (T >= 3 ? PART_OVH_KB_DP4A : 0);
+    return mma ? PART_OVH_KB_MMA : (T >= 3 ? PART_OVH_KB_DP4A : PART_OVH_KB_FEW);
 }
 
 template <int MAXG>
@@ -170,12 +171,18 @@ qgemv_status make_plan(const GroupSpec *gs, int n, int T, bool ggml, bool argmax
     }
     // The partition's fixed cost of each group instance (each GEMV a CTA
     // meets costs a group barrier and its activation image).  Per-CTA timing
-    // probes of the 36-layer 3B set fitted about 12 us per GEMV at T = 8 and
-    // 5 us at T = 4 beyond the per-byte costs; the step times of a sweep of
-    // the charge (0, 128, 256, 448, 704 KB at T = 8) were best at 256 KB,
-    // and 176 KB at T = 4 beat none.  The int8-image groups stay at 18/16
+    // probes fitted about 12 us per GEMV at T = 8, 5 us at T = 4 (36-layer
+    // 3B set) and 2 us at T = 1 (28-layer 1.5B set) beyond the per-byte
+    // costs; same-box sweeps of the charge were best at 256 KB (T = 8; 0,
+    // 128, 448 and 704 KB slower), 176 KB (T = 4; 96 and 320 KB slower) and
+    // 96 KB (T = 1, 2: the 1.5B set 0.7 % and the MoE gather 9 % faster than
+    // none; 144, 192, 320 KB slower).  The int8-image groups stay at 18/16
     // per byte (20/16 measured worse).
-    P.part_ovh_kb = partition_overhead_kb(T, mma);
+    // (A launch of one matrix has nothing to balance: the charge would only
+    // leave its first CTAs idle.)
+    long long instances = 0;
+    for (int i = 0; i < n; ++i) instances += gs[i].count;
+    P.part_ovh_kb = instances > 1 ? partition_overhead_kb(T, mma) : 0;
     const long long ovh = static_cast<long long>(P.part_ovh_kb) * 1024 * 16;
     long long off = CNT_AREA;  // data
     long long cnt_off = 4;     // counters (argmax arrival counter at 0)
