@@ -1993,24 +1993,28 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
             }
             if (tid == 0) *H.am_cnt = 0u;
         } else if (s_last) {
-            // every CTA's candidate pair, one per thread, then a warp and a CTA merge
+            // the warps split the tokens: warp w merges token w % T over part
+            // w / T of the CTAs' candidate pairs (one pair per lane in turn),
+            // then one thread per token merges the parts
             __threadfence();
-#pragma unroll
-            for (int t = 0; t < T; ++t) {
+            const int parts = nw / T;  // nw >= 8 >= T
+            if (warp < parts * T) {
+                const int t = warp % T, p = warp / T;
                 unsigned long long m1 = 0ull, m2 = 0ull;
-                for (unsigned c = tid; c < gridDim.x; c += nthreads)
+#pragma unroll 4
+                for (unsigned c = p * 32 + lane; c < gridDim.x; c += parts * 32)
                     top2_merge(m1, m2, __ldcg(H.am_cand + (static_cast<long long>(c) * T + t) * 2),
                                __ldcg(H.am_cand + (static_cast<long long>(c) * T + t) * 2 + 1));
                 top2_warp(m1, m2);
                 if (lane == 0) {
-                    s_best[(warp * T + t) * 2] = m1;
-                    s_best[(warp * T + t) * 2 + 1] = m2;
+                    s_best[(p * T + t) * 2] = m1;
+                    s_best[(p * T + t) * 2 + 1] = m2;
                 }
             }
             __syncthreads();
             if (tid < T) {
                 unsigned long long m1 = 0ull, m2 = 0ull;
-                for (int w = 0; w < nw; ++w)
+                for (int w = 0; w < parts; ++w)
                     top2_merge(m1, m2, s_best[(w * T + tid) * 2], s_best[(w * T + tid) * 2 + 1]);
                 if (H.am_idx != nullptr) H.am_idx[tid] = key_row(m1);
                 if (H.am_idx2 != nullptr) {
