@@ -64,9 +64,11 @@
  * allow it never write weights).
  *
  * Workspace.  Calls that take (ws, ws_bytes) use it for split-K partial
- * sums, completion counters and argmax candidates.  The matching *_workspace_bytes query gives the
- * size (device-independent, at least 16 KB).  Its first 16 KB hold
- * completion counters and must be zero-filled once before the first use
+ * sums, completion counters and argmax candidates.  The matching
+ * *_workspace_bytes query gives the size (device-independent, at least 16
+ * KB).  Its first 16 KB hold completion counters (and, in their last 64
+ * bytes, the argmax's running maxima) and must be zero-filled once before
+ * the first use
  * (e.g. cudaMemsetAsync); every call that completes without a device-status
  * error leaves them at zero again, so a workspace can be reused directly,
  * by calls of any kind and shape, as long as it is large enough.
