@@ -826,43 +826,6 @@ __device__ __forceinline__ void build_fold_constants(uint8_t *img, int K, int ti
     }
 }
 
-// One block of 32 fp32 activations quantised to Q8_0 by one thread, with the
-// warp quantiser's steps (the maximum is exact in any order, so the bytes are
-// the same): the codes as two uint4 (elements 0..15, 16..31) and the fp16
-// scale.  vec: x is 16-byte aligned.
-__device__ __forceinline__ void q8_block_thread(const float *x, bool vec, uint4 &qa, uint4 &qb, unsigned short &dh)
-{
-    float v[QK];
-    if (vec) {
-#pragma unroll
-        for (int i = 0; i < QK / 4; ++i) {
-            const float4 f = __ldcg(reinterpret_cast<const float4 *>(x) + i);
-            v[4 * i] = f.x;
-            v[4 * i + 1] = f.y;
-            v[4 * i + 2] = f.z;
-            v[4 * i + 3] = f.w;
-        }
-    } else {
-#pragma unroll
-        for (int i = 0; i < QK; ++i) v[i] = __ldcg(x + i);
-    }
-    float amax = fabsf(v[0]);
-#pragma unroll
-    for (int i = 1; i < QK; ++i) amax = fmaxf(amax, fabsf(v[i]));
-    float d, id;
-    q8_scale(amax, d, id);
-    unsigned w[QK / 4];
-#pragma unroll
-    for (int k = 0; k < QK / 4; ++k)
-        w[k] = (static_cast<unsigned>(q8_code(v[4 * k], id)) & 0xFFu) |
-               ((static_cast<unsigned>(q8_code(v[4 * k + 1], id)) & 0xFFu) << 8) |
-               ((static_cast<unsigned>(q8_code(v[4 * k + 2], id)) & 0xFFu) << 16) |
-               ((static_cast<unsigned>(q8_code(v[4 * k + 3], id)) & 0xFFu) << 24);
-    qa = make_uint4(w[0], w[1], w[2], w[3]);
-    qb = make_uint4(w[4], w[5], w[6], w[7]);
-    dh = q8_half(d);
-}
-
 // One run's int8 activation image quantised in the kernel from fp32
 // activations x[T][K] in global memory, with its per-block constants, in one
 // pass, for images of at most nthreads / 8 blocks: the bytes a copy of the

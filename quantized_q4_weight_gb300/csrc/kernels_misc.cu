@@ -63,22 +63,43 @@ struct QuantList {
 
 __global__ void __launch_bounds__(256) quantize_list_kernel(const __grid_constant__ QuantList L)
 {
+    // The grid is small enough to be resident at once, so a dependent
+    // kernel launched early cannot take the SMs this one still needs.
     pdl_launch_dependents();
     pdl_wait();
-    const int lane = threadIdx.x & 31;
-    int i = 0;
-    for (long long gb = (static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x) >> 5; gb < L.block_begin[L.n];
-         gb += (static_cast<long long>(gridDim.x) * blockDim.x) >> 5) {
-        while (L.block_begin[i + 1] <= gb) ++i;  // blocks are visited in increasing order per warp
-        const long long xqb = static_cast<long long>(L.T) * L.K[i] + ((2ll * L.T * (L.K[i] / QK) + 15) & ~15ll);
-        quantize_block_warp(L.x[i], L.xq[i], L.T, L.K[i], gb - L.block_begin[i], xqb, lane);
+    const long long total = L.block_begin[L.n];
+    for (long long gb = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; gb < total;
+         gb += static_cast<long long>(gridDim.x) * blockDim.x) {
+        int lo = 0, hi = L.n;  // the item holding block gb: block_begin[lo] <= gb < block_begin[lo + 1]
+        while (hi - lo > 1) {
+            const int mid = (lo + hi) >> 1;
+            if (L.block_begin[mid] <= gb) lo = mid;
+            else hi = mid;
+        }
+        const int K = L.K[lo], nb = K / QK, T = L.T;
+        const long long rem = gb - L.block_begin[lo];
+        const int r = static_cast<int>(rem / nb), b = static_cast<int>(rem - static_cast<long long>(r) * nb);
+        const float *x = L.x[lo] + static_cast<long long>(r) * K + b * QK;
+        uint4 qa, qb;
+        unsigned short dh;
+        q8_block_thread(x, (reinterpret_cast<uintptr_t>(x) & 15) == 0, qa, qb, dh);
+        uint8_t *dst = L.xq[lo];
+        uint4 *dq = reinterpret_cast<uint4 *>(dst + static_cast<long long>(r) * K + b * QK);
+        dq[0] = qa;
+        dq[1] = qb;
+        reinterpret_cast<unsigned short *>(dst + static_cast<long long>(T) * K)[rem] = dh;
+        if (rem == 0) {  // zero the padding after the scales
+            const long long used = static_cast<long long>(T) * K + 2ll * T * nb;
+            const long long xqb = static_cast<long long>(T) * K + ((2ll * T * nb + 15) & ~15ll);
+            for (long long p = used; p < xqb; ++p) dst[p] = 0;
+        }
     }
 }
 
 cudaError_t launch_quantize_list(const float *const *x, uint8_t *const *xq, const long long *K, int n, int T,
-                                 cudaStream_t st)
+                                 int max_ctas, cudaStream_t st)
 {
-    if (n < 1 || n > MAXG_SEQ) return cudaErrorInvalidValue;
+    if (n < 1 || n > MAXG_SEQ || max_ctas < 1) return cudaErrorInvalidValue;
     QuantList L;
     memset(&L, 0, sizeof(L));
     L.n = n;
@@ -89,8 +110,8 @@ cudaError_t launch_quantize_list(const float *const *x, uint8_t *const *xq, cons
         L.K[i] = static_cast<int>(K[i]);
         L.block_begin[i + 1] = L.block_begin[i] + static_cast<long long>(T) * (K[i] / QK);
     }
-    long long grid = (L.block_begin[n] + 7) / 8;
-    if (grid > 65535) grid = 65535;
+    long long grid = (L.block_begin[n] + 255) / 256;  // one thread per block of 32 values
+    if (grid > max_ctas) grid = max_ctas;
     cudaLaunchConfig_t cfg = {};
     cfg.gridDim = dim3(static_cast<unsigned>(grid));
     cfg.blockDim = dim3(256);

@@ -1154,7 +1154,7 @@ static qgemv_status launch_seq(const qgemv_seq_item *items, int n, qgemv_wlayout
                     sp[i].xq = w + off;
                     off += align_up(xq_bytes_host(T, sp[i].K), 256);
                 }
-                if (launch_quantize_list(xs.data(), xqs.data(), ks.data(), cn, T, st) != cudaSuccess)
+                if (launch_quantize_list(xs.data(), xqs.data(), ks.data(), cn, T, 2 * dev.sms, st) != cudaSuccess)
                     return QGEMV_ERR_CUDA;
             }
             if (launch_tc(sp.data(), cn, T, w, dev.sms, dev.status, st) != cudaSuccess) return QGEMV_ERR_CUDA;

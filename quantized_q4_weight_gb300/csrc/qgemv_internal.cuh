@@ -344,6 +344,44 @@ __device__ __forceinline__ void q8_scale(float amax, float &d, float &id)
 __device__ __forceinline__ int q8_code(float v, float id) { return static_cast<int>(roundf(__fmul_rn(v, id))); }
 __device__ __forceinline__ unsigned short q8_half(float d) { return __half_as_ushort(__float2half_rn(d)); }
 
+// One block of 32 fp32 activations quantised to Q8_0 by one thread, with the
+// warp quantiser's steps (the maximum is exact in any order, so the bytes are
+// the same): the codes as two uint4 (elements 0..15, 16..31) and the fp16
+// scale.  vec: x is 16-byte aligned.
+__device__ __forceinline__ void q8_block_thread(const float *x, bool vec, uint4 &qa, uint4 &qb, unsigned short &dh)
+{
+    float v[QK];
+    if (vec) {
+#pragma unroll
+        for (int i = 0; i < QK / 4; ++i) {
+            const float4 f = __ldcg(reinterpret_cast<const float4 *>(x) + i);
+            v[4 * i] = f.x;
+            v[4 * i + 1] = f.y;
+            v[4 * i + 2] = f.z;
+            v[4 * i + 3] = f.w;
+        }
+    } else {
+#pragma unroll
+        for (int i = 0; i < QK; ++i) v[i] = __ldcg(x + i);
+    }
+    float amax = fabsf(v[0]);
+#pragma unroll
+    for (int i = 1; i < QK; ++i) amax = fmaxf(amax, fabsf(v[i]));
+    float d, id;
+    q8_scale(amax, d, id);
+    unsigned w[QK / 4];
+#pragma unroll
+    for (int k = 0; k < QK / 4; ++k)
+        w[k] = (static_cast<unsigned>(q8_code(v[4 * k], id)) & 0xFFu) |
+               ((static_cast<unsigned>(q8_code(v[4 * k + 1], id)) & 0xFFu) << 8) |
+               ((static_cast<unsigned>(q8_code(v[4 * k + 2], id)) & 0xFFu) << 16) |
+               ((static_cast<unsigned>(q8_code(v[4 * k + 3], id)) & 0xFFu) << 24);
+    qa = make_uint4(w[0], w[1], w[2], w[3]);
+    qb = make_uint4(w[4], w[5], w[6], w[7]);
+    dh = q8_half(d);
+}
+
+
 // h = SiLU(g) * u, quantised to planar Q8_0 for the down projection (minfer
 // README M15: the FFN between the GEMVs of a decode step).  exp by Cody and
 // Waite's method (W. J. Cody, W. Waite, "Software Manual for the Elementary

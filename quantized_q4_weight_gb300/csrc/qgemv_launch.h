@@ -63,9 +63,10 @@ bool tc_eligible(const TcSpec *s, int n, int T);
 long long tc_ws_bytes(const TcSpec *s, int n, int grid);
 cudaError_t launch_tc(const TcSpec *s, int n, int T, uint8_t *ws, int grid, unsigned *status, cudaStream_t st);
 // Q8_0 quantisation of n activation blocks x[i] (fp32 [T][K[i]]) into planar
-// buffers xq[i] (kernels_misc.cu): one launch for a whole sequence.
+// buffers xq[i] (kernels_misc.cu): one launch for a whole sequence, of at
+// most max_ctas CTAs of 256 threads (few enough to be resident at once).
 cudaError_t launch_quantize_list(const float *const *x, uint8_t *const *xq, const long long *K, int n, int T,
-                                 cudaStream_t st);
+                                 int max_ctas, cudaStream_t st);
 
 // The decode FFN step in one cooperative launch (ffn_fused.cu), T <= 4,
 // packed weights, d_model % 16 == 0, d_ff % 32 == 0, one CTA per SM of a
