@@ -1392,10 +1392,6 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
         }
     }
     __syncthreads();
-    // A gather's expert ids may be written by the preceding kernel: its
-    // stage walkers and run table read them only after the dependency wait
-    // (everything above overlaps the preceding kernel's end).
-    if (H.ids != nullptr) pdl_wait();
     // Warm-up: the warps ask L2 for the first bytes of this CTA's weights (in
     // its first group, packed slabs only) in 16 KB pieces, one piece per
     // warp in turn (so that no warp, thread 0's least, waits on many
@@ -1458,12 +1454,12 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
             }
             const int local = static_cast<int>(ra - g.item_begin);
             const int e = local / g.items_per_inst;
-            int expert = e, bad = 0;
-            if (H.ids != nullptr) {
-                expert = __ldg(H.ids + e);
-                bad = (expert < 0 || expert >= H.n_experts) ? 1 : 0;
-                if (bad) expert = 0;
-            }
+            // a gather's expert ids may still be written by the preceding
+            // kernel: its runs take expert 0 here, and after the dependency
+            // wait each run's weights and bad-id flag are patched (the
+            // table's shape does not depend on the ids: every expert of a
+            // matrix has the same shape)
+            const int expert = H.ids != nullptr ? 0 : e, bad = 0;
             RunInfo &R = runs[nr];
             R.Wi = g.W + static_cast<long long>(expert) * g.w_stride;
             R.y = g.y + static_cast<long long>(e) * g.y_stride;
@@ -1505,6 +1501,8 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
     const uint64_t pol_w = l2_policy_evict_first();
     const uint64_t pol_x = l2_policy_evict_last();
     const int nruns = s_nruns;
+    // (the run-synced mode's stage walkers read a gather's ids themselves)
+    if (H.ids != nullptr && nruns == 0) pdl_wait();
 
     Top2Lane<T, MMA> st;  // the lane's two best keys per token (argmax launches)
 #pragma unroll
@@ -1563,6 +1561,22 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
             // in consumption order start at ring.slot
             Walker cur;
             cur.init(runs, head_b, b, tail_e, head_b, a, tail_e);
+            if (gidx == 0 && H.ids != nullptr) {
+                // a gather's expert ids, now that the preceding kernel is
+                // done: each run's weights and bad-id flag
+                pdl_wait();
+                for (int r = tid; r < nruns; r += nthreads) {
+                    RunInfo &R = runs[r];
+                    const Group &g = gcache[R.gi - g0];
+                    int expert = __ldg(H.ids + R.e);
+                    const int bad = (expert < 0 || expert >= H.n_experts) ? 1 : 0;
+                    if (bad) expert = 0;
+                    R.Wi = g.W + static_cast<long long>(expert) * g.w_stride;
+                    R.bad = bad;
+                }
+                __syncthreads();
+                if (cur.valid) cur.load_run(runs);
+            }
             cur.skip_untransferred(runs, ggml);
             for (int d = 0; d < D && cur.valid; ++d) {
                 ring.issue(lane, (ring.slot + d) % D, cur.src(), cur.bytes(), pol_w);
@@ -1570,7 +1584,7 @@ __global__ void __launch_bounds__(max_warps_for(T, MMA) * 32, 1) qgemv_stream_ke
                 cur.skip_untransferred(runs, ggml);
             }
             if (gidx == 0) {
-                if (H.ids == nullptr) pdl_wait();  // (a gather waited before its run table)
+                if (H.ids == nullptr) pdl_wait();  // (a gather waited above, before reading its ids)
             } else {
                 // every warp is done with the previous group's activations and
                 // hand-off sums; the whole CTA stops together after an abort
