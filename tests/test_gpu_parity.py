@@ -359,6 +359,50 @@ def test_gather_matches_single_calls(orc, layout):
     assert q.device_status() == 0
 
 
+@pytest.mark.parametrize("T", [3, 6])
+def test_gather_several_tokens_and_bad_ids(orc, T):
+    """Gathers at several tokens (dp4a at T = 3, the tensor cores at T = 6),
+    many slots over a grid of CTAs, repeated ids: each slot bit-identical to
+    a single call on its expert and within the bound of the oracle; then one
+    slot with an id out of range (nothing read for it, its output untouched,
+    the status word set) while the others stay bit-identical."""
+    n_experts, N, K = 10, 1024, 2048
+    per = q.q4_0_bytes(N, K)
+    Wg_all = [synth.q4_0_weights(2100 + e, N, K) for e in range(n_experts)]
+    W = torch.cat([q.pack_q4_0(to_dev(w), N, K) for w in Wg_all])
+    ids_np = np.array([4, 9, 4, 0, 7, 2, 9, 5], np.int32)
+    n_ids = ids_np.size
+    xs = synth.activations(2200 + T, n_ids * T, K)
+    xqb = q.xq_bytes(T, K)
+    xq = q.quantize_q8_0(torch.from_numpy(xs).to(DEV), T, K, batch=n_ids)
+    y = torch.full((n_ids, T, N), float("nan"), dtype=torch.float32, device=DEV)
+    gm = q.gather_mats([(W, per, xq, xqb, y, T * N, N, K)])
+    ws = q.new_workspace(q.gather_workspace_bytes(gm, n_ids, T))
+    q.gemv_gather(gm, torch.from_numpy(ids_np).to(DEV), n_experts, q.W_PACKED, T, ws)
+    torch.cuda.synchronize()
+    assert q.device_status() == 0
+    ref = []
+    for s_ in range(n_ids):
+        e = int(ids_np[s_])
+        yref = q.gemv(W[e * per:(e + 1) * per], q.W_PACKED, xq[s_ * xqb:(s_ + 1) * xqb], N, K, T,
+                      ws_for(N, K, T)).cpu()
+        ref.append(yref)
+        assert torch.equal(y[s_].cpu().view(torch.int32), yref.view(torch.int32)), s_
+        y64, S = orc.gemv(Wg_all[e], N, K, orc.quantize(xs[s_ * T:(s_ + 1) * T]), T)
+        check_close(y[s_].cpu().numpy(), y64, S, f"gather T={T} slot {s_}")
+    bad_np = ids_np.copy()
+    bad_np[5] = n_experts                                   # out of range
+    y.fill_(-1.0)
+    q.gemv_gather(gm, torch.from_numpy(bad_np).to(DEV), n_experts, q.W_PACKED, T, ws)
+    torch.cuda.synchronize()
+    assert q.device_status() == 7                           # QGEMV_ERR_BAD_ID
+    assert torch.all(y[5] == -1.0)
+    for s_ in range(n_ids):
+        if s_ != 5:
+            assert torch.equal(y[s_].cpu().view(torch.int32), ref[s_].view(torch.int32)), s_
+    assert q.device_status() == 0
+
+
 # ----------------------------------------------------------------- workspace contract
 
 def test_workspace_left_zeroed_and_reusable(orc):
